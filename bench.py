@@ -1,0 +1,411 @@
+#!/usr/bin/env python
+"""Benchmark of the chunked SDM write/read forward on GB300: forward tokens/s, and the
+Phase-2 gather/DW achieved HBM bandwidth against the measured peak.
+
+A step is one full sdm_write_read call (Phase 1, solve, and all Nt Phase-2 steps) over the
+workload P=8 streams x T=4096 tokens, C=64, S=65536 x D=128 bf16 bank, W=R=16 Zipf(1.1) slots
+(seeded synthetic inputs, ``sdm_inputs``). The call is captured once in a CUDA graph and
+replayed; before every step the bank is reset from a pristine copy and a 512 MiB buffer is
+written to flush L2 (both outside the per-step CUDA events).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With N > 1 (torchrun, one rank per GPU) every rank runs its own copy of the workload
+(different seed): weak scaling, no collective on the data path; value = all ranks' tokens /
+the slowest rank's time. ``--impl reference`` times the CPU oracle (fp64 token loop, plain C)
+on the host cores instead, rank 0 only.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import sdm_inputs as si  # noqa: E402
+
+METRIC = "SDM forward tokens/s on 1 GB300; Phase-2 achieved HBM GB/s vs peak"
+UNIT = "tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=1, help="index into sdm_inputs.WORKLOADS")
+    ap.add_argument("--profile-steps", type=int, default=3)
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def workload_config(wl, inputs):
+    return {"workload": wl.name, "P": wl.P, "T": wl.T, "C": wl.C, "S": wl.S, "D": wl.D,
+            "W": wl.W, "R": wl.R, "bank_dtype": wl.dtype, "slots": wl.slots,
+            "valid_tokens": int(inputs["valid"].sum()), "seed": wl.seed,
+            "l2": "flushed before every step (512 MiB write); bank reset from a pristine copy"}
+
+
+# ------------------------------------------------------------------------------------------
+# algorithmic bytes
+# ------------------------------------------------------------------------------------------
+
+def algorithmic_bytes(wl, inputs):
+    """Bank bytes the method must move, summed over all steps: per chunk, one read of every
+    distinct row it touches (writes and reads) and one write of every distinct written row.
+    Split as the gather's reads (|U_w u U_r| rows), the DW's read+write (2 |U_w|) and the
+    Phase-2 minimum (|U_w u U_r| + |U_w|)."""
+    es = 4 if wl.dtype == "f32" else 2
+    row = wl.D * es
+    g_rows = dw_rows = 0
+    for p in range(wl.P):
+        v = int(inputs["valid"][p])
+        for ti in range(wl.Nt):
+            lo, hi = ti * wl.C, min(v, ti * wl.C + wl.C)
+            if hi <= lo:
+                continue
+            uw = np.unique(inputs["write_slots"][p, lo:hi])
+            ur = np.unique(inputs["read_slots"][p, lo:hi])
+            g_rows += np.union1d(uw, ur).size
+            dw_rows += uw.size
+    return {"gather": g_rows * row, "dw": 2 * dw_rows * row, "phase2": (g_rows + dw_rows) * row}
+
+
+# ------------------------------------------------------------------------------------------
+# clocks
+# ------------------------------------------------------------------------------------------
+
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) of the SM clock and throttle reasons of one GPU."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.path = tempfile.mktemp(suffix=".csv")
+        self.proc = None
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(gpu_index)], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def traffic_record(kernel: str):
+    """DRAM bytes per launch of ``kernel`` from the committed ncu summary, if the kernel's
+    source is unchanged since the capture (else None)."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        rec = json.load(open(path))[kernel]
+        src = open(os.path.join(ROOT, "sparse_addressed_delta_gb300", "csrc", rec["source"]), "rb").read()
+        if hashlib.sha256(src).hexdigest()[:16] != rec["source_sha256_16"]:
+            return None
+        return float(rec["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------------------------------------
+# CPU oracle timing (the reference arm and the cpu_baseline field)
+# ------------------------------------------------------------------------------------------
+
+def time_oracle(wl, inputs, budget_s: float = 10.0, max_reps: int = 5):
+    import oracle
+
+    x = oracle.from_stored(inputs, wl.dtype)
+    threads = max(1, min(wl.P, os.cpu_count() or 1))
+    tokens = int(inputs["valid"].sum())
+    times = []
+    t_start = time.perf_counter()
+    while len(times) < max_reps and (not times or time.perf_counter() - t_start < budget_s):
+        t0 = time.perf_counter()
+        oracle.sequential(x["bank"], x["ws"], x["k"], x["g"], x["beta"], x["v"], x["rs"], x["q"],
+                          x["valid"], nthreads=threads)
+        times.append(time.perf_counter() - t0)
+    t = statistics.median(times)
+    return {"value": tokens / t, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"the whole workload ({tokens} tokens), fp64 token loop in C, OpenMP over "
+                      f"streams, median of {len(times)} runs ({t:.3f} s each)"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    wl = si.WORKLOADS[args.workload]
+    inputs = si.generate(wl)
+    import oracle
+
+    x = oracle.from_stored(inputs, wl.dtype)
+    threads = max(1, min(wl.P, os.cpu_count() or 1))
+    tokens = int(inputs["valid"].sum())
+
+    def step():
+        t0 = time.perf_counter()
+        oracle.sequential(x["bank"], x["ws"], x["k"], x["g"], x["beta"], x["v"], x["rs"], x["q"],
+                          x["valid"], nthreads=threads)
+        return time.perf_counter() - t0
+
+    for _ in range(args.warmup):
+        step()
+    times = [step() for _ in range(args.steps)]
+    t = statistics.mean(times)
+    value = tokens / t
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(wl, inputs),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": f"the whole workload ({tokens} tokens) per step, fp64 "
+                                       "token loop in C, OpenMP over streams"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------------------------
+# our arm
+# ------------------------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import sparse_addressed_delta_gb300 as sdm
+
+    world, rank, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://", world_size=world, rank=rank,
+                                device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    base = si.WORKLOADS[args.workload]
+    wl = base.replace(seed=base.seed + 1000 * rank) if world > 1 else base
+    inputs = si.generate(wl)
+    dt = torch.float32 if wl.dtype == "f32" else torch.bfloat16
+
+    def tens(name):
+        t = torch.from_numpy(np.ascontiguousarray(inputs[name]))
+        if wl.dtype == "bf16" and inputs[name].dtype == np.uint16:
+            t = t.view(torch.bfloat16)
+        return t
+
+    host = {k: tens(k).pin_memory() for k in ("write_slots", "write_w", "log_decay", "beta", "v",
+                                              "read_slots", "read_w", "valid")}
+    d_in = {k: v.to(dev) for k, v in host.items()}
+    bank0 = tens("bank").to(dev)
+    bank = bank0.clone()
+    shape = sdm.make_shape(wl.P, wl.T, wl.C, wl.S, wl.D, wl.W, wl.R, dt)
+    ws = sdm.alloc_workspace(shape, dev)
+    readings = torch.empty((wl.P, wl.T, wl.D), dtype=dt, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    tokens = int(inputs["valid"].sum())
+    launches_per_call = sdm.launch_count(shape)
+
+    stream = torch.cuda.Stream(device=dev)
+
+    def call():
+        sdm.sdm_write_read(bank, d_in["write_slots"], d_in["write_w"], d_in["log_decay"],
+                           d_in["beta"], d_in["v"], d_in["read_slots"], d_in["read_w"],
+                           d_in["valid"], chunk_size=wl.C, workspace=ws, readings=readings,
+                           stream=stream)
+
+    with torch.cuda.stream(stream):
+        call()                                   # eager run (sets kernel attributes)
+    stream.synchronize()
+    st = sdm.device_status(ws, stream)
+    if st["code"] != 0:
+        raise RuntimeError(f"device status {st}")
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        call()
+
+    def prepare():
+        bank.copy_(bank0)
+        flush.zero_()
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            prepare()
+            graph.replay()
+    stream.synchronize()
+
+    # ---- timed region: K graph replays, device-timed per step ----
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for k in range(args.steps):
+            prepare()
+            ev[k][0].record(stream)
+            graph.replay()
+            ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    wall1 = time.perf_counter()
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    ms = statistics.mean(step_ms)
+    ms_t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
+    ms_max = float(ms_t.item())
+    value = world * tokens / (ms_max / 1e3)
+
+    # ---- per-kernel device times (same protocol, events around every launch) ----
+    fam_ms = {k: 0.0 for k in sdm.KERNEL_KINDS}
+    fam_n = {k: 0 for k in sdm.KERNEL_KINDS}
+    for _ in range(args.profile_steps):
+        with torch.cuda.stream(stream):
+            prepare()
+        _, prof = sdm.profile_write_read(bank, d_in["write_slots"], d_in["write_w"],
+                                         d_in["log_decay"], d_in["beta"], d_in["v"],
+                                         d_in["read_slots"], d_in["read_w"], d_in["valid"],
+                                         chunk_size=wl.C, workspace=ws, readings=readings,
+                                         stream=stream)
+        for k, (t, n) in prof.items():
+            fam_ms[k] += t
+            fam_n[k] += n
+    kernels = {k: {"ms_per_call": fam_ms[k] / args.profile_steps,
+                   "launches_per_call": fam_n[k] // args.profile_steps,
+                   "us_per_launch": 1e3 * fam_ms[k] / max(1, fam_n[k]),
+                   "share": fam_ms[k] / max(1e-12, sum(fam_ms.values()))}
+               for k in sdm.KERNEL_KINDS}
+
+    # ---- roofline of the dominant kernel and of the Phase-2 gather + DW pair ----
+    alg = algorithmic_bytes(wl, inputs)
+    peak, peak_src = measured_peak()
+    dom = max(("gather", "dw", "phase1", "solve", "dualmm"), key=lambda k: fam_ms[k])
+    hbm_alg = {"gather": alg["gather"], "dw": alg["dw"]}
+    roofline = None
+    if dom in hbm_alg:
+        per_launch = hbm_alg[dom] / wl.Nt
+        secs = fam_ms[dom] / max(1, fam_n[dom]) / 1e3
+        ach = per_launch / secs / 1e9
+        roofline = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
+                    "frac": ach / peak, "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
+                    "alg_bytes_per_launch": per_launch, "traffic": traffic_record(dom)}
+    else:
+        roofline = {"kernel": dom, "bound": "alu", "note": "dominant kernel is not HBM-bound"}
+    p2_secs = (fam_ms["gather"] + fam_ms["dw"]) / args.profile_steps / 1e3
+    p2_ach = alg["phase2"] / p2_secs / 1e9
+    phase2 = {"kernels": "gather + dw", "alg_bytes_per_call": alg["phase2"],
+              "achieved": p2_ach, "peak": peak, "unit": "GB/s", "frac": p2_ach / peak}
+
+    # ---- end to end through the public API: pinned host inputs in, readings out ----
+    h_read = torch.empty((wl.P, wl.T, wl.D), dtype=dt, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = h_read.numel() * h_read.element_size()
+    e2e_ms = []
+    with torch.cuda.stream(stream):
+        for k in range(max(3, args.steps // 2)):
+            prepare()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for name, t in host.items():
+                d_in[name].copy_(t, non_blocking=True)
+            graph.replay()
+            h_read.copy_(readings, non_blocking=True)
+            b.record(stream)
+            b.synchronize()
+            e2e_ms.append(a.elapsed_time(b))
+    e2e_t = torch.tensor([statistics.mean(e2e_ms)], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(e2e_t, op=dist.ReduceOp.MAX)
+    e2e = {"value": world * tokens / (float(e2e_t.item()) / 1e3), "unit": UNIT,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "path": "pinned host inputs -> device buffers, graph replay of sdm_write_read, "
+                   "readings -> pinned host"}
+
+    cpu = None
+    if rank == 0 and world == 1:
+        cpu = time_oracle(wl, inputs)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f32", "storage_dtype": wl.dtype, "data": "synthetic",
+                "config": workload_config(wl, inputs), "roofline": roofline,
+                "phase2_roofline": phase2, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": launches_per_call * args.steps, "clocks": clk,
+                "step_ms": {"min": min(step_ms), "median": statistics.median(step_ms),
+                            "max": max(step_ms)},
+                "wall_s_timed_region": wall1 - wall0, "gpu": torch.cuda.get_device_name(dev)}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,184 @@
+/*
+ * sdm.h -- C ABI of libsdm.so, the GB300 (sm_103a) chunked sparse-delta-memory (SDM)
+ * write/read.
+ *
+ * The operation (sparse-delta-memory 2.0.0, memory_ops.py: the SDMWriteRead docstring's
+ * token loop and the module docstring's chunked form). P parallel streams of T tokens each
+ * advance their own bank of S rows x D columns. Per token t of stream p, in order:
+ *
+ *     a_j    = B[s_j]                 j = 0..W-1, the token's W distinct write slots
+ *     d_j    = exp(g_j) * a_j         only the written rows decay
+ *     ret    = sum_j k_j * d_j        retrieved
+ *     u      = beta * (v - ret)       delta_v
+ *     B[s_j] = d_j + k_j * u          decay-and-write
+ *     o      = sum_i q_i * B[r_i]     readings over the R read slots, after the write
+ *
+ * The library computes it in chunks of C tokens (Phase 1: per-slot log-decays, the dedup
+ * plan, gather weights and the Gram matrices A and QK; the WY solve X = (I + tril(beta A,
+ * -1))^-1, QX = QK X; Phase 2: Nt = ceil(T / C) sequential steps of gather, dual matmul and
+ * decay-and-write), which reproduces the token loop up to floating-point rounding.
+ *
+ * Conventions shared by every entry point
+ *   - Pointers named "device" are CUDA device pointers on the current device; "host" ones
+ *     are ordinary host memory. The caller owns every buffer and the stream.
+ *   - The library never allocates memory and never synchronizes, except where an entry
+ *     point says so (sdm_get_device_status).
+ *   - Arrays are dense row-major with the shapes given. "bank dtype" means float32
+ *     (SDM_F32) or bfloat16 (SDM_BF16) elements, as set in sdm_shape.bank_dtype.
+ *   - stream is a cudaStream_t (NULL = the legacy default stream).
+ *   - Every argument is checked before any work is queued; a refused call returns a
+ *     negative sdm_status, queues nothing, and sdm_last_error() describes the reason.
+ *   - Results are bitwise reproducible for fixed inputs, shape and GPU type: every bank
+ *     row has one writer per step and every sum runs in a fixed order.
+ */
+#ifndef SDM_H
+#define SDM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SDM_OK = 0,
+    SDM_ERR_INVALID = -1,      /* bad argument: null pointer, size out of range */
+    SDM_ERR_UNSUPPORTED = -2,  /* valid but not built: e.g. a head_dim without a kernel */
+    SDM_ERR_CUDA = -3,         /* a CUDA runtime call failed (message in sdm_last_error) */
+    SDM_ERR_TIMEOUT = -4,      /* reserved: a bounded device-side wait gave up */
+    SDM_ERR_WORKSPACE = -5,    /* workspace null, too small or not 256-byte aligned */
+    SDM_ERR_DEVICE = -6        /* the device reported bad input (sdm_get_device_status) */
+} sdm_status;
+
+typedef enum { SDM_F32 = 0, SDM_BF16 = 1 } sdm_dtype;
+
+/* Shape of one call (memory_ops.py, _Layout: P, T, C, Nt, W, R, head_dim).
+ *   P  parallel streams, >= 1
+ *   T  tokens per stream, >= 1
+ *   C  chunk size, 16..256 (the pages' MIN_CHUNK..MAX_CHUNK)
+ *   S  bank rows per stream, 1..2^31-1; stream p owns bank rows [p*S, (p+1)*S)
+ *   D  columns per row (head_dim): 32, 64, 128, 256 or 512
+ *   W  write slots per token, 1..256 (MAX_WIDTH); distinct within a token
+ *   R  read slots per token, 1..256
+ *   bank_dtype  SDM_F32 or SDM_BF16
+ *   slab_steps  Phase-2 steps whose Phase-1 state is held at once; 0 = automatic. The
+ *               results do not depend on it (Phase 1 and the solve are per chunk).
+ *   flags       0 (reserved)
+ * P * ceil(T / C) * C must be below 2^31. */
+typedef struct {
+    int32_t P, T, C, S, D, W, R;
+    int32_t bank_dtype;
+    int32_t slab_steps;
+    int32_t flags;
+} sdm_shape;
+
+/* Device status block, read by sdm_get_device_status. */
+typedef struct {
+    int32_t code;                  /* 0, or SDM_ERR_DEVICE when a slot was out of range */
+    int32_t first_bad_token;       /* stream-major token index (p*T + t) of a bad slot, or -1 */
+    int64_t bad_slots;             /* write/read entries whose slot was outside [0, S) */
+    int64_t repeated_write_slots;  /* write entries repeating a slot of their own token */
+} sdm_device_status;
+
+/* Bytes of device workspace sdm_write_read needs for this shape (0 if the shape is
+ * refused; sdm_last_error says why). Independent of T once T spans more steps than one
+ * slab holds. */
+size_t sdm_workspace_bytes(const sdm_shape *shape);
+
+/* The chunked SDM write/read forward (memory_ops.py: sdm_write_read, no-grad call).
+ *
+ *   bank          device, [P*S, D] bank dtype; read and advanced in place to its final state
+ *   write_slots   device, [P, T, W] int32, per-stream slot ids in [0, S), distinct per token
+ *   write_w       device, [P, T, W] bank dtype, write weights k
+ *   log_decay     device, [P, T, W] float32, g (one log-decay per write entry)
+ *   beta          device, [P, T]    float32, write strength
+ *   v             device, [P, T, D] bank dtype, values
+ *   read_slots    device, [P, T, R] int32, slot ids in [0, S)
+ *   read_w        device, [P, T, R] bank dtype, read weights q
+ *   valid_tokens  device, [P] int32 in [0, T] (values outside are clamped to it), or NULL
+ *                 for all T. Tokens t >= valid[p] are
+ *                 padding: they touch no bank row, their inputs are never read, and their
+ *                 readings rows are zero.
+ *   readings      device, [P, T, D] bank dtype, written (every row)
+ *   workspace     device, >= sdm_workspace_bytes(shape) bytes, 256-byte aligned; its
+ *                 contents need no initialization and are scratch after the call
+ *   stream        cudaStream_t the work is queued on
+ *
+ * Returns SDM_OK once the work is queued (asynchronous). A slot outside [0, S) is not
+ * dereferenced: the entry is dropped, and the device status (sdm_get_device_status) reports
+ * SDM_ERR_DEVICE; repeated write slots in a token are counted there (results for such a
+ * token are unspecified). The bank, readings and inputs must not overlap. */
+int sdm_write_read(const sdm_shape *shape, void *bank, const int32_t *write_slots,
+                   const void *write_w, const float *log_decay, const float *beta,
+                   const void *v, const int32_t *read_slots, const void *read_w,
+                   const int32_t *valid_tokens, void *readings, void *workspace,
+                   size_t workspace_bytes, void *stream);
+
+/* Kernel families, in launch order within a slab: Phase 1 and the solve once per slab, then
+ * gather, dual matmul and DW once per step. */
+enum {
+    SDM_KERNEL_PHASE1 = 0,
+    SDM_KERNEL_SOLVE = 1,
+    SDM_KERNEL_GATHER = 2,
+    SDM_KERNEL_DUALMM = 3,
+    SDM_KERNEL_DW = 4,
+    SDM_KERNEL_KINDS = 5
+};
+
+/* sdm_write_read with a CUDA event recorded before every kernel launch and after the last,
+ * for per-kernel device times (same arguments and results). kernel_ms and launches are host
+ * arrays of SDM_KERNEL_KINDS entries: the summed milliseconds between a launch's event and
+ * the next one, and the launch count, of each kernel family. Creates and destroys its own
+ * events and synchronizes the stream before returning: a measuring tool, not for CUDA graph
+ * capture. */
+int sdm_profile_write_read(const sdm_shape *shape, void *bank, const int32_t *write_slots,
+                           const void *write_w, const float *log_decay, const float *beta,
+                           const void *v, const int32_t *read_slots, const void *read_w,
+                           const int32_t *valid_tokens, void *readings, void *workspace,
+                           size_t workspace_bytes, float *kernel_ms, int32_t *launches,
+                           void *stream);
+
+/* Phase 1 and the solve only, for every chunk of the call, with their outputs copied to
+ * caller buffers (all device, float32 unless noted; N = P * ceil(T / C) chunks, chunk
+ * n = ti * P + p is chunk ti of stream p, i.e. time-major as in phase2_kernels.py):
+ *   perm        [N, C*W] int32   entry index e = t*W + j at each position of the chunk's
+ *                                sorted write row (sorted by (slot, e)); -1 past the valid
+ *                                entries
+ *   group_start [N, C*W] uint8   1 where a group (a run of one slot) begins
+ *   owner       [N, C*W] uint8   1 at the last entry of a group (the group's writer)
+ *   ngroups     [N]      int32   groups (distinct written slots) of the chunk
+ *   lw, gw, dw  [N, C*W]         per write entry, token-major: running log-decay of its
+ *                                slot (inclusive), gather weight k*exp(lw), DW weight
+ *                                k*exp(lend - lw)
+ *   lr, qw      [N, C*R]         per read entry: running log-decay of its slot at its token,
+ *                                gather weight q*exp(lr)
+ *   A, QK, X, QX [N, C, C]       Gram matrices and the solve (X unit lower triangular, +0
+ *                                above the diagonal; QX = QK X)
+ * Any output pointer may be NULL (not copied). The workspace is the one sdm_write_read
+ * takes for the same shape. The bank is not touched. */
+int sdm_phase1_debug(const sdm_shape *shape, const int32_t *write_slots, const void *write_w,
+                     const float *log_decay, const float *beta, const int32_t *read_slots,
+                     const void *read_w, const int32_t *valid_tokens, int32_t *perm,
+                     uint8_t *group_start, uint8_t *owner, int32_t *ngroups, float *lw,
+                     float *gw, float *dw, float *lr, float *qw, float *A, float *QK, float *X,
+                     float *QX, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Reads the device status block of the last call that used this workspace. Synchronizes
+ * the stream. status: host pointer. Returns SDM_OK, or SDM_ERR_CUDA. */
+int sdm_get_device_status(const void *workspace, sdm_device_status *status, void *stream);
+
+/* Number of kernel launches sdm_write_read queues for this shape (0 if refused). */
+int64_t sdm_launch_count(const sdm_shape *shape);
+
+/* Thread-local description of the last refused call or CUDA error ("" if none). */
+const char *sdm_last_error(void);
+
+/* Library version string. */
+const char *sdm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SDM_H */

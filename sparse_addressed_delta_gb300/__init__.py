@@ -1,0 +1,271 @@
+"""GB300 (sm_103a) chunked sparse-delta-memory write/read.
+
+A thin ctypes binding of ``libsdm.so`` (the C ABI in ``include/sdm.h``): it checks tensor
+shapes, dtypes and devices, allocates the outputs and the workspace with PyTorch, and passes
+raw device pointers and the current CUDA stream. Every step of the computation runs in the
+library's CUDA kernels; there is no other implementation to fall back on, and a missing
+library is an error.
+
+Main entry point: :func:`sdm_write_read` (sparse-delta-memory 2.0.0, memory_ops.py
+``sdm_write_read``, no-grad call) -> readings, with the bank advanced in place.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Dict, Optional
+
+import torch
+
+__all__ = ["sdm_write_read", "profile_write_read", "workspace_bytes", "launch_count",
+           "phase1_debug", "KERNEL_KINDS",
+           "device_status", "SdmError", "Shape", "library", "library_path", "version"]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_HERE, "libsdm.so")
+
+SDM_F32, SDM_BF16 = 0, 1
+KERNEL_KINDS = ("phase1", "solve", "gather", "dualmm", "dw")
+_STATUS = {0: "SDM_OK", -1: "SDM_ERR_INVALID", -2: "SDM_ERR_UNSUPPORTED", -3: "SDM_ERR_CUDA",
+           -4: "SDM_ERR_TIMEOUT", -5: "SDM_ERR_WORKSPACE", -6: "SDM_ERR_DEVICE"}
+
+
+class SdmError(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(f"{_STATUS.get(code, code)}: {message}")
+        self.code = code
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("P", ctypes.c_int32), ("T", ctypes.c_int32), ("C", ctypes.c_int32),
+                ("S", ctypes.c_int32), ("D", ctypes.c_int32), ("W", ctypes.c_int32),
+                ("R", ctypes.c_int32), ("bank_dtype", ctypes.c_int32),
+                ("slab_steps", ctypes.c_int32), ("flags", ctypes.c_int32)]
+
+
+class _DeviceStatus(ctypes.Structure):
+    _fields_ = [("code", ctypes.c_int32), ("first_bad_token", ctypes.c_int32),
+                ("bad_slots", ctypes.c_int64), ("repeated_write_slots", ctypes.c_int64)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library() -> ctypes.CDLL:
+    """The loaded libsdm.so (built in-tree by ``__graft_entry__.build()``)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(library_path):
+                raise ImportError(
+                    f"libsdm.so is not built ({library_path} is missing); run "
+                    "`python -c 'import __graft_entry__ as g; g.build()'` first")
+            lib = ctypes.CDLL(library_path)
+            vp, sz, i32, i64 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_int64
+            sp = ctypes.POINTER(Shape)
+            lib.sdm_workspace_bytes.argtypes = [sp]
+            lib.sdm_workspace_bytes.restype = sz
+            lib.sdm_launch_count.argtypes = [sp]
+            lib.sdm_launch_count.restype = i64
+            lib.sdm_write_read.argtypes = [sp] + [vp] * 10 + [vp, sz, vp]
+            lib.sdm_write_read.restype = i32
+            lib.sdm_profile_write_read.argtypes = ([sp] + [vp] * 10 + [vp, sz]
+                                                   + [ctypes.POINTER(ctypes.c_float),
+                                                      ctypes.POINTER(ctypes.c_int32), vp])
+            lib.sdm_profile_write_read.restype = i32
+            lib.sdm_phase1_debug.argtypes = [sp] + [vp] * 7 + [vp] * 13 + [vp, sz, vp]
+            lib.sdm_phase1_debug.restype = i32
+            lib.sdm_get_device_status.argtypes = [vp, ctypes.POINTER(_DeviceStatus), vp]
+            lib.sdm_get_device_status.restype = i32
+            lib.sdm_last_error.argtypes = []
+            lib.sdm_last_error.restype = ctypes.c_char_p
+            lib.sdm_version.argtypes = []
+            lib.sdm_version.restype = ctypes.c_char_p
+            _lib = lib
+    return _lib
+
+
+def version() -> str:
+    return library().sdm_version().decode()
+
+
+def _check(rc: int) -> None:
+    if rc != 0:
+        raise SdmError(rc, library().sdm_last_error().decode())
+
+
+def _dtype_code(dtype: torch.dtype) -> int:
+    if dtype == torch.float32:
+        return SDM_F32
+    if dtype == torch.bfloat16:
+        return SDM_BF16
+    raise TypeError(f"bank dtype must be float32 or bfloat16, got {dtype}")
+
+
+def make_shape(P, T, C, S, D, W, R, dtype, slab_steps: int = 0) -> Shape:
+    code = dtype if isinstance(dtype, int) else _dtype_code(dtype)
+    return Shape(P, T, C, S, D, W, R, code, slab_steps, 0)
+
+
+def workspace_bytes(shape: Shape) -> int:
+    n = library().sdm_workspace_bytes(ctypes.byref(shape))
+    if n == 0:
+        raise SdmError(-1, library().sdm_last_error().decode())
+    return int(n)
+
+
+def launch_count(shape: Shape) -> int:
+    return int(library().sdm_launch_count(ctypes.byref(shape)))
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t: torch.Tensor, name: str, shape, dtype, device) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, the bank on {device}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def alloc_workspace(shape: Shape, device) -> torch.Tensor:
+    """A workspace tensor (uint8, 256-byte aligned by the caching allocator)."""
+    return torch.empty(workspace_bytes(shape), dtype=torch.uint8, device=device)
+
+
+def _stream_ptr(stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def sdm_write_read(bank: torch.Tensor, write_slots: torch.Tensor, write_w: torch.Tensor,
+                   log_decay: torch.Tensor, beta: torch.Tensor, v: torch.Tensor,
+                   read_slots: torch.Tensor, read_w: torch.Tensor,
+                   valid_tokens: Optional[torch.Tensor] = None, *, chunk_size: int,
+                   slab_steps: int = 0, workspace: Optional[torch.Tensor] = None,
+                   readings: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Chunked SDM write/read over P streams; returns readings [P, T, D] and advances
+    ``bank`` ([P*S, D], float32 or bfloat16, stream p owning rows [p*S, (p+1)*S)) in place.
+
+    write_slots [P, T, W] int32; write_w [P, T, W] bank dtype; log_decay [P, T, W] float32;
+    beta [P, T] float32; v [P, T, D] bank dtype; read_slots [P, T, R] int32; read_w
+    [P, T, R] bank dtype; valid_tokens [P] int32 (None: all T valid).
+    """
+    if write_slots.dim() != 3:
+        raise ValueError("write_slots must be [P, T, W]")
+    P, T, W = write_slots.shape
+    R = read_slots.shape[-1]
+    if bank.dim() != 2 or bank.shape[0] % P:
+        raise ValueError(f"bank must be [P*S, D] with P={P}, got {tuple(bank.shape)}")
+    S, D = bank.shape[0] // P, bank.shape[1]
+    dev, dt = bank.device, bank.dtype
+    if dev.type != "cuda":
+        raise ValueError("the bank must be a CUDA tensor")
+    _need(bank, "bank", (P * S, D), dt, dev)
+    _need(write_slots, "write_slots", (P, T, W), torch.int32, dev)
+    _need(write_w, "write_w", (P, T, W), dt, dev)
+    _need(log_decay, "log_decay", (P, T, W), torch.float32, dev)
+    _need(beta, "beta", (P, T), torch.float32, dev)
+    _need(v, "v", (P, T, D), dt, dev)
+    _need(read_slots, "read_slots", (P, T, R), torch.int32, dev)
+    _need(read_w, "read_w", (P, T, R), dt, dev)
+    if valid_tokens is not None:
+        _need(valid_tokens, "valid_tokens", (P,), torch.int32, dev)
+    shape = make_shape(P, T, chunk_size, S, D, W, R, dt, slab_steps)
+    if readings is None:
+        readings = torch.empty((P, T, D), dtype=dt, device=dev)
+    else:
+        _need(readings, "readings", (P, T, D), dt, dev)
+    if workspace is None:
+        workspace = alloc_workspace(shape, dev)
+    with torch.cuda.device(dev):
+        rc = library().sdm_write_read(
+            ctypes.byref(shape), _ptr(bank), _ptr(write_slots), _ptr(write_w), _ptr(log_decay),
+            _ptr(beta), _ptr(v), _ptr(read_slots), _ptr(read_w), _ptr(valid_tokens),
+            _ptr(readings), _ptr(workspace), workspace.numel(), _stream_ptr(stream))
+    _check(rc)
+    return readings
+
+
+def profile_write_read(bank, write_slots, write_w, log_decay, beta, v, read_slots, read_w,
+                       valid_tokens=None, *, chunk_size: int, slab_steps: int = 0,
+                       workspace=None, readings=None, stream=None):
+    """One sdm_write_read call with CUDA events around every kernel launch (synchronizes).
+    Returns (readings, {family: (total_ms, launches)}) for the families in KERNEL_KINDS."""
+    P, T, W = write_slots.shape
+    R = read_slots.shape[-1]
+    S, D = bank.shape[0] // P, bank.shape[1]
+    dev, dt = bank.device, bank.dtype
+    shape = make_shape(P, T, chunk_size, S, D, W, R, dt, slab_steps)
+    if readings is None:
+        readings = torch.empty((P, T, D), dtype=dt, device=dev)
+    if workspace is None:
+        workspace = alloc_workspace(shape, dev)
+    for t, name in ((write_slots, "write_slots"), (read_slots, "read_slots")):
+        _need(t, name, t.shape, torch.int32, dev)
+    ms = (ctypes.c_float * len(KERNEL_KINDS))()
+    cnt = (ctypes.c_int32 * len(KERNEL_KINDS))()
+    with torch.cuda.device(dev):
+        rc = library().sdm_profile_write_read(
+            ctypes.byref(shape), _ptr(bank), _ptr(write_slots), _ptr(write_w), _ptr(log_decay),
+            _ptr(beta), _ptr(v), _ptr(read_slots), _ptr(read_w), _ptr(valid_tokens),
+            _ptr(readings), _ptr(workspace), workspace.numel(), ms, cnt, _stream_ptr(stream))
+    _check(rc)
+    return readings, {k: (float(ms[i]), int(cnt[i])) for i, k in enumerate(KERNEL_KINDS)}
+
+
+def phase1_debug(write_slots, write_w, log_decay, beta, read_slots, read_w, valid_tokens=None,
+                 *, S: int, D: int, chunk_size: int, slab_steps: int = 0,
+                 stream=None) -> Dict[str, torch.Tensor]:
+    """Phase 1 and the solve of every chunk (time-major chunk n = ti*P + p), as tensors:
+    perm, group_start, owner [N, C*W]; ngroups [N]; lw, gw, dw [N, C*W]; lr, qw [N, C*R];
+    A, QK, X, QX [N, C, C]."""
+    P, T, W = write_slots.shape
+    R = read_slots.shape[-1]
+    dev, dt = write_w.device, write_w.dtype
+    C = chunk_size
+    shape = make_shape(P, T, C, S, D, W, R, dt, slab_steps)
+    N = P * (-(-T // C))
+    f32 = dict(dtype=torch.float32, device=dev)
+    out = {
+        "perm": torch.empty((N, C * W), dtype=torch.int32, device=dev),
+        "group_start": torch.empty((N, C * W), dtype=torch.uint8, device=dev),
+        "owner": torch.empty((N, C * W), dtype=torch.uint8, device=dev),
+        "ngroups": torch.empty((N,), dtype=torch.int32, device=dev),
+        "lw": torch.empty((N, C * W), **f32), "gw": torch.empty((N, C * W), **f32),
+        "dw": torch.empty((N, C * W), **f32), "lr": torch.empty((N, C * R), **f32),
+        "qw": torch.empty((N, C * R), **f32), "A": torch.empty((N, C, C), **f32),
+        "QK": torch.empty((N, C, C), **f32), "X": torch.empty((N, C, C), **f32),
+        "QX": torch.empty((N, C, C), **f32),
+    }
+    ws = alloc_workspace(shape, dev)
+    order = ["perm", "group_start", "owner", "ngroups", "lw", "gw", "dw", "lr", "qw", "A", "QK",
+             "X", "QX"]
+    with torch.cuda.device(dev):
+        rc = library().sdm_phase1_debug(
+            ctypes.byref(shape), _ptr(write_slots), _ptr(write_w), _ptr(log_decay), _ptr(beta),
+            _ptr(read_slots), _ptr(read_w), _ptr(valid_tokens), *[_ptr(out[k]) for k in order],
+            _ptr(ws), ws.numel(), _stream_ptr(stream))
+    _check(rc)
+    out["workspace"] = ws
+    return out
+
+
+def device_status(workspace: torch.Tensor, stream=None) -> Dict[str, int]:
+    """The device status block of the last call that used ``workspace`` (synchronizes)."""
+    st = _DeviceStatus()
+    with torch.cuda.device(workspace.device):
+        _check(library().sdm_get_device_status(_ptr(workspace), ctypes.byref(st),
+                                               _stream_ptr(stream)))
+    return {"code": st.code, "first_bad_token": st.first_bad_token, "bad_slots": st.bad_slots,
+            "repeated_write_slots": st.repeated_write_slots}

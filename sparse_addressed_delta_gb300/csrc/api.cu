@@ -1,0 +1,361 @@
+// C ABI of libsdm (declared and documented in include/sdm.h): argument checks, the workspace
+// layout, and the launch sequence of the chunked write/read.
+//
+// Launch sequence of sdm_write_read (sparse-delta-memory 2.0.0, memory_ops.py module
+// docstring "Forward"; the slabs follow _sdm_forward's bounded-memory no-grad steps):
+//   status block cleared
+//   for each slab of `ns` steps:        Phase 1 (one CTA per chunk), WY solve
+//       for each step ti of the slab:   gather -> dual matmul -> DW
+// Everything is queued on the caller's stream; nothing is allocated and nothing synchronizes.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <vector>
+
+#include "sdm_internal.cuh"
+
+namespace sdm {
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
+int fail(int code, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char *what) {
+    return fail(SDM_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+// Checks the shape; fills d. Returns SDM_OK or a refusal (message set).
+int check_shape(const sdm_shape *s, Dims &d) {
+    if (!s) return fail(SDM_ERR_INVALID, "shape is NULL");
+    if (s->P < 1) return fail(SDM_ERR_INVALID, "P must be >= 1, got %d", s->P);
+    if (s->T < 1) return fail(SDM_ERR_INVALID, "T must be >= 1, got %d", s->T);
+    if (s->C < kMinChunk || s->C > kMaxChunk)
+        return fail(SDM_ERR_INVALID, "chunk size C must be in %d..%d, got %d", kMinChunk,
+                    kMaxChunk, s->C);
+    if (s->S < 1) return fail(SDM_ERR_INVALID, "S must be >= 1, got %d", s->S);
+    if (s->W < 1 || s->W > kMaxWidth || s->R < 1 || s->R > kMaxWidth)
+        return fail(SDM_ERR_INVALID, "W and R must be in 1..%d, got W=%d R=%d", kMaxWidth, s->W,
+                    s->R);
+    if (s->bank_dtype != SDM_F32 && s->bank_dtype != SDM_BF16)
+        return fail(SDM_ERR_INVALID, "bank_dtype must be SDM_F32 (0) or SDM_BF16 (1), got %d",
+                    s->bank_dtype);
+    if (s->slab_steps < 0) return fail(SDM_ERR_INVALID, "slab_steps must be >= 0");
+    if (s->flags != 0) return fail(SDM_ERR_INVALID, "flags must be 0, got %d", s->flags);
+    if (s->D != 32 && s->D != 64 && s->D != 128 && s->D != 256 && s->D != 512)
+        return fail(SDM_ERR_UNSUPPORTED, "head_dim D=%d has no kernel (32, 64, 128, 256, 512)",
+                    s->D);
+    const long long Nt = (s->T + (long long)s->C - 1) / s->C;
+    if ((long long)s->P * Nt * s->C >= (1LL << 31))
+        return fail(SDM_ERR_INVALID, "P * ceil(T/C) * C = %lld token rows exceed 2^31 - 1",
+                    (long long)s->P * Nt * s->C);
+    d.P = s->P; d.T = s->T; d.C = s->C; d.S = s->S; d.D = s->D; d.W = s->W; d.R = s->R;
+    d.Nt = (int)Nt;
+    d.dtype = s->bank_dtype;
+    return SDM_OK;
+}
+
+size_t per_chunk_bytes(const Dims &d) {
+    const size_t CW = (size_t)d.C * d.W, CR = (size_t)d.C * d.R, CC = (size_t)d.C * d.C;
+    return 4 * (8 * CW + 1) + 4 * 2 * CR + 4 * 4 * CC + 8;
+}
+
+int slab_steps(const Dims &d, int requested) {
+    if (requested > 0) return requested < d.Nt ? requested : d.Nt;
+    const size_t per_step = per_chunk_bytes(d) * d.P;
+    if (per_step * d.Nt <= kSlabBudget) return d.Nt;
+    long ns = (long)(kSlabBudget / per_step);
+    const long min_steps = (kRefSms + d.P - 1) / d.P;   // at least one chunk per SM
+    if (ns < min_steps) ns = min_steps;
+    if (ns < 1) ns = 1;
+    return ns < d.Nt ? (int)ns : d.Nt;
+}
+
+}  // namespace
+
+int phase1_ctas(const Dims &d, int ns) {
+    const long N = (long)ns * d.P;
+    const long cap = (long)(d.C * d.W <= 4096 ? 2 : 1) * kRefSms;
+    return (int)(N < cap ? N : cap);
+}
+
+// Byte layout of the workspace (every array 256-byte aligned), in assignment order.
+#define SDM_LAYOUT(F)                                                         \
+    F(status, DevStatus, 1)                                                   \
+    F(perm, int32_t, N * CW)                                                  \
+    F(wdw, float, N * CW)                                                     \
+    F(goff, int32_t, N * (CW + 1))                                            \
+    F(gslot, int32_t, N * CW)                                                 \
+    F(gfac, float, N * CW)                                                    \
+    F(ngroups, int32_t, N)                                                    \
+    F(nvalid, int32_t, N)                                                     \
+    F(gw, float, N * CW)                                                      \
+    F(qw, float, N * CR)                                                      \
+    F(lw, float, N * CW)                                                      \
+    F(lr, float, N * CR)                                                      \
+    F(A, float, N * CC)                                                       \
+    F(QK, float, N * CC)                                                      \
+    F(X, float, N * CC)                                                       \
+    F(QX, float, N * CC)                                                      \
+    F(keys, unsigned long long, G * 2 * CW)                                   \
+    F(inv, int32_t, G * CW)                                                   \
+    F(lws, float, G * CW)                                                     \
+    F(pgid, int32_t, G * CW)                                                  \
+    F(lend, float, G * CW)                                                    \
+    F(kf, float, G * CW)                                                      \
+    F(rlo, int32_t, G * CR)                                                   \
+    F(rhi, int32_t, G * CR)                                                   \
+    F(ret, float, P * CD)                                                     \
+    F(inter, float, P * CD)                                                   \
+    F(dv, float, P * CD)
+
+size_t layout_bytes(const Dims &d, int ns, int G_) {
+    const size_t N = (size_t)ns * d.P, P = d.P, CW = (size_t)d.C * d.W, CR = (size_t)d.C * d.R,
+                 CC = (size_t)d.C * d.C, CD = (size_t)d.C * d.D, G = G_;
+    size_t off = 0;
+#define X_SIZE(name, type, count) off += up(sizeof(type) * (size_t)(count));
+    SDM_LAYOUT(X_SIZE)
+#undef X_SIZE
+    return off;
+}
+
+Work layout_assign(const Dims &d, int ns, int G_, void *base) {
+    const size_t N = (size_t)ns * d.P, P = d.P, CW = (size_t)d.C * d.W, CR = (size_t)d.C * d.R,
+                 CC = (size_t)d.C * d.C, CD = (size_t)d.C * d.D, G = G_;
+    Work w;
+    memset(&w, 0, sizeof(w));
+    char *p = static_cast<char *>(base);
+    size_t off = 0;
+#define X_ASSIGN(name, type, count)                                   \
+    w.name = reinterpret_cast<type *>(p + off);                       \
+    off += up(sizeof(type) * (size_t)(count));
+    SDM_LAYOUT(X_ASSIGN)
+#undef X_ASSIGN
+    w.ns = ns;
+    w.G = G_;
+    return w;
+}
+
+namespace {
+
+struct Prepared {
+    Dims d;
+    int ns, G;
+    size_t bytes;
+};
+
+int prepare(const sdm_shape *shape, Prepared &pr) {
+    int rc = check_shape(shape, pr.d);
+    if (rc) return rc;
+    pr.ns = slab_steps(pr.d, shape->slab_steps);
+    pr.G = phase1_ctas(pr.d, pr.ns);
+    pr.bytes = layout_bytes(pr.d, pr.ns, pr.G);
+    return SDM_OK;
+}
+
+int check_workspace(const Prepared &pr, void *ws, size_t bytes) {
+    if (!ws) return fail(SDM_ERR_WORKSPACE, "workspace is NULL");
+    if (reinterpret_cast<uintptr_t>(ws) % kAlign)
+        return fail(SDM_ERR_WORKSPACE, "workspace must be %zu-byte aligned", kAlign);
+    if (bytes < pr.bytes)
+        return fail(SDM_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", bytes, pr.bytes);
+    return SDM_OK;
+}
+
+// Events around every launch of a profiled call (one before each launch, one after the last).
+struct Recorder {
+    std::vector<cudaEvent_t> ev;
+    std::vector<int> kind;
+    cudaError_t mark(int k, cudaStream_t st) {
+        cudaEvent_t e;
+        cudaError_t err = cudaEventCreate(&e);
+        if (err != cudaSuccess) return err;
+        ev.push_back(e);
+        if (k >= 0) kind.push_back(k);
+        return cudaEventRecord(e, st);
+    }
+};
+
+int check_inputs(const Inputs &in, bool need_bank) {
+    if ((need_bank && !in.bank) || !in.ws || !in.kw || !in.g || !in.beta || !in.rs || !in.qw)
+        return fail(SDM_ERR_INVALID, "a required input pointer is NULL");
+    if (need_bank && (!in.v || !in.readings))
+        return fail(SDM_ERR_INVALID, "v and readings must not be NULL");
+    if (need_bank && (reinterpret_cast<uintptr_t>(in.bank) % 16 ||
+                      reinterpret_cast<uintptr_t>(in.readings) % 16))
+        return fail(SDM_ERR_INVALID, "bank and readings must be 16-byte aligned");
+    return SDM_OK;
+}
+
+// The launch sequence of one forward call (see the file comment).
+int run_forward(const Prepared &pr, const Inputs &in, void *workspace, cudaStream_t st,
+                Recorder *rec) {
+    const Dims &d = pr.d;
+    Work w = layout_assign(d, pr.ns, pr.G, workspace);
+    cudaError_t e = cudaMemsetAsync(w.status, 0, sizeof(DevStatus), st);
+    if (e != cudaSuccess) return cuda_fail(e, "status clear");
+#define SDM_LAUNCH(kind, call, what)                                                       \
+    do {                                                                                   \
+        if (rec && (e = rec->mark(kind, st)) != cudaSuccess) return cuda_fail(e, "event");  \
+        if ((e = (call)) != cudaSuccess) return cuda_fail(e, what);                        \
+    } while (0)
+    for (int s0 = 0; s0 < d.Nt; s0 += pr.ns) {
+        const int nsteps = (d.Nt - s0) < pr.ns ? (d.Nt - s0) : pr.ns;
+        SDM_LAUNCH(SDM_KERNEL_PHASE1, launch_phase1(d, in, w, s0, nsteps, st), "phase1");
+        SDM_LAUNCH(SDM_KERNEL_SOLVE, launch_solve(d, in, w, s0, nsteps, st), "solve");
+        for (int ti = s0; ti < s0 + nsteps; ++ti) {
+            SDM_LAUNCH(SDM_KERNEL_GATHER, launch_gather(d, in, w, s0, ti, st), "gather");
+            SDM_LAUNCH(SDM_KERNEL_DUALMM, launch_dualmm(d, in, w, s0, ti, st), "dual matmul");
+            SDM_LAUNCH(SDM_KERNEL_DW, launch_dw(d, in, w, s0, ti, st), "dw");
+        }
+    }
+#undef SDM_LAUNCH
+    if (rec && (e = rec->mark(-1, st)) != cudaSuccess) return cuda_fail(e, "event");
+    return SDM_OK;
+}
+
+}  // namespace
+}  // namespace sdm
+
+using namespace sdm;
+
+extern "C" {
+
+const char *sdm_last_error(void) { return g_err; }
+
+const char *sdm_version(void) { return "sdm-gb300 0.1 (sm_103a)"; }
+
+size_t sdm_workspace_bytes(const sdm_shape *shape) {
+    Prepared pr;
+    if (prepare(shape, pr)) return 0;
+    g_err[0] = 0;
+    return pr.bytes;
+}
+
+int64_t sdm_launch_count(const sdm_shape *shape) {
+    Prepared pr;
+    if (prepare(shape, pr)) return 0;
+    const int64_t slabs = (pr.d.Nt + pr.ns - 1) / pr.ns;
+    return slabs * 2 + (int64_t)pr.d.Nt * 3;
+}
+
+int sdm_write_read(const sdm_shape *shape, void *bank, const int32_t *write_slots,
+                   const void *write_w, const float *log_decay, const float *beta,
+                   const void *v, const int32_t *read_slots, const void *read_w,
+                   const int32_t *valid_tokens, void *readings, void *workspace,
+                   size_t workspace_bytes, void *stream) {
+    Prepared pr;
+    int rc = prepare(shape, pr);
+    if (rc) return rc;
+    Inputs in{bank, write_slots, write_w, log_decay, beta, v, read_slots, read_w, valid_tokens,
+              readings};
+    if ((rc = check_inputs(in, true))) return rc;
+    if ((rc = check_workspace(pr, workspace, workspace_bytes))) return rc;
+    g_err[0] = 0;
+    return run_forward(pr, in, workspace, static_cast<cudaStream_t>(stream), nullptr);
+}
+
+int sdm_profile_write_read(const sdm_shape *shape, void *bank, const int32_t *write_slots,
+                           const void *write_w, const float *log_decay, const float *beta,
+                           const void *v, const int32_t *read_slots, const void *read_w,
+                           const int32_t *valid_tokens, void *readings, void *workspace,
+                           size_t workspace_bytes, float *kernel_ms, int32_t *launches,
+                           void *stream) {
+    Prepared pr;
+    int rc = prepare(shape, pr);
+    if (rc) return rc;
+    Inputs in{bank, write_slots, write_w, log_decay, beta, v, read_slots, read_w, valid_tokens,
+              readings};
+    if ((rc = check_inputs(in, true))) return rc;
+    if ((rc = check_workspace(pr, workspace, workspace_bytes))) return rc;
+    if (!kernel_ms || !launches) return fail(SDM_ERR_INVALID, "kernel_ms and launches must not be NULL");
+    g_err[0] = 0;
+    Recorder r;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    rc = run_forward(pr, in, workspace, st, &r);
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (!rc && e != cudaSuccess) rc = cuda_fail(e, "profile synchronize");
+    for (int k = 0; k < SDM_KERNEL_KINDS; ++k) { kernel_ms[k] = 0.f; launches[k] = 0; }
+    if (!rc) {
+        for (size_t i = 0; i + 1 < r.ev.size(); ++i) {
+            float ms = 0.f;
+            e = cudaEventElapsedTime(&ms, r.ev[i], r.ev[i + 1]);
+            if (e != cudaSuccess) { rc = cuda_fail(e, "profile elapsed time"); break; }
+            kernel_ms[r.kind[i]] += ms;
+            launches[r.kind[i]] += 1;
+        }
+    }
+    for (cudaEvent_t ev : r.ev) cudaEventDestroy(ev);
+    return rc;
+}
+
+int sdm_phase1_debug(const sdm_shape *shape, const int32_t *write_slots, const void *write_w,
+                     const float *log_decay, const float *beta, const int32_t *read_slots,
+                     const void *read_w, const int32_t *valid_tokens, int32_t *perm,
+                     uint8_t *group_start, uint8_t *owner, int32_t *ngroups, float *lw,
+                     float *gw, float *dw, float *lr, float *qw, float *A, float *QK, float *X,
+                     float *QX, void *workspace, size_t workspace_bytes, void *stream) {
+    Prepared pr;
+    int rc = prepare(shape, pr);
+    if (rc) return rc;
+    Inputs in{nullptr, write_slots, write_w, log_decay, beta, nullptr, read_slots, read_w,
+              valid_tokens, nullptr};
+    if ((rc = check_inputs(in, false))) return rc;
+    if ((rc = check_workspace(pr, workspace, workspace_bytes))) return rc;
+    if ((perm != nullptr) != (group_start != nullptr) || (perm != nullptr) != (owner != nullptr) ||
+        (perm != nullptr) != (dw != nullptr))
+        return fail(SDM_ERR_INVALID, "perm, group_start, owner and dw are requested together");
+    g_err[0] = 0;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const Dims &d = pr.d;
+    Work w = layout_assign(d, pr.ns, pr.G, workspace);
+    const size_t CW = (size_t)d.C * d.W, CR = (size_t)d.C * d.R, CC = (size_t)d.C * d.C;
+    cudaError_t e = cudaMemsetAsync(w.status, 0, sizeof(DevStatus), st);
+    if (e != cudaSuccess) return cuda_fail(e, "status clear");
+    for (int s0 = 0; s0 < d.Nt; s0 += pr.ns) {
+        const int nsteps = (d.Nt - s0) < pr.ns ? (d.Nt - s0) : pr.ns;
+        const size_t N = (size_t)nsteps * d.P, n0 = (size_t)s0 * d.P;
+        if ((e = launch_phase1(d, in, w, s0, nsteps, st)) != cudaSuccess) return cuda_fail(e, "phase1");
+        if ((e = launch_solve(d, in, w, s0, nsteps, st)) != cudaSuccess) return cuda_fail(e, "solve");
+        if (perm && (e = launch_debug_expand(d, w, (int)N, perm + n0 * CW, group_start + n0 * CW,
+                                             owner + n0 * CW, dw + n0 * CW, st)) != cudaSuccess)
+            return cuda_fail(e, "debug expand");
+        struct { void *dst; const void *src; size_t per; } cp[] = {
+            {ngroups, w.ngroups, 4}, {lw, w.lw, 4 * CW}, {gw, w.gw, 4 * CW},
+            {lr, w.lr, 4 * CR}, {qw, w.qw, 4 * CR}, {A, w.A, 4 * CC}, {QK, w.QK, 4 * CC},
+            {X, w.X, 4 * CC}, {QX, w.QX, 4 * CC}};
+        for (auto &c : cp) {
+            if (!c.dst) continue;
+            e = cudaMemcpyAsync(static_cast<char *>(c.dst) + n0 * c.per, c.src, N * c.per,
+                                cudaMemcpyDeviceToDevice, st);
+            if (e != cudaSuccess) return cuda_fail(e, "debug copy");
+        }
+    }
+    return SDM_OK;
+}
+
+int sdm_get_device_status(const void *workspace, sdm_device_status *status, void *stream) {
+    if (!workspace || !status) return fail(SDM_ERR_INVALID, "workspace and status must not be NULL");
+    DevStatus h;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(&h, workspace, sizeof(h), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "status read");
+    status->code = h.code;
+    status->first_bad_token = h.first_bad_plus1 - 1;
+    status->bad_slots = (int64_t)h.bad_slots;
+    status->repeated_write_slots = (int64_t)h.repeated_write_slots;
+    return SDM_OK;
+}
+
+}  // extern "C"

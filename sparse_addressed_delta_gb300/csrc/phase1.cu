@@ -1,0 +1,392 @@
+// Phase 1 of the chunked SDM write/read: the memory-independent quantities of every chunk
+// (sparse-delta-memory 2.0.0, memory_ops.py module docstring, "Phase 1"; the sorted kind row
+// and its groups are the phase2_kernels.py module docstring's "Determinism" paragraph).
+//
+// One CTA per chunk (a persistent grid walks the slab's chunks). For chunk (p, ti) with n
+// valid tokens:
+//   1. the n*W write entries e = t*W + j are sorted by (slot, e): a stable LSD radix sort on
+//      the slot bits of 64-bit keys (slot << 32 | e), in global scratch private to the CTA;
+//   2. a group is a run of one slot in that row; its members are the slot's writes in token
+//      order. A segmented scan of g along the row gives lw, the running log-decay of the slot
+//      at each write (inclusive), and its group total lend;
+//   3. gather weights gw = k exp(lw), DW weights dw = k exp(lend - lw), the group factor
+//      exp(lend), and for each read entry (slot r, token t): lr = lw of the last write of r at
+//      a token <= t (0 if none), qw = q exp(lr);
+//   4. A[t][u] = sum over pairs of writes of one slot at tokens u < t of
+//      k_t k_u exp(lw_t - lw_u), and QK[t][u] = the same over (read at t, write at u <= t)
+//      with q_t and lr_t: one warp per row, its lanes over the earlier members of each group
+//      (distinct tokens, so no two lanes add to one element), entries of the row in order.
+// Every exponent is a difference of running log-decays of one slot; all sums run in a fixed
+// order, so the outputs are bitwise reproducible.
+#include "sdm_internal.cuh"
+
+namespace sdm {
+namespace {
+
+constexpr int NT = 512;          // threads per Phase-1 CTA
+constexpr int NW = NT / 32;
+
+struct P1Smem {
+    int hist[256];
+    int base[256];
+    int tile_total[256];
+    int wcnt[NW][256];
+    float wv[NW];
+    int wf[NW];
+    int wi[NW];
+    float total_v;
+    int total_i;
+    float row[NW][kMaxChunk];
+};
+
+// One stable counting pass of the LSD radix sort: n keys from `in` to `out` by the 8-bit
+// digit at `shift`. Tiles of NT keys keep their order: a key's rank among equal digits of its
+// warp (match_any) plus the counts of earlier warps and earlier tiles.
+__device__ void radix_pass(const unsigned long long *in, unsigned long long *out, int n,
+                           int shift, P1Smem &sm) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int i = tid; i < 256; i += NT) sm.hist[i] = 0;
+    for (int i = tid; i < NW * 256; i += NT) (&sm.wcnt[0][0])[i] = 0;
+    __syncthreads();
+    for (int i = tid; i < n; i += NT) atomicAdd(&sm.hist[(int)((in[i] >> shift) & 255ull)], 1);
+    __syncthreads();
+    if (warp == 0) {
+        int v[8], s = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) { v[k] = sm.hist[lane * 8 + k]; s += v[k]; }
+        int incl = s;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += y;
+        }
+        int run = incl - s;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) { sm.base[lane * 8 + k] = run; run += v[k]; }
+    }
+    __syncthreads();
+    for (int tile = 0; tile < n; tile += NT) {
+        const int i = tile + tid;
+        const bool ok = i < n;
+        const unsigned long long key = ok ? in[i] : 0ull;
+        const int d = ok ? (int)((key >> shift) & 255ull) : 256;
+        const unsigned peers = __match_any_sync(0xffffffffu, d);
+        const int rank = __popc(peers & ((1u << lane) - 1u));
+        if (ok && lane == __ffs(peers) - 1) sm.wcnt[warp][d] = __popc(peers);
+        __syncthreads();
+        for (int dd = tid; dd < 256; dd += NT) {
+            int run = 0;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                int c = sm.wcnt[w][dd];
+                sm.wcnt[w][dd] = run;
+                run += c;
+            }
+            sm.tile_total[dd] = run;
+        }
+        __syncthreads();
+        if (ok) out[sm.base[d] + sm.wcnt[warp][d] + rank] = key;
+        __syncthreads();
+        for (int dd = tid; dd < 256; dd += NT) {
+            sm.base[dd] += sm.tile_total[dd];
+#pragma unroll
+            for (int w = 0; w < NW; ++w) sm.wcnt[w][dd] = 0;
+        }
+        __syncthreads();
+    }
+}
+
+// Block-wide inclusive scan of (segment head, value) pairs with a carried-in prefix; returns
+// each thread's inclusive value and sets `carry` (all threads) to the last thread's value.
+__device__ float seg_scan(bool head, float val, float carry_in, float &carry, P1Smem &sm) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int f = head ? 1 : 0;
+    float v = val;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        float pv = __shfl_up_sync(0xffffffffu, v, off);
+        int pf = __shfl_up_sync(0xffffffffu, f, off);
+        if (lane >= off) {
+            if (!f) v = pv + v;
+            f |= pf;
+        }
+    }
+    if (lane == 31) { sm.wv[warp] = v; sm.wf[warp] = f; }
+    __syncthreads();
+    if (warp == 0) {
+        float wv = lane < NW ? sm.wv[lane] : 0.f;
+        int wf = lane < NW ? sm.wf[lane] : 0;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            float pv = __shfl_up_sync(0xffffffffu, wv, off);
+            int pf = __shfl_up_sync(0xffffffffu, wf, off);
+            if (lane >= off) {
+                if (!wf) wv = pv + wv;
+                wf |= pf;
+            }
+        }
+        float ev = __shfl_up_sync(0xffffffffu, wv, 1);
+        int ef = __shfl_up_sync(0xffffffffu, wf, 1);
+        float pre = (lane == 0) ? carry_in : (ef ? ev : carry_in + ev);
+        if (lane < NW) sm.wv[lane] = pre;
+        if (lane == NW - 1) sm.total_v = wf ? wv : carry_in + wv;
+    }
+    __syncthreads();
+    float out = f ? v : sm.wv[warp] + v;
+    carry = sm.total_v;
+    __syncthreads();
+    return out;
+}
+
+// Block-wide inclusive scan of ints with a carried-in prefix.
+__device__ int int_scan(int val, int carry_in, int &carry, P1Smem &sm) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int v = val;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= off) v += y;
+    }
+    if (lane == 31) sm.wi[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        int wv = lane < NW ? sm.wi[lane] : 0;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, wv, off);
+            if (lane >= off) wv += y;
+        }
+        int ex = __shfl_up_sync(0xffffffffu, wv, 1);
+        if (lane < NW) sm.wi[lane] = carry_in + (lane == 0 ? 0 : ex);
+        if (lane == NW - 1) sm.total_i = carry_in + wv;
+    }
+    __syncthreads();
+    int out = sm.wi[warp] + v;
+    carry = sm.total_i;
+    __syncthreads();
+    return out;
+}
+
+__device__ __forceinline__ void report_bad_slot(DevStatus *st, int token) {
+    atomicAdd(&st->bad_slots, 1ull);
+    atomicCAS(&st->first_bad_plus1, 0, token + 1);
+    st->code = SDM_ERR_DEVICE;
+}
+
+template <typename WT>
+__global__ void __launch_bounds__(NT) k_phase1(Dims d, Inputs in, Work w, int step0, int nsteps) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    P1Smem &sm = *reinterpret_cast<P1Smem *>(smem_raw);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int C = d.C, W = d.W, R = d.R, S = d.S;
+    const int CW = C * W, CR = C * R, CC = C * C;
+    const WT *kw = static_cast<const WT *>(in.kw);
+    const WT *qwin = static_cast<const WT *>(in.qw);
+    const int N = nsteps * d.P;
+    const int bits = S <= 1 ? 0 : 32 - __clz(S - 1);
+    const int passes = (bits + 7) / 8;
+
+    unsigned long long *keyA = w.keys + (size_t)blockIdx.x * 2 * CW;
+    unsigned long long *keyB = keyA + CW;
+    int32_t *inv = w.inv + (size_t)blockIdx.x * CW;
+    float *lws = w.lws + (size_t)blockIdx.x * CW;
+    int32_t *pgid = w.pgid + (size_t)blockIdx.x * CW;
+    float *lend = w.lend + (size_t)blockIdx.x * CW;
+    float *kf = w.kf + (size_t)blockIdx.x * CW;
+    int32_t *rlo = w.rlo + (size_t)blockIdx.x * CR;
+    int32_t *rhi = w.rhi + (size_t)blockIdx.x * CR;
+
+    for (int n = blockIdx.x; n < N; n += gridDim.x) {
+        const int p = n % d.P, ti = step0 + n / d.P;
+        const int tok0 = ti * C;
+        const int nv = chunk_valid(in.valid, p, d.T, tok0, C);
+        const int nw = nv * W, nr = nv * R;
+        const size_t tok_base = (size_t)p * d.T + tok0;
+        const int32_t *ws = in.ws + tok_base * W;
+        const int32_t *rs = in.rs + tok_base * R;
+        const float *g = in.g + tok_base * W;
+        const WT *k = kw + tok_base * W;
+        const WT *q = qwin + tok_base * R;
+
+        int32_t *perm = w.perm + (size_t)n * CW;
+        float *wdw = w.wdw + (size_t)n * CW;
+        int32_t *goff = w.goff + (size_t)n * (CW + 1);
+        int32_t *gslot = w.gslot + (size_t)n * CW;
+        float *gfac = w.gfac + (size_t)n * CW;
+        float *gw = w.gw + (size_t)n * CW;
+        float *qw = w.qw + (size_t)n * CR;
+        float *lw = w.lw + (size_t)n * CW;
+        float *lr = w.lr + (size_t)n * CR;
+        float *A = w.A + (size_t)n * CC;
+        float *QK = w.QK + (size_t)n * CC;
+
+        // 1. keys (a slot outside [0, S) is reported and sorted as slot 0 with weight 0 and
+        //    log-decay 0, so that it adds nothing anywhere)
+        for (int i = tid; i < nw; i += NT) {
+            int s = ws[i];
+            float kk = to_f32(k[i]);
+            if ((unsigned)s >= (unsigned)S) {
+                report_bad_slot(w.status, (int)(tok_base + i / W));
+                s = 0;
+                kk = 0.f;
+            }
+            kf[i] = kk;
+            keyA[i] = ((unsigned long long)(unsigned)s << 32) | (unsigned)i;
+        }
+        for (int i = tid; i < nr; i += NT) {
+            if ((unsigned)rs[i] >= (unsigned)S) report_bad_slot(w.status, (int)(tok_base + i / R));
+        }
+        __syncthreads();
+        unsigned long long *src = keyA, *dst = keyB;
+        for (int ps = 0; ps < passes; ++ps) {
+            radix_pass(src, dst, nw, 32 + 8 * ps, sm);
+            unsigned long long *t = src; src = dst; dst = t;
+        }
+        const unsigned long long *srt = src;
+
+        // 2. groups and running log-decays along the sorted row
+        float carry_v = 0.f;
+        int carry_i = 0;
+        for (int tile = 0; tile < nw; tile += NT) {
+            const int pos = tile + tid;
+            const bool ok = pos < nw;
+            unsigned long long key = ok ? srt[pos] : 0ull;
+            const int slot = (int)(key >> 32), e = (int)(key & 0xffffffffu);
+            bool head = ok && (pos == 0 || (int)(srt[pos - 1] >> 32) != slot);
+            float gv = 0.f;
+            if (ok) {
+                gv = ((unsigned)ws[e] < (unsigned)S) ? g[e] : 0.f;
+                perm[pos] = e;
+                inv[e] = pos;
+                if (!head && (int)(srt[pos - 1] & 0xffffffffu) / W == e / W)
+                    atomicAdd(&w.status->repeated_write_slots, 1ull);
+            }
+            float cv, lv;
+            lv = seg_scan(head, gv, carry_v, cv, sm);
+            carry_v = cv;
+            int ci;
+            int gid = int_scan(head ? 1 : 0, carry_i, ci, sm) - 1;
+            carry_i = ci;
+            if (ok) {
+                lws[pos] = lv;
+                lw[e] = lv;
+                pgid[pos] = gid;
+                if (head) { goff[gid] = pos; gslot[gid] = slot; }
+                const bool tail = (pos == nw - 1) || (int)(srt[pos + 1] >> 32) != slot;
+                if (tail) {
+                    lend[gid] = lv;
+                    gfac[gid] = expf(lv);
+                }
+            }
+        }
+        const int ng = carry_i;
+        if (tid == 0) {
+            w.ngroups[n] = ng;
+            w.nvalid[n] = nv;
+            goff[ng] = nw;
+        }
+        __syncthreads();
+
+        // 3. weights
+        for (int pos = tid; pos < nw; pos += NT) {
+            const int e = perm[pos];
+            const float kk = kf[e];
+            const float l = lws[pos];
+            wdw[pos] = kk * expf(lend[pgid[pos]] - l);
+            gw[e] = kk * expf(l);
+        }
+        for (int er = tid; er < nr; er += NT) {
+            const int t = er / R;
+            const int r = rs[er];
+            int lo = 0, hi = -1;
+            float l = 0.f;
+            if ((unsigned)r < (unsigned)S) {
+                const unsigned long long target =
+                    ((unsigned long long)(unsigned)r << 32) | (unsigned)(t * W + W - 1);
+                int a = 0, b = nw;
+                while (a < b) {
+                    int mid = (a + b) >> 1;
+                    if (srt[mid] <= target) a = mid + 1; else b = mid;
+                }
+                const int pos = a - 1;
+                if (pos >= 0 && (int)(srt[pos] >> 32) == r) {
+                    hi = pos;
+                    lo = goff[pgid[pos]];
+                    l = lws[pos];
+                }
+            }
+            rlo[er] = lo;
+            rhi[er] = hi;
+            lr[er] = l;
+            qw[er] = ((unsigned)r < (unsigned)S) ? to_f32(q[er]) * expf(l) : 0.f;
+        }
+        __syncthreads();
+
+        // 4. A and QK, one warp per token row
+        float *row = sm.row[warp];
+        for (int t = warp; t < C; t += NW) {
+            for (int c = lane; c < C; c += 32) row[c] = 0.f;
+            __syncwarp();
+            if (t < nv) {
+                for (int j = 0; j < W; ++j) {
+                    const int e = t * W + j;
+                    const float ka = kf[e];
+                    if (ka == 0.f) continue;
+                    const int pos = inv[e];
+                    const int gs = goff[pgid[pos]];
+                    const float la = lws[pos];
+                    for (int m = gs + lane; m < pos; m += 32) {
+                        const int eb = perm[m];
+                        row[eb / W] += ka * kf[eb] * expf(la - lws[m]);
+                    }
+                    __syncwarp();
+                }
+            }
+            for (int c = lane; c < C; c += 32) A[(size_t)t * C + c] = row[c];
+            __syncwarp();
+            for (int c = lane; c < C; c += 32) row[c] = 0.f;
+            __syncwarp();
+            if (t < nv) {
+                for (int i = 0; i < R; ++i) {
+                    const int er = t * R + i;
+                    const int lo = rlo[er], hi = rhi[er];
+                    if (hi < 0) continue;
+                    const float qa = to_f32(q[er]);
+                    const float la = lr[er];
+                    for (int m = lo + lane; m <= hi; m += 32) {
+                        const int eb = perm[m];
+                        row[eb / W] += qa * kf[eb] * expf(la - lws[m]);
+                    }
+                    __syncwarp();
+                }
+            }
+            for (int c = lane; c < C; c += 32) QK[(size_t)t * C + c] = row[c];
+            __syncwarp();
+        }
+        // tails of the per-entry rows past the valid entries (read by nothing but the debug
+        // copy; written so that every output element is defined)
+        for (int i = nw + tid; i < CW; i += NT) { perm[i] = -1; gw[i] = 0.f; lw[i] = 0.f; wdw[i] = 0.f; }
+        for (int i = nr + tid; i < CR; i += NT) { qw[i] = 0.f; lr[i] = 0.f; }
+        __syncthreads();
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_phase1(const Dims &d, const Inputs &in, const Work &w, int step0, int nsteps,
+                          cudaStream_t st) {
+    const size_t smem = sizeof(P1Smem);
+    const int grid = w.G;
+    if (d.dtype == SDM_BF16) {
+        auto kern = k_phase1<__nv_bfloat16>;
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        kern<<<grid, NT, smem, st>>>(d, in, w, step0, nsteps);
+    } else {
+        auto kern = k_phase1<float>;
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        kern<<<grid, NT, smem, st>>>(d, in, w, step0, nsteps);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace sdm

@@ -1,0 +1,386 @@
+// Phase 2 of the chunked SDM write/read: one step ti covers chunk ti of all P streams
+// (sparse-delta-memory 2.0.0, phase2_kernels.py module docstring: "forward gather -> dual
+// matmul -> DW"; the dual matmul's definition is the _sdm_dual_matmul docstring).
+//
+//   gather   retrieved[t] = sum_j gw[t][j] B[s_tj],  inter[t] = sum_i qw[t][i] B[r_ti]
+//            (B = the bank at the start of the chunk), f32 rows [P][C][D]
+//   dual mm  u_pre = beta (v - retrieved);  delta_v = X u_pre;  readings = QX u_pre + inter
+//   DW       for every written slot s (one group of the sorted write row):
+//            B[s] = exp(lend_s) B[s] + sum_{members m, sorted order} dw_m delta_v[t_m]
+//            in f32, rounded once at the store; the group's single warp is the row's only
+//            writer, so the step is deterministic without atomics.
+//
+// Rows of a warp: lane l holds columns [l*CPL, (l+1)*CPL) of a row (CPL = D / 32), so one
+// warp-wide load moves a whole bank row with 4..64-byte vectors per lane.
+#include "sdm_internal.cuh"
+
+namespace sdm {
+namespace {
+
+constexpr int kBlock = 256;           // threads of the gather and DW blocks
+constexpr int kWarps = kBlock / 32;
+
+// ---------------------------------------------------------------------------------------
+// gather: WPT warps per token split the token's entries; their partial sums are added in
+// warp order (a fixed order, WPT a function of the shape only)
+// ---------------------------------------------------------------------------------------
+template <typename BT, int CPL, int WPT>
+__global__ void __launch_bounds__(kBlock) k_gather(Dims d, Inputs in, Work w, int step0, int ti) {
+    constexpr int TPB = kWarps / WPT;
+    __shared__ float part[(WPT > 1) ? kWarps : 1][2][(WPT > 1) ? 32 * CPL : 1];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tb = warp / WPT, sub = warp % WPT;
+    const int C = d.C, D = d.D, W = d.W, R = d.R;
+    const int gtok = blockIdx.x * TPB + tb;
+    const int p = gtok / C, t = gtok - p * C;
+    const int n = (ti - step0) * d.P + p;
+    bool active = gtok < d.P * C;
+    if (active) active = t < w.nvalid[n];
+
+    float ar[CPL], ai[CPL];
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) { ar[c] = 0.f; ai[c] = 0.f; }
+    if (active) {
+        const size_t tok = (size_t)p * d.T + (size_t)ti * C + t;
+        const BT *bank = static_cast<const BT *>(in.bank) + (size_t)p * d.S * D + lane * CPL;
+        const unsigned S = (unsigned)d.S;
+        {
+            const int32_t *ws = in.ws + tok * W;
+            const float *gw = w.gw + (size_t)n * C * W + (size_t)t * W;
+            const int j0 = sub * W / WPT, j1 = (sub + 1) * W / WPT;
+            int j = j0;
+            for (; j + 4 <= j1; j += 4) {
+                int s[4];
+                float wt[4], x[4][CPL];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) { s[u] = ws[j + u]; wt[u] = gw[j + u]; }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    if ((unsigned)s[u] < S) load_vec<BT, CPL, true>(bank + (size_t)s[u] * D, x[u]);
+                    else {
+#pragma unroll
+                        for (int c = 0; c < CPL; ++c) x[u][c] = 0.f;
+                        wt[u] = 0.f;
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+#pragma unroll
+                    for (int c = 0; c < CPL; ++c) ar[c] = fmaf(wt[u], x[u][c], ar[c]);
+            }
+            for (; j < j1; ++j) {
+                const int s = ws[j];
+                if ((unsigned)s >= S) continue;
+                float x[CPL];
+                load_vec<BT, CPL, true>(bank + (size_t)s * D, x);
+                const float wt = gw[j];
+#pragma unroll
+                for (int c = 0; c < CPL; ++c) ar[c] = fmaf(wt, x[c], ar[c]);
+            }
+        }
+        {
+            const int32_t *rs = in.rs + tok * R;
+            const float *qw = w.qw + (size_t)n * C * R + (size_t)t * R;
+            const int i0 = sub * R / WPT, i1 = (sub + 1) * R / WPT;
+            int i = i0;
+            for (; i + 4 <= i1; i += 4) {
+                int s[4];
+                float wt[4], x[4][CPL];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) { s[u] = rs[i + u]; wt[u] = qw[i + u]; }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    if ((unsigned)s[u] < S) load_vec<BT, CPL, true>(bank + (size_t)s[u] * D, x[u]);
+                    else {
+#pragma unroll
+                        for (int c = 0; c < CPL; ++c) x[u][c] = 0.f;
+                        wt[u] = 0.f;
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+#pragma unroll
+                    for (int c = 0; c < CPL; ++c) ai[c] = fmaf(wt[u], x[u][c], ai[c]);
+            }
+            for (; i < i1; ++i) {
+                const int s = rs[i];
+                if ((unsigned)s >= S) continue;
+                float x[CPL];
+                load_vec<BT, CPL, true>(bank + (size_t)s * D, x);
+                const float wt = qw[i];
+#pragma unroll
+                for (int c = 0; c < CPL; ++c) ai[c] = fmaf(wt, x[c], ai[c]);
+            }
+        }
+    }
+    const size_t row = ((size_t)p * C + t) * D + lane * CPL;
+    if constexpr (WPT == 1) {
+        if (active) {
+            store_vec<float, CPL>(w.ret + row, ar);
+            store_vec<float, CPL>(w.inter + row, ai);
+        }
+    } else {
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+            part[warp][0][lane * CPL + c] = ar[c];
+            part[warp][1][lane * CPL + c] = ai[c];
+        }
+        __syncthreads();
+        if (active && sub == 0) {
+#pragma unroll
+            for (int s = 1; s < WPT; ++s)
+#pragma unroll
+                for (int c = 0; c < CPL; ++c) {
+                    ar[c] += part[warp + s][0][lane * CPL + c];
+                    ai[c] += part[warp + s][1][lane * CPL + c];
+                }
+            store_vec<float, CPL>(w.ret + row, ar);
+            store_vec<float, CPL>(w.inter + row, ai);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// dual matmul: a [BM rows x BN columns] tile of delta_v and readings of one chunk
+// ---------------------------------------------------------------------------------------
+constexpr int BM = 32, BN = 64;
+
+template <typename BT>
+__global__ void __launch_bounds__(kBlock) k_dualmm(Dims d, Inputs in, Work w, int step0, int ti) {
+    extern __shared__ __align__(16) float dm_smem[];
+    const int C = d.C, D = d.D;
+    const int m0 = blockIdx.x * BM, d0 = blockIdx.y * BN, p = blockIdx.z;
+    const int n = (ti - step0) * d.P + p;
+    const int nv = w.nvalid[n];
+    float *Xs = dm_smem;
+    float *Qs = Xs + BM * C;
+    float *Us = Qs + BM * C;
+    const float *X = w.X + (size_t)n * C * C;
+    const float *QX = w.QX + (size_t)n * C * C;
+    const size_t tok0 = (size_t)p * d.T + (size_t)ti * C;
+    const BT *v = static_cast<const BT *>(in.v);
+    const float *ret = w.ret + (size_t)p * C * D;
+    const float *inter = w.inter + (size_t)p * C * D;
+
+    for (int idx = threadIdx.x; idx < BM * C; idx += kBlock) {
+        const int r = idx / C, k = idx - r * C;
+        const int row = m0 + r;
+        Xs[idx] = row < C ? X[(size_t)row * C + k] : 0.f;
+        Qs[idx] = row < C ? QX[(size_t)row * C + k] : 0.f;
+    }
+    for (int idx = threadIdx.x; idx < C * BN; idx += kBlock) {
+        const int k = idx / BN, c = idx - k * BN;
+        const int col = d0 + c;
+        float u = 0.f;
+        if (k < nv && col < D)
+            u = in.beta[tok0 + k] * (to_f32(v[(tok0 + k) * D + col]) - ret[(size_t)k * D + col]);
+        Us[idx] = u;
+    }
+    __syncthreads();
+
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    const int r0 = ty * 2, c0 = tx * 4;
+    float ax[2][4] = {}, aq[2][4] = {};
+    for (int k = 0; k < C; ++k) {
+        const float4 u = *reinterpret_cast<const float4 *>(Us + k * BN + c0);
+        const float uu[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+            const float x = Xs[(r0 + rr) * C + k], q = Qs[(r0 + rr) * C + k];
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                ax[rr][cc] = fmaf(x, uu[cc], ax[rr][cc]);
+                aq[rr][cc] = fmaf(q, uu[cc], aq[rr][cc]);
+            }
+        }
+    }
+    BT *out = static_cast<BT *>(in.readings);
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+        const int row = m0 + r0 + rr;
+        const int col = d0 + c0;
+        if (row >= C || col >= D) continue;
+        float dvv[4], rd[4];
+        const bool live = row < nv;
+        if (live) {
+            float it[4];
+            load_vec<float, 4, false>(inter + (size_t)row * D + col, it);
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) { dvv[cc] = ax[rr][cc]; rd[cc] = aq[rr][cc] + it[cc]; }
+        } else {
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) { dvv[cc] = 0.f; rd[cc] = 0.f; }
+        }
+        store_vec<float, 4>(w.dv + ((size_t)p * C + row) * D + col, dvv);
+        if ((size_t)ti * C + row < (size_t)d.T) store_vec<BT, 4>(out + (tok0 + row) * D + col, rd);
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// DW: one warp per group (distinct written slot) of each chunk of the step
+// ---------------------------------------------------------------------------------------
+template <typename BT, int CPL>
+__global__ void __launch_bounds__(kBlock) k_dw(Dims d, Inputs in, Work w, int step0, int ti) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int p = blockIdx.y;
+    const int n = (ti - step0) * d.P + p;
+    const int C = d.C, D = d.D, W = d.W, CW = C * W;
+    const int ng = w.ngroups[n];
+    const int32_t *goff = w.goff + (size_t)n * (CW + 1);
+    const int32_t *gslot = w.gslot + (size_t)n * CW;
+    const float *gfac = w.gfac + (size_t)n * CW;
+    const int32_t *perm = w.perm + (size_t)n * CW;
+    const float *wdw = w.wdw + (size_t)n * CW;
+    const float *dvp = w.dv + (size_t)p * C * D + lane * CPL;
+    BT *bank = static_cast<BT *>(in.bank) + (size_t)p * d.S * D + lane * CPL;
+    for (int g = blockIdx.x * kWarps + warp; g < ng; g += gridDim.x * kWarps) {
+        const int o0 = goff[g], o1 = goff[g + 1];
+        BT *row = bank + (size_t)gslot[g] * D;
+        const float f = gfac[g];
+        float acc[CPL];
+        load_vec<BT, CPL, false>(row, acc);
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) acc[c] *= f;
+        int m = o0;
+        for (; m + 4 <= o1; m += 4) {
+            float x[4][CPL], wt[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                wt[u] = wdw[m + u];
+                load_vec<float, CPL, false>(dvp + (size_t)(perm[m + u] / W) * D, x[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int c = 0; c < CPL; ++c) acc[c] = fmaf(wt[u], x[u][c], acc[c]);
+        }
+        for (; m < o1; ++m) {
+            float x[CPL];
+            const float wt = wdw[m];
+            load_vec<float, CPL, false>(dvp + (size_t)(perm[m] / W) * D, x);
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) acc[c] = fmaf(wt, x[c], acc[c]);
+        }
+        store_vec<BT, CPL>(row, acc);
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// debug: the plan's per-position flags and token-major DW weights of a slab's chunks
+// ---------------------------------------------------------------------------------------
+__global__ void k_debug_expand(Dims d, Work w, int32_t *perm_out, uint8_t *gs_out,
+                               uint8_t *ow_out, float *dw_out) {
+    const int n = blockIdx.x;
+    const int CW = d.C * d.W;
+    const int nw = w.nvalid[n] * d.W;
+    const int ng = w.ngroups[n];
+    const int32_t *perm = w.perm + (size_t)n * CW;
+    const int32_t *goff = w.goff + (size_t)n * (CW + 1);
+    const float *wdw = w.wdw + (size_t)n * CW;
+    perm_out += (size_t)n * CW;
+    gs_out += (size_t)n * CW;
+    ow_out += (size_t)n * CW;
+    dw_out += (size_t)n * CW;
+    for (int i = threadIdx.x; i < CW; i += blockDim.x) {
+        perm_out[i] = i < nw ? perm[i] : -1;
+        gs_out[i] = 0;
+        ow_out[i] = 0;
+        dw_out[i] = 0.f;
+    }
+    __syncthreads();
+    for (int g = threadIdx.x; g < ng; g += blockDim.x) {
+        gs_out[goff[g]] = 1;
+        ow_out[goff[g + 1] - 1] = 1;
+    }
+    for (int i = threadIdx.x; i < nw; i += blockDim.x) dw_out[perm[i]] = wdw[i];
+}
+
+// ---------------------------------------------------------------------------------------
+// dispatch
+// ---------------------------------------------------------------------------------------
+int gather_wpt(const Dims &d) {
+    const long tokens = (long)d.P * d.C;
+    int wpt = 1;
+    while (wpt < 8 && tokens * wpt < 32L * kRefSms && 2 * wpt <= (d.W < d.R ? d.W : d.R)) wpt *= 2;
+    return wpt;
+}
+
+template <typename BT, int CPL>
+cudaError_t gather_cpl(const Dims &d, const Inputs &in, const Work &w, int step0, int ti,
+                       cudaStream_t st) {
+    const int wpt = gather_wpt(d);
+    const int tokens = d.P * d.C;
+    const int tpb = kWarps / wpt;
+    const int grid = (tokens + tpb - 1) / tpb;
+    switch (wpt) {
+        case 1: k_gather<BT, CPL, 1><<<grid, kBlock, 0, st>>>(d, in, w, step0, ti); break;
+        case 2: k_gather<BT, CPL, 2><<<grid, kBlock, 0, st>>>(d, in, w, step0, ti); break;
+        case 4: k_gather<BT, CPL, 4><<<grid, kBlock, 0, st>>>(d, in, w, step0, ti); break;
+        default: k_gather<BT, CPL, 8><<<grid, kBlock, 0, st>>>(d, in, w, step0, ti); break;
+    }
+    return cudaGetLastError();
+}
+
+template <typename BT, int CPL>
+cudaError_t dw_cpl(const Dims &d, const Inputs &in, const Work &w, int step0, int ti,
+                   cudaStream_t st) {
+    int gx = (8 * kRefSms + d.P - 1) / d.P;
+    const int max_groups = d.C * d.W;
+    const int need = (max_groups + kWarps - 1) / kWarps;
+    if (gx > need) gx = need;
+    if (gx < 1) gx = 1;
+    dim3 grid(gx, d.P);
+    k_dw<BT, CPL><<<grid, kBlock, 0, st>>>(d, in, w, step0, ti);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+#define SDM_DISPATCH_D(FN, BT)                                      \
+    switch (d.D) {                                                  \
+        case 32: return FN<BT, 1>(d, in, w, step0, ti, st);         \
+        case 64: return FN<BT, 2>(d, in, w, step0, ti, st);         \
+        case 128: return FN<BT, 4>(d, in, w, step0, ti, st);        \
+        case 256: return FN<BT, 8>(d, in, w, step0, ti, st);        \
+        case 512: return FN<BT, 16>(d, in, w, step0, ti, st);       \
+        default: return cudaErrorInvalidValue;                      \
+    }
+
+cudaError_t launch_gather(const Dims &d, const Inputs &in, const Work &w, int step0, int ti,
+                          cudaStream_t st) {
+    if (d.dtype == SDM_BF16) { SDM_DISPATCH_D(gather_cpl, __nv_bfloat16) }
+    SDM_DISPATCH_D(gather_cpl, float)
+}
+
+cudaError_t launch_dw(const Dims &d, const Inputs &in, const Work &w, int step0, int ti,
+                      cudaStream_t st) {
+    if (d.dtype == SDM_BF16) { SDM_DISPATCH_D(dw_cpl, __nv_bfloat16) }
+    SDM_DISPATCH_D(dw_cpl, float)
+}
+
+cudaError_t launch_dualmm(const Dims &d, const Inputs &in, const Work &w, int step0, int ti,
+                          cudaStream_t st) {
+    const size_t smem = sizeof(float) * ((size_t)2 * BM * d.C + (size_t)d.C * BN);
+    dim3 grid((d.C + BM - 1) / BM, (d.D + BN - 1) / BN, d.P);
+    if (d.dtype == SDM_BF16) {
+        auto kern = k_dualmm<__nv_bfloat16>;
+        if (smem > 48 * 1024)
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        kern<<<grid, kBlock, smem, st>>>(d, in, w, step0, ti);
+    } else {
+        auto kern = k_dualmm<float>;
+        if (smem > 48 * 1024)
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        kern<<<grid, kBlock, smem, st>>>(d, in, w, step0, ti);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_debug_expand(const Dims &d, const Work &w, int nchunks, int32_t *perm,
+                                uint8_t *gstart, uint8_t *owner, float *dw_tok,
+                                cudaStream_t st) {
+    k_debug_expand<<<nchunks, kBlock, 0, st>>>(d, w, perm, gstart, owner, dw_tok);
+    return cudaGetLastError();
+}
+
+}  // namespace sdm

@@ -1,0 +1,182 @@
+// Internal declarations of libsdm: workspace layout, kernel argument blocks and small
+// device helpers shared by the kernels. Nothing here is part of the C ABI (include/sdm.h).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "sdm.h"
+
+namespace sdm {
+
+constexpr int kMinChunk = 16;
+constexpr int kMaxChunk = 256;
+constexpr int kMaxWidth = 256;
+constexpr int kRefSms = 152;            // GB300 SM count: sizes grids and slabs (shape-only)
+constexpr size_t kAlign = 256;
+constexpr size_t kSlabBudget = size_t(256) << 20;   // per-chunk Phase-1 state held at once
+
+// Device status block at the start of the workspace (sdm_device_status, with the first bad
+// token stored +1 so that a zero fill means "none").
+struct DevStatus {
+    int32_t code;
+    int32_t first_bad_plus1;
+    unsigned long long bad_slots;
+    unsigned long long repeated_write_slots;
+};
+
+struct Dims {
+    int P, T, C, S, D, W, R, Nt;
+    int dtype;   // SDM_F32 / SDM_BF16
+};
+
+// Device pointers of one slab's workspace. N = ns * P chunks; chunk n of the slab is step
+// (step0 + n / P) of stream n % P.
+struct Work {
+    DevStatus *status;
+    // Phase-1 outputs, per chunk
+    int32_t *perm;      // [N][CW]   entry e = t*W + j at each sorted position
+    float *wdw;         // [N][CW]   DW weight at each sorted position
+    int32_t *goff;      // [N][CW+1] group start positions, goff[ngroups] = n_entries
+    int32_t *gslot;     // [N][CW]   slot of each group
+    float *gfac;        // [N][CW]   exp(lend) of each group
+    int32_t *ngroups;   // [N]
+    int32_t *nvalid;    // [N]       valid tokens of the chunk
+    float *gw;          // [N][CW]   token-major gather weights of the writes
+    float *qw;          // [N][CR]   token-major gather weights of the reads
+    float *lw;          // [N][CW]   token-major running log-decay of the writes
+    float *lr;          // [N][CR]   token-major running log-decay of the reads
+    float *A, *QK, *X, *QX;   // [N][C*C]
+    // Phase-1 scratch, per Phase-1 CTA
+    unsigned long long *keys;   // [G][2][CW]
+    int32_t *inv;       // [G][CW]  sorted position of each entry
+    float *lws;         // [G][CW]  running log-decay at each sorted position
+    int32_t *pgid;      // [G][CW]  group id of each sorted position
+    float *lend;        // [G][CW]  log-decay total of each group
+    float *kf;          // [G][CW]  write weight of each entry as float (0 for a bad slot)
+    int32_t *rlo;       // [G][CR]  first write position of the read's slot group
+    int32_t *rhi;       // [G][CR]  last write position at or before the read's token (-1: none)
+    // Phase-2 step buffers
+    float *ret;         // [P][C*D]
+    float *inter;       // [P][C*D]
+    float *dv;          // [P][C*D]
+    int ns;             // steps per slab
+    int G;              // Phase-1 CTAs
+};
+
+struct Inputs {
+    void *bank;
+    const int32_t *ws;
+    const void *kw;
+    const float *g;
+    const float *beta;
+    const void *v;
+    const int32_t *rs;
+    const void *qw;
+    const int32_t *valid;   // may be null
+    void *readings;
+};
+
+// ---------------------------------------------------------------------------------------
+// host-side layout (api.cu)
+// ---------------------------------------------------------------------------------------
+size_t layout_bytes(const Dims &d, int ns, int G);
+Work layout_assign(const Dims &d, int ns, int G, void *base);
+int phase1_ctas(const Dims &d, int ns);
+
+// ---------------------------------------------------------------------------------------
+// launchers (one per kernel family); every one returns cudaGetLastError()
+// ---------------------------------------------------------------------------------------
+cudaError_t launch_phase1(const Dims &d, const Inputs &in, const Work &w, int step0, int nsteps,
+                          cudaStream_t st);
+cudaError_t launch_solve(const Dims &d, const Inputs &in, const Work &w, int step0, int nsteps,
+                         cudaStream_t st);
+cudaError_t launch_gather(const Dims &d, const Inputs &in, const Work &w, int step0, int ti,
+                          cudaStream_t st);
+cudaError_t launch_dualmm(const Dims &d, const Inputs &in, const Work &w, int step0, int ti,
+                          cudaStream_t st);
+cudaError_t launch_dw(const Dims &d, const Inputs &in, const Work &w, int step0, int ti,
+                      cudaStream_t st);
+cudaError_t launch_debug_expand(const Dims &d, const Work &w, int nchunks, int32_t *perm,
+                                uint8_t *gstart, uint8_t *owner, float *dw_tok,
+                                cudaStream_t st);
+
+// ---------------------------------------------------------------------------------------
+// device helpers
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+
+// Loads N consecutive elements of type T (N * sizeof(T) a power of two, 2..64 bytes,
+// address aligned to it) as floats.
+template <typename T, int N, bool NC>
+__device__ __forceinline__ void load_vec(const T *p, float (&o)[N]) {
+    constexpr int BYTES = N * (int)sizeof(T);
+    static_assert(BYTES >= 2 && BYTES <= 64 && (BYTES & (BYTES - 1)) == 0, "vector size");
+    if constexpr (BYTES >= 16) {
+        constexpr int V = BYTES / 16;
+        const uint4 *q = reinterpret_cast<const uint4 *>(p);
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+            uint4 u = NC ? __ldg(q + i) : q[i];
+            const T *e = reinterpret_cast<const T *>(&u);
+            constexpr int PER = 16 / (int)sizeof(T);
+#pragma unroll
+            for (int k = 0; k < PER; ++k) o[i * PER + k] = to_f32(e[k]);
+        }
+    } else if constexpr (BYTES == 8) {
+        const uint2 *q = reinterpret_cast<const uint2 *>(p);
+        uint2 u = NC ? __ldg(q) : *q;
+        const T *e = reinterpret_cast<const T *>(&u);
+#pragma unroll
+        for (int k = 0; k < N; ++k) o[k] = to_f32(e[k]);
+    } else if constexpr (BYTES == 4) {
+        const unsigned *q = reinterpret_cast<const unsigned *>(p);
+        unsigned u = NC ? __ldg(q) : *q;
+        const T *e = reinterpret_cast<const T *>(&u);
+#pragma unroll
+        for (int k = 0; k < N; ++k) o[k] = to_f32(e[k]);
+    } else {
+        const unsigned short *q = reinterpret_cast<const unsigned short *>(p);
+        unsigned short u = NC ? __ldg(q) : *q;
+        o[0] = to_f32(*reinterpret_cast<const T *>(&u));
+    }
+}
+
+template <typename T, int N>
+__device__ __forceinline__ void store_vec(T *p, const float (&x)[N]) {
+    constexpr int BYTES = N * (int)sizeof(T);
+    static_assert(BYTES >= 2 && BYTES <= 64 && (BYTES & (BYTES - 1)) == 0, "vector size");
+    alignas(16) T tmp[N];
+#pragma unroll
+    for (int k = 0; k < N; ++k) tmp[k] = from_f32<T>(x[k]);
+    if constexpr (BYTES >= 16) {
+        uint4 *q = reinterpret_cast<uint4 *>(p);
+        const uint4 *s = reinterpret_cast<const uint4 *>(tmp);
+#pragma unroll
+        for (int i = 0; i < BYTES / 16; ++i) q[i] = s[i];
+    } else if constexpr (BYTES == 8) {
+        *reinterpret_cast<uint2 *>(p) = *reinterpret_cast<const uint2 *>(tmp);
+    } else if constexpr (BYTES == 4) {
+        *reinterpret_cast<unsigned *>(p) = *reinterpret_cast<const unsigned *>(tmp);
+    } else {
+        p[0] = tmp[0];
+    }
+}
+
+__device__ __forceinline__ int chunk_valid(const int32_t *valid, int p, int T, int tok0, int C) {
+    int v = valid ? valid[p] : T;
+    v = v < 0 ? 0 : (v > T ? T : v);
+    int n = v - tok0;
+    return n < 0 ? 0 : (n > C ? C : n);
+}
+
+}  // namespace sdm

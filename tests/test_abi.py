@@ -1,0 +1,81 @@
+"""The C ABI library without a GPU: it loads, exports every function include/sdm.h declares,
+and sizes/refuses shapes on the host (no compute call needs a device here)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import sparse_addressed_delta_gb300 as sdm
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "sdm.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(sdm_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = sdm.library()
+    names = declared_functions()
+    assert "sdm_write_read" in names and len(names) >= 6
+    for name in names:
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_version_string():
+    assert "sm_103a" in sdm.version()
+
+
+def test_workspace_bytes_host_only():
+    s = sdm.make_shape(8, 4096, 64, 65536, 128, 16, 16, sdm.SDM_BF16)
+    n = sdm.workspace_bytes(s)
+    assert n > 0 and n % 256 == 0
+    # the slab is bounded: more tokens do not grow the workspace past the slab budget
+    big = sdm.make_shape(4, 16384, 256, 1 << 20, 256, 256, 256, sdm.SDM_BF16)
+    huge = sdm.make_shape(4, 1 << 19, 256, 1 << 20, 256, 256, 256, sdm.SDM_BF16)
+    assert sdm.workspace_bytes(huge) == sdm.workspace_bytes(big)
+    # explicit slabs: fewer steps held, less workspace
+    s1 = sdm.make_shape(8, 4096, 64, 65536, 128, 16, 16, sdm.SDM_BF16, slab_steps=4)
+    assert sdm.workspace_bytes(s1) < n
+
+
+def test_launch_count():
+    s = sdm.make_shape(8, 4096, 64, 65536, 128, 16, 16, sdm.SDM_BF16)
+    assert sdm.launch_count(s) == 2 + 3 * 64
+    s = sdm.make_shape(1, 100, 16, 64, 64, 4, 4, sdm.SDM_F32, slab_steps=3)
+    nt = 7
+    assert sdm.launch_count(s) == 2 * 3 + 3 * nt
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(C=8), -1), (dict(C=300), -1), (dict(W=0), -1), (dict(R=257), -1), (dict(P=0), -1),
+    (dict(T=0), -1), (dict(S=0), -1), (dict(D=96), -2), (dict(dtype=7), -1),
+    (dict(P=1 << 16, T=1 << 16), -1)])
+def test_refusals(kw, code):
+    base = dict(P=2, T=64, C=16, S=128, D=64, W=4, R=4, dtype=sdm.SDM_F32)
+    base.update(kw)
+    s = sdm.Shape(base["P"], base["T"], base["C"], base["S"], base["D"], base["W"], base["R"],
+                  base["dtype"], 0, 0)
+    assert sdm.library().sdm_workspace_bytes(ctypes.byref(s)) == 0
+    msg = sdm.library().sdm_last_error().decode()
+    assert msg
+    with pytest.raises(sdm.SdmError) as e:
+        sdm.workspace_bytes(s)
+
+
+def test_write_read_refuses_before_any_work():
+    """A null pointer or a short workspace is refused on the host, before any launch."""
+    lib = sdm.library()
+    s = sdm.make_shape(1, 32, 16, 64, 64, 4, 4, sdm.SDM_F32)
+    rc = lib.sdm_write_read(ctypes.byref(s), None, None, None, None, None, None, None, None,
+                            None, None, None, 0, None)
+    assert rc == -1
+    fake = ctypes.c_void_p(1 << 40)
+    rc = lib.sdm_write_read(ctypes.byref(s), fake, fake, fake, fake, fake, fake, fake, fake,
+                            None, fake, fake, 16, None)
+    assert rc == -5 and "workspace" in lib.sdm_last_error().decode()

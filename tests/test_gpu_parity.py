@@ -1,0 +1,185 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle, on the GPU."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sdm_inputs as si
+import sparse_addressed_delta_gb300 as sdm
+from sdm_case import (TOL, compare_with_oracle, f64, oracle_args, run_gpu, small_workload,
+                      to_device)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    sdm.library()
+
+
+def check(wl, inputs=None, slab_steps=0):
+    inputs = si.generate(wl) if inputs is None else inputs
+    dev = to_device(inputs, wl)
+    r, b, ws = run_gpu(wl, dev, slab_steps)
+    st = sdm.device_status(ws)
+    assert st["code"] == 0 and st["bad_slots"] == 0 and st["repeated_write_slots"] == 0, st
+    er, eb = compare_with_oracle(wl, inputs, r, b)
+    tol = TOL[wl.dtype]
+    assert er <= tol and eb <= tol, (wl.name, er, eb)
+    return er, eb
+
+
+def test_workload0_full():
+    er, eb = check(si.WORKLOADS[0])
+    assert er <= 1e-4 and eb <= 1e-4
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("D", [32, 64, 128, 256, 512])
+def test_head_dims(dtype, D):
+    check(small_workload(P=2, T=77, C=16, S=50, D=D, W=3, R=5, dtype=dtype, seed=D))
+
+
+@pytest.mark.parametrize("C", [16, 32, 48, 64, 100, 128, 256])
+def test_chunk_sizes_ragged(C):
+    """Several chunks per stream, a ragged last chunk and ragged valid tokens."""
+    check(small_workload(P=3, T=3 * C + 7, C=C, S=97, D=64, W=5, R=4, seed=C))
+
+
+@pytest.mark.parametrize("W,R", [(1, 1), (1, 7), (16, 16), (33, 9), (64, 64)])
+def test_widths(W, R):
+    check(small_workload(P=2, T=150, C=32, S=max(200, 3 * W), D=64, W=W, R=R,
+                         slots="zipf1.1", seed=W * 100 + R))
+
+
+def test_dense_collisions_tiny_bank():
+    """A bank of W rows: every token writes every row (groups of the whole chunk)."""
+    check(small_workload(P=2, T=130, C=64, S=8, D=32, W=8, R=8, slots="uniform", seed=5))
+
+
+def test_mix_slots_bf16():
+    check(small_workload(P=2, T=300, C=64, S=4096, D=128, W=32, R=32, dtype="bf16",
+                         slots="mix", seed=9))
+
+
+def test_empty_streams_and_full_padding():
+    wl = small_workload(P=4, T=64, C=16, S=40, D=64, W=3, R=3, ragged=False, seed=3)
+    inputs = si.generate(wl)
+    inputs["valid"] = np.array([0, 1, 17, 64], np.int32)
+    for k in ("write_slots", "read_slots"):
+        inputs[k][0] = 0
+        inputs[k][1, 1:] = 0
+        inputs[k][2, 17:] = 0
+    dev = to_device(inputs, wl)
+    r, b, _ = run_gpu(wl, dev)
+    assert not f64(r[0]).any() and not f64(r[1, 1:]).any() and not f64(r[2, 17:]).any()
+    assert torch.equal(b[:wl.S], dev["bank"][:wl.S])
+    er, eb = compare_with_oracle(wl, inputs, r, b)
+    assert er <= 1e-4 and eb <= 1e-4
+
+
+def test_padding_inputs_never_read():
+    """NaN in every input of a padding token changes nothing, bit for bit."""
+    wl = small_workload(P=3, T=90, C=32, S=64, D=64, W=4, R=4, ragged=True, seed=8)
+    inputs = si.generate(wl)
+    dev = to_device(inputs, wl)
+    r1, b1, _ = run_gpu(wl, dev)
+    pad = torch.arange(wl.T, device="cuda")[None, :] >= dev["valid"][:, None]
+    for k in ("write_w", "log_decay", "v", "read_w"):
+        dev[k][pad] = float("nan")
+    dev["beta"][pad] = float("nan")
+    dev["write_slots"][pad] = -5
+    dev["read_slots"][pad] = 1 << 30
+    r2, b2, ws = run_gpu(wl, dev)
+    assert torch.equal(r1, r2) and torch.equal(b1, b2)
+    assert sdm.device_status(ws)["code"] == 0
+
+
+def test_deterministic_bitwise():
+    wl = small_workload(P=4, T=256, C=64, S=300, D=128, W=16, R=16, dtype="bf16", seed=11)
+    dev = to_device(si.generate(wl), wl)
+    r1, b1, _ = run_gpu(wl, dev)
+    r2, b2, _ = run_gpu(wl, dev)
+    assert torch.equal(r1, r2) and torch.equal(b1, b2)
+
+
+def test_slab_invariance_bitwise():
+    wl = small_workload(P=3, T=200, C=16, S=100, D=64, W=4, R=4, seed=12)
+    dev = to_device(si.generate(wl), wl)
+    r0, b0, _ = run_gpu(wl, dev, slab_steps=0)
+    for ns in (1, 2, 5):
+        r, b, _ = run_gpu(wl, dev, slab_steps=ns)
+        assert torch.equal(r, r0) and torch.equal(b, b0), ns
+
+
+def test_bad_slot_is_reported_not_dereferenced():
+    wl = small_workload(P=2, T=40, C=16, S=64, D=64, W=4, R=4, ragged=False, seed=13)
+    inputs = si.generate(wl)
+    inputs["write_slots"][1, 5, 2] = 1 << 30
+    inputs["read_slots"][0, 9, 1] = -3
+    dev = to_device(inputs, wl)
+    _, _, ws = run_gpu(wl, dev)
+    st = sdm.device_status(ws)
+    assert st["code"] == -6 and st["bad_slots"] == 2
+    assert st["first_bad_token"] in (1 * wl.T + 5, 9)
+
+
+def test_repeated_write_slot_is_counted():
+    wl = small_workload(P=1, T=40, C=16, S=64, D=64, W=4, R=4, ragged=False, seed=14)
+    inputs = si.generate(wl)
+    inputs["write_slots"][0, 7, 3] = inputs["write_slots"][0, 7, 0]
+    dev = to_device(inputs, wl)
+    _, _, ws = run_gpu(wl, dev)
+    assert sdm.device_status(ws)["repeated_write_slots"] == 1
+
+
+def test_phase1_plan_and_intermediates():
+    """Phase 1 and the solve against the oracle's chunked form, chunk by chunk: the dedup
+    plan bit for bit, the values within float32 rounding."""
+    wl = small_workload(P=2, T=70, C=16, S=20, D=32, W=4, R=3, ragged=True, seed=15)
+    inputs = si.generate(wl)
+    dev = to_device(inputs, wl)
+    out = sdm.phase1_debug(dev["write_slots"], dev["write_w"], dev["log_decay"], dev["beta"],
+                           dev["read_slots"], dev["read_w"], dev["valid"], S=wl.S, D=wl.D,
+                           chunk_size=wl.C)
+    torch.cuda.synchronize()
+    x = oracle.from_stored(inputs, wl.dtype)
+    C, W, R = wl.C, wl.W, wl.R
+    for ti in range(wl.Nt):
+        for p in range(wl.P):
+            n = ti * wl.P + p
+            nv = int(np.clip(inputs["valid"][p] - ti * C, 0, C))
+            pl = oracle.plan(inputs["write_slots"][p, ti * C:ti * C + nv])
+            m = nv * W
+            assert out["perm"][n, :m].cpu().numpy().tolist() == pl["perm"].tolist()
+            assert (out["perm"][n, m:] == -1).all()
+            assert out["group_start"][n, :m].cpu().numpy().tolist() == pl["group_start"].tolist()
+            assert out["owner"][n, :m].cpu().numpy().tolist() == pl["owner"].tolist()
+            assert int(out["ngroups"][n]) == pl["groups"]
+            _, _, d = oracle.chunked(C, *oracle_args(x), debug=(p, ti))
+            for key, ref in (("lw", d["lw"]), ("gw", d["gw"]), ("dw", d["dw"]), ("lr", d["lr"]),
+                             ("qw", d["qw"]), ("A", d["A"]), ("QK", d["QK"]), ("X", d["X"]),
+                             ("QX", d["QX"])):
+                got = out[key][n].double().cpu().numpy().reshape(ref.shape)
+                scale = max(np.abs(ref).max(), 1e-30)
+                assert np.abs(got - ref).max() <= 2e-6 * scale + 1e-30, (key, ti, p)
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4])
+def test_full_size_workloads(cfg):
+    """The four larger workloads at full size, whole readings and final bank."""
+    wl = si.WORKLOADS[cfg]
+    inputs = si.generate(wl)
+    dev = to_device(inputs, wl)
+    r, b, ws = run_gpu(wl, dev)
+    st = sdm.device_status(ws)
+    assert st["code"] == 0 and st["repeated_write_slots"] == 0, st
+    del dev
+    group = max(1, min(8, (1 << 30) // (wl.S * wl.D * 8)))   # about 1 GiB of fp64 bank per group
+    er, eb = compare_with_oracle(wl, inputs, r, b, streams_per_call=group, nthreads=group)
+    tol = TOL[wl.dtype]
+    print(f"{wl.name}: readings err {er:.3e}, bank err {eb:.3e} (tol {tol})")
+    assert er <= tol and eb <= tol

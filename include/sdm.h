@@ -64,8 +64,15 @@ typedef enum { SDM_F32 = 0, SDM_BF16 = 1 } sdm_dtype;
  *   bank_dtype  SDM_F32 or SDM_BF16
  *   slab_steps  Phase-2 steps whose Phase-1 state is held at once; 0 = automatic. The
  *               results do not depend on it (Phase 1 and the solve are per chunk).
- *   flags       0 (reserved)
- * P * ceil(T / C) * C must be below 2^31. */
+ *   flags       0, or SDM_FLAG_PER_STEP_KERNELS
+ * P * ceil(T / C) * C must be below 2^31.
+ *
+ * Phase 2 runs by default as one persistent kernel per slab in which each CTA owns one
+ * stream and one 16-byte slice of bank columns for all the slab's steps (the forward acts on
+ * every column independently once Phase 1 and the solve are done). SDM_FLAG_PER_STEP_KERNELS
+ * runs it instead as three kernels per step (gather, dual matmul, DW over all streams), as
+ * the pages lay it out. Both are deterministic; their results differ only by rounding. */
+#define SDM_FLAG_PER_STEP_KERNELS 1
 typedef struct {
     int32_t P, T, C, S, D, W, R;
     int32_t bank_dtype;
@@ -116,14 +123,16 @@ int sdm_write_read(const sdm_shape *shape, void *bank, const int32_t *write_slot
                    size_t workspace_bytes, void *stream);
 
 /* Kernel families, in launch order within a slab: Phase 1 and the solve once per slab, then
- * gather, dual matmul and DW once per step. */
+ * the fused Phase-2 kernel once per slab, or (SDM_FLAG_PER_STEP_KERNELS) gather, dual matmul
+ * and DW once per step. */
 enum {
     SDM_KERNEL_PHASE1 = 0,
     SDM_KERNEL_SOLVE = 1,
     SDM_KERNEL_GATHER = 2,
     SDM_KERNEL_DUALMM = 3,
     SDM_KERNEL_DW = 4,
-    SDM_KERNEL_KINDS = 5
+    SDM_KERNEL_PHASE2 = 5,   /* the fused Phase-2 kernel (gather + dual matmul + DW) */
+    SDM_KERNEL_KINDS = 6
 };
 
 /* sdm_write_read with a CUDA event recorded before every kernel launch and after the last,

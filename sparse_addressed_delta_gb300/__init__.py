@@ -27,7 +27,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 library_path = os.path.join(_HERE, "libsdm.so")
 
 SDM_F32, SDM_BF16 = 0, 1
-KERNEL_KINDS = ("phase1", "solve", "gather", "dualmm", "dw")
+KERNEL_KINDS = ("phase1", "solve", "gather", "dualmm", "dw", "phase2")
+FLAG_PER_STEP_KERNELS = 1
 _STATUS = {0: "SDM_OK", -1: "SDM_ERR_INVALID", -2: "SDM_ERR_UNSUPPORTED", -3: "SDM_ERR_CUDA",
            -4: "SDM_ERR_TIMEOUT", -5: "SDM_ERR_WORKSPACE", -6: "SDM_ERR_DEVICE"}
 
@@ -105,9 +106,9 @@ def _dtype_code(dtype: torch.dtype) -> int:
     raise TypeError(f"bank dtype must be float32 or bfloat16, got {dtype}")
 
 
-def make_shape(P, T, C, S, D, W, R, dtype, slab_steps: int = 0) -> Shape:
+def make_shape(P, T, C, S, D, W, R, dtype, slab_steps: int = 0, flags: int = 0) -> Shape:
     code = dtype if isinstance(dtype, int) else _dtype_code(dtype)
-    return Shape(P, T, C, S, D, W, R, code, slab_steps, 0)
+    return Shape(P, T, C, S, D, W, R, code, slab_steps, flags)
 
 
 def workspace_bytes(shape: Shape) -> int:
@@ -153,7 +154,8 @@ def sdm_write_read(bank: torch.Tensor, write_slots: torch.Tensor, write_w: torch
                    read_slots: torch.Tensor, read_w: torch.Tensor,
                    valid_tokens: Optional[torch.Tensor] = None, *, chunk_size: int,
                    slab_steps: int = 0, workspace: Optional[torch.Tensor] = None,
-                   readings: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+                   readings: Optional[torch.Tensor] = None, stream=None,
+                   flags: int = 0) -> torch.Tensor:
     """Chunked SDM write/read over P streams; returns readings [P, T, D] and advances
     ``bank`` ([P*S, D], float32 or bfloat16, stream p owning rows [p*S, (p+1)*S)) in place.
 
@@ -181,7 +183,7 @@ def sdm_write_read(bank: torch.Tensor, write_slots: torch.Tensor, write_w: torch
     _need(read_w, "read_w", (P, T, R), dt, dev)
     if valid_tokens is not None:
         _need(valid_tokens, "valid_tokens", (P,), torch.int32, dev)
-    shape = make_shape(P, T, chunk_size, S, D, W, R, dt, slab_steps)
+    shape = make_shape(P, T, chunk_size, S, D, W, R, dt, slab_steps, flags)
     if readings is None:
         readings = torch.empty((P, T, D), dtype=dt, device=dev)
     else:
@@ -199,14 +201,14 @@ def sdm_write_read(bank: torch.Tensor, write_slots: torch.Tensor, write_w: torch
 
 def profile_write_read(bank, write_slots, write_w, log_decay, beta, v, read_slots, read_w,
                        valid_tokens=None, *, chunk_size: int, slab_steps: int = 0,
-                       workspace=None, readings=None, stream=None):
+                       workspace=None, readings=None, stream=None, flags: int = 0):
     """One sdm_write_read call with CUDA events around every kernel launch (synchronizes).
     Returns (readings, {family: (total_ms, launches)}) for the families in KERNEL_KINDS."""
     P, T, W = write_slots.shape
     R = read_slots.shape[-1]
     S, D = bank.shape[0] // P, bank.shape[1]
     dev, dt = bank.device, bank.dtype
-    shape = make_shape(P, T, chunk_size, S, D, W, R, dt, slab_steps)
+    shape = make_shape(P, T, chunk_size, S, D, W, R, dt, slab_steps, flags)
     if readings is None:
         readings = torch.empty((P, T, D), dtype=dt, device=dev)
     if workspace is None:

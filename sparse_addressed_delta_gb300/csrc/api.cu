@@ -51,7 +51,8 @@ int check_shape(const sdm_shape *s, Dims &d) {
         return fail(SDM_ERR_INVALID, "bank_dtype must be SDM_F32 (0) or SDM_BF16 (1), got %d",
                     s->bank_dtype);
     if (s->slab_steps < 0) return fail(SDM_ERR_INVALID, "slab_steps must be >= 0");
-    if (s->flags != 0) return fail(SDM_ERR_INVALID, "flags must be 0, got %d", s->flags);
+    if (s->flags & ~SDM_FLAG_PER_STEP_KERNELS)
+        return fail(SDM_ERR_INVALID, "unknown flags 0x%x", (unsigned)s->flags);
     if (s->D != 32 && s->D != 64 && s->D != 128 && s->D != 256 && s->D != 512)
         return fail(SDM_ERR_UNSUPPORTED, "head_dim D=%d has no kernel (32, 64, 128, 256, 512)",
                     s->D);
@@ -62,6 +63,7 @@ int check_shape(const sdm_shape *s, Dims &d) {
     d.P = s->P; d.T = s->T; d.C = s->C; d.S = s->S; d.D = s->D; d.W = s->W; d.R = s->R;
     d.Nt = (int)Nt;
     d.dtype = s->bank_dtype;
+    d.per_step = (s->flags & SDM_FLAG_PER_STEP_KERNELS) ? 1 : 0;
     return SDM_OK;
 }
 
@@ -213,6 +215,11 @@ int run_forward(const Prepared &pr, const Inputs &in, void *workspace, cudaStrea
         const int nsteps = (d.Nt - s0) < pr.ns ? (d.Nt - s0) : pr.ns;
         SDM_LAUNCH(SDM_KERNEL_PHASE1, launch_phase1(d, in, w, s0, nsteps, st), "phase1");
         SDM_LAUNCH(SDM_KERNEL_SOLVE, launch_solve(d, in, w, s0, nsteps, st), "solve");
+        if (!d.per_step) {
+            SDM_LAUNCH(SDM_KERNEL_PHASE2, launch_phase2_fused(d, in, w, s0, nsteps, st),
+                       "phase2");
+            continue;
+        }
         for (int ti = s0; ti < s0 + nsteps; ++ti) {
             SDM_LAUNCH(SDM_KERNEL_GATHER, launch_gather(d, in, w, s0, ti, st), "gather");
             SDM_LAUNCH(SDM_KERNEL_DUALMM, launch_dualmm(d, in, w, s0, ti, st), "dual matmul");
@@ -246,7 +253,7 @@ int64_t sdm_launch_count(const sdm_shape *shape) {
     Prepared pr;
     if (prepare(shape, pr)) return 0;
     const int64_t slabs = (pr.d.Nt + pr.ns - 1) / pr.ns;
-    return slabs * 2 + (int64_t)pr.d.Nt * 3;
+    return pr.d.per_step ? slabs * 2 + (int64_t)pr.d.Nt * 3 : slabs * 3;
 }
 
 int sdm_write_read(const sdm_shape *shape, void *bank, const int32_t *write_slots,

@@ -30,6 +30,7 @@ struct DevStatus {
 struct Dims {
     int P, T, C, S, D, W, R, Nt;
     int dtype;   // SDM_F32 / SDM_BF16
+    int per_step;   // 1: Phase 2 as three kernels per step; 0: one fused kernel per slab
 };
 
 // Device pointers of one slab's workspace. N = ns * P chunks; chunk n of the slab is step
@@ -99,6 +100,9 @@ cudaError_t launch_dualmm(const Dims &d, const Inputs &in, const Work &w, int st
                           cudaStream_t st);
 cudaError_t launch_dw(const Dims &d, const Inputs &in, const Work &w, int step0, int ti,
                       cudaStream_t st);
+cudaError_t launch_phase2_fused(const Dims &d, const Inputs &in, const Work &w, int step0,
+                                int nsteps, cudaStream_t st);
+size_t phase2_fused_smem(const Dims &d);
 cudaError_t launch_debug_expand(const Dims &d, const Work &w, int nchunks, int32_t *perm,
                                 uint8_t *gstart, uint8_t *owner, float *dw_tok,
                                 cudaStream_t st);

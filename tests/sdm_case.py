@@ -36,16 +36,16 @@ def to_device(inputs, wl, device="cuda"):
             "read_slots": i("read_slots"), "read_w": f("read_w"), "valid": i("valid")}
 
 
-def run_gpu(wl, dev_inputs, slab_steps: int = 0, bank=None, workspace=None):
+def run_gpu(wl, dev_inputs, slab_steps: int = 0, bank=None, workspace=None, flags: int = 0):
     """One sdm_write_read call; returns (readings, final bank, workspace); the bank in
     ``dev_inputs`` is not modified (a copy is advanced) unless ``bank`` is given."""
     b = dev_inputs["bank"].clone() if bank is None else bank
-    shape = sdm.make_shape(wl.P, wl.T, wl.C, wl.S, wl.D, wl.W, wl.R, b.dtype, slab_steps)
+    shape = sdm.make_shape(wl.P, wl.T, wl.C, wl.S, wl.D, wl.W, wl.R, b.dtype, slab_steps, flags)
     ws = sdm.alloc_workspace(shape, b.device) if workspace is None else workspace
     r = sdm.sdm_write_read(b, dev_inputs["write_slots"], dev_inputs["write_w"],
                            dev_inputs["log_decay"], dev_inputs["beta"], dev_inputs["v"],
                            dev_inputs["read_slots"], dev_inputs["read_w"], dev_inputs["valid"],
-                           chunk_size=wl.C, slab_steps=slab_steps, workspace=ws)
+                           chunk_size=wl.C, slab_steps=slab_steps, workspace=ws, flags=flags)
     torch.cuda.synchronize()
     return r, b, ws
 

@@ -46,21 +46,27 @@ def test_workspace_bytes_host_only():
 
 def test_launch_count():
     s = sdm.make_shape(8, 4096, 64, 65536, 128, 16, 16, sdm.SDM_BF16)
+    assert sdm.launch_count(s) == 3                      # Phase 1, solve, fused Phase 2
+    s = sdm.make_shape(8, 4096, 64, 65536, 128, 16, 16, sdm.SDM_BF16,
+                       flags=sdm.FLAG_PER_STEP_KERNELS)
     assert sdm.launch_count(s) == 2 + 3 * 64
+    nt, slabs = 7, 3
     s = sdm.make_shape(1, 100, 16, 64, 64, 4, 4, sdm.SDM_F32, slab_steps=3)
-    nt = 7
-    assert sdm.launch_count(s) == 2 * 3 + 3 * nt
+    assert sdm.launch_count(s) == 3 * slabs
+    s = sdm.make_shape(1, 100, 16, 64, 64, 4, 4, sdm.SDM_F32, slab_steps=3,
+                       flags=sdm.FLAG_PER_STEP_KERNELS)
+    assert sdm.launch_count(s) == 2 * slabs + 3 * nt
 
 
 @pytest.mark.parametrize("kw,code", [
     (dict(C=8), -1), (dict(C=300), -1), (dict(W=0), -1), (dict(R=257), -1), (dict(P=0), -1),
-    (dict(T=0), -1), (dict(S=0), -1), (dict(D=96), -2), (dict(dtype=7), -1),
+    (dict(T=0), -1), (dict(S=0), -1), (dict(D=96), -2), (dict(dtype=7), -1), (dict(flags=6), -1),
     (dict(P=1 << 16, T=1 << 16), -1)])
 def test_refusals(kw, code):
-    base = dict(P=2, T=64, C=16, S=128, D=64, W=4, R=4, dtype=sdm.SDM_F32)
+    base = dict(P=2, T=64, C=16, S=128, D=64, W=4, R=4, dtype=sdm.SDM_F32, flags=0)
     base.update(kw)
     s = sdm.Shape(base["P"], base["T"], base["C"], base["S"], base["D"], base["W"], base["R"],
-                  base["dtype"], 0, 0)
+                  base["dtype"], 0, base["flags"])
     assert sdm.library().sdm_workspace_bytes(ctypes.byref(s)) == 0
     msg = sdm.library().sdm_last_error().decode()
     assert msg

@@ -20,16 +20,23 @@ def _cuda():
     sdm.library()
 
 
-def check(wl, inputs=None, slab_steps=0):
+PATHS = [0, sdm.FLAG_PER_STEP_KERNELS]      # fused Phase 2 (default), per-step kernels
+
+
+def check(wl, inputs=None, slab_steps=0, flags=(0, sdm.FLAG_PER_STEP_KERNELS)):
+    """Both Phase-2 paths against the oracle (and each other, within the tolerance)."""
     inputs = si.generate(wl) if inputs is None else inputs
     dev = to_device(inputs, wl)
-    r, b, ws = run_gpu(wl, dev, slab_steps)
-    st = sdm.device_status(ws)
-    assert st["code"] == 0 and st["bad_slots"] == 0 and st["repeated_write_slots"] == 0, st
-    er, eb = compare_with_oracle(wl, inputs, r, b)
     tol = TOL[wl.dtype]
-    assert er <= tol and eb <= tol, (wl.name, er, eb)
-    return er, eb
+    errs = []
+    for fl in flags:
+        r, b, ws = run_gpu(wl, dev, slab_steps, flags=fl)
+        st = sdm.device_status(ws)
+        assert st["code"] == 0 and st["bad_slots"] == 0 and st["repeated_write_slots"] == 0, st
+        er, eb = compare_with_oracle(wl, inputs, r, b)
+        assert er <= tol and eb <= tol, (wl.name, fl, er, eb)
+        errs.append((er, eb))
+    return errs[0]
 
 
 def test_workload0_full():
@@ -65,7 +72,8 @@ def test_mix_slots_bf16():
                          slots="mix", seed=9))
 
 
-def test_empty_streams_and_full_padding():
+@pytest.mark.parametrize("flags", PATHS)
+def test_empty_streams_and_full_padding(flags):
     wl = small_workload(P=4, T=64, C=16, S=40, D=64, W=3, R=3, ragged=False, seed=3)
     inputs = si.generate(wl)
     inputs["valid"] = np.array([0, 1, 17, 64], np.int32)
@@ -74,44 +82,47 @@ def test_empty_streams_and_full_padding():
         inputs[k][1, 1:] = 0
         inputs[k][2, 17:] = 0
     dev = to_device(inputs, wl)
-    r, b, _ = run_gpu(wl, dev)
+    r, b, _ = run_gpu(wl, dev, flags=flags)
     assert not f64(r[0]).any() and not f64(r[1, 1:]).any() and not f64(r[2, 17:]).any()
     assert torch.equal(b[:wl.S], dev["bank"][:wl.S])
     er, eb = compare_with_oracle(wl, inputs, r, b)
     assert er <= 1e-4 and eb <= 1e-4
 
 
-def test_padding_inputs_never_read():
+@pytest.mark.parametrize("flags", PATHS)
+def test_padding_inputs_never_read(flags):
     """NaN in every input of a padding token changes nothing, bit for bit."""
     wl = small_workload(P=3, T=90, C=32, S=64, D=64, W=4, R=4, ragged=True, seed=8)
     inputs = si.generate(wl)
     dev = to_device(inputs, wl)
-    r1, b1, _ = run_gpu(wl, dev)
+    r1, b1, _ = run_gpu(wl, dev, flags=flags)
     pad = torch.arange(wl.T, device="cuda")[None, :] >= dev["valid"][:, None]
     for k in ("write_w", "log_decay", "v", "read_w"):
         dev[k][pad] = float("nan")
     dev["beta"][pad] = float("nan")
     dev["write_slots"][pad] = -5
     dev["read_slots"][pad] = 1 << 30
-    r2, b2, ws = run_gpu(wl, dev)
+    r2, b2, ws = run_gpu(wl, dev, flags=flags)
     assert torch.equal(r1, r2) and torch.equal(b1, b2)
     assert sdm.device_status(ws)["code"] == 0
 
 
-def test_deterministic_bitwise():
+@pytest.mark.parametrize("flags", PATHS)
+def test_deterministic_bitwise(flags):
     wl = small_workload(P=4, T=256, C=64, S=300, D=128, W=16, R=16, dtype="bf16", seed=11)
     dev = to_device(si.generate(wl), wl)
-    r1, b1, _ = run_gpu(wl, dev)
-    r2, b2, _ = run_gpu(wl, dev)
+    r1, b1, _ = run_gpu(wl, dev, flags=flags)
+    r2, b2, _ = run_gpu(wl, dev, flags=flags)
     assert torch.equal(r1, r2) and torch.equal(b1, b2)
 
 
-def test_slab_invariance_bitwise():
+@pytest.mark.parametrize("flags", PATHS)
+def test_slab_invariance_bitwise(flags):
     wl = small_workload(P=3, T=200, C=16, S=100, D=64, W=4, R=4, seed=12)
     dev = to_device(si.generate(wl), wl)
-    r0, b0, _ = run_gpu(wl, dev, slab_steps=0)
+    r0, b0, _ = run_gpu(wl, dev, slab_steps=0, flags=flags)
     for ns in (1, 2, 5):
-        r, b, _ = run_gpu(wl, dev, slab_steps=ns)
+        r, b, _ = run_gpu(wl, dev, slab_steps=ns, flags=flags)
         assert torch.equal(r, r0) and torch.equal(b, b0), ns
 
 
@@ -170,7 +181,8 @@ def test_phase1_plan_and_intermediates():
 
 @pytest.mark.parametrize("cfg", [1, 2, 3, 4])
 def test_full_size_workloads(cfg):
-    """The four larger workloads at full size, whole readings and final bank."""
+    """The four larger workloads at full size (the launch configuration bench.py times),
+    whole readings and final bank."""
     wl = si.WORKLOADS[cfg]
     inputs = si.generate(wl)
     dev = to_device(inputs, wl)

@@ -180,6 +180,34 @@ int sdm_get_device_status(const void *workspace, sdm_device_status *status, void
 /* Number of kernel launches sdm_write_read queues for this shape (0 if refused). */
 int64_t sdm_launch_count(const sdm_shape *shape);
 
+/* Bytes of the static device scratch sdm_write_read_noalloc uses (16 MiB per GPU). */
+#define SDM_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+
+/* sdm_write_read for callers that cannot allocate device memory. The pages have no
+ * counterpart: this entry point serves hosts that own every byte of device memory (an engine
+ * or plugin host with its own pool, or a fixed-footprint or real-time service) and cannot call
+ * cudaMalloc, or do not want to, as cudaMalloc may synchronize the device. Instead of a caller
+ * workspace it uses one static device array of SDM_NOALLOC_SCRATCH_BYTES that lives in the
+ * library: the CUDA driver reserves it on every GPU that loads the library, and it stays
+ * reserved until the process exits. The caller still provides the bank, the inputs and the
+ * readings (same arguments, layouts and results as sdm_write_read, without workspace).
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress,
+ *     with that device current), once per device; make that first call before any CUDA
+ *     stream capture.
+ *   - Phase-2 slabs are sized to fit the array (results do not depend on the slab size). A
+ *     shape that does not fit even at one step per slab, or an explicit slab_steps that does
+ *     not fit, is refused with SDM_ERR_WORKSPACE before any work.
+ *   - Every call shares the one array, which keeps the last call's contents; the call clears
+ *     what must start at zero itself. Calls whose work overlaps on the GPU (other streams,
+ *     other host threads) race on the array: serialize them.
+ *   - The device status of such a call is not readable through sdm_get_device_status (slots
+ *     outside [0, S) are still never dereferenced). */
+int sdm_write_read_noalloc(const sdm_shape *shape, void *bank, const int32_t *write_slots,
+                           const void *write_w, const float *log_decay, const float *beta,
+                           const void *v, const int32_t *read_slots, const void *read_w,
+                           const int32_t *valid_tokens, void *readings, void *stream);
+
 /* Thread-local description of the last refused call or CUDA error ("" if none). */
 const char *sdm_last_error(void);
 

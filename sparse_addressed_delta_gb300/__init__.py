@@ -19,7 +19,7 @@ from typing import Dict, Optional
 
 import torch
 
-__all__ = ["sdm_write_read", "profile_write_read", "workspace_bytes", "launch_count",
+__all__ = ["sdm_write_read", "sdm_write_read_noalloc", "profile_write_read", "workspace_bytes", "launch_count",
            "phase1_debug", "KERNEL_KINDS",
            "device_status", "SdmError", "Shape", "library", "library_path", "version"]
 
@@ -73,6 +73,8 @@ def library() -> ctypes.CDLL:
             lib.sdm_launch_count.restype = i64
             lib.sdm_write_read.argtypes = [sp] + [vp] * 10 + [vp, sz, vp]
             lib.sdm_write_read.restype = i32
+            lib.sdm_write_read_noalloc.argtypes = [sp] + [vp] * 10 + [vp]
+            lib.sdm_write_read_noalloc.restype = i32
             lib.sdm_profile_write_read.argtypes = ([sp] + [vp] * 10 + [vp, sz]
                                                    + [ctypes.POINTER(ctypes.c_float),
                                                       ctypes.POINTER(ctypes.c_int32), vp])
@@ -195,6 +197,38 @@ def sdm_write_read(bank: torch.Tensor, write_slots: torch.Tensor, write_w: torch
             ctypes.byref(shape), _ptr(bank), _ptr(write_slots), _ptr(write_w), _ptr(log_decay),
             _ptr(beta), _ptr(v), _ptr(read_slots), _ptr(read_w), _ptr(valid_tokens),
             _ptr(readings), _ptr(workspace), workspace.numel(), _stream_ptr(stream))
+    _check(rc)
+    return readings
+
+
+def sdm_write_read_noalloc(bank: torch.Tensor, write_slots: torch.Tensor,
+                           write_w: torch.Tensor, log_decay: torch.Tensor, beta: torch.Tensor,
+                           v: torch.Tensor, read_slots: torch.Tensor, read_w: torch.Tensor,
+                           valid_tokens: Optional[torch.Tensor] = None, *, chunk_size: int,
+                           readings: torch.Tensor, slab_steps: int = 0, stream=None,
+                           flags: int = 0) -> torch.Tensor:
+    """sdm_write_read for callers that cannot allocate device memory: the library's static
+    device scratch (16 MiB per GPU) replaces the workspace, and the caller passes the
+    readings buffer, so the call allocates nothing. Calls overlapping on the GPU race on the
+    shared scratch; the first call on a device should come before any CUDA graph capture."""
+    P, T, W = write_slots.shape
+    R = read_slots.shape[-1]
+    S, D = bank.shape[0] // P, bank.shape[1]
+    dev, dt = bank.device, bank.dtype
+    for t, name, shp, typ in ((bank, "bank", (P * S, D), dt), (write_slots, "write_slots", (P, T, W), torch.int32),
+                              (write_w, "write_w", (P, T, W), dt), (log_decay, "log_decay", (P, T, W), torch.float32),
+                              (beta, "beta", (P, T), torch.float32), (v, "v", (P, T, D), dt),
+                              (read_slots, "read_slots", (P, T, R), torch.int32), (read_w, "read_w", (P, T, R), dt),
+                              (readings, "readings", (P, T, D), dt)):
+        _need(t, name, shp, typ, dev)
+    if valid_tokens is not None:
+        _need(valid_tokens, "valid_tokens", (P,), torch.int32, dev)
+    shape = make_shape(P, T, chunk_size, S, D, W, R, dt, slab_steps, flags)
+    with torch.cuda.device(dev):
+        rc = library().sdm_write_read_noalloc(
+            ctypes.byref(shape), _ptr(bank), _ptr(write_slots), _ptr(write_w), _ptr(log_decay),
+            _ptr(beta), _ptr(v), _ptr(read_slots), _ptr(read_w), _ptr(valid_tokens),
+            _ptr(readings), _stream_ptr(stream))
     _check(rc)
     return readings
 

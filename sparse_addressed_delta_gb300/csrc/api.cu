@@ -29,6 +29,18 @@ int fail(int code, const char *fmt, ...) {
     return code;
 }
 
+}  // namespace
+
+int set_error(int code, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+namespace {
+
 int cuda_fail(cudaError_t e, const char *what) {
     return fail(SDM_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }

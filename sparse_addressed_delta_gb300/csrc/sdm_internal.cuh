@@ -80,6 +80,9 @@ struct Inputs {
     void *readings;
 };
 
+// Sets the thread's sdm_last_error() message; returns code.
+int set_error(int code, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
+
 // ---------------------------------------------------------------------------------------
 // host-side layout (api.cu)
 // ---------------------------------------------------------------------------------------

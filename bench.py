@@ -51,6 +51,9 @@ def parse_args():
     ap.add_argument("--profile-steps", type=int, default=3)
     ap.add_argument("--per-step-kernels", action="store_true",
                     help="run Phase 2 as three kernels per step instead of the fused kernel")
+    ap.add_argument("--ncu-run", type=int, default=0, metavar="K",
+                    help="profiling target: run K plain (eager) calls on the workload and exit, "
+                         "printing no benchmark line")
     return ap.parse_args()
 
 
@@ -408,8 +411,38 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_for_profiler(args):
+    """K eager sdm_write_read calls on the workload, for an external profiler (ncu)."""
+    import torch
+
+    import sparse_addressed_delta_gb300 as sdm
+
+    wl = si.WORKLOADS[args.workload]
+    inputs = si.generate(wl)
+    dev = torch.device("cuda", 0)
+    dt = torch.float32 if wl.dtype == "f32" else torch.bfloat16
+
+    def tens(name):
+        t = torch.from_numpy(np.ascontiguousarray(inputs[name]))
+        if wl.dtype == "bf16" and inputs[name].dtype == np.uint16:
+            t = t.view(torch.bfloat16)
+        return t.to(dev)
+
+    d = {k: tens(k) for k in inputs}
+    flags = sdm.FLAG_PER_STEP_KERNELS if args.per_step_kernels else 0
+    for _ in range(args.ncu_run):
+        sdm.sdm_write_read(d["bank"], d["write_slots"], d["write_w"], d["log_decay"], d["beta"],
+                           d["v"], d["read_slots"], d["read_w"], d["valid"], chunk_size=wl.C,
+                           flags=flags)
+    torch.cuda.synchronize()
+    print(f"ncu target: {args.ncu_run} calls of {wl.name} done")
+
+
 def main():
     args = parse_args()
+    if args.ncu_run:
+        run_for_profiler(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

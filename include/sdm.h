@@ -115,7 +115,8 @@ size_t sdm_workspace_bytes(const sdm_shape *shape);
  * Returns SDM_OK once the work is queued (asynchronous). A slot outside [0, S) is not
  * dereferenced: the entry is dropped, and the device status (sdm_get_device_status) reports
  * SDM_ERR_DEVICE; repeated write slots in a token are counted there (results for such a
- * token are unspecified). The bank, readings and inputs must not overlap. */
+ * token are unspecified). The bank, readings and inputs must not overlap; bank, v and
+ * readings must be 16-byte aligned (SDM_ERR_INVALID otherwise). */
 int sdm_write_read(const sdm_shape *shape, void *bank, const int32_t *write_slots,
                    const void *write_w, const float *log_decay, const float *beta,
                    const void *v, const int32_t *read_slots, const void *read_w,

@@ -81,7 +81,7 @@ int check_shape(const sdm_shape *s, Dims &d) {
 
 size_t per_chunk_bytes(const Dims &d) {
     const size_t CW = (size_t)d.C * d.W, CR = (size_t)d.C * d.R, CC = (size_t)d.C * d.C;
-    return 4 * (8 * CW + 1) + 4 * 2 * CR + 4 * 4 * CC + 8;
+    return 4 * (11 * CW + 1) + 4 * 2 * CR + 4 * 4 * CC + 8;
 }
 
 int slab_steps(const Dims &d, int requested) {
@@ -113,6 +113,9 @@ int phase1_ctas(const Dims &d, int ns) {
     F(gfac, float, N * CW)                                                    \
     F(ngroups, int32_t, N)                                                    \
     F(nvalid, int32_t, N)                                                     \
+    F(minfo, int32_t, N * CW)                                                 \
+    F(mslot, int32_t, N * CW)                                                 \
+    F(mfac, float, N * CW)                                                    \
     F(gw, float, N * CW)                                                      \
     F(qw, float, N * CR)                                                      \
     F(lw, float, N * CW)                                                      \
@@ -125,6 +128,7 @@ int phase1_ctas(const Dims &d, int ns) {
     F(inv, int32_t, G * CW)                                                   \
     F(lws, float, G * CW)                                                     \
     F(pgid, int32_t, G * CW)                                                  \
+    F(pgs, int32_t, G * CW)                                                   \
     F(lend, float, G * CW)                                                    \
     F(kf, float, G * CW)                                                      \
     F(rlo, int32_t, G * CR)                                                   \
@@ -206,8 +210,9 @@ int check_inputs(const Inputs &in, bool need_bank) {
     if (need_bank && (!in.v || !in.readings))
         return fail(SDM_ERR_INVALID, "v and readings must not be NULL");
     if (need_bank && (reinterpret_cast<uintptr_t>(in.bank) % 16 ||
-                      reinterpret_cast<uintptr_t>(in.readings) % 16))
-        return fail(SDM_ERR_INVALID, "bank and readings must be 16-byte aligned");
+                      reinterpret_cast<uintptr_t>(in.readings) % 16 ||
+                      reinterpret_cast<uintptr_t>(in.v) % 16))
+        return fail(SDM_ERR_INVALID, "bank, v and readings must be 16-byte aligned");
     return SDM_OK;
 }
 

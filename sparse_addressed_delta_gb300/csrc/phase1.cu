@@ -174,7 +174,8 @@ __device__ __forceinline__ void report_bad_slot(DevStatus *st, int token) {
 }
 
 template <typename WT>
-__global__ void __launch_bounds__(NT) k_phase1(Dims d, Inputs in, Work w, int step0, int nsteps) {
+__global__ void __launch_bounds__(NT) k_phase1(Dims d, Inputs in, Work w, int step0, int nsteps,
+                                               int scratch_in_smem) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     P1Smem &sm = *reinterpret_cast<P1Smem *>(smem_raw);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -183,18 +184,41 @@ __global__ void __launch_bounds__(NT) k_phase1(Dims d, Inputs in, Work w, int st
     const WT *kw = static_cast<const WT *>(in.kw);
     const WT *qwin = static_cast<const WT *>(in.qw);
     const int N = nsteps * d.P;
+    const unsigned magW = div_magic(W);
+    // sort keys are (slot << 32 | t << 8 | j): the low word orders like e = t*W + j, and the
+    // token of an entry is a shift away
+    auto ent_of = [W](unsigned low) { return (int)(low >> 8) * W + (int)(low & 255u); };
     const int bits = S <= 1 ? 0 : 32 - __clz(S - 1);
     const int passes = (bits + 7) / 8;
 
-    unsigned long long *keyA = w.keys + (size_t)blockIdx.x * 2 * CW;
+    // per-chunk scratch: in shared memory after P1Smem when it fits, else the CTA's slice of
+    // the workspace (same layout either way)
+    unsigned long long *keyA;
+    int32_t *inv, *pgid, *pgs, *rlo, *rhi;
+    float *lws, *lend, *kf;
+    if (scratch_in_smem) {
+        unsigned char *q = smem_raw + ((sizeof(P1Smem) + 15) & ~size_t(15));
+        keyA = reinterpret_cast<unsigned long long *>(q); q += sizeof(unsigned long long) * 2 * CW;
+        inv = reinterpret_cast<int32_t *>(q); q += 4 * (size_t)CW;
+        pgid = reinterpret_cast<int32_t *>(q); q += 4 * (size_t)CW;
+        pgs = reinterpret_cast<int32_t *>(q); q += 4 * (size_t)CW;
+        lws = reinterpret_cast<float *>(q); q += 4 * (size_t)CW;
+        lend = reinterpret_cast<float *>(q); q += 4 * (size_t)CW;
+        kf = reinterpret_cast<float *>(q); q += 4 * (size_t)CW;
+        rlo = reinterpret_cast<int32_t *>(q); q += 4 * (size_t)CR;
+        rhi = reinterpret_cast<int32_t *>(q);
+    } else {
+        keyA = w.keys + (size_t)blockIdx.x * 2 * CW;
+        inv = w.inv + (size_t)blockIdx.x * CW;
+        pgid = w.pgid + (size_t)blockIdx.x * CW;
+        pgs = w.pgs + (size_t)blockIdx.x * CW;
+        lws = w.lws + (size_t)blockIdx.x * CW;
+        lend = w.lend + (size_t)blockIdx.x * CW;
+        kf = w.kf + (size_t)blockIdx.x * CW;
+        rlo = w.rlo + (size_t)blockIdx.x * CR;
+        rhi = w.rhi + (size_t)blockIdx.x * CR;
+    }
     unsigned long long *keyB = keyA + CW;
-    int32_t *inv = w.inv + (size_t)blockIdx.x * CW;
-    float *lws = w.lws + (size_t)blockIdx.x * CW;
-    int32_t *pgid = w.pgid + (size_t)blockIdx.x * CW;
-    float *lend = w.lend + (size_t)blockIdx.x * CW;
-    float *kf = w.kf + (size_t)blockIdx.x * CW;
-    int32_t *rlo = w.rlo + (size_t)blockIdx.x * CR;
-    int32_t *rhi = w.rhi + (size_t)blockIdx.x * CR;
 
     for (int n = blockIdx.x; n < N; n += gridDim.x) {
         const int p = n % d.P, ti = step0 + n / d.P;
@@ -217,28 +241,36 @@ __global__ void __launch_bounds__(NT) k_phase1(Dims d, Inputs in, Work w, int st
         float *qw = w.qw + (size_t)n * CR;
         float *lw = w.lw + (size_t)n * CW;
         float *lr = w.lr + (size_t)n * CR;
+        int32_t *minfo = w.minfo + (size_t)n * CW;
+        int32_t *mslot = w.mslot + (size_t)n * CW;
+        float *mfac = w.mfac + (size_t)n * CW;
         float *A = w.A + (size_t)n * CC;
         float *QK = w.QK + (size_t)n * CC;
 
-        // 1. keys (a slot outside [0, S) is reported and sorted as slot 0 with weight 0 and
-        //    log-decay 0, so that it adds nothing anywhere)
+        // 1. keys (a slot outside [0, S) is reported and sorted as slot S, after every real
+        //    slot, with weight 0 and log-decay 0: it adds nothing anywhere and no DW writes it)
+        int bad = 0;
         for (int i = tid; i < nw; i += NT) {
             int s = ws[i];
             float kk = to_f32(k[i]);
             if ((unsigned)s >= (unsigned)S) {
                 report_bad_slot(w.status, (int)(tok_base + i / W));
-                s = 0;
+                s = S;
                 kk = 0.f;
+                bad = 1;
             }
             kf[i] = kk;
-            keyA[i] = ((unsigned long long)(unsigned)s << 32) | (unsigned)i;
+            const int t = div_by(i, magW);
+            keyA[i] = ((unsigned long long)(unsigned)s << 32) | ((unsigned)t << 8) |
+                      (unsigned)(i - t * W);
         }
         for (int i = tid; i < nr; i += NT) {
             if ((unsigned)rs[i] >= (unsigned)S) report_bad_slot(w.status, (int)(tok_base + i / R));
         }
-        __syncthreads();
+        // slot S may need one more radix digit than the real slots
+        const int npass = __syncthreads_or(bad) ? (32 - __clz(S) + 7) / 8 : passes;
         unsigned long long *src = keyA, *dst = keyB;
-        for (int ps = 0; ps < passes; ++ps) {
+        for (int ps = 0; ps < npass; ++ps) {
             radix_pass(src, dst, nw, 32 + 8 * ps, sm);
             unsigned long long *t = src; src = dst; dst = t;
         }
@@ -251,14 +283,15 @@ __global__ void __launch_bounds__(NT) k_phase1(Dims d, Inputs in, Work w, int st
             const int pos = tile + tid;
             const bool ok = pos < nw;
             unsigned long long key = ok ? srt[pos] : 0ull;
-            const int slot = (int)(key >> 32), e = (int)(key & 0xffffffffu);
+            const unsigned low = (unsigned)(key & 0xffffffffu);
+            const int slot = (int)(key >> 32), e = ent_of(low);
             bool head = ok && (pos == 0 || (int)(srt[pos - 1] >> 32) != slot);
             float gv = 0.f;
             if (ok) {
                 gv = ((unsigned)ws[e] < (unsigned)S) ? g[e] : 0.f;
                 perm[pos] = e;
                 inv[e] = pos;
-                if (!head && (int)(srt[pos - 1] & 0xffffffffu) / W == e / W)
+                if (!head && ((unsigned)srt[pos - 1] >> 8) == (low >> 8))
                     atomicAdd(&w.status->repeated_write_slots, 1ull);
             }
             float cv, lv;
@@ -273,10 +306,16 @@ __global__ void __launch_bounds__(NT) k_phase1(Dims d, Inputs in, Work w, int st
                 pgid[pos] = gid;
                 if (head) { goff[gid] = pos; gslot[gid] = slot; }
                 const bool tail = (pos == nw - 1) || (int)(srt[pos + 1] >> 32) != slot;
+                float fac = 0.f;
                 if (tail) {
                     lend[gid] = lv;
-                    gfac[gid] = expf(lv);
+                    fac = expf(lv);
+                    gfac[gid] = fac;
                 }
+                minfo[pos] = (int)(low >> 8) | (int)((low & 255u) << 8) | (head ? 1 << 16 : 0) |
+                             (tail ? 1 << 17 : 0);
+                mslot[pos] = slot;
+                mfac[pos] = fac;
             }
         }
         const int ng = carry_i;
@@ -286,23 +325,27 @@ __global__ void __launch_bounds__(NT) k_phase1(Dims d, Inputs in, Work w, int st
             goff[ng] = nw;
         }
         __syncthreads();
+        // group start of every sorted position (one lookup instead of a chain later)
+        for (int pos = tid; pos < nw; pos += NT) pgs[pos] = goff[pgid[pos]];
+        __syncthreads();
 
         // 3. weights
         for (int pos = tid; pos < nw; pos += NT) {
-            const int e = perm[pos];
+            const int e = ent_of((unsigned)srt[pos]);
             const float kk = kf[e];
             const float l = lws[pos];
             wdw[pos] = kk * expf(lend[pgid[pos]] - l);
             gw[e] = kk * expf(l);
         }
+        const unsigned magR = div_magic(R);
         for (int er = tid; er < nr; er += NT) {
-            const int t = er / R;
+            const int t = div_by(er, magR);
             const int r = rs[er];
             int lo = 0, hi = -1;
             float l = 0.f;
             if ((unsigned)r < (unsigned)S) {
                 const unsigned long long target =
-                    ((unsigned long long)(unsigned)r << 32) | (unsigned)(t * W + W - 1);
+                    ((unsigned long long)(unsigned)r << 32) | ((unsigned)t << 8) | 255u;
                 int a = 0, b = nw;
                 while (a < b) {
                     int mid = (a + b) >> 1;
@@ -311,7 +354,7 @@ __global__ void __launch_bounds__(NT) k_phase1(Dims d, Inputs in, Work w, int st
                 const int pos = a - 1;
                 if (pos >= 0 && (int)(srt[pos] >> 32) == r) {
                     hi = pos;
-                    lo = goff[pgid[pos]];
+                    lo = pgs[pos];
                     l = lws[pos];
                 }
             }
@@ -333,11 +376,11 @@ __global__ void __launch_bounds__(NT) k_phase1(Dims d, Inputs in, Work w, int st
                     const float ka = kf[e];
                     if (ka == 0.f) continue;
                     const int pos = inv[e];
-                    const int gs = goff[pgid[pos]];
+                    const int gs = pgs[pos];
                     const float la = lws[pos];
                     for (int m = gs + lane; m < pos; m += 32) {
-                        const int eb = perm[m];
-                        row[eb / W] += ka * kf[eb] * expf(la - lws[m]);
+                        const unsigned lb = (unsigned)srt[m];
+                        row[lb >> 8] += ka * kf[ent_of(lb)] * expf(la - lws[m]);
                     }
                     __syncwarp();
                 }
@@ -354,8 +397,8 @@ __global__ void __launch_bounds__(NT) k_phase1(Dims d, Inputs in, Work w, int st
                     const float qa = to_f32(q[er]);
                     const float la = lr[er];
                     for (int m = lo + lane; m <= hi; m += 32) {
-                        const int eb = perm[m];
-                        row[eb / W] += qa * kf[eb] * expf(la - lws[m]);
+                        const unsigned lb = (unsigned)srt[m];
+                        row[lb >> 8] += qa * kf[ent_of(lb)] * expf(la - lws[m]);
                     }
                     __syncwarp();
                 }
@@ -373,18 +416,25 @@ __global__ void __launch_bounds__(NT) k_phase1(Dims d, Inputs in, Work w, int st
 
 }  // namespace
 
+size_t phase1_scratch_smem(const Dims &d) {
+    const size_t CW = (size_t)d.C * d.W, CR = (size_t)d.C * d.R;
+    return ((sizeof(P1Smem) + 15) & ~size_t(15)) + 8 * 2 * CW + 4 * 6 * CW + 4 * 2 * CR;
+}
+
 cudaError_t launch_phase1(const Dims &d, const Inputs &in, const Work &w, int step0, int nsteps,
                           cudaStream_t st) {
-    const size_t smem = sizeof(P1Smem);
+    const size_t full = phase1_scratch_smem(d);
+    const int in_smem = full <= kPhase1SmemMax ? 1 : 0;
+    const size_t smem = in_smem ? full : sizeof(P1Smem);
     const int grid = w.G;
     if (d.dtype == SDM_BF16) {
         auto kern = k_phase1<__nv_bfloat16>;
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        kern<<<grid, NT, smem, st>>>(d, in, w, step0, nsteps);
+        kern<<<grid, NT, smem, st>>>(d, in, w, step0, nsteps, in_smem);
     } else {
         auto kern = k_phase1<float>;
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        kern<<<grid, NT, smem, st>>>(d, in, w, step0, nsteps);
+        kern<<<grid, NT, smem, st>>>(d, in, w, step0, nsteps, in_smem);
     }
     return cudaGetLastError();
 }

@@ -235,6 +235,7 @@ __global__ void __launch_bounds__(kBlock) k_dw(Dims d, Inputs in, Work w, int st
     BT *bank = static_cast<BT *>(in.bank) + (size_t)p * d.S * D + lane * CPL;
     for (int g = blockIdx.x * kWarps + warp; g < ng; g += gridDim.x * kWarps) {
         const int o0 = goff[g], o1 = goff[g + 1];
+        if ((unsigned)gslot[g] >= (unsigned)d.S) continue;
         BT *row = bank + (size_t)gslot[g] * D;
         const float f = gfac[g];
         float acc[CPL];

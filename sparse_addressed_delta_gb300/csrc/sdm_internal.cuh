@@ -17,6 +17,8 @@ constexpr int kMaxWidth = 256;
 constexpr int kRefSms = 152;            // GB300 SM count: sizes grids and slabs (shape-only)
 constexpr size_t kAlign = 256;
 constexpr size_t kSlabBudget = size_t(256) << 20;   // per-chunk Phase-1 state held at once
+constexpr size_t kPhase1SmemMax = 200 * 1024;        // Phase-1 scratch kept on chip up to this
+constexpr size_t kPipeSmemMax = 224 * 1024;          // pipelined Phase 2 when two stages fit
 
 // Device status block at the start of the workspace (sdm_device_status, with the first bad
 // token stored +1 so that a zero fill means "none").
@@ -47,6 +49,9 @@ struct Work {
     int32_t *nvalid;    // [N]       valid tokens of the chunk
     float *gw;          // [N][CW]   token-major gather weights of the writes
     float *qw;          // [N][CR]   token-major gather weights of the reads
+    int32_t *minfo;     // [N][CW]   sorted position: t | j << 8 | head << 16 | tail << 17
+    int32_t *mslot;     // [N][CW]   slot of each sorted position
+    float *mfac;        // [N][CW]   exp(lend) of the group at its tail position (else 0)
     float *lw;          // [N][CW]   token-major running log-decay of the writes
     float *lr;          // [N][CR]   token-major running log-decay of the reads
     float *A, *QK, *X, *QX;   // [N][C*C]
@@ -55,6 +60,7 @@ struct Work {
     int32_t *inv;       // [G][CW]  sorted position of each entry
     float *lws;         // [G][CW]  running log-decay at each sorted position
     int32_t *pgid;      // [G][CW]  group id of each sorted position
+    int32_t *pgs;       // [G][CW]  group start position of each sorted position
     float *lend;        // [G][CW]  log-decay total of each group
     float *kf;          // [G][CW]  write weight of each entry as float (0 for a bad slot)
     int32_t *rlo;       // [G][CR]  first write position of the read's slot group
@@ -177,6 +183,29 @@ __device__ __forceinline__ void store_vec(T *p, const float (&x)[N]) {
     } else {
         p[0] = tmp[0];
     }
+}
+
+// Exact e / W for 0 <= e < 2^16 and 1 <= W <= 256 with m = ceil(2^24 / W): the rounding error
+// of the reciprocal is below e / 2^24 < 1/256 <= 1/W, which never carries past an integer.
+__host__ __device__ __forceinline__ unsigned div_magic(int W) {
+    return (unsigned)(((1u << 24) + (unsigned)W - 1u) / (unsigned)W);
+}
+__device__ __forceinline__ int div_by(int e, unsigned magic) {
+    return (int)(((unsigned long long)(unsigned)e * magic) >> 24);
+}
+
+__device__ __forceinline__ void cp_async4(void *smem_dst, const void *gsrc) {
+    const unsigned d = (unsigned)__cvta_generic_to_shared(smem_dst);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(d), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gsrc) {
+    const unsigned d = (unsigned)__cvta_generic_to_shared(smem_dst);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(d), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
 __device__ __forceinline__ int chunk_valid(const int32_t *valid, int p, int T, int tok0, int C) {

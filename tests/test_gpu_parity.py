@@ -126,16 +126,27 @@ def test_slab_invariance_bitwise(flags):
         assert torch.equal(r, r0) and torch.equal(b, b0), ns
 
 
-def test_bad_slot_is_reported_not_dereferenced():
+@pytest.mark.parametrize("flags", PATHS)
+def test_bad_slot_is_reported_and_dropped(flags):
+    """A slot outside [0, S) is reported and its entry dropped: the result equals the call
+    in which that entry has weight 0 and log-decay 0 on an unused slot."""
     wl = small_workload(P=2, T=40, C=16, S=64, D=64, W=4, R=4, ragged=False, seed=13)
     inputs = si.generate(wl)
+    ref_in = {k: v.copy() for k, v in inputs.items()}
     inputs["write_slots"][1, 5, 2] = 1 << 30
     inputs["read_slots"][0, 9, 1] = -3
-    dev = to_device(inputs, wl)
-    _, _, ws = run_gpu(wl, dev)
+    free = sorted(set(range(wl.S)) - set(ref_in["write_slots"][1, 5].tolist()))[0]
+    ref_in["write_slots"][1, 5, 2] = free
+    ref_in["write_w"][1, 5, 2] = 0
+    ref_in["log_decay"][1, 5, 2] = 0
+    ref_in["read_w"][0, 9, 1] = 0
+    r, b, ws = run_gpu(wl, to_device(inputs, wl), flags=flags)
     st = sdm.device_status(ws)
     assert st["code"] == -6 and st["bad_slots"] == 2
     assert st["first_bad_token"] in (1 * wl.T + 5, 9)
+    r2, b2, _ = run_gpu(wl, to_device(ref_in, wl), flags=flags)
+    assert (r - r2).abs().max() <= 1e-5 * r2.abs().max()
+    assert (b - b2).abs().max() <= 1e-5 * b2.abs().max()
 
 
 def test_repeated_write_slot_is_counted():

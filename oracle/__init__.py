@@ -68,7 +68,8 @@ def _load():
             lib.sdm_oracle_plan.restype = I
             lib.sdm_oracle_backward.argtypes = [I, I, I, I, I, I, _f64p, _i32p, _f64p, _f64p,
                                                 _f64p, _f64p, _i32p, _f64p, _i32p, _f64p,
-                                                _f64p, _f64p, _f64p, _f64p, _f64p, _f64p, I]
+                                                _dbl_or_null, _f64p, _f64p, _f64p, _f64p,
+                                                _f64p, _f64p, I]
             lib.sdm_oracle_backward.restype = I
             _lib = lib
     return _lib
@@ -160,10 +161,13 @@ def plan(slots) -> Dict[str, np.ndarray]:
     return {"perm": perm, "group_start": gs, "owner": ow, "only": on, "groups": int(groups)}
 
 
-def backward(bank, ws, k, g, beta, v, rs, q, valid, grad_readings, nthreads: int = 1):
-    """Reverse mode of the token loop. Returns a dict with grad_bank [P*S, D], grad_v,
-    grad_beta, grad_write_w, grad_log_decay, grad_read_w and restored_bank (the bank after
-    forward + backward, which equals the initial bank)."""
+def backward(bank, ws, k, g, beta, v, rs, q, valid, grad_readings, nthreads: int = 1,
+             grad_final_bank=None):
+    """Reverse mode of the token loop. ``grad_final_bank`` (optional, [P*S, D]) is the loss
+    gradient with respect to the final bank. Returns a dict with grad_bank [P*S, D] (with
+    respect to the initial bank), grad_v, grad_beta, grad_write_w, grad_log_decay,
+    grad_read_w and restored_bank (the bank after forward + backward, which equals the
+    initial bank)."""
     B = _f64(bank).copy()
     ws, rs = _i32(ws), _i32(rs)
     P, T, S, D, W, R = _dims(B, ws, rs, v)
@@ -174,9 +178,15 @@ def backward(bank, ws, k, g, beta, v, rs, q, valid, grad_readings, nthreads: int
     dk = np.zeros((P, T, W), np.float64)
     dg = np.zeros((P, T, W), np.float64)
     dq = np.zeros((P, T, R), np.float64)
+    gfb = None
+    if grad_final_bank is not None:
+        gfb = _f64(grad_final_bank)
+        if gfb.shape != (P * S, D):
+            raise ValueError(f"grad_final_bank must be {(P * S, D)}, got {gfb.shape}")
     rc = _load().sdm_oracle_backward(P, T, S, D, W, R, B, ws, _f64(k), _f64(g), _f64(beta),
-                                     _f64(v), rs, _f64(q), valid, _f64(grad_readings), dB, dv,
-                                     db, dk, dg, dq, int(nthreads))
+                                     _f64(v), rs, _f64(q), valid, _f64(grad_readings),
+                                     None if gfb is None else gfb.ctypes.data, dB, dv, db, dk,
+                                     dg, dq, int(nthreads))
     _check(rc, "backward")
     return {"grad_bank": dB, "grad_v": dv, "grad_beta": db, "grad_write_w": dk,
             "grad_log_decay": dg, "grad_read_w": dq, "restored_bank": B}

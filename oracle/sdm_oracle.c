@@ -447,8 +447,9 @@ int sdm_oracle_plan(int n, int width, const int32_t *slots, int32_t *perm, uint8
 static int backward_stream(int T, int S, int D, int W, int R, double *B, const int32_t *ws,
                            const double *k, const double *g, const double *beta,
                            const double *v, const int32_t *rs, const double *q, int valid,
-                           const double *dout, double *dB, double *dv, double *dbeta,
-                           double *dk, double *dg, double *dq, double *a_log, double *tmp) {
+                           const double *dout, const double *dB_final, double *dB, double *dv,
+                           double *dbeta, double *dk, double *dg, double *dq, double *a_log,
+                           double *tmp) {
     double *out = tmp;                    /* [T*D] forward readings (unused) */
     double *a = out + (size_t)T * D;      /* [W*D] */
     double *ret = a + (size_t)W * D;      /* [D] */
@@ -460,7 +461,10 @@ static int backward_stream(int T, int S, int D, int W, int R, double *B, const i
     int rc = sequential_stream(T, S, D, W, R, B, ws, k, g, beta, v, rs, q, valid, out, a, ret,
                                a_log);
     if (rc) return rc;
-    memset(dB, 0, sizeof(double) * (size_t)S * D);
+    if (dB_final)
+        memcpy(dB, dB_final, sizeof(double) * (size_t)S * D);
+    else
+        memset(dB, 0, sizeof(double) * (size_t)S * D);
     memset(dv, 0, sizeof(double) * (size_t)T * D);
     memset(dbeta, 0, sizeof(double) * (size_t)T);
     memset(dk, 0, sizeof(double) * (size_t)T * W);
@@ -532,14 +536,16 @@ static int backward_stream(int T, int S, int D, int W, int R, double *B, const i
 }
 
 /* Forward + reverse over all streams. bank: in = initial bank; out = the initial bank
- * again (the backward restores it exactly). Gradients: dbank [P*S, D], dv [P,T,D],
- * dbeta [P,T], dk [P,T,W], dg [P,T,W], dq [P,T,R]. Memory: T*W*D doubles of logged rows
- * per stream in flight. */
+ * again (the backward restores it exactly). dbank_final (nullable) is the loss gradient with
+ * respect to the final bank (zero when NULL). Gradients: dbank [P*S, D] (with respect to the
+ * initial bank), dv [P,T,D], dbeta [P,T], dk [P,T,W], dg [P,T,W], dq [P,T,R]. Memory:
+ * T*W*D doubles of logged rows per stream in flight. */
 int sdm_oracle_backward(int P, int T, int S, int D, int W, int R, double *bank,
                         const int32_t *ws, const double *k, const double *g, const double *beta,
                         const double *v, const int32_t *rs, const double *q,
-                        const int32_t *valid, const double *dout, double *dbank, double *dv,
-                        double *dbeta, double *dk, double *dg, double *dq, int nthreads) {
+                        const int32_t *valid, const double *dout, const double *dbank_final,
+                        double *dbank, double *dv, double *dbeta, double *dk, double *dg,
+                        double *dq, int nthreads) {
     if (check_sizes(P, T, S, D, W, R)) return ORACLE_EINVAL;
     for (int p = 0; p < P; ++p)
         if (valid[p] < 0 || valid[p] > T) return ORACLE_EINVAL;
@@ -562,7 +568,9 @@ int sdm_oracle_backward(int P, int T, int S, int D, int W, int R, double *bank,
             size_t o = (size_t)p * T;
             rc = backward_stream(T, S, D, W, R, bank + (size_t)p * S * D, ws + o * W, k + o * W,
                                  g + o * W, beta + o, v + o * D, rs + o * R, q + o * R,
-                                 valid[p], dout + o * D, dbank + (size_t)p * S * D, dv + o * D,
+                                 valid[p], dout + o * D,
+                                 dbank_final ? dbank_final + (size_t)p * S * D : NULL,
+                                 dbank + (size_t)p * S * D, dv + o * D,
                                  dbeta + o, dk + o * W, dg + o * W, dq + o * R, a_log, tmp);
         }
         free(a_log);

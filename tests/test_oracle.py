@@ -249,17 +249,21 @@ def test_plan_matches_brute_force_grouping(seed):
 # backward
 # ---------------------------------------------------------------------------------------
 
-def test_backward_finite_differences_and_restore():
+@pytest.mark.parametrize("with_final", [False, True])
+def test_backward_finite_differences_and_restore(with_final):
+    """Loss = <dO, readings> (+ <G, final bank>): every gradient against central
+    differences of the token loop."""
     _, x = rand_case(P=2, T=9, S=5, D=3, W=2, R=2, seed=21, ragged=False)
     x["valid"] = np.array([9, 6], np.int32)
     rng = np.random.default_rng(22)
     dO = rng.standard_normal((2, 9, 3))
-    gr = oracle.backward(*args(x), dO)
+    G = rng.standard_normal((10, 3)) if with_final else None
+    gr = oracle.backward(*args(x), dO, grad_final_bank=G)
     np.testing.assert_array_equal(gr["restored_bank"], x["bank"])
 
     def loss(y):
-        o, _ = oracle.sequential(*args(y))
-        return float((o * dO).sum())
+        o, B = oracle.sequential(*args(y))
+        return float((o * dO).sum()) + (float((B * G).sum()) if with_final else 0.0)
 
     h = 1e-6
     for key, gkey in (("bank", "grad_bank"), ("v", "grad_v"), ("beta", "grad_beta"),

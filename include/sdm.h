@@ -123,6 +123,49 @@ int sdm_write_read(const sdm_shape *shape, void *bank, const int32_t *write_slot
                    const int32_t *valid_tokens, void *readings, void *workspace,
                    size_t workspace_bytes, void *stream);
 
+/* Bytes of the snapshot a saving forward keeps for the backward: the pre-write (chunk
+ * start) row of every written slot of every chunk, Nt * P * C * W rows of D bank-dtype
+ * elements (memory_ops.py: the snapshot of the saving forward, snapshot_quant "none"). */
+size_t sdm_saved_bytes(const sdm_shape *shape);
+
+/* The saving forward (memory_ops.py SDMWriteRead.forward): sdm_write_read plus the snapshot.
+ * saved: device, >= sdm_saved_bytes(shape) bytes, 16-byte aligned, written (positions of
+ * slots that are not written stay untouched). Same results as sdm_write_read. */
+int sdm_write_read_save(const sdm_shape *shape, void *bank, const int32_t *write_slots,
+                        const void *write_w, const float *log_decay, const float *beta,
+                        const void *v, const int32_t *read_slots, const void *read_w,
+                        const int32_t *valid_tokens, void *readings, void *saved,
+                        size_t saved_bytes, void *workspace, size_t workspace_bytes,
+                        void *stream);
+
+/* Bytes of device workspace sdm_write_read_backward needs (0 if refused). */
+size_t sdm_backward_workspace_bytes(const sdm_shape *shape);
+
+/* The backward (memory_ops.py SDMWriteRead.backward: the steps in reverse, the matmuls
+ * through the solve and the Phase-1 backward), after sdm_write_read_save with the same shape
+ * and inputs.
+ *   bank           device [P*S, D]: in, the final bank the saving forward left; out, the
+ *                  initial bank, restored exactly from the snapshot
+ *   inputs         the forward's inputs, unchanged
+ *   saved          the snapshot written by sdm_write_read_save
+ *   grad_readings  device [P, T, D] bank dtype: dL/d(readings) (padding rows are ignored)
+ *   grad_bank      device [P*S, D] float32, in place: in, dL/d(final bank) (zero if the loss
+ *                  does not read the final bank); out, dL/d(initial bank)
+ *   grad_v         device [P, T, D] float32, out
+ *   grad_beta      device [P, T] float32, out
+ *   grad_write_w   device [P, T, W] float32, out   (dL/dk)
+ *   grad_log_decay device [P, T, W] float32, out   (dL/dg)
+ *   grad_read_w    device [P, T, R] float32, out   (dL/dq)
+ * Gradients of padding tokens are zero. Asynchronous; deterministic. */
+int sdm_write_read_backward(const sdm_shape *shape, void *bank, const int32_t *write_slots,
+                            const void *write_w, const float *log_decay, const float *beta,
+                            const void *v, const int32_t *read_slots, const void *read_w,
+                            const int32_t *valid_tokens, const void *saved, size_t saved_bytes,
+                            const void *grad_readings, float *grad_bank, float *grad_v,
+                            float *grad_beta, float *grad_write_w, float *grad_log_decay,
+                            float *grad_read_w, void *workspace, size_t workspace_bytes,
+                            void *stream);
+
 /* Kernel families, in launch order within a slab: Phase 1 and the solve once per slab, then
  * the fused Phase-2 kernel once per slab, or (SDM_FLAG_PER_STEP_KERNELS) gather, dual matmul
  * and DW once per step. */

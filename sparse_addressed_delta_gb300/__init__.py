@@ -19,7 +19,8 @@ from typing import Dict, Optional
 
 import torch
 
-__all__ = ["sdm_write_read", "sdm_write_read_noalloc", "profile_write_read", "workspace_bytes", "launch_count",
+__all__ = ["sdm_write_read", "sdm_write_read_save", "sdm_write_read_backward",
+           "sdm_write_read_noalloc", "profile_write_read", "workspace_bytes", "launch_count",
            "phase1_debug", "KERNEL_KINDS",
            "device_status", "SdmError", "Shape", "library", "library_path", "version"]
 
@@ -73,6 +74,15 @@ def library() -> ctypes.CDLL:
             lib.sdm_launch_count.restype = i64
             lib.sdm_write_read.argtypes = [sp] + [vp] * 10 + [vp, sz, vp]
             lib.sdm_write_read.restype = i32
+            lib.sdm_saved_bytes.argtypes = [sp]
+            lib.sdm_saved_bytes.restype = sz
+            lib.sdm_backward_workspace_bytes.argtypes = [sp]
+            lib.sdm_backward_workspace_bytes.restype = sz
+            lib.sdm_write_read_save.argtypes = [sp] + [vp] * 10 + [vp, sz, vp, sz, vp]
+            lib.sdm_write_read_save.restype = i32
+            lib.sdm_write_read_backward.argtypes = ([sp] + [vp] * 9 + [vp, sz] + [vp] * 7
+                                                    + [vp, sz, vp])
+            lib.sdm_write_read_backward.restype = i32
             lib.sdm_write_read_noalloc.argtypes = [sp] + [vp] * 10 + [vp]
             lib.sdm_write_read_noalloc.restype = i32
             lib.sdm_profile_write_read.argtypes = ([sp] + [vp] * 10 + [vp, sz]
@@ -199,6 +209,85 @@ def sdm_write_read(bank: torch.Tensor, write_slots: torch.Tensor, write_w: torch
             _ptr(readings), _ptr(workspace), workspace.numel(), _stream_ptr(stream))
     _check(rc)
     return readings
+
+
+def _shape_of(bank, write_slots, read_slots, chunk_size, slab_steps=0, flags=0):
+    P, T, W = write_slots.shape
+    R = read_slots.shape[-1]
+    S, D = bank.shape[0] // P, bank.shape[1]
+    return make_shape(P, T, chunk_size, S, D, W, R, bank.dtype, slab_steps, flags), (P, T, S, D, W, R)
+
+
+def saved_bytes(shape: Shape) -> int:
+    n = library().sdm_saved_bytes(ctypes.byref(shape))
+    if n == 0:
+        raise SdmError(-1, library().sdm_last_error().decode())
+    return int(n)
+
+
+def sdm_write_read_save(bank, write_slots, write_w, log_decay, beta, v, read_slots, read_w,
+                        valid_tokens=None, *, chunk_size: int, slab_steps: int = 0,
+                        workspace=None, readings=None, saved=None, stream=None, flags: int = 0):
+    """The saving forward: sdm_write_read plus the snapshot the backward needs.
+    Returns (readings, saved)."""
+    shape, (P, T, S, D, W, R) = _shape_of(bank, write_slots, read_slots, chunk_size,
+                                          slab_steps, flags)
+    dev, dt = bank.device, bank.dtype
+    for t, name, shp, typ in ((bank, "bank", (P * S, D), dt), (write_slots, "write_slots", (P, T, W), torch.int32),
+                              (write_w, "write_w", (P, T, W), dt), (log_decay, "log_decay", (P, T, W), torch.float32),
+                              (beta, "beta", (P, T), torch.float32), (v, "v", (P, T, D), dt),
+                              (read_slots, "read_slots", (P, T, R), torch.int32), (read_w, "read_w", (P, T, R), dt)):
+        _need(t, name, shp, typ, dev)
+    if readings is None:
+        readings = torch.empty((P, T, D), dtype=dt, device=dev)
+    if workspace is None:
+        workspace = alloc_workspace(shape, dev)
+    if saved is None:
+        saved = torch.empty(saved_bytes(shape), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        rc = library().sdm_write_read_save(
+            ctypes.byref(shape), _ptr(bank), _ptr(write_slots), _ptr(write_w), _ptr(log_decay),
+            _ptr(beta), _ptr(v), _ptr(read_slots), _ptr(read_w), _ptr(valid_tokens),
+            _ptr(readings), _ptr(saved), saved.numel(), _ptr(workspace), workspace.numel(),
+            _stream_ptr(stream))
+    _check(rc)
+    return readings, saved
+
+
+def sdm_write_read_backward(bank, write_slots, write_w, log_decay, beta, v, read_slots, read_w,
+                            valid_tokens, saved, grad_readings, *, chunk_size: int,
+                            grad_bank=None, slab_steps: int = 0, workspace=None, stream=None):
+    """The backward after sdm_write_read_save: restores ``bank`` to its initial state and
+    returns a dict of float32 gradients (grad_bank, grad_v, grad_beta, grad_write_w,
+    grad_log_decay, grad_read_w). ``grad_bank`` (optional, [P*S, D] float32) is the loss
+    gradient with respect to the final bank; it is updated in place to the gradient with
+    respect to the initial bank."""
+    shape, (P, T, S, D, W, R) = _shape_of(bank, write_slots, read_slots, chunk_size, slab_steps)
+    dev, dt = bank.device, bank.dtype
+    _need(grad_readings, "grad_readings", (P, T, D), dt, dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    if grad_bank is None:
+        grad_bank = torch.zeros((P * S, D), **f32)
+    _need(grad_bank, "grad_bank", (P * S, D), torch.float32, dev)
+    out = {"grad_bank": grad_bank, "grad_v": torch.empty((P, T, D), **f32),
+           "grad_beta": torch.empty((P, T), **f32), "grad_write_w": torch.empty((P, T, W), **f32),
+           "grad_log_decay": torch.empty((P, T, W), **f32),
+           "grad_read_w": torch.empty((P, T, R), **f32)}
+    if workspace is None:
+        n = library().sdm_backward_workspace_bytes(ctypes.byref(shape))
+        if n == 0:
+            raise SdmError(-1, library().sdm_last_error().decode())
+        workspace = torch.empty(n, dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        rc = library().sdm_write_read_backward(
+            ctypes.byref(shape), _ptr(bank), _ptr(write_slots), _ptr(write_w), _ptr(log_decay),
+            _ptr(beta), _ptr(v), _ptr(read_slots), _ptr(read_w), _ptr(valid_tokens),
+            _ptr(saved), saved.numel(), _ptr(grad_readings), _ptr(out["grad_bank"]),
+            _ptr(out["grad_v"]), _ptr(out["grad_beta"]), _ptr(out["grad_write_w"]),
+            _ptr(out["grad_log_decay"]), _ptr(out["grad_read_w"]), _ptr(workspace),
+            workspace.numel(), _stream_ptr(stream))
+    _check(rc)
+    return out
 
 
 def sdm_write_read_noalloc(bank: torch.Tensor, write_slots: torch.Tensor,

@@ -76,6 +76,7 @@ int check_shape(const sdm_shape *s, Dims &d) {
     d.Nt = (int)Nt;
     d.dtype = s->bank_dtype;
     d.per_step = (s->flags & SDM_FLAG_PER_STEP_KERNELS) ? 1 : 0;
+    d.bwd = 0;
     return SDM_OK;
 }
 
@@ -133,13 +134,40 @@ int phase1_ctas(const Dims &d, int ns) {
     F(kf, float, G * CW)                                                      \
     F(rlo, int32_t, G * CR)                                                   \
     F(rhi, int32_t, G * CR)                                                   \
+    F(wkey, unsigned long long, B * N * CW)                                   \
+    F(wlws, float, B * N * CW)                                                \
+    F(wpgs, int32_t, B * N * CW)                                              \
+    F(wpge, int32_t, B * N * CW)                                              \
+    F(dwt, float, B * N * CW)                                                 \
+    F(rkey, unsigned long long, B * N * CR)                                   \
+    F(rgoff, int32_t, B * N * (CR + 1))                                       \
+    F(rgslot, int32_t, B * N * CR)                                            \
+    F(rng, int32_t, B * N)                                                    \
+    F(rkeys, unsigned long long, B * G * 2 * CR)                              \
+    F(bu, float, B * P * CD)                                                  \
+    F(bup, float, B * P * CD)                                                 \
+    F(bdret, float, B * P * CD)                                               \
+    F(bdo, float, B * P * CD)                                                 \
+    F(bdX, float, B * P * CC)                                                 \
+    F(bdQX, float, B * P * CC)                                                \
+    F(bdQK, float, B * P * CC)                                                \
+    F(bT, float, B * P * CC)                                                  \
+    F(bdA, float, B * P * CC)                                                 \
+    F(bdb2, float, B * P * DT * C)                                            \
+    F(bddw, float, B * P * CW)                                                \
+    F(bdgw, float, B * P * CW)                                                \
+    F(bdqw, float, B * P * CR)                                                \
+    F(bdfac, float, B * P * CW)                                               \
+    F(bdlam, float, B * P * CW)                                               \
+    F(bdlr, float, B * P * CR)                                                \
     F(ret, float, P * CD)                                                     \
     F(inter, float, P * CD)                                                   \
     F(dv, float, P * CD)
 
 size_t layout_bytes(const Dims &d, int ns, int G_) {
     const size_t N = (size_t)ns * d.P, P = d.P, CW = (size_t)d.C * d.W, CR = (size_t)d.C * d.R,
-                 CC = (size_t)d.C * d.C, CD = (size_t)d.C * d.D, G = G_;
+                 CC = (size_t)d.C * d.C, CD = (size_t)d.C * d.D, G = G_, B = d.bwd ? 1 : 0,
+                 C = d.C, DT = ((size_t)d.D + 31) / 32;
     size_t off = 0;
 #define X_SIZE(name, type, count) off += up(sizeof(type) * (size_t)(count));
     SDM_LAYOUT(X_SIZE)
@@ -149,7 +177,8 @@ size_t layout_bytes(const Dims &d, int ns, int G_) {
 
 Work layout_assign(const Dims &d, int ns, int G_, void *base) {
     const size_t N = (size_t)ns * d.P, P = d.P, CW = (size_t)d.C * d.W, CR = (size_t)d.C * d.R,
-                 CC = (size_t)d.C * d.C, CD = (size_t)d.C * d.D, G = G_;
+                 CC = (size_t)d.C * d.C, CD = (size_t)d.C * d.D, G = G_, B = d.bwd ? 1 : 0,
+                 C = d.C, DT = ((size_t)d.D + 31) / 32;
     Work w;
     memset(&w, 0, sizeof(w));
     char *p = static_cast<char *>(base);
@@ -172,9 +201,10 @@ struct Prepared {
     size_t bytes;
 };
 
-int prepare(const sdm_shape *shape, Prepared &pr) {
+int prepare(const sdm_shape *shape, Prepared &pr, int bwd = 0) {
     int rc = check_shape(shape, pr.d);
     if (rc) return rc;
+    pr.d.bwd = bwd;
     pr.ns = slab_steps(pr.d, shape->slab_steps);
     pr.G = phase1_ctas(pr.d, pr.ns);
     pr.bytes = layout_bytes(pr.d, pr.ns, pr.G);
@@ -282,7 +312,7 @@ int sdm_write_read(const sdm_shape *shape, void *bank, const int32_t *write_slot
     int rc = prepare(shape, pr);
     if (rc) return rc;
     Inputs in{bank, write_slots, write_w, log_decay, beta, v, read_slots, read_w, valid_tokens,
-              readings};
+              readings, nullptr};
     if ((rc = check_inputs(in, true))) return rc;
     if ((rc = check_workspace(pr, workspace, workspace_bytes))) return rc;
     g_err[0] = 0;
@@ -299,7 +329,7 @@ int sdm_profile_write_read(const sdm_shape *shape, void *bank, const int32_t *wr
     int rc = prepare(shape, pr);
     if (rc) return rc;
     Inputs in{bank, write_slots, write_w, log_decay, beta, v, read_slots, read_w, valid_tokens,
-              readings};
+              readings, nullptr};
     if ((rc = check_inputs(in, true))) return rc;
     if ((rc = check_workspace(pr, workspace, workspace_bytes))) return rc;
     if (!kernel_ms || !launches) return fail(SDM_ERR_INVALID, "kernel_ms and launches must not be NULL");
@@ -323,6 +353,84 @@ int sdm_profile_write_read(const sdm_shape *shape, void *bank, const int32_t *wr
     return rc;
 }
 
+size_t sdm_saved_bytes(const sdm_shape *shape) {
+    Dims d;
+    if (check_shape(shape, d)) return 0;
+    g_err[0] = 0;
+    const size_t es = d.dtype == SDM_BF16 ? 2 : 4;
+    return (size_t)d.Nt * d.P * d.C * d.W * d.D * es;
+}
+
+int sdm_write_read_save(const sdm_shape *shape, void *bank, const int32_t *write_slots,
+                        const void *write_w, const float *log_decay, const float *beta,
+                        const void *v, const int32_t *read_slots, const void *read_w,
+                        const int32_t *valid_tokens, void *readings, void *saved,
+                        size_t saved_bytes, void *workspace, size_t workspace_bytes,
+                        void *stream) {
+    Prepared pr;
+    int rc = prepare(shape, pr);
+    if (rc) return rc;
+    Inputs in{bank, write_slots, write_w, log_decay, beta, v, read_slots, read_w, valid_tokens,
+              readings, saved};
+    if ((rc = check_inputs(in, true))) return rc;
+    if ((rc = check_workspace(pr, workspace, workspace_bytes))) return rc;
+    const size_t need = sdm_saved_bytes(shape);
+    if (!saved || saved_bytes < need || reinterpret_cast<uintptr_t>(saved) % 16)
+        return fail(SDM_ERR_WORKSPACE, "saved buffer must hold %zu bytes, 16-byte aligned", need);
+    g_err[0] = 0;
+    return run_forward(pr, in, workspace, static_cast<cudaStream_t>(stream), nullptr);
+}
+
+size_t sdm_backward_workspace_bytes(const sdm_shape *shape) {
+    Prepared pr;
+    if (prepare(shape, pr, 1)) return 0;
+    g_err[0] = 0;
+    return pr.bytes;
+}
+
+int sdm_write_read_backward(const sdm_shape *shape, void *bank, const int32_t *write_slots,
+                            const void *write_w, const float *log_decay, const float *beta,
+                            const void *v, const int32_t *read_slots, const void *read_w,
+                            const int32_t *valid_tokens, const void *saved, size_t saved_bytes,
+                            const void *grad_readings, float *grad_bank, float *grad_v,
+                            float *grad_beta, float *grad_write_w, float *grad_log_decay,
+                            float *grad_read_w, void *workspace, size_t workspace_bytes,
+                            void *stream) {
+    Prepared pr;
+    int rc = prepare(shape, pr, 1);
+    if (rc) return rc;
+    Inputs in{bank, write_slots, write_w, log_decay, beta, v, read_slots, read_w, valid_tokens,
+              const_cast<void *>(grad_readings), const_cast<void *>(saved)};
+    if ((rc = check_inputs(in, true))) return rc;
+    if ((rc = check_workspace(pr, workspace, workspace_bytes))) return rc;
+    const size_t need = sdm_saved_bytes(shape);
+    if (!saved || saved_bytes < need || reinterpret_cast<uintptr_t>(saved) % 16)
+        return fail(SDM_ERR_WORKSPACE, "saved buffer must hold %zu bytes, 16-byte aligned", need);
+    if (!grad_bank || !grad_v || !grad_beta || !grad_write_w || !grad_log_decay || !grad_read_w)
+        return fail(SDM_ERR_INVALID, "gradient output pointers must not be NULL");
+    if (reinterpret_cast<uintptr_t>(grad_bank) % 16)
+        return fail(SDM_ERR_INVALID, "grad_bank must be 16-byte aligned");
+    g_err[0] = 0;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const Dims &d = pr.d;
+    Work w = layout_assign(d, pr.ns, pr.G, workspace);
+    BwdOut o{grad_readings, grad_bank, grad_v, grad_beta, grad_write_w, grad_log_decay,
+             grad_read_w};
+    cudaError_t e = cudaMemsetAsync(w.status, 0, sizeof(DevStatus), st);
+    if (e != cudaSuccess) return cuda_fail(e, "status clear");
+    const int nslabs = (d.Nt + pr.ns - 1) / pr.ns;
+    for (int sl = nslabs - 1; sl >= 0; --sl) {
+        const int s0 = sl * pr.ns;
+        const int nsteps = (d.Nt - s0) < pr.ns ? (d.Nt - s0) : pr.ns;
+        if ((e = launch_phase1(d, in, w, s0, nsteps, st)) != cudaSuccess) return cuda_fail(e, "phase1");
+        if ((e = launch_solve(d, in, w, s0, nsteps, st)) != cudaSuccess) return cuda_fail(e, "solve");
+        for (int ti = s0 + nsteps - 1; ti >= s0; --ti)
+            if ((e = launch_backward_step(d, in, w, o, s0, ti, st)) != cudaSuccess)
+                return cuda_fail(e, "backward step");
+    }
+    return SDM_OK;
+}
+
 int sdm_phase1_debug(const sdm_shape *shape, const int32_t *write_slots, const void *write_w,
                      const float *log_decay, const float *beta, const int32_t *read_slots,
                      const void *read_w, const int32_t *valid_tokens, int32_t *perm,
@@ -333,7 +441,7 @@ int sdm_phase1_debug(const sdm_shape *shape, const int32_t *write_slots, const v
     int rc = prepare(shape, pr);
     if (rc) return rc;
     Inputs in{nullptr, write_slots, write_w, log_decay, beta, nullptr, read_slots, read_w,
-              valid_tokens, nullptr};
+              valid_tokens, nullptr, nullptr};
     if ((rc = check_inputs(in, false))) return rc;
     if ((rc = check_workspace(pr, workspace, workspace_bytes))) return rc;
     if ((perm != nullptr) != (group_start != nullptr) || (perm != nullptr) != (owner != nullptr) ||

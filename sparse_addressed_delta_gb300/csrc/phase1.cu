@@ -334,8 +334,10 @@ __global__ void __launch_bounds__(NT) k_phase1(Dims d, Inputs in, Work w, int st
             const int e = ent_of((unsigned)srt[pos]);
             const float kk = kf[e];
             const float l = lws[pos];
-            wdw[pos] = kk * expf(lend[pgid[pos]] - l);
+            const float dwv = kk * expf(lend[pgid[pos]] - l);
+            wdw[pos] = dwv;
             gw[e] = kk * expf(l);
+            if (d.bwd) w.dwt[(size_t)n * CW + e] = dwv;
         }
         const unsigned magR = div_magic(R);
         for (int er = tid; er < nr; er += NT) {
@@ -408,6 +410,52 @@ __global__ void __launch_bounds__(NT) k_phase1(Dims d, Inputs in, Work w, int st
         }
         // tails of the per-entry rows past the valid entries (read by nothing but the debug
         // copy; written so that every output element is defined)
+        if (d.bwd) {
+            // 5. what the backward reads back: the sorted write row with its running log-decays
+            //    and group bounds, and the read kind row sorted by (slot, t, i) with its groups
+            for (int pos = tid; pos < nw; pos += NT) {
+                const size_t o = (size_t)n * CW + pos;
+                w.wkey[o] = srt[pos];
+                w.wlws[o] = lws[pos];
+                w.wpgs[o] = pgs[pos];
+                w.wpge[o] = goff[pgid[pos] + 1];
+            }
+            unsigned long long *rA = w.rkeys + (size_t)blockIdx.x * 2 * CR;
+            unsigned long long *rB = rA + CR;
+            int rbad = 0;
+            for (int i = tid; i < nr; i += NT) {
+                int sl = rs[i];
+                if ((unsigned)sl >= (unsigned)S) { sl = S; rbad = 1; }
+                const int t = div_by(i, magR);
+                rA[i] = ((unsigned long long)(unsigned)sl << 32) | ((unsigned)t << 8) |
+                        (unsigned)(i - t * R);
+            }
+            const int rpass = __syncthreads_or(rbad) ? (32 - __clz(S) + 7) / 8 : passes;
+            unsigned long long *rsrc = rA, *rdst = rB;
+            for (int ps = 0; ps < rpass; ++ps) {
+                radix_pass(rsrc, rdst, nr, 32 + 8 * ps, sm);
+                unsigned long long *tt = rsrc; rsrc = rdst; rdst = tt;
+            }
+            int32_t *rgoff = w.rgoff + (size_t)n * (CR + 1);
+            int32_t *rgslot = w.rgslot + (size_t)n * CR;
+            int rcarry = 0;
+            for (int tile = 0; tile < nr; tile += NT) {
+                const int pos = tile + tid;
+                const bool ok = pos < nr;
+                const unsigned long long key = ok ? rsrc[pos] : 0ull;
+                const int sl = (int)(key >> 32);
+                const bool head = ok && (pos == 0 || (int)(rsrc[pos - 1] >> 32) != sl);
+                int ci;
+                const int gid = int_scan(head ? 1 : 0, rcarry, ci, sm) - 1;
+                rcarry = ci;
+                if (ok) {
+                    w.rkey[(size_t)n * CR + pos] = key;
+                    if (head) { rgoff[gid] = pos; rgslot[gid] = sl; }
+                }
+            }
+            if (tid == 0) { w.rng[n] = rcarry; rgoff[rcarry] = nr; }
+            __syncthreads();
+        }
         for (int i = nw + tid; i < CW; i += NT) { perm[i] = -1; gw[i] = 0.f; lw[i] = 0.f; wdw[i] = 0.f; }
         for (int i = nr + tid; i < CR; i += NT) { qw[i] = 0.f; lr[i] = 0.f; }
         __syncthreads();

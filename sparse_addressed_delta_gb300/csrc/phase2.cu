@@ -240,6 +240,10 @@ __global__ void __launch_bounds__(kBlock) k_dw(Dims d, Inputs in, Work w, int st
         const float f = gfac[g];
         float acc[CPL];
         load_vec<BT, CPL, false>(row, acc);
+        if (in.snap)
+            store_vec<BT, CPL>(static_cast<BT *>(in.snap) +
+                                   ((size_t)(ti * d.P + p) * CW + (o1 - 1)) * D + lane * CPL,
+                               acc);
 #pragma unroll
         for (int c = 0; c < CPL; ++c) acc[c] *= f;
         int m = o0;

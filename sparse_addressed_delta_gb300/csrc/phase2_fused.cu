@@ -228,6 +228,9 @@ __global__ void __launch_bounds__(NT) k_phase2_fused(Dims d, Inputs in, Work w, 
             BT *row = bank + (size_t)gslot[g] * D;
             float acc[V];
             load_vec<BT, V, false>(row, acc);
+            if (in.snap)
+                store_vec<BT, V>(static_cast<BT *>(in.snap) +
+                                     ((size_t)(ti * d.P + p) * CW + (o1 - 1)) * D + c0, acc);
             const float f = gfac[g];
 #pragma unroll
             for (int c = 0; c < V; ++c) acc[c] *= f;
@@ -648,7 +651,11 @@ __global__ void __launch_bounds__(NT2) k_phase2_pipe(Dims d, Inputs in, Work w, 
             }
             if ((info >> 17) & 1) {
                 float b0[V], o[V];
-                piece_to_f32<BT>(b0s[t * W + ((info >> 8) & 255)], b0);
+                const uint4 braw = b0s[t * W + ((info >> 8) & 255)];
+                piece_to_f32<BT>(braw, b0);
+                if (in.snap)
+                    *reinterpret_cast<uint4 *>(static_cast<BT *>(in.snap) +
+                                               ((size_t)(ti * d.P + p) * CW + m) * D + c0) = braw;
                 const float fac = smfac[m];
 #pragma unroll
                 for (int c = 0; c < V; ++c) o[c] = fmaf(fac, b0[c], run[c]);

@@ -33,6 +33,7 @@ struct Dims {
     int P, T, C, S, D, W, R, Nt;
     int dtype;   // SDM_F32 / SDM_BF16
     int per_step;   // 1: Phase 2 as three kernels per step; 0: one fused kernel per slab
+    int bwd;        // 1: Phase 1 also keeps what the backward reads (sorted rows, read plan)
 };
 
 // Device pointers of one slab's workspace. N = ns * P chunks; chunk n of the slab is step
@@ -65,6 +66,34 @@ struct Work {
     float *kf;          // [G][CW]  write weight of each entry as float (0 for a bad slot)
     int32_t *rlo;       // [G][CR]  first write position of the read's slot group
     int32_t *rhi;       // [G][CR]  last write position at or before the read's token (-1: none)
+    // kept for the backward (sized only when Dims::bwd)
+    unsigned long long *wkey;   // [N][CW]  sorted write keys (slot << 32 | t << 8 | j)
+    float *wlws;        // [N][CW]   running log-decay at each sorted position
+    int32_t *wpgs;      // [N][CW]   group start of each sorted position
+    int32_t *wpge;      // [N][CW]   group end (exclusive) of each sorted position
+    float *dwt;         // [N][CW]   token-major DW weights
+    unsigned long long *rkey;   // [N][CR]  sorted read keys (slot << 32 | t << 8 | i)
+    int32_t *rgoff;     // [N][CR+1] read group starts, rgoff[rng] = n_reads
+    int32_t *rgslot;    // [N][CR]   slot of each read group
+    int32_t *rng;       // [N]       read groups
+    unsigned long long *rkeys;  // [G][2][CR] read sort scratch
+    // backward step buffers (sized only when Dims::bwd)
+    float *bu;          // [P][C*D]  delta_v recomputed
+    float *bup;         // [P][C*D]  u_pre recomputed
+    float *bdret;       // [P][C*D]  gradient of retrieved
+    float *bdo;         // [P][C*D]  upstream readings gradient, zero past the valid tokens
+    float *bdX;         // [P][C*C]  dX, then dX + QK^T dQX
+    float *bdQX;        // [P][C*C]
+    float *bdQK;        // [P][C*C]
+    float *bT;          // [P][C*C]  X^T (dX + QK^T dQX)
+    float *bdA;         // [P][C*C]  dL, then beta * dL (strictly lower)
+    float *bdb2;        // [P][DT][C] per-column-tile partial <du_pre, v - retrieved>
+    float *bddw;        // [P][CW]   <dB1[s], u_t> per write entry (token-major)
+    float *bdgw;        // [P][CW]   <dretrieved_t, B0[s]> per write entry
+    float *bdqw;        // [P][CR]   <dO_t, B0[r]> per read entry
+    float *bdfac;       // [P][CW]   <dB1[s], B0[s]> at each group's head position
+    float *bdlam;       // [P][CW]   d(log-decay running sum) at each sorted write position
+    float *bdlr;        // [P][CR]   d(read running log-decay) at each sorted read position
     // Phase-2 step buffers
     float *ret;         // [P][C*D]
     float *inter;       // [P][C*D]
@@ -84,10 +113,23 @@ struct Inputs {
     const void *qw;
     const int32_t *valid;   // may be null
     void *readings;
+    void *snap;             // saving forward: [Nt*P][C*W][D] bank dtype, B0 rows of the written
+                            // slots at their group's tail position; null otherwise
 };
 
 // Sets the thread's sdm_last_error() message; returns code.
 int set_error(int code, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
+
+// Outputs of the backward (all float32 except grad_readings, which is in the bank dtype).
+struct BwdOut {
+    const void *grad_readings;   // [P, T, D] upstream gradient of the readings
+    float *grad_bank;            // [P*S, D] in: d/d(final bank); out: d/d(initial bank)
+    float *grad_v;               // [P, T, D]
+    float *grad_beta;            // [P, T]
+    float *grad_write_w;         // [P, T, W]
+    float *grad_log_decay;       // [P, T, W]
+    float *grad_read_w;          // [P, T, R]
+};
 
 // ---------------------------------------------------------------------------------------
 // host-side layout (api.cu)
@@ -112,6 +154,8 @@ cudaError_t launch_dw(const Dims &d, const Inputs &in, const Work &w, int step0,
 cudaError_t launch_phase2_fused(const Dims &d, const Inputs &in, const Work &w, int step0,
                                 int nsteps, cudaStream_t st);
 size_t phase2_fused_smem(const Dims &d);
+cudaError_t launch_backward_step(const Dims &d, const Inputs &in, const Work &w,
+                                 const BwdOut &o, int step0, int ti, cudaStream_t st);
 cudaError_t launch_debug_expand(const Dims &d, const Work &w, int nchunks, int32_t *perm,
                                 uint8_t *gstart, uint8_t *owner, float *dw_tok,
                                 cudaStream_t st);

@@ -72,7 +72,10 @@ class Err:
 
     def add(self, gpu: np.ndarray, ref: np.ndarray):
         if ref.size:
-            self.num = max(self.num, float(np.abs(gpu - ref).max()))
+            if not np.all(np.isfinite(gpu)):
+                self.num = float("inf")          # a NaN or inf result is never within tolerance
+            else:
+                self.num = max(self.num, float(np.abs(gpu - ref).max()))
             self.den = max(self.den, float(np.abs(ref).max()))
 
     @property

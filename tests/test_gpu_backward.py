@@ -1,0 +1,174 @@
+"""Parity of the CUDA backward (through the C ABI) with the oracle's reverse-mode token loop.
+
+Per gradient tensor the error is max |gpu - oracle| / max |oracle|, bounded by 1e-4 for
+float32 banks (the forward's float32 tolerance, applied to every gradient); the bank must be
+restored to its initial state bit for bit.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sdm_inputs as si
+import sparse_addressed_delta_gb300 as sdm
+from sdm_case import Err, f64, small_workload, stored_tensor, to_device
+
+pytestmark = pytest.mark.gpu
+
+GRADS = ("grad_bank", "grad_v", "grad_beta", "grad_write_w", "grad_log_decay", "grad_read_w")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    sdm.library()
+
+
+def gpu_backward(wl, inputs, grad_readings, grad_final=None, slab_steps=0, flags=0):
+    dev = to_device(inputs, wl)
+    bank = dev["bank"].clone()
+    args = (dev["write_slots"], dev["write_w"], dev["log_decay"], dev["beta"], dev["v"],
+            dev["read_slots"], dev["read_w"], dev["valid"])
+    readings, saved = sdm.sdm_write_read_save(bank, *args, chunk_size=wl.C,
+                                              slab_steps=slab_steps, flags=flags)
+    gr = stored_tensor(grad_readings, wl.dtype, "cuda")
+    gb = None if grad_final is None else torch.from_numpy(
+        np.ascontiguousarray(grad_final, dtype=np.float32)).cuda()
+    out = sdm.sdm_write_read_backward(bank, *args, saved, gr, chunk_size=wl.C, grad_bank=gb,
+                                      slab_steps=slab_steps)
+    torch.cuda.synchronize()
+    return readings, bank, dev["bank"], out
+
+
+def oracle_backward(wl, inputs, grad_readings, grad_final=None, streams_per_call=None,
+                    nthreads=4):
+    """Oracle gradients, a group of streams at a time; returns {name: fp64 array}."""
+    P, S = wl.P, wl.S
+    spc = streams_per_call or P
+    res = {k: [] for k in GRADS}
+    for lo in range(0, P, spc):
+        hi = min(P, lo + spc)
+        sub = {k: inputs[k][lo:hi] for k in ("write_slots", "write_w", "log_decay", "beta", "v",
+                                             "read_slots", "read_w", "valid")}
+        sub["bank"] = inputs["bank"][lo * S:hi * S]
+        x = oracle.from_stored(sub, wl.dtype)
+        g = si.stored_to_f64(grad_readings[lo:hi], wl.dtype)
+        gf = None if grad_final is None else grad_final[lo * S:hi * S]
+        r = oracle.backward(x["bank"], x["ws"], x["k"], x["g"], x["beta"], x["v"], x["rs"],
+                            x["q"], x["valid"], g, nthreads=nthreads, grad_final_bank=gf)
+        for k in GRADS:
+            res[k].append(r[k])
+    return {k: np.concatenate(v, axis=0) for k, v in res.items()}
+
+
+def errors(out, ref):
+    errs = {}
+    for k in GRADS:
+        e = Err()
+        e.add(f64(out[k]), ref[k])
+        errs[k] = e.value
+    return errs
+
+
+def make_case(wl, with_final=False, seed=100):
+    inputs = si.generate(wl)
+    rng = np.random.default_rng(seed)
+    gr = rng.standard_normal((wl.P, wl.T, wl.D))
+    pad = np.arange(wl.T)[None, :] >= inputs["valid"][:, None]
+    gr[pad] = 0.0
+    grad_readings = si.to_stored(gr, wl.dtype)
+    grad_final = rng.standard_normal((wl.P * wl.S, wl.D)).astype(np.float32) if with_final else None
+    return inputs, grad_readings, grad_final
+
+
+def check(wl, with_final=False, tol=1e-4, slab_steps=0, flags=0):
+    inputs, gr, gf = make_case(wl, with_final)
+    _, bank, bank0, out = gpu_backward(wl, inputs, gr, gf, slab_steps, flags)
+    assert torch.equal(bank, bank0), "bank not restored exactly"
+    ref = oracle_backward(wl, inputs, gr, gf)
+    errs = errors(out, ref)
+    bad = {k: v for k, v in errs.items() if not v <= tol}
+    assert not bad, (wl.name, errs)
+    return errs
+
+
+@pytest.mark.parametrize("with_final", [False, True])
+def test_backward_dense_collisions(with_final):
+    check(small_workload(P=2, T=70, C=16, S=20, D=32, W=4, R=3, ragged=True, seed=31),
+          with_final=with_final)
+
+
+@pytest.mark.parametrize("C,D,W,R,S", [(16, 64, 1, 1, 8), (32, 64, 8, 5, 64), (64, 128, 16, 16, 500),
+                                       (48, 32, 6, 7, 40), (128, 128, 64, 64, 4096)])
+def test_backward_shapes(C, D, W, R, S):
+    check(small_workload(P=3, T=2 * C + 9, C=C, S=S, D=D, W=W, R=R, ragged=True,
+                         seed=C + W))
+
+
+def test_backward_uniform_slots_fp32():
+    check(small_workload(P=2, T=200, C=64, S=10000, D=128, W=32, R=32, slots="uniform",
+                         ragged=False, seed=33))
+
+
+@pytest.mark.parametrize("flags", [0, sdm.FLAG_PER_STEP_KERNELS])
+def test_backward_slabs_and_paths(flags):
+    """The snapshot written by either Phase-2 path, and slabs of one step."""
+    check(small_workload(P=2, T=100, C=16, S=30, D=64, W=4, R=4, seed=34), slab_steps=2,
+          flags=flags)
+
+
+def test_backward_deterministic():
+    wl = small_workload(P=2, T=130, C=32, S=50, D=64, W=8, R=8, seed=35)
+    inputs, gr, gf = make_case(wl, True)
+    _, _, _, o1 = gpu_backward(wl, inputs, gr, gf)
+    _, _, _, o2 = gpu_backward(wl, inputs, gr, gf)
+    for k in GRADS:
+        assert torch.equal(o1[k], o2[k]), k
+
+
+def test_backward_bf16_bank():
+    """bfloat16 bank: gradients within the bf16 forward tolerance."""
+    errs = check(small_workload(P=2, T=100, C=32, S=60, D=64, W=8, R=8, dtype="bf16", seed=36),
+                 tol=5e-2)
+    print(errs)
+
+
+def test_backward_full_size_workload3():
+    """P=16, T=4096, C=128, S=131072 x 128 fp32, W=R=64 uniform: every gradient within
+    1e-4 of the oracle and the bank restored exactly."""
+    wl = si.WORKLOADS[3]
+    inputs = si.generate(wl)
+    gr = inputs["grad_readings"]
+    _, bank, bank0, out = gpu_backward(wl, inputs, gr)
+    assert torch.equal(bank, bank0), "bank not restored exactly"
+    ref = oracle_backward(wl, inputs, gr, streams_per_call=8, nthreads=8)
+    errs = errors(out, ref)
+    print(f"{wl.name}: " + ", ".join(f"{k} {v:.2e}" for k, v in errs.items()))
+    assert all(v <= 1e-4 for v in errs.values()), errs
+
+
+def test_backward_workspace_poison():
+    """The backward reads no workspace byte it has not written: NaN-filled and zero-filled
+    workspaces give the same gradients, bit for bit."""
+    wl = small_workload(P=2, T=75, C=32, S=40, D=64, W=8, R=8, ragged=True, seed=37)
+    inputs, gr, gf = make_case(wl, True)
+    shape = sdm.make_shape(wl.P, wl.T, wl.C, wl.S, wl.D, wl.W, wl.R, torch.float32)
+    n = sdm.library().sdm_backward_workspace_bytes(__import__("ctypes").byref(shape))
+    results = []
+    for fill in (0x00, 0xFF):
+        dev = to_device(inputs, wl)
+        bank = dev["bank"].clone()
+        args = (dev["write_slots"], dev["write_w"], dev["log_decay"], dev["beta"], dev["v"],
+                dev["read_slots"], dev["read_w"], dev["valid"])
+        _, saved = sdm.sdm_write_read_save(bank, *args, chunk_size=wl.C)
+        ws = torch.full((n,), fill, dtype=torch.uint8, device="cuda")
+        out = sdm.sdm_write_read_backward(
+            bank, *args, saved, stored_tensor(gr, wl.dtype, "cuda"), chunk_size=wl.C,
+            grad_bank=torch.from_numpy(gf).cuda(), workspace=ws)
+        torch.cuda.synchronize()
+        results.append(out)
+    for k in GRADS:
+        assert torch.isfinite(results[1][k]).all(), k
+        assert torch.equal(results[0][k], results[1][k]), k

@@ -206,3 +206,21 @@ def test_full_size_workloads(cfg):
     tol = TOL[wl.dtype]
     print(f"{wl.name}: readings err {er:.3e}, bank err {eb:.3e} (tol {tol})")
     assert er <= tol and eb <= tol
+
+
+@pytest.mark.parametrize("flags", PATHS)
+@pytest.mark.parametrize("C,W", [(16, 4), (128, 64)])
+def test_workspace_poison(flags, C, W):
+    """Every workspace byte the call reads it has written first: a NaN-filled workspace gives
+    the same bits as a zero-filled one."""
+    wl = small_workload(P=3, T=3 * C + 5, C=C, S=300, D=64, W=W, R=W, dtype="bf16", seed=C)
+    dev = to_device(si.generate(wl), wl)
+    shape = sdm.make_shape(wl.P, wl.T, wl.C, wl.S, wl.D, wl.W, wl.R, torch.bfloat16, 0, flags)
+    n = sdm.workspace_bytes(shape)
+    outs = []
+    for fill in (0x00, 0xFF):
+        ws = torch.full((n,), fill, dtype=torch.uint8, device="cuda")
+        r, b, _ = run_gpu(wl, dev, workspace=ws, flags=flags)
+        outs.append((r, b))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    assert torch.isfinite(outs[1][0].float()).all()

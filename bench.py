@@ -51,6 +51,8 @@ def parse_args():
     ap.add_argument("--profile-steps", type=int, default=3)
     ap.add_argument("--per-step-kernels", action="store_true",
                     help="run Phase 2 as three kernels per step instead of the fused kernel")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the saving forward + backward (one step = both calls) instead")
     ap.add_argument("--ncu-run", type=int, default=0, metavar="K",
                     help="profiling target: run K plain (eager) calls on the workload and exit, "
                          "printing no benchmark line")
@@ -411,6 +413,101 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_backward(args):
+    """Saving forward + backward on one GPU: one step = sdm_write_read_save then
+    sdm_write_read_backward (with a zero upstream gradient on the final bank), captured in one
+    CUDA graph; the bank is reset and L2 flushed before each step outside the events."""
+    import torch
+
+    import sparse_addressed_delta_gb300 as sdm
+
+    wl = si.WORKLOADS[args.workload]
+    inputs = si.generate(wl)
+    dev = torch.device("cuda", 0)
+    dt = torch.float32 if wl.dtype == "f32" else torch.bfloat16
+
+    def tens(name):
+        t = torch.from_numpy(np.ascontiguousarray(inputs[name]))
+        if wl.dtype == "bf16" and inputs[name].dtype == np.uint16:
+            t = t.view(torch.bfloat16)
+        return t.to(dev)
+
+    d = {k: tens(k) for k in inputs}
+    if "grad_readings" not in d:
+        d["grad_readings"] = torch.randn((wl.P, wl.T, wl.D), device=dev).to(dt)
+    bank0 = d["bank"]
+    bank = bank0.clone()
+    shape = sdm.make_shape(wl.P, wl.T, wl.C, wl.S, wl.D, wl.W, wl.R, dt)
+    ws = sdm.alloc_workspace(shape, dev)
+    nb = sdm.library().sdm_backward_workspace_bytes(__import__("ctypes").byref(shape))
+    wsb = torch.empty(nb, dtype=torch.uint8, device=dev)
+    saved = torch.empty(sdm.saved_bytes(shape), dtype=torch.uint8, device=dev)
+    readings = torch.empty((wl.P, wl.T, wl.D), dtype=dt, device=dev)
+    gbank = torch.zeros((wl.P * wl.S, wl.D), dtype=torch.float32, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    tokens = int(inputs["valid"].sum())
+    args_in = (d["write_slots"], d["write_w"], d["log_decay"], d["beta"], d["v"],
+               d["read_slots"], d["read_w"], d["valid"])
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        sdm.sdm_write_read_save(bank, *args_in, chunk_size=wl.C, workspace=ws, readings=readings,
+                                saved=saved, stream=stream)
+        gbank.zero_()
+        sdm.sdm_write_read_backward(bank, *args_in, saved, d["grad_readings"], chunk_size=wl.C,
+                                    grad_bank=gbank, workspace=wsb, stream=stream)
+    stream.synchronize()
+    if not torch.equal(bank, bank0):
+        raise RuntimeError("backward did not restore the bank")
+    def fwd():
+        sdm.sdm_write_read_save(bank, *args_in, chunk_size=wl.C, workspace=ws, readings=readings,
+                                saved=saved, stream=stream)
+
+    def bwd():
+        gbank.zero_()
+        sdm.sdm_write_read_backward(bank, *args_in, saved, d["grad_readings"], chunk_size=wl.C,
+                                    grad_bank=gbank, workspace=wsb, stream=stream)
+
+    gf, gb = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gf, stream=stream):
+        fwd()
+    with torch.cuda.graph(gb, stream=stream):
+        bwd()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            bank.copy_(bank0)
+            flush.zero_()
+            gf.replay()
+            gb.replay()
+    stream.synchronize()
+    clocks = ClockSampler(0)
+    with torch.cuda.stream(stream):
+        for k in range(args.steps):
+            bank.copy_(bank0)
+            flush.zero_()
+            ev[k][0].record(stream)
+            gf.replay()
+            ev[k][1].record(stream)
+            gb.replay()
+            ev[k][2].record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if not torch.equal(bank, bank0):
+        raise RuntimeError("backward did not restore the bank")
+    fwd_ms = statistics.mean(a.elapsed_time(b) for a, b, _ in ev)
+    bwd_ms = statistics.mean(b.elapsed_time(c) for _, b, c in ev)
+    ms = fwd_ms + bwd_ms
+    line = {"metric": "SDM forward+backward tokens/s on 1 GB300", "value": tokens / (ms / 1e3),
+            "unit": UNIT, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "storage_dtype": wl.dtype, "data": "synthetic",
+            "config": workload_config(wl, inputs),
+            "split_ms": {"saving_forward": fwd_ms, "backward": bwd_ms},
+            "saved_bytes": saved.numel(), "backward_workspace_bytes": nb, "clocks": clk,
+            "gpu": torch.cuda.get_device_name(dev)}
+    print(json.dumps(line), flush=True)
+
+
 def run_for_profiler(args):
     """K eager sdm_write_read calls on the workload, for an external profiler (ncu)."""
     import torch
@@ -442,6 +539,9 @@ def main():
     args = parse_args()
     if args.ncu_run:
         run_for_profiler(args)
+        return
+    if args.backward:
+        run_backward(args)
         return
     if args.impl == "reference":
         run_reference(args)

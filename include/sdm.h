@@ -67,11 +67,13 @@ typedef enum { SDM_F32 = 0, SDM_BF16 = 1 } sdm_dtype;
  *   flags       0, or SDM_FLAG_PER_STEP_KERNELS
  * P * ceil(T / C) * C must be below 2^31.
  *
- * Phase 2 runs by default as one persistent kernel per slab in which each CTA owns one
- * stream and one 16-byte slice of bank columns for all the slab's steps (the forward acts on
- * every column independently once Phase 1 and the solve are done). SDM_FLAG_PER_STEP_KERNELS
- * runs it instead as three kernels per step (gather, dual matmul, DW over all streams), as
- * the pages lay it out. Both are deterministic; their results differ only by rounding. */
+ * Phase 2 runs as one persistent kernel per slab in which each CTA owns one stream and one
+ * 16-byte slice of bank columns for all the slab's steps (the forward acts on every column
+ * independently once Phase 1 and the solve are done), when two steps of its per-chunk
+ * metadata fit in shared memory (about C * (W + R) <= 4K entries); otherwise, or with
+ * SDM_FLAG_PER_STEP_KERNELS, as three kernels per step (gather, dual matmul, DW over all
+ * streams), as the pages lay it out. Both are deterministic; their results differ only by
+ * rounding. */
 #define SDM_FLAG_PER_STEP_KERNELS 1
 typedef struct {
     int32_t P, T, C, S, D, W, R;

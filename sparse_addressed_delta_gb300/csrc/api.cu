@@ -75,8 +75,8 @@ int check_shape(const sdm_shape *s, Dims &d) {
     d.P = s->P; d.T = s->T; d.C = s->C; d.S = s->S; d.D = s->D; d.W = s->W; d.R = s->R;
     d.Nt = (int)Nt;
     d.dtype = s->bank_dtype;
-    d.per_step = (s->flags & SDM_FLAG_PER_STEP_KERNELS) ? 1 : 0;
     d.bwd = 0;
+    d.per_step = ((s->flags & SDM_FLAG_PER_STEP_KERNELS) || !phase2_fused_fits(d)) ? 1 : 0;
     return SDM_OK;
 }
 

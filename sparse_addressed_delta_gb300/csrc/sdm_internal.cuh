@@ -153,7 +153,8 @@ cudaError_t launch_dw(const Dims &d, const Inputs &in, const Work &w, int step0,
                       cudaStream_t st);
 cudaError_t launch_phase2_fused(const Dims &d, const Inputs &in, const Work &w, int step0,
                                 int nsteps, cudaStream_t st);
-size_t phase2_fused_smem(const Dims &d);
+size_t phase2_pipe_smem(const Dims &d);
+bool phase2_fused_fits(const Dims &d);
 cudaError_t launch_backward_step(const Dims &d, const Inputs &in, const Work &w,
                                  const BwdOut &o, int step0, int ti, cudaStream_t st);
 cudaError_t launch_debug_expand(const Dims &d, const Work &w, int nchunks, int32_t *perm,

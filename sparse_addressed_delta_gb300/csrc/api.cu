@@ -82,7 +82,7 @@ int check_shape(const sdm_shape *s, Dims &d) {
 
 size_t per_chunk_bytes(const Dims &d) {
     const size_t CW = (size_t)d.C * d.W, CR = (size_t)d.C * d.R, CC = (size_t)d.C * d.C;
-    return 4 * (11 * CW + 1) + 4 * 2 * CR + 4 * 4 * CC + 8;
+    return 4 * (11 * CW + 4) + 4 * 2 * CR + 4 * 4 * CC + 24;
 }
 
 int slab_steps(const Dims &d, int requested) {
@@ -109,7 +109,8 @@ int phase1_ctas(const Dims &d, int ns) {
     F(status, DevStatus, 1)                                                   \
     F(perm, int32_t, N * CW)                                                  \
     F(wdw, float, N * CW)                                                     \
-    F(goff, int32_t, N * (CW + 1))                                            \
+    F(goff, int32_t, N * (CW + 4))                                            \
+    F(ng4, int4, N)                                                           \
     F(gslot, int32_t, N * CW)                                                 \
     F(gfac, float, N * CW)                                                    \
     F(ngroups, int32_t, N)                                                    \

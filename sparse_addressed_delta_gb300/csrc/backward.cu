@@ -46,7 +46,7 @@ __global__ void __launch_bounds__(NTB) k_b_restore(Dims d, Inputs in, Work w, in
     const int p = blockIdx.y, n = local_n(d, step0, ti, p);
     const int CW = d.C * d.W, D = d.D;
     const int ng = w.ngroups[n];
-    const int32_t *goff = w.goff + (size_t)n * (CW + 1);
+    const int32_t *goff = w.goff + (size_t)n * goff_stride(CW);
     const int32_t *gslot = w.gslot + (size_t)n * CW;
     BT *bank = static_cast<BT *>(in.bank) + (size_t)p * d.S * D + lane * CPL;
     const BT *snap = static_cast<const BT *>(in.snap) + (size_t)(ti * d.P + p) * CW * D + lane * CPL;
@@ -349,7 +349,7 @@ __global__ void __launch_bounds__(NTB) k_b_dots(Dims d, Inputs in, Work w, const
                 for (int c = 0; c < CPL; ++c) a = fmaf(y[c], x[c], a);
             }
             a = warp_sum(a);
-            if (lane == 0) w.bdfac[(size_t)p * CW + w.goff[(size_t)n * (CW + 1) + g]] = a;
+            if (lane == 0) w.bdfac[(size_t)p * CW + w.goff[(size_t)n * goff_stride(CW) + g]] = a;
         }
     }
 }
@@ -363,7 +363,7 @@ __global__ void __launch_bounds__(NTB) k_b_dbw(Dims d, Work w, float *gbank, int
     const int p = blockIdx.y, n = local_n(d, step0, ti, p);
     const int C = d.C, D = d.D, W = d.W, CW = C * W;
     const int ng = w.ngroups[n];
-    const int32_t *goff = w.goff + (size_t)n * (CW + 1);
+    const int32_t *goff = w.goff + (size_t)n * goff_stride(CW);
     const int32_t *gslot = w.gslot + (size_t)n * CW;
     const float *gfac = w.gfac + (size_t)n * CW;
     const int32_t *perm = w.perm + (size_t)n * CW;

@@ -234,7 +234,7 @@ __global__ void __launch_bounds__(NT) k_phase1(Dims d, Inputs in, Work w, int st
 
         int32_t *perm = w.perm + (size_t)n * CW;
         float *wdw = w.wdw + (size_t)n * CW;
-        int32_t *goff = w.goff + (size_t)n * (CW + 1);
+        int32_t *goff = w.goff + (size_t)n * goff_stride(CW);
         int32_t *gslot = w.gslot + (size_t)n * CW;
         float *gfac = w.gfac + (size_t)n * CW;
         float *gw = w.gw + (size_t)n * CW;
@@ -321,6 +321,7 @@ __global__ void __launch_bounds__(NT) k_phase1(Dims d, Inputs in, Work w, int st
         const int ng = carry_i;
         if (tid == 0) {
             w.ngroups[n] = ng;
+            w.ng4[n] = make_int4(ng, 0, 0, 0);
             w.nvalid[n] = nv;
             goff[ng] = nw;
         }

@@ -226,7 +226,7 @@ __global__ void __launch_bounds__(kBlock) k_dw(Dims d, Inputs in, Work w, int st
     const int n = (ti - step0) * d.P + p;
     const int C = d.C, D = d.D, W = d.W, CW = C * W;
     const int ng = w.ngroups[n];
-    const int32_t *goff = w.goff + (size_t)n * (CW + 1);
+    const int32_t *goff = w.goff + (size_t)n * goff_stride(CW);
     const int32_t *gslot = w.gslot + (size_t)n * CW;
     const float *gfac = w.gfac + (size_t)n * CW;
     const int32_t *perm = w.perm + (size_t)n * CW;
@@ -280,7 +280,7 @@ __global__ void k_debug_expand(Dims d, Work w, int32_t *perm_out, uint8_t *gs_ou
     const int nw = w.nvalid[n] * d.W;
     const int ng = w.ngroups[n];
     const int32_t *perm = w.perm + (size_t)n * CW;
-    const int32_t *goff = w.goff + (size_t)n * (CW + 1);
+    const int32_t *goff = w.goff + (size_t)n * goff_stride(CW);
     const float *wdw = w.wdw + (size_t)n * CW;
     perm_out += (size_t)n * CW;
     gs_out += (size_t)n * CW;

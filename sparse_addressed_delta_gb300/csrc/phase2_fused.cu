@@ -26,16 +26,16 @@ struct Vec16 {                  // one 16-byte piece of a bank row
 // Pipelined variant for chunks whose per-step metadata fits in shared memory twice: the
 // next step's slots, weights, v pieces, beta, X, QX and sorted member records are copied into
 // the other stage with cp.async while the current step computes. The gather keeps the B0
-// pieces of the written rows in shared memory, and the DW is a block-wide segmented scan over
-// the sorted members (each thread a fixed run of positions, a fixed combine tree), so Zipf-hot
-// groups are summed by many threads. The group's tail position writes the row:
-//   B[s] = (sum of dw * delta_v over the group, scan order) + exp(lend) * B0[s].
+// pieces of the written rows in shared memory; the dual matmul runs on the tensor cores; the
+// DW gives each group (distinct written slot) to one thread, which sums its members in sorted
+// order from shared memory and writes the row once:
+//   B[s] = (sum of dw * delta_v over the group, sorted order) + exp(lend) * B0[s].
 // ---------------------------------------------------------------------------------------
 constexpr int NT2 = 512;
 constexpr int NW2 = NT2 / 32;
 
 struct StageLayout {     // byte offsets inside one stage
-    int wslot, wgw, rslot, rqw, vpc, beta, xs, qs, minfo, mdw, mslot, mfac, bytes;
+    int wslot, wgw, rslot, rqw, vpc, beta, xs, qs, minfo, mdw, mslot, mfac, goff, scal, bytes;
 };
 
 __host__ __device__ inline int align16(int x) { return (x + 15) & ~15; }
@@ -58,14 +58,37 @@ __host__ __device__ inline StageLayout stage_layout(int C, int W, int R) {
     L.mdw = o; o = align16(o + 4 * CW);
     L.mslot = o; o = align16(o + 4 * CW);
     L.mfac = o; o = align16(o + 4 * CW);
+    L.goff = o; o = align16(o + 4 * goff_stride(CW));
+    L.scal = o; o = align16(o + 16);
     L.bytes = o;
     return L;
 }
 
-// Bytes after the two stages: u_pre, inter, delta_v [C][V] f32, the B0 pieces [CW][16 B] and
-// the scan's warp totals.
+// Bytes after the two stages: u_pre, inter, delta_v [C][V] f32 and the B0 pieces [CW][16 B].
 __host__ __device__ inline int pipe_tail_bytes(int C, int W, int V) {
-    return 3 * 4 * C * V + 16 * C * W + NW2 * 4 * (V + 1) * 2;
+    return 3 * 4 * C * V + 16 * C * W;
+}
+
+// ---------------------------------------------------------------------------------------
+// warp-level tensor-core product for the per-step dual matmul: mma.sync m16n8k8 with TF32
+// operands and f32 accumulation (a 64 x 64 by 64 x 8 product per CTA and step is far below
+// a tcgen05 tile; these stay in registers). Fragment layout (PTX ISA, m16n8k8 .tf32):
+// g = lane / 4, i = lane % 4; A: a0 (g, i), a1 (g + 8, i), a2 (g, i + 4), a3 (g + 8, i + 4);
+// B: b0 (i, g), b1 (i + 4, g); C: c0 (g, 2i), c1 (g, 2i + 1), c2 (g + 8, 2i), c3 (g + 8, 2i + 1).
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ unsigned to_tf32(float x) {
+    unsigned r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
+__device__ __forceinline__ void mma_tf32(float (&c)[4], const unsigned (&a)[4],
+                                         const unsigned (&b)[2]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
 // cp.async of nbytes (a multiple of 4) from global to shared, 16 bytes at a time when both
@@ -116,7 +139,6 @@ __global__ void __launch_bounds__(NT2) k_phase2_pipe(Dims d, Inputs in, Work w, 
     float *is = us + C * V;                                      // [C][V]
     float *dvs = is + C * V;                                     // [C][V]
     uint4 *b0s = reinterpret_cast<uint4 *>(dvs + C * V);         // [CW] B0 pieces (raw)
-    float *wtot = reinterpret_cast<float *>(b0s + CW);           // [NW2][V + 1] scan totals
 
     BT *bank = static_cast<BT *>(in.bank) + (size_t)p * d.S * D + c0;
     const BT *vin = static_cast<const BT *>(in.v);
@@ -139,6 +161,10 @@ __global__ void __launch_bounds__(NT2) k_phase2_pipe(Dims d, Inputs in, Work w, 
         const int nv = nvalid_of(ti);
         const int nw = nv * W, nr = nv * R;
         const size_t tok0 = (size_t)p * d.T + (size_t)ti * C;
+        const float *X = w.X + (size_t)n * C * C;
+        const float *QX = w.QX + (size_t)n * C * C;
+        for (int t = tid; t < nv; t += NT2)
+            cp_async16(b + L.vpc + 16 * t, vin + (tok0 + t) * D + c0);
         copy_async(b + L.wslot, in.ws + tok0 * W, 4 * nw, tid, NT2);
         copy_async(b + L.wgw, w.gw + (size_t)n * CW, 4 * nw, tid, NT2);
         copy_async(b + L.rslot, in.rs + tok0 * R, 4 * nr, tid, NT2);
@@ -148,10 +174,8 @@ __global__ void __launch_bounds__(NT2) k_phase2_pipe(Dims d, Inputs in, Work w, 
         copy_async(b + L.mdw, w.wdw + (size_t)n * CW, 4 * nw, tid, NT2);
         copy_async(b + L.mslot, w.mslot + (size_t)n * CW, 4 * nw, tid, NT2);
         copy_async(b + L.mfac, w.mfac + (size_t)n * CW, 4 * nw, tid, NT2);
-        for (int t = tid; t < nv; t += NT2)
-            cp_async16(b + L.vpc + 16 * t, vin + (tok0 + t) * D + c0);
-        const float *X = w.X + (size_t)n * C * C;
-        const float *QX = w.QX + (size_t)n * C * C;
+        copy_async(b + L.goff, w.goff + (size_t)n * goff_stride(CW), 4 * (nw + 1), tid, NT2);
+        if (tid == 0) cp_async16(b + L.scal, w.ng4 + n);
         if ((C & 3) == 0) {   // rows r < nv, whole rows, 16 bytes at a time
             const int q4 = C >> 2;
             for (int i = tid; i < nv * q4; i += NT2) {
@@ -202,7 +226,6 @@ __global__ void __launch_bounds__(NT2) k_phase2_pipe(Dims d, Inputs in, Work w, 
         const float *smfac = reinterpret_cast<const float *>(b + L.mfac);
         const int ti = step0 + ls;
         const int nv = nvalid_of(ti);
-        const int nw = nv * W;
         const size_t tok0 = (size_t)p * d.T + (size_t)ti * C;
 
         // ---- gather (the write pieces are also kept as B0 for the DW) ----
@@ -278,164 +301,115 @@ __global__ void __launch_bounds__(NT2) k_phase2_pipe(Dims d, Inputs in, Work w, 
         }
         __syncthreads();
 
-        // ---- dual matmul: 8 lanes per row split k (k = ks, ks + 8, ...), tree-reduced ----
+        // ---- dual matmul on the tensor cores: one warp per (matrix, 16-row tile) ----
+        // delta_v = X u_pre (matrix 0) and readings = QX u_pre + inter (matrix 1), over the
+        // nv valid rows and k < nv (X and QX are zero past the diagonal and u_pre is zero past
+        // nv). Float32 banks use the 3xTF32 split (hi*lo + lo*hi + hi*hi) for float32 accuracy.
         {
-            const int ks = tid & 7;
-            for (int t0 = 0; t0 < C; t0 += NT2 / 8) {
-                const int t = t0 + (tid >> 3);
-                float ax[V], aq[V];
+            const int g4 = lane >> 2, i4 = lane & 3;
+            const int mt = (nv + 15) >> 4, kt = (nv + 7) >> 3;
+            for (int job = warp; job < 2 * mt; job += NW2) {
+                const int mat = job & 1, r0 = (job >> 1) * 16;
+                const float *A = (mat ? qs : xs) + r0 * XP;
+                float c[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int k0 = 0; k0 < kt * 8; k0 += 8) {
+                    const float af[4] = {A[g4 * XP + k0 + i4], A[(g4 + 8) * XP + k0 + i4],
+                                         A[g4 * XP + k0 + i4 + 4], A[(g4 + 8) * XP + k0 + i4 + 4]};
+                    const float bf[2] = {g4 < V ? us[(k0 + i4) * V + g4] : 0.f,
+                                         g4 < V ? us[(k0 + i4 + 4) * V + g4] : 0.f};
+                    unsigned ah[4], bh[2];
 #pragma unroll
-                for (int c = 0; c < V; ++c) { ax[c] = 0.f; aq[c] = 0.f; }
-                if (t < nv) {
-                    const float *xr = xs + t * XP, *qr = qs + t * XP;
-                    for (int k = ks; k < nv; k += 8) {
-                        const float xv = xr[k], qv = qr[k];
-                        const float4 *up = reinterpret_cast<const float4 *>(us + k * V);
+                    for (int q = 0; q < 4; ++q) ah[q] = to_tf32(af[q]);
+                    bh[0] = to_tf32(bf[0]);
+                    bh[1] = to_tf32(bf[1]);
+                    if constexpr (sizeof(BT) == 4) {
+                        unsigned al[4], bl[2];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) al[q] = to_tf32(af[q] - __uint_as_float(ah[q]));
+                        bl[0] = to_tf32(bf[0] - __uint_as_float(bh[0]));
+                        bl[1] = to_tf32(bf[1] - __uint_as_float(bh[1]));
+                        mma_tf32(c, ah, bl);
+                        mma_tf32(c, al, bh);
+                    }
+                    mma_tf32(c, ah, bh);
+                }
+                // c0 (g, 2i), c1 (g, 2i+1), c2 (g+8, 2i), c3 (g+8, 2i+1)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int t = r0 + g4 + (q >> 1) * 8, col = 2 * i4 + (q & 1);
+                    if (col < V && t < C) {
+                        const float val = t < nv ? c[q] : 0.f;
+                        if (mat == 0) dvs[t * V + col] = val;
+                        else is[t * V + col] = t < nv ? val + is[t * V + col] : 0.f;
+                    }
+                }
+            }
+            // rows of whole 16-row tiles past nv were covered; rows from 16 * mt to C are padding
+            for (int o = 16 * mt * V + tid; o < C * V; o += NT2) { dvs[o] = 0.f; is[o] = 0.f; }
+        }
+        __syncthreads();
+        for (int t = tid; t < C; t += NT2) {
+            if ((size_t)ti * C + t >= (size_t)d.T) continue;
+            float rd[V];
+#pragma unroll
+            for (int c = 0; c < V; ++c) rd[c] = is[t * V + c];
+            store_vec<BT, V>(out + (tok0 + t) * D + c0, rd);
+        }
+
+        // ---- DW: one thread per group (distinct written slot), members in sorted order ----
+        {
+            const int32_t *sgoff = reinterpret_cast<const int32_t *>(b + L.goff);
+            const int ng = nv > 0 ? *reinterpret_cast<const int32_t *>(b + L.scal) : 0;
+            for (int g = tid; g < ng; g += NT2) {
+                const int o0 = sgoff[g], o1 = sgoff[g + 1];
+                float acc[V];
+#pragma unroll
+                for (int c = 0; c < V; ++c) acc[c] = 0.f;
+                int m = o0;
+                for (; m + 4 <= o1; m += 4) {
+                    int inf[4];
+                    float wt[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) { inf[q] = sminfo[m + q]; wt[q] = smdw[m + q]; }
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float4 *dv4 = reinterpret_cast<const float4 *>(dvs + (inf[q] & 255) * V);
 #pragma unroll
                         for (int h = 0; h < V / 4; ++h) {
-                            const float4 u4 = up[h];
-                            ax[4 * h + 0] = fmaf(xv, u4.x, ax[4 * h + 0]);
-                            ax[4 * h + 1] = fmaf(xv, u4.y, ax[4 * h + 1]);
-                            ax[4 * h + 2] = fmaf(xv, u4.z, ax[4 * h + 2]);
-                            ax[4 * h + 3] = fmaf(xv, u4.w, ax[4 * h + 3]);
-                            aq[4 * h + 0] = fmaf(qv, u4.x, aq[4 * h + 0]);
-                            aq[4 * h + 1] = fmaf(qv, u4.y, aq[4 * h + 1]);
-                            aq[4 * h + 2] = fmaf(qv, u4.z, aq[4 * h + 2]);
-                            aq[4 * h + 3] = fmaf(qv, u4.w, aq[4 * h + 3]);
+                            const float4 x = dv4[h];
+                            acc[4 * h + 0] = fmaf(wt[q], x.x, acc[4 * h + 0]);
+                            acc[4 * h + 1] = fmaf(wt[q], x.y, acc[4 * h + 1]);
+                            acc[4 * h + 2] = fmaf(wt[q], x.z, acc[4 * h + 2]);
+                            acc[4 * h + 3] = fmaf(wt[q], x.w, acc[4 * h + 3]);
                         }
                     }
                 }
+                for (; m < o1; ++m) {
+                    const float wt = smdw[m];
+                    const float4 *dv4 = reinterpret_cast<const float4 *>(dvs + (sminfo[m] & 255) * V);
 #pragma unroll
-                for (int off = 4; off > 0; off >>= 1) {
-#pragma unroll
-                    for (int c = 0; c < V; ++c) {
-                        ax[c] += __shfl_down_sync(0xffffffffu, ax[c], off, 8);
-                        aq[c] += __shfl_down_sync(0xffffffffu, aq[c], off, 8);
+                    for (int h = 0; h < V / 4; ++h) {
+                        const float4 x = dv4[h];
+                        acc[4 * h + 0] = fmaf(wt, x.x, acc[4 * h + 0]);
+                        acc[4 * h + 1] = fmaf(wt, x.y, acc[4 * h + 1]);
+                        acc[4 * h + 2] = fmaf(wt, x.z, acc[4 * h + 2]);
+                        acc[4 * h + 3] = fmaf(wt, x.w, acc[4 * h + 3]);
                     }
                 }
-                if (ks == 0 && t < C) {
-                    float rd[V];
-#pragma unroll
-                    for (int c = 0; c < V; ++c) {
-                        dvs[t * V + c] = t < nv ? ax[c] : 0.f;
-                        rd[c] = t < nv ? aq[c] + is[t * V + c] : 0.f;
-                    }
-                    if ((size_t)ti * C + t < (size_t)d.T)
-                        store_vec<BT, V>(out + (tok0 + t) * D + c0, rd);
-                }
-            }
-        }
-        __syncthreads();
-
-        // ---- DW: segmented scan over the sorted members ----
-        const int mpt = (nw + NT2 - 1) / NT2;
-        const int m0 = tid * mpt, m1 = (m0 + mpt) < nw ? (m0 + mpt) : nw;
-        float acc[V];
-        int f = 0;
-#pragma unroll
-        for (int c = 0; c < V; ++c) acc[c] = 0.f;
-        for (int m = m0; m < m1; ++m) {
-            const int info = sminfo[m];
-            const float wt = smdw[m];
-            const float *dv = dvs + (info & 255) * V;
-            if ((info >> 16) & 1) {
-                f = 1;
-#pragma unroll
-                for (int c = 0; c < V; ++c) acc[c] = wt * dv[c];
-            } else {
-#pragma unroll
-                for (int c = 0; c < V; ++c) acc[c] = fmaf(wt, dv[c], acc[c]);
-            }
-        }
-        // inclusive scan of (f, acc) over the warp, then over the warps' totals
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int pf = __shfl_up_sync(0xffffffffu, f, off);
-            float pv[V];
-#pragma unroll
-            for (int c = 0; c < V; ++c) pv[c] = __shfl_up_sync(0xffffffffu, acc[c], off);
-            if (lane >= off) {
-                if (!f) {
-#pragma unroll
-                    for (int c = 0; c < V; ++c) acc[c] = pv[c] + acc[c];
-                }
-                f |= pf;
-            }
-        }
-        if (lane == 31) {
-#pragma unroll
-            for (int c = 0; c < V; ++c) wtot[warp * (V + 1) + c] = acc[c];
-            wtot[warp * (V + 1) + V] = (float)f;
-        }
-        // exclusive value within the warp: the inclusive value of the lane before
-        int ef = __shfl_up_sync(0xffffffffu, f, 1);
-        float ev[V];
-#pragma unroll
-        for (int c = 0; c < V; ++c) ev[c] = __shfl_up_sync(0xffffffffu, acc[c], 1);
-        if (lane == 0) {
-            ef = 0;
-#pragma unroll
-            for (int c = 0; c < V; ++c) ev[c] = 0.f;
-        }
-        __syncthreads();
-        if (warp == 0) {
-            float tv[V];
-            int tf = lane < NW2 ? (int)wtot[lane * (V + 1) + V] : 0;
-#pragma unroll
-            for (int c = 0; c < V; ++c) tv[c] = lane < NW2 ? wtot[lane * (V + 1) + c] : 0.f;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const int pf = __shfl_up_sync(0xffffffffu, tf, off);
-                float pv[V];
-#pragma unroll
-                for (int c = 0; c < V; ++c) pv[c] = __shfl_up_sync(0xffffffffu, tv[c], off);
-                if (lane >= off) {
-                    if (!tf) {
-#pragma unroll
-                        for (int c = 0; c < V; ++c) tv[c] = pv[c] + tv[c];
-                    }
-                    tf |= pf;
-                }
-            }
-            // exclusive prefix of warp `lane`: inclusive value of warp lane-1
-            float xv[V];
-#pragma unroll
-            for (int c = 0; c < V; ++c) xv[c] = __shfl_up_sync(0xffffffffu, tv[c], 1);
-            if (lane < NW2) {
-#pragma unroll
-                for (int c = 0; c < V; ++c) wtot[NW2 * (V + 1) + lane * V + c] = lane ? xv[c] : 0.f;
-            }
-        }
-        __syncthreads();
-        // carry into this thread's run: the warp prefix combined with the lane prefix
-        float run[V];
-#pragma unroll
-        for (int c = 0; c < V; ++c)
-            run[c] = ef ? ev[c] : wtot[NW2 * (V + 1) + warp * V + c] + ev[c];
-        for (int m = m0; m < m1; ++m) {
-            const int info = sminfo[m];
-            const float wt = smdw[m];
-            const int t = info & 255;
-            const float *dv = dvs + t * V;
-            if ((info >> 16) & 1) {
-#pragma unroll
-                for (int c = 0; c < V; ++c) run[c] = wt * dv[c];
-            } else {
-#pragma unroll
-                for (int c = 0; c < V; ++c) run[c] = fmaf(wt, dv[c], run[c]);
-            }
-            if ((info >> 17) & 1) {
+                const int tinf = sminfo[o1 - 1];
+                const uint4 braw = b0s[(tinf & 255) * W + ((tinf >> 8) & 255)];
                 float b0[V], o[V];
-                const uint4 braw = b0s[t * W + ((info >> 8) & 255)];
                 piece_to_f32<BT>(braw, b0);
-                if (in.snap)
-                    *reinterpret_cast<uint4 *>(static_cast<BT *>(in.snap) +
-                                               ((size_t)(ti * d.P + p) * CW + m) * D + c0) = braw;
-                const float fac = smfac[m];
+                const float fac = smfac[o1 - 1];
 #pragma unroll
-                for (int c = 0; c < V; ++c) o[c] = fmaf(fac, b0[c], run[c]);
-                const int sl = smslot[m];
-                if ((unsigned)sl < S) store_vec<BT, V>(bank + (size_t)sl * D, o);
+                for (int c = 0; c < V; ++c) o[c] = fmaf(fac, b0[c], acc[c]);
+                const int sl = smslot[o1 - 1];
+                if ((unsigned)sl < S) {
+                    store_vec<BT, V>(bank + (size_t)sl * D, o);
+                    if (in.snap)
+                        *reinterpret_cast<uint4 *>(static_cast<BT *>(in.snap) +
+                                                   ((size_t)(ti * d.P + p) * CW + (o1 - 1)) * D + c0) = braw;
+                }
             }
         }
         __syncthreads();
@@ -450,24 +424,30 @@ size_t phase2_pipe_smem(const Dims &d) {
     return (size_t)2 * L.bytes + (size_t)pipe_tail_bytes(d.C, d.W, V);
 }
 
-bool phase2_fused_fits(const Dims &d) { return phase2_pipe_smem(d) <= kPipeSmemMax; }
+bool phase2_fused_fits(const Dims &d) {
+    return d.C % 16 == 0 && phase2_pipe_smem(d) <= kPipeSmemMax;
+}
+
+namespace {
+
+template <typename BT>
+cudaError_t launch_pipe(const Dims &d, const Inputs &in, const Work &w, int step0, int nsteps,
+                        cudaStream_t st, size_t smem) {
+    const int grid = d.P * (d.D / (16 / (int)sizeof(BT)));
+    auto kern = k_phase2_pipe<BT>;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    kern<<<grid, NT2, smem, st>>>(d, in, w, step0, nsteps);
+    return cudaGetLastError();
+}
+
+}  // namespace
 
 cudaError_t launch_phase2_fused(const Dims &d, const Inputs &in, const Work &w, int step0,
                                 int nsteps, cudaStream_t st) {
-    const int V = d.dtype == SDM_BF16 ? 8 : 4;
-    const int grid = d.P * (d.D / V);
     const size_t pipe = phase2_pipe_smem(d);
     if (pipe > kPipeSmemMax) return cudaErrorInvalidConfiguration;
-    if (d.dtype == SDM_BF16) {
-        auto kern = k_phase2_pipe<__nv_bfloat16>;
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pipe);
-        kern<<<grid, NT2, pipe, st>>>(d, in, w, step0, nsteps);
-    } else {
-        auto kern = k_phase2_pipe<float>;
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pipe);
-        kern<<<grid, NT2, pipe, st>>>(d, in, w, step0, nsteps);
-    }
-    return cudaGetLastError();
+    if (d.dtype == SDM_BF16) return launch_pipe<__nv_bfloat16>(d, in, w, step0, nsteps, st, pipe);
+    return launch_pipe<float>(d, in, w, step0, nsteps, st, pipe);
 }
 
 }  // namespace sdm

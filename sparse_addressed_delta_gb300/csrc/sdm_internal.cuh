@@ -43,7 +43,9 @@ struct Work {
     // Phase-1 outputs, per chunk
     int32_t *perm;      // [N][CW]   entry e = t*W + j at each sorted position
     float *wdw;         // [N][CW]   DW weight at each sorted position
-    int32_t *goff;      // [N][CW+1] group start positions, goff[ngroups] = n_entries
+    int32_t *goff;      // [N][CW+4] group start positions, goff[ngroups] = n_entries (the
+                        //           stride keeps every chunk's row 16-byte aligned)
+    int4 *ng4;          // [N]       (ngroups, 0, 0, 0): the group count as one 16-byte word
     int32_t *gslot;     // [N][CW]   slot of each group
     float *gfac;        // [N][CW]   exp(lend) of each group
     int32_t *ngroups;   // [N]
@@ -252,6 +254,8 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
+
+__host__ __device__ __forceinline__ int goff_stride(int CW) { return CW + 4; }
 
 __device__ __forceinline__ int chunk_valid(const int32_t *valid, int p, int T, int tok0, int C) {
     int v = valid ? valid[p] : T;

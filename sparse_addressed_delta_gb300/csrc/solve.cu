@@ -4,98 +4,154 @@
 // the chunk's valid tokens are identity rows of X (zero rows of QX), so a ragged chunk is the
 // leading block's inverse.
 //
-// GB300 design: one CTA per chunk, one thread per column of X. Column c of a unit lower
-// triangular inverse depends only on itself (X[i][c] = -beta_i sum_{k=c}^{i-1} A[i][k] X[k][c]),
-// so the threads never wait on one another; each keeps its column's nonzero part (rows c..C-1)
-// in shared memory, packed as a triangle (C(C+1)/2 floats, 128.5 KB at C = 256). A and QK are
-// staged in shared memory too when they fit (C <= 128), else read from L2 with consecutive
-// threads on consecutive columns. Each dot product runs as four interleaved partial sums
-// (fixed order) to break the FMA dependency chain. All arithmetic is full float32: the
-// inverse amplifies rounding, so no reduced-precision tensor path is used.
+// Blocked forward substitution, one CTA (256 threads) per chunk, 16 x 16 blocks (nb = C/16):
+//   1. the diagonal blocks D_i = (I + L_ii)^-1 are inverted at once, one thread per column
+//      of a block (forward substitution inside 16 rows);
+//   2. block row by block row, i = 1 .. nb-1:  T_ij = sum_{k=j}^{i-1} L_ik X_kj  (j < i, all
+//      elements in parallel), then X_ij = -D_i T_ij;
+//   3. QX_ij = sum_{k=j}^{i} QK_ik X_kj for every lower block, block row by block row.
+// X lives in shared memory as packed lower blocks (nb(nb+1)/2 x 1 KB: 136 KB at C = 256); the
+// current block row of L (or QK) and the T blocks are staged next to it. Every product is full
+// float32 FFMA in a fixed order: the inverse amplifies rounding, so no reduced-precision path.
 #include "sdm_internal.cuh"
 
 namespace sdm {
 namespace {
 
-__device__ __forceinline__ int tri_base(int c, int C) { return c * C - (c * (c - 1)) / 2; }
+constexpr int NTS = 256;
+constexpr int BS = 16;                 // block size
+constexpr int BB = BS * BS;            // floats per block
 
-// sum_{k=k0}^{k1-1} a[k] * xc[k - k0], four partial sums in a fixed order
-__device__ __forceinline__ float dot4(const float *a, const float *x, int n) {
-    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-    int k = 0;
-    for (; k + 4 <= n; k += 4) {
-        s0 = fmaf(a[k], x[k], s0);
-        s1 = fmaf(a[k + 1], x[k + 1], s1);
-        s2 = fmaf(a[k + 2], x[k + 2], s2);
-        s3 = fmaf(a[k + 3], x[k + 3], s3);
-    }
-    for (; k < n; ++k) s0 = fmaf(a[k], x[k], s0);
-    return (s0 + s1) + (s2 + s3);
-}
+__host__ __device__ __forceinline__ int tri(int i) { return i * (i + 1) / 2; }
 
-template <bool STAGE>
-__global__ void __launch_bounds__(kMaxChunk) k_solve(Dims d, Inputs in, Work w, int step0,
-                                                    int nsteps) {
-    extern __shared__ float sm[];
+__global__ void __launch_bounds__(NTS) k_solve(Dims d, Inputs in, Work w, int step0, int nsteps) {
+    extern __shared__ __align__(16) float ssm[];
     const int C = d.C;
+    const int nb = (C + BS - 1) / BS;
     const int n = blockIdx.x;
-    const int c = threadIdx.x;
+    const int tid = threadIdx.x;
     const int p = n % d.P, ti = step0 + n / d.P;
     const int nv = w.nvalid[n];
-    const float *Ag = w.A + (size_t)n * C * C;
-    const float *QKg = w.QK + (size_t)n * C * C;
+    const int nvb = (nv + BS - 1) / BS;          // block rows holding valid tokens
+    const float *A = w.A + (size_t)n * C * C;
+    const float *QK = w.QK + (size_t)n * C * C;
     float *X = w.X + (size_t)n * C * C;
     float *QX = w.QX + (size_t)n * C * C;
     const float *beta = in.beta + (size_t)p * d.T + (size_t)ti * C;
-    float *xs = sm;                                    // packed triangle
-    const int tri = C * (C + 1) / 2;
-    const float *A = Ag, *QK = QKg;
-    if (STAGE) {
-        float *as = sm + ((tri + 3) & ~3);
-        float *qs = as + C * C;
-        for (int i = c; i < C * C; i += blockDim.x) { as[i] = Ag[i]; qs[i] = QKg[i]; }
-        __syncthreads();
-        A = as;
-        QK = qs;
-    }
-    float *xc = xs + tri_base(c, C);   // xc[i - c] = X[i][c], i >= c
+    float *Xp = ssm;                             // packed lower blocks of X
+    float *Lr = Xp + tri(nb) * BB;               // current block row of L / QK  [nb][16][16]
+    float *Tb = Lr + nb * BB;                    // T blocks                     [nb][16][16]
 
-    if (c < nv) {
-        xc[0] = 1.f;
-        for (int i = c + 1; i < nv; ++i)
-            xc[i - c] = -beta[i] * dot4(A + (size_t)i * C + c, xc, i - c);
-    }
-    // write X and QX row by row (consecutive threads on consecutive columns)
-    for (int i = 0; i < C; ++i) {
-        float x, qx = 0.f;
-        if (i < nv && c < nv) {
-            x = (c <= i) ? xc[i - c] : 0.f;
-            if (c <= i) qx = dot4(QK + (size_t)i * C + c, xc, i - c + 1);
-        } else {
-            x = (i == c) ? 1.f : 0.f;
+    // L (or QK) element (R, K) of the chunk, zero outside the valid tokens
+    auto lval = [&](int R, int K) {
+        return (R < nv && K < R) ? beta[R] * A[(size_t)R * C + K] : 0.f;
+    };
+
+    // 1. diagonal inverses: thread (block b, column c) substitutes down its column
+    for (int job = tid; job < nvb * BS; job += NTS) {
+        const int b = job / BS, c = job - b * BS;
+        float *Dk = Xp + (tri(b) + b) * BB;
+        float x[BS];
+#pragma unroll
+        for (int r = 0; r < BS; ++r) x[r] = (r == c) ? 1.f : 0.f;
+#pragma unroll
+        for (int r = 1; r < BS; ++r) {
+            const int R = b * BS + r;
+            float s = 0.f;
+#pragma unroll
+            for (int k = 0; k < BS; ++k)
+                if (k < r) s = fmaf(lval(R, b * BS + k), x[k], s);
+            if (r > c) x[r] = -s;
         }
-        X[(size_t)i * C + c] = x;
-        QX[(size_t)i * C + c] = qx;
+#pragma unroll
+        for (int r = 0; r < BS; ++r) Dk[r * BS + c] = x[r];
+    }
+    __syncthreads();
+
+    // 2. block rows
+    for (int i = 1; i < nvb; ++i) {
+        for (int e = tid; e < i * BB; e += NTS) {
+            const int k = e / BB, rc = e - k * BB, r = rc / BS, c = rc - r * BS;
+            Lr[e] = lval(i * BS + r, k * BS + c);
+        }
+        __syncthreads();
+        for (int e = tid; e < i * BB; e += NTS) {
+            const int j = e / BB, rc = e - j * BB, r = rc / BS, c = rc - r * BS;
+            float s = 0.f;
+            for (int k = j; k < i; ++k) {
+                const float *Lk = Lr + k * BB + r * BS;
+                const float *Xk = Xp + (tri(k) + j) * BB + c;
+#pragma unroll
+                for (int m = 0; m < BS; ++m) s = fmaf(Lk[m], Xk[m * BS], s);
+            }
+            Tb[e] = s;
+        }
+        __syncthreads();
+        const float *Di = Xp + (tri(i) + i) * BB;
+        for (int e = tid; e < i * BB; e += NTS) {
+            const int j = e / BB, rc = e - j * BB, r = rc / BS, c = rc - r * BS;
+            const float *T = Tb + j * BB + c;
+            float s = 0.f;
+            for (int m = 0; m <= r; ++m) s = fmaf(Di[r * BS + m], T[m * BS], s);
+            Xp[(tri(i) + j) * BB + rc] = -s;
+        }
+        __syncthreads();
+    }
+
+    // 3. QX, block row by block row; written out with X
+    for (int i = 0; i < nb; ++i) {
+        if (i < nvb) {
+            for (int e = tid; e < (i + 1) * BB; e += NTS) {
+                const int k = e / BB, rc = e - k * BB, r = rc / BS, c = rc - r * BS;
+                const int R = i * BS + r, K = k * BS + c;
+                Lr[e] = (R < nv && K <= R) ? QK[(size_t)R * C + K] : 0.f;
+            }
+            __syncthreads();
+            for (int e = tid; e < (i + 1) * BB; e += NTS) {
+                const int j = e / BB, rc = e - j * BB, r = rc / BS, c = rc - r * BS;
+                float s = 0.f;
+                for (int k = j; k <= i; ++k) {
+                    const float *Qk = Lr + k * BB + r * BS;
+                    const float *Xk = Xp + (tri(k) + j) * BB + c;
+#pragma unroll
+                    for (int m = 0; m < BS; ++m) s = fmaf(Qk[m], Xk[m * BS], s);
+                }
+                Tb[e] = s;
+            }
+            __syncthreads();
+        }
+        // rows i*16 .. i*16+15 of X and QX (consecutive threads on consecutive columns)
+        for (int e = tid; e < BS * C; e += NTS) {
+            const int r = e / C, u = e - r * C, t = i * BS + r;
+            if (t >= C) continue;
+            float x, q = 0.f;
+            if (t < nv && u < nv) {
+                const int j = u / BS;
+                x = (u <= t) ? Xp[(tri(i) + j) * BB + r * BS + (u - j * BS)] : 0.f;
+                if (j <= i) q = Tb[j * BB + r * BS + (u - j * BS)];
+            } else {
+                x = (t == u) ? 1.f : 0.f;
+            }
+            X[(size_t)t * C + u] = x;
+            QX[(size_t)t * C + u] = q;
+        }
+        __syncthreads();
     }
 }
 
 }  // namespace
 
+size_t solve_smem_bytes(int C) {
+    const int nb = (C + BS - 1) / BS;
+    return sizeof(float) * (size_t)(tri(nb) + 2 * nb) * BB;
+}
+
 cudaError_t launch_solve(const Dims &d, const Inputs &in, const Work &w, int step0, int nsteps,
                          cudaStream_t st) {
-    const size_t tri = (size_t)d.C * (d.C + 1) / 2;
-    const size_t staged = sizeof(float) * (((tri + 3) & ~size_t(3)) + 2 * (size_t)d.C * d.C);
-    if (staged <= 200 * 1024) {
-        if (staged > 48 * 1024)
-            cudaFuncSetAttribute(k_solve<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)staged);
-        k_solve<true><<<nsteps * d.P, d.C, staged, st>>>(d, in, w, step0, nsteps);
-    } else {
-        const size_t smem = sizeof(float) * tri;
-        cudaFuncSetAttribute(k_solve<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem);
-        k_solve<false><<<nsteps * d.P, d.C, smem, st>>>(d, in, w, step0, nsteps);
-    }
+    const size_t smem = solve_smem_bytes(d.C);
+    if (smem > 48 * 1024)
+        cudaFuncSetAttribute(k_solve, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    k_solve<<<nsteps * d.P, NTS, smem, st>>>(d, in, w, step0, nsteps);
     return cudaGetLastError();
 }
 

@@ -76,13 +76,14 @@ int check_shape(const sdm_shape *s, Dims &d) {
     d.Nt = (int)Nt;
     d.dtype = s->bank_dtype;
     d.bwd = 0;
+    d.xp = d.C;
     d.per_step = ((s->flags & SDM_FLAG_PER_STEP_KERNELS) || !phase2_fused_fits(d)) ? 1 : 0;
     return SDM_OK;
 }
 
 size_t per_chunk_bytes(const Dims &d) {
     const size_t CW = (size_t)d.C * d.W, CR = (size_t)d.C * d.R, CC = (size_t)d.C * d.C;
-    return 4 * (11 * CW + 4) + 4 * 2 * CR + 4 * 4 * CC + 24;
+    return 4 * (11 * CW + 4) + 4 * 3 * CR + 4 * 4 * CC + 24;
 }
 
 int slab_steps(const Dims &d, int requested) {
@@ -116,16 +117,16 @@ int phase1_ctas(const Dims &d, int ns) {
     F(ngroups, int32_t, N)                                                    \
     F(nvalid, int32_t, N)                                                     \
     F(minfo, int32_t, N * CW)                                                 \
-    F(mslot, int32_t, N * CW)                                                 \
-    F(mfac, float, N * CW)                                                    \
+    F(wsl, int32_t, N * CW)                                                   \
+    F(rsl, int32_t, N * CR)                                                   \
     F(gw, float, N * CW)                                                      \
     F(qw, float, N * CR)                                                      \
     F(lw, float, N * CW)                                                      \
     F(lr, float, N * CR)                                                      \
     F(A, float, N * CC)                                                       \
     F(QK, float, N * CC)                                                      \
-    F(X, float, N * CC)                                                       \
-    F(QX, float, N * CC)                                                      \
+    F(X, float, N * CX)                                                       \
+    F(QX, float, N * CX)                                                      \
     F(keys, unsigned long long, G * 2 * CW)                                   \
     F(inv, int32_t, G * CW)                                                   \
     F(lws, float, G * CW)                                                     \
@@ -168,7 +169,7 @@ int phase1_ctas(const Dims &d, int ns) {
 size_t layout_bytes(const Dims &d, int ns, int G_) {
     const size_t N = (size_t)ns * d.P, P = d.P, CW = (size_t)d.C * d.W, CR = (size_t)d.C * d.R,
                  CC = (size_t)d.C * d.C, CD = (size_t)d.C * d.D, G = G_, B = d.bwd ? 1 : 0,
-                 C = d.C, DT = ((size_t)d.D + 31) / 32;
+                 C = d.C, DT = ((size_t)d.D + 31) / 32, CX = (size_t)d.C * d.xp;
     size_t off = 0;
 #define X_SIZE(name, type, count) off += up(sizeof(type) * (size_t)(count));
     SDM_LAYOUT(X_SIZE)
@@ -179,7 +180,7 @@ size_t layout_bytes(const Dims &d, int ns, int G_) {
 Work layout_assign(const Dims &d, int ns, int G_, void *base) {
     const size_t N = (size_t)ns * d.P, P = d.P, CW = (size_t)d.C * d.W, CR = (size_t)d.C * d.R,
                  CC = (size_t)d.C * d.C, CD = (size_t)d.C * d.D, G = G_, B = d.bwd ? 1 : 0,
-                 C = d.C, DT = ((size_t)d.D + 31) / 32;
+                 C = d.C, DT = ((size_t)d.D + 31) / 32, CX = (size_t)d.C * d.xp;
     Work w;
     memset(&w, 0, sizeof(w));
     char *p = static_cast<char *>(base);
@@ -206,6 +207,7 @@ int prepare(const sdm_shape *shape, Prepared &pr, int bwd = 0) {
     int rc = check_shape(shape, pr.d);
     if (rc) return rc;
     pr.d.bwd = bwd;
+    pr.d.xp = x_row_pitch(pr.d);
     pr.ns = slab_steps(pr.d, shape->slab_steps);
     pr.G = phase1_ctas(pr.d, pr.ns);
     pr.bytes = layout_bytes(pr.d, pr.ns, pr.G);
@@ -465,12 +467,20 @@ int sdm_phase1_debug(const sdm_shape *shape, const int32_t *write_slots, const v
             return cuda_fail(e, "debug expand");
         struct { void *dst; const void *src; size_t per; } cp[] = {
             {ngroups, w.ngroups, 4}, {lw, w.lw, 4 * CW}, {gw, w.gw, 4 * CW},
-            {lr, w.lr, 4 * CR}, {qw, w.qw, 4 * CR}, {A, w.A, 4 * CC}, {QK, w.QK, 4 * CC},
-            {X, w.X, 4 * CC}, {QX, w.QX, 4 * CC}};
+            {lr, w.lr, 4 * CR}, {qw, w.qw, 4 * CR}, {A, w.A, 4 * CC}, {QK, w.QK, 4 * CC}};
         for (auto &c : cp) {
             if (!c.dst) continue;
             e = cudaMemcpyAsync(static_cast<char *>(c.dst) + n0 * c.per, c.src, N * c.per,
                                 cudaMemcpyDeviceToDevice, st);
+            if (e != cudaSuccess) return cuda_fail(e, "debug copy");
+        }
+        // X and QX rows at the workspace pitch -> dense [C][C]
+        const float *xsrc[2] = {w.X, w.QX};
+        float *xdst[2] = {X, QX};
+        for (int m = 0; m < 2; ++m) {
+            if (!xdst[m]) continue;
+            e = cudaMemcpy2DAsync(xdst[m] + n0 * CC, 4 * (size_t)d.C, xsrc[m], 4 * (size_t)d.xp,
+                                  4 * (size_t)d.C, N * d.C, cudaMemcpyDeviceToDevice, st);
             if (e != cudaSuccess) return cuda_fail(e, "debug copy");
         }
     }

@@ -242,8 +242,8 @@ __global__ void __launch_bounds__(NT) k_phase1(Dims d, Inputs in, Work w, int st
         float *lw = w.lw + (size_t)n * CW;
         float *lr = w.lr + (size_t)n * CR;
         int32_t *minfo = w.minfo + (size_t)n * CW;
-        int32_t *mslot = w.mslot + (size_t)n * CW;
-        float *mfac = w.mfac + (size_t)n * CW;
+        int32_t *wsl = w.wsl + (size_t)n * CW;
+        int32_t *rsl = w.rsl + (size_t)n * CR;
         float *A = w.A + (size_t)n * CC;
         float *QK = w.QK + (size_t)n * CC;
 
@@ -260,12 +260,15 @@ __global__ void __launch_bounds__(NT) k_phase1(Dims d, Inputs in, Work w, int st
                 bad = 1;
             }
             kf[i] = kk;
+            wsl[i] = s;
             const int t = div_by(i, magW);
             keyA[i] = ((unsigned long long)(unsigned)s << 32) | ((unsigned)t << 8) |
                       (unsigned)(i - t * W);
         }
         for (int i = tid; i < nr; i += NT) {
-            if ((unsigned)rs[i] >= (unsigned)S) report_bad_slot(w.status, (int)(tok_base + i / R));
+            const int r = rs[i];
+            if ((unsigned)r >= (unsigned)S) report_bad_slot(w.status, (int)(tok_base + i / R));
+            rsl[i] = (unsigned)r < (unsigned)S ? r : S;
         }
         // slot S may need one more radix digit than the real slots
         const int npass = __syncthreads_or(bad) ? (32 - __clz(S) + 7) / 8 : passes;
@@ -275,6 +278,7 @@ __global__ void __launch_bounds__(NT) k_phase1(Dims d, Inputs in, Work w, int st
             unsigned long long *t = src; src = dst; dst = t;
         }
         const unsigned long long *srt = src;
+        float2 *tkk = reinterpret_cast<float2 *>(dst);   // (token bits, k) per sorted position
 
         // 2. groups and running log-decays along the sorted row
         float carry_v = 0.f;
@@ -291,6 +295,7 @@ __global__ void __launch_bounds__(NT) k_phase1(Dims d, Inputs in, Work w, int st
                 gv = ((unsigned)ws[e] < (unsigned)S) ? g[e] : 0.f;
                 perm[pos] = e;
                 inv[e] = pos;
+                tkk[pos] = make_float2(__int_as_float((int)(low >> 8)), kf[e]);
                 if (!head && ((unsigned)srt[pos - 1] >> 8) == (low >> 8))
                     atomicAdd(&w.status->repeated_write_slots, 1ull);
             }
@@ -306,16 +311,12 @@ __global__ void __launch_bounds__(NT) k_phase1(Dims d, Inputs in, Work w, int st
                 pgid[pos] = gid;
                 if (head) { goff[gid] = pos; gslot[gid] = slot; }
                 const bool tail = (pos == nw - 1) || (int)(srt[pos + 1] >> 32) != slot;
-                float fac = 0.f;
                 if (tail) {
                     lend[gid] = lv;
-                    fac = expf(lv);
-                    gfac[gid] = fac;
+                    gfac[gid] = expf(lv);
                 }
                 minfo[pos] = (int)(low >> 8) | (int)((low & 255u) << 8) | (head ? 1 << 16 : 0) |
                              (tail ? 1 << 17 : 0);
-                mslot[pos] = slot;
-                mfac[pos] = fac;
             }
         }
         const int ng = carry_i;
@@ -368,24 +369,40 @@ __global__ void __launch_bounds__(NT) k_phase1(Dims d, Inputs in, Work w, int st
         }
         __syncthreads();
 
-        // 4. A and QK, one warp per token row
+        // 4. A and QK, one warp per token row. The row's entries are looked up one per lane;
+        //    entries with earlier members of their group (a ballot) are then taken in entry
+        //    order, the lanes over those members. (token, k) of every sorted position is kept
+        //    in the free radix buffer, next to its running log-decay.
         float *row = sm.row[warp];
         for (int t = warp; t < C; t += NW) {
             for (int c = lane; c < C; c += 32) row[c] = 0.f;
             __syncwarp();
             if (t < nv) {
-                for (int j = 0; j < W; ++j) {
-                    const int e = t * W + j;
-                    const float ka = kf[e];
-                    if (ka == 0.f) continue;
-                    const int pos = inv[e];
-                    const int gs = pgs[pos];
-                    const float la = lws[pos];
-                    for (int m = gs + lane; m < pos; m += 32) {
-                        const unsigned lb = (unsigned)srt[m];
-                        row[lb >> 8] += ka * kf[ent_of(lb)] * expf(la - lws[m]);
+                for (int j0 = 0; j0 < W; j0 += 32) {
+                    const int j = j0 + lane;
+                    float ka = 0.f, la = 0.f;
+                    int pos = 0, gs = 0;
+                    if (j < W) {
+                        const int e = t * W + j;
+                        ka = kf[e];
+                        pos = inv[e];
+                        gs = pgs[pos];
+                        la = lws[pos];
                     }
-                    __syncwarp();
+                    unsigned todo = __ballot_sync(0xffffffffu, ka != 0.f && pos > gs);
+                    while (todo) {
+                        const int src = __ffs(todo) - 1;
+                        todo &= todo - 1;
+                        const float kb = __shfl_sync(0xffffffffu, ka, src);
+                        const float lb = __shfl_sync(0xffffffffu, la, src);
+                        const int pb = __shfl_sync(0xffffffffu, pos, src);
+                        const int gb = __shfl_sync(0xffffffffu, gs, src);
+                        for (int m = gb + lane; m < pb; m += 32) {
+                            const float2 tk = tkk[m];
+                            row[__float_as_int(tk.x)] += kb * tk.y * expf(lb - lws[m]);
+                        }
+                        __syncwarp();
+                    }
                 }
             }
             for (int c = lane; c < C; c += 32) A[(size_t)t * C + c] = row[c];
@@ -393,17 +410,33 @@ __global__ void __launch_bounds__(NT) k_phase1(Dims d, Inputs in, Work w, int st
             for (int c = lane; c < C; c += 32) row[c] = 0.f;
             __syncwarp();
             if (t < nv) {
-                for (int i = 0; i < R; ++i) {
-                    const int er = t * R + i;
-                    const int lo = rlo[er], hi = rhi[er];
-                    if (hi < 0) continue;
-                    const float qa = to_f32(q[er]);
-                    const float la = lr[er];
-                    for (int m = lo + lane; m <= hi; m += 32) {
-                        const unsigned lb = (unsigned)srt[m];
-                        row[lb >> 8] += qa * kf[ent_of(lb)] * expf(la - lws[m]);
+                for (int i0 = 0; i0 < R; i0 += 32) {
+                    const int i = i0 + lane;
+                    float qa = 0.f, la = 0.f;
+                    int lo = 0, hi = -1;
+                    if (i < R) {
+                        const int er = t * R + i;
+                        lo = rlo[er];
+                        hi = rhi[er];
+                        if (hi >= 0) {
+                            qa = to_f32(q[er]);
+                            la = lr[er];
+                        }
                     }
-                    __syncwarp();
+                    unsigned todo = __ballot_sync(0xffffffffu, hi >= 0);
+                    while (todo) {
+                        const int src = __ffs(todo) - 1;
+                        todo &= todo - 1;
+                        const float qb = __shfl_sync(0xffffffffu, qa, src);
+                        const float lb = __shfl_sync(0xffffffffu, la, src);
+                        const int lob = __shfl_sync(0xffffffffu, lo, src);
+                        const int hib = __shfl_sync(0xffffffffu, hi, src);
+                        for (int m = lob + lane; m <= hib; m += 32) {
+                            const float2 tk = tkk[m];
+                            row[__float_as_int(tk.x)] += qb * tk.y * expf(lb - lws[m]);
+                        }
+                        __syncwarp();
+                    }
                 }
             }
             for (int c = lane; c < C; c += 32) QK[(size_t)t * C + c] = row[c];
@@ -457,8 +490,10 @@ __global__ void __launch_bounds__(NT) k_phase1(Dims d, Inputs in, Work w, int st
             if (tid == 0) { w.rng[n] = rcarry; rgoff[rcarry] = nr; }
             __syncthreads();
         }
-        for (int i = nw + tid; i < CW; i += NT) { perm[i] = -1; gw[i] = 0.f; lw[i] = 0.f; wdw[i] = 0.f; }
-        for (int i = nr + tid; i < CR; i += NT) { qw[i] = 0.f; lr[i] = 0.f; }
+        for (int i = nw + tid; i < CW; i += NT) {
+            perm[i] = -1; gw[i] = 0.f; lw[i] = 0.f; wdw[i] = 0.f; wsl[i] = S;
+        }
+        for (int i = nr + tid; i < CR; i += NT) { qw[i] = 0.f; lr[i] = 0.f; rsl[i] = S; }
         __syncthreads();
     }
 }

@@ -9,7 +9,7 @@
 // of its own stream's rows, step after step, and only ever waits on its own threads.
 //
 // The bank pieces a step writes are read back by the next step's gather through L1/L2 in the
-// same CTA, ordered by the step's closing __syncthreads (no read-only cache path). The kernel
+// same CTA, ordered by the step's closing barrier (no read-only cache path). The kernel
 // runs when two stages of per-step metadata fit in shared memory (launch_phase2_fused says
 // whether); larger chunks use the per-step kernels of phase2.cu.
 #include "sdm_internal.cuh"
@@ -22,20 +22,36 @@ struct Vec16 {                  // one 16-byte piece of a bank row
     static constexpr int N = 16 / sizeof(BT);
 };
 
-// ---------------------------------------------------------------------------------------
 // Pipelined variant for chunks whose per-step metadata fits in shared memory twice: the
-// next step's slots, weights, v pieces, beta, X, QX and sorted member records are copied into
-// the other stage with cp.async while the current step computes. The gather keeps the B0
-// pieces of the written rows in shared memory; the dual matmul runs on the tensor cores; the
-// DW gives each group (distinct written slot) to one thread, which sums its members in sorted
-// order from shared memory and writes the row once:
+// next step's slots, weights, X, QX and sorted member records are brought into the other
+// stage by bulk copies (the TMA unit, one mbarrier per stage) and its v pieces and beta by
+// cp.async, while the current step computes. The gather keeps the B0 pieces of the written rows
+// in shared memory; the dual matmul runs on the tensor cores; the DW gives each group (distinct
+// written slot) to one thread, which sums its members in sorted order from shared memory and
+// writes the row once:
 //   B[s] = (sum of dw * delta_v over the group, sorted order) + exp(lend) * B0[s].
 // ---------------------------------------------------------------------------------------
-constexpr int NT2 = 512;
+constexpr int NT2 = 512;          // compute threads (16 warps)
 constexpr int NW2 = NT2 / 32;
+constexpr int NP2 = NT2 + 32;     // + one producer warp that only issues the stage copies
 
-struct StageLayout {     // byte offsets inside one stage
-    int wslot, wgw, rslot, rqw, vpc, beta, xs, qs, minfo, mdw, mslot, mfac, goff, scal, bytes;
+// barrier 1: the compute warps only (the producer warp never waits on it)
+__device__ __forceinline__ void compute_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(NT2) : "memory");
+}
+__device__ __forceinline__ bool compute_sync_or(bool v) {
+    unsigned r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 1, %2, p;\n"
+        " selp.u32 %0, 1, 0, q;\n}"
+        : "=r"(r)
+        : "r"((unsigned)v), "n"(NT2)
+        : "memory");
+    return r != 0;
+}
+
+struct StageLayout {     // byte offsets inside one stage (every array 16-byte aligned)
+    int wslot, wgw, rslot, rqw, minfo, mdw, gslot, gfac, goff, scal, xs, qs, vpc, beta, bytes;
 };
 
 __host__ __device__ inline int align16(int x) { return (x + 15) & ~15; }
@@ -50,23 +66,30 @@ __host__ __device__ inline StageLayout stage_layout(int C, int W, int R) {
     L.wgw = o; o = align16(o + 4 * CW);
     L.rslot = o; o = align16(o + 4 * CR);
     L.rqw = o; o = align16(o + 4 * CR);
-    L.vpc = o; o = align16(o + 16 * C);
-    L.beta = o; o = align16(o + 4 * C);
-    L.xs = o; o = align16(o + 4 * C * XP);
-    L.qs = o; o = align16(o + 4 * C * XP);
     L.minfo = o; o = align16(o + 4 * CW);
     L.mdw = o; o = align16(o + 4 * CW);
-    L.mslot = o; o = align16(o + 4 * CW);
-    L.mfac = o; o = align16(o + 4 * CW);
+    L.gslot = o; o = align16(o + 4 * CW);
+    L.gfac = o; o = align16(o + 4 * CW);
     L.goff = o; o = align16(o + 4 * goff_stride(CW));
     L.scal = o; o = align16(o + 16);
+    L.xs = o; o = align16(o + 4 * C * XP);
+    L.qs = o; o = align16(o + 4 * C * XP);
+    L.vpc = o; o = align16(o + 16 * C);
+    L.beta = o; o = align16(o + 4 * C);
     L.bytes = o;
     return L;
 }
 
-// Bytes after the two stages: u_pre, inter, delta_v [C][V] f32 and the B0 pieces [CW][16 B].
+// Bytes the bulk copies of one stage move (everything before vpc; X and QX whole, padded rows)
+__host__ __device__ inline unsigned stage_bulk_bytes(int C, int W, int R) {
+    const int CW = C * W, CR = C * R;
+    return (unsigned)(4 * (6 * CW + 2 * CR + goff_stride(CW)) + 16 + 2 * 4 * C * x_pitch(C));
+}
+
+// Bytes after the two stages: u_pre, inter, delta_v [C][V] f32, the B0 pieces [CW][16 B] and
+// the stage mbarriers (full[2], empty[2]).
 __host__ __device__ inline int pipe_tail_bytes(int C, int W, int V) {
-    return 3 * 4 * C * V + 16 * C * W;
+    return 3 * 4 * C * V + 16 * C * W + 32;
 }
 
 // ---------------------------------------------------------------------------------------
@@ -91,20 +114,6 @@ __device__ __forceinline__ void mma_tf32(float (&c)[4], const unsigned (&a)[4],
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
-// cp.async of nbytes (a multiple of 4) from global to shared, 16 bytes at a time when both
-// ends are 16-byte aligned
-__device__ __forceinline__ void copy_async(unsigned char *dst, const void *src, int nbytes, int tid,
-                                           int nthr) {
-    const unsigned char *s8 = static_cast<const unsigned char *>(src);
-    if (((reinterpret_cast<uintptr_t>(s8) | reinterpret_cast<uintptr_t>(dst)) & 15) == 0) {
-        const int n16 = nbytes >> 4;
-        for (int i = tid; i < n16; i += nthr) cp_async16(dst + 16 * i, s8 + 16 * i);
-        for (int i = n16 * 4 + tid; i < (nbytes >> 2); i += nthr) cp_async4(dst + 4 * i, s8 + 4 * i);
-    } else {
-        for (int i = tid; i < (nbytes >> 2); i += nthr) cp_async4(dst + 4 * i, s8 + 4 * i);
-    }
-}
-
 template <typename BT>
 __device__ __forceinline__ void piece_to_f32(const uint4 &u, float (&o)[16 / sizeof(BT)]) {
     if constexpr (sizeof(BT) == 2) {
@@ -123,7 +132,7 @@ __device__ __forceinline__ void piece_to_f32(const uint4 &u, float (&o)[16 / siz
 }
 
 template <typename BT>
-__global__ void __launch_bounds__(NT2) k_phase2_pipe(Dims d, Inputs in, Work w, int step0,
+__global__ void __launch_bounds__(NP2) k_phase2_pipe(Dims d, Inputs in, Work w, int step0,
                                                     int nsteps) {
     constexpr int V = Vec16<BT>::N;
     extern __shared__ __align__(16) unsigned char psm[];
@@ -139,6 +148,10 @@ __global__ void __launch_bounds__(NT2) k_phase2_pipe(Dims d, Inputs in, Work w, 
     float *is = us + C * V;                                      // [C][V]
     float *dvs = is + C * V;                                     // [C][V]
     uint4 *b0s = reinterpret_cast<uint4 *>(dvs + C * V);         // [CW] B0 pieces (raw)
+    // full[st]: stage st landed (1 expect-tx arrival + 32 producer-lane cp.async arrivals and
+    // the bulk bytes); empty[st]: the compute warps are done with stage st (1 arrival)
+    unsigned long long *full = reinterpret_cast<unsigned long long *>(b0s + CW);
+    unsigned long long *empty = full + 2;
 
     BT *bank = static_cast<BT *>(in.bank) + (size_t)p * d.S * D + c0;
     const BT *vin = static_cast<const BT *>(in.v);
@@ -153,44 +166,75 @@ __global__ void __launch_bounds__(NT2) k_phase2_pipe(Dims d, Inputs in, Work w, 
         return r < 0 ? 0 : (r > C ? C : r);
     };
 
-    // cp.async of step ls's metadata into stage st (all threads)
+    // stage st for step ls, issued by the producer warp: lanes 0..11 bulk-copy the workspace
+    // arrays (16-byte aligned chunk offsets, C % 16 == 0), every lane cp.asyncs the v pieces and
+    // beta of its tokens and then arrives on full[st] when those have landed
     auto issue = [&](int ls, int st) {
         unsigned char *b = psm + st * L.bytes;
         const int ti = step0 + ls;
         const int n = ls * d.P + p;
         const int nv = nvalid_of(ti);
-        const int nw = nv * W, nr = nv * R;
         const size_t tok0 = (size_t)p * d.T + (size_t)ti * C;
-        const float *X = w.X + (size_t)n * C * C;
-        const float *QX = w.QX + (size_t)n * C * C;
-        for (int t = tid; t < nv; t += NT2)
-            cp_async16(b + L.vpc + 16 * t, vin + (tok0 + t) * D + c0);
-        copy_async(b + L.wslot, in.ws + tok0 * W, 4 * nw, tid, NT2);
-        copy_async(b + L.wgw, w.gw + (size_t)n * CW, 4 * nw, tid, NT2);
-        copy_async(b + L.rslot, in.rs + tok0 * R, 4 * nr, tid, NT2);
-        copy_async(b + L.rqw, w.qw + (size_t)n * CR, 4 * nr, tid, NT2);
-        copy_async(b + L.beta, in.beta + tok0, 4 * nv, tid, NT2);
-        copy_async(b + L.minfo, w.minfo + (size_t)n * CW, 4 * nw, tid, NT2);
-        copy_async(b + L.mdw, w.wdw + (size_t)n * CW, 4 * nw, tid, NT2);
-        copy_async(b + L.mslot, w.mslot + (size_t)n * CW, 4 * nw, tid, NT2);
-        copy_async(b + L.mfac, w.mfac + (size_t)n * CW, 4 * nw, tid, NT2);
-        copy_async(b + L.goff, w.goff + (size_t)n * goff_stride(CW), 4 * (nw + 1), tid, NT2);
-        if (tid == 0) cp_async16(b + L.scal, w.ng4 + n);
-        if ((C & 3) == 0) {   // rows r < nv, whole rows, 16 bytes at a time
-            const int q4 = C >> 2;
-            for (int i = tid; i < nv * q4; i += NT2) {
-                const int r = div_by(i, magQ), k = (i - r * q4) * 4;
-                cp_async16(b + L.xs + 4 * (r * XP + k), X + (size_t)r * C + k);
-                cp_async16(b + L.qs + 4 * (r * XP + k), QX + (size_t)r * C + k);
+        unsigned long long *bar = full + st;
+        if (lane == 0) mbar_arrive_expect_tx(bar, stage_bulk_bytes(C, W, R));
+        __syncwarp();
+        if (lane < 12) {
+            const void *src;
+            int off, bytes;
+            switch (lane) {
+                case 0: src = w.wsl + (size_t)n * CW; off = L.wslot; bytes = 4 * CW; break;
+                case 1: src = w.gw + (size_t)n * CW; off = L.wgw; bytes = 4 * CW; break;
+                case 2: src = w.rsl + (size_t)n * CR; off = L.rslot; bytes = 4 * CR; break;
+                case 3: src = w.qw + (size_t)n * CR; off = L.rqw; bytes = 4 * CR; break;
+                case 4: src = w.minfo + (size_t)n * CW; off = L.minfo; bytes = 4 * CW; break;
+                case 5: src = w.wdw + (size_t)n * CW; off = L.mdw; bytes = 4 * CW; break;
+                case 6: src = w.gslot + (size_t)n * CW; off = L.gslot; bytes = 4 * CW; break;
+                case 7: src = w.gfac + (size_t)n * CW; off = L.gfac; bytes = 4 * CW; break;
+                case 8:
+                    src = w.goff + (size_t)n * goff_stride(CW);
+                    off = L.goff;
+                    bytes = 4 * goff_stride(CW);
+                    break;
+                case 9: src = w.ng4 + n; off = L.scal; bytes = 16; break;
+                case 10: src = w.X + (size_t)n * C * XP; off = L.xs; bytes = 4 * C * XP; break;
+                default: src = w.QX + (size_t)n * C * XP; off = L.qs; bytes = 4 * C * XP; break;
             }
-        } else {
-            for (int r = warp; r < nv; r += NW2)
-                for (int k = lane; k < C; k += 32) {
-                    cp_async4(b + L.xs + 4 * (r * XP + k), X + (size_t)r * C + k);
-                    cp_async4(b + L.qs + 4 * (r * XP + k), QX + (size_t)r * C + k);
-                }
+            bulk_g2s(b + off, src, (unsigned)bytes, bar);
         }
+        for (int t = lane; t < nv; t += 32) {
+            cp_async16(b + L.vpc + 16 * t, vin + (tok0 + t) * D + c0);
+            cp_async4(b + L.beta + 4 * t, in.beta + tok0 + t);
+        }
+        cp_async_mbar_arrive_noinc(bar);
     };
+
+    if (tid == 0) {
+        mbar_init(full, 33);
+        mbar_init(full + 1, 33);
+        mbar_init(empty, 1);
+        mbar_init(empty + 1, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == NW2) {
+        // producer: stage st is reissued once the compute warps released it (step ls - 2)
+        int issued = 0;
+        for (int ls = 0; ls < nsteps; ++ls) {
+            const int st = ls & 1;
+            if (ls >= 2 && !mbar_wait_bounded(empty + st, (unsigned)((ls - 2) >> 1) & 1u)) {
+                if (lane == 0) atomicCAS(&w.status->code, 0, (int)SDM_ERR_TIMEOUT);
+                break;
+            }
+            issue(ls, st);
+            issued = ls + 1;
+        }
+        // leave only after the last issued copies of both stages have landed
+        for (int ls = issued - 2 < 0 ? 0 : issued - 2; ls < issued; ++ls)
+            mbar_wait_bounded(full + (ls & 1), (unsigned)(ls >> 1) & 1u);
+        cp_async_wait<0>();
+        return;
+    }
 
     int tpt = NT2 / C;
     if (tpt > 32) tpt = 32;
@@ -199,18 +243,14 @@ __global__ void __launch_bounds__(NT2) k_phase2_pipe(Dims d, Inputs in, Work w, 
     const int tpb = NT2 / tpt;
     const int sub = tid % tpt;
 
-    issue(0, 0);
-    cp_async_commit();
     for (int ls = 0; ls < nsteps; ++ls) {
         const int st = ls & 1;
-        if (ls + 1 < nsteps) {
-            issue(ls + 1, st ^ 1);
-            cp_async_commit();
-            cp_async_wait<1>();
-        } else {
-            cp_async_wait<0>();
+        const bool ok = mbar_wait_bounded(full + st, (unsigned)(ls >> 1) & 1u);
+        if (compute_sync_or(!ok)) {
+            // a stage did not land: report and stop (the producer drains its own copies)
+            if (tid == 0) atomicCAS(&w.status->code, 0, (int)SDM_ERR_TIMEOUT);
+            return;
         }
-        __syncthreads();
         const unsigned char *b = psm + st * L.bytes;
         const int32_t *swslot = reinterpret_cast<const int32_t *>(b + L.wslot);
         const float *swgw = reinterpret_cast<const float *>(b + L.wgw);
@@ -222,8 +262,8 @@ __global__ void __launch_bounds__(NT2) k_phase2_pipe(Dims d, Inputs in, Work w, 
         const float *qs = reinterpret_cast<const float *>(b + L.qs);
         const int32_t *sminfo = reinterpret_cast<const int32_t *>(b + L.minfo);
         const float *smdw = reinterpret_cast<const float *>(b + L.mdw);
-        const int32_t *smslot = reinterpret_cast<const int32_t *>(b + L.mslot);
-        const float *smfac = reinterpret_cast<const float *>(b + L.mfac);
+        const int32_t *sgslot = reinterpret_cast<const int32_t *>(b + L.gslot);
+        const float *sgfac = reinterpret_cast<const float *>(b + L.gfac);
         const int ti = step0 + ls;
         const int nv = nvalid_of(ti);
         const size_t tok0 = (size_t)p * d.T + (size_t)ti * C;
@@ -299,7 +339,7 @@ __global__ void __launch_bounds__(NT2) k_phase2_pipe(Dims d, Inputs in, Work w, 
                 }
             }
         }
-        __syncthreads();
+        compute_sync();
 
         // ---- dual matmul on the tensor cores: one warp per (matrix, 16-row tile) ----
         // delta_v = X u_pre (matrix 0) and readings = QX u_pre + inter (matrix 1), over the
@@ -347,7 +387,7 @@ __global__ void __launch_bounds__(NT2) k_phase2_pipe(Dims d, Inputs in, Work w, 
             // rows of whole 16-row tiles past nv were covered; rows from 16 * mt to C are padding
             for (int o = 16 * mt * V + tid; o < C * V; o += NT2) { dvs[o] = 0.f; is[o] = 0.f; }
         }
-        __syncthreads();
+        compute_sync();
         for (int t = tid; t < C; t += NT2) {
             if ((size_t)ti * C + t >= (size_t)d.T) continue;
             float rd[V];
@@ -400,10 +440,10 @@ __global__ void __launch_bounds__(NT2) k_phase2_pipe(Dims d, Inputs in, Work w, 
                 const uint4 braw = b0s[(tinf & 255) * W + ((tinf >> 8) & 255)];
                 float b0[V], o[V];
                 piece_to_f32<BT>(braw, b0);
-                const float fac = smfac[o1 - 1];
+                const float fac = sgfac[g];
 #pragma unroll
                 for (int c = 0; c < V; ++c) o[c] = fmaf(fac, b0[c], acc[c]);
-                const int sl = smslot[o1 - 1];
+                const int sl = sgslot[g];
                 if ((unsigned)sl < S) {
                     store_vec<BT, V>(bank + (size_t)sl * D, o);
                     if (in.snap)
@@ -412,7 +452,8 @@ __global__ void __launch_bounds__(NT2) k_phase2_pipe(Dims d, Inputs in, Work w, 
                 }
             }
         }
-        __syncthreads();
+        compute_sync();
+        if (tid == 0) mbar_arrive(empty + st);   // stage st may be refilled
     }
 }
 
@@ -436,7 +477,7 @@ cudaError_t launch_pipe(const Dims &d, const Inputs &in, const Work &w, int step
     const int grid = d.P * (d.D / (16 / (int)sizeof(BT)));
     auto kern = k_phase2_pipe<BT>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    kern<<<grid, NT2, smem, st>>>(d, in, w, step0, nsteps);
+    kern<<<grid, NP2, smem, st>>>(d, in, w, step0, nsteps);
     return cudaGetLastError();
 }
 
@@ -445,7 +486,7 @@ cudaError_t launch_pipe(const Dims &d, const Inputs &in, const Work &w, int step
 cudaError_t launch_phase2_fused(const Dims &d, const Inputs &in, const Work &w, int step0,
                                 int nsteps, cudaStream_t st) {
     const size_t pipe = phase2_pipe_smem(d);
-    if (pipe > kPipeSmemMax) return cudaErrorInvalidConfiguration;
+    if (pipe > kPipeSmemMax || d.xp != x_pitch(d.C)) return cudaErrorInvalidConfiguration;
     if (d.dtype == SDM_BF16) return launch_pipe<__nv_bfloat16>(d, in, w, step0, nsteps, st, pipe);
     return launch_pipe<float>(d, in, w, step0, nsteps, st, pipe);
 }

@@ -19,6 +19,7 @@ constexpr size_t kAlign = 256;
 constexpr size_t kSlabBudget = size_t(256) << 20;   // per-chunk Phase-1 state held at once
 constexpr size_t kPhase1SmemMax = 200 * 1024;        // Phase-1 scratch kept on chip up to this
 constexpr size_t kPipeSmemMax = 224 * 1024;          // pipelined Phase 2 when two stages fit
+constexpr long kSpinLimit = 1L << 22;   // mbarrier polls before a wait gives up (seconds at most)
 
 // Device status block at the start of the workspace (sdm_device_status, with the first bad
 // token stored +1 so that a zero fill means "none").
@@ -34,7 +35,11 @@ struct Dims {
     int dtype;   // SDM_F32 / SDM_BF16
     int per_step;   // 1: Phase 2 as three kernels per step; 0: one fused kernel per slab
     int bwd;        // 1: Phase 1 also keeps what the backward reads (sorted rows, read plan)
+    int xp;         // row pitch (floats) of X and QX in the workspace: C + 4 for the pipelined
+                    // Phase 2 (one bulk copy lands rows at a bank-conflict-free pitch), else C
 };
+
+inline int x_row_pitch(const Dims &d) { return (d.per_step || d.bwd) ? d.C : d.C + 4; }
 
 // Device pointers of one slab's workspace. N = ns * P chunks; chunk n of the slab is step
 // (step0 + n / P) of stream n % P.
@@ -53,11 +58,13 @@ struct Work {
     float *gw;          // [N][CW]   token-major gather weights of the writes
     float *qw;          // [N][CR]   token-major gather weights of the reads
     int32_t *minfo;     // [N][CW]   sorted position: t | j << 8 | head << 16 | tail << 17
-    int32_t *mslot;     // [N][CW]   slot of each sorted position
-    float *mfac;        // [N][CW]   exp(lend) of the group at its tail position (else 0)
+    int32_t *wsl;       // [N][CW]   token-major write slots (S for a slot outside [0, S) and
+    int32_t *rsl;       // [N][CR]   past the valid entries), read slots likewise: the chunk's
+                        //           slots at an aligned address for bulk copies
     float *lw;          // [N][CW]   token-major running log-decay of the writes
     float *lr;          // [N][CR]   token-major running log-decay of the reads
-    float *A, *QK, *X, *QX;   // [N][C*C]
+    float *A, *QK;      // [N][C*C]
+    float *X, *QX;      // [N][C][xp]
     // Phase-1 scratch, per Phase-1 CTA
     unsigned long long *keys;   // [G][2][CW]
     int32_t *inv;       // [G][CW]  sorted position of each entry
@@ -253,6 +260,57 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+// Bulk global -> shared copies completed on an mbarrier (the TMA unit moves the bytes; one
+// thread issues a copy). Addresses 16-byte aligned, sizes multiples of 16.
+__device__ __forceinline__ unsigned smem_u32(const void *p) {
+    return (unsigned)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(unsigned long long *bar, unsigned count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(unsigned long long *bar, unsigned bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(unsigned long long *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+// arrive on `bar` once every cp.async this thread issued so far has landed (the arrival is
+// counted in the barrier's initial count)
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(unsigned long long *bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, unsigned bytes,
+                                         unsigned long long *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(unsigned long long *bar, unsigned parity) {
+    unsigned ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Waits for the phase of `parity` to complete; false if it did not within kSpinLimit polls.
+__device__ __forceinline__ bool mbar_wait_bounded(unsigned long long *bar, unsigned parity) {
+    for (long it = 0; it < kSpinLimit; ++it)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
 }
 
 __host__ __device__ __forceinline__ int goff_stride(int CW) { return CW + 4; }

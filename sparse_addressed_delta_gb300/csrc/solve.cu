@@ -1,8 +1,8 @@
 // The per-chunk WY solve (sparse-delta-memory 2.0.0, wy_solve.py module docstring):
 //   X = (I + L)^-1 with L = tril(diag(beta) A, -1), and QX = QK X,
-// both dense row-major [C, C] float32 with +0 above the diagonal; rows and columns at or past
-// the chunk's valid tokens are identity rows of X (zero rows of QX), so a ragged chunk is the
-// leading block's inverse.
+// both row-major [C, C] float32 (row pitch Dims::xp, padding zero) with +0 above the diagonal;
+// rows and columns at or past the chunk's valid tokens are identity rows of X (zero rows of
+// QX), so a ragged chunk is the leading block's inverse.
 //
 // Blocked forward substitution, one CTA (256 threads) per chunk, 16 x 16 blocks (nb = C/16):
 //   1. the diagonal blocks D_i = (I + L_ii)^-1 are inverted at once, one thread per column
@@ -35,8 +35,9 @@ __global__ void __launch_bounds__(NTS) k_solve(Dims d, Inputs in, Work w, int st
     const int nvb = (nv + BS - 1) / BS;          // block rows holding valid tokens
     const float *A = w.A + (size_t)n * C * C;
     const float *QK = w.QK + (size_t)n * C * C;
-    float *X = w.X + (size_t)n * C * C;
-    float *QX = w.QX + (size_t)n * C * C;
+    const int xp = d.xp;
+    float *X = w.X + (size_t)n * C * xp;
+    float *QX = w.QX + (size_t)n * C * xp;
     const float *beta = in.beta + (size_t)p * d.T + (size_t)ti * C;
     float *Xp = ssm;                             // packed lower blocks of X
     float *Lr = Xp + tri(nb) * BB;               // current block row of L / QK  [nb][16][16]
@@ -121,9 +122,14 @@ __global__ void __launch_bounds__(NTS) k_solve(Dims d, Inputs in, Work w, int st
             __syncthreads();
         }
         // rows i*16 .. i*16+15 of X and QX (consecutive threads on consecutive columns)
-        for (int e = tid; e < BS * C; e += NTS) {
-            const int r = e / C, u = e - r * C, t = i * BS + r;
+        for (int e = tid; e < BS * xp; e += NTS) {
+            const int r = e / xp, u = e - r * xp, t = i * BS + r;
             if (t >= C) continue;
+            if (u >= C) {   // pitch padding
+                X[(size_t)t * xp + u] = 0.f;
+                QX[(size_t)t * xp + u] = 0.f;
+                continue;
+            }
             float x, q = 0.f;
             if (t < nv && u < nv) {
                 const int j = u / BS;
@@ -132,8 +138,8 @@ __global__ void __launch_bounds__(NTS) k_solve(Dims d, Inputs in, Work w, int st
             } else {
                 x = (t == u) ? 1.f : 0.f;
             }
-            X[(size_t)t * C + u] = x;
-            QX[(size_t)t * C + u] = q;
+            X[(size_t)t * xp + u] = x;
+            QX[(size_t)t * xp + u] = q;
         }
         __syncthreads();
     }

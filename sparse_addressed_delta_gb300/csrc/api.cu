@@ -112,6 +112,7 @@ int phase1_ctas(const Dims &d, int ns) {
     F(wdw, float, N * CW)                                                     \
     F(goff, int32_t, N * (CW + 4))                                            \
     F(ng4, int4, N)                                                           \
+    F(gord, int32_t, N * CW)                                                  \
     F(gslot, int32_t, N * CW)                                                 \
     F(gfac, float, N * CW)                                                    \
     F(ngroups, int32_t, N)                                                    \

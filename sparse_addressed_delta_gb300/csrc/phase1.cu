@@ -260,7 +260,7 @@ __global__ void __launch_bounds__(NT) k_phase1(Dims d, Inputs in, Work w, int st
                 bad = 1;
             }
             kf[i] = kk;
-            wsl[i] = s;
+            wsl[i] = s < S ? s : kNoEntry;
             const int t = div_by(i, magW);
             keyA[i] = ((unsigned long long)(unsigned)s << 32) | ((unsigned)t << 8) |
                       (unsigned)(i - t * W);
@@ -268,7 +268,7 @@ __global__ void __launch_bounds__(NT) k_phase1(Dims d, Inputs in, Work w, int st
         for (int i = tid; i < nr; i += NT) {
             const int r = rs[i];
             if ((unsigned)r >= (unsigned)S) report_bad_slot(w.status, (int)(tok_base + i / R));
-            rsl[i] = (unsigned)r < (unsigned)S ? r : S;
+            rsl[i] = (unsigned)r < (unsigned)S ? r : kNoEntry;
         }
         // slot S may need one more radix digit than the real slots
         const int npass = __syncthreads_or(bad) ? (32 - __clz(S) + 7) / 8 : passes;
@@ -322,7 +322,6 @@ __global__ void __launch_bounds__(NT) k_phase1(Dims d, Inputs in, Work w, int st
         const int ng = carry_i;
         if (tid == 0) {
             w.ngroups[n] = ng;
-            w.ng4[n] = make_int4(ng, 0, 0, 0);
             w.nvalid[n] = nv;
             goff[ng] = nw;
         }
@@ -490,10 +489,30 @@ __global__ void __launch_bounds__(NT) k_phase1(Dims d, Inputs in, Work w, int st
             if (tid == 0) { w.rng[n] = rcarry; rgoff[rcarry] = nr; }
             __syncthreads();
         }
-        for (int i = nw + tid; i < CW; i += NT) {
-            perm[i] = -1; gw[i] = 0.f; lw[i] = 0.f; wdw[i] = 0.f; wsl[i] = S;
+        // 6. the DW order for the pipelined Phase 2: one stable radix pass over a size digit
+        //    (0 for a group of >= kHotGroup members, else 1 + kHotGroup - size) in the free
+        //    radix buffers
+        __syncthreads();   // the Gram rows are done with the (token, k) buffer
+        {
+            unsigned long long *ka = keyA, *kb = keyB;
+            int hot = 0;
+            for (int g = tid; g < ng; g += NT) {
+                const int sz = goff[g + 1] - goff[g];
+                const unsigned dig = sz >= kHotGroup ? 0u : (unsigned)(1 + kHotGroup - sz);
+                hot += sz >= kHotGroup;
+                ka[g] = ((unsigned long long)dig << 32) | (unsigned)g;
+            }
+            int nhot;
+            int_scan(hot, 0, nhot, sm);
+            radix_pass(ka, kb, ng, 32, sm);
+            int32_t *go = w.gord + (size_t)n * CW;
+            for (int i = tid; i < ng; i += NT) go[i] = (int)(unsigned)kb[i];
+            if (tid == 0) w.ng4[n] = make_int4(ng, nhot, 0, 0);
         }
-        for (int i = nr + tid; i < CR; i += NT) { qw[i] = 0.f; lr[i] = 0.f; rsl[i] = S; }
+        for (int i = nw + tid; i < CW; i += NT) {
+            perm[i] = -1; gw[i] = 0.f; lw[i] = 0.f; wdw[i] = 0.f; wsl[i] = kNoEntry;
+        }
+        for (int i = nr + tid; i < CR; i += NT) { qw[i] = 0.f; lr[i] = 0.f; rsl[i] = kNoEntry; }
         __syncthreads();
     }
 }

@@ -51,7 +51,7 @@ __device__ __forceinline__ bool compute_sync_or(bool v) {
 }
 
 struct StageLayout {     // byte offsets inside one stage (every array 16-byte aligned)
-    int wslot, wgw, rslot, rqw, minfo, mdw, gslot, gfac, goff, scal, xs, qs, vpc, beta, bytes;
+    int wslot, wgw, rslot, rqw, minfo, mdw, gslot, gfac, goff, gord, scal, xs, qs, vpc, beta, bytes;
 };
 
 __host__ __device__ inline int align16(int x) { return (x + 15) & ~15; }
@@ -71,6 +71,7 @@ __host__ __device__ inline StageLayout stage_layout(int C, int W, int R) {
     L.gslot = o; o = align16(o + 4 * CW);
     L.gfac = o; o = align16(o + 4 * CW);
     L.goff = o; o = align16(o + 4 * goff_stride(CW));
+    L.gord = o; o = align16(o + 4 * CW);
     L.scal = o; o = align16(o + 16);
     L.xs = o; o = align16(o + 4 * C * XP);
     L.qs = o; o = align16(o + 4 * C * XP);
@@ -83,13 +84,17 @@ __host__ __device__ inline StageLayout stage_layout(int C, int W, int R) {
 // Bytes the bulk copies of one stage move (everything before vpc; X and QX whole, padded rows)
 __host__ __device__ inline unsigned stage_bulk_bytes(int C, int W, int R) {
     const int CW = C * W, CR = C * R;
-    return (unsigned)(4 * (6 * CW + 2 * CR + goff_stride(CW)) + 16 + 2 * 4 * C * x_pitch(C));
+    return (unsigned)(4 * (7 * CW + 2 * CR + goff_stride(CW)) + 16 + 2 * 4 * C * x_pitch(C));
 }
 
-// Bytes after the two stages: u_pre, inter, delta_v [C][V] f32, the B0 pieces [CW][16 B] and
-// the stage mbarriers (full[2], empty[2]).
+// delta_v rows in shared memory are kDvPitch floats apart: 48 bytes spread a warp's random-row
+// 16-byte reads over all eight 16-byte bank groups
+constexpr int kDvPitch = 12;
+
+// Bytes after the two stages: u_pre, inter [C][V] f32, delta_v [C][kDvPitch] f32, the B0 pieces
+// [CW][16 B], the DW's new piece per group [CW][16 B] and the stage mbarriers (full[2], empty[2]).
 __host__ __device__ inline int pipe_tail_bytes(int C, int W, int V) {
-    return 3 * 4 * C * V + 16 * C * W + 32;
+    return 2 * 4 * C * V + 4 * C * kDvPitch + 2 * 16 * C * W + 32;
 }
 
 // ---------------------------------------------------------------------------------------
@@ -131,6 +136,58 @@ __device__ __forceinline__ void piece_to_f32(const uint4 &u, float (&o)[16 / siz
     }
 }
 
+// the 16-byte bank piece of V floats, rounded to the bank type exactly as store_vec does
+template <typename BT>
+__device__ __forceinline__ uint4 pack_piece(const float (&o)[16 / sizeof(BT)]) {
+    alignas(16) BT tmp[16 / sizeof(BT)];
+#pragma unroll
+    for (int k = 0; k < (int)(16 / sizeof(BT)); ++k) tmp[k] = from_f32<BT>(o[k]);
+    return *reinterpret_cast<const uint4 *>(tmp);
+}
+
+// a += w * x for two columns at once (one packed FFMA2, each half rounded like fmaf)
+__device__ __forceinline__ void fma2(float &a0, float &a1, float w, float x0, float x1) {
+    const float2 r = __ffma2_rn(make_float2(w, w), make_float2(x0, x1), make_float2(a0, a1));
+    a0 = r.x;
+    a1 = r.y;
+}
+
+template <int V>
+__device__ __forceinline__ void add_piece(float (&acc)[V], float w, const float (&x)[V]) {
+#pragma unroll
+    for (int c = 0; c < V; c += 2) fma2(acc[c], acc[c + 1], w, x[c], x[c + 1]);
+}
+
+// Reduce-scatter of N values over the 2 * off lanes of a group (xor butterflies, off halving):
+// at each level a lane keeps the half its lane bit selects and adds the partner's copy of it,
+// so the levels move N/2, N/4, ... values instead of N. When one value is left, further
+// levels add it across the remaining lanes and only the lowest of them emits it. Calls
+// emit(index in 0..N-1, sum) for every value the lane ends up owning. Fixed order: bitwise
+// reproducible.
+template <int N, typename F>
+__device__ __forceinline__ void reduce_scatter(float (&v)[N], int off, int lane, int base, F &&emit) {
+    if constexpr (N == 1) {
+        const int span = off;   // lanes below this bit hold copies after the butterflies
+        for (; off > 0; off >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
+        if (span == 0 || (lane & (2 * span - 1)) == 0) emit(base, v[0]);
+    } else {
+        if (off == 0) {
+#pragma unroll
+            for (int i = 0; i < N; ++i) emit(base + i, v[i]);
+            return;
+        }
+        const bool up = (lane & off) != 0;
+        float h[N / 2];
+#pragma unroll
+        for (int i = 0; i < N / 2; ++i) {
+            const float send = up ? v[i] : v[i + N / 2];
+            const float keep = up ? v[i + N / 2] : v[i];
+            h[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+        reduce_scatter<N / 2>(h, off >> 1, lane, base + (up ? N / 2 : 0), emit);
+    }
+}
+
 template <typename BT>
 __global__ void __launch_bounds__(NP2) k_phase2_pipe(Dims d, Inputs in, Work w, int step0,
                                                     int nsteps) {
@@ -146,11 +203,12 @@ __global__ void __launch_bounds__(NP2) k_phase2_pipe(Dims d, Inputs in, Work w, 
 
     float *us = reinterpret_cast<float *>(psm + 2 * L.bytes);   // [C][V]
     float *is = us + C * V;                                      // [C][V]
-    float *dvs = is + C * V;                                     // [C][V]
-    uint4 *b0s = reinterpret_cast<uint4 *>(dvs + C * V);         // [CW] B0 pieces (raw)
+    float *dvs = is + C * V;                                     // [C][kDvPitch]
+    uint4 *b0s = reinterpret_cast<uint4 *>(dvs + C * kDvPitch);  // [CW] B0 pieces (raw)
+    uint4 *dwout = b0s + CW;                                      // [CW] new piece per group
     // full[st]: stage st landed (1 expect-tx arrival + 32 producer-lane cp.async arrivals and
     // the bulk bytes); empty[st]: the compute warps are done with stage st (1 arrival)
-    unsigned long long *full = reinterpret_cast<unsigned long long *>(b0s + CW);
+    unsigned long long *full = reinterpret_cast<unsigned long long *>(dwout + CW);
     unsigned long long *empty = full + 2;
 
     BT *bank = static_cast<BT *>(in.bank) + (size_t)p * d.S * D + c0;
@@ -166,7 +224,7 @@ __global__ void __launch_bounds__(NP2) k_phase2_pipe(Dims d, Inputs in, Work w, 
         return r < 0 ? 0 : (r > C ? C : r);
     };
 
-    // stage st for step ls, issued by the producer warp: lanes 0..11 bulk-copy the workspace
+    // stage st for step ls, issued by the producer warp: lanes 0..12 bulk-copy the workspace
     // arrays (16-byte aligned chunk offsets, C % 16 == 0), every lane cp.asyncs the v pieces and
     // beta of its tokens and then arrives on full[st] when those have landed
     auto issue = [&](int ls, int st) {
@@ -178,7 +236,7 @@ __global__ void __launch_bounds__(NP2) k_phase2_pipe(Dims d, Inputs in, Work w, 
         unsigned long long *bar = full + st;
         if (lane == 0) mbar_arrive_expect_tx(bar, stage_bulk_bytes(C, W, R));
         __syncwarp();
-        if (lane < 12) {
+        if (lane < 13) {
             const void *src;
             int off, bytes;
             switch (lane) {
@@ -197,6 +255,11 @@ __global__ void __launch_bounds__(NP2) k_phase2_pipe(Dims d, Inputs in, Work w, 
                     break;
                 case 9: src = w.ng4 + n; off = L.scal; bytes = 16; break;
                 case 10: src = w.X + (size_t)n * C * XP; off = L.xs; bytes = 4 * C * XP; break;
+                case 11:
+                    src = w.gord + (size_t)n * CW;
+                    off = L.gord;
+                    bytes = 4 * CW;
+                    break;
                 default: src = w.QX + (size_t)n * C * XP; off = L.qs; bytes = 4 * C * XP; break;
             }
             bulk_g2s(b + off, src, (unsigned)bytes, bar);
@@ -236,12 +299,44 @@ __global__ void __launch_bounds__(NP2) k_phase2_pipe(Dims d, Inputs in, Work w, 
         return;
     }
 
+    // gather mapping: token gt = tid / tpt, its W + R entries (writes first) split over tpt
+    // lanes (q = sub, sub + tpt, ...); tpt is a power of two with tpt * C <= NT2, so one pass
+    // covers every token
     int tpt = NT2 / C;
     if (tpt > 32) tpt = 32;
     if (tpt < 1) tpt = 1;
     while (tpt & (tpt - 1)) tpt &= tpt - 1;
-    const int tpb = NT2 / tpt;
     const int sub = tid % tpt;
+    const int gt = tid / tpt;
+    const int E = W + R;
+
+    // The first PF entries of a lane are fetched one step ahead: while step ls computes, the
+    // pieces of step ls + 1 are loaded into registers, except for entries linked to a group of
+    // step ls (its slot is written there), which take that group's new piece from dwout. Every
+    // other bank row is final for step ls + 1 once step ls - 1 has ended, so the early load
+    // reads the right value.
+    constexpr int PF = 4;
+    uint4 pf[PF];
+    int lk[PF];   // -2: no entry; -1: piece in pf; >= 0: dwout[lk]
+    auto prefetch = [&](int ls_n, const unsigned char *bn) {
+        const int nvn = nvalid_of(step0 + ls_n);
+        const int32_t *wsl = reinterpret_cast<const int32_t *>(bn + L.wslot) + gt * W;
+        const int32_t *rsl = reinterpret_cast<const int32_t *>(bn + L.rslot) + gt * R;
+#pragma unroll
+        for (int k = 0; k < PF; ++k) {
+            const int q = sub + k * tpt;
+            lk[k] = -2;
+            if (gt < nvn && q < E) {
+                const int v = q < W ? wsl[q] : rsl[q - W];
+                if (v >= 0) {
+                    lk[k] = -1;
+                    pf[k] = *reinterpret_cast<const uint4 *>(bank + (size_t)v * D);
+                } else if (v != kNoEntry) {
+                    lk[k] = -1 - v;
+                }
+            }
+        }
+    };
 
     for (int ls = 0; ls < nsteps; ++ls) {
         const int st = ls & 1;
@@ -267,35 +362,52 @@ __global__ void __launch_bounds__(NP2) k_phase2_pipe(Dims d, Inputs in, Work w, 
         const int ti = step0 + ls;
         const int nv = nvalid_of(ti);
         const size_t tok0 = (size_t)p * d.T + (size_t)ti * C;
+        if (ls == 0) prefetch(0, b);
 
         // ---- gather (the write pieces are also kept as B0 for the DW) ----
-        // The token's W + R entries (writes first) are split over its tpt lanes; each lane
-        // issues up to GB loads before using any, and adds them in entry order.
-        constexpr int GB = 8;
-        const int E = W + R;
-        for (int tb = 0; tb < C; tb += tpb) {
-            const int t = tb + tid / tpt;
+        // each lane adds its entries in entry order: the PF early ones, then the rest fetched
+        // now, GB at a time before any is used; a shuffle tree then sums the token's lanes
+        {
+            constexpr int GB = 4;
             float ar[V], ai[V];
 #pragma unroll
             for (int c = 0; c < V; ++c) { ar[c] = 0.f; ai[c] = 0.f; }
-            if (t < nv) {
-                const int32_t *wsl = swslot + t * W;
-                const float *wg = swgw + t * W;
-                const int32_t *rsl = srslot + t * R;
-                const float *rq = srqw + t * R;
-                for (int q0 = sub; q0 < E; q0 += GB * tpt) {
+            if (gt < nv) {
+                const int32_t *wsl = swslot + gt * W;
+                const float *wg = swgw + gt * W;
+                const int32_t *rsl = srslot + gt * R;
+                const float *rq = srqw + gt * R;
+#pragma unroll
+                for (int k = 0; k < PF; ++k) {
+                    const int q = sub + k * tpt;
+                    if (q < E) {
+                        const uint4 u = lk[k] >= 0 ? dwout[lk[k]]
+                                                   : (lk[k] == -1 ? pf[k] : make_uint4(0u, 0u, 0u, 0u));
+                        if (q < W) b0s[gt * W + q] = u;
+                        if (lk[k] != -2) {
+                            float x[V];
+                            piece_to_f32<BT>(u, x);
+                            if (q < W) add_piece<V>(ar, wg[q], x);
+                            else add_piece<V>(ai, rq[q - W], x);
+                        }
+                    }
+                }
+                for (int q0 = sub + PF * tpt; q0 < E; q0 += GB * tpt) {
                     uint4 u[GB];
-                    float wt[GB];
+                    bool has[GB];
 #pragma unroll
                     for (int k = 0; k < GB; ++k) {
                         const int q = q0 + k * tpt;
                         u[k] = make_uint4(0u, 0u, 0u, 0u);
-                        wt[k] = 0.f;
+                        has[k] = false;
                         if (q < E) {
-                            const int sl = q < W ? wsl[q] : rsl[q - W];
-                            if ((unsigned)sl < S) {
-                                wt[k] = q < W ? wg[q] : rq[q - W];
-                                u[k] = *reinterpret_cast<const uint4 *>(bank + (size_t)sl * D);
+                            const int v = q < W ? wsl[q] : rsl[q - W];
+                            if (v >= 0) {
+                                u[k] = *reinterpret_cast<const uint4 *>(bank + (size_t)v * D);
+                                has[k] = true;
+                            } else if (v != kNoEntry) {
+                                u[k] = dwout[-1 - v];
+                                has[k] = true;
                             }
                         }
                     }
@@ -303,41 +415,30 @@ __global__ void __launch_bounds__(NP2) k_phase2_pipe(Dims d, Inputs in, Work w, 
                     for (int k = 0; k < GB; ++k) {
                         const int q = q0 + k * tpt;
                         if (q < E) {
-                            float x[V];
-                            piece_to_f32<BT>(u[k], x);
-                            if (q < W) {
-                                b0s[t * W + q] = u[k];
-#pragma unroll
-                                for (int c = 0; c < V; ++c) ar[c] = fmaf(wt[k], x[c], ar[c]);
-                            } else {
-#pragma unroll
-                                for (int c = 0; c < V; ++c) ai[c] = fmaf(wt[k], x[c], ai[c]);
+                            if (q < W) b0s[gt * W + q] = u[k];
+                            if (has[k]) {
+                                float x[V];
+                                piece_to_f32<BT>(u[k], x);
+                                if (q < W) add_piece<V>(ar, wg[q], x);
+                                else add_piece<V>(ai, rq[q - W], x);
                             }
                         }
                     }
                 }
             }
-            for (int off = tpt >> 1; off > 0; off >>= 1) {
+            // sum over the token's lanes; each lane ends with a share of the 2V sums
+            // (retrieved columns 0..V-1, then inter) and writes u_pre / inter for it
+            float val[2 * V];
 #pragma unroll
-                for (int c = 0; c < V; ++c) {
-                    ar[c] += __shfl_down_sync(0xffffffffu, ar[c], off, tpt);
-                    ai[c] += __shfl_down_sync(0xffffffffu, ai[c], off, tpt);
-                }
-            }
-            if (sub == 0 && t < C) {
-                if (t < nv) {
-                    const BT *vp16 = svpc + t * V;
-                    const float bt = sbeta[t];
-#pragma unroll
-                    for (int c = 0; c < V; ++c) {
-                        us[t * V + c] = bt * (to_f32(vp16[c]) - ar[c]);
-                        is[t * V + c] = ai[c];
-                    }
-                } else {
-#pragma unroll
-                    for (int c = 0; c < V; ++c) { us[t * V + c] = 0.f; is[t * V + c] = 0.f; }
-                }
-            }
+            for (int c = 0; c < V; ++c) { val[c] = ar[c]; val[V + c] = ai[c]; }
+            const bool live = gt < nv;
+            const BT *vp16 = svpc + gt * V;
+            const float bt = live ? sbeta[gt] : 0.f;
+            reduce_scatter<2 * V>(val, tpt >> 1, lane, 0, [&](int idx, float x) {
+                if (gt >= C) return;
+                if (idx < V) us[gt * V + idx] = live ? bt * (to_f32(vp16[idx]) - x) : 0.f;
+                else is[gt * V + idx - V] = live ? x : 0.f;
+            });
         }
         compute_sync();
 
@@ -379,15 +480,27 @@ __global__ void __launch_bounds__(NP2) k_phase2_pipe(Dims d, Inputs in, Work w, 
                     const int t = r0 + g4 + (q >> 1) * 8, col = 2 * i4 + (q & 1);
                     if (col < V && t < C) {
                         const float val = t < nv ? c[q] : 0.f;
-                        if (mat == 0) dvs[t * V + col] = val;
+                        if (mat == 0) dvs[t * kDvPitch + col] = val;
                         else is[t * V + col] = t < nv ? val + is[t * V + col] : 0.f;
                     }
                 }
             }
             // rows of whole 16-row tiles past nv were covered; rows from 16 * mt to C are padding
-            for (int o = 16 * mt * V + tid; o < C * V; o += NT2) { dvs[o] = 0.f; is[o] = 0.f; }
+            for (int o = 16 * mt * V + tid; o < C * V; o += NT2) {
+                dvs[(o / V) * kDvPitch + o % V] = 0.f;
+                is[o] = 0.f;
+            }
         }
-        compute_sync();
+        // ---- early loads of step ls + 1 (warps without a matmul tile start at once) ----
+        bool ok_next = true;
+        if (ls + 1 < nsteps) {
+            ok_next = mbar_wait_bounded(full + (st ^ 1), (unsigned)((ls + 1) >> 1) & 1u);
+            if (ok_next) prefetch(ls + 1, psm + (st ^ 1) * L.bytes);
+        }
+        if (compute_sync_or(!ok_next)) {
+            if (tid == 0) atomicCAS(&w.status->code, 0, (int)SDM_ERR_TIMEOUT);
+            return;
+        }
         for (int t = tid; t < C; t += NT2) {
             if ((size_t)ti * C + t >= (size_t)d.T) continue;
             float rd[V];
@@ -396,46 +509,17 @@ __global__ void __launch_bounds__(NP2) k_phase2_pipe(Dims d, Inputs in, Work w, 
             store_vec<BT, V>(out + (tok0 + t) * D + c0, rd);
         }
 
-        // ---- DW: one thread per group (distinct written slot), members in sorted order ----
+        // ---- DW: B[s] = (sum of dw * delta_v over the group's members, sorted order) +
+        //      exp(lend) * B0[s], one writer per written slot. A group of >= kHotGroup members
+        //      gets a warp (lane l adds members l, l + 32, ..., then a fixed xor tree); every
+        //      other group a thread (members in order), in Phase 1's size order. ----
         {
             const int32_t *sgoff = reinterpret_cast<const int32_t *>(b + L.goff);
-            const int ng = nv > 0 ? *reinterpret_cast<const int32_t *>(b + L.scal) : 0;
-            for (int g = tid; g < ng; g += NT2) {
-                const int o0 = sgoff[g], o1 = sgoff[g + 1];
-                float acc[V];
-#pragma unroll
-                for (int c = 0; c < V; ++c) acc[c] = 0.f;
-                int m = o0;
-                for (; m + 4 <= o1; m += 4) {
-                    int inf[4];
-                    float wt[4];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) { inf[q] = sminfo[m + q]; wt[q] = smdw[m + q]; }
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const float4 *dv4 = reinterpret_cast<const float4 *>(dvs + (inf[q] & 255) * V);
-#pragma unroll
-                        for (int h = 0; h < V / 4; ++h) {
-                            const float4 x = dv4[h];
-                            acc[4 * h + 0] = fmaf(wt[q], x.x, acc[4 * h + 0]);
-                            acc[4 * h + 1] = fmaf(wt[q], x.y, acc[4 * h + 1]);
-                            acc[4 * h + 2] = fmaf(wt[q], x.z, acc[4 * h + 2]);
-                            acc[4 * h + 3] = fmaf(wt[q], x.w, acc[4 * h + 3]);
-                        }
-                    }
-                }
-                for (; m < o1; ++m) {
-                    const float wt = smdw[m];
-                    const float4 *dv4 = reinterpret_cast<const float4 *>(dvs + (sminfo[m] & 255) * V);
-#pragma unroll
-                    for (int h = 0; h < V / 4; ++h) {
-                        const float4 x = dv4[h];
-                        acc[4 * h + 0] = fmaf(wt, x.x, acc[4 * h + 0]);
-                        acc[4 * h + 1] = fmaf(wt, x.y, acc[4 * h + 1]);
-                        acc[4 * h + 2] = fmaf(wt, x.z, acc[4 * h + 2]);
-                        acc[4 * h + 3] = fmaf(wt, x.w, acc[4 * h + 3]);
-                    }
-                }
+            const int4 sc = *reinterpret_cast<const int4 *>(b + L.scal);
+            const int ng = nv > 0 ? sc.x : 0, nhot = nv > 0 ? sc.y : 0;
+            const int32_t *sgord = reinterpret_cast<const int32_t *>(b + L.gord);
+            // the group's row: B0 from the gather, the new piece to the bank and to dwout
+            auto finish = [&](int g, int o1, const float (&acc)[V]) {
                 const int tinf = sminfo[o1 - 1];
                 const uint4 braw = b0s[(tinf & 255) * W + ((tinf >> 8) & 255)];
                 float b0[V], o[V];
@@ -445,11 +529,53 @@ __global__ void __launch_bounds__(NP2) k_phase2_pipe(Dims d, Inputs in, Work w, 
                 for (int c = 0; c < V; ++c) o[c] = fmaf(fac, b0[c], acc[c]);
                 const int sl = sgslot[g];
                 if ((unsigned)sl < S) {
-                    store_vec<BT, V>(bank + (size_t)sl * D, o);
+                    const uint4 packed = pack_piece<BT>(o);
+                    *reinterpret_cast<uint4 *>(bank + (size_t)sl * D) = packed;
+                    dwout[g] = packed;
                     if (in.snap)
                         *reinterpret_cast<uint4 *>(static_cast<BT *>(in.snap) +
                                                    ((size_t)(ti * d.P + p) * CW + (o1 - 1)) * D + c0) = braw;
                 }
+            };
+            auto add_member = [&](int m, float (&acc)[V]) {
+                const float wt = smdw[m];
+                const float4 *dv4 =
+                    reinterpret_cast<const float4 *>(dvs + (sminfo[m] & 255) * kDvPitch);
+#pragma unroll
+                for (int h = 0; h < V / 4; ++h) {
+                    const float4 x = dv4[h];
+                    fma2(acc[4 * h + 0], acc[4 * h + 1], wt, x.x, x.y);
+                    fma2(acc[4 * h + 2], acc[4 * h + 3], wt, x.z, x.w);
+                }
+            };
+            for (int h = warp; h < nhot; h += NW2) {
+                const int g = sgord[h];
+                const int o0 = sgoff[g], o1 = sgoff[g + 1];
+                float acc[V];
+#pragma unroll
+                for (int c = 0; c < V; ++c) acc[c] = 0.f;
+                for (int m = o0 + lane; m < o1; m += 32) add_member(m, acc);
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+                    for (int c = 0; c < V; ++c) acc[c] += __shfl_xor_sync(0xffffffffu, acc[c], off);
+                if (lane == 0) finish(g, o1, acc);
+            }
+            // the other groups, largest first, so that a warp's lanes loop about equally long;
+            // they start at the last thread, away from the warps that took a hot group
+            for (int i = nhot + (NT2 - 1 - tid); i < ng; i += NT2) {
+                const int g = sgord[i];
+                const int o0 = sgoff[g], o1 = sgoff[g + 1];
+                float acc[V];
+#pragma unroll
+                for (int c = 0; c < V; ++c) acc[c] = 0.f;
+                int m = o0;
+                for (; m + 4 <= o1; m += 4) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) add_member(m + q, acc);
+                }
+                for (; m < o1; ++m) add_member(m, acc);
+                finish(g, o1, acc);
             }
         }
         compute_sync();

@@ -20,6 +20,7 @@ constexpr size_t kSlabBudget = size_t(256) << 20;   // per-chunk Phase-1 state h
 constexpr size_t kPhase1SmemMax = 200 * 1024;        // Phase-1 scratch kept on chip up to this
 constexpr size_t kPipeSmemMax = 224 * 1024;          // pipelined Phase 2 when two stages fit
 constexpr long kSpinLimit = 1L << 22;   // mbarrier polls before a wait gives up (seconds at most)
+constexpr int32_t kNoEntry = INT32_MIN;  // Work::wsl / rsl: no entry
 
 // Device status block at the start of the workspace (sdm_device_status, with the first bad
 // token stored +1 so that a zero fill means "none").
@@ -50,7 +51,9 @@ struct Work {
     float *wdw;         // [N][CW]   DW weight at each sorted position
     int32_t *goff;      // [N][CW+4] group start positions, goff[ngroups] = n_entries (the
                         //           stride keeps every chunk's row 16-byte aligned)
-    int4 *ng4;          // [N]       (ngroups, 0, 0, 0): the group count as one 16-byte word
+    int4 *ng4;          // [N]       (ngroups, hot groups, 0, 0) as one 16-byte word
+    int32_t *gord;      // [N][CW]   DW order: the groups of >= kHotGroup members (ascending),
+                        //           then the others by size, largest first (ascending within)
     int32_t *gslot;     // [N][CW]   slot of each group
     float *gfac;        // [N][CW]   exp(lend) of each group
     int32_t *ngroups;   // [N]
@@ -58,9 +61,12 @@ struct Work {
     float *gw;          // [N][CW]   token-major gather weights of the writes
     float *qw;          // [N][CR]   token-major gather weights of the reads
     int32_t *minfo;     // [N][CW]   sorted position: t | j << 8 | head << 16 | tail << 17
-    int32_t *wsl;       // [N][CW]   token-major write slots (S for a slot outside [0, S) and
-    int32_t *rsl;       // [N][CR]   past the valid entries), read slots likewise: the chunk's
-                        //           slots at an aligned address for bulk copies
+    // token-major source of each entry's B0 piece for the pipelined Phase 2 (bulk-copied):
+    // v >= 0 the bank row v; v = -1 - g: the new piece of group g of the same stream's previous
+    // step in the slab (that step wrote the row); kNoEntry: no entry (slot outside [0, S) or a
+    // token past the valid ones). Phase 1 writes the slots, the solve kernel the links.
+    int32_t *wsl;       // [N][CW]
+    int32_t *rsl;       // [N][CR]
     float *lw;          // [N][CW]   token-major running log-decay of the writes
     float *lr;          // [N][CR]   token-major running log-decay of the reads
     float *A, *QK;      // [N][C*C]
@@ -314,6 +320,8 @@ __device__ __forceinline__ bool mbar_wait_bounded(unsigned long long *bar, unsig
 }
 
 __host__ __device__ __forceinline__ int goff_stride(int CW) { return CW + 4; }
+// a group with at least kHotGroup members is summed by a whole warp in the pipelined DW
+constexpr int kHotGroup = 16;
 
 __device__ __forceinline__ int chunk_valid(const int32_t *valid, int p, int T, int tok0, int C) {
     int v = valid ? valid[p] : T;

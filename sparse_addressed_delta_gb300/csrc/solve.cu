@@ -4,6 +4,9 @@
 // rows and columns at or past the chunk's valid tokens are identity rows of X (zero rows of
 // QX), so a ragged chunk is the leading block's inverse.
 //
+// The same CTA also links the chunk's entries to the previous step's groups for the pipelined
+// Phase 2 (see below).
+//
 // Blocked forward substitution, one CTA (256 threads) per chunk, 16 x 16 blocks (nb = C/16):
 //   1. the diagonal blocks D_i = (I + L_ii)^-1 are inverted at once, one thread per column
 //      of a block (forward substitution inside 16 rows);
@@ -42,6 +45,28 @@ __global__ void __launch_bounds__(NTS) k_solve(Dims d, Inputs in, Work w, int st
     float *Xp = ssm;                             // packed lower blocks of X
     float *Lr = Xp + tri(nb) * BB;               // current block row of L / QK  [nb][16][16]
     float *Tb = Lr + nb * BB;                    // T blocks                     [nb][16][16]
+
+    // Links for the pipelined Phase 2 (every chunk after the first of the slab): an entry
+    // whose slot the stream's previous step writes is pointed at that group's new piece
+    // (-1 - g) instead of the bank row. The previous chunk's groups are sorted by slot.
+    if (!d.per_step && !d.bwd && n >= d.P) {
+        const int CW = C * d.W, CR = C * d.R, np = n - d.P;
+        const int ngp = w.ngroups[np];
+        const int32_t *gsp = w.gslot + (size_t)np * CW;
+        int32_t *wsl = w.wsl + (size_t)n * CW;
+        int32_t *rsl = w.rsl + (size_t)n * CR;
+        for (int i = tid; i < CW + CR; i += NTS) {
+            int32_t *ent = i < CW ? wsl + i : rsl + (i - CW);
+            const int v = *ent;
+            if (v < 0) continue;
+            int lo = 0, hi = ngp;
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (gsp[mid] < v) lo = mid + 1; else hi = mid;
+            }
+            if (lo < ngp && gsp[lo] == v) *ent = -1 - lo;
+        }
+    }
 
     // L (or QK) element (R, K) of the chunk, zero outside the valid tokens
     auto lval = [&](int R, int K) {

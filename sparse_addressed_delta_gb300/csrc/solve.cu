@@ -14,7 +14,8 @@
 //      elements in parallel), then X_ij = -D_i T_ij;
 //   3. QX_ij = sum_{k=j}^{i} QK_ik X_kj for every lower block, block row by block row.
 // X lives in shared memory as packed lower blocks (nb(nb+1)/2 x 1 KB: 136 KB at C = 256); the
-// current block row of L (or QK) and the T blocks are staged next to it. Every product is full
+// current block row of L (or QK) and the T blocks are staged next to it; for C <= 32 the
+// chunk's A, QK and beta are first copied on chip whole. Every product is full
 // float32 FFMA in a fixed order: the inverse amplifies rounding, so no reduced-precision path.
 #include "sdm_internal.cuh"
 
@@ -27,8 +28,44 @@ constexpr int BB = BS * BS;            // floats per block
 
 __host__ __device__ __forceinline__ int tri(int i) { return i * (i + 1) / 2; }
 
+// links are written for the pipelined Phase 2 only
+__host__ __device__ __forceinline__ bool solve_links(const Dims &d) { return !d.per_step && !d.bwd; }
+// A, QK and beta of the chunk are copied on chip first for small chunks (one round of loads
+// instead of one per block row); from C = 64 on the copies would cost more in CTAs per SM
+// than they save
+__host__ __device__ __forceinline__ bool solve_staged(const Dims &d) { return d.C <= 32 && d.C % 4 == 0; }
+__host__ __device__ __forceinline__ int staged_pitch(int C) { return C + 4; }
+
+// dynamic shared memory: X blocks, L/QK block row, T blocks; then (staged) A, QK [C][C+4] and
+// beta [C]; then (links) the previous chunk's group slots [CW] and this chunk's entries
+// [CW + CR]
+struct SolveSmem {
+    size_t a, q, beta, gsl, ent, bytes;
+};
+__host__ __device__ inline SolveSmem solve_layout(const Dims &d) {
+    const int nb = (d.C + BS - 1) / BS;
+    SolveSmem L;
+    size_t o = sizeof(float) * (size_t)(tri(nb) + 2 * nb) * BB;
+    L.a = L.q = L.beta = L.gsl = L.ent = o;
+    if (solve_staged(d)) {
+        const size_t m = sizeof(float) * (size_t)d.C * staged_pitch(d.C);
+        L.a = o; o += m;
+        L.q = o; o += m;
+        L.beta = o; o += sizeof(float) * (size_t)d.C;
+    }
+    if (solve_links(d)) {
+        const size_t CW = (size_t)d.C * d.W, CR = (size_t)d.C * d.R;
+        L.gsl = o; o += sizeof(int32_t) * CW;
+        L.ent = o; o += sizeof(int32_t) * (CW + CR);
+    }
+    L.bytes = o;
+    return L;
+}
+
 __global__ void __launch_bounds__(NTS) k_solve(Dims d, Inputs in, Work w, int step0, int nsteps) {
     extern __shared__ __align__(16) float ssm[];
+    unsigned char *sraw = reinterpret_cast<unsigned char *>(ssm);
+    const SolveSmem SL = solve_layout(d);
     const int C = d.C;
     const int nb = (C + BS - 1) / BS;
     const int n = blockIdx.x;
@@ -46,47 +83,97 @@ __global__ void __launch_bounds__(NTS) k_solve(Dims d, Inputs in, Work w, int st
     float *Lr = Xp + tri(nb) * BB;               // current block row of L / QK  [nb][16][16]
     float *Tb = Lr + nb * BB;                    // T blocks                     [nb][16][16]
 
+    // staged copies of the valid rows of A and QK and of beta (cp.async, 16 bytes a copy)
+    const bool staged = solve_staged(d);
+    int ap = C;
+    if (staged) {
+        float *As = reinterpret_cast<float *>(sraw + SL.a);
+        float *Qs = reinterpret_cast<float *>(sraw + SL.q);
+        float *bs = reinterpret_cast<float *>(sraw + SL.beta);
+        ap = staged_pitch(C);
+        const int q4 = C / 4;
+        for (int i = tid; i < nv * q4; i += NTS) {
+            const int r = i / q4, k = (i - r * q4) * 4;
+            cp_async16(As + r * ap + k, A + (size_t)r * C + k);
+            cp_async16(Qs + r * ap + k, QK + (size_t)r * C + k);
+        }
+        for (int r = tid; r < nv; r += NTS) cp_async4(bs + r, beta + r);
+        cp_async_commit();
+        A = As;
+        QK = Qs;
+        beta = bs;
+    }
+
     // Links for the pipelined Phase 2 (every chunk after the first of the slab): an entry
     // whose slot the stream's previous step writes is pointed at that group's new piece
-    // (-1 - g) instead of the bank row. The previous chunk's groups are sorted by slot.
-    if (!d.per_step && !d.bwd && n >= d.P) {
-        const int CW = C * d.W, CR = C * d.R, np = n - d.P;
+    // (-1 - g) instead of the bank row. The previous chunk's groups are sorted by slot; the
+    // search runs in shared memory, four branch-free lower bounds at a time.
+    if (solve_links(d) && n >= d.P) {
+        const int CW = C * d.W, CR = C * d.R, NE = CW + CR, np = n - d.P;
         const int ngp = w.ngroups[np];
-        const int32_t *gsp = w.gslot + (size_t)np * CW;
+        int32_t *gsp = reinterpret_cast<int32_t *>(sraw + SL.gsl);
+        int32_t *ent = reinterpret_cast<int32_t *>(sraw + SL.ent);
         int32_t *wsl = w.wsl + (size_t)n * CW;
         int32_t *rsl = w.rsl + (size_t)n * CR;
-        for (int i = tid; i < CW + CR; i += NTS) {
-            int32_t *ent = i < CW ? wsl + i : rsl + (i - CW);
-            const int v = *ent;
-            if (v < 0) continue;
-            int lo = 0, hi = ngp;
-            while (lo < hi) {
-                const int mid = (lo + hi) >> 1;
-                if (gsp[mid] < v) lo = mid + 1; else hi = mid;
+        for (int i = tid; i < ngp; i += NTS) gsp[i] = w.gslot[(size_t)np * CW + i];
+        for (int i = tid; i < NE; i += NTS) ent[i] = i < CW ? wsl[i] : rsl[i - CW];
+        __syncthreads();
+        for (int i0 = tid; i0 < NE; i0 += 4 * NTS) {
+            int v[4], base[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int i = i0 + k * NTS;
+                v[k] = i < NE ? ent[i] : -1;
+                base[k] = 0;
             }
-            if (lo < ngp && gsp[lo] == v) *ent = -1 - lo;
+            for (int len = ngp; len > 1;) {
+                const int half = len >> 1;
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    if (gsp[base[k] + half - 1] < v[k]) base[k] += half;
+                len -= half;
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int i = i0 + k * NTS;
+                if (i >= NE || v[k] < 0 || ngp == 0) continue;
+                // base is the last position whose predecessors are all < v
+                const int lb = base[k] + (gsp[base[k]] < v[k] ? 1 : 0);
+                if (lb < ngp && gsp[lb] == v[k]) {
+                    if (i < CW) wsl[i] = -1 - lb;
+                    else rsl[i - CW] = -1 - lb;
+                }
+            }
         }
     }
+    if (staged) cp_async_wait<0>();
+    __syncthreads();
 
     // L (or QK) element (R, K) of the chunk, zero outside the valid tokens
     auto lval = [&](int R, int K) {
-        return (R < nv && K < R) ? beta[R] * A[(size_t)R * C + K] : 0.f;
+        return (R < nv && K < R) ? beta[R] * A[(size_t)R * ap + K] : 0.f;
     };
 
-    // 1. diagonal inverses: thread (block b, column c) substitutes down its column
+    // 1. diagonal inverses: the diagonal blocks of L are staged (coalesced), then thread
+    //    (block b, column c) substitutes down its column
+    for (int e = tid; e < nvb * BB; e += NTS) {
+        const int b = e / BB, rc = e - b * BB, r = rc / BS, c = rc - r * BS;
+        Lr[e] = lval(b * BS + r, b * BS + c);
+    }
+    __syncthreads();
     for (int job = tid; job < nvb * BS; job += NTS) {
         const int b = job / BS, c = job - b * BS;
         float *Dk = Xp + (tri(b) + b) * BB;
+        const float *Lb = Lr + b * BB;
         float x[BS];
 #pragma unroll
         for (int r = 0; r < BS; ++r) x[r] = (r == c) ? 1.f : 0.f;
 #pragma unroll
         for (int r = 1; r < BS; ++r) {
-            const int R = b * BS + r;
             float s = 0.f;
 #pragma unroll
             for (int k = 0; k < BS; ++k)
-                if (k < r) s = fmaf(lval(R, b * BS + k), x[k], s);
+                if (k < r) s = fmaf(Lb[r * BS + k], x[k], s);
             if (r > c) x[r] = -s;
         }
 #pragma unroll
@@ -130,7 +217,7 @@ __global__ void __launch_bounds__(NTS) k_solve(Dims d, Inputs in, Work w, int st
             for (int e = tid; e < (i + 1) * BB; e += NTS) {
                 const int k = e / BB, rc = e - k * BB, r = rc / BS, c = rc - r * BS;
                 const int R = i * BS + r, K = k * BS + c;
-                Lr[e] = (R < nv && K <= R) ? QK[(size_t)R * C + K] : 0.f;
+                Lr[e] = (R < nv && K <= R) ? QK[(size_t)R * ap + K] : 0.f;
             }
             __syncthreads();
             for (int e = tid; e < (i + 1) * BB; e += NTS) {
@@ -172,14 +259,11 @@ __global__ void __launch_bounds__(NTS) k_solve(Dims d, Inputs in, Work w, int st
 
 }  // namespace
 
-size_t solve_smem_bytes(int C) {
-    const int nb = (C + BS - 1) / BS;
-    return sizeof(float) * (size_t)(tri(nb) + 2 * nb) * BB;
-}
+size_t solve_smem_bytes(const Dims &d) { return solve_layout(d).bytes; }
 
 cudaError_t launch_solve(const Dims &d, const Inputs &in, const Work &w, int step0, int nsteps,
                          cudaStream_t st) {
-    const size_t smem = solve_smem_bytes(d.C);
+    const size_t smem = solve_smem_bytes(d);
     if (smem > 48 * 1024)
         cudaFuncSetAttribute(k_solve, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     k_solve<<<nsteps * d.P, NTS, smem, st>>>(d, in, w, step0, nsteps);

@@ -422,12 +422,16 @@ __global__ void __launch_bounds__(NTB) k_b_dbr(Dims d, Work w, float *gbank, int
 }
 
 // ---------------------------------------------------------------------------------------
-// Phase-1 backward (one CTA per chunk): dk, dq, dg
+// Phase-1 backward: dk, dq, dg, in three launches per step (stage 0: reads, 1: writes, 2:
+// groups; each stage needs the previous one's results for the whole chunk). A launch has
+// gridDim.x CTAs per stream, each taking a contiguous share of the sorted entries, one warp per
+// entry (a thread per group in stage 2).
 // ---------------------------------------------------------------------------------------
 template <typename WT>
 __global__ void __launch_bounds__(NTB) k_b_phase1(Dims d, Inputs in, Work w, float *gk,
-                                                 float *gg, float *gq, int step0, int ti) {
-    const int p = blockIdx.x, n = local_n(d, step0, ti, p);
+                                                 float *gg, float *gq, int step0, int ti,
+                                                 int stage) {
+    const int p = blockIdx.y, n = local_n(d, step0, ti, p);
     const int C = d.C, W = d.W, R = d.R, CW = C * W, CR = C * R;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nv = w.nvalid[n], nw = nv * W, nr = nv * R;
@@ -475,8 +479,18 @@ __global__ void __launch_bounds__(NTB) k_b_phase1(Dims d, Inputs in, Work w, flo
         return a;
     };
 
+    // this CTA's share [b0, b1) of the n entries of a stage
+    auto share = [&](int cnt, int &b0, int &b1) {
+        const int per = (cnt + gridDim.x - 1) / gridDim.x;
+        b0 = blockIdx.x * per;
+        b1 = b0 + per < cnt ? b0 + per : cnt;
+    };
+    int b0, b1;
+
     // (i) reads: dq and the gradient of their running log-decay
-    for (int rp = warp; rp < nr; rp += NWB) {
+    if (stage == 0) {
+    share(nr, b0, b1);
+    for (int rp = b0 + warp; rp < b1; rp += NWB) {
         const unsigned long long key = rkey[rp];
         const unsigned r = (unsigned)(key >> 32);
         const unsigned low = (unsigned)key;
@@ -502,9 +516,17 @@ __global__ void __launch_bounds__(NTB) k_b_phase1(Dims d, Inputs in, Work w, flo
             dlr[rp] = dl;
         }
     }
-    __syncthreads();
+    // padding tokens of the chunk: zero gradients
+    if (blockIdx.x == 0) {
+        const int tmax = (size_t)ti * C + C <= (size_t)d.T ? C : d.T - ti * C;
+        for (int i = nr + threadIdx.x; i < tmax * R; i += NTB) gq[tok0 * R + i] = 0.f;
+    }
+    return;
+    }
     // (ii) writes: dk and the gradient of their running log-decay
-    for (int pa = warp; pa < nw; pa += NWB) {
+    if (stage == 1) {
+    share(nw, b0, b1);
+    for (int pa = b0 + warp; pa < b1; pa += NWB) {
         const unsigned long long key = wkey[pa];
         const unsigned s = (unsigned)(key >> 32);
         const unsigned low = (unsigned)key;
@@ -544,9 +566,15 @@ __global__ void __launch_bounds__(NTB) k_b_phase1(Dims d, Inputs in, Work w, flo
             dlam[pa] = dlam_a;
         }
     }
-    __syncthreads();
+    if (blockIdx.x == 0) {
+        const int tmax = (size_t)ti * C + C <= (size_t)d.T ? C : d.T - ti * C;
+        for (int i = nw + threadIdx.x; i < tmax * W; i += NTB) gk[tok0 * W + i] = 0.f;
+    }
+    return;
+    }
     // (iii) per group: the gradient of its total log-decay, then dg as suffix sums
-    for (int pa = threadIdx.x; pa < nw; pa += NTB) {
+    share(nw, b0, b1);
+    for (int pa = b0 + threadIdx.x; pa < b1; pa += NTB) {
         if (pgs[pa] != pa) continue;              // one thread per group (its head)
         const unsigned s = (unsigned)(wkey[pa] >> 32);
         const int ge = pge[pa];
@@ -567,10 +595,10 @@ __global__ void __launch_bounds__(NTB) k_b_phase1(Dims d, Inputs in, Work w, flo
             gg[(tok0 + (lb >> 8)) * W + (lb & 255u)] = s < S ? run : 0.f;
         }
     }
-    // padding tokens of the chunk: zero gradients
-    const int tmax = (size_t)ti * C + C <= (size_t)d.T ? C : d.T - ti * C;
-    for (int i = nw + threadIdx.x; i < tmax * W; i += NTB) { gk[tok0 * W + i] = 0.f; gg[tok0 * W + i] = 0.f; }
-    for (int i = nr + threadIdx.x; i < tmax * R; i += NTB) gq[tok0 * R + i] = 0.f;
+    if (blockIdx.x == 0) {
+        const int tmax = (size_t)ti * C + C <= (size_t)d.T ? C : d.T - ti * C;
+        for (int i = nw + threadIdx.x; i < tmax * W; i += NTB) gg[tok0 * W + i] = 0.f;
+    }
 }
 
 template <typename T>
@@ -621,8 +649,15 @@ cudaError_t backward_step(const Dims &d, const Inputs &in, const Work &w, const 
     if (gr > gx) gr = gx;
     if (gr < 1) gr = 1;
     k_b_dbr<CPL><<<dim3(gr, P), NTB, 0, st>>>(d, w, o.grad_bank, step0, ti);
-    k_b_phase1<BT><<<P, NTB, 0, st>>>(d, in, w, o.grad_write_w, o.grad_log_decay, o.grad_read_w,
-                                       step0, ti);
+    // Phase-1 backward: about 8 entries per warp and stage (one warp walks an entry's members)
+    const int per_cta = 8 * NWB;
+    int gb = (d.C * (d.W > d.R ? d.W : d.R) + per_cta - 1) / per_cta;
+    const int gmax = (8 * kRefSms + P - 1) / P;
+    if (gb > gmax) gb = gmax;
+    if (gb < 1) gb = 1;
+    for (int stage = 0; stage < 3; ++stage)
+        k_b_phase1<BT><<<dim3(gb, P), NTB, 0, st>>>(d, in, w, o.grad_write_w, o.grad_log_decay,
+                                                   o.grad_read_w, step0, ti, stage);
     return cudaGetLastError();
 }
 

@@ -223,6 +223,34 @@ int sdm_phase1_debug(const sdm_shape *shape, const int32_t *write_slots, const v
  * the stream. status: host pointer. Returns SDM_OK, or SDM_ERR_CUDA. */
 int sdm_get_device_status(const void *workspace, sdm_device_status *status, void *stream);
 
+/* Bytes of device workspace sdm_write_read_host needs: the sdm_write_read workspace plus a
+ * device copy of the inputs (0 if the shape is refused). */
+size_t sdm_host_workspace_bytes(const sdm_shape *shape);
+
+/* The forward with its inputs and readings in host memory: what sdm_write_read computes, for a
+ * caller whose data lives on the host (the sparse-delta-memory 2.0.0 memory_ops.py
+ * sdm_write_read call with CPU tensors). The pages have no host-side variant; this one exists
+ * so that one call covers the whole path including the transfers.
+ *   - bank: device memory, advanced in place as in sdm_write_read.
+ *   - write_slots ... valid_tokens: host memory, same layouts as sdm_write_read (valid_tokens
+ *     may be NULL). Page-locked (pinned) memory lets the copies run asynchronously.
+ *   - readings: page-locked host memory mapped into the device address space (cudaHostAlloc /
+ *     cudaMallocHost, or cudaHostRegister with cudaHostRegisterMapped), [P, T, D] in the bank
+ *     dtype, 16-byte aligned. The Phase-2 kernels store the readings straight into it; it is
+ *     complete when the call's work on `stream` has finished. Other memory is refused with
+ *     SDM_ERR_INVALID before any work.
+ *   - workspace: device memory of at least sdm_host_workspace_bytes(shape) bytes, 256-byte
+ *     aligned; it holds the device copy of the inputs.
+ * The inputs other than v are copied on `stream` before Phase 1; v is copied on a second,
+ * library-owned stream (created once per device) and joined before Phase 2, so that its copy
+ * runs under Phase 1 and the solve. All work is ordered after the previous work on `stream` and
+ * before later work on it; the call is asynchronous and may be captured in a CUDA graph. */
+int sdm_write_read_host(const sdm_shape *shape, void *bank, const int32_t *write_slots,
+                        const void *write_w, const float *log_decay, const float *beta,
+                        const void *v, const int32_t *read_slots, const void *read_w,
+                        const int32_t *valid_tokens, void *readings, void *workspace,
+                        size_t workspace_bytes, void *stream);
+
 /* Number of kernel launches sdm_write_read queues for this shape (0 if refused). */
 int64_t sdm_launch_count(const sdm_shape *shape);
 

@@ -83,6 +83,10 @@ def library() -> ctypes.CDLL:
             lib.sdm_write_read_backward.argtypes = ([sp] + [vp] * 9 + [vp, sz] + [vp] * 7
                                                     + [vp, sz, vp])
             lib.sdm_write_read_backward.restype = i32
+            lib.sdm_host_workspace_bytes.argtypes = [sp]
+            lib.sdm_host_workspace_bytes.restype = sz
+            lib.sdm_write_read_host.argtypes = [sp] + [vp] * 10 + [vp, sz, vp]
+            lib.sdm_write_read_host.restype = i32
             lib.sdm_write_read_noalloc.argtypes = [sp] + [vp] * 10 + [vp]
             lib.sdm_write_read_noalloc.restype = i32
             lib.sdm_profile_write_read.argtypes = ([sp] + [vp] * 10 + [vp, sz]
@@ -204,6 +208,57 @@ def sdm_write_read(bank: torch.Tensor, write_slots: torch.Tensor, write_w: torch
         workspace = alloc_workspace(shape, dev)
     with torch.cuda.device(dev):
         rc = library().sdm_write_read(
+            ctypes.byref(shape), _ptr(bank), _ptr(write_slots), _ptr(write_w), _ptr(log_decay),
+            _ptr(beta), _ptr(v), _ptr(read_slots), _ptr(read_w), _ptr(valid_tokens),
+            _ptr(readings), _ptr(workspace), workspace.numel(), _stream_ptr(stream))
+    _check(rc)
+    return readings
+
+
+def host_workspace_bytes(shape: Shape) -> int:
+    n = library().sdm_host_workspace_bytes(ctypes.byref(shape))
+    if n == 0:
+        raise SdmError(-1, library().sdm_last_error().decode())
+    return n
+
+
+def sdm_write_read_host(bank: torch.Tensor, write_slots: torch.Tensor, write_w: torch.Tensor,
+                        log_decay: torch.Tensor, beta: torch.Tensor, v: torch.Tensor,
+                        read_slots: torch.Tensor, read_w: torch.Tensor,
+                        valid_tokens: Optional[torch.Tensor] = None, *, chunk_size: int,
+                        readings: Optional[torch.Tensor] = None, slab_steps: int = 0,
+                        workspace: Optional[torch.Tensor] = None, stream=None,
+                        flags: int = 0) -> torch.Tensor:
+    """sdm_write_read with the inputs in host memory and the readings written to pinned host
+    memory ([P, T, D], bank dtype); the bank stays on its GPU. Same arguments and layouts as
+    ``sdm_write_read``; pinned inputs make the copies asynchronous."""
+    if write_slots.dim() != 3:
+        raise ValueError("write_slots must be [P, T, W]")
+    P, T, W = write_slots.shape
+    R = read_slots.shape[-1]
+    if bank.dim() != 2 or bank.shape[0] % P or bank.device.type != "cuda":
+        raise ValueError(f"bank must be a CUDA tensor [P*S, D] with P={P}")
+    S, D = bank.shape[0] // P, bank.shape[1]
+    dev, dt, cpu = bank.device, bank.dtype, torch.device("cpu")
+    _need(bank, "bank", (P * S, D), dt, dev)
+    _need(write_slots, "write_slots", (P, T, W), torch.int32, cpu)
+    _need(write_w, "write_w", (P, T, W), dt, cpu)
+    _need(log_decay, "log_decay", (P, T, W), torch.float32, cpu)
+    _need(beta, "beta", (P, T), torch.float32, cpu)
+    _need(v, "v", (P, T, D), dt, cpu)
+    _need(read_slots, "read_slots", (P, T, R), torch.int32, cpu)
+    _need(read_w, "read_w", (P, T, R), dt, cpu)
+    if valid_tokens is not None:
+        _need(valid_tokens, "valid_tokens", (P,), torch.int32, cpu)
+    shape = make_shape(P, T, chunk_size, S, D, W, R, dt, slab_steps, flags)
+    if readings is None:
+        readings = torch.empty((P, T, D), dtype=dt, pin_memory=True)
+    else:
+        _need(readings, "readings", (P, T, D), dt, cpu)
+    if workspace is None:
+        workspace = torch.empty(host_workspace_bytes(shape), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        rc = library().sdm_write_read_host(
             ctypes.byref(shape), _ptr(bank), _ptr(write_slots), _ptr(write_w), _ptr(log_decay),
             _ptr(beta), _ptr(v), _ptr(read_slots), _ptr(read_w), _ptr(valid_tokens),
             _ptr(readings), _ptr(workspace), workspace.numel(), _stream_ptr(stream))

@@ -11,6 +11,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <mutex>
 #include <vector>
 
 #include "sdm_internal.cuh"
@@ -252,7 +253,7 @@ int check_inputs(const Inputs &in, bool need_bank) {
 
 // The launch sequence of one forward call (see the file comment).
 int run_forward(const Prepared &pr, const Inputs &in, void *workspace, cudaStream_t st,
-                Recorder *rec) {
+                Recorder *rec, cudaEvent_t phase2_ready = nullptr) {
     const Dims &d = pr.d;
     Work w = layout_assign(d, pr.ns, pr.G, workspace);
     cudaError_t e = cudaMemsetAsync(w.status, 0, sizeof(DevStatus), st);
@@ -266,6 +267,8 @@ int run_forward(const Prepared &pr, const Inputs &in, void *workspace, cudaStrea
         const int nsteps = (d.Nt - s0) < pr.ns ? (d.Nt - s0) : pr.ns;
         SDM_LAUNCH(SDM_KERNEL_PHASE1, launch_phase1(d, in, w, s0, nsteps, st), "phase1");
         SDM_LAUNCH(SDM_KERNEL_SOLVE, launch_solve(d, in, w, s0, nsteps, st), "solve");
+        if (phase2_ready && s0 == 0 && (e = cudaStreamWaitEvent(st, phase2_ready, 0)) != cudaSuccess)
+            return cuda_fail(e, "wait for v");
         if (!d.per_step) {
             SDM_LAUNCH(SDM_KERNEL_PHASE2, launch_phase2_fused(d, in, w, s0, nsteps, st),
                        "phase2");
@@ -279,6 +282,43 @@ int run_forward(const Prepared &pr, const Inputs &in, void *workspace, cudaStrea
     }
 #undef SDM_LAUNCH
     if (rec && (e = rec->mark(-1, st)) != cudaSuccess) return cuda_fail(e, "event");
+    return SDM_OK;
+}
+
+// Device copies of the host inputs, after the sdm_write_read workspace (256-byte aligned).
+struct HostStage {
+    size_t ws, kw, g, beta, v, rs, qw, valid, bytes;
+};
+HostStage host_stage(const Dims &d, size_t base) {
+    const size_t PT = (size_t)d.P * d.T, es = d.dtype == SDM_BF16 ? 2 : 4;
+    HostStage h;
+    size_t o = up(base);
+    h.ws = o; o = up(o + 4 * PT * d.W);
+    h.kw = o; o = up(o + es * PT * d.W);
+    h.g = o; o = up(o + 4 * PT * d.W);
+    h.beta = o; o = up(o + 4 * PT);
+    h.v = o; o = up(o + es * PT * d.D);
+    h.rs = o; o = up(o + 4 * PT * d.R);
+    h.qw = o; o = up(o + es * PT * d.R);
+    h.valid = o; o = up(o + 4 * (size_t)d.P);
+    h.bytes = o;
+    return h;
+}
+
+// The library's second stream on the current device (for the v copy of sdm_write_read_host).
+std::mutex g_side_mu;
+cudaStream_t g_side[64];
+int side_stream(cudaStream_t *out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(SDM_ERR_UNSUPPORTED, "device ordinal %d", dev);
+    std::lock_guard<std::mutex> lock(g_side_mu);
+    if (!g_side[dev]) {
+        e = cudaStreamCreateWithFlags(&g_side[dev], cudaStreamNonBlocking);
+        if (e != cudaSuccess) return cuda_fail(e, "side stream");
+    }
+    *out = g_side[dev];
     return SDM_OK;
 }
 
@@ -500,6 +540,82 @@ int sdm_get_device_status(const void *workspace, sdm_device_status *status, void
     status->bad_slots = (int64_t)h.bad_slots;
     status->repeated_write_slots = (int64_t)h.repeated_write_slots;
     return SDM_OK;
+}
+
+size_t sdm_host_workspace_bytes(const sdm_shape *shape) {
+    Prepared pr;
+    if (prepare(shape, pr)) return 0;
+    g_err[0] = 0;
+    return host_stage(pr.d, pr.bytes).bytes;
+}
+
+int sdm_write_read_host(const sdm_shape *shape, void *bank, const int32_t *write_slots,
+                        const void *write_w, const float *log_decay, const float *beta,
+                        const void *v, const int32_t *read_slots, const void *read_w,
+                        const int32_t *valid_tokens, void *readings, void *workspace,
+                        size_t workspace_bytes, void *stream) {
+    Prepared pr;
+    int rc = prepare(shape, pr);
+    if (rc) return rc;
+    const Dims &d = pr.d;
+    const HostStage hs = host_stage(d, pr.bytes);
+    if (!bank || !write_slots || !write_w || !log_decay || !beta || !v || !read_slots ||
+        !read_w || !readings)
+        return fail(SDM_ERR_INVALID, "a required pointer is NULL");
+    if (!workspace || reinterpret_cast<uintptr_t>(workspace) % kAlign)
+        return fail(SDM_ERR_WORKSPACE, "workspace must be %zu-byte aligned device memory", kAlign);
+    if (workspace_bytes < hs.bytes)
+        return fail(SDM_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", workspace_bytes,
+                    hs.bytes);
+    // readings: mapped page-locked host memory, written by the kernels through its device address
+    cudaPointerAttributes at;
+    cudaError_t e = cudaPointerGetAttributes(&at, readings);
+    if (e != cudaSuccess || at.type != cudaMemoryTypeHost || !at.devicePointer) {
+        cudaGetLastError();
+        return fail(SDM_ERR_INVALID, "readings must be mapped page-locked host memory");
+    }
+    void *rdev = at.devicePointer;
+    if (reinterpret_cast<uintptr_t>(bank) % 16 || reinterpret_cast<uintptr_t>(rdev) % 16)
+        return fail(SDM_ERR_INVALID, "bank and readings must be 16-byte aligned");
+    g_err[0] = 0;
+    cudaStream_t st = static_cast<cudaStream_t>(stream), side;
+    if ((rc = side_stream(&side))) return rc;
+    char *base = static_cast<char *>(workspace);
+    const size_t PT = (size_t)d.P * d.T, es = d.dtype == SDM_BF16 ? 2 : 4;
+    Inputs in{bank, reinterpret_cast<const int32_t *>(base + hs.ws), base + hs.kw,
+              reinterpret_cast<const float *>(base + hs.g),
+              reinterpret_cast<const float *>(base + hs.beta), base + hs.v,
+              reinterpret_cast<const int32_t *>(base + hs.rs), base + hs.qw,
+              valid_tokens ? reinterpret_cast<const int32_t *>(base + hs.valid) : nullptr, rdev,
+              nullptr};
+    cudaEvent_t ev_start = nullptr, ev_v = nullptr;
+    auto done = [&](int r) {
+        if (ev_start) cudaEventDestroy(ev_start);
+        if (ev_v) cudaEventDestroy(ev_v);
+        return r;
+    };
+    if ((e = cudaEventCreateWithFlags(&ev_start, cudaEventDisableTiming)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&ev_v, cudaEventDisableTiming)) != cudaSuccess)
+        return done(cuda_fail(e, "event"));
+    // v on the side stream, after the work already queued on `stream`
+    if ((e = cudaEventRecord(ev_start, st)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(side, ev_start, 0)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(base + hs.v, v, es * PT * d.D, cudaMemcpyHostToDevice, side)) !=
+            cudaSuccess ||
+        (e = cudaEventRecord(ev_v, side)) != cudaSuccess)
+        return done(cuda_fail(e, "v copy"));
+    struct { size_t off; const void *src; size_t bytes; } cp[] = {
+        {hs.ws, write_slots, 4 * PT * d.W}, {hs.kw, write_w, es * PT * d.W},
+        {hs.g, log_decay, 4 * PT * d.W},    {hs.beta, beta, 4 * PT},
+        {hs.rs, read_slots, 4 * PT * d.R},  {hs.qw, read_w, es * PT * d.R},
+        {hs.valid, valid_tokens, 4 * (size_t)d.P}};
+    for (auto &c : cp) {
+        if (!c.src) continue;
+        if ((e = cudaMemcpyAsync(base + c.off, c.src, c.bytes, cudaMemcpyHostToDevice, st)) !=
+            cudaSuccess)
+            return done(cuda_fail(e, "input copy"));
+    }
+    return done(run_forward(pr, in, workspace, st, nullptr, ev_v));
 }
 
 }  // extern "C"

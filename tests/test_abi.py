@@ -88,3 +88,12 @@ def test_write_read_refuses_before_any_work():
     rc = lib.sdm_write_read(ctypes.byref(s), fake, fake, fake, fake, fake, fake, fake, fake,
                             None, fake, fake, 16, None)
     assert rc == -5 and "workspace" in lib.sdm_last_error().decode()
+
+
+def test_host_workspace_holds_the_inputs():
+    s = sdm.make_shape(8, 4096, 64, 65536, 128, 16, 16, sdm.SDM_BF16)
+    per_token = 16 * 4 + 16 * 2 + 16 * 4 + 4 + 128 * 2 + 16 * 4 + 16 * 2
+    assert sdm.host_workspace_bytes(s) >= sdm.workspace_bytes(s) + 8 * 4096 * per_token
+    bad = sdm.make_shape(8, 4096, 64, 65536, 100, 16, 16, sdm.SDM_BF16)
+    with pytest.raises(sdm.SdmError):
+        sdm.host_workspace_bytes(bad)

@@ -241,9 +241,10 @@ size_t sdm_host_workspace_bytes(const sdm_shape *shape);
  *     SDM_ERR_INVALID before any work.
  *   - workspace: device memory of at least sdm_host_workspace_bytes(shape) bytes, 256-byte
  *     aligned; it holds the device copy of the inputs.
- * The inputs other than v are copied on `stream` before Phase 1; v is copied on a second,
- * library-owned stream (created once per device) and joined before Phase 2, so that its copy
- * runs under Phase 1 and the solve. All work is ordered after the previous work on `stream` and
+ * The inputs other than v are copied on `stream` before Phase 1 (by one kernel reading the host
+ * pages when all of them are mapped page-locked memory, else by one transfer each); v is copied
+ * on a second, library-owned stream (created once per device) and joined before Phase 2, so
+ * that its copy runs under Phase 1 and the solve. All work is ordered after the previous work on `stream` and
  * before later work on it; the call is asynchronous and may be captured in a CUDA graph. */
 int sdm_write_read_host(const sdm_shape *shape, void *bank, const int32_t *write_slots,
                         const void *write_w, const float *log_decay, const float *beta,

@@ -597,24 +597,49 @@ int sdm_write_read_host(const sdm_shape *shape, void *bank, const int32_t *write
     if ((e = cudaEventCreateWithFlags(&ev_start, cudaEventDisableTiming)) != cudaSuccess ||
         (e = cudaEventCreateWithFlags(&ev_v, cudaEventDisableTiming)) != cudaSuccess)
         return done(cuda_fail(e, "event"));
-    // v on the side stream, after the work already queued on `stream`
+    // the inputs of Phase 1 and the solve on `stream`, then v on the side stream (after them,
+    // so that the two copies do not share the link; v has Phase 1 and the solve to land)
+    struct { size_t off; const void *src; size_t bytes; } cp[] = {
+        {hs.ws, write_slots, 4 * PT * d.W}, {hs.kw, write_w, es * PT * d.W},
+        {hs.g, log_decay, 4 * PT * d.W},    {hs.beta, beta, 4 * PT},
+        {hs.rs, read_slots, 4 * PT * d.R},  {hs.qw, read_w, es * PT * d.R},
+        {hs.valid, valid_tokens, 4 * (size_t)d.P}};
+    // all of them mapped page-locked memory (16-byte aligned, whole 16-byte units): one copy
+    // kernel reads them through their device addresses; otherwise one transfer per array
+    HostCopyTable tab;
+    tab.n = 0;
+    bool mapped = true;
+    for (auto &c : cp) {
+        if (!c.src) continue;
+        cudaPointerAttributes pa;
+        if (cudaPointerGetAttributes(&pa, c.src) != cudaSuccess || pa.type != cudaMemoryTypeHost ||
+            !pa.devicePointer || (reinterpret_cast<uintptr_t>(pa.devicePointer) & 15) ||
+            (c.bytes & 15)) {
+            cudaGetLastError();
+            mapped = false;
+            break;
+        }
+        tab.src[tab.n] = static_cast<const uint4 *>(pa.devicePointer);
+        tab.dst[tab.n] = reinterpret_cast<uint4 *>(base + c.off);
+        tab.n16[tab.n] = (long long)(c.bytes / 16);
+        ++tab.n;
+    }
+    if (mapped) {
+        if ((e = launch_host_copy(tab, st)) != cudaSuccess) return done(cuda_fail(e, "input copy"));
+    } else {
+        for (auto &c : cp) {
+            if (!c.src) continue;
+            if ((e = cudaMemcpyAsync(base + c.off, c.src, c.bytes, cudaMemcpyHostToDevice, st)) !=
+                cudaSuccess)
+                return done(cuda_fail(e, "input copy"));
+        }
+    }
     if ((e = cudaEventRecord(ev_start, st)) != cudaSuccess ||
         (e = cudaStreamWaitEvent(side, ev_start, 0)) != cudaSuccess ||
         (e = cudaMemcpyAsync(base + hs.v, v, es * PT * d.D, cudaMemcpyHostToDevice, side)) !=
             cudaSuccess ||
         (e = cudaEventRecord(ev_v, side)) != cudaSuccess)
         return done(cuda_fail(e, "v copy"));
-    struct { size_t off; const void *src; size_t bytes; } cp[] = {
-        {hs.ws, write_slots, 4 * PT * d.W}, {hs.kw, write_w, es * PT * d.W},
-        {hs.g, log_decay, 4 * PT * d.W},    {hs.beta, beta, 4 * PT},
-        {hs.rs, read_slots, 4 * PT * d.R},  {hs.qw, read_w, es * PT * d.R},
-        {hs.valid, valid_tokens, 4 * (size_t)d.P}};
-    for (auto &c : cp) {
-        if (!c.src) continue;
-        if ((e = cudaMemcpyAsync(base + c.off, c.src, c.bytes, cudaMemcpyHostToDevice, st)) !=
-            cudaSuccess)
-            return done(cuda_fail(e, "input copy"));
-    }
     return done(run_forward(pr, in, workspace, st, nullptr, ev_v));
 }
 

@@ -169,6 +169,15 @@ cudaError_t launch_dw(const Dims &d, const Inputs &in, const Work &w, int step0,
 cudaError_t launch_phase2_fused(const Dims &d, const Inputs &in, const Work &w, int step0,
                                 int nsteps, cudaStream_t st);
 size_t phase2_pipe_smem(const Dims &d);
+// sdm_write_read_host: arrays copied from mapped page-locked host memory by one kernel
+// (device addresses of the host pages; 16-byte aligned; sizes in 16-byte units)
+struct HostCopyTable {
+    const uint4 *src[8];
+    uint4 *dst[8];
+    long long n16[8];
+    int n;
+};
+cudaError_t launch_host_copy(const HostCopyTable &t, cudaStream_t st);
 bool phase2_fused_fits(const Dims &d);
 cudaError_t launch_backward_step(const Dims &d, const Inputs &in, const Work &w,
                                  const BwdOut &o, int step0, int ti, cudaStream_t st);

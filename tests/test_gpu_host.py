@@ -116,3 +116,20 @@ def test_host_call_refuses_unmapped_readings():
                                 readings=pageable)
     torch.cuda.synchronize()
     assert torch.equal(bank, dev["bank"])      # refused before any work
+
+
+def test_host_call_pageable_inputs():
+    """Inputs in ordinary (pageable) host memory take the per-array transfer path."""
+    wl = small_workload(P=2, T=260, C=64, S=800, D=128, W=16, R=16, dtype="bf16", seed=8,
+                        ragged=True)
+    inputs = si.generate(wl)
+    dev = to_device(inputs, wl)
+    pinned = host_inputs(inputs, wl)
+    pageable = {k: t.clone() for k, t in pinned.items()}
+    assert not pageable["v"].is_pinned()
+    ref = dev["bank"].clone()
+    r_ref = sdm.sdm_write_read(ref, *(dev[k] for k in NAMES), chunk_size=wl.C).cpu()
+    bank = dev["bank"].clone()
+    r = sdm.sdm_write_read_host(bank, *(pageable[k] for k in NAMES), chunk_size=wl.C)
+    torch.cuda.synchronize()
+    assert torch.equal(r, r_ref) and torch.equal(bank, ref)

@@ -81,10 +81,15 @@ __host__ __device__ inline StageLayout stage_layout(int C, int W, int R) {
     return L;
 }
 
-// Bytes the bulk copies of one stage move (everything before vpc; X and QX whole, padded rows)
-__host__ __device__ inline unsigned stage_bulk_bytes(int C, int W, int R) {
+// Bytes the bulk copies of one stage move: part A (the entries' slots and links, which the
+// previous step needs for its early loads) and part B (everything else before vpc; X and QX
+// whole, padded rows)
+__host__ __device__ inline unsigned stage_bytes_a(int C, int W, int R) {
+    return (unsigned)(4 * (C * W + C * R));
+}
+__host__ __device__ inline unsigned stage_bytes_b(int C, int W, int R) {
     const int CW = C * W, CR = C * R;
-    return (unsigned)(4 * (7 * CW + 2 * CR + goff_stride(CW)) + 16 + 2 * 4 * C * x_pitch(C));
+    return (unsigned)(4 * (6 * CW + CR + goff_stride(CW)) + 16 + 2 * 4 * C * x_pitch(C));
 }
 
 // delta_v rows in shared memory are kDvPitch floats apart: 48 bytes spread a warp's random-row
@@ -92,9 +97,10 @@ __host__ __device__ inline unsigned stage_bulk_bytes(int C, int W, int R) {
 constexpr int kDvPitch = 12;
 
 // Bytes after the two stages: u_pre, inter [C][V] f32, delta_v [C][kDvPitch] f32, the B0 pieces
-// [CW][16 B], the DW's new piece per group [CW][16 B] and the stage mbarriers (full[2], empty[2]).
+// [CW][16 B], the DW's new piece per group [CW][16 B] and the stage mbarriers (fullA[2],
+// fullB[2], empty[2]).
 __host__ __device__ inline int pipe_tail_bytes(int C, int W, int V) {
-    return 2 * 4 * C * V + 4 * C * kDvPitch + 2 * 16 * C * W + 32;
+    return 2 * 4 * C * V + 4 * C * kDvPitch + 2 * 16 * C * W + 48;
 }
 
 // ---------------------------------------------------------------------------------------
@@ -206,10 +212,12 @@ __global__ void __launch_bounds__(NP2) k_phase2_pipe(Dims d, Inputs in, Work w, 
     float *dvs = is + C * V;                                     // [C][kDvPitch]
     uint4 *b0s = reinterpret_cast<uint4 *>(dvs + C * kDvPitch);  // [CW] B0 pieces (raw)
     uint4 *dwout = b0s + CW;                                      // [CW] new piece per group
-    // full[st]: stage st landed (1 expect-tx arrival + 32 producer-lane cp.async arrivals and
+    // fullA[st]: the slots/links of stage st landed (1 expect-tx arrival and their bytes);
+    // fullB[st]: the rest landed (1 expect-tx arrival + 32 producer-lane cp.async arrivals and
     // the bulk bytes); empty[st]: the compute warps are done with stage st (1 arrival)
-    unsigned long long *full = reinterpret_cast<unsigned long long *>(dwout + CW);
-    unsigned long long *empty = full + 2;
+    unsigned long long *fullA = reinterpret_cast<unsigned long long *>(dwout + CW);
+    unsigned long long *fullB = fullA + 2;
+    unsigned long long *empty = fullA + 4;
 
     BT *bank = static_cast<BT *>(in.bank) + (size_t)p * d.S * D + c0;
     const BT *vin = static_cast<const BT *>(in.v);
@@ -224,56 +232,64 @@ __global__ void __launch_bounds__(NP2) k_phase2_pipe(Dims d, Inputs in, Work w, 
         return r < 0 ? 0 : (r > C ? C : r);
     };
 
-    // stage st for step ls, issued by the producer warp: lanes 0..12 bulk-copy the workspace
-    // arrays (16-byte aligned chunk offsets, C % 16 == 0), every lane cp.asyncs the v pieces and
-    // beta of its tokens and then arrives on full[st] when those have landed
+    // stage st for step ls, issued by the producer warp: lanes 0 and 1 bulk-copy the slots and
+    // links (part A), then lanes 0..10 the other workspace arrays (part B; 16-byte aligned chunk
+    // offsets, C % 16 == 0); every lane cp.asyncs the v pieces and beta of its tokens and then
+    // arrives on fullB[st] when those have landed
     auto issue = [&](int ls, int st) {
         unsigned char *b = psm + st * L.bytes;
         const int ti = step0 + ls;
         const int n = ls * d.P + p;
         const int nv = nvalid_of(ti);
         const size_t tok0 = (size_t)p * d.T + (size_t)ti * C;
-        unsigned long long *bar = full + st;
-        if (lane == 0) mbar_arrive_expect_tx(bar, stage_bulk_bytes(C, W, R));
+        unsigned long long *barA = fullA + st, *barB = fullB + st;
+        if (lane == 0) {
+            mbar_arrive_expect_tx(barA, stage_bytes_a(C, W, R));
+            mbar_arrive_expect_tx(barB, stage_bytes_b(C, W, R));
+        }
         __syncwarp();
-        if (lane < 13) {
+        if (lane == 0) bulk_g2s(b + L.wslot, w.wsl + (size_t)n * CW, 4u * CW, barA);
+        if (lane == 1) bulk_g2s(b + L.rslot, w.rsl + (size_t)n * CR, 4u * CR, barA);
+        __syncwarp();
+        if (lane < 11) {
             const void *src;
             int off, bytes;
             switch (lane) {
-                case 0: src = w.wsl + (size_t)n * CW; off = L.wslot; bytes = 4 * CW; break;
-                case 1: src = w.gw + (size_t)n * CW; off = L.wgw; bytes = 4 * CW; break;
-                case 2: src = w.rsl + (size_t)n * CR; off = L.rslot; bytes = 4 * CR; break;
-                case 3: src = w.qw + (size_t)n * CR; off = L.rqw; bytes = 4 * CR; break;
-                case 4: src = w.minfo + (size_t)n * CW; off = L.minfo; bytes = 4 * CW; break;
-                case 5: src = w.wdw + (size_t)n * CW; off = L.mdw; bytes = 4 * CW; break;
-                case 6: src = w.gslot + (size_t)n * CW; off = L.gslot; bytes = 4 * CW; break;
-                case 7: src = w.gfac + (size_t)n * CW; off = L.gfac; bytes = 4 * CW; break;
-                case 8:
+                case 0: src = w.gw + (size_t)n * CW; off = L.wgw; bytes = 4 * CW; break;
+                case 1: src = w.qw + (size_t)n * CR; off = L.rqw; bytes = 4 * CR; break;
+                case 2: src = w.minfo + (size_t)n * CW; off = L.minfo; bytes = 4 * CW; break;
+                case 3: src = w.wdw + (size_t)n * CW; off = L.mdw; bytes = 4 * CW; break;
+                case 4: src = w.gslot + (size_t)n * CW; off = L.gslot; bytes = 4 * CW; break;
+                case 5: src = w.gfac + (size_t)n * CW; off = L.gfac; bytes = 4 * CW; break;
+                case 6:
                     src = w.goff + (size_t)n * goff_stride(CW);
                     off = L.goff;
                     bytes = 4 * goff_stride(CW);
                     break;
-                case 9: src = w.ng4 + n; off = L.scal; bytes = 16; break;
-                case 10: src = w.X + (size_t)n * C * XP; off = L.xs; bytes = 4 * C * XP; break;
-                case 11:
-                    src = w.gord + (size_t)n * CW;
-                    off = L.gord;
-                    bytes = 4 * CW;
-                    break;
+                case 7: src = w.ng4 + n; off = L.scal; bytes = 16; break;
+                case 8: src = w.X + (size_t)n * C * XP; off = L.xs; bytes = 4 * C * XP; break;
+                case 9: src = w.gord + (size_t)n * CW; off = L.gord; bytes = 4 * CW; break;
                 default: src = w.QX + (size_t)n * C * XP; off = L.qs; bytes = 4 * C * XP; break;
             }
-            bulk_g2s(b + off, src, (unsigned)bytes, bar);
+            bulk_g2s(b + off, src, (unsigned)bytes, barB);
         }
         for (int t = lane; t < nv; t += 32) {
             cp_async16(b + L.vpc + 16 * t, vin + (tok0 + t) * D + c0);
             cp_async4(b + L.beta + 4 * t, in.beta + tok0 + t);
         }
-        cp_async_mbar_arrive_noinc(bar);
+        cp_async_mbar_arrive_noinc(barB);
+    };
+    // both parts of stage (ls & 1) for step ls
+    auto wait_stage = [&](int ls) {
+        const unsigned par = (unsigned)(ls >> 1) & 1u;
+        return mbar_wait_bounded(fullA + (ls & 1), par) && mbar_wait_bounded(fullB + (ls & 1), par);
     };
 
     if (tid == 0) {
-        mbar_init(full, 33);
-        mbar_init(full + 1, 33);
+        mbar_init(fullA, 1);
+        mbar_init(fullA + 1, 1);
+        mbar_init(fullB, 33);
+        mbar_init(fullB + 1, 33);
         mbar_init(empty, 1);
         mbar_init(empty + 1, 1);
         fence_mbar_init();
@@ -293,8 +309,7 @@ __global__ void __launch_bounds__(NP2) k_phase2_pipe(Dims d, Inputs in, Work w, 
             issued = ls + 1;
         }
         // leave only after the last issued copies of both stages have landed
-        for (int ls = issued - 2 < 0 ? 0 : issued - 2; ls < issued; ++ls)
-            mbar_wait_bounded(full + (ls & 1), (unsigned)(ls >> 1) & 1u);
+        for (int ls = issued - 2 < 0 ? 0 : issued - 2; ls < issued; ++ls) wait_stage(ls);
         cp_async_wait<0>();
         return;
     }
@@ -340,7 +355,7 @@ __global__ void __launch_bounds__(NP2) k_phase2_pipe(Dims d, Inputs in, Work w, 
 
     for (int ls = 0; ls < nsteps; ++ls) {
         const int st = ls & 1;
-        const bool ok = mbar_wait_bounded(full + st, (unsigned)(ls >> 1) & 1u);
+        const bool ok = wait_stage(ls);
         if (compute_sync_or(!ok)) {
             // a stage did not land: report and stop (the producer drains its own copies)
             if (tid == 0) atomicCAS(&w.status->code, 0, (int)SDM_ERR_TIMEOUT);
@@ -494,7 +509,8 @@ __global__ void __launch_bounds__(NP2) k_phase2_pipe(Dims d, Inputs in, Work w, 
         // ---- early loads of step ls + 1 (warps without a matmul tile start at once) ----
         bool ok_next = true;
         if (ls + 1 < nsteps) {
-            ok_next = mbar_wait_bounded(full + (st ^ 1), (unsigned)((ls + 1) >> 1) & 1u);
+            // only part A (slots and links) is needed for the early loads
+            ok_next = mbar_wait_bounded(fullA + (st ^ 1), (unsigned)((ls + 1) >> 1) & 1u);
             if (ok_next) prefetch(ls + 1, psm + (st ^ 1) * L.bytes);
         }
         if (compute_sync_or(!ok_next)) {

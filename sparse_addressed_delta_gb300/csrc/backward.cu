@@ -603,8 +603,7 @@ __global__ void __launch_bounds__(NTB) k_b_phase1(Dims d, Inputs in, Work w, flo
 
 template <typename T>
 void set_smem(T kern, size_t bytes) {
-    if (bytes > 48 * 1024)
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    set_kernel_smem(kern, bytes);
 }
 
 void gemm(const GemmOp &g, int batch, cudaStream_t st) {

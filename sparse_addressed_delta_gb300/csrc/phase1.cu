@@ -174,7 +174,7 @@ __device__ __forceinline__ void report_bad_slot(DevStatus *st, int token) {
 }
 
 template <typename WT>
-__global__ void __launch_bounds__(NT) k_phase1(Dims d, Inputs in, Work w, int step0, int nsteps,
+__global__ void __launch_bounds__(NT, 2) k_phase1(Dims d, Inputs in, Work w, int step0, int nsteps,
                                                int scratch_in_smem) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     P1Smem &sm = *reinterpret_cast<P1Smem *>(smem_raw);
@@ -489,25 +489,43 @@ __global__ void __launch_bounds__(NT) k_phase1(Dims d, Inputs in, Work w, int st
             if (tid == 0) { w.rng[n] = rcarry; rgoff[rcarry] = nr; }
             __syncthreads();
         }
-        // 6. the DW order for the pipelined Phase 2: one stable radix pass over a size digit
-        //    (0 for a group of >= kHotGroup members, else 1 + kHotGroup - size) in the free
-        //    radix buffers
-        __syncthreads();   // the Gram rows are done with the (token, k) buffer
+        // 6. the DW order for the pipelined Phase 2: the groups of >= kHotGroup members first,
+        //    then the others by size, largest first (a counting sort over 1 + kHotGroup size
+        //    classes; the order inside a class is arbitrary, as a group's sum does not depend
+        //    on which thread computes it). Warp-aggregated shared-memory atomics.
         {
-            unsigned long long *ka = keyA, *kb = keyB;
-            int hot = 0;
-            for (int g = tid; g < ng; g += NT) {
+            constexpr int NB = kHotGroup + 1;
+            int *cnt = sm.hist, *cur = sm.hist + NB, *bas = sm.base;
+            for (int i = tid; i < 2 * NB; i += NT) sm.hist[i] = 0;
+            __syncthreads();
+            auto digit = [&](int g) {
                 const int sz = goff[g + 1] - goff[g];
-                const unsigned dig = sz >= kHotGroup ? 0u : (unsigned)(1 + kHotGroup - sz);
-                hot += sz >= kHotGroup;
-                ka[g] = ((unsigned long long)dig << 32) | (unsigned)g;
+                return sz >= kHotGroup ? 0 : 1 + kHotGroup - sz;
+            };
+            for (int g0 = 0; g0 < ng; g0 += NT) {
+                const int g = g0 + tid;
+                const int dig = g < ng ? digit(g) : NB;
+                const unsigned peers = __match_any_sync(0xffffffffu, dig);
+                if (dig < NB && lane == __ffs(peers) - 1) atomicAdd(&cnt[dig], __popc(peers));
             }
-            int nhot;
-            int_scan(hot, 0, nhot, sm);
-            radix_pass(ka, kb, ng, 32, sm);
+            __syncthreads();
+            if (tid == 0) {
+                int run = 0;
+                for (int k = 0; k < NB; ++k) { bas[k] = run; run += cnt[k]; }
+                w.ng4[n] = make_int4(ng, cnt[0], 0, 0);
+            }
+            __syncthreads();
             int32_t *go = w.gord + (size_t)n * CW;
-            for (int i = tid; i < ng; i += NT) go[i] = (int)(unsigned)kb[i];
-            if (tid == 0) w.ng4[n] = make_int4(ng, nhot, 0, 0);
+            for (int g0 = 0; g0 < ng; g0 += NT) {
+                const int g = g0 + tid;
+                const int dig = g < ng ? digit(g) : NB;
+                const unsigned peers = __match_any_sync(0xffffffffu, dig);
+                const int leader = __ffs(peers) - 1;
+                int first = 0;
+                if (dig < NB && lane == leader) first = atomicAdd(&cur[dig], __popc(peers));
+                first = __shfl_sync(0xffffffffu, first, leader);
+                if (dig < NB) go[bas[dig] + first + __popc(peers & ((1u << lane) - 1u))] = g;
+            }
         }
         for (int i = nw + tid; i < CW; i += NT) {
             perm[i] = -1; gw[i] = 0.f; lw[i] = 0.f; wdw[i] = 0.f; wsl[i] = kNoEntry;
@@ -532,11 +550,11 @@ cudaError_t launch_phase1(const Dims &d, const Inputs &in, const Work &w, int st
     const int grid = w.G;
     if (d.dtype == SDM_BF16) {
         auto kern = k_phase1<__nv_bfloat16>;
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        set_kernel_smem(kern, smem);
         kern<<<grid, NT, smem, st>>>(d, in, w, step0, nsteps, in_smem);
     } else {
         auto kern = k_phase1<float>;
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        set_kernel_smem(kern, smem);
         kern<<<grid, NT, smem, st>>>(d, in, w, step0, nsteps, in_smem);
     }
     return cudaGetLastError();

@@ -369,13 +369,11 @@ cudaError_t launch_dualmm(const Dims &d, const Inputs &in, const Work &w, int st
     dim3 grid((d.C + BM - 1) / BM, (d.D + BN - 1) / BN, d.P);
     if (d.dtype == SDM_BF16) {
         auto kern = k_dualmm<__nv_bfloat16>;
-        if (smem > 48 * 1024)
-            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        set_kernel_smem(kern, smem);
         kern<<<grid, kBlock, smem, st>>>(d, in, w, step0, ti);
     } else {
         auto kern = k_dualmm<float>;
-        if (smem > 48 * 1024)
-            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        set_kernel_smem(kern, smem);
         kern<<<grid, kBlock, smem, st>>>(d, in, w, step0, ti);
     }
     return cudaGetLastError();

@@ -618,7 +618,7 @@ cudaError_t launch_pipe(const Dims &d, const Inputs &in, const Work &w, int step
                         cudaStream_t st, size_t smem) {
     const int grid = d.P * (d.D / (16 / (int)sizeof(BT)));
     auto kern = k_phase2_pipe<BT>;
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    set_kernel_smem(kern, smem);
     kern<<<grid, NP2, smem, st>>>(d, in, w, step0, nsteps);
     return cudaGetLastError();
 }

@@ -329,6 +329,13 @@ __device__ __forceinline__ bool mbar_wait_bounded(unsigned long long *bar, unsig
 }
 
 __host__ __device__ __forceinline__ int goff_stride(int CW) { return CW + 4; }
+
+// Dynamic shared memory limit of a kernel (the driver keeps choosing the carveout: forcing the
+// largest one measured slower for the pipelined Phase 2, whose gather uses the L1 that is left)
+template <typename K>
+inline void set_kernel_smem(K kern, size_t bytes) {
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
 // a group with at least kHotGroup members is summed by a whole warp in the pipelined DW
 constexpr int kHotGroup = 16;
 

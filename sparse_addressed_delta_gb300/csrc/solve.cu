@@ -264,8 +264,7 @@ size_t solve_smem_bytes(const Dims &d) { return solve_layout(d).bytes; }
 cudaError_t launch_solve(const Dims &d, const Inputs &in, const Work &w, int step0, int nsteps,
                          cudaStream_t st) {
     const size_t smem = solve_smem_bytes(d);
-    if (smem > 48 * 1024)
-        cudaFuncSetAttribute(k_solve, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    set_kernel_smem(k_solve, smem);
     k_solve<<<nsteps * d.P, NTS, smem, st>>>(d, in, w, step0, nsteps);
     return cudaGetLastError();
 }

@@ -3,8 +3,9 @@
 // matmul -> DW"; the dual matmul's definition is the _sdm_dual_matmul docstring).
 //
 //   gather   retrieved[t] = sum_j gw[t][j] B[s_tj],  inter[t] = sum_i qw[t][i] B[r_ti]
-//            (B = the bank at the start of the chunk), f32 rows [P][C][D]
-//   dual mm  u_pre = beta (v - retrieved);  delta_v = X u_pre;  readings = QX u_pre + inter
+//            (B = the bank at the start of the chunk), u_pre = beta (v - retrieved);
+//            f32 rows [P][C][D] of u_pre and inter
+//   dual mm  delta_v = X u_pre;  readings = QX u_pre + inter (TF32 tensor cores)
 //   DW       for every written slot s (one group of the sorted write row):
 //            B[s] = exp(lend_s) B[s] + sum_{members m, sorted order} dw_m delta_v[t_m]
 //            in f32, rounded once at the store; the group's single warp is the row's only
@@ -114,11 +115,19 @@ __global__ void __launch_bounds__(kBlock) k_gather(Dims d, Inputs in, Work w, in
         }
     }
     const size_t row = ((size_t)p * C + t) * D + lane * CPL;
+    // u_pre = beta (v - retrieved), kept for the dual matmul in place of retrieved
+    auto finish = [&]() {
+        const size_t tok = (size_t)p * d.T + (size_t)ti * C + t;
+        float vv[CPL];
+        load_vec<BT, CPL, false>(static_cast<const BT *>(in.v) + tok * D + lane * CPL, vv);
+        const float bt = in.beta[tok];
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) ar[c] = bt * (vv[c] - ar[c]);
+        store_vec<float, CPL>(w.ret + row, ar);
+        store_vec<float, CPL>(w.inter + row, ai);
+    };
     if constexpr (WPT == 1) {
-        if (active) {
-            store_vec<float, CPL>(w.ret + row, ar);
-            store_vec<float, CPL>(w.inter + row, ai);
-        }
+        if (active) finish();
     } else {
 #pragma unroll
         for (int c = 0; c < CPL; ++c) {
@@ -134,85 +143,124 @@ __global__ void __launch_bounds__(kBlock) k_gather(Dims d, Inputs in, Work w, in
                     ar[c] += part[warp + s][0][lane * CPL + c];
                     ai[c] += part[warp + s][1][lane * CPL + c];
                 }
-            store_vec<float, CPL>(w.ret + row, ar);
-            store_vec<float, CPL>(w.inter + row, ai);
+            finish();
         }
     }
 }
 
 // ---------------------------------------------------------------------------------------
-// dual matmul: a [BM rows x BN columns] tile of delta_v and readings of one chunk
+// dual matmul on the tensor cores: a 16-row x 64-column tile of delta_v = X u_pre and of
+// readings = QX u_pre + inter of one chunk per CTA. X and QX rows and the u_pre tile are
+// copied on chip (cp.async, 16 bytes at a time where aligned); 4 warps, each one matrix and
+// four n8 tiles, mma.sync m16n8k8 TF32 (3xTF32 for float32 banks, as in the pipelined kernel).
 // ---------------------------------------------------------------------------------------
-constexpr int BM = 32, BN = 64;
+constexpr int MM_R = 16, MM_N = 64, MM_T = 128;
+
+__host__ __device__ inline int mm_kpad(int C) { return (C + 7) & ~7; }
+__host__ __device__ inline int mm_apitch(int C) { return mm_kpad(C) + 4; }   // conflict-free A
+constexpr int MM_UP = MM_N + 8;                                                // conflict-free B
 
 template <typename BT>
-__global__ void __launch_bounds__(kBlock) k_dualmm(Dims d, Inputs in, Work w, int step0, int ti) {
+__global__ void __launch_bounds__(MM_T) k_dualmm(Dims d, Inputs in, Work w, int step0, int ti) {
     extern __shared__ __align__(16) float dm_smem[];
-    const int C = d.C, D = d.D;
-    const int m0 = blockIdx.x * BM, d0 = blockIdx.y * BN, p = blockIdx.z;
+    const int C = d.C, D = d.D, K = mm_kpad(C), AP = mm_apitch(C);
+    const int m0 = blockIdx.x * MM_R, d0 = blockIdx.y * MM_N, p = blockIdx.z;
     const int n = (ti - step0) * d.P + p;
     const int nv = w.nvalid[n];
-    float *Xs = dm_smem;
-    float *Qs = Xs + BM * C;
-    float *Us = Qs + BM * C;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    float *Xs = dm_smem;                 // [16][AP]
+    float *Qs = Xs + MM_R * AP;          // [16][AP]
+    float *Us = Qs + MM_R * AP;          // [K][MM_UP]
     const float *X = w.X + (size_t)n * C * C;
     const float *QX = w.QX + (size_t)n * C * C;
-    const size_t tok0 = (size_t)p * d.T + (size_t)ti * C;
-    const BT *v = static_cast<const BT *>(in.v);
-    const float *ret = w.ret + (size_t)p * C * D;
+    const float *U = w.ret + (size_t)p * C * D;
     const float *inter = w.inter + (size_t)p * C * D;
+    const size_t tok0 = (size_t)p * d.T + (size_t)ti * C;
 
-    for (int idx = threadIdx.x; idx < BM * C; idx += kBlock) {
-        const int r = idx / C, k = idx - r * C;
-        const int row = m0 + r;
-        Xs[idx] = row < C ? X[(size_t)row * C + k] : 0.f;
-        Qs[idx] = row < C ? QX[(size_t)row * C + k] : 0.f;
+    // X, QX rows m0..m0+15 (zero past C and past column C), u_pre rows k < nv (zero beyond)
+    const bool a16 = (C & 3) == 0;
+    for (int idx = tid; idx < MM_R * K; idx += MM_T) {
+        const int r = idx / K, k = idx - r * K, row = m0 + r;
+        if (row < C && k < C) {
+            if (a16) {
+                if ((k & 3) == 0) {
+                    cp_async16(Xs + r * AP + k, X + (size_t)row * C + k);
+                    cp_async16(Qs + r * AP + k, QX + (size_t)row * C + k);
+                }
+            } else {
+                cp_async4(Xs + r * AP + k, X + (size_t)row * C + k);
+                cp_async4(Qs + r * AP + k, QX + (size_t)row * C + k);
+            }
+        } else {
+            Xs[r * AP + k] = 0.f;
+            Qs[r * AP + k] = 0.f;
+        }
     }
-    for (int idx = threadIdx.x; idx < C * BN; idx += kBlock) {
-        const int k = idx / BN, c = idx - k * BN;
-        const int col = d0 + c;
-        float u = 0.f;
-        if (k < nv && col < D)
-            u = in.beta[tok0 + k] * (to_f32(v[(tok0 + k) * D + col]) - ret[(size_t)k * D + col]);
-        Us[idx] = u;
+    const int ncol = D - d0 < MM_N ? D - d0 : MM_N;
+    for (int idx = tid; idx < K * (MM_N / 4); idx += MM_T) {
+        const int k = idx / (MM_N / 4), c = (idx - k * (MM_N / 4)) * 4;
+        if (k < nv && c < ncol) cp_async16(Us + k * MM_UP + c, U + (size_t)k * D + d0 + c);
+        else *reinterpret_cast<float4 *>(Us + k * MM_UP + c) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
+    cp_async_commit();
+    cp_async_wait<0>();
     __syncthreads();
 
-    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-    const int r0 = ty * 2, c0 = tx * 4;
-    float ax[2][4] = {}, aq[2][4] = {};
-    for (int k = 0; k < C; ++k) {
-        const float4 u = *reinterpret_cast<const float4 *>(Us + k * BN + c0);
-        const float uu[4] = {u.x, u.y, u.z, u.w};
+    const int g4 = lane >> 2, i4 = lane & 3;
+    const int mat = warp >> 1, nb = (warp & 1) * 4;          // this warp: matrix, first n8 tile
+    const float *A = mat ? Qs : Xs;
+    float acc[4][4];
 #pragma unroll
-        for (int rr = 0; rr < 2; ++rr) {
-            const float x = Xs[(r0 + rr) * C + k], q = Qs[(r0 + rr) * C + k];
+    for (int j = 0; j < 4; ++j)
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                ax[rr][cc] = fmaf(x, uu[cc], ax[rr][cc]);
-                aq[rr][cc] = fmaf(q, uu[cc], aq[rr][cc]);
+        for (int q = 0; q < 4; ++q) acc[j][q] = 0.f;
+    const int kend = mm_kpad(nv < C ? nv : C);                // u_pre is zero past nv
+    for (int k0 = 0; k0 < kend; k0 += 8) {
+        const float af[4] = {A[g4 * AP + k0 + i4], A[(g4 + 8) * AP + k0 + i4],
+                             A[g4 * AP + k0 + i4 + 4], A[(g4 + 8) * AP + k0 + i4 + 4]};
+        unsigned ah[4], al[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) ah[q] = to_tf32(af[q]);
+        if constexpr (sizeof(BT) == 4) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) al[q] = to_tf32(af[q] - __uint_as_float(ah[q]));
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int col = (nb + j) * 8 + g4;
+            const float bf[2] = {Us[(k0 + i4) * MM_UP + col], Us[(k0 + i4 + 4) * MM_UP + col]};
+            unsigned bh[2] = {to_tf32(bf[0]), to_tf32(bf[1])};
+            if constexpr (sizeof(BT) == 4) {
+                unsigned bl[2] = {to_tf32(bf[0] - __uint_as_float(bh[0])),
+                                  to_tf32(bf[1] - __uint_as_float(bh[1]))};
+                mma_tf32(acc[j], ah, bl);
+                mma_tf32(acc[j], al, bh);
             }
+            mma_tf32(acc[j], ah, bh);
         }
     }
+
     BT *out = static_cast<BT *>(in.readings);
 #pragma unroll
-    for (int rr = 0; rr < 2; ++rr) {
-        const int row = m0 + r0 + rr;
-        const int col = d0 + c0;
-        if (row >= C || col >= D) continue;
-        float dvv[4], rd[4];
-        const bool live = row < nv;
-        if (live) {
-            float it[4];
-            load_vec<float, 4, false>(inter + (size_t)row * D + col, it);
+    for (int j = 0; j < 4; ++j) {
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) { dvv[cc] = ax[rr][cc]; rd[cc] = aq[rr][cc] + it[cc]; }
-        } else {
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) { dvv[cc] = 0.f; rd[cc] = 0.f; }
+        for (int h = 0; h < 2; ++h) {                 // rows g4 and g4 + 8, two columns each
+            const int row = m0 + g4 + 8 * h, col = d0 + (nb + j) * 8 + 2 * i4;
+            if (row >= C || col >= D) continue;
+            const bool live = row < nv;
+            float o[2] = {live ? acc[j][2 * h] : 0.f, live ? acc[j][2 * h + 1] : 0.f};
+            if (mat == 0) {
+                store_vec<float, 2>(w.dv + ((size_t)p * C + row) * D + col, o);
+            } else if ((size_t)ti * C + row < (size_t)d.T) {
+                if (live) {
+                    float it[2];
+                    load_vec<float, 2, false>(inter + (size_t)row * D + col, it);
+                    o[0] += it[0];
+                    o[1] += it[1];
+                }
+                store_vec<BT, 2>(out + (tok0 + row) * D + col, o);
+            }
         }
-        store_vec<float, 4>(w.dv + ((size_t)p * C + row) * D + col, dvv);
-        if ((size_t)ti * C + row < (size_t)d.T) store_vec<BT, 4>(out + (tok0 + row) * D + col, rd);
     }
 }
 
@@ -365,16 +413,17 @@ cudaError_t launch_dw(const Dims &d, const Inputs &in, const Work &w, int step0,
 
 cudaError_t launch_dualmm(const Dims &d, const Inputs &in, const Work &w, int step0, int ti,
                           cudaStream_t st) {
-    const size_t smem = sizeof(float) * ((size_t)2 * BM * d.C + (size_t)d.C * BN);
-    dim3 grid((d.C + BM - 1) / BM, (d.D + BN - 1) / BN, d.P);
+    const size_t smem =
+        sizeof(float) * ((size_t)2 * MM_R * mm_apitch(d.C) + (size_t)mm_kpad(d.C) * MM_UP);
+    dim3 grid((d.C + MM_R - 1) / MM_R, (d.D + MM_N - 1) / MM_N, d.P);
     if (d.dtype == SDM_BF16) {
         auto kern = k_dualmm<__nv_bfloat16>;
         set_kernel_smem(kern, smem);
-        kern<<<grid, kBlock, smem, st>>>(d, in, w, step0, ti);
+        kern<<<grid, MM_T, smem, st>>>(d, in, w, step0, ti);
     } else {
         auto kern = k_dualmm<float>;
         set_kernel_smem(kern, smem);
-        kern<<<grid, kBlock, smem, st>>>(d, in, w, step0, ti);
+        kern<<<grid, MM_T, smem, st>>>(d, in, w, step0, ti);
     }
     return cudaGetLastError();
 }

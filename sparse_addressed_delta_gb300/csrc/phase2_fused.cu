@@ -104,27 +104,9 @@ __host__ __device__ inline int pipe_tail_bytes(int C, int W, int V) {
 }
 
 // ---------------------------------------------------------------------------------------
-// warp-level tensor-core product for the per-step dual matmul: mma.sync m16n8k8 with TF32
-// operands and f32 accumulation (a 64 x 64 by 64 x 8 product per CTA and step is far below
-// a tcgen05 tile; these stay in registers). Fragment layout (PTX ISA, m16n8k8 .tf32):
-// g = lane / 4, i = lane % 4; A: a0 (g, i), a1 (g + 8, i), a2 (g, i + 4), a3 (g + 8, i + 4);
-// B: b0 (i, g), b1 (i + 4, g); C: c0 (g, 2i), c1 (g, 2i + 1), c2 (g + 8, 2i), c3 (g + 8, 2i + 1).
+// the per-step dual matmul runs on the tensor cores with mma.sync (to_tf32 / mma_tf32 in the
+// internal header): a 64 x 64 by 64 x 8 product per CTA and step is far below a tcgen05 tile
 // ---------------------------------------------------------------------------------------
-__device__ __forceinline__ unsigned to_tf32(float x) {
-    unsigned r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
-}
-
-__device__ __forceinline__ void mma_tf32(float (&c)[4], const unsigned (&a)[4],
-                                         const unsigned (&b)[2]) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
-}
-
 template <typename BT>
 __device__ __forceinline__ void piece_to_f32(const uint4 &u, float (&o)[16 / sizeof(BT)]) {
     if constexpr (sizeof(BT) == 2) {

@@ -277,6 +277,25 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
+// TF32 tensor-core product of a 16 x 8 tile, f32 accumulation (mma.sync m16n8k8, PTX ISA
+// fragment layout: g = lane / 4, i = lane % 4; A: a0 (g, i), a1 (g + 8, i), a2 (g, i + 4),
+// a3 (g + 8, i + 4); B: b0 (i, g), b1 (i + 4, g); C: c0 (g, 2i), c1 (g, 2i + 1), c2 (g + 8, 2i),
+// c3 (g + 8, 2i + 1)). Float32 operands go through the 3xTF32 split (hi*lo + lo*hi + hi*hi).
+__device__ __forceinline__ unsigned to_tf32(float x) {
+    unsigned r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
+__device__ __forceinline__ void mma_tf32(float (&c)[4], const unsigned (&a)[4],
+                                         const unsigned (&b)[2]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
 // Bulk global -> shared copies completed on an mbarrier (the TMA unit moves the bytes; one
 // thread issues a copy). Addresses 16-byte aligned, sizes multiples of 16.
 __device__ __forceinline__ unsigned smem_u32(const void *p) {

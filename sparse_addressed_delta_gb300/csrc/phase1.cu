@@ -340,31 +340,48 @@ __global__ void __launch_bounds__(NT, 2) k_phase1(Dims d, Inputs in, Work w, int
             gw[e] = kk * expf(l);
             if (d.bwd) w.dwt[(size_t)n * CW + e] = dwv;
         }
+        // each read finds the last write of its slot at a token <= its own: an upper bound in
+        // the sorted write row, four reads per thread at a time, branch-free (the same probe
+        // count for all of them, so the four searches overlap)
         const unsigned magR = div_magic(R);
-        for (int er = tid; er < nr; er += NT) {
-            const int t = div_by(er, magR);
-            const int r = rs[er];
-            int lo = 0, hi = -1;
-            float l = 0.f;
-            if ((unsigned)r < (unsigned)S) {
-                const unsigned long long target =
-                    ((unsigned long long)(unsigned)r << 32) | ((unsigned)t << 8) | 255u;
-                int a = 0, b = nw;
-                while (a < b) {
-                    int mid = (a + b) >> 1;
-                    if (srt[mid] <= target) a = mid + 1; else b = mid;
-                }
-                const int pos = a - 1;
-                if (pos >= 0 && (int)(srt[pos] >> 32) == r) {
-                    hi = pos;
-                    lo = pgs[pos];
-                    l = lws[pos];
-                }
+        for (int er0 = tid; er0 < nr; er0 += 4 * NT) {
+            unsigned long long target[4];
+            int base[4], r[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int er = er0 + k * NT;
+                r[k] = er < nr ? rs[er] : -1;
+                const int t = er < nr ? div_by(er, magR) : 0;
+                target[k] = ((unsigned long long)(unsigned)r[k] << 32) | ((unsigned)t << 8) | 255u;
+                base[k] = 0;
             }
-            rlo[er] = lo;
-            rhi[er] = hi;
-            lr[er] = l;
-            qw[er] = ((unsigned)r < (unsigned)S) ? to_f32(q[er]) * expf(l) : 0.f;
+            for (int len = nw; len > 1;) {
+                const int half = len >> 1;
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    if (srt[base[k] + half - 1] <= target[k]) base[k] += half;
+                len -= half;
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int er = er0 + k * NT;
+                if (er >= nr) continue;
+                int lo = 0, hi = -1;
+                float l = 0.f;
+                const bool valid = (unsigned)r[k] < (unsigned)S;
+                if (valid && nw > 0) {
+                    const int pos = base[k] + (srt[base[k]] <= target[k] ? 1 : 0) - 1;
+                    if (pos >= 0 && (int)(srt[pos] >> 32) == r[k]) {
+                        hi = pos;
+                        lo = pgs[pos];
+                        l = lws[pos];
+                    }
+                }
+                rlo[er] = lo;
+                rhi[er] = hi;
+                lr[er] = l;
+                qw[er] = valid ? to_f32(q[er]) * expf(l) : 0.f;
+            }
         }
         __syncthreads();
 

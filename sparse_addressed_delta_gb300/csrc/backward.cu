@@ -192,7 +192,7 @@ __global__ void __launch_bounds__(NTB) k_b_mm1(Dims d, Inputs in, Work w, const 
 }
 
 // ---------------------------------------------------------------------------------------
-// batched FFMA GEMM: Out[b] = alpha op(A[b]) op(B[b]) (+ Out[b]), then a mask
+// batched GEMM: Out[b] = alpha op(A[b]) op(B[b]) (+ Out[b]), then a mask
 // ---------------------------------------------------------------------------------------
 struct GemmOp {
     const float *A, *B;
@@ -207,56 +207,89 @@ struct GemmOp {
 };
 
 constexpr int GT = 64, GK = 16;
+constexpr int GAP = GK + 4;     // A tile [64][GK] pitch: conflict-free fragment loads
+constexpr int GBP = GT + 8;     // B tile [GK][64] pitch: conflict-free fragment loads
+constexpr int GTHREADS = 128;   // 4 warps, a 32 x 32 quarter of the 64 x 64 tile each
 
-__global__ void __launch_bounds__(NTB) k_bgemm(GemmOp g) {
-    __shared__ float As[GK][GT + 4];
-    __shared__ float Bs[GK][GT + 4];
+// Batched GEMM on the tensor cores: mma.sync m16n8k8 with the 3xTF32 split (hi*lo + lo*hi +
+// hi*hi), which keeps float32 accuracy; every output element sums its k terms in a fixed order.
+__global__ void __launch_bounds__(GTHREADS) k_bgemm(GemmOp g) {
+    __shared__ __align__(16) float As[GT * GAP];
+    __shared__ __align__(16) float Bs[GK * GBP];
     const int b = blockIdx.z;
     const int m0 = blockIdx.y * GT, n0 = blockIdx.x * GT;
     const float *A = g.A + b * g.sa;
     const float *B = g.B + b * g.sb;
     float *O = g.Out + b * g.so;
-    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-    float acc[4][4] = {};
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g4 = lane >> 2, i4 = lane & 3;
+    const int wm = (warp >> 1) * 32, wn = (warp & 1) * 32;
+    float acc[2][4][4];
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[i][j][q] = 0.f;
     for (int k0 = 0; k0 < g.K; k0 += GK) {
-        for (int idx = threadIdx.x; idx < GK * GT; idx += NTB) {
-            const int kk = idx / GT, mm = idx - kk * GT;
+        for (int idx = tid; idx < GK * GT; idx += GTHREADS) {
+            // consecutive threads on the operand's contiguous index
+            const int kk = g.ta ? idx / GT : idx % GK, mm = g.ta ? idx % GT : idx / GK;
             const int gm = m0 + mm, gk = k0 + kk;
-            float a = 0.f;
-            if (gm < g.M && gk < g.K) a = g.ta ? A[(size_t)gk * g.lda + gm] : A[(size_t)gm * g.lda + gk];
-            As[kk][mm] = a;
-            const int gn = n0 + mm;
-            float bb = 0.f;
-            if (gn < g.N && gk < g.K) bb = g.tb ? B[(size_t)gn * g.ldb + gk] : B[(size_t)gk * g.ldb + gn];
-            Bs[kk][mm] = bb;
+            As[mm * GAP + kk] = (gm < g.M && gk < g.K)
+                                    ? (g.ta ? A[(size_t)gk * g.lda + gm] : A[(size_t)gm * g.lda + gk])
+                                    : 0.f;
+            const int kb = g.tb ? idx % GK : idx / GT, nn = g.tb ? idx / GK : idx % GT;
+            const int gn = n0 + nn, gkb = k0 + kb;
+            Bs[kb * GBP + nn] = (gn < g.N && gkb < g.K)
+                                    ? (g.tb ? B[(size_t)gn * g.ldb + gkb] : B[(size_t)gkb * g.ldb + gn])
+                                    : 0.f;
         }
         __syncthreads();
 #pragma unroll
-        for (int kk = 0; kk < GK; ++kk) {
-            float a[4], bb[4];
+        for (int ks = 0; ks < GK; ks += 8) {
+            unsigned ah[2][4], al[2][4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) { a[i] = As[kk][ty * 4 + i]; bb[i] = Bs[kk][tx * 4 + i]; }
+            for (int i = 0; i < 2; ++i) {
+                const float *Ar = As + (wm + 16 * i + g4) * GAP + ks + i4;
+                const float af[4] = {Ar[0], Ar[8 * GAP], Ar[4], Ar[8 * GAP + 4]};
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+                for (int q = 0; q < 4; ++q) {
+                    ah[i][q] = to_tf32(af[q]);
+                    al[i][q] = to_tf32(af[q] - __uint_as_float(ah[i][q]));
+                }
+            }
 #pragma unroll
-                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], bb[j], acc[i][j]);
+            for (int j = 0; j < 4; ++j) {
+                const float *Bc = Bs + (ks + i4) * GBP + wn + 8 * j + g4;
+                const float bf[2] = {Bc[0], Bc[4 * GBP]};
+                const unsigned bh[2] = {to_tf32(bf[0]), to_tf32(bf[1])};
+                const unsigned bl[2] = {to_tf32(bf[0] - __uint_as_float(bh[0])),
+                                        to_tf32(bf[1] - __uint_as_float(bh[1]))};
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    mma_tf32(acc[i][j], ah[i], bl);
+                    mma_tf32(acc[i][j], al[i], bh);
+                    mma_tf32(acc[i][j], ah[i], bh);
+                }
+            }
         }
         __syncthreads();
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int r = m0 + ty * 4 + i;
-        if (r >= g.M) continue;
+    for (int i = 0; i < 2; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int c = n0 + tx * 4 + j;
-            if (c >= g.N) continue;
-            float v = g.alpha * acc[i][j];
-            if (g.accum) v += O[(size_t)r * g.ldo + c];
-            if ((g.mask == 1 && c > r) || (g.mask == 2 && c >= r)) v = 0.f;
-            O[(size_t)r * g.ldo + c] = v;
-        }
-    }
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int r = m0 + wm + 16 * i + g4 + (q >> 1) * 8;
+                const int c = n0 + wn + 8 * j + 2 * i4 + (q & 1);
+                if (r >= g.M || c >= g.N) continue;
+                float v = g.alpha * acc[i][j][q];
+                if (g.accum) v += O[(size_t)r * g.ldo + c];
+                if ((g.mask == 1 && c > r) || (g.mask == 2 && c >= r)) v = 0.f;
+                O[(size_t)r * g.ldo + c] = v;
+            }
 }
 
 // dA = beta dL (strictly lower, in place) and grad_beta = <dL, A> per row + the mm1 partials
@@ -608,7 +641,7 @@ void set_smem(T kern, size_t bytes) {
 
 void gemm(const GemmOp &g, int batch, cudaStream_t st) {
     dim3 grid((g.N + GT - 1) / GT, (g.M + GT - 1) / GT, batch);
-    k_bgemm<<<grid, NTB, 0, st>>>(g);
+    k_bgemm<<<grid, GTHREADS, 0, st>>>(g);
 }
 
 template <typename BT, int CPL>

@@ -490,26 +490,26 @@ __global__ void __launch_bounds__(NTB) k_b_phase1(Dims d, Inputs in, Work w, flo
     auto kval = [&](unsigned low) {   // write weight of a sorted write key's entry
         return to_f32(kin[(int)(low >> 8) * W + (int)(low & 255u)]);
     };
-    // the last write of slot r at a token <= t, as a sorted position (-1: none)
-    auto last_write = [&](unsigned r, int t) {
-        const unsigned long long target = ((unsigned long long)r << 32) | ((unsigned)t << 8) | 255u;
-        int a = 0, b = nw;
-        while (a < b) {
-            const int mid = (a + b) >> 1;
-            if (wkey[mid] <= target) a = mid + 1; else b = mid;
+    // branch-free searches in a sorted key row, K at a time (the same probe count for all, so
+    // the K searches overlap): upper bound (first key > target) or lower bound (first key >=)
+    extern __shared__ int32_t bp1_found[];   // per entry of this CTA's share (see below)
+    auto bounds = [&](const unsigned long long *row, int len0, const unsigned long long (&tg)[4],
+                      bool upper, int (&res)[4]) {
+        int base[4] = {0, 0, 0, 0};
+        for (int len = len0; len > 1;) {
+            const int half = len >> 1;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const unsigned long long v = row[base[k] + half - 1];
+                if (upper ? v <= tg[k] : v < tg[k]) base[k] += half;
+            }
+            len -= half;
         }
-        const int pos = a - 1;
-        return (pos >= 0 && (unsigned)(wkey[pos] >> 32) == r) ? pos : -1;
-    };
-    // first sorted read position with key >= (r, t)
-    auto read_lower = [&](unsigned r, int t) {
-        const unsigned long long target = ((unsigned long long)r << 32) | ((unsigned)t << 8);
-        int a = 0, b = nr;
-        while (a < b) {
-            const int mid = (a + b) >> 1;
-            if (rkey[mid] < target) a = mid + 1; else b = mid;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const unsigned long long v = len0 > 0 ? row[base[k]] : 0ull;
+            res[k] = len0 > 0 ? base[k] + ((upper ? v <= tg[k] : v < tg[k]) ? 1 : 0) : 0;
         }
-        return a;
     };
 
     // this CTA's share [b0, b1) of the n entries of a stage
@@ -523,6 +523,27 @@ __global__ void __launch_bounds__(NTB) k_b_phase1(Dims d, Inputs in, Work w, flo
     // (i) reads: dq and the gradient of their running log-decay
     if (stage == 0) {
     share(nr, b0, b1);
+    // the last write of each read's slot at a token <= the read's (-1: none)
+    for (int i0 = b0 + (int)threadIdx.x; i0 < b1; i0 += 4 * NTB) {
+        unsigned long long tg[4];
+        int res[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int i = i0 + k * NTB < b1 ? i0 + k * NTB : b0;
+            const unsigned long long key = rkey[i];
+            tg[k] = (key & 0xffffffff00000000ull) | (((unsigned)key >> 8) << 8) | 255u;
+        }
+        bounds(wkey, nw, tg, true, res);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int i = i0 + k * NTB;
+            if (i >= b1) continue;
+            const int pos = res[k] - 1;
+            bp1_found[i - b0] =
+                (pos >= 0 && (wkey[pos] >> 32) == (tg[k] >> 32)) ? pos : -1;
+        }
+    }
+    __syncthreads();
     for (int rp = b0 + warp; rp < b1; rp += NWB) {
         const unsigned long long key = rkey[rp];
         const unsigned r = (unsigned)(key >> 32);
@@ -531,7 +552,7 @@ __global__ void __launch_bounds__(NTB) k_b_phase1(Dims d, Inputs in, Work w, flo
         float dq = 0.f, dl = 0.f;
         if (r < S) {
             const float q = to_f32(qin[e]), l = lr[e];
-            const int hi = last_write(r, t);
+            const int hi = bp1_found[rp - b0];
             float sum = 0.f;
             if (hi >= 0) {
                 for (int m = pgs[hi] + lane; m <= hi; m += 32) {
@@ -559,6 +580,28 @@ __global__ void __launch_bounds__(NTB) k_b_phase1(Dims d, Inputs in, Work w, flo
     // (ii) writes: dk and the gradient of their running log-decay
     if (stage == 1) {
     share(nw, b0, b1);
+    // the sorted reads of each write's slot at tokens >= the write's: [r0, r1)
+    for (int i0 = b0 + (int)threadIdx.x; i0 < b1; i0 += 2 * NTB) {
+        unsigned long long tg[4];
+        int res[4];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int i = i0 + k * NTB < b1 ? i0 + k * NTB : b0;
+            const unsigned long long key = wkey[i];
+            const unsigned long long slot = key & 0xffffffff00000000ull;
+            tg[2 * k] = slot | (((unsigned)key >> 8) << 8);
+            tg[2 * k + 1] = slot | ((unsigned long long)C << 8);
+        }
+        bounds(rkey, nr, tg, false, res);
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int i = i0 + k * NTB;
+            if (i >= b1) continue;
+            bp1_found[2 * (i - b0)] = res[2 * k];
+            bp1_found[2 * (i - b0) + 1] = res[2 * k + 1];
+        }
+    }
+    __syncthreads();
     for (int pa = b0 + warp; pa < b1; pa += NWB) {
         const unsigned long long key = wkey[pa];
         const unsigned s = (unsigned)(key >> 32);
@@ -579,7 +622,7 @@ __global__ void __launch_bounds__(NTB) k_b_phase1(Dims d, Inputs in, Work w, flo
                 s2 = fmaf(dA[(size_t)(lc >> 8) * C + ta], kval(lc) * expf(lws[m] - la), s2);
             }
             const int tnext = (pa + 1 < ge) ? (int)((unsigned)wkey[pa + 1] >> 8) : C;
-            const int r0 = read_lower(s, ta), r1 = read_lower(s, C);
+            const int r0 = bp1_found[2 * (pa - b0)], r1 = bp1_found[2 * (pa - b0) + 1];
             for (int m = r0 + lane; m < r1; m += 32) {
                 const unsigned lr_ = (unsigned)rkey[m];
                 const int tr = (int)(lr_ >> 8), er = tr * R + (int)(lr_ & 255u);
@@ -687,9 +730,12 @@ cudaError_t backward_step(const Dims &d, const Inputs &in, const Work &w, const 
     const int gmax = (8 * kRefSms + P - 1) / P;
     if (gb > gmax) gb = gmax;
     if (gb < 1) gb = 1;
+    const int most = d.C * (d.W > d.R ? d.W : d.R);
+    const size_t found_bytes = 2 * sizeof(int32_t) * (size_t)((most + gb - 1) / gb);
+    set_smem(k_b_phase1<BT>, found_bytes);
     for (int stage = 0; stage < 3; ++stage)
-        k_b_phase1<BT><<<dim3(gb, P), NTB, 0, st>>>(d, in, w, o.grad_write_w, o.grad_log_decay,
-                                                   o.grad_read_w, step0, ti, stage);
+        k_b_phase1<BT><<<dim3(gb, P), NTB, found_bytes, st>>>(
+            d, in, w, o.grad_write_w, o.grad_log_decay, o.grad_read_w, step0, ti, stage);
     return cudaGetLastError();
 }
 

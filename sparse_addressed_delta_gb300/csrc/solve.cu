@@ -34,6 +34,8 @@ __host__ __device__ __forceinline__ bool solve_links(const Dims &d) { return !d.
 // instead of one per block row); from C = 64 on the copies would cost more in CTAs per SM
 // than they save
 __host__ __device__ __forceinline__ bool solve_staged(const Dims &d) { return d.C <= 32 && d.C % 4 == 0; }
+// QK alone (read only by the last phase, so its copy lands under the earlier ones) up to C = 64
+__host__ __device__ __forceinline__ bool solve_staged_qk(const Dims &d) { return d.C <= 64 && d.C % 4 == 0; }
 __host__ __device__ __forceinline__ int staged_pitch(int C) { return C + 4; }
 
 // dynamic shared memory: X blocks, L/QK block row, T blocks; then (staged) A, QK [C][C+4] and
@@ -47,10 +49,12 @@ __host__ __device__ inline SolveSmem solve_layout(const Dims &d) {
     SolveSmem L;
     size_t o = sizeof(float) * (size_t)(tri(nb) + 2 * nb) * BB;
     L.a = L.q = L.beta = L.gsl = L.ent = o;
-    if (solve_staged(d)) {
-        const size_t m = sizeof(float) * (size_t)d.C * staged_pitch(d.C);
-        L.a = o; o += m;
+    const size_t m = sizeof(float) * (size_t)d.C * staged_pitch(d.C);
+    if (solve_staged_qk(d)) {
         L.q = o; o += m;
+    }
+    if (solve_staged(d)) {
+        L.a = o; o += m;
         L.beta = o; o += sizeof(float) * (size_t)d.C;
     }
     if (solve_links(d)) {
@@ -83,26 +87,34 @@ __global__ void __launch_bounds__(NTS) k_solve(Dims d, Inputs in, Work w, int st
     float *Lr = Xp + tri(nb) * BB;               // current block row of L / QK  [nb][16][16]
     float *Tb = Lr + nb * BB;                    // T blocks                     [nb][16][16]
 
-    // staged copies of the valid rows of A and QK and of beta (cp.async, 16 bytes a copy)
-    const bool staged = solve_staged(d);
-    int ap = C;
+    // staged copies of the valid rows of QK (and for small chunks of A and beta): cp.async,
+    // 16 bytes a copy, landing while the links and the first phases run
+    const bool staged = solve_staged(d), staged_qk = solve_staged_qk(d);
+    int ap = C, qp = C;
+    if (staged_qk) {
+        float *Qs = reinterpret_cast<float *>(sraw + SL.q);
+        qp = staged_pitch(C);
+        const int q4 = C / 4;
+        for (int i = tid; i < nv * q4; i += NTS) {
+            const int r = i / q4, k = (i - r * q4) * 4;
+            cp_async16(Qs + r * qp + k, QK + (size_t)r * C + k);
+        }
+        QK = Qs;
+    }
     if (staged) {
         float *As = reinterpret_cast<float *>(sraw + SL.a);
-        float *Qs = reinterpret_cast<float *>(sraw + SL.q);
         float *bs = reinterpret_cast<float *>(sraw + SL.beta);
         ap = staged_pitch(C);
         const int q4 = C / 4;
         for (int i = tid; i < nv * q4; i += NTS) {
             const int r = i / q4, k = (i - r * q4) * 4;
             cp_async16(As + r * ap + k, A + (size_t)r * C + k);
-            cp_async16(Qs + r * ap + k, QK + (size_t)r * C + k);
         }
         for (int r = tid; r < nv; r += NTS) cp_async4(bs + r, beta + r);
-        cp_async_commit();
         A = As;
-        QK = Qs;
         beta = bs;
     }
+    cp_async_commit();
 
     // Links for the pipelined Phase 2 (every chunk after the first of the slab): an entry
     // whose slot the stream's previous step writes is pointed at that group's new piece
@@ -148,6 +160,7 @@ __global__ void __launch_bounds__(NTS) k_solve(Dims d, Inputs in, Work w, int st
     }
     if (staged) cp_async_wait<0>();
     __syncthreads();
+    const bool qk_ready = !staged_qk || staged;   // else the QK copy is awaited before QX
 
     // L (or QK) element (R, K) of the chunk, zero outside the valid tokens
     auto lval = [&](int R, int K) {
@@ -212,12 +225,16 @@ __global__ void __launch_bounds__(NTS) k_solve(Dims d, Inputs in, Work w, int st
     }
 
     // 3. QX, block row by block row; written out with X
+    if (!qk_ready) {
+        cp_async_wait<0>();
+        __syncthreads();
+    }
     for (int i = 0; i < nb; ++i) {
         if (i < nvb) {
             for (int e = tid; e < (i + 1) * BB; e += NTS) {
                 const int k = e / BB, rc = e - k * BB, r = rc / BS, c = rc - r * BS;
                 const int R = i * BS + r, K = k * BS + c;
-                Lr[e] = (R < nv && K <= R) ? QK[(size_t)R * ap + K] : 0.f;
+                Lr[e] = (R < nv && K <= R) ? QK[(size_t)R * qp + K] : 0.f;
             }
             __syncthreads();
             for (int e = tid; e < (i + 1) * BB; e += NTS) {

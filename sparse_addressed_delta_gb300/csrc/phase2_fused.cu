@@ -8,10 +8,13 @@
 // decay-and-write are all column-wise. A CTA therefore reads and writes only its own columns
 // of its own stream's rows, step after step, and only ever waits on its own threads.
 //
-// The bank pieces a step writes are read back by the next step's gather through L1/L2 in the
-// same CTA, ordered by the step's closing barrier (no read-only cache path). The kernel
-// runs when two stages of per-step metadata fit in shared memory (launch_phase2_fused says
-// whether); larger chunks use the per-step kernels of phase2.cu.
+// The bank rows a step writes reach the next step without a memory round trip: the solve kernel
+// links each entry of a chunk to the group of the previous step that writes its slot, and the
+// DW keeps every group's new piece in shared memory; every other row is loaded from the bank
+// one step early (it is final once the step before has ended: ordered by the closing barrier,
+// plain loads, no read-only cache path). The kernel runs when two stages of per-step metadata
+// fit in shared memory (launch_phase2_fused says whether); larger chunks use the per-step
+// kernels of phase2.cu.
 #include "sdm_internal.cuh"
 
 namespace sdm {
@@ -22,13 +25,14 @@ struct Vec16 {                  // one 16-byte piece of a bank row
     static constexpr int N = 16 / sizeof(BT);
 };
 
-// Pipelined variant for chunks whose per-step metadata fits in shared memory twice: the
-// next step's slots, weights, X, QX and sorted member records are brought into the other
-// stage by bulk copies (the TMA unit, one mbarrier per stage) and its v pieces and beta by
-// cp.async, while the current step computes. The gather keeps the B0 pieces of the written rows
-// in shared memory; the dual matmul runs on the tensor cores; the DW gives each group (distinct
-// written slot) to one thread, which sums its members in sorted order from shared memory and
-// writes the row once:
+// Pipelined variant for chunks whose per-step metadata fits in shared memory twice: a
+// producer warp brings the next step's slots/links, weights, member records, DW order, X and
+// QX into the other stage with bulk copies (the TMA unit; part A, the slots and links, on its
+// own mbarrier so that the early loads can start) and its v pieces and beta with cp.async,
+// while the 16 compute warps run the current step. The gather keeps the B0 pieces of the
+// written rows in shared memory; the dual matmul runs on the tensor cores; the DW gives each
+// hot group a warp and every other group a thread, which sum the members in sorted order from
+// shared memory and write the row once:
 //   B[s] = (sum of dw * delta_v over the group, sorted order) + exp(lend) * B0[s].
 // ---------------------------------------------------------------------------------------
 constexpr int NT2 = 512;          // compute threads (16 warps)

@@ -5,7 +5,8 @@
 // One CTA per chunk (a persistent grid walks the slab's chunks). For chunk (p, ti) with n
 // valid tokens:
 //   1. the n*W write entries e = t*W + j are sorted by (slot, e): a stable LSD radix sort on
-//      the slot bits of 64-bit keys (slot << 32 | e), in global scratch private to the CTA;
+//      the slot bits of 64-bit keys (slot << 32 | t << 8 | j), in shared memory when the
+//      chunk's scratch fits (else in global scratch private to the CTA);
 //   2. a group is a run of one slot in that row; its members are the slot's writes in token
 //      order. A segmented scan of g along the row gives lw, the running log-decay of the slot
 //      at each write (inclusive), and its group total lend;
@@ -15,7 +16,11 @@
 //   4. A[t][u] = sum over pairs of writes of one slot at tokens u < t of
 //      k_t k_u exp(lw_t - lw_u), and QK[t][u] = the same over (read at t, write at u <= t)
 //      with q_t and lr_t: one warp per row, its lanes over the earlier members of each group
-//      (distinct tokens, so no two lanes add to one element), entries of the row in order.
+//      (distinct tokens, so no two lanes add to one element), entries of the row in order;
+//   5. (backward mode) the sorted write row with its running sums and group bounds, and the
+//      read entries sorted by slot with their groups;
+//   6. for the pipelined Phase 2: the slots of the entries (Work::wsl / rsl) and the DW order
+//      of the groups (hot groups first, then by size).
 // Every exponent is a difference of running log-decays of one slot; all sums run in a fixed
 // order, so the outputs are bitwise reproducible.
 #include "sdm_internal.cuh"

@@ -265,10 +265,13 @@ __global__ void __launch_bounds__(MM_T) k_dualmm(Dims d, Inputs in, Work w, int 
 }
 
 // ---------------------------------------------------------------------------------------
-// DW: one warp per group (distinct written slot) of each chunk of the step
+// DW: one warp per group (distinct written slot) of each chunk of the step; a warp takes NG
+// groups at once (the next ones of its stride) so that their metadata and B0 row loads are in
+// flight together
 // ---------------------------------------------------------------------------------------
 template <typename BT, int CPL>
 __global__ void __launch_bounds__(kBlock) k_dw(Dims d, Inputs in, Work w, int step0, int ti) {
+    constexpr int NG = CPL <= 8 ? 2 : 1;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int p = blockIdx.y;
     const int n = (ti - step0) * d.P + p;
@@ -281,40 +284,63 @@ __global__ void __launch_bounds__(kBlock) k_dw(Dims d, Inputs in, Work w, int st
     const float *wdw = w.wdw + (size_t)n * CW;
     const float *dvp = w.dv + (size_t)p * C * D + lane * CPL;
     BT *bank = static_cast<BT *>(in.bank) + (size_t)p * d.S * D + lane * CPL;
-    for (int g = blockIdx.x * kWarps + warp; g < ng; g += gridDim.x * kWarps) {
-        const int o0 = goff[g], o1 = goff[g + 1];
-        if ((unsigned)gslot[g] >= (unsigned)d.S) continue;
-        BT *row = bank + (size_t)gslot[g] * D;
-        const float f = gfac[g];
-        float acc[CPL];
-        load_vec<BT, CPL, false>(row, acc);
-        if (in.snap)
-            store_vec<BT, CPL>(static_cast<BT *>(in.snap) +
-                                   ((size_t)(ti * d.P + p) * CW + (o1 - 1)) * D + lane * CPL,
-                               acc);
+    const int stride = gridDim.x * kWarps;
+    for (int g0 = blockIdx.x * kWarps + warp; g0 < ng; g0 += NG * stride) {
+        int o0[NG], o1[NG];
+        bool live[NG];
+        BT *row[NG];
+        float f[NG], acc[NG][CPL];
 #pragma unroll
-        for (int c = 0; c < CPL; ++c) acc[c] *= f;
-        int m = o0;
-        for (; m + 4 <= o1; m += 4) {
-            float x[4][CPL], wt[4];
+        for (int k = 0; k < NG; ++k) {
+            const int g = g0 + k * stride;
+            live[k] = g < ng;
+            const int sl = live[k] ? gslot[g] : -1;
+            live[k] = live[k] && (unsigned)sl < (unsigned)d.S;
+            o0[k] = live[k] ? goff[g] : 0;
+            o1[k] = live[k] ? goff[g + 1] : 0;
+            f[k] = live[k] ? gfac[g] : 0.f;
+            row[k] = bank + (size_t)(live[k] ? sl : 0) * D;
+        }
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                wt[u] = wdw[m + u];
-                load_vec<float, CPL, false>(dvp + (size_t)(perm[m + u] / W) * D, x[u]);
+        for (int k = 0; k < NG; ++k) {
+            if (live[k]) {
+                load_vec<BT, CPL, false>(row[k], acc[k]);
+            } else {
+#pragma unroll
+                for (int c = 0; c < CPL; ++c) acc[k][c] = 0.f;
             }
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-#pragma unroll
-                for (int c = 0; c < CPL; ++c) acc[c] = fmaf(wt[u], x[u][c], acc[c]);
         }
-        for (; m < o1; ++m) {
-            float x[CPL];
-            const float wt = wdw[m];
-            load_vec<float, CPL, false>(dvp + (size_t)(perm[m] / W) * D, x);
 #pragma unroll
-            for (int c = 0; c < CPL; ++c) acc[c] = fmaf(wt, x[c], acc[c]);
+        for (int k = 0; k < NG; ++k) {
+            if (!live[k]) continue;
+            if (in.snap)
+                store_vec<BT, CPL>(static_cast<BT *>(in.snap) +
+                                       ((size_t)(ti * d.P + p) * CW + (o1[k] - 1)) * D + lane * CPL,
+                                   acc[k]);
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) acc[k][c] *= f[k];
+            int m = o0[k];
+            for (; m + 4 <= o1[k]; m += 4) {
+                float x[4][CPL], wt[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    wt[u] = wdw[m + u];
+                    load_vec<float, CPL, false>(dvp + (size_t)(perm[m + u] / W) * D, x[u]);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+#pragma unroll
+                    for (int c = 0; c < CPL; ++c) acc[k][c] = fmaf(wt[u], x[u][c], acc[k][c]);
+            }
+            for (; m < o1[k]; ++m) {
+                float x[CPL];
+                const float wt = wdw[m];
+                load_vec<float, CPL, false>(dvp + (size_t)(perm[m] / W) * D, x);
+#pragma unroll
+                for (int c = 0; c < CPL; ++c) acc[k][c] = fmaf(wt, x[c], acc[k][c]);
+            }
+            store_vec<BT, CPL>(row[k], acc[k]);
         }
-        store_vec<BT, CPL>(row, acc);
     }
 }
 

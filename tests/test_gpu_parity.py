@@ -62,6 +62,19 @@ def test_widths(W, R):
                          slots="zipf1.1", seed=W * 100 + R))
 
 
+@pytest.mark.parametrize("C,W,R,dtype", [(64, 20, 20, "bf16"), (32, 40, 40, "f32")])
+def test_pipelined_more_entries_than_early_loads(C, W, R, dtype):
+    """Pipelined Phase 2 with more than four entries per gather lane: the entries past the
+    early-loaded ones (linked or not) are fetched in the step itself. Small banks make many
+    entries link to the previous step's groups."""
+    wl = small_workload(P=2, T=5 * C + 3, C=C, S=300, D=128, W=W, R=R, dtype=dtype,
+                        slots="zipf1.1", seed=C + W)
+    shape = sdm.make_shape(wl.P, wl.T, wl.C, wl.S, wl.D, wl.W, wl.R,
+                           torch.float32 if dtype == "f32" else torch.bfloat16)
+    assert sdm.launch_count(shape) == 3          # the pipelined kernel runs
+    check(wl)
+
+
 def test_dense_collisions_tiny_bank():
     """A bank of W rows: every token writes every row (groups of the whole chunk)."""
     check(small_workload(P=2, T=130, C=64, S=8, D=32, W=8, R=8, slots="uniform", seed=5))

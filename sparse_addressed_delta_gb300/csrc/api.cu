@@ -102,6 +102,7 @@ int slab_steps(const Dims &d, int requested) {
 
 int phase1_ctas(const Dims &d, int ns) {
     const long N = (long)ns * d.P;
+    if (phase1_split(d)) return (int)N;   // one CTA, and one scratch slot, per chunk
     const long cap = (long)(d.C * d.W <= 4096 ? 2 : 1) * kRefSms;
     return (int)(N < cap ? N : cap);
 }
@@ -113,6 +114,7 @@ int phase1_ctas(const Dims &d, int ns) {
     F(wdw, float, N * CW)                                                     \
     F(goff, int32_t, N * (CW + 4))                                            \
     F(ng4, int4, N)                                                           \
+    F(p1sel, int32_t, N)                                                      \
     F(gord, int32_t, N * CW)                                                  \
     F(gslot, int32_t, N * CW)                                                 \
     F(gfac, float, N * CW)                                                    \
@@ -344,7 +346,8 @@ int64_t sdm_launch_count(const sdm_shape *shape) {
     Prepared pr;
     if (prepare(shape, pr)) return 0;
     const int64_t slabs = (pr.d.Nt + pr.ns - 1) / pr.ns;
-    return pr.d.per_step ? slabs * 2 + (int64_t)pr.d.Nt * 3 : slabs * 3;
+    const int64_t p1 = phase1_split(pr.d) ? 2 : 1;   // Phase 1 (+ its row kernel), per slab
+    return pr.d.per_step ? slabs * (p1 + 1) + (int64_t)pr.d.Nt * 3 : slabs * (p1 + 2);
 }
 
 int sdm_write_read(const sdm_shape *shape, void *bank, const int32_t *write_slots,

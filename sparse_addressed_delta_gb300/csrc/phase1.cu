@@ -178,6 +178,161 @@ __device__ __forceinline__ void report_bad_slot(DevStatus *st, int token) {
     st->code = SDM_ERR_DEVICE;
 }
 
+// Pointers and counts of one chunk for Phase-1 steps 3 and 4 (the sorted write row and the
+// scratch of steps 1-2, in shared or global memory).
+template <typename WT>
+struct P1Chunk {
+    const int32_t *rs;
+    const WT *q;
+    const unsigned long long *srt;
+    const float2 *tkk;
+    const int32_t *inv, *pgid, *pgs;
+    const float *lws, *lend, *kf;
+    int32_t *rlo, *rhi;
+    float *wdw, *gw, *qw, *lr, *A, *QK, *dwt;
+    int nv, nw, nr, C, W, R, S;
+};
+
+// 3a. weights of the sorted positions [pos0, pos1): gw = k exp(lw), dw = k exp(lend - lw)
+template <typename WT>
+__device__ void p1_weights(const P1Chunk<WT> &c, int pos0, int pos1, int tid, int nthr) {
+    for (int pos = pos0 + tid; pos < pos1; pos += nthr) {
+        const unsigned low = (unsigned)c.srt[pos];
+        const int e = (int)(low >> 8) * c.W + (int)(low & 255u);
+        const float kk = c.kf[e];
+        const float l = c.lws[pos];
+        const float dwv = kk * expf(c.lend[c.pgid[pos]] - l);
+        c.wdw[pos] = dwv;
+        c.gw[e] = kk * expf(l);
+        if (c.dwt) c.dwt[e] = dwv;
+    }
+}
+
+// 3b. each read entry in [er_lo, er_hi) finds the last write of its slot at a token <= its own:
+// an upper bound in the sorted write row, four reads per thread at a time, branch-free (the
+// same probe count for all of them, so the four searches overlap); then lr and qw
+template <typename WT>
+__device__ void p1_reads(const P1Chunk<WT> &c, int er_lo, int er_hi, int tid, int nthr) {
+    const unsigned magR = div_magic(c.R);
+    for (int er0 = er_lo + tid; er0 < er_hi; er0 += 4 * nthr) {
+        unsigned long long target[4];
+        int base[4], r[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int er = er0 + k * nthr;
+            r[k] = er < er_hi ? c.rs[er] : -1;
+            const int t = er < er_hi ? div_by(er, magR) : 0;
+            target[k] = ((unsigned long long)(unsigned)r[k] << 32) | ((unsigned)t << 8) | 255u;
+            base[k] = 0;
+        }
+        for (int len = c.nw; len > 1;) {
+            const int half = len >> 1;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                if (c.srt[base[k] + half - 1] <= target[k]) base[k] += half;
+            len -= half;
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int er = er0 + k * nthr;
+            if (er >= er_hi) continue;
+            int lo = 0, hi = -1;
+            float l = 0.f;
+            const bool valid = (unsigned)r[k] < (unsigned)c.S;
+            if (valid && c.nw > 0) {
+                const int pos = base[k] + (c.srt[base[k]] <= target[k] ? 1 : 0) - 1;
+                if (pos >= 0 && (int)(c.srt[pos] >> 32) == r[k]) {
+                    hi = pos;
+                    lo = c.pgs[pos];
+                    l = c.lws[pos];
+                }
+            }
+            c.rlo[er] = lo;
+            c.rhi[er] = hi;
+            c.lr[er] = l;
+            c.qw[er] = valid ? to_f32(c.q[er]) * expf(l) : 0.f;
+        }
+    }
+}
+
+// 4. rows [t0, t1) of A and QK, one warp per token row. The row's entries are looked up one per
+//    lane; entries with earlier members of their group (a ballot) are then taken in entry
+//    order, the lanes over those members. (token, k) of every sorted position is kept in the
+//    free radix buffer, next to its running log-decay.
+template <typename WT>
+__device__ void p1_gram(const P1Chunk<WT> &c, int t0, int t1, int warp, int nwarps, int lane,
+                        float *row) {
+    const int C = c.C, W = c.W, R = c.R;
+    for (int t = t0 + warp; t < t1; t += nwarps) {
+        for (int x = lane; x < C; x += 32) row[x] = 0.f;
+        __syncwarp();
+        if (t < c.nv) {
+            for (int j0 = 0; j0 < W; j0 += 32) {
+                const int j = j0 + lane;
+                float ka = 0.f, la = 0.f;
+                int pos = 0, gs = 0;
+                if (j < W) {
+                    const int e = t * W + j;
+                    ka = c.kf[e];
+                    pos = c.inv[e];
+                    gs = c.pgs[pos];
+                    la = c.lws[pos];
+                }
+                unsigned todo = __ballot_sync(0xffffffffu, ka != 0.f && pos > gs);
+                while (todo) {
+                    const int src = __ffs(todo) - 1;
+                    todo &= todo - 1;
+                    const float kb = __shfl_sync(0xffffffffu, ka, src);
+                    const float lb = __shfl_sync(0xffffffffu, la, src);
+                    const int pb = __shfl_sync(0xffffffffu, pos, src);
+                    const int gb = __shfl_sync(0xffffffffu, gs, src);
+                    for (int m = gb + lane; m < pb; m += 32) {
+                        const float2 tk = c.tkk[m];
+                        row[__float_as_int(tk.x)] += kb * tk.y * expf(lb - c.lws[m]);
+                    }
+                    __syncwarp();
+                }
+            }
+        }
+        for (int x = lane; x < C; x += 32) c.A[(size_t)t * C + x] = row[x];
+        __syncwarp();
+        for (int x = lane; x < C; x += 32) row[x] = 0.f;
+        __syncwarp();
+        if (t < c.nv) {
+            for (int i0 = 0; i0 < R; i0 += 32) {
+                const int i = i0 + lane;
+                float qa = 0.f, la = 0.f;
+                int lo = 0, hi = -1;
+                if (i < R) {
+                    const int er = t * R + i;
+                    lo = c.rlo[er];
+                    hi = c.rhi[er];
+                    if (hi >= 0) {
+                        qa = to_f32(c.q[er]);
+                        la = c.lr[er];
+                    }
+                }
+                unsigned todo = __ballot_sync(0xffffffffu, hi >= 0);
+                while (todo) {
+                    const int src = __ffs(todo) - 1;
+                    todo &= todo - 1;
+                    const float qb = __shfl_sync(0xffffffffu, qa, src);
+                    const float lb = __shfl_sync(0xffffffffu, la, src);
+                    const int lob = __shfl_sync(0xffffffffu, lo, src);
+                    const int hib = __shfl_sync(0xffffffffu, hi, src);
+                    for (int m = lob + lane; m <= hib; m += 32) {
+                        const float2 tk = c.tkk[m];
+                        row[__float_as_int(tk.x)] += qb * tk.y * expf(lb - c.lws[m]);
+                    }
+                    __syncwarp();
+                }
+            }
+        }
+        for (int x = lane; x < C; x += 32) c.QK[(size_t)t * C + x] = row[x];
+        __syncwarp();
+    }
+}
+
 template <typename WT>
 __global__ void __launch_bounds__(NT, 2) k_phase1(Dims d, Inputs in, Work w, int step0, int nsteps,
                                                int scratch_in_smem) {
@@ -189,7 +344,7 @@ __global__ void __launch_bounds__(NT, 2) k_phase1(Dims d, Inputs in, Work w, int
     const WT *kw = static_cast<const WT *>(in.kw);
     const WT *qwin = static_cast<const WT *>(in.qw);
     const int N = nsteps * d.P;
-    const unsigned magW = div_magic(W);
+    const unsigned magW = div_magic(W), magR = div_magic(R);
     // sort keys are (slot << 32 | t << 8 | j): the low word orders like e = t*W + j, and the
     // token of an entry is a shift away
     auto ent_of = [W](unsigned low) { return (int)(low >> 8) * W + (int)(low & 255u); };
@@ -224,6 +379,9 @@ __global__ void __launch_bounds__(NT, 2) k_phase1(Dims d, Inputs in, Work w, int
         rhi = w.rhi + (size_t)blockIdx.x * CR;
     }
     unsigned long long *keyB = keyA + CW;
+    // chunks whose scratch lives in global memory leave steps 3 and 4 to k_phase1_rows (the
+    // grid then has one CTA per chunk, so the scratch of chunk n stays in slot n)
+    const bool split = !scratch_in_smem;
 
     for (int n = blockIdx.x; n < N; n += gridDim.x) {
         const int p = n % d.P, ti = step0 + n / d.P;
@@ -335,133 +493,20 @@ __global__ void __launch_bounds__(NT, 2) k_phase1(Dims d, Inputs in, Work w, int
         for (int pos = tid; pos < nw; pos += NT) pgs[pos] = goff[pgid[pos]];
         __syncthreads();
 
-        // 3. weights
-        for (int pos = tid; pos < nw; pos += NT) {
-            const int e = ent_of((unsigned)srt[pos]);
-            const float kk = kf[e];
-            const float l = lws[pos];
-            const float dwv = kk * expf(lend[pgid[pos]] - l);
-            wdw[pos] = dwv;
-            gw[e] = kk * expf(l);
-            if (d.bwd) w.dwt[(size_t)n * CW + e] = dwv;
-        }
-        // each read finds the last write of its slot at a token <= its own: an upper bound in
-        // the sorted write row, four reads per thread at a time, branch-free (the same probe
-        // count for all of them, so the four searches overlap)
-        const unsigned magR = div_magic(R);
-        for (int er0 = tid; er0 < nr; er0 += 4 * NT) {
-            unsigned long long target[4];
-            int base[4], r[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int er = er0 + k * NT;
-                r[k] = er < nr ? rs[er] : -1;
-                const int t = er < nr ? div_by(er, magR) : 0;
-                target[k] = ((unsigned long long)(unsigned)r[k] << 32) | ((unsigned)t << 8) | 255u;
-                base[k] = 0;
-            }
-            for (int len = nw; len > 1;) {
-                const int half = len >> 1;
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    if (srt[base[k] + half - 1] <= target[k]) base[k] += half;
-                len -= half;
-            }
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int er = er0 + k * NT;
-                if (er >= nr) continue;
-                int lo = 0, hi = -1;
-                float l = 0.f;
-                const bool valid = (unsigned)r[k] < (unsigned)S;
-                if (valid && nw > 0) {
-                    const int pos = base[k] + (srt[base[k]] <= target[k] ? 1 : 0) - 1;
-                    if (pos >= 0 && (int)(srt[pos] >> 32) == r[k]) {
-                        hi = pos;
-                        lo = pgs[pos];
-                        l = lws[pos];
-                    }
-                }
-                rlo[er] = lo;
-                rhi[er] = hi;
-                lr[er] = l;
-                qw[er] = valid ? to_f32(q[er]) * expf(l) : 0.f;
-            }
-        }
-        __syncthreads();
-
-        // 4. A and QK, one warp per token row. The row's entries are looked up one per lane;
-        //    entries with earlier members of their group (a ballot) are then taken in entry
-        //    order, the lanes over those members. (token, k) of every sorted position is kept
-        //    in the free radix buffer, next to its running log-decay.
-        float *row = sm.row[warp];
-        for (int t = warp; t < C; t += NW) {
-            for (int c = lane; c < C; c += 32) row[c] = 0.f;
-            __syncwarp();
-            if (t < nv) {
-                for (int j0 = 0; j0 < W; j0 += 32) {
-                    const int j = j0 + lane;
-                    float ka = 0.f, la = 0.f;
-                    int pos = 0, gs = 0;
-                    if (j < W) {
-                        const int e = t * W + j;
-                        ka = kf[e];
-                        pos = inv[e];
-                        gs = pgs[pos];
-                        la = lws[pos];
-                    }
-                    unsigned todo = __ballot_sync(0xffffffffu, ka != 0.f && pos > gs);
-                    while (todo) {
-                        const int src = __ffs(todo) - 1;
-                        todo &= todo - 1;
-                        const float kb = __shfl_sync(0xffffffffu, ka, src);
-                        const float lb = __shfl_sync(0xffffffffu, la, src);
-                        const int pb = __shfl_sync(0xffffffffu, pos, src);
-                        const int gb = __shfl_sync(0xffffffffu, gs, src);
-                        for (int m = gb + lane; m < pb; m += 32) {
-                            const float2 tk = tkk[m];
-                            row[__float_as_int(tk.x)] += kb * tk.y * expf(lb - lws[m]);
-                        }
-                        __syncwarp();
-                    }
-                }
-            }
-            for (int c = lane; c < C; c += 32) A[(size_t)t * C + c] = row[c];
-            __syncwarp();
-            for (int c = lane; c < C; c += 32) row[c] = 0.f;
-            __syncwarp();
-            if (t < nv) {
-                for (int i0 = 0; i0 < R; i0 += 32) {
-                    const int i = i0 + lane;
-                    float qa = 0.f, la = 0.f;
-                    int lo = 0, hi = -1;
-                    if (i < R) {
-                        const int er = t * R + i;
-                        lo = rlo[er];
-                        hi = rhi[er];
-                        if (hi >= 0) {
-                            qa = to_f32(q[er]);
-                            la = lr[er];
-                        }
-                    }
-                    unsigned todo = __ballot_sync(0xffffffffu, hi >= 0);
-                    while (todo) {
-                        const int src = __ffs(todo) - 1;
-                        todo &= todo - 1;
-                        const float qb = __shfl_sync(0xffffffffu, qa, src);
-                        const float lb = __shfl_sync(0xffffffffu, la, src);
-                        const int lob = __shfl_sync(0xffffffffu, lo, src);
-                        const int hib = __shfl_sync(0xffffffffu, hi, src);
-                        for (int m = lob + lane; m <= hib; m += 32) {
-                            const float2 tk = tkk[m];
-                            row[__float_as_int(tk.x)] += qb * tk.y * expf(lb - lws[m]);
-                        }
-                        __syncwarp();
-                    }
-                }
-            }
-            for (int c = lane; c < C; c += 32) QK[(size_t)t * C + c] = row[c];
-            __syncwarp();
+        const P1Chunk<WT> pc{rs, q, srt, tkk, inv, pgid, pgs, lws, lend, kf, rlo, rhi,
+                             wdw, gw, qw, lr, A, QK,
+                             d.bwd ? w.dwt + (size_t)n * CW : nullptr,
+                             nv, nw, nr, C, W, R, S};
+        if (split) {
+            // steps 3 and 4 run in k_phase1_rows, over many CTAs per chunk; it finds the
+            // sorted row in the radix buffer recorded here
+            if (tid == 0) w.p1sel[n] = srt == keyA ? 0 : 1;
+        } else {
+            // 3. weights and the reads' last writes; 4. the Gram rows
+            p1_weights(pc, 0, nw, tid, NT);
+            p1_reads(pc, 0, nr, tid, NT);
+            __syncthreads();
+            p1_gram(pc, 0, C, warp, NW, lane, sm.row[warp]);
         }
         // tails of the per-entry rows past the valid entries (read by nothing but the debug
         // copy; written so that every output element is defined)
@@ -557,6 +602,44 @@ __global__ void __launch_bounds__(NT, 2) k_phase1(Dims d, Inputs in, Work w, int
     }
 }
 
+// Steps 3 and 4 of the chunks whose scratch is in global memory: CTA (rb, n) takes a share of
+// chunk n's sorted positions (weights), the reads of its KR token rows and those rows of A and
+// QK. 8 warps, one row at a time each.
+constexpr int KR = 16;          // token rows per CTA
+constexpr int NTR = 256;
+
+template <typename WT>
+__global__ void __launch_bounds__(NTR) k_phase1_rows(Dims d, Inputs in, Work w, int step0) {
+    __shared__ float rows[NTR / 32][kMaxChunk];
+    const int n = blockIdx.y, rb = blockIdx.x, nrb = gridDim.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int C = d.C, W = d.W, R = d.R, CW = C * W, CR = C * R, CC = C * C;
+    const int p = n % d.P, ti = step0 + n / d.P;
+    const int tok0 = ti * C;
+    const int nv = chunk_valid(in.valid, p, d.T, tok0, C);
+    const int nw = nv * W, nr = nv * R;
+    const size_t tok_base = (size_t)p * d.T + tok0;
+    const unsigned long long *keyA = w.keys + (size_t)n * 2 * CW;
+    const unsigned long long *srt = w.p1sel[n] ? keyA + CW : keyA;
+    const float2 *tkk = reinterpret_cast<const float2 *>(w.p1sel[n] ? keyA : keyA + CW);
+    const P1Chunk<WT> pc{in.rs + tok_base * R, static_cast<const WT *>(in.qw) + tok_base * R,
+                         srt, tkk, w.inv + (size_t)n * CW, w.pgid + (size_t)n * CW,
+                         w.pgs + (size_t)n * CW, w.lws + (size_t)n * CW, w.lend + (size_t)n * CW,
+                         w.kf + (size_t)n * CW, w.rlo + (size_t)n * CR, w.rhi + (size_t)n * CR,
+                         w.wdw + (size_t)n * CW, w.gw + (size_t)n * CW, w.qw + (size_t)n * CR,
+                         w.lr + (size_t)n * CR, w.A + (size_t)n * CC, w.QK + (size_t)n * CC,
+                         d.bwd ? w.dwt + (size_t)n * CW : nullptr,
+                         nv, nw, nr, C, W, R, d.S};
+    const int per = (nw + nrb - 1) / nrb;
+    const int pos0 = rb * per, pos1 = pos0 + per < nw ? pos0 + per : nw;
+    p1_weights(pc, pos0, pos1, tid, NTR);
+    const int t0 = rb * KR, t1 = t0 + KR < C ? t0 + KR : C;
+    const int r1 = (t1 < nv ? t1 : nv) * R;
+    p1_reads(pc, t0 * R < r1 ? t0 * R : r1, r1, tid, NTR);
+    __syncthreads();
+    p1_gram(pc, t0, t1, warp, NTR / 32, lane, rows[warp]);
+}
+
 }  // namespace
 
 size_t phase1_scratch_smem(const Dims &d) {
@@ -564,20 +647,25 @@ size_t phase1_scratch_smem(const Dims &d) {
     return ((sizeof(P1Smem) + 15) & ~size_t(15)) + 8 * 2 * CW + 4 * 6 * CW + 4 * 2 * CR;
 }
 
+bool phase1_split(const Dims &d) { return phase1_scratch_smem(d) > kPhase1SmemMax; }
+
 cudaError_t launch_phase1(const Dims &d, const Inputs &in, const Work &w, int step0, int nsteps,
                           cudaStream_t st) {
     const size_t full = phase1_scratch_smem(d);
     const int in_smem = full <= kPhase1SmemMax ? 1 : 0;
     const size_t smem = in_smem ? full : sizeof(P1Smem);
     const int grid = w.G;
+    const dim3 rows_grid((d.C + KR - 1) / KR, nsteps * d.P);
     if (d.dtype == SDM_BF16) {
         auto kern = k_phase1<__nv_bfloat16>;
         set_kernel_smem(kern, smem);
         kern<<<grid, NT, smem, st>>>(d, in, w, step0, nsteps, in_smem);
+        if (!in_smem) k_phase1_rows<__nv_bfloat16><<<rows_grid, NTR, 0, st>>>(d, in, w, step0);
     } else {
         auto kern = k_phase1<float>;
         set_kernel_smem(kern, smem);
         kern<<<grid, NT, smem, st>>>(d, in, w, step0, nsteps, in_smem);
+        if (!in_smem) k_phase1_rows<float><<<rows_grid, NTR, 0, st>>>(d, in, w, step0);
     }
     return cudaGetLastError();
 }

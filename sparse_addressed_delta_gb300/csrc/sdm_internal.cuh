@@ -52,6 +52,7 @@ struct Work {
     int32_t *goff;      // [N][CW+4] group start positions, goff[ngroups] = n_entries (the
                         //           stride keeps every chunk's row 16-byte aligned)
     int4 *ng4;          // [N]       (ngroups, hot groups, 0, 0) as one 16-byte word
+    int32_t *p1sel;     // [N]       radix buffer holding the sorted write row (scratch in HBM)
     int32_t *gord;      // [N][CW]   DW order: the groups of >= kHotGroup members (ascending),
                         //           then the others by size, largest first (ascending within)
     int32_t *gslot;     // [N][CW]   slot of each group
@@ -169,6 +170,8 @@ cudaError_t launch_dw(const Dims &d, const Inputs &in, const Work &w, int step0,
 cudaError_t launch_phase2_fused(const Dims &d, const Inputs &in, const Work &w, int step0,
                                 int nsteps, cudaStream_t st);
 size_t phase2_pipe_smem(const Dims &d);
+// Phase-1 scratch in global memory: steps 3 and 4 run in a second kernel over row blocks
+bool phase1_split(const Dims &d);
 // sdm_write_read_host: arrays copied from mapped page-locked host memory by one kernel
 // (device addresses of the host pages; 16-byte aligned; sizes in 16-byte units)
 struct HostCopyTable {

@@ -56,9 +56,10 @@ def test_launch_count():
     s = sdm.make_shape(1, 100, 16, 64, 64, 4, 4, sdm.SDM_F32, slab_steps=3,
                        flags=sdm.FLAG_PER_STEP_KERNELS)
     assert sdm.launch_count(s) == 2 * slabs + 3 * nt
-    # chunks whose metadata does not fit on chip twice take the per-step kernels
+    # chunks whose metadata does not fit on chip twice take the per-step kernels; chunks whose
+    # Phase-1 scratch does not fit on chip add Phase 1's row kernel
     s = sdm.make_shape(16, 4096, 128, 131072, 128, 64, 64, sdm.SDM_F32, slab_steps=32)
-    assert sdm.launch_count(s) == 2 + 3 * 32
+    assert sdm.launch_count(s) == 3 + 3 * 32
 
 
 @pytest.mark.parametrize("kw,code", [

@@ -103,7 +103,7 @@ int slab_steps(const Dims &d, int requested) {
 int phase1_ctas(const Dims &d, int ns) {
     const long N = (long)ns * d.P;
     if (phase1_split(d)) return (int)N;   // one CTA, and one scratch slot, per chunk
-    const long cap = (long)(d.C * d.W <= 4096 ? 2 : 1) * kRefSms;
+    const long cap = 2L * kRefSms;        // scratch on chip: two CTAs per SM
     return (int)(N < cap ? N : cap);
 }
 

@@ -17,7 +17,8 @@ constexpr int kMaxWidth = 256;
 constexpr int kRefSms = 152;            // GB300 SM count: sizes grids and slabs (shape-only)
 constexpr size_t kAlign = 256;
 constexpr size_t kSlabBudget = size_t(256) << 20;   // per-chunk Phase-1 state held at once
-constexpr size_t kPhase1SmemMax = 200 * 1024;        // Phase-1 scratch kept on chip up to this
+constexpr size_t kPhase1SmemMax = 110 * 1024;        // Phase-1 scratch kept on chip up to this
+                                                     // (two CTAs per SM); larger: split Phase 1
 constexpr size_t kPipeSmemMax = 224 * 1024;          // pipelined Phase 2 when two stages fit
 constexpr long kSpinLimit = 1L << 22;   // mbarrier polls before a wait gives up (seconds at most)
 constexpr int32_t kNoEntry = INT32_MIN;  // Work::wsl / rsl: no entry

@@ -339,14 +339,15 @@ __global__ void __launch_bounds__(NP2) k_phase2_pipe(Dims d, Inputs in, Work w, 
         }
     };
 
+    // the first stage; each later one is awaited by the step before it, ahead of its closing
+    // barrier
+    if (compute_sync_or(!wait_stage(0))) {
+        // a stage did not land: report and stop (the producer drains its own copies)
+        if (tid == 0) atomicCAS(&w.status->code, 0, (int)SDM_ERR_TIMEOUT);
+        return;
+    }
     for (int ls = 0; ls < nsteps; ++ls) {
         const int st = ls & 1;
-        const bool ok = wait_stage(ls);
-        if (compute_sync_or(!ok)) {
-            // a stage did not land: report and stop (the producer drains its own copies)
-            if (tid == 0) atomicCAS(&w.status->code, 0, (int)SDM_ERR_TIMEOUT);
-            return;
-        }
         const unsigned char *b = psm + st * L.bytes;
         const int32_t *swslot = reinterpret_cast<const int32_t *>(b + L.wslot);
         const float *swgw = reinterpret_cast<const float *>(b + L.wgw);
@@ -580,7 +581,11 @@ __global__ void __launch_bounds__(NP2) k_phase2_pipe(Dims d, Inputs in, Work w, 
                 finish(g, o1, acc);
             }
         }
-        compute_sync();
+        const bool ok = ls + 1 < nsteps ? wait_stage(ls + 1) : true;
+        if (compute_sync_or(!ok)) {
+            if (tid == 0) atomicCAS(&w.status->code, 0, (int)SDM_ERR_TIMEOUT);
+            return;
+        }
         if (tid == 0) mbar_arrive(empty + st);   // stage st may be refilled
     }
 }

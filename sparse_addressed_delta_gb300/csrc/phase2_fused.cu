@@ -300,16 +300,19 @@ __global__ void __launch_bounds__(NP2) k_phase2_pipe(Dims d, Inputs in, Work w, 
         return;
     }
 
-    // gather mapping: token gt = tid / tpt, its W + R entries (writes first) split over tpt
-    // lanes (q = sub, sub + tpt, ...); tpt is a power of two with tpt * C <= NT2, so one pass
-    // covers every token
+    // gather mapping: token gt = tid / tpt; the first half of its tpt lanes sum its write
+    // entries and the second half its read entries (entry q = hl, hl + half, ... of the kind);
+    // tpt is a power of two with tpt * C <= NT2 (C <= 256 gives tpt >= 2), so one pass covers
+    // every token
     int tpt = NT2 / C;
     if (tpt > 32) tpt = 32;
-    if (tpt < 1) tpt = 1;
     while (tpt & (tpt - 1)) tpt &= tpt - 1;
+    const int half = tpt >> 1;
     const int sub = tid % tpt;
     const int gt = tid / tpt;
-    const int E = W + R;
+    const bool rd = sub >= half;     // this lane sums read entries (else write entries)
+    const int hl = rd ? sub - half : sub;
+    const int ne = rd ? R : W;       // entries of the lane's kind per token
 
     // The first PF entries of a lane are fetched one step ahead: while step ls computes, the
     // pieces of step ls + 1 are loaded into registers, except for entries linked to a group of
@@ -321,14 +324,14 @@ __global__ void __launch_bounds__(NP2) k_phase2_pipe(Dims d, Inputs in, Work w, 
     int lk[PF];   // -2: no entry; -1: piece in pf; >= 0: dwout[lk]
     auto prefetch = [&](int ls_n, const unsigned char *bn) {
         const int nvn = nvalid_of(step0 + ls_n);
-        const int32_t *wsl = reinterpret_cast<const int32_t *>(bn + L.wslot) + gt * W;
-        const int32_t *rsl = reinterpret_cast<const int32_t *>(bn + L.rslot) + gt * R;
+        const int32_t *sl = rd ? reinterpret_cast<const int32_t *>(bn + L.rslot) + gt * R
+                               : reinterpret_cast<const int32_t *>(bn + L.wslot) + gt * W;
 #pragma unroll
         for (int k = 0; k < PF; ++k) {
-            const int q = sub + k * tpt;
+            const int q = hl + k * half;
             lk[k] = -2;
-            if (gt < nvn && q < E) {
-                const int v = q < W ? wsl[q] : rsl[q - W];
+            if (gt < nvn && q < ne) {
+                const int v = sl[q];
                 if (v >= 0) {
                     lk[k] = -1;
                     pf[k] = *reinterpret_cast<const uint4 *>(bank + (size_t)v * D);
@@ -368,42 +371,40 @@ __global__ void __launch_bounds__(NP2) k_phase2_pipe(Dims d, Inputs in, Work w, 
 
         // ---- gather (the write pieces are also kept as B0 for the DW) ----
         // each lane adds its entries in entry order: the PF early ones, then the rest fetched
-        // now, GB at a time before any is used; a shuffle tree then sums the token's lanes
+        // now, GB at a time before any is used; a shuffle tree then sums the lanes of the kind
         {
             constexpr int GB = 4;
-            float ar[V], ai[V];
+            float acc[V];
 #pragma unroll
-            for (int c = 0; c < V; ++c) { ar[c] = 0.f; ai[c] = 0.f; }
+            for (int c = 0; c < V; ++c) acc[c] = 0.f;
             if (gt < nv) {
-                const int32_t *wsl = swslot + gt * W;
-                const float *wg = swgw + gt * W;
-                const int32_t *rsl = srslot + gt * R;
-                const float *rq = srqw + gt * R;
+                const int32_t *sl = rd ? srslot + gt * R : swslot + gt * W;
+                const float *wt = rd ? srqw + gt * R : swgw + gt * W;
+                uint4 *b0 = b0s + gt * W;
 #pragma unroll
                 for (int k = 0; k < PF; ++k) {
-                    const int q = sub + k * tpt;
-                    if (q < E) {
+                    const int q = hl + k * half;
+                    if (q < ne) {
                         const uint4 u = lk[k] >= 0 ? dwout[lk[k]]
                                                    : (lk[k] == -1 ? pf[k] : make_uint4(0u, 0u, 0u, 0u));
-                        if (q < W) b0s[gt * W + q] = u;
+                        if (!rd) b0[q] = u;
                         if (lk[k] != -2) {
                             float x[V];
                             piece_to_f32<BT>(u, x);
-                            if (q < W) add_piece<V>(ar, wg[q], x);
-                            else add_piece<V>(ai, rq[q - W], x);
+                            add_piece<V>(acc, wt[q], x);
                         }
                     }
                 }
-                for (int q0 = sub + PF * tpt; q0 < E; q0 += GB * tpt) {
+                for (int q0 = hl + PF * half; q0 < ne; q0 += GB * half) {
                     uint4 u[GB];
                     bool has[GB];
 #pragma unroll
                     for (int k = 0; k < GB; ++k) {
-                        const int q = q0 + k * tpt;
+                        const int q = q0 + k * half;
                         u[k] = make_uint4(0u, 0u, 0u, 0u);
                         has[k] = false;
-                        if (q < E) {
-                            const int v = q < W ? wsl[q] : rsl[q - W];
+                        if (q < ne) {
+                            const int v = sl[q];
                             if (v >= 0) {
                                 u[k] = *reinterpret_cast<const uint4 *>(bank + (size_t)v * D);
                                 has[k] = true;
@@ -415,31 +416,27 @@ __global__ void __launch_bounds__(NP2) k_phase2_pipe(Dims d, Inputs in, Work w, 
                     }
 #pragma unroll
                     for (int k = 0; k < GB; ++k) {
-                        const int q = q0 + k * tpt;
-                        if (q < E) {
-                            if (q < W) b0s[gt * W + q] = u[k];
+                        const int q = q0 + k * half;
+                        if (q < ne) {
+                            if (!rd) b0[q] = u[k];
                             if (has[k]) {
                                 float x[V];
                                 piece_to_f32<BT>(u[k], x);
-                                if (q < W) add_piece<V>(ar, wg[q], x);
-                                else add_piece<V>(ai, rq[q - W], x);
+                                add_piece<V>(acc, wt[q], x);
                             }
                         }
                     }
                 }
             }
-            // sum over the token's lanes; each lane ends with a share of the 2V sums
-            // (retrieved columns 0..V-1, then inter) and writes u_pre / inter for it
-            float val[2 * V];
-#pragma unroll
-            for (int c = 0; c < V; ++c) { val[c] = ar[c]; val[V + c] = ai[c]; }
+            // sum over the kind's lanes; each lane ends with a share of the V sums and writes
+            // u_pre (write lanes: retrieved) or inter (read lanes) for it
             const bool live = gt < nv;
             const BT *vp16 = svpc + gt * V;
             const float bt = live ? sbeta[gt] : 0.f;
-            reduce_scatter<2 * V>(val, tpt >> 1, lane, 0, [&](int idx, float x) {
+            reduce_scatter<V>(acc, half >> 1, lane, 0, [&](int idx, float x) {
                 if (gt >= C) return;
-                if (idx < V) us[gt * V + idx] = live ? bt * (to_f32(vp16[idx]) - x) : 0.f;
-                else is[gt * V + idx - V] = live ? x : 0.f;
+                if (!rd) us[gt * V + idx] = live ? bt * (to_f32(vp16[idx]) - x) : 0.f;
+                else is[gt * V + idx] = live ? x : 0.f;
             });
         }
         compute_sync();
@@ -514,8 +511,8 @@ __global__ void __launch_bounds__(NP2) k_phase2_pipe(Dims d, Inputs in, Work w, 
 
         // ---- DW: B[s] = (sum of dw * delta_v over the group's members, sorted order) +
         //      exp(lend) * B0[s], one writer per written slot. A group of >= kHotGroup members
-        //      gets a warp (lane l adds members l, l + 32, ..., then a fixed xor tree); every
-        //      other group a thread (members in order), in Phase 1's size order. ----
+        //      gets a warp (lane l adds members l, l + 32, ..., then a fixed reduce-scatter);
+        //      every other group a thread (members in order), in Phase 1's size order. ----
         {
             const int32_t *sgoff = reinterpret_cast<const int32_t *>(b + L.goff);
             const int4 sc = *reinterpret_cast<const int4 *>(b + L.scal);
@@ -558,11 +555,22 @@ __global__ void __launch_bounds__(NP2) k_phase2_pipe(Dims d, Inputs in, Work w, 
 #pragma unroll
                 for (int c = 0; c < V; ++c) acc[c] = 0.f;
                 for (int m = o0 + lane; m < o1; m += 32) add_member(m, acc);
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1)
-#pragma unroll
-                    for (int c = 0; c < V; ++c) acc[c] += __shfl_xor_sync(0xffffffffu, acc[c], off);
-                if (lane == 0) finish(g, o1, acc);
+                // a reduce-scatter leaves column c's sum on one lane, which finishes that column:
+                // the V lanes store the piece together (one 16-byte segment per warp store)
+                const int tinf = sminfo[o1 - 1];
+                const int pos = (tinf & 255) * W + ((tinf >> 8) & 255);
+                const float fac = sgfac[g];
+                const int sl = sgslot[g];
+                reduce_scatter<V>(acc, 16, lane, 0, [&](int c, float x) {
+                    const BT b0 = reinterpret_cast<const BT *>(b0s + pos)[c];
+                    const BT o = from_f32<BT>(fmaf(fac, to_f32(b0), x));
+                    if ((unsigned)sl < S) {
+                        bank[(size_t)sl * D + c] = o;
+                        reinterpret_cast<BT *>(dwout + g)[c] = o;
+                        if (in.snap)
+                            static_cast<BT *>(in.snap)[((size_t)(ti * d.P + p) * CW + (o1 - 1)) * D + c0 + c] = b0;
+                    }
+                });
             }
             // the other groups, largest first, so that a warp's lanes loop about equally long;
             // they start at the last thread, away from the warps that took a hot group

@@ -14,8 +14,10 @@
 //      elements in parallel), then X_ij = -D_i T_ij;
 //   3. QX_ij = sum_{k=j}^{i} QK_ik X_kj for every lower block, block row by block row.
 // X lives in shared memory as packed lower blocks (nb(nb+1)/2 x 1 KB: 136 KB at C = 256); the
-// current block row of L (or QK) and the T blocks are staged next to it; for C <= 32 the
-// chunk's A, QK and beta are first copied on chip whole. Every product is full
+// current block row of L (or QK, when it is not copied on chip whole) and the T blocks are
+// staged next to it; for C <= 32 the chunk's A and beta, and for C <= 64 its QK, are first
+// copied on chip whole. In steps 2 and 3 a thread computes four adjacent columns of one row
+// (one left-hand value and one 16-byte piece of an X row per four FMAs). Every product is full
 // float32 FFMA in a fixed order: the inverse amplifies rounding, so no reduced-precision path.
 #include "sdm_internal.cuh"
 
@@ -25,6 +27,8 @@ namespace {
 constexpr int NTS = 256;
 constexpr int BS = 16;                 // block size
 constexpr int BB = BS * BS;            // floats per block
+constexpr int LRP = BS + 1;            // row pitch of the staged L / QK blocks (no bank conflicts
+constexpr int LB = BS * LRP;           // between the rows that one warp reads)
 
 __host__ __device__ __forceinline__ int tri(int i) { return i * (i + 1) / 2; }
 
@@ -47,7 +51,7 @@ struct SolveSmem {
 __host__ __device__ inline SolveSmem solve_layout(const Dims &d) {
     const int nb = (d.C + BS - 1) / BS;
     SolveSmem L;
-    size_t o = sizeof(float) * (size_t)(tri(nb) + 2 * nb) * BB;
+    size_t o = sizeof(float) * ((size_t)(tri(nb) + nb) * BB + (size_t)nb * LB);
     L.a = L.q = L.beta = L.gsl = L.ent = o;
     const size_t m = sizeof(float) * (size_t)d.C * staged_pitch(d.C);
     if (solve_staged_qk(d)) {
@@ -73,7 +77,7 @@ __global__ void __launch_bounds__(NTS) k_solve(Dims d, Inputs in, Work w, int st
     const int C = d.C;
     const int nb = (C + BS - 1) / BS;
     const int n = blockIdx.x;
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int p = n % d.P, ti = step0 + n / d.P;
     const int nv = w.nvalid[n];
     const int nvb = (nv + BS - 1) / BS;          // block rows holding valid tokens
@@ -84,8 +88,8 @@ __global__ void __launch_bounds__(NTS) k_solve(Dims d, Inputs in, Work w, int st
     float *QX = w.QX + (size_t)n * C * xp;
     const float *beta = in.beta + (size_t)p * d.T + (size_t)ti * C;
     float *Xp = ssm;                             // packed lower blocks of X
-    float *Lr = Xp + tri(nb) * BB;               // current block row of L / QK  [nb][16][16]
-    float *Tb = Lr + nb * BB;                    // T blocks                     [nb][16][16]
+    float *Lr = Xp + tri(nb) * BB;               // current block row of L / QK  [nb][16][LRP]
+    float *Tb = Lr + nb * LB;                    // T blocks                     [nb][16][16]
 
     // staged copies of the valid rows of QK (and for small chunks of A and beta): cp.async,
     // 16 bytes a copy, landing while the links and the first phases run
@@ -171,13 +175,13 @@ __global__ void __launch_bounds__(NTS) k_solve(Dims d, Inputs in, Work w, int st
     //    (block b, column c) substitutes down its column
     for (int e = tid; e < nvb * BB; e += NTS) {
         const int b = e / BB, rc = e - b * BB, r = rc / BS, c = rc - r * BS;
-        Lr[e] = lval(b * BS + r, b * BS + c);
+        Lr[b * LB + r * LRP + c] = lval(b * BS + r, b * BS + c);
     }
     __syncthreads();
     for (int job = tid; job < nvb * BS; job += NTS) {
         const int b = job / BS, c = job - b * BS;
         float *Dk = Xp + (tri(b) + b) * BB;
-        const float *Lb = Lr + b * BB;
+        const float *Lb = Lr + b * LB;
         float x[BS];
 #pragma unroll
         for (int r = 0; r < BS; ++r) x[r] = (r == c) ? 1.f : 0.f;
@@ -186,7 +190,7 @@ __global__ void __launch_bounds__(NTS) k_solve(Dims d, Inputs in, Work w, int st
             float s = 0.f;
 #pragma unroll
             for (int k = 0; k < BS; ++k)
-                if (k < r) s = fmaf(Lb[r * BS + k], x[k], s);
+                if (k < r) s = fmaf(Lb[r * LRP + k], x[k], s);
             if (r > c) x[r] = -s;
         }
 #pragma unroll
@@ -194,81 +198,136 @@ __global__ void __launch_bounds__(NTS) k_solve(Dims d, Inputs in, Work w, int st
     }
     __syncthreads();
 
+    // A thread computes a quad: four adjacent columns (c .. c+3) of one row r of block j, so one
+    // left-hand value and one 16-byte piece of an X row feed four FMAs (k and m ascending, as a
+    // plain dot product).
+    auto quad = [](int qd, int &j, int &r, int &c) {
+        j = qd >> 6;
+        r = (qd >> 2) & 15;
+        c = (qd & 3) * 4;
+    };
+    auto fma4 = [](float4 &s, float a, const float4 &x) {
+        s.x = fmaf(a, x.x, s.x);
+        s.y = fmaf(a, x.y, s.y);
+        s.z = fmaf(a, x.z, s.z);
+        s.w = fmaf(a, x.w, s.w);
+    };
+
     // 2. block rows
     for (int i = 1; i < nvb; ++i) {
         for (int e = tid; e < i * BB; e += NTS) {
             const int k = e / BB, rc = e - k * BB, r = rc / BS, c = rc - r * BS;
-            Lr[e] = lval(i * BS + r, k * BS + c);
+            Lr[k * LB + r * LRP + c] = lval(i * BS + r, k * BS + c);
         }
         __syncthreads();
-        for (int e = tid; e < i * BB; e += NTS) {
-            const int j = e / BB, rc = e - j * BB, r = rc / BS, c = rc - r * BS;
-            float s = 0.f;
+        for (int qd = tid; qd < i * 64; qd += NTS) {
+            int j, r, c;
+            quad(qd, j, r, c);
+            float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int k = j; k < i; ++k) {
-                const float *Lk = Lr + k * BB + r * BS;
+                const float *Lk = Lr + k * LB + r * LRP;
                 const float *Xk = Xp + (tri(k) + j) * BB + c;
 #pragma unroll
-                for (int m = 0; m < BS; ++m) s = fmaf(Lk[m], Xk[m * BS], s);
+                for (int m = 0; m < BS; ++m)
+                    fma4(s, Lk[m], *reinterpret_cast<const float4 *>(Xk + m * BS));
             }
-            Tb[e] = s;
+            *reinterpret_cast<float4 *>(Tb + j * BB + r * BS + c) = s;
         }
         __syncthreads();
         const float *Di = Xp + (tri(i) + i) * BB;
-        for (int e = tid; e < i * BB; e += NTS) {
-            const int j = e / BB, rc = e - j * BB, r = rc / BS, c = rc - r * BS;
+        for (int qd = tid; qd < i * 64; qd += NTS) {
+            int j, r, c;
+            quad(qd, j, r, c);
             const float *T = Tb + j * BB + c;
-            float s = 0.f;
-            for (int m = 0; m <= r; ++m) s = fmaf(Di[r * BS + m], T[m * BS], s);
-            Xp[(tri(i) + j) * BB + rc] = -s;
+            float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int m = 0; m <= r; ++m)
+                fma4(s, Di[r * BS + m], *reinterpret_cast<const float4 *>(T + m * BS));
+            *reinterpret_cast<float4 *>(Xp + (tri(i) + j) * BB + r * BS + c) =
+                make_float4(-s.x, -s.y, -s.z, -s.w);
         }
         __syncthreads();
     }
 
-    // 3. QX, block row by block row; written out with X
+    // 3. QX, block row by block row; written out with X. QK is read from its staged copy when
+    //    there is one, else its block row is staged like L's.
     if (!qk_ready) {
         cp_async_wait<0>();
         __syncthreads();
     }
+    const bool vec = (xp & 3) == 0;     // X / QX rows are 16-byte aligned
     for (int i = 0; i < nb; ++i) {
         if (i < nvb) {
-            for (int e = tid; e < (i + 1) * BB; e += NTS) {
-                const int k = e / BB, rc = e - k * BB, r = rc / BS, c = rc - r * BS;
-                const int R = i * BS + r, K = k * BS + c;
-                Lr[e] = (R < nv && K <= R) ? QK[(size_t)R * qp + K] : 0.f;
-            }
-            __syncthreads();
-            for (int e = tid; e < (i + 1) * BB; e += NTS) {
-                const int j = e / BB, rc = e - j * BB, r = rc / BS, c = rc - r * BS;
-                float s = 0.f;
-                for (int k = j; k <= i; ++k) {
-                    const float *Qk = Lr + k * BB + r * BS;
-                    const float *Xk = Xp + (tri(k) + j) * BB + c;
-#pragma unroll
-                    for (int m = 0; m < BS; ++m) s = fmaf(Qk[m], Xk[m * BS], s);
+            const float *Qrow;
+            int qpitch, qblock;
+            if (staged_qk) {
+                Qrow = QK + (size_t)i * BS * qp;   // valid rows, zero above the diagonal
+                qpitch = qp;
+                qblock = BS;
+            } else {
+                for (int e = tid; e < (i + 1) * BB; e += NTS) {
+                    const int k = e / BB, rc = e - k * BB, r = rc / BS, c = rc - r * BS;
+                    const int R = i * BS + r, K = k * BS + c;
+                    Lr[k * LB + r * LRP + c] = (R < nv && K <= R) ? QK[(size_t)R * qp + K] : 0.f;
                 }
-                Tb[e] = s;
+                __syncthreads();
+                Qrow = Lr;
+                qpitch = LRP;
+                qblock = LB;
+            }
+            for (int qd = tid; qd < (i + 1) * 64; qd += NTS) {
+                int j, r, c;
+                quad(qd, j, r, c);
+                float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (i * BS + r < nv) {
+                    for (int k = j; k <= i; ++k) {
+                        const float *Qk = Qrow + (size_t)k * qblock + r * qpitch;
+                        const float *Xk = Xp + (tri(k) + j) * BB + c;
+#pragma unroll
+                        for (int m = 0; m < BS; ++m)
+                            fma4(s, Qk[m], *reinterpret_cast<const float4 *>(Xk + m * BS));
+                    }
+                }
+                *reinterpret_cast<float4 *>(Tb + j * BB + r * BS + c) = s;
             }
             __syncthreads();
         }
-        // rows i*16 .. i*16+15 of X and QX (consecutive threads on consecutive columns)
-        for (int e = tid; e < BS * xp; e += NTS) {
-            const int r = e / xp, u = e - r * xp, t = i * BS + r;
-            if (t >= C) continue;
-            if (u >= C) {   // pitch padding
-                X[(size_t)t * xp + u] = 0.f;
-                QX[(size_t)t * xp + u] = 0.f;
-                continue;
-            }
-            float x, q = 0.f;
-            if (t < nv && u < nv) {
+        // rows i*16 .. i*16+15 of X and QX: warp w takes rows w, w + 8; its lanes take
+        // consecutive 16-byte pieces (or single columns when the pitch is not a multiple of 4)
+        auto xq = [&](int r, int u, float &x, float &q) {
+            const int t = i * BS + r;
+            q = 0.f;
+            if (u >= C) {
+                x = 0.f;                       // pitch padding
+            } else if (t < nv && u < nv) {
                 const int j = u / BS;
                 x = (u <= t) ? Xp[(tri(i) + j) * BB + r * BS + (u - j * BS)] : 0.f;
                 if (j <= i) q = Tb[j * BB + r * BS + (u - j * BS)];
             } else {
                 x = (t == u) ? 1.f : 0.f;
             }
-            X[(size_t)t * xp + u] = x;
-            QX[(size_t)t * xp + u] = q;
+        };
+        for (int r = warp; r < BS; r += NTS / 32) {
+            const int t = i * BS + r;
+            if (t >= C) break;
+            float *xrow = X + (size_t)t * xp, *qrow = QX + (size_t)t * xp;
+            if (vec) {
+                for (int u4 = lane * 4; u4 < xp; u4 += 128) {
+                    float4 x, q;
+                    xq(r, u4, x.x, q.x);
+                    xq(r, u4 + 1, x.y, q.y);
+                    xq(r, u4 + 2, x.z, q.z);
+                    xq(r, u4 + 3, x.w, q.w);
+                    *reinterpret_cast<float4 *>(xrow + u4) = x;
+                    *reinterpret_cast<float4 *>(qrow + u4) = q;
+                }
+            } else {
+                for (int u = lane; u < xp; u += 32) {
+                    float x, q;
+                    xq(r, u, x, q);
+                    xrow[u] = x;
+                    qrow[u] = q;
+                }
+            }
         }
         __syncthreads();
     }

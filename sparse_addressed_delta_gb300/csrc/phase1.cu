@@ -255,82 +255,102 @@ __device__ void p1_reads(const P1Chunk<WT> &c, int er_lo, int er_hi, int tid, in
     }
 }
 
-// 4. rows [t0, t1) of A and QK, one warp per token row. The row's entries are looked up one per
-//    lane; entries with earlier members of their group (a ballot) are then taken in entry
-//    order, the lanes over those members. (token, k) of every sorted position is kept in the
+// 4. rows [t0, t1) of A and QK. A warp takes two token rows at a time when both fit in its row
+//    buffer (2 C <= kMaxChunk), one half-warp per row, else one row with all lanes. The row's
+//    entries are looked up one per lane; entries with earlier members of their group (a ballot)
+//    are then taken in entry order, the lanes of the row over those members (distinct tokens,
+//    so no two lanes add to one element). (token, k) of every sorted position is kept in the
 //    free radix buffer, next to its running log-decay.
-template <typename WT>
-__device__ void p1_gram(const P1Chunk<WT> &c, int t0, int t1, int warp, int nwarps, int lane,
-                        float *row) {
+template <typename WT, bool TWO>
+__device__ void p1_gram_rows(const P1Chunk<WT> &c, int t0, int t1, int warp, int nwarps, int lane,
+                             float *row) {
     const int C = c.C, W = c.W, R = c.R;
-    for (int t = t0 + warp; t < t1; t += nwarps) {
-        for (int x = lane; x < C; x += 32) row[x] = 0.f;
+    constexpr int lpr = TWO ? 16 : 32;                  // lanes per row
+    const int hsel = TWO ? lane >> 4 : 0;
+    const int hl = lane & (lpr - 1);
+    const unsigned hmask = TWO ? 0xffffu << (16 * hsel) : 0xffffffffu;
+    constexpr int rpw = TWO ? 2 : 1;                    // rows per warp and pass
+    float *rw = row + hsel * C;
+    for (int tb = t0 + warp * rpw; tb < t1; tb += nwarps * rpw) {
+        const int t = tb + hsel;
+        const bool live = t < t1;                       // else this half only joins the shuffles
+        const bool act = live && t < c.nv;
+        for (int x = hl; x < C; x += lpr) rw[x] = 0.f;
         __syncwarp();
-        if (t < c.nv) {
-            for (int j0 = 0; j0 < W; j0 += 32) {
-                const int j = j0 + lane;
-                float ka = 0.f, la = 0.f;
-                int pos = 0, gs = 0;
-                if (j < W) {
-                    const int e = t * W + j;
-                    ka = c.kf[e];
-                    pos = c.inv[e];
-                    gs = c.pgs[pos];
-                    la = c.lws[pos];
+        for (int j0 = 0; j0 < W; j0 += lpr) {
+            const int j = j0 + hl;
+            float ka = 0.f, la = 0.f;
+            int pos = 0, gs = 0;
+            if (act && j < W) {
+                const int e = t * W + j;
+                ka = c.kf[e];
+                pos = c.inv[e];
+                gs = c.pgs[pos];
+                la = c.lws[pos];
+            }
+            unsigned todo = __ballot_sync(0xffffffffu, ka != 0.f && pos > gs) & hmask;
+            while (__any_sync(0xffffffffu, todo != 0u)) {
+                const bool has = todo != 0u;
+                const int src = has ? __ffs(todo) - 1 : lane;
+                todo &= todo - 1u;
+                const float kb = __shfl_sync(0xffffffffu, ka, src);
+                const float lb = __shfl_sync(0xffffffffu, la, src);
+                const int pb = __shfl_sync(0xffffffffu, pos, src);
+                const int gb = __shfl_sync(0xffffffffu, gs, src);
+                const int pe = has ? pb : gb;
+                for (int m = gb + hl; m < pe; m += lpr) {
+                    const float2 tk = c.tkk[m];
+                    rw[__float_as_int(tk.x)] += kb * tk.y * expf(lb - c.lws[m]);
                 }
-                unsigned todo = __ballot_sync(0xffffffffu, ka != 0.f && pos > gs);
-                while (todo) {
-                    const int src = __ffs(todo) - 1;
-                    todo &= todo - 1;
-                    const float kb = __shfl_sync(0xffffffffu, ka, src);
-                    const float lb = __shfl_sync(0xffffffffu, la, src);
-                    const int pb = __shfl_sync(0xffffffffu, pos, src);
-                    const int gb = __shfl_sync(0xffffffffu, gs, src);
-                    for (int m = gb + lane; m < pb; m += 32) {
-                        const float2 tk = c.tkk[m];
-                        row[__float_as_int(tk.x)] += kb * tk.y * expf(lb - c.lws[m]);
-                    }
-                    __syncwarp();
-                }
+                __syncwarp();
             }
         }
-        for (int x = lane; x < C; x += 32) c.A[(size_t)t * C + x] = row[x];
+        if (live)
+            for (int x = hl; x < C; x += lpr) c.A[(size_t)t * C + x] = rw[x];
         __syncwarp();
-        for (int x = lane; x < C; x += 32) row[x] = 0.f;
+        for (int x = hl; x < C; x += lpr) rw[x] = 0.f;
         __syncwarp();
-        if (t < c.nv) {
-            for (int i0 = 0; i0 < R; i0 += 32) {
-                const int i = i0 + lane;
-                float qa = 0.f, la = 0.f;
-                int lo = 0, hi = -1;
-                if (i < R) {
-                    const int er = t * R + i;
-                    lo = c.rlo[er];
-                    hi = c.rhi[er];
-                    if (hi >= 0) {
-                        qa = to_f32(c.q[er]);
-                        la = c.lr[er];
-                    }
-                }
-                unsigned todo = __ballot_sync(0xffffffffu, hi >= 0);
-                while (todo) {
-                    const int src = __ffs(todo) - 1;
-                    todo &= todo - 1;
-                    const float qb = __shfl_sync(0xffffffffu, qa, src);
-                    const float lb = __shfl_sync(0xffffffffu, la, src);
-                    const int lob = __shfl_sync(0xffffffffu, lo, src);
-                    const int hib = __shfl_sync(0xffffffffu, hi, src);
-                    for (int m = lob + lane; m <= hib; m += 32) {
-                        const float2 tk = c.tkk[m];
-                        row[__float_as_int(tk.x)] += qb * tk.y * expf(lb - c.lws[m]);
-                    }
-                    __syncwarp();
+        for (int i0 = 0; i0 < R; i0 += lpr) {
+            const int i = i0 + hl;
+            float qa = 0.f, la = 0.f;
+            int lo = 0, hi = -1;
+            if (act && i < R) {
+                const int er = t * R + i;
+                lo = c.rlo[er];
+                hi = c.rhi[er];
+                if (hi >= 0) {
+                    qa = to_f32(c.q[er]);
+                    la = c.lr[er];
                 }
             }
+            unsigned todo = __ballot_sync(0xffffffffu, hi >= 0) & hmask;
+            while (__any_sync(0xffffffffu, todo != 0u)) {
+                const bool has = todo != 0u;
+                const int src = has ? __ffs(todo) - 1 : lane;
+                todo &= todo - 1u;
+                const float qb = __shfl_sync(0xffffffffu, qa, src);
+                const float lb = __shfl_sync(0xffffffffu, la, src);
+                const int lob = __shfl_sync(0xffffffffu, lo, src);
+                const int hib = __shfl_sync(0xffffffffu, hi, src);
+                const int he = has ? hib : lob - 1;
+                for (int m = lob + hl; m <= he; m += lpr) {
+                    const float2 tk = c.tkk[m];
+                    rw[__float_as_int(tk.x)] += qb * tk.y * expf(lb - c.lws[m]);
+                }
+                __syncwarp();
+            }
         }
-        for (int x = lane; x < C; x += 32) c.QK[(size_t)t * C + x] = row[x];
+        if (live)
+            for (int x = hl; x < C; x += lpr) c.QK[(size_t)t * C + x] = rw[x];
         __syncwarp();
     }
+}
+
+template <typename WT>
+__device__ __forceinline__ void p1_gram(const P1Chunk<WT> &c, int t0, int t1, int warp, int nwarps,
+                                        int lane, float *row) {
+    if (2 * c.C <= kMaxChunk) p1_gram_rows<WT, true>(c, t0, t1, warp, nwarps, lane, row);
+    else p1_gram_rows<WT, false>(c, t0, t1, warp, nwarps, lane, row);
 }
 
 template <typename WT>

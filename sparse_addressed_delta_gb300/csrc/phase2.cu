@@ -265,13 +265,17 @@ __global__ void __launch_bounds__(MM_T) k_dualmm(Dims d, Inputs in, Work w, int 
 }
 
 // ---------------------------------------------------------------------------------------
-// DW: one warp per group (distinct written slot) of each chunk of the step; a warp takes NG
-// groups at once (the next ones of its stride) so that their metadata and B0 row loads are in
-// flight together
+// DW: one warp per group (distinct written slot) of each chunk of the step. A warp takes NG
+// groups at once (the next ones of its stride): lane k < NG loads group k's slot, bounds,
+// factor and first member with coalesced-by-lane loads, the warp broadcasts them by shuffle
+// and issues all NG B0 row loads and first-member delta_v loads before any arithmetic. Further
+// members are fetched 32 at a time the same way (lane l loads member l's token and weight).
+// Each row adds its members in sorted order after exp(lend) B0: the order of the sum is that
+// of the group, whatever NG is.
 // ---------------------------------------------------------------------------------------
 template <typename BT, int CPL>
-__global__ void __launch_bounds__(kBlock) k_dw(Dims d, Inputs in, Work w, int step0, int ti) {
-    constexpr int NG = CPL <= 8 ? 2 : 1;
+__global__ void __launch_bounds__(kBlock, 2) k_dw(Dims d, Inputs in, Work w, int step0, int ti) {
+    constexpr int NG = CPL <= 2 ? 8 : (CPL <= 8 ? 4 : 2);   // 2 NG CPL floats of row data
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int p = blockIdx.y;
     const int n = (ti - step0) * d.P + p;
@@ -284,27 +288,31 @@ __global__ void __launch_bounds__(kBlock) k_dw(Dims d, Inputs in, Work w, int st
     const float *wdw = w.wdw + (size_t)n * CW;
     const float *dvp = w.dv + (size_t)p * C * D + lane * CPL;
     BT *bank = static_cast<BT *>(in.bank) + (size_t)p * d.S * D + lane * CPL;
+    const unsigned magic = div_magic(W);
     const int stride = gridDim.x * kWarps;
     for (int g0 = blockIdx.x * kWarps + warp; g0 < ng; g0 += NG * stride) {
-        int o0[NG], o1[NG];
-        bool live[NG];
-        BT *row[NG];
-        float f[NG], acc[NG][CPL];
-#pragma unroll
-        for (int k = 0; k < NG; ++k) {
-            const int g = g0 + k * stride;
-            live[k] = g < ng;
-            const int sl = live[k] ? gslot[g] : -1;
-            live[k] = live[k] && (unsigned)sl < (unsigned)d.S;
-            o0[k] = live[k] ? goff[g] : 0;
-            o1[k] = live[k] ? goff[g + 1] : 0;
-            f[k] = live[k] ? gfac[g] : 0.f;
-            row[k] = bank + (size_t)(live[k] ? sl : 0) * D;
+        // lane k < NG: group g0 + k * stride
+        int msl = -1, mo0 = 0, mo1 = 0, mt = 0;
+        float mf = 0.f, mw = 0.f;
+        if (lane < NG) {
+            const int g = g0 + lane * stride;
+            if (g < ng) {
+                msl = gslot[g];
+                mo0 = goff[g];
+                mo1 = goff[g + 1];
+                mf = gfac[g];
+                mt = div_by(perm[mo0], magic);
+                mw = wdw[mo0];
+                if ((unsigned)msl >= (unsigned)d.S) msl = -1;
+            }
         }
+        int sl[NG], o0[NG], o1[NG];
+        float f[NG], w1[NG], acc[NG][CPL], x[NG][CPL];
 #pragma unroll
         for (int k = 0; k < NG; ++k) {
-            if (live[k]) {
-                load_vec<BT, CPL, false>(row[k], acc[k]);
+            sl[k] = __shfl_sync(0xffffffffu, msl, k);
+            if (sl[k] >= 0) {
+                load_vec<BT, CPL, false>(bank + (size_t)sl[k] * D, acc[k]);
             } else {
 #pragma unroll
                 for (int c = 0; c < CPL; ++c) acc[k][c] = 0.f;
@@ -312,34 +320,57 @@ __global__ void __launch_bounds__(kBlock) k_dw(Dims d, Inputs in, Work w, int st
         }
 #pragma unroll
         for (int k = 0; k < NG; ++k) {
-            if (!live[k]) continue;
+            const int t1 = __shfl_sync(0xffffffffu, mt, k);
+            o0[k] = __shfl_sync(0xffffffffu, mo0, k);
+            o1[k] = __shfl_sync(0xffffffffu, mo1, k);
+            f[k] = __shfl_sync(0xffffffffu, mf, k);
+            w1[k] = __shfl_sync(0xffffffffu, mw, k);
+            if (sl[k] >= 0) {
+                load_vec<float, CPL, false>(dvp + (size_t)t1 * D, x[k]);
+            } else {
+#pragma unroll
+                for (int c = 0; c < CPL; ++c) x[k][c] = 0.f;
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < NG; ++k) {
+            if (sl[k] < 0) continue;                                // warp-uniform
             if (in.snap)
                 store_vec<BT, CPL>(static_cast<BT *>(in.snap) +
                                        ((size_t)(ti * d.P + p) * CW + (o1[k] - 1)) * D + lane * CPL,
                                    acc[k]);
 #pragma unroll
-            for (int c = 0; c < CPL; ++c) acc[k][c] *= f[k];
-            int m = o0[k];
-            for (; m + 4 <= o1[k]; m += 4) {
-                float x[4][CPL], wt[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    wt[u] = wdw[m + u];
-                    load_vec<float, CPL, false>(dvp + (size_t)(perm[m + u] / W) * D, x[u]);
+            for (int c = 0; c < CPL; ++c) acc[k][c] = fmaf(w1[k], x[k][c], acc[k][c] * f[k]);
+            for (int m = o0[k] + 1; m < o1[k]; m += 32) {
+                const int cnt = o1[k] - m < 32 ? o1[k] - m : 32;
+                int pt = 0;
+                float pw = 0.f;
+                if (lane < cnt) {
+                    pt = div_by(perm[m + lane], magic);
+                    pw = wdw[m + lane];
                 }
+                for (int u0 = 0; u0 < cnt; u0 += 4) {
+                    float y[4][CPL], wt[4];
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
+                    for (int u = 0; u < 4; ++u) {
+                        const int tu = __shfl_sync(0xffffffffu, pt, (u0 + u) & 31);
+                        wt[u] = __shfl_sync(0xffffffffu, pw, (u0 + u) & 31);
+                        if (u0 + u < cnt) {
+                            load_vec<float, CPL, false>(dvp + (size_t)tu * D, y[u]);
+                        } else {
 #pragma unroll
-                    for (int c = 0; c < CPL; ++c) acc[k][c] = fmaf(wt[u], x[u][c], acc[k][c]);
+                            for (int c = 0; c < CPL; ++c) y[u][c] = 0.f;
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        if (u0 + u >= cnt) break;
+#pragma unroll
+                        for (int c = 0; c < CPL; ++c) acc[k][c] = fmaf(wt[u], y[u][c], acc[k][c]);
+                    }
+                }
             }
-            for (; m < o1[k]; ++m) {
-                float x[CPL];
-                const float wt = wdw[m];
-                load_vec<float, CPL, false>(dvp + (size_t)(perm[m] / W) * D, x);
-#pragma unroll
-                for (int c = 0; c < CPL; ++c) acc[k][c] = fmaf(wt, x[c], acc[k][c]);
-            }
-            store_vec<BT, CPL>(row[k], acc[k]);
+            store_vec<BT, CPL>(bank + (size_t)sl[k] * D, acc[k]);
         }
     }
 }

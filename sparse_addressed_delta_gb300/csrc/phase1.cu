@@ -238,6 +238,7 @@ __device__ void p1_reads(const P1Chunk<WT> &c, int er_lo, int er_hi, int tid, in
             if (er >= er_hi) continue;
             int lo = 0, hi = -1;
             float l = 0.f;
+            const float qf = __int_as_float(c.rhi[er]);   // q, staged there by step 1
             const bool valid = (unsigned)r[k] < (unsigned)c.S;
             if (valid && c.nw > 0) {
                 const int pos = base[k] + (c.srt[base[k]] <= target[k] ? 1 : 0) - 1;
@@ -250,7 +251,7 @@ __device__ void p1_reads(const P1Chunk<WT> &c, int er_lo, int er_hi, int tid, in
             c.rlo[er] = lo;
             c.rhi[er] = hi;
             c.lr[er] = l;
-            c.qw[er] = valid ? to_f32(c.q[er]) * expf(l) : 0.f;
+            c.qw[er] = valid ? qf * expf(l) : 0.f;
         }
     }
 }
@@ -375,6 +376,7 @@ __global__ void __launch_bounds__(NT, 2) k_phase1(Dims d, Inputs in, Work w, int
     // the workspace (same layout either way)
     unsigned long long *keyA;
     int32_t *inv, *pgid, *pgs, *rlo, *rhi;
+    int32_t *sgo = nullptr;   // group starts of the chunk on chip (else the chunk's goff row)
     float *lws, *lend, *kf;
     if (scratch_in_smem) {
         unsigned char *q = smem_raw + ((sizeof(P1Smem) + 15) & ~size_t(15));
@@ -386,7 +388,8 @@ __global__ void __launch_bounds__(NT, 2) k_phase1(Dims d, Inputs in, Work w, int
         lend = reinterpret_cast<float *>(q); q += 4 * (size_t)CW;
         kf = reinterpret_cast<float *>(q); q += 4 * (size_t)CW;
         rlo = reinterpret_cast<int32_t *>(q); q += 4 * (size_t)CR;
-        rhi = reinterpret_cast<int32_t *>(q);
+        rhi = reinterpret_cast<int32_t *>(q); q += 4 * (size_t)CR;
+        sgo = reinterpret_cast<int32_t *>(q);
     } else {
         keyA = w.keys + (size_t)blockIdx.x * 2 * CW;
         inv = w.inv + (size_t)blockIdx.x * CW;
@@ -418,6 +421,7 @@ __global__ void __launch_bounds__(NT, 2) k_phase1(Dims d, Inputs in, Work w, int
         int32_t *perm = w.perm + (size_t)n * CW;
         float *wdw = w.wdw + (size_t)n * CW;
         int32_t *goff = w.goff + (size_t)n * goff_stride(CW);
+        int32_t *go = scratch_in_smem ? sgo : goff;
         int32_t *gslot = w.gslot + (size_t)n * CW;
         float *gfac = w.gfac + (size_t)n * CW;
         float *gw = w.gw + (size_t)n * CW;
@@ -443,6 +447,7 @@ __global__ void __launch_bounds__(NT, 2) k_phase1(Dims d, Inputs in, Work w, int
                 bad = 1;
             }
             kf[i] = kk;
+            pgs[i] = __float_as_int(s == S ? 0.f : g[i]);   // g (0 if dropped), read in step 2
             wsl[i] = s < S ? s : kNoEntry;
             const int t = div_by(i, magW);
             keyA[i] = ((unsigned long long)(unsigned)s << 32) | ((unsigned)t << 8) |
@@ -452,6 +457,7 @@ __global__ void __launch_bounds__(NT, 2) k_phase1(Dims d, Inputs in, Work w, int
             const int r = rs[i];
             if ((unsigned)r >= (unsigned)S) report_bad_slot(w.status, (int)(tok_base + i / R));
             rsl[i] = (unsigned)r < (unsigned)S ? r : kNoEntry;
+            rhi[i] = __float_as_int(to_f32(q[i]));   // q, read back in step 3
         }
         // slot S may need one more radix digit than the real slots
         const int npass = __syncthreads_or(bad) ? (32 - __clz(S) + 7) / 8 : passes;
@@ -475,7 +481,7 @@ __global__ void __launch_bounds__(NT, 2) k_phase1(Dims d, Inputs in, Work w, int
             bool head = ok && (pos == 0 || (int)(srt[pos - 1] >> 32) != slot);
             float gv = 0.f;
             if (ok) {
-                gv = ((unsigned)ws[e] < (unsigned)S) ? g[e] : 0.f;
+                gv = __int_as_float(pgs[e]);
                 perm[pos] = e;
                 inv[e] = pos;
                 tkk[pos] = make_float2(__int_as_float((int)(low >> 8)), kf[e]);
@@ -492,7 +498,11 @@ __global__ void __launch_bounds__(NT, 2) k_phase1(Dims d, Inputs in, Work w, int
                 lws[pos] = lv;
                 lw[e] = lv;
                 pgid[pos] = gid;
-                if (head) { goff[gid] = pos; gslot[gid] = slot; }
+                if (head) {
+                    goff[gid] = pos;
+                    gslot[gid] = slot;
+                    if (scratch_in_smem) sgo[gid] = pos;
+                }
                 const bool tail = (pos == nw - 1) || (int)(srt[pos + 1] >> 32) != slot;
                 if (tail) {
                     lend[gid] = lv;
@@ -507,10 +517,11 @@ __global__ void __launch_bounds__(NT, 2) k_phase1(Dims d, Inputs in, Work w, int
             w.ngroups[n] = ng;
             w.nvalid[n] = nv;
             goff[ng] = nw;
+            if (scratch_in_smem) sgo[ng] = nw;
         }
         __syncthreads();
         // group start of every sorted position (one lookup instead of a chain later)
-        for (int pos = tid; pos < nw; pos += NT) pgs[pos] = goff[pgid[pos]];
+        for (int pos = tid; pos < nw; pos += NT) pgs[pos] = go[pgid[pos]];
         __syncthreads();
 
         const P1Chunk<WT> pc{rs, q, srt, tkk, inv, pgid, pgs, lws, lend, kf, rlo, rhi,
@@ -538,7 +549,7 @@ __global__ void __launch_bounds__(NT, 2) k_phase1(Dims d, Inputs in, Work w, int
                 w.wkey[o] = srt[pos];
                 w.wlws[o] = lws[pos];
                 w.wpgs[o] = pgs[pos];
-                w.wpge[o] = goff[pgid[pos] + 1];
+                w.wpge[o] = go[pgid[pos] + 1];
             }
             unsigned long long *rA = w.rkeys + (size_t)blockIdx.x * 2 * CR;
             unsigned long long *rB = rA + CR;
@@ -586,7 +597,7 @@ __global__ void __launch_bounds__(NT, 2) k_phase1(Dims d, Inputs in, Work w, int
             for (int i = tid; i < 2 * NB; i += NT) sm.hist[i] = 0;
             __syncthreads();
             auto digit = [&](int g) {
-                const int sz = goff[g + 1] - goff[g];
+                const int sz = go[g + 1] - go[g];
                 return sz >= kHotGroup ? 0 : 1 + kHotGroup - sz;
             };
             for (int g0 = 0; g0 < ng; g0 += NT) {
@@ -602,7 +613,7 @@ __global__ void __launch_bounds__(NT, 2) k_phase1(Dims d, Inputs in, Work w, int
                 w.ng4[n] = make_int4(ng, cnt[0], 0, 0);
             }
             __syncthreads();
-            int32_t *go = w.gord + (size_t)n * CW;
+            int32_t *gord = w.gord + (size_t)n * CW;
             for (int g0 = 0; g0 < ng; g0 += NT) {
                 const int g = g0 + tid;
                 const int dig = g < ng ? digit(g) : NB;
@@ -611,7 +622,7 @@ __global__ void __launch_bounds__(NT, 2) k_phase1(Dims d, Inputs in, Work w, int
                 int first = 0;
                 if (dig < NB && lane == leader) first = atomicAdd(&cur[dig], __popc(peers));
                 first = __shfl_sync(0xffffffffu, first, leader);
-                if (dig < NB) go[bas[dig] + first + __popc(peers & ((1u << lane) - 1u))] = g;
+                if (dig < NB) gord[bas[dig] + first + __popc(peers & ((1u << lane) - 1u))] = g;
             }
         }
         for (int i = nw + tid; i < CW; i += NT) {
@@ -664,7 +675,8 @@ __global__ void __launch_bounds__(NTR) k_phase1_rows(Dims d, Inputs in, Work w, 
 
 size_t phase1_scratch_smem(const Dims &d) {
     const size_t CW = (size_t)d.C * d.W, CR = (size_t)d.C * d.R;
-    return ((sizeof(P1Smem) + 15) & ~size_t(15)) + 8 * 2 * CW + 4 * 6 * CW + 4 * 2 * CR;
+    return ((sizeof(P1Smem) + 15) & ~size_t(15)) + 8 * 2 * CW + 4 * 6 * CW + 4 * 2 * CR +
+           4 * (CW + 4);   // + the group starts
 }
 
 bool phase1_split(const Dims &d) { return phase1_scratch_smem(d) > kPhase1SmemMax; }

@@ -268,14 +268,15 @@ __global__ void __launch_bounds__(MM_T) k_dualmm(Dims d, Inputs in, Work w, int 
 // DW: one warp per group (distinct written slot) of each chunk of the step. A warp takes NG
 // groups at once (the next ones of its stride): lane k < NG loads group k's slot, bounds,
 // factor and first member with coalesced-by-lane loads, the warp broadcasts them by shuffle
-// and issues all NG B0 row loads and first-member delta_v loads before any arithmetic. Further
+// and issues all NG B0 row loads and first-member delta_v loads before any arithmetic (the
+// kernel is bound by the B0 rows in flight per SM: 16 warps x NG). Further
 // members are fetched 32 at a time the same way (lane l loads member l's token and weight).
 // Each row adds its members in sorted order after exp(lend) B0: the order of the sum is that
 // of the group, whatever NG is.
 // ---------------------------------------------------------------------------------------
 template <typename BT, int CPL>
 __global__ void __launch_bounds__(kBlock, 2) k_dw(Dims d, Inputs in, Work w, int step0, int ti) {
-    constexpr int NG = CPL <= 2 ? 8 : (CPL <= 8 ? 4 : 2);   // 2 NG CPL floats of row data
+    constexpr int NG = CPL <= 4 ? 8 : (CPL <= 8 ? 4 : 2);   // 2 NG CPL floats of row data
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int p = blockIdx.y;
     const int n = (ti - step0) * d.P + p;
@@ -306,8 +307,8 @@ __global__ void __launch_bounds__(kBlock, 2) k_dw(Dims d, Inputs in, Work w, int
                 if ((unsigned)msl >= (unsigned)d.S) msl = -1;
             }
         }
-        int sl[NG], o0[NG], o1[NG];
-        float f[NG], w1[NG], acc[NG][CPL], x[NG][CPL];
+        int sl[NG];
+        float acc[NG][CPL], x[NG][CPL];
 #pragma unroll
         for (int k = 0; k < NG; ++k) {
             sl[k] = __shfl_sync(0xffffffffu, msl, k);
@@ -321,10 +322,6 @@ __global__ void __launch_bounds__(kBlock, 2) k_dw(Dims d, Inputs in, Work w, int
 #pragma unroll
         for (int k = 0; k < NG; ++k) {
             const int t1 = __shfl_sync(0xffffffffu, mt, k);
-            o0[k] = __shfl_sync(0xffffffffu, mo0, k);
-            o1[k] = __shfl_sync(0xffffffffu, mo1, k);
-            f[k] = __shfl_sync(0xffffffffu, mf, k);
-            w1[k] = __shfl_sync(0xffffffffu, mw, k);
             if (sl[k] >= 0) {
                 load_vec<float, CPL, false>(dvp + (size_t)t1 * D, x[k]);
             } else {
@@ -334,15 +331,20 @@ __global__ void __launch_bounds__(kBlock, 2) k_dw(Dims d, Inputs in, Work w, int
         }
 #pragma unroll
         for (int k = 0; k < NG; ++k) {
+            // the group's bounds, factor and first weight, from lane k
+            const int o0 = __shfl_sync(0xffffffffu, mo0, k);
+            const int o1 = __shfl_sync(0xffffffffu, mo1, k);
+            const float f = __shfl_sync(0xffffffffu, mf, k);
+            const float w1 = __shfl_sync(0xffffffffu, mw, k);
             if (sl[k] < 0) continue;                                // warp-uniform
             if (in.snap)
                 store_vec<BT, CPL>(static_cast<BT *>(in.snap) +
-                                       ((size_t)(ti * d.P + p) * CW + (o1[k] - 1)) * D + lane * CPL,
+                                       ((size_t)(ti * d.P + p) * CW + (o1 - 1)) * D + lane * CPL,
                                    acc[k]);
 #pragma unroll
-            for (int c = 0; c < CPL; ++c) acc[k][c] = fmaf(w1[k], x[k][c], acc[k][c] * f[k]);
-            for (int m = o0[k] + 1; m < o1[k]; m += 32) {
-                const int cnt = o1[k] - m < 32 ? o1[k] - m : 32;
+            for (int c = 0; c < CPL; ++c) acc[k][c] = fmaf(w1, x[k][c], acc[k][c] * f);
+            for (int m = o0 + 1; m < o1; m += 32) {
+                const int cnt = o1 - m < 32 ? o1 - m : 32;
                 int pt = 0;
                 float pw = 0.f;
                 if (lane < cnt) {
@@ -434,7 +436,8 @@ cudaError_t gather_cpl(const Dims &d, const Inputs &in, const Work &w, int step0
 template <typename BT, int CPL>
 cudaError_t dw_cpl(const Dims &d, const Inputs &in, const Work &w, int step0, int ti,
                    cudaStream_t st) {
-    int gx = (8 * kRefSms + d.P - 1) / d.P;
+    // two waves of the two CTAs an SM holds (measured best among one to eight CTAs per SM)
+    int gx = (4 * kRefSms + d.P - 1) / d.P;
     const int max_groups = d.C * d.W;
     const int need = (max_groups + kWarps - 1) / kWarps;
     if (gx > need) gx = need;

@@ -209,36 +209,59 @@ __global__ void __launch_bounds__(MM_T) k_dualmm(Dims d, Inputs in, Work w, int 
     const int g4 = lane >> 2, i4 = lane & 3;
     const int mat = warp >> 1, nb = (warp & 1) * 4;          // this warp: matrix, first n8 tile
     const float *A = mat ? Qs : Xs;
-    float acc[4][4];
+    // independent accumulator chains: even and odd k-steps apart (h), and for float32 banks the
+    // two small 3xTF32 terms apart from hi*hi (accs); summed once at the end in a fixed order
+    constexpr int NS = sizeof(BT) == 4 ? 2 : 1;
+    float acc[2][4][4], accs[NS][4][4];
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[h][j][q] = 0.f;
+#pragma unroll
+    for (int h = 0; h < NS; ++h)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) accs[h][j][q] = 0.f;
+    const int kend = mm_kpad(nv < C ? nv : C);                // u_pre is zero past nv
+    for (int k00 = 0; k00 < kend; k00 += 16) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int k0 = k00 + 8 * h;
+            if (k0 >= kend) break;
+            const float af[4] = {A[g4 * AP + k0 + i4], A[(g4 + 8) * AP + k0 + i4],
+                                 A[g4 * AP + k0 + i4 + 4], A[(g4 + 8) * AP + k0 + i4 + 4]};
+            unsigned ah[4], al[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) ah[q] = to_tf32(af[q]);
+            if constexpr (sizeof(BT) == 4) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) al[q] = to_tf32(af[q] - __uint_as_float(ah[q]));
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int col = (nb + j) * 8 + g4;
+                const float bf[2] = {Us[(k0 + i4) * MM_UP + col], Us[(k0 + i4 + 4) * MM_UP + col]};
+                unsigned bh[2] = {to_tf32(bf[0]), to_tf32(bf[1])};
+                if constexpr (sizeof(BT) == 4) {
+                    unsigned bl[2] = {to_tf32(bf[0] - __uint_as_float(bh[0])),
+                                      to_tf32(bf[1] - __uint_as_float(bh[1]))};
+                    mma_tf32(accs[h & (NS - 1)][j], ah, bl);
+                    mma_tf32(accs[h & (NS - 1)][j], al, bh);
+                }
+                mma_tf32(acc[h][j], ah, bh);
+            }
+        }
+    }
 #pragma unroll
     for (int j = 0; j < 4; ++j)
 #pragma unroll
-        for (int q = 0; q < 4; ++q) acc[j][q] = 0.f;
-    const int kend = mm_kpad(nv < C ? nv : C);                // u_pre is zero past nv
-    for (int k0 = 0; k0 < kend; k0 += 8) {
-        const float af[4] = {A[g4 * AP + k0 + i4], A[(g4 + 8) * AP + k0 + i4],
-                             A[g4 * AP + k0 + i4 + 4], A[(g4 + 8) * AP + k0 + i4 + 4]};
-        unsigned ah[4], al[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) ah[q] = to_tf32(af[q]);
-        if constexpr (sizeof(BT) == 4) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) al[q] = to_tf32(af[q] - __uint_as_float(ah[q]));
+        for (int q = 0; q < 4; ++q) {
+            acc[0][j][q] += acc[1][j][q];
+            if constexpr (sizeof(BT) == 4) acc[0][j][q] += accs[0][j][q] + accs[NS - 1][j][q];
         }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int col = (nb + j) * 8 + g4;
-            const float bf[2] = {Us[(k0 + i4) * MM_UP + col], Us[(k0 + i4 + 4) * MM_UP + col]};
-            unsigned bh[2] = {to_tf32(bf[0]), to_tf32(bf[1])};
-            if constexpr (sizeof(BT) == 4) {
-                unsigned bl[2] = {to_tf32(bf[0] - __uint_as_float(bh[0])),
-                                  to_tf32(bf[1] - __uint_as_float(bh[1]))};
-                mma_tf32(acc[j], ah, bl);
-                mma_tf32(acc[j], al, bh);
-            }
-            mma_tf32(acc[j], ah, bh);
-        }
-    }
 
     BT *out = static_cast<BT *>(in.readings);
 #pragma unroll
@@ -248,7 +271,7 @@ __global__ void __launch_bounds__(MM_T) k_dualmm(Dims d, Inputs in, Work w, int 
             const int row = m0 + g4 + 8 * h, col = d0 + (nb + j) * 8 + 2 * i4;
             if (row >= C || col >= D) continue;
             const bool live = row < nv;
-            float o[2] = {live ? acc[j][2 * h] : 0.f, live ? acc[j][2 * h + 1] : 0.f};
+            float o[2] = {live ? acc[0][j][2 * h] : 0.f, live ? acc[0][j][2 * h + 1] : 0.f};
             if (mat == 0) {
                 store_vec<float, 2>(w.dv + ((size_t)p * C + row) * D + col, o);
             } else if ((size_t)ti * C + row < (size_t)d.T) {
@@ -411,9 +434,13 @@ __global__ void k_debug_expand(Dims d, Work w, int32_t *perm_out, uint8_t *gs_ou
 // dispatch
 // ---------------------------------------------------------------------------------------
 int gather_wpt(const Dims &d) {
+    // warps per token: enough warps for the whole GPU, more of them for rows of 512 bytes or
+    // more (measured: 32 warps per SM suit 256-byte rows, 64 the 512-byte ones)
     const long tokens = (long)d.P * d.C;
+    const int row_bytes = d.D * (d.dtype == SDM_BF16 ? 2 : 4);
+    const long target = (row_bytes >= 512 ? 64L : 32L) * kRefSms;
     int wpt = 1;
-    while (wpt < 8 && tokens * wpt < 32L * kRefSms && 2 * wpt <= (d.W < d.R ? d.W : d.R)) wpt *= 2;
+    while (wpt < 8 && tokens * wpt < target && 2 * wpt <= (d.W < d.R ? d.W : d.R)) wpt *= 2;
     return wpt;
 }
 

@@ -285,10 +285,12 @@ __device__ __forceinline__ void cp_async_wait() {
 // fragment layout: g = lane / 4, i = lane % 4; A: a0 (g, i), a1 (g + 8, i), a2 (g, i + 4),
 // a3 (g + 8, i + 4); B: b0 (i, g), b1 (i + 4, g); C: c0 (g, 2i), c1 (g, 2i + 1), c2 (g + 8, 2i),
 // c3 (g + 8, 2i + 1)). Float32 operands go through the 3xTF32 split (hi*lo + lo*hi + hi*hi).
+// TF32 operand of a finite float: round to nearest, ties away from zero, on the bit pattern
+// (add half a unit in the last of the ten kept mantissa bits to the magnitude, then clear the
+// thirteen low bits; a carry into the exponent is the correct rounding up). Two integer
+// operations, where the conversion instruction costs more inside the dual matmul's loop.
 __device__ __forceinline__ unsigned to_tf32(float x) {
-    unsigned r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
+    return (__float_as_uint(x) + 0x1000u) & 0xffffe000u;
 }
 
 __device__ __forceinline__ void mma_tf32(float (&c)[4], const unsigned (&a)[4],

@@ -156,18 +156,24 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def traffic_record(kernel: str):
-    """DRAM bytes per launch of ``kernel`` from the committed ncu summary, if the kernel's
-    source is unchanged since the capture (else None)."""
+def traffic_record(kernel: str, workload: str):
+    """DRAM bytes per launch of ``kernel`` on ``workload`` from the committed ncu summary, if
+    every source the record names is unchanged since the capture (else None)."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
-        rec = json.load(open(path))[kernel]
-        src = open(os.path.join(ROOT, "sparse_addressed_delta_gb300", "csrc", rec["source"]), "rb").read()
-        if hashlib.sha256(src).hexdigest()[:16] != rec["source_sha256_16"]:
-            return None
-        return float(rec["dram_bytes_per_launch"])
+        for rec in json.load(open(path))[kernel]:
+            if rec["workload"] != workload:
+                continue
+            h = hashlib.sha256()
+            for name in rec["sources"]:
+                h.update(open(os.path.join(ROOT, "sparse_addressed_delta_gb300", "csrc", name),
+                              "rb").read())
+            if h.hexdigest()[:16] != rec["sources_sha256_16"]:
+                return None
+            return float(rec["dram_bytes_per_launch"])
     except Exception:
         return None
+    return None
 
 
 # ------------------------------------------------------------------------------------------
@@ -358,7 +364,8 @@ def run_ours(args):
         ach = per_launch / secs / 1e9
         roofline = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
                     "frac": ach / peak, "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
-                    "alg_bytes_per_launch": per_launch, "traffic": traffic_record(dom)}
+                    "alg_bytes_per_launch": per_launch,
+                    "traffic": traffic_record(dom, wl.name)}
     else:
         roofline = {"kernel": dom, "bound": "alu", "note": "dominant kernel is not HBM-bound"}
     p2_ms = fam_ms["gather"] + fam_ms["dw"] + fam_ms["phase2"]

@@ -66,6 +66,23 @@ def dist_env():
     return world, rank, local
 
 
+def rank_totals(ms: float, tokens: int, world: int, device=None):
+    """Whole-job figures of a weak-scaling run: (the slowest rank's time, all ranks' tokens).
+    Every rank calls it with its own numbers; with world > 1 it reduces over the default
+    process group (MAX of the times, SUM of the tokens: ranks draw different seeds, so their
+    valid-token counts differ on ragged workloads). Works with the nccl and gloo backends."""
+    if world <= 1:
+        return float(ms), int(tokens)
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    n = torch.tensor([int(tokens)], dtype=torch.int64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(n, op=dist.ReduceOp.SUM)
+    return float(t.item()), int(n.item())
+
+
 def workload_config(wl, inputs):
     return {"workload": wl.name, "P": wl.P, "T": wl.T, "C": wl.C, "S": wl.S, "D": wl.D,
             "W": wl.W, "R": wl.R, "bank_dtype": wl.dtype, "slots": wl.slots,
@@ -324,11 +341,8 @@ def run_ours(args):
     clk = clocks.stop()
     step_ms = [a.elapsed_time(b) for a, b in ev]
     ms = statistics.mean(step_ms)
-    ms_t = torch.tensor([ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
-    ms_max = float(ms_t.item())
-    value = world * tokens / (ms_max / 1e3)
+    ms_max, tokens_all = rank_totals(ms, tokens, world, dev)
+    value = tokens_all / (ms_max / 1e3)
 
     # ---- per-kernel device times (same protocol, events around every launch) ----
     fam_ms = {k: 0.0 for k in sdm.KERNEL_KINDS}
@@ -409,10 +423,8 @@ def run_ours(args):
                 e2e_ms.append(a.elapsed_time(b))
     if not torch.equal(h_read, readings.cpu()):
         raise RuntimeError("the host-buffer call does not reproduce the device call's readings")
-    e2e_t = torch.tensor([statistics.mean(e2e_ms)], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(e2e_t, op=dist.ReduceOp.MAX)
-    e2e = {"value": world * tokens / (float(e2e_t.item()) / 1e3), "unit": UNIT,
+    e2e_max, _ = rank_totals(statistics.mean(e2e_ms), tokens, world, dev)
+    e2e = {"value": tokens_all / (e2e_max / 1e3), "unit": UNIT,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "path": "sdm_write_read_host: pinned host inputs copied in by the call (v on a "
                    "second stream under Phase 1), readings stored into pinned host memory by "

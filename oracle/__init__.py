@@ -11,6 +11,9 @@ Functions (every one cites the definition it follows in ``sdm_oracle.c``):
   plan        the sorted kind row, groups, owners and single-entry flags of one chunk
               (phase2_kernels.py module docstring)
   backward    reverse mode of the token loop, with the bank restored
+  backward_snapshot
+              the reverse mode as the chunked backward runs it from a stored (optionally
+              bfloat16) snapshot of the rows each chunk writes (memory_ops.py snapshot_quant)
 
 Pins (tests/test_oracle.py): dense brute force, closed forms (scalar delta rule, pure
 decay), chunk-size invariance, the solve identity, brute-force grouping and central
@@ -71,6 +74,12 @@ def _load():
                                                 _dbl_or_null, _f64p, _f64p, _f64p, _f64p,
                                                 _f64p, _f64p, I]
             lib.sdm_oracle_backward.restype = I
+            lib.sdm_oracle_backward_snapshot.argtypes = [I, I, I, I, I, I, I, I, _f64p, _i32p,
+                                                         _f64p, _f64p, _f64p, _f64p, _i32p,
+                                                         _f64p, _i32p, _f64p, _dbl_or_null,
+                                                         _f64p, _f64p, _f64p, _f64p, _f64p,
+                                                         _f64p, I]
+            lib.sdm_oracle_backward_snapshot.restype = I
             _lib = lib
     return _lib
 
@@ -188,6 +197,40 @@ def backward(bank, ws, k, g, beta, v, rs, q, valid, grad_readings, nthreads: int
                                      None if gfb is None else gfb.ctypes.data, dB, dv, db, dk,
                                      dg, dq, int(nthreads))
     _check(rc, "backward")
+    return {"grad_bank": dB, "grad_v": dv, "grad_beta": db, "grad_write_w": dk,
+            "grad_log_decay": dg, "grad_read_w": dq, "restored_bank": B}
+
+
+SNAPSHOT_MODES = {"none": 0, "bf16": 1}
+
+
+def backward_snapshot(bank, ws, k, g, beta, v, rs, q, valid, grad_readings, *, chunk_size: int,
+                      snapshot: str = "bf16", nthreads: int = 1, grad_final_bank=None):
+    """Reverse mode as the chunked backward runs it from a stored snapshot: chunks in reverse,
+    each restoring its written rows to Q(their value at the chunk start) ("none": Q is the
+    identity; "bf16": float32 then bfloat16 rounding, to nearest even), re-running the chunk and
+    taking its reverse pass. Same outputs as ``backward``; ``restored_bank`` holds Q(initial
+    value) on every row a valid token writes."""
+    B = _f64(bank).copy()
+    ws, rs = _i32(ws), _i32(rs)
+    P, T, S, D, W, R = _dims(B, ws, rs, v)
+    valid = _i32(np.full(P, T) if valid is None else valid)
+    dB = np.zeros((P * S, D), np.float64)
+    dv = np.zeros((P, T, D), np.float64)
+    db = np.zeros((P, T), np.float64)
+    dk = np.zeros((P, T, W), np.float64)
+    dg = np.zeros((P, T, W), np.float64)
+    dq = np.zeros((P, T, R), np.float64)
+    gfb = None
+    if grad_final_bank is not None:
+        gfb = _f64(grad_final_bank)
+        if gfb.shape != (P * S, D):
+            raise ValueError(f"grad_final_bank must be {(P * S, D)}, got {gfb.shape}")
+    rc = _load().sdm_oracle_backward_snapshot(
+        P, T, int(chunk_size), S, D, W, R, SNAPSHOT_MODES[snapshot], B, ws, _f64(k), _f64(g),
+        _f64(beta), _f64(v), rs, _f64(q), valid, _f64(grad_readings),
+        None if gfb is None else gfb.ctypes.data, dB, dv, db, dk, dg, dq, int(nthreads))
+    _check(rc, "backward_snapshot")
     return {"grad_bank": dB, "grad_v": dv, "grad_beta": db, "grad_write_w": dk,
             "grad_log_decay": dg, "grad_read_w": dq, "restored_bank": B}
 

@@ -444,33 +444,21 @@ int sdm_oracle_plan(int n, int width, const int32_t *slots, int32_t *perm, uint8
  *   dg_j = <dd_j, d_j> (= exp(g_j) <dd_j, a_j>) ;  dB[s_j] = exp(g_j) dd_j
  *   restore B[s_j] = a_j
  * ------------------------------------------------------------------------------------ */
-static int backward_stream(int T, int S, int D, int W, int R, double *B, const int32_t *ws,
-                           const double *k, const double *g, const double *beta,
-                           const double *v, const int32_t *rs, const double *q, int valid,
-                           const double *dout, const double *dB_final, double *dB, double *dv,
-                           double *dbeta, double *dk, double *dg, double *dq, double *a_log,
-                           double *tmp) {
-    double *out = tmp;                    /* [T*D] forward readings (unused) */
-    double *a = out + (size_t)T * D;      /* [W*D] */
-    double *ret = a + (size_t)W * D;      /* [D] */
-    double *d = ret + D;                  /* [W*D] */
+/* The reverse pass over tokens t_hi - 1 .. t_lo of one stream (the per-token step above),
+ * with B the bank after token t_hi - 1 and a_log the pre-write rows of those tokens; leaves B
+ * as it was before token t_lo and adds into dB (the running bank gradient). */
+static void reverse_tokens(int t_lo, int t_hi, int D, int W, int R, double *B,
+                           const int32_t *ws, const double *k, const double *g,
+                           const double *beta, const double *v, const int32_t *rs,
+                           const double *q, const double *dout, double *dB, double *dv,
+                           double *dbeta, double *dk, double *dg, double *dq,
+                           const double *a_log, double *tmp) {
+    double *d = tmp;                      /* [W*D] */
     double *dd = d + (size_t)W * D;       /* [W*D] */
     double *du = dd + (size_t)W * D;      /* [D] */
     double *u = du + D;                   /* [D] */
     double *rt = u + D;                   /* [D] */
-    int rc = sequential_stream(T, S, D, W, R, B, ws, k, g, beta, v, rs, q, valid, out, a, ret,
-                               a_log);
-    if (rc) return rc;
-    if (dB_final)
-        memcpy(dB, dB_final, sizeof(double) * (size_t)S * D);
-    else
-        memset(dB, 0, sizeof(double) * (size_t)S * D);
-    memset(dv, 0, sizeof(double) * (size_t)T * D);
-    memset(dbeta, 0, sizeof(double) * (size_t)T);
-    memset(dk, 0, sizeof(double) * (size_t)T * W);
-    memset(dg, 0, sizeof(double) * (size_t)T * W);
-    memset(dq, 0, sizeof(double) * (size_t)T * R);
-    for (int t = valid - 1; t >= 0; --t) {
+    for (int t = t_hi - 1; t >= t_lo; --t) {
         const int32_t *s = ws + (size_t)t * W, *r = rs + (size_t)t * R;
         const double *kt = k + (size_t)t * W, *gt = g + (size_t)t * W, *qt = q + (size_t)t * R;
         const double *vt = v + (size_t)t * D, *dO = dout + (size_t)t * D;
@@ -532,7 +520,168 @@ static int backward_stream(int T, int S, int D, int W, int R, double *B, const i
             }
         }
     }
+}
+
+static int backward_stream(int T, int S, int D, int W, int R, double *B, const int32_t *ws,
+                           const double *k, const double *g, const double *beta,
+                           const double *v, const int32_t *rs, const double *q, int valid,
+                           const double *dout, const double *dB_final, double *dB, double *dv,
+                           double *dbeta, double *dk, double *dg, double *dq, double *a_log,
+                           double *tmp) {
+    double *out = tmp;                    /* [T*D] forward readings (unused) */
+    double *a = out + (size_t)T * D;      /* [W*D] */
+    double *ret = a + (size_t)W * D;      /* [D] */
+    double *rev = ret + D;                /* [2*W*D + 3*D] scratch of reverse_tokens */
+    int rc = sequential_stream(T, S, D, W, R, B, ws, k, g, beta, v, rs, q, valid, out, a, ret,
+                               a_log);
+    if (rc) return rc;
+    if (dB_final)
+        memcpy(dB, dB_final, sizeof(double) * (size_t)S * D);
+    else
+        memset(dB, 0, sizeof(double) * (size_t)S * D);
+    memset(dv, 0, sizeof(double) * (size_t)T * D);
+    memset(dbeta, 0, sizeof(double) * (size_t)T);
+    memset(dk, 0, sizeof(double) * (size_t)T * W);
+    memset(dg, 0, sizeof(double) * (size_t)T * W);
+    memset(dq, 0, sizeof(double) * (size_t)T * R);
+    reverse_tokens(0, valid, D, W, R, B, ws, k, g, beta, v, rs, q, dout, dB, dv, dbeta, dk, dg,
+                   dq, a_log, rev);
     return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------------------
+ * Reverse mode with a stored snapshot, one stream (memory_ops.py, sdm_write_read docstring:
+ * snapshot_quant, "the backward restores ... the written rows to their dequantized snapshot";
+ * phase2_kernels.py module docstring: DW stores the snapshot, Phase A restores the rows).
+ * The backward walks the chunks in reverse. For chunk c it
+ *   1. restores every row the chunk's valid tokens write to Q(its value at the chunk start),
+ *      the snapshot the forward kept (Q = identity for "none", bfloat16 rounding for "bf16");
+ *   2. re-runs the chunk's tokens from that bank, logging their pre-write rows;
+ *   3. takes the reverse pass of those tokens (reverse_tokens), which puts the bank back to
+ *      its state at step 1 and carries dB to the chunk before.
+ * With Q = identity this is the reverse mode above. Q(x) rounds x first to float32 (the
+ * precision of the float32 bank the snapshot is taken from), then to bfloat16, to nearest
+ * even: add 0x7fff plus the lowest kept bit to the float32 pattern and clear 16 bits.
+ * ------------------------------------------------------------------------------------ */
+static double quant_bf16(double x) {
+    float f = (float)x;
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    u += 0x7fffu + ((u >> 16) & 1u);
+    u &= 0xffff0000u;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+static int backward_snapshot_stream(int T, int C, int S, int D, int W, int R, int mode, double *B,
+                                    const int32_t *ws, const double *k, const double *g,
+                                    const double *beta, const double *v, const int32_t *rs,
+                                    const double *q, int valid, const double *dout,
+                                    const double *dB_final, double *dB, double *dv, double *dbeta,
+                                    double *dk, double *dg, double *dq, double *a_log,
+                                    double *snap, double *tmp) {
+    double *out = tmp;                    /* [T*D] readings of the re-runs (unused) */
+    double *a = out + (size_t)T * D;      /* [W*D] */
+    double *ret = a + (size_t)W * D;      /* [D] */
+    double *rev = ret + D;                /* [2*W*D + 3*D] */
+    const int Nt = (T + C - 1) / C;
+    /* forward, chunk by chunk: the snapshot of each write entry is its row at the chunk start */
+    for (int c = 0; c < Nt; ++c) {
+        const int t0 = c * C, t1 = t0 + C < valid ? t0 + C : valid;
+        for (int t = t0; t < t1; ++t)
+            for (int j = 0; j < W; ++j) {
+                const int32_t sl = ws[(size_t)t * W + j];
+                if (sl < 0 || sl >= S) return ORACLE_EINVAL;
+                memcpy(snap + ((size_t)t * W + j) * D, B + (size_t)sl * D, sizeof(double) * D);
+            }
+        if (t1 > t0) {
+            int rc = sequential_stream(t1 - t0, S, D, W, R, B, ws + (size_t)t0 * W,
+                                       k + (size_t)t0 * W, g + (size_t)t0 * W, beta + t0,
+                                       v + (size_t)t0 * D, rs + (size_t)t0 * R,
+                                       q + (size_t)t0 * R, t1 - t0, out, a, ret, NULL);
+            if (rc) return rc;
+        }
+    }
+    if (dB_final)
+        memcpy(dB, dB_final, sizeof(double) * (size_t)S * D);
+    else
+        memset(dB, 0, sizeof(double) * (size_t)S * D);
+    memset(dv, 0, sizeof(double) * (size_t)T * D);
+    memset(dbeta, 0, sizeof(double) * (size_t)T);
+    memset(dk, 0, sizeof(double) * (size_t)T * W);
+    memset(dg, 0, sizeof(double) * (size_t)T * W);
+    memset(dq, 0, sizeof(double) * (size_t)T * R);
+    for (int c = Nt - 1; c >= 0; --c) {
+        const int t0 = c * C, t1 = t0 + C < valid ? t0 + C : valid;
+        if (t1 <= t0) continue;
+        /* 1. restore the chunk's written rows from the snapshot */
+        for (int t = t0; t < t1; ++t)
+            for (int j = 0; j < W; ++j) {
+                const double *sr = snap + ((size_t)t * W + j) * D;
+                double *row = B + (size_t)ws[(size_t)t * W + j] * D;
+                for (int e = 0; e < D; ++e) row[e] = mode ? quant_bf16(sr[e]) : sr[e];
+            }
+        /* 2. re-run the chunk, logging the pre-write rows at their tokens */
+        int rc = sequential_stream(t1 - t0, S, D, W, R, B, ws + (size_t)t0 * W,
+                                   k + (size_t)t0 * W, g + (size_t)t0 * W, beta + t0,
+                                   v + (size_t)t0 * D, rs + (size_t)t0 * R, q + (size_t)t0 * R,
+                                   t1 - t0, out, a, ret, a_log + (size_t)t0 * W * D);
+        if (rc) return rc;
+        /* 3. the reverse pass of the chunk's tokens */
+        reverse_tokens(t0, t1, D, W, R, B, ws, k, g, beta, v, rs, q, dout, dB, dv, dbeta, dk, dg,
+                       dq, a_log, rev);
+    }
+    return ORACLE_OK;
+}
+
+/* Reverse mode with a stored snapshot over all streams (arguments as sdm_oracle_backward,
+ * plus the chunk size C and mode 0 = "none", 1 = "bf16"). bank: in = initial bank; out = the
+ * bank the backward leaves: every row some valid token writes holds Q(its initial value). */
+int sdm_oracle_backward_snapshot(int P, int T, int C, int S, int D, int W, int R, int mode,
+                                 double *bank, const int32_t *ws, const double *k,
+                                 const double *g, const double *beta, const double *v,
+                                 const int32_t *rs, const double *q, const int32_t *valid,
+                                 const double *dout, const double *dbank_final, double *dbank,
+                                 double *dv, double *dbeta, double *dk, double *dg, double *dq,
+                                 int nthreads) {
+    if (check_sizes(P, T, S, D, W, R) || C < 1 || (mode != 0 && mode != 1)) return ORACLE_EINVAL;
+    for (int p = 0; p < P; ++p)
+        if (valid[p] < 0 || valid[p] > T) return ORACLE_EINVAL;
+    int status = ORACLE_OK;
+#ifdef _OPENMP
+    if (nthreads < 1) nthreads = 1;
+#pragma omp parallel for num_threads(nthreads) schedule(dynamic, 1)
+#else
+    (void)nthreads;
+#endif
+    for (int p = 0; p < P; ++p) {
+        size_t logn = (size_t)T * W * D;
+        size_t tmpn = (size_t)T * D + 3 * (size_t)W * D + 4 * (size_t)D;
+        double *a_log = (double *)malloc(sizeof(double) * logn);
+        double *snap = (double *)malloc(sizeof(double) * logn);
+        double *tmp = (double *)malloc(sizeof(double) * tmpn);
+        int rc;
+        if (!a_log || !snap || !tmp) {
+            rc = ORACLE_ENOMEM;
+        } else {
+            size_t o = (size_t)p * T;
+            rc = backward_snapshot_stream(
+                T, C, S, D, W, R, mode, bank + (size_t)p * S * D, ws + o * W, k + o * W,
+                g + o * W, beta + o, v + o * D, rs + o * R, q + o * R, valid[p], dout + o * D,
+                dbank_final ? dbank_final + (size_t)p * S * D : NULL, dbank + (size_t)p * S * D,
+                dv + o * D, dbeta + o, dk + o * W, dg + o * W, dq + o * R, a_log, snap, tmp);
+        }
+        free(a_log);
+        free(snap);
+        free(tmp);
+        if (rc) {
+#ifdef _OPENMP
+#pragma omp critical
+#endif
+            status = rc;
+        }
+    }
+    return status;
 }
 
 /* Forward + reverse over all streams. bank: in = initial bank; out = the initial bank

@@ -279,3 +279,86 @@ def test_backward_finite_differences_and_restore(with_final):
             fd = (loss(yp) - loss(ym)) / (2 * h)
             an = gr[gkey].reshape(-1)[fi]
             assert abs(fd - an) <= 1e-6 * max(1.0, abs(fd)), (key, fi, fd, an)
+
+
+# ---------------------------------------------------------------------------------------
+# reverse mode from a stored snapshot (memory_ops.py sdm_write_read: snapshot_quant)
+# ---------------------------------------------------------------------------------------
+
+GRAD_KEYS = ("grad_bank", "grad_v", "grad_beta", "grad_write_w", "grad_log_decay",
+             "grad_read_w")
+
+
+def bf16_of_f32(x):
+    """bfloat16 rounding (to nearest even) of the float32 value of x, by torch's conversion."""
+    import torch
+
+    return torch.from_numpy(np.asarray(x, np.float64)).float().bfloat16().double().numpy()
+
+
+@pytest.mark.parametrize("C", [1, 3, 8, 64])
+@pytest.mark.parametrize("with_final", [False, True])
+def test_backward_snapshot_none_is_the_reverse_mode(C, with_final):
+    """With an unrounded snapshot the chunked reverse pass is the token loop's reverse mode,
+    bit for bit, at any chunk size (rows written in several chunks, ragged valid tokens)."""
+    _, x = rand_case(P=2, T=23, S=7, D=3, W=3, R=2, seed=41)
+    rng = np.random.default_rng(42)
+    dO = rng.standard_normal((2, 23, 3))
+    G = rng.standard_normal((14, 3)) if with_final else None
+    ref = oracle.backward(*args(x), dO, grad_final_bank=G)
+    got = oracle.backward_snapshot(*args(x), dO, chunk_size=C, snapshot="none", grad_final_bank=G)
+    for key in GRAD_KEYS + ("restored_bank",):
+        np.testing.assert_array_equal(got[key], ref[key], err_msg=key)
+
+
+def test_backward_snapshot_bf16_restores_rounded_initial_rows():
+    """A bfloat16 snapshot leaves every row some valid token writes at bf16(its initial
+    value), and every other row untouched, whatever the chunking."""
+    _, x = rand_case(P=2, T=37, S=11, D=4, W=3, R=2, seed=43)
+    dO = np.random.default_rng(44).standard_normal((2, 37, 4))
+    written = np.zeros(2 * 11, bool)
+    for p in range(2):
+        for t in range(x["valid"][p]):
+            written[p * 11 + x["ws"][p, t]] = True
+    expect = x["bank"].copy()
+    expect[written] = bf16_of_f32(x["bank"][written])
+    for C in (4, 16):
+        got = oracle.backward_snapshot(*args(x), dO, chunk_size=C, snapshot="bf16")
+        np.testing.assert_array_equal(got["restored_bank"], expect)
+
+
+def test_backward_snapshot_bf16_is_the_reverse_mode_of_the_rounded_bank():
+    """When no chunk touches a row that an earlier chunk wrote, every chunk starts from the
+    rounded initial values of the rows it writes (and of later chunks' rows it reads), so
+    the bf16-snapshot backward equals the exact reverse mode run on the bank whose written
+    rows are rounded beforehand."""
+    P, T, C, S, D, W, R = 2, 24, 6, 40, 3, 2, 3
+    Nt = T // C
+    K = S // (Nt + 1)                      # chunk c writes slots [cK, (c+1)K); the top K stay unwritten
+    rng = np.random.default_rng(45)
+    ws = np.zeros((P, T, W), np.int32)
+    rs = np.zeros((P, T, R), np.int32)
+    for p in range(P):
+        for t in range(T):
+            c = t // C
+            ws[p, t] = c * K + rng.choice(K, W, replace=False)
+            rs[p, t] = rng.integers(c * K, S, R)          # its own range, later ones, unwritten
+    x = {"bank": rng.standard_normal((P * S, D)) * 0.5, "ws": ws,
+         "k": rng.uniform(0.1, 0.9, (P, T, W)), "g": -0.1 * rng.uniform(0, 1, (P, T, W)),
+         "beta": rng.uniform(0.2, 0.9, (P, T)), "v": rng.standard_normal((P, T, D)), "rs": rs,
+         "q": rng.uniform(0.1, 0.9, (P, T, R)), "valid": np.array([T, T - 5], np.int32)}
+    dO = rng.standard_normal((P, T, D))
+    written = np.zeros(P * S, bool)
+    for p in range(P):
+        for t in range(x["valid"][p]):
+            written[p * S + ws[p, t]] = True
+    y = dict(x)
+    y["bank"] = x["bank"].copy()
+    y["bank"][written] = bf16_of_f32(x["bank"][written])
+    ref = oracle.backward(*args(y), dO)
+    got = oracle.backward_snapshot(*args(x), dO, chunk_size=C, snapshot="bf16")
+    for key in GRAD_KEYS + ("restored_bank",):
+        np.testing.assert_array_equal(got[key], ref[key], err_msg=key)
+    # and the rounding changes the gradients (the snapshot is not silently exact)
+    exact = oracle.backward(*args(x), dO)
+    assert rel(got["grad_write_w"], exact["grad_write_w"]) > 1e-6

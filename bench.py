@@ -53,6 +53,8 @@ def parse_args():
                     help="run Phase 2 as three kernels per step instead of the fused kernel")
     ap.add_argument("--backward", action="store_true",
                     help="time the saving forward + backward (one step = both calls) instead")
+    ap.add_argument("--snapshot-quant", choices=["none", "bf16"], default="none",
+                    help="with --backward: store the snapshot of a float32 bank in bfloat16")
     ap.add_argument("--ncu-run", type=int, default=0, metavar="K",
                     help="profiling target: run K plain (eager) calls on the workload and exit, "
                          "printing no benchmark line")
@@ -474,7 +476,9 @@ def run_backward(args):
         d["grad_readings"] = torch.randn((wl.P, wl.T, wl.D), device=dev).to(dt)
     bank0 = d["bank"]
     bank = bank0.clone()
-    shape = sdm.make_shape(wl.P, wl.T, wl.C, wl.S, wl.D, wl.W, wl.R, dt)
+    sq = args.snapshot_quant
+    shape = sdm.make_shape(wl.P, wl.T, wl.C, wl.S, wl.D, wl.W, wl.R, dt,
+                           flags=sdm.SNAPSHOT_QUANT[sq])
     ws = sdm.alloc_workspace(shape, dev)
     nb = sdm.library().sdm_backward_workspace_bytes(__import__("ctypes").byref(shape))
     wsb = torch.empty(nb, dtype=torch.uint8, device=dev)
@@ -485,24 +489,35 @@ def run_backward(args):
     tokens = int(inputs["valid"].sum())
     args_in = (d["write_slots"], d["write_w"], d["log_decay"], d["beta"], d["v"],
                d["read_slots"], d["read_w"], d["valid"])
+    # the bank the backward leaves: the initial one, or with a bfloat16 snapshot of a float32
+    # bank, its written rows rounded to bfloat16
+    restored = bank0
+    if sq == "bf16" and dt == torch.float32:
+        rows = np.unique(np.concatenate([p * wl.S + inputs["write_slots"][p, :int(v)].ravel()
+                                         for p, v in enumerate(inputs["valid"])]))
+        idx = torch.from_numpy(rows.astype(np.int64)).to(dev)
+        restored = bank0.clone()
+        restored[idx] = bank0[idx].bfloat16().float()
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
         sdm.sdm_write_read_save(bank, *args_in, chunk_size=wl.C, workspace=ws, readings=readings,
-                                saved=saved, stream=stream)
+                                saved=saved, stream=stream, snapshot_quant=sq)
         gbank.zero_()
         sdm.sdm_write_read_backward(bank, *args_in, saved, d["grad_readings"], chunk_size=wl.C,
-                                    grad_bank=gbank, workspace=wsb, stream=stream)
+                                    grad_bank=gbank, workspace=wsb, stream=stream,
+                                    snapshot_quant=sq)
     stream.synchronize()
-    if not torch.equal(bank, bank0):
+    if not torch.equal(bank, restored):
         raise RuntimeError("backward did not restore the bank")
     def fwd():
         sdm.sdm_write_read_save(bank, *args_in, chunk_size=wl.C, workspace=ws, readings=readings,
-                                saved=saved, stream=stream)
+                                saved=saved, stream=stream, snapshot_quant=sq)
 
     def bwd():
         gbank.zero_()
         sdm.sdm_write_read_backward(bank, *args_in, saved, d["grad_readings"], chunk_size=wl.C,
-                                    grad_bank=gbank, workspace=wsb, stream=stream)
+                                    grad_bank=gbank, workspace=wsb, stream=stream,
+                                    snapshot_quant=sq)
 
     gf, gb = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
     with torch.cuda.graph(gf, stream=stream):
@@ -529,7 +544,7 @@ def run_backward(args):
             ev[k][2].record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
-    if not torch.equal(bank, bank0):
+    if not torch.equal(bank, restored):
         raise RuntimeError("backward did not restore the bank")
     fwd_ms = statistics.mean(a.elapsed_time(b) for a, b, _ in ev)
     bwd_ms = statistics.mean(b.elapsed_time(c) for _, b, c in ev)
@@ -540,7 +555,8 @@ def run_backward(args):
             "dtype": "f32", "storage_dtype": wl.dtype, "data": "synthetic",
             "config": workload_config(wl, inputs),
             "split_ms": {"saving_forward": fwd_ms, "backward": bwd_ms},
-            "saved_bytes": saved.numel(), "backward_workspace_bytes": nb, "clocks": clk,
+            "snapshot_quant": sq, "saved_bytes": saved.numel(),
+            "backward_workspace_bytes": nb, "clocks": clk,
             "gpu": torch.cuda.get_device_name(dev)}
     print(json.dumps(line), flush=True)
 

@@ -64,7 +64,7 @@ typedef enum { SDM_F32 = 0, SDM_BF16 = 1 } sdm_dtype;
  *   bank_dtype  SDM_F32 or SDM_BF16
  *   slab_steps  Phase-2 steps whose Phase-1 state is held at once; 0 = automatic. The
  *               results do not depend on it (Phase 1 and the solve are per chunk).
- *   flags       0, or SDM_FLAG_PER_STEP_KERNELS
+ *   flags       0, or SDM_FLAG_PER_STEP_KERNELS and/or SDM_FLAG_SNAPSHOT_BF16
  * P * ceil(T / C) * C must be below 2^31.
  *
  * Phase 2 runs as one persistent kernel per slab in which each CTA owns one stream and one
@@ -75,6 +75,15 @@ typedef enum { SDM_F32 = 0, SDM_BF16 = 1 } sdm_dtype;
  * streams), as the pages lay it out. Both are deterministic; their results differ only by
  * rounding. */
 #define SDM_FLAG_PER_STEP_KERNELS 1
+/* Snapshot of the saving forward in bfloat16 (memory_ops.py sdm_write_read: snapshot_quant
+ * "bf16"; phase2_kernels.py SNAPSHOT_QUANT_MODES). On a float32 bank the saving forward stores
+ * every snapshot row rounded to bfloat16 (to nearest even), which halves sdm_saved_bytes, and
+ * the backward restores each written row to that rounded value and computes the gradients
+ * from it: rows written by the call end at bf16(initial value) instead of their exact initial
+ * value. On a bfloat16 bank the snapshot is bfloat16 already and the flag changes nothing.
+ * sdm_write_read_save and sdm_write_read_backward must be given the same flag; the other
+ * entry points ignore it. */
+#define SDM_FLAG_SNAPSHOT_BF16 2
 typedef struct {
     int32_t P, T, C, S, D, W, R;
     int32_t bank_dtype;
@@ -127,7 +136,8 @@ int sdm_write_read(const sdm_shape *shape, void *bank, const int32_t *write_slot
 
 /* Bytes of the snapshot a saving forward keeps for the backward: the pre-write (chunk
  * start) row of every written slot of every chunk, Nt * P * C * W rows of D bank-dtype
- * elements (memory_ops.py: the snapshot of the saving forward, snapshot_quant "none"). */
+ * elements (memory_ops.py: the snapshot of the saving forward, snapshot_quant "none"), or of
+ * D bfloat16 elements with SDM_FLAG_SNAPSHOT_BF16 (snapshot_quant "bf16"). */
 size_t sdm_saved_bytes(const sdm_shape *shape);
 
 /* The saving forward (memory_ops.py SDMWriteRead.forward): sdm_write_read plus the snapshot.
@@ -147,7 +157,9 @@ size_t sdm_backward_workspace_bytes(const sdm_shape *shape);
  * through the solve and the Phase-1 backward), after sdm_write_read_save with the same shape
  * and inputs.
  *   bank           device [P*S, D]: in, the final bank the saving forward left; out, the
- *                  initial bank, restored exactly from the snapshot
+ *                  initial bank, restored exactly from the snapshot (with
+ *                  SDM_FLAG_SNAPSHOT_BF16 on a float32 bank: every row a valid token writes
+ *                  holds bf16(its initial value), the others their exact initial value)
  *   inputs         the forward's inputs, unchanged
  *   saved          the snapshot written by sdm_write_read_save
  *   grad_readings  device [P, T, D] bank dtype: dL/d(readings) (padding rows are ignored)

@@ -19,7 +19,7 @@ from typing import Dict, Optional
 
 import torch
 
-__all__ = ["sdm_write_read", "sdm_write_read_save", "sdm_write_read_backward",
+__all__ = ["FLAG_SNAPSHOT_BF16", "sdm_write_read", "sdm_write_read_save", "sdm_write_read_backward",
            "sdm_write_read_noalloc", "profile_write_read", "workspace_bytes", "launch_count",
            "phase1_debug", "KERNEL_KINDS",
            "device_status", "SdmError", "Shape", "library", "library_path", "version"]
@@ -30,6 +30,8 @@ library_path = os.path.join(_HERE, "libsdm.so")
 SDM_F32, SDM_BF16 = 0, 1
 KERNEL_KINDS = ("phase1", "solve", "gather", "dualmm", "dw", "phase2")
 FLAG_PER_STEP_KERNELS = 1
+FLAG_SNAPSHOT_BF16 = 2
+SNAPSHOT_QUANT = {"none": 0, "bf16": FLAG_SNAPSHOT_BF16}
 _STATUS = {0: "SDM_OK", -1: "SDM_ERR_INVALID", -2: "SDM_ERR_UNSUPPORTED", -3: "SDM_ERR_CUDA",
            -4: "SDM_ERR_TIMEOUT", -5: "SDM_ERR_WORKSPACE", -6: "SDM_ERR_DEVICE"}
 
@@ -280,11 +282,22 @@ def saved_bytes(shape: Shape) -> int:
     return int(n)
 
 
+def _snapshot_flag(snapshot_quant: str) -> int:
+    if snapshot_quant not in SNAPSHOT_QUANT:
+        raise ValueError(f"snapshot_quant must be one of {tuple(SNAPSHOT_QUANT)}, "
+                         f"got {snapshot_quant!r}")
+    return SNAPSHOT_QUANT[snapshot_quant]
+
+
 def sdm_write_read_save(bank, write_slots, write_w, log_decay, beta, v, read_slots, read_w,
                         valid_tokens=None, *, chunk_size: int, slab_steps: int = 0,
-                        workspace=None, readings=None, saved=None, stream=None, flags: int = 0):
+                        workspace=None, readings=None, saved=None, stream=None, flags: int = 0,
+                        snapshot_quant: str = "none"):
     """The saving forward: sdm_write_read plus the snapshot the backward needs.
+    ``snapshot_quant`` "bf16" stores the snapshot of a float32 bank in bfloat16 (half the
+    bytes; the backward then restores the written rows to their rounded values).
     Returns (readings, saved)."""
+    flags |= _snapshot_flag(snapshot_quant)
     shape, (P, T, S, D, W, R) = _shape_of(bank, write_slots, read_slots, chunk_size,
                                           slab_steps, flags)
     dev, dt = bank.device, bank.dtype
@@ -311,13 +324,16 @@ def sdm_write_read_save(bank, write_slots, write_w, log_decay, beta, v, read_slo
 
 def sdm_write_read_backward(bank, write_slots, write_w, log_decay, beta, v, read_slots, read_w,
                             valid_tokens, saved, grad_readings, *, chunk_size: int,
-                            grad_bank=None, slab_steps: int = 0, workspace=None, stream=None):
-    """The backward after sdm_write_read_save: restores ``bank`` to its initial state and
-    returns a dict of float32 gradients (grad_bank, grad_v, grad_beta, grad_write_w,
-    grad_log_decay, grad_read_w). ``grad_bank`` (optional, [P*S, D] float32) is the loss
-    gradient with respect to the final bank; it is updated in place to the gradient with
-    respect to the initial bank."""
-    shape, (P, T, S, D, W, R) = _shape_of(bank, write_slots, read_slots, chunk_size, slab_steps)
+                            grad_bank=None, slab_steps: int = 0, workspace=None, stream=None,
+                            snapshot_quant: str = "none"):
+    """The backward after sdm_write_read_save (with the same ``snapshot_quant``): restores
+    ``bank`` to its initial state (with "bf16", the rows the call wrote to their bfloat16
+    rounding) and returns a dict of float32 gradients (grad_bank, grad_v, grad_beta,
+    grad_write_w, grad_log_decay, grad_read_w). ``grad_bank`` (optional, [P*S, D] float32) is
+    the loss gradient with respect to the final bank; it is updated in place to the gradient
+    with respect to the initial bank."""
+    shape, (P, T, S, D, W, R) = _shape_of(bank, write_slots, read_slots, chunk_size, slab_steps,
+                                          _snapshot_flag(snapshot_quant))
     dev, dt = bank.device, bank.dtype
     _need(grad_readings, "grad_readings", (P, T, D), dt, dev)
     f32 = dict(dtype=torch.float32, device=dev)

@@ -64,7 +64,7 @@ int check_shape(const sdm_shape *s, Dims &d) {
         return fail(SDM_ERR_INVALID, "bank_dtype must be SDM_F32 (0) or SDM_BF16 (1), got %d",
                     s->bank_dtype);
     if (s->slab_steps < 0) return fail(SDM_ERR_INVALID, "slab_steps must be >= 0");
-    if (s->flags & ~SDM_FLAG_PER_STEP_KERNELS)
+    if (s->flags & ~(SDM_FLAG_PER_STEP_KERNELS | SDM_FLAG_SNAPSHOT_BF16))
         return fail(SDM_ERR_INVALID, "unknown flags 0x%x", (unsigned)s->flags);
     if (s->D != 32 && s->D != 64 && s->D != 128 && s->D != 256 && s->D != 512)
         return fail(SDM_ERR_UNSUPPORTED, "head_dim D=%d has no kernel (32, 64, 128, 256, 512)",
@@ -79,6 +79,7 @@ int check_shape(const sdm_shape *s, Dims &d) {
     d.bwd = 0;
     d.xp = d.C;
     d.per_step = ((s->flags & SDM_FLAG_PER_STEP_KERNELS) || !phase2_fused_fits(d)) ? 1 : 0;
+    d.snapq = ((s->flags & SDM_FLAG_SNAPSHOT_BF16) && d.dtype == SDM_F32) ? 1 : 0;
     return SDM_OK;
 }
 
@@ -404,7 +405,7 @@ size_t sdm_saved_bytes(const sdm_shape *shape) {
     Dims d;
     if (check_shape(shape, d)) return 0;
     g_err[0] = 0;
-    const size_t es = d.dtype == SDM_BF16 ? 2 : 4;
+    const size_t es = (d.dtype == SDM_BF16 || d.snapq) ? 2 : 4;
     return (size_t)d.Nt * d.P * d.C * d.W * d.D * es;
 }
 

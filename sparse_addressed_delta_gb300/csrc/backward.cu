@@ -38,7 +38,8 @@ __device__ __forceinline__ int local_n(const Dims &d, int step0, int ti, int p) 
 }
 
 // ---------------------------------------------------------------------------------------
-// restore: B0 rows of the written slots from the snapshot (one warp per group)
+// restore: B0 rows of the written slots from the snapshot (one warp per group); a bfloat16
+// snapshot of a float32 bank puts back the rounded rows
 // ---------------------------------------------------------------------------------------
 template <typename BT, int CPL>
 __global__ void __launch_bounds__(NTB) k_b_restore(Dims d, Inputs in, Work w, int step0, int ti) {
@@ -49,12 +50,17 @@ __global__ void __launch_bounds__(NTB) k_b_restore(Dims d, Inputs in, Work w, in
     const int32_t *goff = w.goff + (size_t)n * goff_stride(CW);
     const int32_t *gslot = w.gslot + (size_t)n * CW;
     BT *bank = static_cast<BT *>(in.bank) + (size_t)p * d.S * D + lane * CPL;
-    const BT *snap = static_cast<const BT *>(in.snap) + (size_t)(ti * d.P + p) * CW * D + lane * CPL;
+    // the snapshot is in the bank dtype, or (d.snapq, float32 banks) in bfloat16
+    const size_t s0 = (size_t)(ti * d.P + p) * CW * D + lane * CPL;
+    const BT *snap = static_cast<const BT *>(in.snap) + s0;
+    const __nv_bfloat16 *snaph = static_cast<const __nv_bfloat16 *>(in.snap) + s0;
     for (int g = blockIdx.x * NWB + warp; g < ng; g += gridDim.x * NWB) {
         const int sl = gslot[g];
         if ((unsigned)sl >= (unsigned)d.S) continue;
         float x[CPL];
-        load_vec<BT, CPL, false>(snap + (size_t)(goff[g + 1] - 1) * D, x);
+        const size_t ro = (size_t)(goff[g + 1] - 1) * D;
+        if (d.snapq) load_vec<__nv_bfloat16, CPL, false>(snaph + ro, x);
+        else load_vec<BT, CPL, false>(snap + ro, x);
         store_vec<BT, CPL>(bank + (size_t)sl * D, x);
     }
 }

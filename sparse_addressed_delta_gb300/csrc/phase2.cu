@@ -360,10 +360,13 @@ __global__ void __launch_bounds__(kBlock, 2) k_dw(Dims d, Inputs in, Work w, int
             const float f = __shfl_sync(0xffffffffu, mf, k);
             const float w1 = __shfl_sync(0xffffffffu, mw, k);
             if (sl[k] < 0) continue;                                // warp-uniform
-            if (in.snap)
-                store_vec<BT, CPL>(static_cast<BT *>(in.snap) +
-                                       ((size_t)(ti * d.P + p) * CW + (o1 - 1)) * D + lane * CPL,
-                                   acc[k]);
+            if (in.snap) {
+                const size_t so = ((size_t)(ti * d.P + p) * CW + (o1 - 1)) * D + lane * CPL;
+                if (d.snapq)   // float32 bank, bfloat16 snapshot
+                    store_vec<__nv_bfloat16, CPL>(static_cast<__nv_bfloat16 *>(in.snap) + so, acc[k]);
+                else
+                    store_vec<BT, CPL>(static_cast<BT *>(in.snap) + so, acc[k]);
+            }
 #pragma unroll
             for (int c = 0; c < CPL; ++c) acc[k][c] = fmaf(w1, x[k][c], acc[k][c] * f);
             for (int m = o0 + 1; m < o1; m += 32) {

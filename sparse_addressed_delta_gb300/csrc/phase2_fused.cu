@@ -532,9 +532,13 @@ __global__ void __launch_bounds__(NP2) k_phase2_pipe(Dims d, Inputs in, Work w, 
                     const uint4 packed = pack_piece<BT>(o);
                     *reinterpret_cast<uint4 *>(bank + (size_t)sl * D) = packed;
                     dwout[g] = packed;
-                    if (in.snap)
-                        *reinterpret_cast<uint4 *>(static_cast<BT *>(in.snap) +
-                                                   ((size_t)(ti * d.P + p) * CW + (o1 - 1)) * D + c0) = braw;
+                    if (in.snap) {
+                        const size_t so = ((size_t)(ti * d.P + p) * CW + (o1 - 1)) * D + c0;
+                        if (d.snapq)   // float32 bank, bfloat16 snapshot: 4 columns, 8 bytes
+                            store_vec<__nv_bfloat16, V>(static_cast<__nv_bfloat16 *>(in.snap) + so, b0);
+                        else
+                            *reinterpret_cast<uint4 *>(static_cast<BT *>(in.snap) + so) = braw;
+                    }
                 }
             };
             auto add_member = [&](int m, float (&acc)[V]) {
@@ -567,8 +571,13 @@ __global__ void __launch_bounds__(NP2) k_phase2_pipe(Dims d, Inputs in, Work w, 
                     if ((unsigned)sl < S) {
                         bank[(size_t)sl * D + c] = o;
                         reinterpret_cast<BT *>(dwout + g)[c] = o;
-                        if (in.snap)
-                            static_cast<BT *>(in.snap)[((size_t)(ti * d.P + p) * CW + (o1 - 1)) * D + c0 + c] = b0;
+                        if (in.snap) {
+                            const size_t so = ((size_t)(ti * d.P + p) * CW + (o1 - 1)) * D + c0 + c;
+                            if (d.snapq)
+                                static_cast<__nv_bfloat16 *>(in.snap)[so] = __float2bfloat16_rn(to_f32(b0));
+                            else
+                                static_cast<BT *>(in.snap)[so] = b0;
+                        }
                     }
                 });
             }

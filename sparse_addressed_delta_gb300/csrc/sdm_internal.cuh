@@ -39,6 +39,7 @@ struct Dims {
     int bwd;        // 1: Phase 1 also keeps what the backward reads (sorted rows, read plan)
     int xp;         // row pitch (floats) of X and QX in the workspace: C + 4 for the pipelined
                     // Phase 2 (one bulk copy lands rows at a bank-conflict-free pitch), else C
+    int snapq;      // 1: the snapshot of a float32 bank is stored in bfloat16
 };
 
 inline int x_row_pitch(const Dims &d) { return (d.per_step || d.bwd) ? d.C : d.C + 4; }

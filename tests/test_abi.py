@@ -98,3 +98,16 @@ def test_host_workspace_holds_the_inputs():
     bad = sdm.make_shape(8, 4096, 64, 65536, 100, 16, 16, sdm.SDM_BF16)
     with pytest.raises(sdm.SdmError):
         sdm.host_workspace_bytes(bad)
+
+
+def test_bf16_snapshot_halves_saved_bytes():
+    """SDM_FLAG_SNAPSHOT_BF16 stores a float32 bank's snapshot in bfloat16: half the bytes;
+    a bfloat16 bank's snapshot is bfloat16 already. Unknown flag bits are refused."""
+    for dt, ratio in ((sdm.SDM_F32, 2), (sdm.SDM_BF16, 1)):
+        plain = sdm.saved_bytes(sdm.make_shape(3, 100, 16, 50, 64, 3, 4, dt))
+        half = sdm.saved_bytes(sdm.make_shape(3, 100, 16, 50, 64, 3, 4, dt,
+                                              flags=sdm.FLAG_SNAPSHOT_BF16))
+        assert plain == 7 * 3 * 16 * 3 * 64 * (4 if dt == sdm.SDM_F32 else 2)
+        assert plain == ratio * half
+    with pytest.raises(sdm.SdmError):
+        sdm.saved_bytes(sdm.make_shape(3, 100, 16, 50, 64, 3, 4, sdm.SDM_F32, flags=8))

@@ -64,7 +64,8 @@ typedef enum { SDM_F32 = 0, SDM_BF16 = 1 } sdm_dtype;
  *   bank_dtype  SDM_F32 or SDM_BF16
  *   slab_steps  Phase-2 steps whose Phase-1 state is held at once; 0 = automatic. The
  *               results do not depend on it (Phase 1 and the solve are per chunk).
- *   flags       0, or SDM_FLAG_PER_STEP_KERNELS and/or SDM_FLAG_SNAPSHOT_BF16
+ *   flags       0, or any of SDM_FLAG_PER_STEP_KERNELS, SDM_FLAG_SNAPSHOT_BF16,
+ *               SDM_FLAG_TOKEN_GATE
  * P * ceil(T / C) * C must be below 2^31.
  *
  * Phase 2 runs as one persistent kernel per slab in which each CTA owns one stream and one
@@ -84,6 +85,11 @@ typedef enum { SDM_F32 = 0, SDM_BF16 = 1 } sdm_dtype;
  * sdm_write_read_save and sdm_write_read_backward must be given the same flag; the other
  * entry points ignore it. */
 #define SDM_FLAG_SNAPSHOT_BF16 2
+/* One log-decay per token (memory_ops.py sdm_write_read: "g: [..., 1] per-token log-decay,
+ * or [..., W] one per write"; key_weighted_decay False). log_decay is then [P, T] float32 and
+ * applies to every row the token writes; the backward's grad_log_decay is [P, T], the sum of
+ * the per-write gradients in write order. Every entry point takes it. */
+#define SDM_FLAG_TOKEN_GATE 4
 typedef struct {
     int32_t P, T, C, S, D, W, R;
     int32_t bank_dtype;
@@ -109,7 +115,8 @@ size_t sdm_workspace_bytes(const sdm_shape *shape);
  *   bank          device, [P*S, D] bank dtype; read and advanced in place to its final state
  *   write_slots   device, [P, T, W] int32, per-stream slot ids in [0, S), distinct per token
  *   write_w       device, [P, T, W] bank dtype, write weights k
- *   log_decay     device, [P, T, W] float32, g (one log-decay per write entry)
+ *   log_decay     device, [P, T, W] float32, g (one log-decay per write entry); [P, T]
+ *                 with SDM_FLAG_TOKEN_GATE (one per token)
  *   beta          device, [P, T]    float32, write strength
  *   v             device, [P, T, D] bank dtype, values
  *   read_slots    device, [P, T, R] int32, slot ids in [0, S)
@@ -168,7 +175,7 @@ size_t sdm_backward_workspace_bytes(const sdm_shape *shape);
  *   grad_v         device [P, T, D] float32, out
  *   grad_beta      device [P, T] float32, out
  *   grad_write_w   device [P, T, W] float32, out   (dL/dk)
- *   grad_log_decay device [P, T, W] float32, out   (dL/dg)
+ *   grad_log_decay device [P, T, W] float32, out   (dL/dg; [P, T] with SDM_FLAG_TOKEN_GATE)
  *   grad_read_w    device [P, T, R] float32, out   (dL/dq)
  * Gradients of padding tokens are zero. Asynchronous; deterministic. */
 int sdm_write_read_backward(const sdm_shape *shape, void *bank, const int32_t *write_slots,

@@ -19,7 +19,7 @@ from typing import Dict, Optional
 
 import torch
 
-__all__ = ["FLAG_SNAPSHOT_BF16", "sdm_write_read", "sdm_write_read_save", "sdm_write_read_backward",
+__all__ = ["FLAG_SNAPSHOT_BF16", "FLAG_TOKEN_GATE", "sdm_write_read", "sdm_write_read_save", "sdm_write_read_backward",
            "sdm_write_read_noalloc", "profile_write_read", "workspace_bytes", "launch_count",
            "phase1_debug", "KERNEL_KINDS",
            "device_status", "SdmError", "Shape", "library", "library_path", "version"]
@@ -31,6 +31,7 @@ SDM_F32, SDM_BF16 = 0, 1
 KERNEL_KINDS = ("phase1", "solve", "gather", "dualmm", "dw", "phase2")
 FLAG_PER_STEP_KERNELS = 1
 FLAG_SNAPSHOT_BF16 = 2
+FLAG_TOKEN_GATE = 4
 SNAPSHOT_QUANT = {"none": 0, "bf16": FLAG_SNAPSHOT_BF16}
 _STATUS = {0: "SDM_OK", -1: "SDM_ERR_INVALID", -2: "SDM_ERR_UNSUPPORTED", -3: "SDM_ERR_CUDA",
            -4: "SDM_ERR_TIMEOUT", -5: "SDM_ERR_WORKSPACE", -6: "SDM_ERR_DEVICE"}
@@ -144,6 +145,15 @@ def _ptr(t: Optional[torch.Tensor]):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+def _gate(log_decay: torch.Tensor, P: int, T: int, W: int):
+    """(flag, shape) of the log-decays: one per write entry, [P, T, W]; or one per token,
+    [P, T] (or [P, T, 1] with W > 1), which sets FLAG_TOKEN_GATE."""
+    shp = tuple(log_decay.shape)
+    if shp == (P, T) or (W > 1 and shp == (P, T, 1)):
+        return FLAG_TOKEN_GATE, shp
+    return 0, (P, T, W)
+
+
 def _need(t: torch.Tensor, name: str, shape, dtype, device) -> None:
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a tensor")
@@ -194,7 +204,9 @@ def sdm_write_read(bank: torch.Tensor, write_slots: torch.Tensor, write_w: torch
     _need(bank, "bank", (P * S, D), dt, dev)
     _need(write_slots, "write_slots", (P, T, W), torch.int32, dev)
     _need(write_w, "write_w", (P, T, W), dt, dev)
-    _need(log_decay, "log_decay", (P, T, W), torch.float32, dev)
+    gflag, gshape = _gate(log_decay, P, T, W)
+    flags |= gflag
+    _need(log_decay, "log_decay", gshape, torch.float32, dev)
     _need(beta, "beta", (P, T), torch.float32, dev)
     _need(v, "v", (P, T, D), dt, dev)
     _need(read_slots, "read_slots", (P, T, R), torch.int32, dev)
@@ -245,7 +257,9 @@ def sdm_write_read_host(bank: torch.Tensor, write_slots: torch.Tensor, write_w: 
     _need(bank, "bank", (P * S, D), dt, dev)
     _need(write_slots, "write_slots", (P, T, W), torch.int32, cpu)
     _need(write_w, "write_w", (P, T, W), dt, cpu)
-    _need(log_decay, "log_decay", (P, T, W), torch.float32, cpu)
+    gflag, gshape = _gate(log_decay, P, T, W)
+    flags |= gflag
+    _need(log_decay, "log_decay", gshape, torch.float32, cpu)
     _need(beta, "beta", (P, T), torch.float32, cpu)
     _need(v, "v", (P, T, D), dt, cpu)
     _need(read_slots, "read_slots", (P, T, R), torch.int32, cpu)
@@ -298,11 +312,13 @@ def sdm_write_read_save(bank, write_slots, write_w, log_decay, beta, v, read_slo
     bytes; the backward then restores the written rows to their rounded values).
     Returns (readings, saved)."""
     flags |= _snapshot_flag(snapshot_quant)
+    P, T, W = write_slots.shape
+    gflag, gshape = _gate(log_decay, P, T, W)
     shape, (P, T, S, D, W, R) = _shape_of(bank, write_slots, read_slots, chunk_size,
-                                          slab_steps, flags)
+                                          slab_steps, flags | gflag)
     dev, dt = bank.device, bank.dtype
     for t, name, shp, typ in ((bank, "bank", (P * S, D), dt), (write_slots, "write_slots", (P, T, W), torch.int32),
-                              (write_w, "write_w", (P, T, W), dt), (log_decay, "log_decay", (P, T, W), torch.float32),
+                              (write_w, "write_w", (P, T, W), dt), (log_decay, "log_decay", gshape, torch.float32),
                               (beta, "beta", (P, T), torch.float32), (v, "v", (P, T, D), dt),
                               (read_slots, "read_slots", (P, T, R), torch.int32), (read_w, "read_w", (P, T, R), dt)):
         _need(t, name, shp, typ, dev)
@@ -332,8 +348,10 @@ def sdm_write_read_backward(bank, write_slots, write_w, log_decay, beta, v, read
     grad_write_w, grad_log_decay, grad_read_w). ``grad_bank`` (optional, [P*S, D] float32) is
     the loss gradient with respect to the final bank; it is updated in place to the gradient
     with respect to the initial bank."""
+    P, T, W = write_slots.shape
+    gflag, gshape = _gate(log_decay, P, T, W)
     shape, (P, T, S, D, W, R) = _shape_of(bank, write_slots, read_slots, chunk_size, slab_steps,
-                                          _snapshot_flag(snapshot_quant))
+                                          _snapshot_flag(snapshot_quant) | gflag)
     dev, dt = bank.device, bank.dtype
     _need(grad_readings, "grad_readings", (P, T, D), dt, dev)
     f32 = dict(dtype=torch.float32, device=dev)
@@ -342,7 +360,7 @@ def sdm_write_read_backward(bank, write_slots, write_w, log_decay, beta, v, read
     _need(grad_bank, "grad_bank", (P * S, D), torch.float32, dev)
     out = {"grad_bank": grad_bank, "grad_v": torch.empty((P, T, D), **f32),
            "grad_beta": torch.empty((P, T), **f32), "grad_write_w": torch.empty((P, T, W), **f32),
-           "grad_log_decay": torch.empty((P, T, W), **f32),
+           "grad_log_decay": torch.empty(gshape, **f32),
            "grad_read_w": torch.empty((P, T, R), **f32)}
     if workspace is None:
         n = library().sdm_backward_workspace_bytes(ctypes.byref(shape))
@@ -375,8 +393,10 @@ def sdm_write_read_noalloc(bank: torch.Tensor, write_slots: torch.Tensor,
     R = read_slots.shape[-1]
     S, D = bank.shape[0] // P, bank.shape[1]
     dev, dt = bank.device, bank.dtype
+    gflag, gshape = _gate(log_decay, P, T, W)
+    flags |= gflag
     for t, name, shp, typ in ((bank, "bank", (P * S, D), dt), (write_slots, "write_slots", (P, T, W), torch.int32),
-                              (write_w, "write_w", (P, T, W), dt), (log_decay, "log_decay", (P, T, W), torch.float32),
+                              (write_w, "write_w", (P, T, W), dt), (log_decay, "log_decay", gshape, torch.float32),
                               (beta, "beta", (P, T), torch.float32), (v, "v", (P, T, D), dt),
                               (read_slots, "read_slots", (P, T, R), torch.int32), (read_w, "read_w", (P, T, R), dt),
                               (readings, "readings", (P, T, D), dt)):
@@ -402,7 +422,8 @@ def profile_write_read(bank, write_slots, write_w, log_decay, beta, v, read_slot
     R = read_slots.shape[-1]
     S, D = bank.shape[0] // P, bank.shape[1]
     dev, dt = bank.device, bank.dtype
-    shape = make_shape(P, T, chunk_size, S, D, W, R, dt, slab_steps, flags)
+    shape = make_shape(P, T, chunk_size, S, D, W, R, dt, slab_steps,
+                       flags | _gate(log_decay, P, T, W)[0])
     if readings is None:
         readings = torch.empty((P, T, D), dtype=dt, device=dev)
     if workspace is None:
@@ -430,7 +451,7 @@ def phase1_debug(write_slots, write_w, log_decay, beta, read_slots, read_w, vali
     R = read_slots.shape[-1]
     dev, dt = write_w.device, write_w.dtype
     C = chunk_size
-    shape = make_shape(P, T, C, S, D, W, R, dt, slab_steps)
+    shape = make_shape(P, T, C, S, D, W, R, dt, slab_steps, _gate(log_decay, P, T, W)[0])
     N = P * (-(-T // C))
     f32 = dict(dtype=torch.float32, device=dev)
     out = {

@@ -64,7 +64,7 @@ int check_shape(const sdm_shape *s, Dims &d) {
         return fail(SDM_ERR_INVALID, "bank_dtype must be SDM_F32 (0) or SDM_BF16 (1), got %d",
                     s->bank_dtype);
     if (s->slab_steps < 0) return fail(SDM_ERR_INVALID, "slab_steps must be >= 0");
-    if (s->flags & ~(SDM_FLAG_PER_STEP_KERNELS | SDM_FLAG_SNAPSHOT_BF16))
+    if (s->flags & ~(SDM_FLAG_PER_STEP_KERNELS | SDM_FLAG_SNAPSHOT_BF16 | SDM_FLAG_TOKEN_GATE))
         return fail(SDM_ERR_INVALID, "unknown flags 0x%x", (unsigned)s->flags);
     if (s->D != 32 && s->D != 64 && s->D != 128 && s->D != 256 && s->D != 512)
         return fail(SDM_ERR_UNSUPPORTED, "head_dim D=%d has no kernel (32, 64, 128, 256, 512)",
@@ -80,6 +80,7 @@ int check_shape(const sdm_shape *s, Dims &d) {
     d.xp = d.C;
     d.per_step = ((s->flags & SDM_FLAG_PER_STEP_KERNELS) || !phase2_fused_fits(d)) ? 1 : 0;
     d.snapq = ((s->flags & SDM_FLAG_SNAPSHOT_BF16) && d.dtype == SDM_F32) ? 1 : 0;
+    d.gate = (s->flags & SDM_FLAG_TOKEN_GATE) ? 1 : 0;
     return SDM_OK;
 }
 
@@ -167,6 +168,7 @@ int phase1_ctas(const Dims &d, int ns) {
     F(bdfac, float, B * P * CW)                                               \
     F(bdlam, float, B * P * CW)                                               \
     F(bdlr, float, B * P * CR)                                                \
+    F(bdgate, float, B * GT * P * CW)                                         \
     F(ret, float, P * CD)                                                     \
     F(inter, float, P * CD)                                                   \
     F(dv, float, P * CD)
@@ -174,7 +176,8 @@ int phase1_ctas(const Dims &d, int ns) {
 size_t layout_bytes(const Dims &d, int ns, int G_) {
     const size_t N = (size_t)ns * d.P, P = d.P, CW = (size_t)d.C * d.W, CR = (size_t)d.C * d.R,
                  CC = (size_t)d.C * d.C, CD = (size_t)d.C * d.D, G = G_, B = d.bwd ? 1 : 0,
-                 C = d.C, DT = ((size_t)d.D + 31) / 32, CX = (size_t)d.C * d.xp;
+                 C = d.C, DT = ((size_t)d.D + 31) / 32, CX = (size_t)d.C * d.xp,
+                 GT = d.gate ? 1 : 0;
     size_t off = 0;
 #define X_SIZE(name, type, count) off += up(sizeof(type) * (size_t)(count));
     SDM_LAYOUT(X_SIZE)
@@ -185,7 +188,8 @@ size_t layout_bytes(const Dims &d, int ns, int G_) {
 Work layout_assign(const Dims &d, int ns, int G_, void *base) {
     const size_t N = (size_t)ns * d.P, P = d.P, CW = (size_t)d.C * d.W, CR = (size_t)d.C * d.R,
                  CC = (size_t)d.C * d.C, CD = (size_t)d.C * d.D, G = G_, B = d.bwd ? 1 : 0,
-                 C = d.C, DT = ((size_t)d.D + 31) / 32, CX = (size_t)d.C * d.xp;
+                 C = d.C, DT = ((size_t)d.D + 31) / 32, CX = (size_t)d.C * d.xp,
+                 GT = d.gate ? 1 : 0;
     Work w;
     memset(&w, 0, sizeof(w));
     char *p = static_cast<char *>(base);
@@ -298,7 +302,7 @@ HostStage host_stage(const Dims &d, size_t base) {
     size_t o = up(base);
     h.ws = o; o = up(o + 4 * PT * d.W);
     h.kw = o; o = up(o + es * PT * d.W);
-    h.g = o; o = up(o + 4 * PT * d.W);
+    h.g = o; o = up(o + 4 * PT * (d.gate ? 1 : d.W));
     h.beta = o; o = up(o + 4 * PT);
     h.v = o; o = up(o + es * PT * d.D);
     h.rs = o; o = up(o + 4 * PT * d.R);
@@ -605,7 +609,7 @@ int sdm_write_read_host(const sdm_shape *shape, void *bank, const int32_t *write
     // so that the two copies do not share the link; v has Phase 1 and the solve to land)
     struct { size_t off; const void *src; size_t bytes; } cp[] = {
         {hs.ws, write_slots, 4 * PT * d.W}, {hs.kw, write_w, es * PT * d.W},
-        {hs.g, log_decay, 4 * PT * d.W},    {hs.beta, beta, 4 * PT},
+        {hs.g, log_decay, 4 * PT * (d.gate ? 1 : d.W)}, {hs.beta, beta, 4 * PT},
         {hs.rs, read_slots, 4 * PT * d.R},  {hs.qw, read_w, es * PT * d.R},
         {hs.valid, valid_tokens, 4 * (size_t)d.P}};
     // all of them mapped page-locked memory (16-byte aligned, whole 16-byte units): one copy

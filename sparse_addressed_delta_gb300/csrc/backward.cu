@@ -674,13 +674,31 @@ __global__ void __launch_bounds__(NTB) k_b_phase1(Dims d, Inputs in, Work w, flo
         for (int m = ge - 1; m >= pa; --m) {
             const unsigned lb = (unsigned)wkey[m];
             run += dlam[m];
-            gg[(tok0 + (lb >> 8)) * W + (lb & 255u)] = s < S ? run : 0.f;
+            const size_t ge_out = (size_t)(lb >> 8) * W + (lb & 255u);
+            if (d.gate) w.bdgate[(size_t)p * CW + ge_out] = s < S ? run : 0.f;
+            else gg[tok0 * W + ge_out] = s < S ? run : 0.f;
         }
     }
     if (blockIdx.x == 0) {
         const int tmax = (size_t)ti * C + C <= (size_t)d.T ? C : d.T - ti * C;
-        for (int i = nw + threadIdx.x; i < tmax * W; i += NTB) gg[tok0 * W + i] = 0.f;
+        for (int i = nw + threadIdx.x; i < tmax * W; i += NTB) {
+            if (d.gate) w.bdgate[(size_t)p * CW + i] = 0.f;
+            else gg[tok0 * W + i] = 0.f;
+        }
     }
+}
+
+// per-token gate: the token's log-decay gradient is the sum of its W per-entry gradients, in
+// entry order (one thread per token of the step's chunk)
+__global__ void __launch_bounds__(NTB) k_b_gate(Dims d, Work w, float *gg, int ti) {
+    const int p = blockIdx.y, CW = d.C * d.W;
+    const int t = blockIdx.x * NTB + threadIdx.x;
+    const int tmax = (size_t)ti * d.C + d.C <= (size_t)d.T ? d.C : d.T - ti * d.C;
+    if (t >= tmax) return;
+    const float *e = w.bdgate + (size_t)p * CW + (size_t)t * d.W;
+    float sum = 0.f;
+    for (int j = 0; j < d.W; ++j) sum += e[j];
+    gg[(size_t)p * d.T + (size_t)ti * d.C + t] = sum;
 }
 
 template <typename T>
@@ -742,6 +760,7 @@ cudaError_t backward_step(const Dims &d, const Inputs &in, const Work &w, const 
     for (int stage = 0; stage < 3; ++stage)
         k_b_phase1<BT><<<dim3(gb, P), NTB, found_bytes, st>>>(
             d, in, w, o.grad_write_w, o.grad_log_decay, o.grad_read_w, step0, ti, stage);
+    if (d.gate) k_b_gate<<<dim3((C + NTB - 1) / NTB, P), NTB, 0, st>>>(d, w, o.grad_log_decay, ti);
     return cudaGetLastError();
 }
 

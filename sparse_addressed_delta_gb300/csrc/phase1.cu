@@ -414,7 +414,7 @@ __global__ void __launch_bounds__(NT, 2) k_phase1(Dims d, Inputs in, Work w, int
         const size_t tok_base = (size_t)p * d.T + tok0;
         const int32_t *ws = in.ws + tok_base * W;
         const int32_t *rs = in.rs + tok_base * R;
-        const float *g = in.g + tok_base * W;
+        const float *g = in.g + tok_base * (d.gate ? 1 : W);   // per entry, or per token
         const WT *k = kw + tok_base * W;
         const WT *q = qwin + tok_base * R;
 
@@ -447,7 +447,8 @@ __global__ void __launch_bounds__(NT, 2) k_phase1(Dims d, Inputs in, Work w, int
                 bad = 1;
             }
             kf[i] = kk;
-            pgs[i] = __float_as_int(s == S ? 0.f : g[i]);   // g (0 if dropped), read in step 2
+            // g (0 if dropped), read in step 2
+            pgs[i] = __float_as_int(s == S ? 0.f : g[d.gate ? div_by(i, magW) : i]);
             wsl[i] = s < S ? s : kNoEntry;
             const int t = div_by(i, magW);
             keyA[i] = ((unsigned long long)(unsigned)s << 32) | ((unsigned)t << 8) |

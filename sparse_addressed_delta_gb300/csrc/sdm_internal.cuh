@@ -40,6 +40,7 @@ struct Dims {
     int xp;         // row pitch (floats) of X and QX in the workspace: C + 4 for the pipelined
                     // Phase 2 (one bulk copy lands rows at a bank-conflict-free pitch), else C
     int snapq;      // 1: the snapshot of a float32 bank is stored in bfloat16
+    int gate;       // 1: one log-decay per token ([P, T]) instead of one per write entry
 };
 
 inline int x_row_pitch(const Dims &d) { return (d.per_step || d.bwd) ? d.C : d.C + 4; }
@@ -112,6 +113,8 @@ struct Work {
     float *bdfac;       // [P][CW]   <dB1[s], B0[s]> at each group's head position
     float *bdlam;       // [P][CW]   d(log-decay running sum) at each sorted write position
     float *bdlr;        // [P][CR]   d(read running log-decay) at each sorted read position
+    float *bdgate;      // [P][CW]   per-entry log-decay gradients of a per-token gate, summed
+                        //           per token at the end of the step
     // Phase-2 step buffers
     float *ret;         // [P][C*D]
     float *inter;       // [P][C*D]

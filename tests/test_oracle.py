@@ -362,3 +362,30 @@ def test_backward_snapshot_bf16_is_the_reverse_mode_of_the_rounded_bank():
     # and the rounding changes the gradients (the snapshot is not silently exact)
     exact = oracle.backward(*args(x), dO)
     assert rel(got["grad_write_w"], exact["grad_write_w"]) > 1e-6
+
+
+def test_per_token_gate_gradient_is_the_sum_over_writes():
+    """One log-decay per token (the pages' g of width 1) is the per-write form with the gate
+    repeated over the token's W writes; its gradient, by central differences of the token
+    loop, is the sum of the W per-write gradients."""
+    _, x = rand_case(P=2, T=9, S=6, D=3, W=3, R=2, seed=51, ragged=False)
+    x["valid"] = np.array([9, 7], np.int32)
+    gt = x["g"][..., 0].copy()                       # [P, T]
+    x["g"] = np.repeat(gt[..., None], 3, axis=2)
+    dO = np.random.default_rng(52).standard_normal((2, 9, 3))
+    gr = oracle.backward(*args(x), dO)
+    dgt = gr["grad_log_decay"].sum(axis=2)
+
+    def loss(gate):
+        y = dict(x)
+        y["g"] = np.repeat(gate[..., None], 3, axis=2)
+        return float((oracle.sequential(*args(y))[0] * dO).sum())
+
+    h = 1e-6
+    for p in range(2):
+        for t in range(9):
+            gp, gm = gt.copy(), gt.copy()
+            gp[p, t] += h
+            gm[p, t] -= h
+            fd = (loss(gp) - loss(gm)) / (2 * h)
+            assert abs(fd - dgt[p, t]) <= 1e-6 * max(1.0, abs(fd)), (p, t, fd, dgt[p, t])

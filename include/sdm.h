@@ -65,7 +65,7 @@ typedef enum { SDM_F32 = 0, SDM_BF16 = 1 } sdm_dtype;
  *   slab_steps  Phase-2 steps whose Phase-1 state is held at once; 0 = automatic. The
  *               results do not depend on it (Phase 1 and the solve are per chunk).
  *   flags       0, or any of SDM_FLAG_PER_STEP_KERNELS, SDM_FLAG_SNAPSHOT_BF16,
- *               SDM_FLAG_TOKEN_GATE
+ *               SDM_FLAG_TOKEN_GATE, SDM_FLAG_SHARED_BANK
  * P * ceil(T / C) * C must be below 2^31.
  *
  * Phase 2 runs as one persistent kernel per slab in which each CTA owns one stream and one
@@ -90,6 +90,14 @@ typedef enum { SDM_F32 = 0, SDM_BF16 = 1 } sdm_dtype;
  * applies to every row the token writes; the backward's grad_log_decay is [P, T], the sum of
  * the per-write gradients in write order. Every entry point takes it. */
 #define SDM_FLAG_TOKEN_GATE 4
+/* One bank shared by all P streams (memory_ops.py sdm_write_read: num_memory_slots 0 with
+ * shared_bank=True): the bank (and the backward's grad_bank) is [S, D] instead of [P*S, D],
+ * and slot ids are rows of it, in [0, S). The caller asserts that no two streams select the
+ * same slot anywhere in the call; the library does not check it. With disjoint slot sets every
+ * row still has one writer and the streams are independent problems, so the results are those
+ * of the streams run one after another on the shared bank, and bitwise reproducible; if two
+ * streams do share a slot the result is unspecified. */
+#define SDM_FLAG_SHARED_BANK 8
 typedef struct {
     int32_t P, T, C, S, D, W, R;
     int32_t bank_dtype;

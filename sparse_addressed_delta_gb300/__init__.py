@@ -19,7 +19,7 @@ from typing import Dict, Optional
 
 import torch
 
-__all__ = ["FLAG_SNAPSHOT_BF16", "FLAG_TOKEN_GATE", "sdm_write_read", "sdm_write_read_save", "sdm_write_read_backward",
+__all__ = ["FLAG_SNAPSHOT_BF16", "FLAG_TOKEN_GATE", "FLAG_SHARED_BANK", "sdm_write_read", "sdm_write_read_save", "sdm_write_read_backward",
            "sdm_write_read_noalloc", "profile_write_read", "workspace_bytes", "launch_count",
            "phase1_debug", "KERNEL_KINDS",
            "device_status", "SdmError", "Shape", "library", "library_path", "version"]
@@ -32,6 +32,7 @@ KERNEL_KINDS = ("phase1", "solve", "gather", "dualmm", "dw", "phase2")
 FLAG_PER_STEP_KERNELS = 1
 FLAG_SNAPSHOT_BF16 = 2
 FLAG_TOKEN_GATE = 4
+FLAG_SHARED_BANK = 8
 SNAPSHOT_QUANT = {"none": 0, "bf16": FLAG_SNAPSHOT_BF16}
 _STATUS = {0: "SDM_OK", -1: "SDM_ERR_INVALID", -2: "SDM_ERR_UNSUPPORTED", -3: "SDM_ERR_CUDA",
            -4: "SDM_ERR_TIMEOUT", -5: "SDM_ERR_WORKSPACE", -6: "SDM_ERR_DEVICE"}
@@ -154,6 +155,17 @@ def _gate(log_decay: torch.Tensor, P: int, T: int, W: int):
     return 0, (P, T, W)
 
 
+def _bank_rows(bank: torch.Tensor, P: int, shared_bank: bool):
+    """(S, bank rows, flag): stream p owns rows [p*S, (p+1)*S) of a [P*S, D] bank, or with
+    ``shared_bank`` all streams use the one [S, D] bank (their slot sets must be disjoint)."""
+    if bank.dim() != 2 or (not shared_bank and bank.shape[0] % P):
+        raise ValueError(f"bank must be [P*S, D] with P={P} (or [S, D] with shared_bank), "
+                         f"got {tuple(bank.shape)}")
+    if shared_bank:
+        return bank.shape[0], bank.shape[0], FLAG_SHARED_BANK
+    return bank.shape[0] // P, bank.shape[0], 0
+
+
 def _need(t: torch.Tensor, name: str, shape, dtype, device) -> None:
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a tensor")
@@ -183,7 +195,7 @@ def sdm_write_read(bank: torch.Tensor, write_slots: torch.Tensor, write_w: torch
                    valid_tokens: Optional[torch.Tensor] = None, *, chunk_size: int,
                    slab_steps: int = 0, workspace: Optional[torch.Tensor] = None,
                    readings: Optional[torch.Tensor] = None, stream=None,
-                   flags: int = 0) -> torch.Tensor:
+                   flags: int = 0, shared_bank: bool = False) -> torch.Tensor:
     """Chunked SDM write/read over P streams; returns readings [P, T, D] and advances
     ``bank`` ([P*S, D], float32 or bfloat16, stream p owning rows [p*S, (p+1)*S)) in place.
 
@@ -195,13 +207,13 @@ def sdm_write_read(bank: torch.Tensor, write_slots: torch.Tensor, write_w: torch
         raise ValueError("write_slots must be [P, T, W]")
     P, T, W = write_slots.shape
     R = read_slots.shape[-1]
-    if bank.dim() != 2 or bank.shape[0] % P:
-        raise ValueError(f"bank must be [P*S, D] with P={P}, got {tuple(bank.shape)}")
-    S, D = bank.shape[0] // P, bank.shape[1]
+    S, rows, sflag = _bank_rows(bank, P, shared_bank)
+    flags |= sflag
+    D = bank.shape[1]
     dev, dt = bank.device, bank.dtype
     if dev.type != "cuda":
         raise ValueError("the bank must be a CUDA tensor")
-    _need(bank, "bank", (P * S, D), dt, dev)
+    _need(bank, "bank", (rows, D), dt, dev)
     _need(write_slots, "write_slots", (P, T, W), torch.int32, dev)
     _need(write_w, "write_w", (P, T, W), dt, dev)
     gflag, gshape = _gate(log_decay, P, T, W)
@@ -242,7 +254,7 @@ def sdm_write_read_host(bank: torch.Tensor, write_slots: torch.Tensor, write_w: 
                         valid_tokens: Optional[torch.Tensor] = None, *, chunk_size: int,
                         readings: Optional[torch.Tensor] = None, slab_steps: int = 0,
                         workspace: Optional[torch.Tensor] = None, stream=None,
-                        flags: int = 0) -> torch.Tensor:
+                        flags: int = 0, shared_bank: bool = False) -> torch.Tensor:
     """sdm_write_read with the inputs in host memory and the readings written to pinned host
     memory ([P, T, D], bank dtype); the bank stays on its GPU. Same arguments and layouts as
     ``sdm_write_read``; pinned inputs make the copies asynchronous."""
@@ -250,11 +262,13 @@ def sdm_write_read_host(bank: torch.Tensor, write_slots: torch.Tensor, write_w: 
         raise ValueError("write_slots must be [P, T, W]")
     P, T, W = write_slots.shape
     R = read_slots.shape[-1]
-    if bank.dim() != 2 or bank.shape[0] % P or bank.device.type != "cuda":
-        raise ValueError(f"bank must be a CUDA tensor [P*S, D] with P={P}")
-    S, D = bank.shape[0] // P, bank.shape[1]
+    S, rows, sflag = _bank_rows(bank, P, shared_bank)
+    flags |= sflag
+    if bank.device.type != "cuda":
+        raise ValueError("the bank must be a CUDA tensor")
+    D = bank.shape[1]
     dev, dt, cpu = bank.device, bank.dtype, torch.device("cpu")
-    _need(bank, "bank", (P * S, D), dt, dev)
+    _need(bank, "bank", (rows, D), dt, dev)
     _need(write_slots, "write_slots", (P, T, W), torch.int32, cpu)
     _need(write_w, "write_w", (P, T, W), dt, cpu)
     gflag, gshape = _gate(log_decay, P, T, W)
@@ -282,11 +296,14 @@ def sdm_write_read_host(bank: torch.Tensor, write_slots: torch.Tensor, write_w: 
     return readings
 
 
-def _shape_of(bank, write_slots, read_slots, chunk_size, slab_steps=0, flags=0):
+def _shape_of(bank, write_slots, read_slots, chunk_size, slab_steps=0, flags=0,
+              shared_bank=False):
     P, T, W = write_slots.shape
     R = read_slots.shape[-1]
-    S, D = bank.shape[0] // P, bank.shape[1]
-    return make_shape(P, T, chunk_size, S, D, W, R, bank.dtype, slab_steps, flags), (P, T, S, D, W, R)
+    S, _, sflag = _bank_rows(bank, P, shared_bank)
+    D = bank.shape[1]
+    return (make_shape(P, T, chunk_size, S, D, W, R, bank.dtype, slab_steps, flags | sflag),
+            (P, T, S, D, W, R))
 
 
 def saved_bytes(shape: Shape) -> int:
@@ -306,7 +323,7 @@ def _snapshot_flag(snapshot_quant: str) -> int:
 def sdm_write_read_save(bank, write_slots, write_w, log_decay, beta, v, read_slots, read_w,
                         valid_tokens=None, *, chunk_size: int, slab_steps: int = 0,
                         workspace=None, readings=None, saved=None, stream=None, flags: int = 0,
-                        snapshot_quant: str = "none"):
+                        snapshot_quant: str = "none", shared_bank: bool = False):
     """The saving forward: sdm_write_read plus the snapshot the backward needs.
     ``snapshot_quant`` "bf16" stores the snapshot of a float32 bank in bfloat16 (half the
     bytes; the backward then restores the written rows to their rounded values).
@@ -315,9 +332,10 @@ def sdm_write_read_save(bank, write_slots, write_w, log_decay, beta, v, read_slo
     P, T, W = write_slots.shape
     gflag, gshape = _gate(log_decay, P, T, W)
     shape, (P, T, S, D, W, R) = _shape_of(bank, write_slots, read_slots, chunk_size,
-                                          slab_steps, flags | gflag)
+                                          slab_steps, flags | gflag, shared_bank)
     dev, dt = bank.device, bank.dtype
-    for t, name, shp, typ in ((bank, "bank", (P * S, D), dt), (write_slots, "write_slots", (P, T, W), torch.int32),
+    rows = S if shared_bank else P * S
+    for t, name, shp, typ in ((bank, "bank", (rows, D), dt), (write_slots, "write_slots", (P, T, W), torch.int32),
                               (write_w, "write_w", (P, T, W), dt), (log_decay, "log_decay", gshape, torch.float32),
                               (beta, "beta", (P, T), torch.float32), (v, "v", (P, T, D), dt),
                               (read_slots, "read_slots", (P, T, R), torch.int32), (read_w, "read_w", (P, T, R), dt)):
@@ -341,7 +359,7 @@ def sdm_write_read_save(bank, write_slots, write_w, log_decay, beta, v, read_slo
 def sdm_write_read_backward(bank, write_slots, write_w, log_decay, beta, v, read_slots, read_w,
                             valid_tokens, saved, grad_readings, *, chunk_size: int,
                             grad_bank=None, slab_steps: int = 0, workspace=None, stream=None,
-                            snapshot_quant: str = "none"):
+                            snapshot_quant: str = "none", shared_bank: bool = False):
     """The backward after sdm_write_read_save (with the same ``snapshot_quant``): restores
     ``bank`` to its initial state (with "bf16", the rows the call wrote to their bfloat16
     rounding) and returns a dict of float32 gradients (grad_bank, grad_v, grad_beta,
@@ -351,13 +369,14 @@ def sdm_write_read_backward(bank, write_slots, write_w, log_decay, beta, v, read
     P, T, W = write_slots.shape
     gflag, gshape = _gate(log_decay, P, T, W)
     shape, (P, T, S, D, W, R) = _shape_of(bank, write_slots, read_slots, chunk_size, slab_steps,
-                                          _snapshot_flag(snapshot_quant) | gflag)
+                                          _snapshot_flag(snapshot_quant) | gflag, shared_bank)
     dev, dt = bank.device, bank.dtype
     _need(grad_readings, "grad_readings", (P, T, D), dt, dev)
     f32 = dict(dtype=torch.float32, device=dev)
+    rows = S if shared_bank else P * S
     if grad_bank is None:
-        grad_bank = torch.zeros((P * S, D), **f32)
-    _need(grad_bank, "grad_bank", (P * S, D), torch.float32, dev)
+        grad_bank = torch.zeros((rows, D), **f32)
+    _need(grad_bank, "grad_bank", (rows, D), torch.float32, dev)
     out = {"grad_bank": grad_bank, "grad_v": torch.empty((P, T, D), **f32),
            "grad_beta": torch.empty((P, T), **f32), "grad_write_w": torch.empty((P, T, W), **f32),
            "grad_log_decay": torch.empty(gshape, **f32),
@@ -384,18 +403,20 @@ def sdm_write_read_noalloc(bank: torch.Tensor, write_slots: torch.Tensor,
                            v: torch.Tensor, read_slots: torch.Tensor, read_w: torch.Tensor,
                            valid_tokens: Optional[torch.Tensor] = None, *, chunk_size: int,
                            readings: torch.Tensor, slab_steps: int = 0, stream=None,
-                           flags: int = 0) -> torch.Tensor:
+                           flags: int = 0, shared_bank: bool = False) -> torch.Tensor:
     """sdm_write_read for callers that cannot allocate device memory: the library's static
     device scratch (16 MiB per GPU) replaces the workspace, and the caller passes the
     readings buffer, so the call allocates nothing. Calls overlapping on the GPU race on the
     shared scratch; the first call on a device should come before any CUDA graph capture."""
     P, T, W = write_slots.shape
     R = read_slots.shape[-1]
-    S, D = bank.shape[0] // P, bank.shape[1]
+    S, rows, sflag = _bank_rows(bank, P, shared_bank)
+    flags |= sflag
+    D = bank.shape[1]
     dev, dt = bank.device, bank.dtype
     gflag, gshape = _gate(log_decay, P, T, W)
     flags |= gflag
-    for t, name, shp, typ in ((bank, "bank", (P * S, D), dt), (write_slots, "write_slots", (P, T, W), torch.int32),
+    for t, name, shp, typ in ((bank, "bank", (rows, D), dt), (write_slots, "write_slots", (P, T, W), torch.int32),
                               (write_w, "write_w", (P, T, W), dt), (log_decay, "log_decay", gshape, torch.float32),
                               (beta, "beta", (P, T), torch.float32), (v, "v", (P, T, D), dt),
                               (read_slots, "read_slots", (P, T, R), torch.int32), (read_w, "read_w", (P, T, R), dt),
@@ -415,12 +436,15 @@ def sdm_write_read_noalloc(bank: torch.Tensor, write_slots: torch.Tensor,
 
 def profile_write_read(bank, write_slots, write_w, log_decay, beta, v, read_slots, read_w,
                        valid_tokens=None, *, chunk_size: int, slab_steps: int = 0,
-                       workspace=None, readings=None, stream=None, flags: int = 0):
+                       workspace=None, readings=None, stream=None, flags: int = 0,
+                       shared_bank: bool = False):
     """One sdm_write_read call with CUDA events around every kernel launch (synchronizes).
     Returns (readings, {family: (total_ms, launches)}) for the families in KERNEL_KINDS."""
     P, T, W = write_slots.shape
     R = read_slots.shape[-1]
-    S, D = bank.shape[0] // P, bank.shape[1]
+    S, _, sflag = _bank_rows(bank, P, shared_bank)
+    flags |= sflag
+    D = bank.shape[1]
     dev, dt = bank.device, bank.dtype
     shape = make_shape(P, T, chunk_size, S, D, W, R, dt, slab_steps,
                        flags | _gate(log_decay, P, T, W)[0])

@@ -64,7 +64,8 @@ int check_shape(const sdm_shape *s, Dims &d) {
         return fail(SDM_ERR_INVALID, "bank_dtype must be SDM_F32 (0) or SDM_BF16 (1), got %d",
                     s->bank_dtype);
     if (s->slab_steps < 0) return fail(SDM_ERR_INVALID, "slab_steps must be >= 0");
-    if (s->flags & ~(SDM_FLAG_PER_STEP_KERNELS | SDM_FLAG_SNAPSHOT_BF16 | SDM_FLAG_TOKEN_GATE))
+    if (s->flags & ~(SDM_FLAG_PER_STEP_KERNELS | SDM_FLAG_SNAPSHOT_BF16 | SDM_FLAG_TOKEN_GATE |
+                     SDM_FLAG_SHARED_BANK))
         return fail(SDM_ERR_INVALID, "unknown flags 0x%x", (unsigned)s->flags);
     if (s->D != 32 && s->D != 64 && s->D != 128 && s->D != 256 && s->D != 512)
         return fail(SDM_ERR_UNSUPPORTED, "head_dim D=%d has no kernel (32, 64, 128, 256, 512)",
@@ -81,6 +82,7 @@ int check_shape(const sdm_shape *s, Dims &d) {
     d.per_step = ((s->flags & SDM_FLAG_PER_STEP_KERNELS) || !phase2_fused_fits(d)) ? 1 : 0;
     d.snapq = ((s->flags & SDM_FLAG_SNAPSHOT_BF16) && d.dtype == SDM_F32) ? 1 : 0;
     d.gate = (s->flags & SDM_FLAG_TOKEN_GATE) ? 1 : 0;
+    d.shared = (s->flags & SDM_FLAG_SHARED_BANK) ? 1 : 0;
     return SDM_OK;
 }
 

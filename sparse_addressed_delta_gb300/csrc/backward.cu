@@ -49,7 +49,7 @@ __global__ void __launch_bounds__(NTB) k_b_restore(Dims d, Inputs in, Work w, in
     const int ng = w.ngroups[n];
     const int32_t *goff = w.goff + (size_t)n * goff_stride(CW);
     const int32_t *gslot = w.gslot + (size_t)n * CW;
-    BT *bank = static_cast<BT *>(in.bank) + (size_t)p * d.S * D + lane * CPL;
+    BT *bank = static_cast<BT *>(in.bank) + stream_row0(d, p) * D + lane * CPL;
     // the snapshot is in the bank dtype, or (d.snapq, float32 banks) in bfloat16
     const size_t s0 = (size_t)(ti * d.P + p) * CW * D + lane * CPL;
     const BT *snap = static_cast<const BT *>(in.snap) + s0;
@@ -90,8 +90,8 @@ __global__ void __launch_bounds__(NTB) k_b_gather(Dims d, Inputs in, Work w, con
     const int32_t *ws = in.ws + tok * W;
     const float *gw = w.gw + (size_t)n * C * W + (size_t)t * W;
     const float *dw = w.dwt + (size_t)n * C * W + (size_t)t * W;
-    const BT *bank = static_cast<const BT *>(in.bank) + (size_t)p * d.S * D + lane * CPL;
-    const float *gb = gbank + (size_t)p * d.S * D + lane * CPL;
+    const BT *bank = static_cast<const BT *>(in.bank) + stream_row0(d, p) * D + lane * CPL;
+    const float *gb = gbank + stream_row0(d, p) * D + lane * CPL;
     float ar[CPL], ad[CPL];
 #pragma unroll
     for (int c = 0; c < CPL; ++c) { ar[c] = 0.f; ad[c] = 0.f; }
@@ -336,8 +336,8 @@ __global__ void __launch_bounds__(NTB) k_b_dots(Dims d, Inputs in, Work w, const
     const int nv = w.nvalid[n];
     const int nw = nv * W, nr = nv * R, ng = w.ngroups[n];
     const size_t tok0 = (size_t)p * d.T + (size_t)ti * C;
-    const BT *bank = static_cast<const BT *>(in.bank) + (size_t)p * d.S * D + lane * CPL;
-    const float *gb = gbank + (size_t)p * d.S * D + lane * CPL;
+    const BT *bank = static_cast<const BT *>(in.bank) + stream_row0(d, p) * D + lane * CPL;
+    const float *gb = gbank + stream_row0(d, p) * D + lane * CPL;
     const float *u = w.bu + (size_t)p * C * D + lane * CPL;
     const float *dret = w.bdret + (size_t)p * C * D + lane * CPL;
     const float *dO = w.bdo + (size_t)p * C * D + lane * CPL;
@@ -408,7 +408,7 @@ __global__ void __launch_bounds__(NTB) k_b_dbw(Dims d, Work w, float *gbank, int
     const int32_t *perm = w.perm + (size_t)n * CW;
     const float *gw = w.gw + (size_t)n * CW;
     const float *dret = w.bdret + (size_t)p * C * D + lane * CPL;
-    float *gb = gbank + (size_t)p * d.S * D + lane * CPL;
+    float *gb = gbank + stream_row0(d, p) * D + lane * CPL;
     const unsigned magW = div_magic(W);
     for (int g = blockIdx.x * NWB + warp; g < ng; g += gridDim.x * NWB) {
         const int sl = gslot[g];
@@ -441,7 +441,7 @@ __global__ void __launch_bounds__(NTB) k_b_dbr(Dims d, Work w, float *gbank, int
     const unsigned long long *rkey = w.rkey + (size_t)n * CR;
     const float *qw = w.qw + (size_t)n * CR;
     const float *dO = w.bdo + (size_t)p * C * D + lane * CPL;
-    float *gb = gbank + (size_t)p * d.S * D + lane * CPL;
+    float *gb = gbank + stream_row0(d, p) * D + lane * CPL;
     for (int g = blockIdx.x * NWB + warp; g < ng; g += gridDim.x * NWB) {
         const int sl = gslot[g];
         if ((unsigned)sl >= (unsigned)d.S) continue;

@@ -43,7 +43,7 @@ __global__ void __launch_bounds__(kBlock) k_gather(Dims d, Inputs in, Work w, in
     for (int c = 0; c < CPL; ++c) { ar[c] = 0.f; ai[c] = 0.f; }
     if (active) {
         const size_t tok = (size_t)p * d.T + (size_t)ti * C + t;
-        const BT *bank = static_cast<const BT *>(in.bank) + (size_t)p * d.S * D + lane * CPL;
+        const BT *bank = static_cast<const BT *>(in.bank) + stream_row0(d, p) * D + lane * CPL;
         const unsigned S = (unsigned)d.S;
         {
             const int32_t *ws = in.ws + tok * W;
@@ -311,7 +311,7 @@ __global__ void __launch_bounds__(kBlock, 2) k_dw(Dims d, Inputs in, Work w, int
     const int32_t *perm = w.perm + (size_t)n * CW;
     const float *wdw = w.wdw + (size_t)n * CW;
     const float *dvp = w.dv + (size_t)p * C * D + lane * CPL;
-    BT *bank = static_cast<BT *>(in.bank) + (size_t)p * d.S * D + lane * CPL;
+    BT *bank = static_cast<BT *>(in.bank) + stream_row0(d, p) * D + lane * CPL;
     const unsigned magic = div_magic(W);
     const int stride = gridDim.x * kWarps;
     for (int g0 = blockIdx.x * kWarps + warp; g0 < ng; g0 += NG * stride) {

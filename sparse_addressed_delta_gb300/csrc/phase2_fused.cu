@@ -205,7 +205,7 @@ __global__ void __launch_bounds__(NP2) k_phase2_pipe(Dims d, Inputs in, Work w, 
     unsigned long long *fullB = fullA + 2;
     unsigned long long *empty = fullA + 4;
 
-    BT *bank = static_cast<BT *>(in.bank) + (size_t)p * d.S * D + c0;
+    BT *bank = static_cast<BT *>(in.bank) + stream_row0(d, p) * D + c0;
     const BT *vin = static_cast<const BT *>(in.v);
     BT *out = static_cast<BT *>(in.readings);
     const unsigned S = (unsigned)d.S;

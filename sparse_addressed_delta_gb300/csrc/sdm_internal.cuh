@@ -41,7 +41,13 @@ struct Dims {
                     // Phase 2 (one bulk copy lands rows at a bank-conflict-free pitch), else C
     int snapq;      // 1: the snapshot of a float32 bank is stored in bfloat16
     int gate;       // 1: one log-decay per token ([P, T]) instead of one per write entry
+    int shared;     // 1: one [S, D] bank for all streams (disjoint slot sets), else [P*S, D]
 };
+
+// first bank row of stream p: its own block of S rows, or row 0 of a shared bank
+__host__ __device__ __forceinline__ size_t stream_row0(const Dims &d, int p) {
+    return d.shared ? 0 : (size_t)p * d.S;
+}
 
 inline int x_row_pitch(const Dims &d) { return (d.per_step || d.bwd) ? d.C : d.C + 4; }
 

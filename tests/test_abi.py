@@ -64,7 +64,7 @@ def test_launch_count():
 
 @pytest.mark.parametrize("kw,code", [
     (dict(C=8), -1), (dict(C=300), -1), (dict(W=0), -1), (dict(R=257), -1), (dict(P=0), -1),
-    (dict(T=0), -1), (dict(S=0), -1), (dict(D=96), -2), (dict(dtype=7), -1), (dict(flags=8), -1),
+    (dict(T=0), -1), (dict(S=0), -1), (dict(D=96), -2), (dict(dtype=7), -1), (dict(flags=16), -1),
     (dict(P=1 << 16, T=1 << 16), -1)])
 def test_refusals(kw, code):
     base = dict(P=2, T=64, C=16, S=128, D=64, W=4, R=4, dtype=sdm.SDM_F32, flags=0)
@@ -110,7 +110,7 @@ def test_bf16_snapshot_halves_saved_bytes():
         assert plain == 7 * 3 * 16 * 3 * 64 * (4 if dt == sdm.SDM_F32 else 2)
         assert plain == ratio * half
     with pytest.raises(sdm.SdmError):
-        sdm.saved_bytes(sdm.make_shape(3, 100, 16, 50, 64, 3, 4, sdm.SDM_F32, flags=8))
+        sdm.saved_bytes(sdm.make_shape(3, 100, 16, 50, 64, 3, 4, sdm.SDM_F32, flags=16))
 
 
 def test_token_gate_flag():

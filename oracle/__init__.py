@@ -14,6 +14,8 @@ Functions (every one cites the definition it follows in ``sdm_oracle.c``):
   backward_snapshot
               the reverse mode as the chunked backward runs it from a stored (optionally
               bfloat16) snapshot of the rows each chunk writes (memory_ops.py snapshot_quant)
+  head_split, head_merge, bank_expand, bank_sum
+              the layer I/O around the op (memory_ops.py "Layer I/O"), as array rearranges
 
 Pins (tests/test_oracle.py): dense brute force, closed forms (scalar delta rule, pure
 decay), chunk-size invariance, the solve identity, brute-force grouping and central
@@ -233,6 +235,32 @@ def backward_snapshot(bank, ws, k, g, beta, v, rs, q, valid, grad_readings, *, c
     _check(rc, "backward_snapshot")
     return {"grad_bank": dB, "grad_v": dv, "grad_beta": db, "grad_write_w": dk,
             "grad_log_decay": dg, "grad_read_w": dq, "restored_bank": B}
+
+
+# ---------------------------------------------------------------------------------------
+# layer I/O (memory_ops.py "Layer I/O"): the definitions as array rearranges
+# ---------------------------------------------------------------------------------------
+
+def head_split(x: np.ndarray, H: int) -> np.ndarray:
+    """rearrange 'b t (h k) -> (b h) t k': [B, T, H*K] -> [B*H, T, K]."""
+    B, T, HK = x.shape
+    return x.reshape(B, T, H, HK // H).transpose(0, 2, 1, 3).reshape(B * H, T, HK // H)
+
+
+def head_merge(x: np.ndarray, H: int) -> np.ndarray:
+    """rearrange '(b h) t d -> b t (h d)': [B*H, T, D] -> [B, T, H*D]."""
+    BH, T, D = x.shape
+    return x.reshape(BH // H, H, T, D).transpose(0, 2, 1, 3).reshape(BH // H, T, H * D)
+
+
+def bank_expand(param: np.ndarray, B: int) -> np.ndarray:
+    """[S, D] -> [B, S, D], every batch copy the parameter bank."""
+    return np.broadcast_to(param, (B,) + param.shape).copy()
+
+
+def bank_sum(x: np.ndarray) -> np.ndarray:
+    """[B, S, D] -> [S, D], the sum over the batch in float64."""
+    return np.asarray(x, np.float64).sum(axis=0)
 
 
 def from_stored(inputs: Dict[str, np.ndarray], dtype: str) -> Dict[str, np.ndarray]:

@@ -389,3 +389,27 @@ def test_per_token_gate_gradient_is_the_sum_over_writes():
             gm[p, t] -= h
             fd = (loss(gp) - loss(gm)) / (2 * h)
             assert abs(fd - dgt[p, t]) <= 1e-6 * max(1.0, abs(fd)), (p, t, fd, dgt[p, t])
+
+
+# ---------------------------------------------------------------------------------------
+# layer I/O (memory_ops.py "Layer I/O")
+# ---------------------------------------------------------------------------------------
+
+def test_head_split_is_the_pages_row_map_and_merge_inverts_it():
+    """dst row (b*H + h)*T + t = src row (b*T + t)*H + h, by explicit loops over the rows of
+    the flattened arrays; merge after split is the identity."""
+    B, T, H, K = 2, 5, 3, 4
+    x = np.arange(B * T * H * K, dtype=np.float64).reshape(B, T, H * K)
+    y = oracle.head_split(x, H)
+    src, dst = x.reshape(-1, K), y.reshape(-1, K)
+    for b in range(B):
+        for h in range(H):
+            for t in range(T):
+                np.testing.assert_array_equal(dst[(b * H + h) * T + t], src[(b * T + t) * H + h])
+    np.testing.assert_array_equal(oracle.head_merge(y, H), x)
+
+
+def test_bank_sum_of_expand_is_b_times_the_bank():
+    p = np.random.default_rng(91).standard_normal((7, 3))
+    np.testing.assert_array_equal(oracle.bank_expand(p, 4)[2], p)
+    np.testing.assert_allclose(oracle.bank_sum(oracle.bank_expand(p, 4)), 4 * p, rtol=1e-15)

@@ -53,6 +53,9 @@ def parse_args():
                     help="run Phase 2 as three kernels per step instead of the fused kernel")
     ap.add_argument("--backward", action="store_true",
                     help="time the saving forward + backward (one step = both calls) instead")
+    ap.add_argument("--layer-io", action="store_true",
+                    help="time the layer I/O kernels (head split/merge, bank expand/sum) on the "
+                         "batch 4 x 8 heads layout of the ragged workload instead")
     ap.add_argument("--snapshot-quant", choices=["none", "bf16"], default="none",
                     help="with --backward: store the snapshot of a float32 bank in bfloat16")
     ap.add_argument("--ncu-run", type=int, default=0, metavar="K",
@@ -588,6 +591,76 @@ def run_for_profiler(args):
     print(f"ncu target: {args.ncu_run} calls of {wl.name} done")
 
 
+def run_layer_io(args):
+    """The layer I/O kernels on the layout of the P=32 = batch 4 x 8 heads workload (T=8192,
+    head_dim 128, S=262144 x 128 bf16 bank): head split [4, 8192, 1024] -> [32, 8192, 128] and
+    back, bank expand [262144, 128] -> [4, 262144, 128] and the batch sum back. Each op is timed
+    with CUDA events over K launches after W warm-ups, L2 flushed (512 MiB write) before each;
+    GB/s counts the bytes read and written once."""
+    import torch
+
+    import sparse_addressed_delta_gb300 as sdm
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    B, H, T, CD, S, D = 4, 8, 8192, 128, 262144, 128
+    g = torch.Generator(device=dev).manual_seed(5)
+    x = torch.randn((B, T, H * CD), device=dev, generator=g).bfloat16()
+    y = sdm.head_split(x, H)
+    param = torch.randn((S, D), device=dev, generator=g).bfloat16()
+    e = sdm.bank_expand(param, B)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    # outputs allocated once: the timed region holds the kernel only (C ABI, current stream)
+    lib, bf, st = sdm.library(), sdm.SDM_BF16, sdm._stream_ptr(None)
+    o_split, o_merge = torch.empty_like(y), torch.empty_like(x)
+    o_exp, o_sum = torch.empty_like(e), torch.empty_like(param)
+    P_ = sdm._ptr
+
+    def run(rc):
+        if rc != 0:
+            raise RuntimeError(lib.sdm_last_error().decode())
+
+    ops = {"head_split": (lambda: run(lib.sdm_head_split(P_(x), P_(o_split), B, T, H, CD, bf, st)),
+                          2 * x.numel() * 2),
+           "head_merge": (lambda: run(lib.sdm_head_merge(P_(y), P_(o_merge), B, T, H, CD, bf, st)),
+                          2 * y.numel() * 2),
+           "bank_expand": (lambda: run(lib.sdm_bank_expand(P_(param), P_(o_exp), B, S, D, bf, st)),
+                           param.numel() * 2 * (1 + B)),
+           "bank_sum": (lambda: run(lib.sdm_bank_sum(P_(e), P_(o_sum), B, S, D, bf, st)),
+                        param.numel() * 2 * (B + 1))}
+    peak, peak_src = measured_peak()
+    res = {}
+    clocks = ClockSampler(0)
+    for name, (fn, nbytes) in ops.items():
+        for _ in range(args.warmup):
+            fn()
+        ts = []
+        for _ in range(args.steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            ts.append(a.elapsed_time(b))
+        ms = statistics.median(ts)
+        res[name] = {"us": 1e3 * ms, "bytes": nbytes, "GB/s": nbytes / ms / 1e6,
+                     "frac": nbytes / ms / 1e6 / peak}
+    clk = clocks.stop()
+    torch.cuda.synchronize()
+    if not (torch.equal(o_split, y) and torch.equal(o_merge, x) and torch.equal(o_exp, e)):
+        raise RuntimeError("layer I/O outputs differ from the binding's")
+    line = {"metric": "SDM layer I/O achieved HBM GB/s (head split/merge, bank expand/sum)",
+            "value": statistics.mean(r["GB/s"] for r in res.values()), "unit": "GB/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "batch 4 x 8 heads, T=8192, head_dim 128; bank 262144 x 128",
+                       "l2": "flushed before every launch (512 MiB write)"},
+            "peak": peak, "peak_source": peak_src, "ops": res, "clocks": clk,
+            "gpu": torch.cuda.get_device_name(dev)}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     if args.ncu_run:
@@ -595,6 +668,9 @@ def main():
         return
     if args.backward:
         run_backward(args)
+        return
+    if args.layer_io:
+        run_layer_io(args)
         return
     if args.impl == "reference":
         run_reference(args)

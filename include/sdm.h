@@ -310,6 +310,33 @@ int sdm_write_read_noalloc(const sdm_shape *shape, void *bank, const int32_t *wr
                            const void *v, const int32_t *read_slots, const void *read_w,
                            const int32_t *valid_tokens, void *readings, void *stream);
 
+/* ---------------------------------------------------------------------------------------
+ * Layer I/O around the write/read (memory_ops.py, "Layer I/O: head split / merge and the
+ * per-batch bank expand"). All pointers are device pointers on the current device, dtype is
+ * SDM_F32 or SDM_BF16, and the work is queued on stream (asynchronous). Each call returns
+ * SDM_OK, or a negative sdm_status for a NULL pointer, bad sizes or a bad dtype (nothing
+ * queued). Deterministic; the copies are bitwise.
+ * --------------------------------------------------------------------------------------- */
+
+/* Head split, rearrange 'b t (h k) -> (b h) t k': src [B, T, H*CD] -> dst [B*H, T, CD], i.e.
+ * dst row (b*H + h)*T + t = src row (b*T + t)*H + h (rows of CD elements). src and dst must not
+ * overlap. */
+int sdm_head_split(const void *src, void *dst, int B, int T, int H, int CD, int dtype,
+                   void *stream);
+
+/* Head merge, the inverse: src [B*H, T, CD] -> dst [B, T, H*CD]. */
+int sdm_head_merge(const void *src, void *dst, int B, int T, int H, int CD, int dtype,
+                   void *stream);
+
+/* Per-batch bank expand: out [B, S, D] = B copies of param [S, D] (the learned bank each
+ * batch element starts from). */
+int sdm_bank_expand(const void *param, void *out, int B, long long S, int D, int dtype,
+                    void *stream);
+
+/* Its adjoint: out [S, D] = sum over b of x [B, S, D], accumulated in float32 in batch order
+ * and rounded once to the dtype (the gradient of the shared parameter bank). B >= 1. */
+int sdm_bank_sum(const void *x, void *out, int B, long long S, int D, int dtype, void *stream);
+
 /* Thread-local description of the last refused call or CUDA error ("" if none). */
 const char *sdm_last_error(void);
 

@@ -19,7 +19,8 @@ from typing import Dict, Optional
 
 import torch
 
-__all__ = ["FLAG_SNAPSHOT_BF16", "FLAG_TOKEN_GATE", "FLAG_SHARED_BANK", "sdm_write_read", "sdm_write_read_save", "sdm_write_read_backward",
+__all__ = ["FLAG_SNAPSHOT_BF16", "FLAG_TOKEN_GATE", "FLAG_SHARED_BANK", "head_split",
+           "head_merge", "bank_expand", "bank_sum", "sdm_write_read", "sdm_write_read_save", "sdm_write_read_backward",
            "sdm_write_read_noalloc", "profile_write_read", "workspace_bytes", "launch_count",
            "phase1_debug", "KERNEL_KINDS",
            "device_status", "SdmError", "Shape", "library", "library_path", "version"]
@@ -101,6 +102,12 @@ def library() -> ctypes.CDLL:
             lib.sdm_phase1_debug.restype = i32
             lib.sdm_get_device_status.argtypes = [vp, ctypes.POINTER(_DeviceStatus), vp]
             lib.sdm_get_device_status.restype = i32
+            for name in ("sdm_head_split", "sdm_head_merge"):
+                getattr(lib, name).argtypes = [vp, vp, i32, i32, i32, i32, i32, vp]
+                getattr(lib, name).restype = i32
+            for name in ("sdm_bank_expand", "sdm_bank_sum"):
+                getattr(lib, name).argtypes = [vp, vp, i32, ctypes.c_longlong, i32, i32, vp]
+                getattr(lib, name).restype = i32
             lib.sdm_last_error.argtypes = []
             lib.sdm_last_error.restype = ctypes.c_char_p
             lib.sdm_version.argtypes = []
@@ -510,3 +517,62 @@ def device_status(workspace: torch.Tensor, stream=None) -> Dict[str, int]:
                                                _stream_ptr(stream)))
     return {"code": st.code, "first_bad_token": st.first_bad_token, "bad_slots": st.bad_slots,
             "repeated_write_slots": st.repeated_write_slots}
+
+
+# ------------------------------------------------------------------------------------------
+# layer I/O (memory_ops.py "Layer I/O: head split / merge and the per-batch bank expand")
+# ------------------------------------------------------------------------------------------
+
+def _io_tensor(x: torch.Tensor, name: str, ndim: int) -> None:
+    if x.device.type != "cuda" or not x.is_contiguous() or x.dim() != ndim:
+        raise ValueError(f"{name} must be a contiguous {ndim}-d CUDA tensor")
+    _dtype_code(x.dtype)
+
+
+def head_split(x: torch.Tensor, H: int, stream=None) -> torch.Tensor:
+    """rearrange(x, 'b t (h k) -> (b h) t k', h=H) as a row copy: [B, T, H*CD] -> [B*H, T, CD]."""
+    _io_tensor(x, "x", 3)
+    B, T, HC = x.shape
+    if HC % H:
+        raise ValueError(f"the last dimension {HC} is not a multiple of H={H}")
+    out = torch.empty((B * H, T, HC // H), dtype=x.dtype, device=x.device)
+    with torch.cuda.device(x.device):
+        _check(library().sdm_head_split(_ptr(x), _ptr(out), B, T, H, HC // H,
+                                        _dtype_code(x.dtype), _stream_ptr(stream)))
+    return out
+
+
+def head_merge(x: torch.Tensor, H: int, stream=None) -> torch.Tensor:
+    """rearrange(x, '(b h) t d -> b t (h d)', h=H): [B*H, T, CD] -> [B, T, H*CD]."""
+    _io_tensor(x, "x", 3)
+    BH, T, CD = x.shape
+    if BH % H:
+        raise ValueError(f"the first dimension {BH} is not a multiple of H={H}")
+    out = torch.empty((BH // H, T, H * CD), dtype=x.dtype, device=x.device)
+    with torch.cuda.device(x.device):
+        _check(library().sdm_head_merge(_ptr(x), _ptr(out), BH // H, T, H, CD,
+                                        _dtype_code(x.dtype), _stream_ptr(stream)))
+    return out
+
+
+def bank_expand(param: torch.Tensor, B: int, stream=None) -> torch.Tensor:
+    """The per-batch bank: [S, D] -> [B, S, D], every copy the parameter bank."""
+    _io_tensor(param, "param", 2)
+    S, D = param.shape
+    out = torch.empty((B, S, D), dtype=param.dtype, device=param.device)
+    with torch.cuda.device(param.device):
+        _check(library().sdm_bank_expand(_ptr(param), _ptr(out), B, S, D,
+                                         _dtype_code(param.dtype), _stream_ptr(stream)))
+    return out
+
+
+def bank_sum(x: torch.Tensor, stream=None) -> torch.Tensor:
+    """The expand's adjoint: [B, S, D] -> [S, D], summed over the batch in float32 in batch
+    order and rounded once to the dtype."""
+    _io_tensor(x, "x", 3)
+    B, S, D = x.shape
+    out = torch.empty((S, D), dtype=x.dtype, device=x.device)
+    with torch.cuda.device(x.device):
+        _check(library().sdm_bank_sum(_ptr(x), _ptr(out), B, S, D, _dtype_code(x.dtype),
+                                      _stream_ptr(stream)))
+    return out

@@ -14,12 +14,12 @@ namespace {
 
 constexpr int kIoThreads = 256;
 
-// dst row r <- src row of r, for the split (SPLIT) or the merge; one warp per row, 16-byte
-// pieces (n16 per row) or 2/4-byte elements (ne per row, es bytes each)
-template <bool SPLIT, bool VEC>
+// dst row r <- src row of r, for the split (SPLIT) or the merge, for rows that do not split
+// into whole 16-byte pieces: one warp per row, 2- or 4-byte elements (ne per row, es bytes)
+template <bool SPLIT>
 __global__ void __launch_bounds__(kIoThreads) k_head_perm(const unsigned char *src,
                                                           unsigned char *dst, long long rows,
-                                                          int H, int T, int n16, int ne, int es) {
+                                                          int H, int T, int ne, int es) {
     const long long warps = (long long)gridDim.x * (kIoThreads / 32);
     const int lane = threadIdx.x & 31;
     for (long long r = (long long)blockIdx.x * (kIoThreads / 32) + (threadIdx.x >> 5); r < rows;
@@ -32,11 +32,7 @@ __global__ void __launch_bounds__(kIoThreads) k_head_perm(const unsigned char *s
             const long long h = r % H, bt = r / H, t = bt % T, b = bt / T;
             srow = (b * H + h) * T + t;
         }
-        if (VEC) {
-            const uint4 *s = reinterpret_cast<const uint4 *>(src) + srow * n16;
-            uint4 *d = reinterpret_cast<uint4 *>(dst) + r * n16;
-            for (int i = lane; i < n16; i += 32) d[i] = s[i];
-        } else if (es == 2) {
+        if (es == 2) {
             const unsigned short *s = reinterpret_cast<const unsigned short *>(src) + srow * ne;
             unsigned short *d = reinterpret_cast<unsigned short *>(dst) + r * ne;
             for (int i = lane; i < ne; i += 32) d[i] = s[i];
@@ -45,6 +41,28 @@ __global__ void __launch_bounds__(kIoThreads) k_head_perm(const unsigned char *s
             unsigned *d = reinterpret_cast<unsigned *>(dst) + r * ne;
             for (int i = lane; i < ne; i += 32) d[i] = s[i];
         }
+    }
+}
+
+// the 16-byte path: one thread per 16-byte piece k of the destination (row k / n16, piece
+// k % n16), so that short rows still keep every lane of a warp busy
+template <bool SPLIT>
+__global__ void __launch_bounds__(kIoThreads) k_head_perm16(const uint4 *src, uint4 *dst,
+                                                           long long pieces, int H, int T,
+                                                           int n16) {
+    const long long stride = (long long)gridDim.x * kIoThreads;
+    for (long long k = (long long)blockIdx.x * kIoThreads + threadIdx.x; k < pieces; k += stride) {
+        const long long r = k / n16;
+        const int i = (int)(k - r * n16);
+        long long srow;
+        if (SPLIT) {
+            const long long t = r % T, bh = r / T, h = bh % H, b = bh / H;
+            srow = (b * T + t) * H + h;
+        } else {
+            const long long h = r % H, bt = r / H, t = bt % T, b = bt / T;
+            srow = (b * H + h) * T + t;
+        }
+        dst[k] = src[srow * n16 + i];
     }
 }
 
@@ -120,12 +138,17 @@ int head_perm(bool split, const void *src, void *dst, int B, int T, int H, int C
     const int grid = grid_for(rows, kIoThreads / 32);
     auto s = static_cast<const unsigned char *>(src);
     auto d = static_cast<unsigned char *>(dst);
-    if (split) {
-        if (vec) k_head_perm<true, true><<<grid, kIoThreads, 0, st>>>(s, d, rows, H, T, n16, CD, es);
-        else k_head_perm<true, false><<<grid, kIoThreads, 0, st>>>(s, d, rows, H, T, n16, CD, es);
+    if (vec) {
+        const long long pieces = rows * n16;
+        const int g16 = grid_for(pieces, kIoThreads);
+        auto s16 = reinterpret_cast<const uint4 *>(s);
+        auto d16 = reinterpret_cast<uint4 *>(d);
+        if (split) k_head_perm16<true><<<g16, kIoThreads, 0, st>>>(s16, d16, pieces, H, T, n16);
+        else k_head_perm16<false><<<g16, kIoThreads, 0, st>>>(s16, d16, pieces, H, T, n16);
+    } else if (split) {
+        k_head_perm<true><<<grid, kIoThreads, 0, st>>>(s, d, rows, H, T, CD, es);
     } else {
-        if (vec) k_head_perm<false, true><<<grid, kIoThreads, 0, st>>>(s, d, rows, H, T, n16, CD, es);
-        else k_head_perm<false, false><<<grid, kIoThreads, 0, st>>>(s, d, rows, H, T, n16, CD, es);
+        k_head_perm<false><<<grid, kIoThreads, 0, st>>>(s, d, rows, H, T, CD, es);
     }
     return io_status(cudaGetLastError());
 }

@@ -16,6 +16,9 @@ Functions (every one cites the definition it follows in ``sdm_oracle.c``):
               bfloat16) snapshot of the rows each chunk writes (memory_ops.py snapshot_quant)
   head_split, head_merge, bank_expand, bank_sum
               the layer I/O around the op (memory_ops.py "Layer I/O"), as array rearranges
+  product_key (module)
+              the exact top-k over product-key slots, the pages' staged selection rule
+              (product_key_topk.py), with its backward
 
 Pins (tests/test_oracle.py): dense brute force, closed forms (scalar delta rule, pure
 decay), chunk-size invariance, the solve identity, brute-force grouping and central

@@ -56,7 +56,7 @@ def test_noalloc_refuses_shapes_beyond_its_scratch():
     if not torch.cuda.is_available():
         pytest.skip("needs a CUDA GPU")
     lib = sdm.library()
-    # config-4-sized chunks need about 26 MB even one step at a time
+    # chunks of P=4, C=256, W=R=256, D=256 need about 26 MB of scratch even one step at a time
     s = sdm.make_shape(4, 16384, 256, 1 << 20, 256, 256, 256, sdm.SDM_BF16)
     fake = ctypes.c_void_p(256)
     rc = lib.sdm_write_read_noalloc(ctypes.byref(s), fake, fake, fake, fake, fake, fake, fake,

@@ -483,7 +483,7 @@ def run_backward(args):
     shape = sdm.make_shape(wl.P, wl.T, wl.C, wl.S, wl.D, wl.W, wl.R, dt,
                            flags=sdm.SNAPSHOT_QUANT[sq])
     ws = sdm.alloc_workspace(shape, dev)
-    nb = sdm.library().sdm_backward_workspace_bytes(__import__("ctypes").byref(shape))
+    nb = sdm.backward_workspace_bytes(shape)
     wsb = torch.empty(nb, dtype=torch.uint8, device=dev)
     saved = torch.empty(sdm.saved_bytes(shape), dtype=torch.uint8, device=dev)
     readings = torch.empty((wl.P, wl.T, wl.D), dtype=dt, device=dev)

@@ -21,7 +21,8 @@ import torch
 
 __all__ = ["FLAG_SNAPSHOT_BF16", "FLAG_TOKEN_GATE", "FLAG_SHARED_BANK", "head_split",
            "head_merge", "bank_expand", "bank_sum", "sdm_write_read", "sdm_write_read_save", "sdm_write_read_backward",
-           "sdm_write_read_noalloc", "profile_write_read", "workspace_bytes", "launch_count",
+           "sdm_write_read_noalloc", "profile_write_read", "workspace_bytes",
+           "backward_workspace_bytes", "launch_count",
            "phase1_debug", "KERNEL_KINDS",
            "device_status", "SdmError", "Shape", "library", "library_path", "version"]
 
@@ -140,6 +141,14 @@ def make_shape(P, T, C, S, D, W, R, dtype, slab_steps: int = 0, flags: int = 0) 
 
 def workspace_bytes(shape: Shape) -> int:
     n = library().sdm_workspace_bytes(ctypes.byref(shape))
+    if n == 0:
+        raise SdmError(-1, library().sdm_last_error().decode())
+    return int(n)
+
+
+def backward_workspace_bytes(shape: Shape) -> int:
+    """Bytes of device workspace sdm_write_read_backward needs for ``shape``."""
+    n = library().sdm_backward_workspace_bytes(ctypes.byref(shape))
     if n == 0:
         raise SdmError(-1, library().sdm_last_error().decode())
     return int(n)
@@ -389,10 +398,7 @@ def sdm_write_read_backward(bank, write_slots, write_w, log_decay, beta, v, read
            "grad_log_decay": torch.empty(gshape, **f32),
            "grad_read_w": torch.empty((P, T, R), **f32)}
     if workspace is None:
-        n = library().sdm_backward_workspace_bytes(ctypes.byref(shape))
-        if n == 0:
-            raise SdmError(-1, library().sdm_last_error().decode())
-        workspace = torch.empty(n, dtype=torch.uint8, device=dev)
+        workspace = torch.empty(backward_workspace_bytes(shape), dtype=torch.uint8, device=dev)
     with torch.cuda.device(dev):
         rc = library().sdm_write_read_backward(
             ctypes.byref(shape), _ptr(bank), _ptr(write_slots), _ptr(write_w), _ptr(log_decay),

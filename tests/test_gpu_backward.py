@@ -157,7 +157,7 @@ def test_backward_workspace_poison():
     wl = small_workload(P=2, T=75, C=32, S=40, D=64, W=8, R=8, ragged=True, seed=37)
     inputs, gr, gf = make_case(wl, True)
     shape = sdm.make_shape(wl.P, wl.T, wl.C, wl.S, wl.D, wl.W, wl.R, torch.float32)
-    n = sdm.library().sdm_backward_workspace_bytes(__import__("ctypes").byref(shape))
+    n = sdm.backward_workspace_bytes(shape)
     results = []
     for fill in (0x00, 0xFF):
         dev = to_device(inputs, wl)

@@ -121,3 +121,27 @@ def test_token_gate_flag():
     assert sdm.workspace_bytes(gated) == sdm.workspace_bytes(plain)
     diff = sdm.host_workspace_bytes(plain) - sdm.host_workspace_bytes(gated)
     assert 4 * 4 * 512 * 15 - 256 <= diff <= 4 * 4 * 512 * 15 + 256
+
+
+def test_binding_infers_flags_from_shapes():
+    """Host logic of the binding (no GPU): the per-token gate from log_decay's shape, the
+    rows of a per-stream or shared bank, the snapshot flag."""
+    import torch
+
+    P, T, W = 3, 10, 4
+    assert sdm._gate(torch.zeros(P, T, W), P, T, W) == (0, (P, T, W))
+    assert sdm._gate(torch.zeros(P, T), P, T, W) == (sdm.FLAG_TOKEN_GATE, (P, T))
+    assert sdm._gate(torch.zeros(P, T, 1), P, T, W) == (sdm.FLAG_TOKEN_GATE, (P, T, 1))
+    assert sdm._gate(torch.zeros(P, T, 1), P, T, 1) == (0, (P, T, 1))   # W = 1: per write
+    bank = torch.zeros(P * 7, 8)
+    assert sdm._bank_rows(bank, P, False) == (7, P * 7, 0)
+    assert sdm._bank_rows(bank, P, True) == (P * 7, P * 7, sdm.FLAG_SHARED_BANK)
+    with pytest.raises(ValueError):
+        sdm._bank_rows(torch.zeros(P * 7 + 1, 8), P, False)
+    assert sdm._snapshot_flag("none") == 0
+    assert sdm._snapshot_flag("bf16") == sdm.FLAG_SNAPSHOT_BF16
+    with pytest.raises(ValueError):
+        sdm._snapshot_flag("fp8")
+    flags = {sdm.FLAG_PER_STEP_KERNELS, sdm.FLAG_SNAPSHOT_BF16, sdm.FLAG_TOKEN_GATE,
+             sdm.FLAG_SHARED_BANK}
+    assert len(flags) == 4 and all(f & (f - 1) == 0 for f in flags)     # distinct bits

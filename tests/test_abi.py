@@ -145,3 +145,13 @@ def test_binding_infers_flags_from_shapes():
     flags = {sdm.FLAG_PER_STEP_KERNELS, sdm.FLAG_SNAPSHOT_BF16, sdm.FLAG_TOKEN_GATE,
              sdm.FLAG_SHARED_BANK}
     assert len(flags) == 4 and all(f & (f - 1) == 0 for f in flags)     # distinct bits
+
+
+def test_binding_flags_match_the_header():
+    hdr = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                            "include", "sdm.h")).read()
+    defs = dict((k, int(v)) for k, v in re.findall(r"#define (SDM_FLAG_\w+) (\d+)", hdr))
+    assert defs == {"SDM_FLAG_PER_STEP_KERNELS": sdm.FLAG_PER_STEP_KERNELS,
+                    "SDM_FLAG_SNAPSHOT_BF16": sdm.FLAG_SNAPSHOT_BF16,
+                    "SDM_FLAG_TOKEN_GATE": sdm.FLAG_TOKEN_GATE,
+                    "SDM_FLAG_SHARED_BANK": sdm.FLAG_SHARED_BANK}

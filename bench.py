@@ -10,6 +10,13 @@ written to flush L2 (both outside the per-step CUDA events).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
+Other measurements (one JSON line each, same timing rules):
+    --workload I                 another of the five workloads (sdm_inputs.WORKLOADS[I])
+    --per-step-kernels           Phase 2 as three kernels per step
+    --backward [--snapshot-quant none|bf16]
+                                 the saving forward + backward (one step = both calls)
+    --layer-io                   the head split/merge and bank expand/sum kernels, in GB/s
+
 With N > 1 (torchrun, one rank per GPU) every rank runs its own copy of the workload
 (different seed): weak scaling, no collective on the data path; value = all ranks' tokens /
 the slowest rank's time. ``--impl reference`` times the CPU oracle (fp64 token loop, plain C)

@@ -3,10 +3,11 @@
 Phase-2 gather/DW achieved HBM bandwidth against the measured peak.
 
 A step is one full sdm_write_read call (Phase 1, solve, and all Nt Phase-2 steps) over the
-workload P=8 streams x T=4096 tokens, C=64, S=65536 x D=128 bf16 bank, W=R=16 Zipf(1.1) slots
-(seeded synthetic inputs, ``sdm_inputs``). The call is captured once in a CUDA graph and
-replayed; before every step the bank is reset from a pristine copy and a 512 MiB buffer is
-written to flush L2 (both outside the per-step CUDA events).
+widest workload: P=4 streams x T=16384 tokens, C=256, S=1048576 x D=256 bf16 bank, W=R=256
+slots per token (half Zipf(1.2), half uniform), slabbed Phase-1 state (seeded synthetic inputs,
+``sdm_inputs``). The call is captured once in a CUDA graph and replayed; before every step the
+bank is reset from a pristine copy and a 512 MiB buffer is written to flush L2 (both outside
+the per-step CUDA events).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -17,10 +18,18 @@ Other measurements (one JSON line each, same timing rules):
                                  the saving forward + backward (one step = both calls)
     --layer-io                   the head split/merge and bank expand/sum kernels, in GB/s
 
+The ``roofline`` object describes the kernel family with the most device time in a call,
+against its own bound: HBM bytes for the gather, DW and fused Phase 2 (one read of every
+distinct row a chunk touches, one write of every distinct row it writes); tensor-core FLOPs for
+the dual matmul (two C x C by C x D products per chunk, against the TF32 rate); FP32 FMA FLOPs
+for the solve (C^3/3 multiply-adds per chunk); and Gram pair terms for Phase 1 (one exp per
+pair of entries of a slot, against the exp unit's rate).
+
 With N > 1 (torchrun, one rank per GPU) every rank runs its own copy of the workload
 (different seed): weak scaling, no collective on the data path; value = all ranks' tokens /
 the slowest rank's time. ``--impl reference`` times the CPU oracle (fp64 token loop, plain C)
-on the host cores instead, rank 0 only.
+on the host cores instead, rank 0 only, on a bounded sample of the workload (the first tokens
+of every stream).
 """
 
 from __future__ import annotations
@@ -51,10 +60,10 @@ FALLBACK_HBM_GBS = 6800.0
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", type=int, default=1, help="index into sdm_inputs.WORKLOADS")
+    ap.add_argument("--workload", type=int, default=4, help="index into sdm_inputs.WORKLOADS")
     ap.add_argument("--profile-steps", type=int, default=3)
     ap.add_argument("--per-step-kernels", action="store_true",
                     help="run Phase 2 as three kernels per step instead of the fused kernel")
@@ -125,6 +134,73 @@ def algorithmic_bytes(wl, inputs):
             g_rows += np.union1d(uw, ur).size
             dw_rows += uw.size
     return {"gather": g_rows * row, "dw": 2 * dw_rows * row, "phase2": (g_rows + dw_rows) * row}
+
+
+def gram_pairs(wl, inputs):
+    """Gram pair terms of the whole call (Phase 1's algorithmic unit): per chunk, every pair of
+    write entries of one slot at tokens u < t (a term of A) and every pair (read of slot s at
+    token t, write of s at token u <= t) (a term of QK). Each term is one exp of a difference of
+    running log-decays, two multiplies and an add."""
+    total = 0
+    C = wl.C
+    for p in range(wl.P):
+        v = int(inputs["valid"][p])
+        for ti in range(wl.Nt):
+            lo, hi = ti * C, min(v, ti * C + C)
+            if hi <= lo:
+                continue
+            w = inputs["write_slots"][p, lo:hi].astype(np.int64)
+            r = inputs["read_slots"][p, lo:hi].astype(np.int64)
+            _, cnt = np.unique(w, return_counts=True)
+            total += int((cnt * (cnt - 1) // 2).sum())
+            tw = np.repeat(np.arange(hi - lo, dtype=np.int64), w.shape[1])
+            key_w = np.sort(w.ravel() * 1024 + tw)
+            tr = np.repeat(np.arange(hi - lo, dtype=np.int64), r.shape[1])
+            rr = r.ravel()
+            total += int((np.searchsorted(key_w, rr * 1024 + tr, side="right")
+                          - np.searchsorted(key_w, rr * 1024, side="left")).sum())
+    return total
+
+
+def kernel_units(wl, inputs, kind, launches_per_call):
+    """(algorithmic units per launch, unit name, bound) of a kernel family; see the module
+    docstring."""
+    es = 4 if wl.dtype == "f32" else 2
+    if kind in ("gather", "dw", "phase2"):
+        alg = algorithmic_bytes(wl, inputs)
+        return alg[kind] / max(1, launches_per_call), "bytes", "hbm"
+    chunks = wl.P * wl.Nt
+    if kind == "dualmm":      # delta_v = X u_pre and readings = QX u_pre per chunk
+        return 2 * 2.0 * wl.C * wl.C * wl.D * chunks / max(1, launches_per_call), "flop", "tensor"
+    if kind == "solve":       # X = (I + L)^-1 (C^3/6 FMA) and QX = QK X (C^3/6 FMA)
+        return 2.0 * (wl.C ** 3 / 3.0) * chunks / max(1, launches_per_call), "flop", "alu"
+    if kind == "phase1":
+        return gram_pairs(wl, inputs) / max(1, launches_per_call), "pair terms", "alu"
+    raise ValueError(kind)
+
+
+def kernel_peak(kind):
+    """(peak, unit, source) for a kernel family's bound on this GPU."""
+    try:
+        mp = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except Exception:
+        mp = {}
+    sm_hz = float(mp.get("sm_max_mhz", 2070.0)) * 1e6
+    if kind in ("gather", "dw", "phase2"):
+        hbm, src = measured_peak()
+        return hbm * 1e9, "GB/s", f"{src} (MEASURED_PEAKS.json hbm_gbs)"
+    if kind == "dualmm":
+        bf16 = float(mp.get("bf16_tflops", 1900.0))
+        return (bf16 * 1e12 * 1.1 / 2.25, "TFLOP/s",
+                f"{'measured' if mp else 'fallback'} bf16 dense {bf16:.0f} TFLOP/s x the nominal "
+                "TF32/bf16 ratio 1.1/2.25")
+    if kind == "solve":
+        return (152 * 128 * 2 * sm_hz, "TFLOP/s",
+                "FP32 FMA: 152 SMs x 128 lanes x 2 flop x max SM clock")
+    if kind == "phase1":
+        return (152 * 16 * sm_hz, "G pair terms/s",
+                "exp unit: 152 SMs x 16 exp per clock x max SM clock, one exp per pair term")
+    raise ValueError(kind)
 
 
 # ------------------------------------------------------------------------------------------
@@ -209,23 +285,57 @@ def traffic_record(kernel: str, workload: str):
 # CPU oracle timing (the reference arm and the cpu_baseline field)
 # ------------------------------------------------------------------------------------------
 
-def time_oracle(wl, inputs, budget_s: float = 10.0, max_reps: int = 5):
+def oracle_sample(wl, inputs, target_s: float):
+    """A bounded sample of the workload for the CPU oracle: the first Ts tokens of every stream
+    (Ts a multiple of C, sized so that one oracle run takes about ``target_s`` seconds on this
+    host; the token loop's cost per token does not depend on the token's position). The bank
+    rows the sample touches are gathered into a compact bank and the sample's slot ids renumbered
+    to match (the oracle copies its whole bank in fp64 on every call; the untouched rows would
+    only add that copy). Returns (fp64 oracle inputs, valid tokens in the sample, Ts, threads)."""
     import oracle
 
-    x = oracle.from_stored(inputs, wl.dtype)
     threads = max(1, min(wl.P, os.cpu_count() or 1))
-    tokens = int(inputs["valid"].sum())
-    times = []
-    t_start = time.perf_counter()
-    while len(times) < max_reps and (not times or time.perf_counter() - t_start < budget_s):
-        t0 = time.perf_counter()
-        oracle.sequential(x["bank"], x["ws"], x["k"], x["g"], x["beta"], x["v"], x["rs"], x["q"],
-                          x["valid"], nthreads=threads)
-        times.append(time.perf_counter() - t0)
+
+    def cut(ts):
+        ws, rs = inputs["write_slots"][:, :ts], inputs["read_slots"][:, :ts]
+        rows = [np.unique(np.concatenate([ws[p].ravel(), rs[p].ravel()])) for p in range(wl.P)]
+        S2 = max(1, max(r.size for r in rows))
+        bank = np.zeros((wl.P * S2, wl.D), inputs["bank"].dtype)
+        ws2, rs2 = np.empty_like(ws), np.empty_like(rs)
+        for p, r in enumerate(rows):
+            bank[p * S2:p * S2 + r.size] = inputs["bank"][p * wl.S + r]
+            ws2[p] = np.searchsorted(r, ws[p])
+            rs2[p] = np.searchsorted(r, rs[p])
+        sub = {k: inputs[k][:, :ts] for k in ("write_w", "log_decay", "beta", "v", "read_w")}
+        sub.update(write_slots=ws2, read_slots=rs2, bank=bank,
+                   valid=np.minimum(inputs["valid"], ts).astype(np.int32))
+        return oracle.from_stored(sub, wl.dtype), int(sub["valid"].sum())
+
+    ts = min(wl.T, wl.C)
+    x, n = cut(ts)
+    t = max(run_oracle(x, threads), 1e-6)
+    ts = int(min(wl.T, max(wl.C, ts * target_s / t // wl.C * wl.C)))
+    x, n = cut(ts)
+    return x, n, ts, threads
+
+
+def run_oracle(x, threads):
+    import oracle
+
+    t0 = time.perf_counter()
+    oracle.sequential(x["bank"], x["ws"], x["k"], x["g"], x["beta"], x["v"], x["rs"], x["q"],
+                      x["valid"], nthreads=threads)
+    return time.perf_counter() - t0
+
+
+def time_oracle(wl, inputs, target_s: float = 3.0, reps: int = 3):
+    x, n, ts, threads = oracle_sample(wl, inputs, target_s)
+    times = [run_oracle(x, threads) for _ in range(reps)]
     t = statistics.median(times)
-    return {"value": tokens / t, "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"the whole workload ({tokens} tokens), fp64 token loop in C, OpenMP over "
-                      f"streams, median of {len(times)} runs ({t:.3f} s each)"}
+    return {"value": n / t, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"the first {ts} of {wl.T} tokens of every stream ({n} tokens; the rows "
+                      "they touch gathered into a compact bank), fp64 token loop in C, OpenMP "
+                      f"over streams, median of {reps} runs ({t:.3f} s each)"}
 
 
 def run_reference(args):
@@ -234,31 +344,23 @@ def run_reference(args):
         return
     wl = si.WORKLOADS[args.workload]
     inputs = si.generate(wl)
-    import oracle
-
-    x = oracle.from_stored(inputs, wl.dtype)
-    threads = max(1, min(wl.P, os.cpu_count() or 1))
-    tokens = int(inputs["valid"].sum())
-
-    def step():
-        t0 = time.perf_counter()
-        oracle.sequential(x["bank"], x["ws"], x["k"], x["g"], x["beta"], x["v"], x["rs"], x["q"],
-                          x["valid"], nthreads=threads)
-        return time.perf_counter() - t0
-
+    # one step = the oracle over a sample of about one second of host work
+    x, n, ts, threads = oracle_sample(wl, inputs, 1.0)
     for _ in range(args.warmup):
-        step()
-    times = [step() for _ in range(args.steps)]
+        run_oracle(x, threads)
+    times = [run_oracle(x, threads) for _ in range(args.steps)]
     t = statistics.mean(times)
-    value = tokens / t
+    value = n / t
+    sample = (f"the first {ts} of {wl.T} tokens of every stream ({n} tokens; the rows they "
+              "touch gathered into a compact bank) per step, fp64 token loop in C, OpenMP over "
+              "streams")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": workload_config(wl, inputs),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                             "sample": f"the whole workload ({tokens} tokens) per step, fp64 "
-                                       "token loop in C, OpenMP over streams"},
+                             "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -380,20 +482,17 @@ def run_ours(args):
     alg = algorithmic_bytes(wl, inputs)
     peak, peak_src = measured_peak()
     dom = max(sdm.KERNEL_KINDS, key=lambda k: fam_ms[k])
-    # algorithmic bank bytes per launch: the per-step kernels move one step's share, the fused
-    # Phase-2 kernel a whole slab's
-    per_launch_alg = {"gather": alg["gather"] / wl.Nt, "dw": alg["dw"] / wl.Nt,
-                      "phase2": alg["phase2"] / max(1, fam_n["phase2"] // args.profile_steps)}
-    if dom in per_launch_alg:
-        per_launch = per_launch_alg[dom]
-        secs = fam_ms[dom] / max(1, fam_n[dom]) / 1e3
-        ach = per_launch / secs / 1e9
-        roofline = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
-                    "frac": ach / peak, "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
-                    "alg_bytes_per_launch": per_launch,
-                    "traffic": traffic_record(dom, wl.name)}
-    else:
-        roofline = {"kernel": dom, "bound": "alu", "note": "dominant kernel is not HBM-bound"}
+    n_per_call = max(1, fam_n[dom] // args.profile_steps)
+    units, unit_name, bound = kernel_units(wl, inputs, dom, n_per_call)
+    secs = fam_ms[dom] / max(1, fam_n[dom]) / 1e3
+    pk, pk_unit, pk_src = kernel_peak(dom)
+    scale = {"GB/s": 1e9, "TFLOP/s": 1e12, "G pair terms/s": 1e9}[pk_unit]
+    ach = units / secs
+    roofline = {"kernel": dom, "bound": bound, "achieved": ach / scale, "peak": pk / scale,
+                "unit": pk_unit, "frac": ach / pk, "peak_source": pk_src,
+                "alg_units_per_launch": units, "alg_unit": unit_name,
+                "launch_us": secs * 1e6,
+                "traffic": traffic_record(dom, wl.name) if bound == "hbm" else None}
     p2_ms = fam_ms["gather"] + fam_ms["dw"] + fam_ms["phase2"]
     p2_secs = p2_ms / args.profile_steps / 1e3
     p2_ach = alg["phase2"] / p2_secs / 1e9

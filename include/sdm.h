@@ -46,7 +46,7 @@ typedef enum {
     SDM_ERR_INVALID = -1,      /* bad argument: null pointer, size out of range */
     SDM_ERR_UNSUPPORTED = -2,  /* valid but not built: e.g. a head_dim without a kernel */
     SDM_ERR_CUDA = -3,         /* a CUDA runtime call failed (message in sdm_last_error) */
-    SDM_ERR_TIMEOUT = -4,      /* reserved: a bounded device-side wait gave up */
+    SDM_ERR_TIMEOUT = -4,      /* device status: a bounded device-side wait gave up */
     SDM_ERR_WORKSPACE = -5,    /* workspace null, too small or not 256-byte aligned */
     SDM_ERR_DEVICE = -6        /* the device reported bad input (sdm_get_device_status) */
 } sdm_status;
@@ -107,7 +107,10 @@ typedef struct {
 
 /* Device status block, read by sdm_get_device_status. */
 typedef struct {
-    int32_t code;                  /* 0, or SDM_ERR_DEVICE when a slot was out of range */
+    int32_t code;                  /* 0; SDM_ERR_DEVICE when a slot was out of range;
+                                      SDM_ERR_TIMEOUT when a kernel's bounded wait on its own
+                                      copies gave up (the kernel then returned early, and the
+                                      bank and readings of the call are incomplete) */
     int32_t first_bad_token;       /* stream-major token index (p*T + t) of a bad slot, or -1 */
     int64_t bad_slots;             /* write/read entries whose slot was outside [0, S) */
     int64_t repeated_write_slots;  /* write entries repeating a slot of their own token */
@@ -290,25 +293,32 @@ int64_t sdm_launch_count(const sdm_shape *shape);
  * or plugin host with its own pool, or a fixed-footprint or real-time service) and cannot call
  * cudaMalloc, or do not want to, as cudaMalloc may synchronize the device. Instead of a caller
  * workspace it uses one static device array of SDM_NOALLOC_SCRATCH_BYTES that lives in the
- * library: the CUDA driver reserves it on every GPU that loads the library, and it stays
- * reserved until the process exits. The caller still provides the bank, the inputs and the
- * readings (same arguments, layouts and results as sdm_write_read, without workspace).
+ * library; once loaded on a GPU it stays reserved there until the process exits. The caller
+ * still provides the bank, the inputs and the readings (same arguments, layouts and results as
+ * sdm_write_read, without workspace).
  *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
- *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress,
- *     with that device current), once per device; make that first call before any CUDA
- *     stream capture.
+ *   - Every call looks up the array's device address (cudaGetSymbolAddress, on the current
+ *     device). Under the CUDA driver's lazy module loading (the default) the first lookup on
+ *     a device is when the driver loads the array and reserves its 16 MiB there, and that
+ *     load can fail like an allocation (SDM_ERR_CUDA). Make the first call at initialization
+ *     time, and before any CUDA stream capture.
  *   - Phase-2 slabs are sized to fit the array (results do not depend on the slab size). A
  *     shape that does not fit even at one step per slab, or an explicit slab_steps that does
  *     not fit, is refused with SDM_ERR_WORKSPACE before any work.
  *   - Every call shares the one array, which keeps the last call's contents; the call clears
  *     what must start at zero itself. Calls whose work overlaps on the GPU (other streams,
  *     other host threads) race on the array: serialize them.
- *   - The device status of such a call is not readable through sdm_get_device_status (slots
- *     outside [0, S) are still never dereferenced). */
+ *   - The device status of the last such call is read with sdm_noalloc_get_device_status
+ *     (slots outside [0, S) are never dereferenced). */
 int sdm_write_read_noalloc(const sdm_shape *shape, void *bank, const int32_t *write_slots,
                            const void *write_w, const float *log_decay, const float *beta,
                            const void *v, const int32_t *read_slots, const void *read_w,
                            const int32_t *valid_tokens, void *readings, void *stream);
+
+/* The device status block of the last sdm_write_read_noalloc call on the current device (it
+ * sits at the start of the static array). Synchronizes the stream. status: host pointer.
+ * Returns SDM_OK, SDM_ERR_INVALID (status NULL) or SDM_ERR_CUDA. No counterpart on the pages. */
+int sdm_noalloc_get_device_status(sdm_device_status *status, void *stream);
 
 /* ---------------------------------------------------------------------------------------
  * Layer I/O around the write/read (memory_ops.py, "Layer I/O: head split / merge and the

@@ -21,7 +21,7 @@ import torch
 
 __all__ = ["FLAG_SNAPSHOT_BF16", "FLAG_TOKEN_GATE", "FLAG_SHARED_BANK", "head_split",
            "head_merge", "bank_expand", "bank_sum", "sdm_write_read", "sdm_write_read_save", "sdm_write_read_backward",
-           "sdm_write_read_noalloc", "profile_write_read", "workspace_bytes",
+           "sdm_write_read_noalloc", "noalloc_device_status", "profile_write_read", "workspace_bytes",
            "backward_workspace_bytes", "launch_count",
            "phase1_debug", "KERNEL_KINDS",
            "device_status", "SdmError", "Shape", "library", "library_path", "version"]
@@ -95,6 +95,8 @@ def library() -> ctypes.CDLL:
             lib.sdm_write_read_host.restype = i32
             lib.sdm_write_read_noalloc.argtypes = [sp] + [vp] * 10 + [vp]
             lib.sdm_write_read_noalloc.restype = i32
+            lib.sdm_noalloc_get_device_status.argtypes = [ctypes.POINTER(_DeviceStatus), vp]
+            lib.sdm_noalloc_get_device_status.restype = i32
             lib.sdm_profile_write_read.argtypes = ([sp] + [vp] * 10 + [vp, sz]
                                                    + [ctypes.POINTER(ctypes.c_float),
                                                       ctypes.POINTER(ctypes.c_int32), vp])
@@ -521,6 +523,17 @@ def device_status(workspace: torch.Tensor, stream=None) -> Dict[str, int]:
     with torch.cuda.device(workspace.device):
         _check(library().sdm_get_device_status(_ptr(workspace), ctypes.byref(st),
                                                _stream_ptr(stream)))
+    return {"code": st.code, "first_bad_token": st.first_bad_token, "bad_slots": st.bad_slots,
+            "repeated_write_slots": st.repeated_write_slots}
+
+
+def noalloc_device_status(device=None, stream=None) -> Dict[str, int]:
+    """The device status block of the last ``sdm_write_read_noalloc`` call on ``device``
+    (default: the current one); synchronizes."""
+    st = _DeviceStatus()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    with torch.cuda.device(dev):
+        _check(library().sdm_noalloc_get_device_status(ctypes.byref(st), _stream_ptr(stream)))
     return {"code": st.code, "first_bad_token": st.first_bad_token, "bad_slots": st.bad_slots,
             "repeated_write_slots": st.repeated_write_slots}
 

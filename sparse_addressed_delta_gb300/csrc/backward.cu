@@ -1,8 +1,8 @@
-// Backward of the chunked SDM write/read (sparse-delta-memory 2.0.0: memory_ops.py module
-// docstring "Backward: Phase 2 in reverse order, then Phase B, the matmuls through the solve,
-// and the Phase-1 backward"; SDMWriteRead.backward's contract: gradients with respect to the
-// bank, v, beta, the write and read weights and the log-decays, the bank restored exactly from
-// the snapshot).
+// Backward of the chunked SDM write/read (sparse-delta-memory 2.0.0 page, memory_ops.py module
+// docstring, "Backward"; SDMWriteRead.backward's contract: gradients with respect to the bank,
+// v, beta, the write and read weights and the log-decays, the bank restored exactly from the
+// snapshot). The steps of the forward are undone from the last to the first; within a step the
+// Phase-2 movers go first, then the products through the solve, then the Phase-1 quantities.
 //
 // Per step ti, in reverse (chunk quantities as in the forward; dB1 = gradient with respect
 // to the bank after the chunk, held in grad_bank, which becomes dB0 in place):

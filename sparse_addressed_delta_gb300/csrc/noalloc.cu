@@ -3,34 +3,22 @@
 // SDM_NOALLOC_SCRATCH_BYTES, which the CUDA driver places when it loads this file's module;
 // the call itself allocates nothing and hands the array's device address to the same launch
 // sequence sdm_write_read runs, with the slab size chosen so that the workspace fits.
-#include <mutex>
-
 #include "sdm_internal.cuh"
 
 namespace {
 
 __device__ __align__(256) unsigned char g_noalloc_scratch[SDM_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 256;
-std::mutex g_mu;
-void *g_scratch_addr[kMaxDevices];   // device address of g_noalloc_scratch, per device ordinal
-
-// The device address of the static scratch on the current device. Host code only knows a
-// host-side stand-in for the symbol, so the address is asked from the runtime once per device,
-// with that device current.
+// The device address of the static scratch on the current device. Host code only holds a
+// host-side stand-in for the symbol, so the address is asked from the runtime, with the device
+// current, on every call: the lookup is a cheap host call once the array is resident, and a new
+// context (after cudaDeviceReset, say) gets its own address instead of a stale one. Under lazy
+// module loading the first lookup on a device is what makes the driver load the array.
 int scratch_address(void **out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return (int)e;
-    if (dev < 0 || dev >= kMaxDevices) return (int)cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_scratch_addr[dev]) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess) return (int)e;
-        g_scratch_addr[dev] = p;
-    }
-    *out = g_scratch_addr[dev];
+    *out = p;
     return 0;
 }
 
@@ -87,4 +75,15 @@ extern "C" int sdm_write_read_noalloc(const sdm_shape *shape, void *bank,
                               cudaGetErrorString((cudaError_t)e));
     return sdm_write_read(&s, bank, write_slots, write_w, log_decay, beta, v, read_slots, read_w,
                           valid_tokens, readings, scratch, cap, stream);
+}
+
+extern "C" int sdm_noalloc_get_device_status(sdm_device_status *status, void *stream) {
+    if (!status) return sdm::set_error(SDM_ERR_INVALID, "status must not be NULL");
+    void *scratch = nullptr;
+    const int e = scratch_address(&scratch);
+    if (e)
+        return sdm::set_error(SDM_ERR_CUDA, "sdm_noalloc_get_device_status: static scratch "
+                              "address: %s", cudaGetErrorString((cudaError_t)e));
+    // the status block sits at the start of the scratch, as it does in a caller workspace
+    return sdm_get_device_status(scratch, status, stream);
 }

@@ -130,10 +130,12 @@ def test_backward_deterministic():
         assert torch.equal(o1[k], o2[k]), k
 
 
-def test_backward_bf16_bank():
-    """bfloat16 bank: gradients within the bf16 forward tolerance."""
-    errs = check(small_workload(P=2, T=100, C=32, S=60, D=64, W=8, R=8, dtype="bf16", seed=36),
-                 tol=5e-2)
+@pytest.mark.parametrize("seed", [36, 37])
+def test_backward_bf16_bank(seed):
+    """bfloat16 bank: every gradient within the bf16 forward tolerance (2e-2) of the oracle's
+    unrounded reverse mode, the bank restored bit for bit."""
+    errs = check(small_workload(P=2, T=100, C=32, S=60, D=64, W=8, R=8, dtype="bf16",
+                                seed=seed), tol=2e-2)
     print(errs)
 
 

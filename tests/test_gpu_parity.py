@@ -171,29 +171,44 @@ def test_repeated_write_slot_is_counted():
     assert sdm.device_status(ws)["repeated_write_slots"] == 1
 
 
-def test_phase1_plan_and_intermediates():
-    """Phase 1 and the solve against the oracle's chunked form, chunk by chunk: the dedup
-    plan bit for bit, the values within float32 rounding."""
-    wl = small_workload(P=2, T=70, C=16, S=20, D=32, W=4, R=3, ragged=True, seed=15)
+def _phase1_launches(wl) -> int:
+    """Phase-1 launches per slab for the shape of ``wl``: 1 with the chunk's scratch on chip,
+    2 when Phase 1 splits into the sort kernel and the row kernel over global scratch (the
+    per-step launch count of one slab is Phase 1 + solve + 3 per step)."""
+    shape = sdm.make_shape(wl.P, wl.T, wl.C, wl.S, wl.D, wl.W, wl.R,
+                           torch.float32 if wl.dtype == "f32" else torch.bfloat16,
+                           wl.Nt, sdm.FLAG_PER_STEP_KERNELS)
+    return sdm.launch_count(shape) - 1 - 3 * wl.Nt
+
+
+def _check_phase1(wl, values=True):
+    """Phase 1 and the solve against the oracle, chunk by chunk: the dedup plan (perm, group
+    starts, owners, group count) bit for bit, and (``values``) lw, gw, dw, lr, qw, A, QK, X and
+    QX within float32 rounding of the oracle's chunked form."""
     inputs = si.generate(wl)
     dev = to_device(inputs, wl)
     out = sdm.phase1_debug(dev["write_slots"], dev["write_w"], dev["log_decay"], dev["beta"],
                            dev["read_slots"], dev["read_w"], dev["valid"], S=wl.S, D=wl.D,
                            chunk_size=wl.C)
     torch.cuda.synchronize()
-    x = oracle.from_stored(inputs, wl.dtype)
-    C, W, R = wl.C, wl.W, wl.R
+    assert sdm.device_status(out["workspace"])["code"] == 0
+    x = oracle.from_stored(inputs, wl.dtype) if values else None
+    C, W = wl.C, wl.W
+    perm, gs, ow = (out[k].cpu().numpy() for k in ("perm", "group_start", "owner"))
+    ng = out["ngroups"].cpu().numpy()
     for ti in range(wl.Nt):
         for p in range(wl.P):
             n = ti * wl.P + p
             nv = int(np.clip(inputs["valid"][p] - ti * C, 0, C))
             pl = oracle.plan(inputs["write_slots"][p, ti * C:ti * C + nv])
             m = nv * W
-            assert out["perm"][n, :m].cpu().numpy().tolist() == pl["perm"].tolist()
-            assert (out["perm"][n, m:] == -1).all()
-            assert out["group_start"][n, :m].cpu().numpy().tolist() == pl["group_start"].tolist()
-            assert out["owner"][n, :m].cpu().numpy().tolist() == pl["owner"].tolist()
-            assert int(out["ngroups"][n]) == pl["groups"]
+            assert np.array_equal(perm[n, :m], pl["perm"]), (ti, p)
+            assert (perm[n, m:] == -1).all()
+            assert np.array_equal(gs[n, :m], pl["group_start"]), (ti, p)
+            assert np.array_equal(ow[n, :m], pl["owner"]), (ti, p)
+            assert int(ng[n]) == pl["groups"]
+            if not values:
+                continue
             _, _, d = oracle.chunked(C, *oracle_args(x), debug=(p, ti))
             for key, ref in (("lw", d["lw"]), ("gw", d["gw"]), ("dw", d["dw"]), ("lr", d["lr"]),
                              ("qw", d["qw"]), ("A", d["A"]), ("QK", d["QK"]), ("X", d["X"]),
@@ -201,6 +216,35 @@ def test_phase1_plan_and_intermediates():
                 got = out[key][n].double().cpu().numpy().reshape(ref.shape)
                 scale = max(np.abs(ref).max(), 1e-30)
                 assert np.abs(got - ref).max() <= 2e-6 * scale + 1e-30, (key, ti, p)
+
+
+def test_phase1_plan_and_intermediates():
+    """The on-chip Phase-1 path (the chunk's scratch in shared memory)."""
+    wl = small_workload(P=2, T=70, C=16, S=20, D=32, W=4, R=3, ragged=True, seed=15)
+    assert _phase1_launches(wl) == 1
+    _check_phase1(wl)
+
+
+@pytest.mark.parametrize("wl,values", [
+    # the ragged workload's chunk shape (C=64, W=R=32, Zipf(1.1))
+    (small_workload(P=2, T=3 * 64 + 9, C=64, S=4096, D=64, W=32, R=32, dtype="bf16",
+                    slots="zipf1.1", ragged=True, seed=16), True),
+    # the forward+backward workload's chunk shape (C=128, W=R=64 uniform), small bank
+    (small_workload(P=2, T=2 * 128 + 50, C=128, S=2048, D=64, W=64, R=64, dtype="f32",
+                    slots="uniform", ragged=True, seed=17), True),
+    # C=256 with the half-Zipf(1.2) mix: hot groups of up to a whole chunk of members
+    (small_workload(P=1, T=300, C=256, S=4096, D=64, W=32, R=32, dtype="bf16", slots="mix",
+                    ragged=False, seed=18), True),
+    # the widest workload's chunk shape (C=256, W=R=256 mix): the plan only (the oracle's
+    # brute-force Gram sums would take minutes at this width)
+    (small_workload(P=1, T=256 + 40, C=256, S=1 << 20, D=64, W=256, R=256, dtype="bf16",
+                    slots="mix", ragged=False, seed=19), False),
+], ids=["c64_w32_zipf", "c128_w64_uniform", "c256_w32_mix", "c256_w256_mix_plan"])
+def test_phase1_split_path(wl, values):
+    """The Phase-1 path over global scratch (sort kernel + row kernel), which the larger
+    workloads take: its dedup plan bit for bit, and the values within float32 rounding."""
+    assert _phase1_launches(wl) == 2
+    _check_phase1(wl, values)
 
 
 @pytest.mark.parametrize("cfg", [1, 2, 3, 4])

@@ -347,6 +347,15 @@ int sdm_bank_expand(const void *param, void *out, int B, long long S, int D, int
  * and rounded once to the dtype (the gradient of the shared parameter bank). B >= 1. */
 int sdm_bank_sum(const void *x, void *out, int B, long long S, int D, int dtype, void *stream);
 
+/* Testing aid: the number of polls after which a kernel's bounded wait for its own bulk copies
+ * gives up (default 2^22, seconds at most), for calls queued after this one, process-wide;
+ * polls < 1 restores the default. A kernel whose wait gives up sets SDM_ERR_TIMEOUT in the
+ * device status, waits (with the default limit) for the copies it has in flight, and returns
+ * early, leaving that call's bank and readings incomplete. Returns the previous limit. The
+ * pages have no counterpart: this exists so that the give-up path can be exercised without
+ * a fault. */
+long long sdm_set_wait_limit(long long polls);
+
 /* Thread-local description of the last refused call or CUDA error ("" if none). */
 const char *sdm_last_error(void);
 

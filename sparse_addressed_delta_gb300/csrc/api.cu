@@ -11,6 +11,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -31,6 +32,12 @@ int fail(int code, const char *fmt, ...) {
 }
 
 }  // namespace
+
+namespace {
+std::atomic<long long> g_wait_limit{kSpinLimit};
+}  // namespace
+
+long long wait_limit() { return g_wait_limit.load(std::memory_order_relaxed); }
 
 int set_error(int code, const char *fmt, ...) {
     va_list ap;
@@ -83,6 +90,7 @@ int check_shape(const sdm_shape *s, Dims &d) {
     d.snapq = ((s->flags & SDM_FLAG_SNAPSHOT_BF16) && d.dtype == SDM_F32) ? 1 : 0;
     d.gate = (s->flags & SDM_FLAG_TOKEN_GATE) ? 1 : 0;
     d.shared = (s->flags & SDM_FLAG_SHARED_BANK) ? 1 : 0;
+    d.spin = wait_limit();
     return SDM_OK;
 }
 
@@ -340,7 +348,13 @@ extern "C" {
 
 const char *sdm_last_error(void) { return g_err; }
 
-const char *sdm_version(void) { return "sdm-gb300 0.1 (sm_103a)"; }
+const char *sdm_version(void) { return "sdm-gb300 0.2 (sm_103a)"; }
+
+long long sdm_set_wait_limit(long long polls) {
+    const long long prev = g_wait_limit.load();
+    g_wait_limit.store(polls < 1 ? kSpinLimit : polls);
+    return prev;
+}
 
 size_t sdm_workspace_bytes(const sdm_shape *shape) {
     Prepared pr;

@@ -22,6 +22,75 @@ constexpr int kBlock = 256;           // threads of the gather and DW blocks
 constexpr int kWarps = kBlock / 32;
 
 // ---------------------------------------------------------------------------------------
+// A lane's piece of a row: N consecutive elements of type T, held as raw 32-bit words and
+// loaded with one vector load, then widened to float32 for the sums (a bfloat16 pair x of a
+// word: low element = x << 16, high element = x & 0xffff0000).
+// ---------------------------------------------------------------------------------------
+template <typename T, int N>
+struct Raw {
+    static constexpr int BYTES = N * (int)sizeof(T);
+    static constexpr int WORDS = BYTES >= 4 ? BYTES / 4 : 1;
+    uint32_t u[WORDS];
+};
+
+template <typename T, int N>
+__device__ __forceinline__ void raw_load(const T *p, Raw<T, N> &r) {
+    constexpr int B = Raw<T, N>::BYTES;
+    if constexpr (B >= 16) {
+#pragma unroll
+        for (int i = 0; i < B / 16; ++i) {
+            const uint4 v = reinterpret_cast<const uint4 *>(p)[i];
+            r.u[4 * i] = v.x; r.u[4 * i + 1] = v.y; r.u[4 * i + 2] = v.z; r.u[4 * i + 3] = v.w;
+        }
+    } else if constexpr (B == 8) {
+        const uint2 v = *reinterpret_cast<const uint2 *>(p);
+        r.u[0] = v.x; r.u[1] = v.y;
+    } else if constexpr (B == 4) {
+        r.u[0] = *reinterpret_cast<const uint32_t *>(p);
+    } else {
+        r.u[0] = *reinterpret_cast<const unsigned short *>(p);
+    }
+}
+
+template <typename T, int N>
+__device__ __forceinline__ void raw_zero(Raw<T, N> &r) {
+#pragma unroll
+    for (int i = 0; i < Raw<T, N>::WORDS; ++i) r.u[i] = 0u;
+}
+
+template <typename T, int N>
+__device__ __forceinline__ void raw_widen(const Raw<T, N> &r, float (&x)[N]) {
+    if constexpr (sizeof(T) == 4) {
+#pragma unroll
+        for (int c = 0; c < N; ++c) x[c] = __uint_as_float(r.u[c]);
+    } else if constexpr (N == 1) {
+        x[0] = __uint_as_float(r.u[0] << 16);
+    } else {
+#pragma unroll
+        for (int c = 0; c < N; c += 2) {
+            x[c] = __uint_as_float(r.u[c / 2] << 16);
+            x[c + 1] = __uint_as_float(r.u[c / 2] & 0xffff0000u);
+        }
+    }
+}
+
+// acc += w * x, two columns at a time with the packed FMA (each half rounded like fmaf)
+template <int N>
+__device__ __forceinline__ void axpy(float (&acc)[N], float w, const float (&x)[N]) {
+    if constexpr (N == 1) {
+        acc[0] = fmaf(w, x[0], acc[0]);
+    } else {
+#pragma unroll
+        for (int c = 0; c < N; c += 2) {
+            const float2 r = __ffma2_rn(make_float2(w, w), make_float2(x[c], x[c + 1]),
+                                        make_float2(acc[c], acc[c + 1]));
+            acc[c] = r.x;
+            acc[c + 1] = r.y;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------------------
 // gather: WPT warps per token split the token's entries; their partial sums are added in
 // warp order (a fixed order, WPT a function of the shape only)
 // ---------------------------------------------------------------------------------------
@@ -288,117 +357,162 @@ __global__ void __launch_bounds__(MM_T) k_dualmm(Dims d, Inputs in, Work w, int 
 }
 
 // ---------------------------------------------------------------------------------------
-// DW: one warp per group (distinct written slot) of each chunk of the step. A warp takes NG
-// groups at once (the next ones of its stride): lane k < NG loads group k's slot, bounds,
-// factor and first member with coalesced-by-lane loads, the warp broadcasts them by shuffle
-// and issues all NG B0 row loads and first-member delta_v loads before any arithmetic (the
-// kernel is bound by the B0 rows in flight per SM: 16 warps x NG). Further
-// members are fetched 32 at a time the same way (lane l loads member l's token and weight).
-// Each row adds its members in sorted order after exp(lend) B0: the order of the sum is that
-// of the group, whatever NG is.
+// DW: every group (distinct written slot) of the step's P chunks.
+//   B[s] = exp(lend_s) B0[s] + sum over the group's members, in sorted order, dw_m delta_v[t_m]
+// in float32, rounded once at the store; one warp writes each element of the row.
+// A CTA owns one chunk and one slice of DS = 32 CPS columns, and first copies the chunk's
+// delta_v slice ([C][DS] float32, at most 128 KB) into shared memory: every delta_v row is read
+// by every group that row's token writes (W groups), so from L2 those few rows would be
+// requested by every SM at once. The CTA's warps then take the chunk's groups in a stride, in
+// the DW order Phase 1 wrote (hot groups first, then by size, so the long member lists spread
+// over the warps). A warp holds the metadata of 32 of its groups (lane l: group l, loaded one
+// batch ahead), loads the B0 slices of U groups before adding any, and reads the members'
+// delta_v from shared memory (member records 32 at a time, one batch ahead).
 // ---------------------------------------------------------------------------------------
-template <typename BT, int CPL>
-__global__ void __launch_bounds__(kBlock, 2) k_dw(Dims d, Inputs in, Work w, int step0, int ti) {
-    constexpr int NG = CPL <= 4 ? 8 : (CPL <= 8 ? 4 : 2);   // 2 NG CPL floats of row data
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int p = blockIdx.y;
+constexpr int DW_T = 1024;                   // threads per DW CTA (32 warps, 64 registers each)
+constexpr int DW_W = DW_T / 32;
+constexpr size_t kDwSmem = 128 * 1024;       // delta_v slice of a chunk in shared memory
+
+// columns per lane of a DW slice: the slice DS = 32 * CPS divides D, and C * DS floats fit in
+// kDwSmem
+__host__ __device__ inline int dw_cps(const Dims &d) {
+    int ds = d.D;
+    while ((size_t)d.C * ds * 4 > kDwSmem && ds > 32) ds >>= 1;
+    return ds / 32;
+}
+
+template <typename BT, int CPS>
+__global__ void __launch_bounds__(DW_T, 1) k_dw(Dims d, Inputs in, Work w, int step0, int ti, int cpp) {
+    extern __shared__ __align__(16) float dvs[];       // [C][DS]
+    constexpr int DS = 32 * CPS;
+    constexpr int RB = CPS * (int)sizeof(BT);
+    constexpr int U = RB >= 32 ? 1 : (RB >= 16 ? 2 : 4);   // B0 slices in flight per warp
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+    const int nsl = d.D / DS;
+    const int pair = blockIdx.x / cpp, ck = blockIdx.x - pair * cpp;
+    const int p = pair / nsl, cs = pair - p * nsl;
     const int n = (ti - step0) * d.P + p;
     const int C = d.C, D = d.D, W = d.W, CW = C * W;
+    const int nv = w.nvalid[n];
+
+    // the chunk's delta_v slice (rows past the valid tokens are never a member's)
+    {
+        const float *src = w.dv + (size_t)p * C * D + (size_t)cs * DS;
+        constexpr int Q = DS / 4;                       // 16-byte pieces per row
+        for (int i = tid; i < nv * Q; i += DW_T) {
+            const int r = i / Q, q = i - r * Q;
+            cp_async16(dvs + r * DS + q * 4, src + (size_t)r * D + q * 4);
+        }
+        cp_async_commit();
+    }
+
     const int ng = w.ngroups[n];
     const int32_t *goff = w.goff + (size_t)n * goff_stride(CW);
     const int32_t *gslot = w.gslot + (size_t)n * CW;
+    const int32_t *gord = w.gord + (size_t)n * CW;
     const float *gfac = w.gfac + (size_t)n * CW;
     const int32_t *perm = w.perm + (size_t)n * CW;
     const float *wdw = w.wdw + (size_t)n * CW;
-    const float *dvp = w.dv + (size_t)p * C * D + lane * CPL;
-    BT *bank = static_cast<BT *>(in.bank) + stream_row0(d, p) * D + lane * CPL;
+    BT *bank = static_cast<BT *>(in.bank) + stream_row0(d, p) * D + (size_t)cs * DS + lane * CPS;
+    const float *dvl = dvs + lane * CPS;
     const unsigned magic = div_magic(W);
-    const int stride = gridDim.x * kWarps;
-    for (int g0 = blockIdx.x * kWarps + warp; g0 < ng; g0 += NG * stride) {
-        // lane k < NG: group g0 + k * stride
-        int msl = -1, mo0 = 0, mo1 = 0, mt = 0;
-        float mf = 0.f, mw = 0.f;
-        if (lane < NG) {
-            const int g = g0 + lane * stride;
-            if (g < ng) {
-                msl = gslot[g];
-                mo0 = goff[g];
-                mo1 = goff[g + 1];
-                mf = gfac[g];
-                mt = div_by(perm[mo0], magic);
-                mw = wdw[mo0];
-                if ((unsigned)msl >= (unsigned)d.S) msl = -1;
-            }
+    const int base = ck * DW_W + warp, stride = cpp * DW_W;
+    const int mine = base < ng ? (ng - base + stride - 1) / stride : 0;
+    const bool snap = in.snap != nullptr;
+
+    // lane l: metadata of this warp's group q + l
+    auto meta = [&](int q, int &sl, int &o0, int &o1, int &t1, float &f, float &w1) {
+        sl = -1; o0 = o1 = t1 = 0; f = w1 = 0.f;
+        if (q + lane < mine) {
+            const int g = gord[base + (q + lane) * stride];
+            sl = gslot[g];
+            if ((unsigned)sl >= (unsigned)d.S) sl = -1;      // the dropped entries' group
+            o0 = goff[g];
+            o1 = goff[g + 1];
+            f = gfac[g];
+            t1 = div_by(perm[o0], magic);
+            w1 = wdw[o0];
         }
-        int sl[NG];
-        float acc[NG][CPL], x[NG][CPL];
-#pragma unroll
-        for (int k = 0; k < NG; ++k) {
-            sl[k] = __shfl_sync(0xffffffffu, msl, k);
-            if (sl[k] >= 0) {
-                load_vec<BT, CPL, false>(bank + (size_t)sl[k] * D, acc[k]);
-            } else {
-#pragma unroll
-                for (int c = 0; c < CPL; ++c) acc[k][c] = 0.f;
-            }
+    };
+    int cslot, co0, co1, ct1, nslot, no0, no1, nt1;
+    float cf, cw1, nf, nw1;
+    meta(0, cslot, co0, co1, ct1, cf, cw1);
+    meta(32, nslot, no0, no1, nt1, nf, nw1);
+    cp_async_wait<0>();
+    __syncthreads();
+
+    for (int b = 0; b < mine; b += 32) {
+        if (b > 0) {
+            cslot = nslot; co0 = no0; co1 = no1; ct1 = nt1; cf = nf; cw1 = nw1;
+            meta(b + 32, nslot, no0, no1, nt1, nf, nw1);
         }
+        const int cnt = mine - b < 32 ? mine - b : 32;
+        for (int k = 0; k < cnt; k += U) {
+            Raw<BT, CPS> r[U];
+            int sl[U];
 #pragma unroll
-        for (int k = 0; k < NG; ++k) {
-            const int t1 = __shfl_sync(0xffffffffu, mt, k);
-            if (sl[k] >= 0) {
-                load_vec<float, CPL, false>(dvp + (size_t)t1 * D, x[k]);
-            } else {
-#pragma unroll
-                for (int c = 0; c < CPL; ++c) x[k][c] = 0.f;
-            }
-        }
-#pragma unroll
-        for (int k = 0; k < NG; ++k) {
-            // the group's bounds, factor and first weight, from lane k
-            const int o0 = __shfl_sync(0xffffffffu, mo0, k);
-            const int o1 = __shfl_sync(0xffffffffu, mo1, k);
-            const float f = __shfl_sync(0xffffffffu, mf, k);
-            const float w1 = __shfl_sync(0xffffffffu, mw, k);
-            if (sl[k] < 0) continue;                                // warp-uniform
-            if (in.snap) {
-                const size_t so = ((size_t)(ti * d.P + p) * CW + (o1 - 1)) * D + lane * CPL;
-                if (d.snapq)   // float32 bank, bfloat16 snapshot
-                    store_vec<__nv_bfloat16, CPL>(static_cast<__nv_bfloat16 *>(in.snap) + so, acc[k]);
-                else
-                    store_vec<BT, CPL>(static_cast<BT *>(in.snap) + so, acc[k]);
+            for (int u = 0; u < U; ++u) {
+                sl[u] = __shfl_sync(0xffffffffu, cslot, (k + u) & 31);
+                if (k + u < cnt && sl[u] >= 0) raw_load(bank + (size_t)sl[u] * D, r[u]);
+                else sl[u] = -1;
             }
 #pragma unroll
-            for (int c = 0; c < CPL; ++c) acc[k][c] = fmaf(w1, x[k][c], acc[k][c] * f);
-            for (int m = o0 + 1; m < o1; m += 32) {
-                const int cnt = o1 - m < 32 ? o1 - m : 32;
-                int pt = 0;
-                float pw = 0.f;
-                if (lane < cnt) {
-                    pt = div_by(perm[m + lane], magic);
-                    pw = wdw[m + lane];
+            for (int u = 0; u < U; ++u) {
+                const int o0 = __shfl_sync(0xffffffffu, co0, (k + u) & 31);
+                const int o1 = __shfl_sync(0xffffffffu, co1, (k + u) & 31);
+                const int t1 = __shfl_sync(0xffffffffu, ct1, (k + u) & 31);
+                const float f = __shfl_sync(0xffffffffu, cf, (k + u) & 31);
+                const float w1 = __shfl_sync(0xffffffffu, cw1, (k + u) & 31);
+                if (sl[u] < 0) continue;                       // warp-uniform
+                float acc[CPS], x[CPS];
+                raw_widen(r[u], acc);
+                if (snap) {
+                    const size_t so = ((size_t)(ti * d.P + p) * CW + (o1 - 1)) * D +
+                                      (size_t)cs * DS + lane * CPS;
+                    if (d.snapq)   // float32 bank, bfloat16 snapshot
+                        store_vec<__nv_bfloat16, CPS>(static_cast<__nv_bfloat16 *>(in.snap) + so, acc);
+                    else
+                        store_vec<BT, CPS>(static_cast<BT *>(in.snap) + so, acc);
                 }
-                for (int u0 = 0; u0 < cnt; u0 += 4) {
-                    float y[4][CPL], wt[4];
+                load_vec<float, CPS, false>(dvl + t1 * DS, x);
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int tu = __shfl_sync(0xffffffffu, pt, (u0 + u) & 31);
-                        wt[u] = __shfl_sync(0xffffffffu, pw, (u0 + u) & 31);
-                        if (u0 + u < cnt) {
-                            load_vec<float, CPL, false>(dvp + (size_t)tu * D, y[u]);
-                        } else {
+                for (int c = 0; c < CPS; ++c) acc[c] = fmaf(w1, x[c], acc[c] * f);
+                // further members in sorted order, records 32 at a time (the next 32 loaded one
+                // batch ahead), 4 delta_v rows read at once
+                int ct = 0;
+                float cwv = 0.f;
+                if (o0 + 1 + lane < o1) {
+                    ct = div_by(perm[o0 + 1 + lane], magic);
+                    cwv = wdw[o0 + 1 + lane];
+                }
+                for (int m = o0 + 1; m < o1; m += 32) {
+                    int nt = 0;
+                    float nwv = 0.f;
+                    if (m + 32 + lane < o1) {
+                        nt = div_by(perm[m + 32 + lane], magic);
+                        nwv = wdw[m + 32 + lane];
+                    }
+                    const int mc = o1 - m < 32 ? o1 - m : 32;
+                    for (int v0 = 0; v0 < mc; v0 += 4) {
+                        float y[4][CPS], wv[4];
 #pragma unroll
-                            for (int c = 0; c < CPL; ++c) y[u][c] = 0.f;
+                        for (int v = 0; v < 4; ++v) {
+                            const int tv = __shfl_sync(0xffffffffu, ct, (v0 + v) & 31);
+                            wv[v] = __shfl_sync(0xffffffffu, cwv, (v0 + v) & 31);
+                            load_vec<float, CPS, false>(dvl + (v0 + v < mc ? tv : 0) * DS, y[v]);
+                        }
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            if (v0 + v >= mc) break;
+#pragma unroll
+                            for (int c = 0; c < CPS; ++c) acc[c] = fmaf(wv[v], y[v][c], acc[c]);
                         }
                     }
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        if (u0 + u >= cnt) break;
-#pragma unroll
-                        for (int c = 0; c < CPL; ++c) acc[k][c] = fmaf(wt[u], y[u][c], acc[k][c]);
-                    }
+                    ct = nt;
+                    cwv = nwv;
                 }
+                store_vec<BT, CPS>(bank + (size_t)sl[u] * D, acc);
             }
-            store_vec<BT, CPL>(bank + (size_t)sl[k] * D, acc[k]);
         }
     }
 }
@@ -438,7 +552,7 @@ __global__ void k_debug_expand(Dims d, Work w, int32_t *perm_out, uint8_t *gs_ou
 // ---------------------------------------------------------------------------------------
 int gather_wpt(const Dims &d) {
     // warps per token: enough warps for the whole GPU, more of them for rows of 512 bytes or
-    // more (measured: 32 warps per SM suit 256-byte rows, 64 the 512-byte ones)
+    // more (32 warps per SM suit 256-byte rows, 64 the 512-byte ones)
     const long tokens = (long)d.P * d.C;
     const int row_bytes = d.D * (d.dtype == SDM_BF16 ? 2 : 4);
     const long target = (row_bytes >= 512 ? 64L : 32L) * kRefSms;
@@ -463,18 +577,32 @@ cudaError_t gather_cpl(const Dims &d, const Inputs &in, const Work &w, int step0
     return cudaGetLastError();
 }
 
+template <typename BT, int CPS>
+cudaError_t dw_cps_launch(const Dims &d, const Inputs &in, const Work &w, int step0, int ti,
+                          cudaStream_t st) {
+    // one 32-warp CTA per SM, the SMs shared out over the (chunk, slice) pairs in whole waves
+    const size_t smem = (size_t)d.C * 32 * CPS * 4;
+    const int pairs = d.P * (d.D / (32 * CPS));
+    int cpp = kRefSms / pairs;
+    const int need = (d.C * d.W + DW_W - 1) / DW_W;
+    if (cpp > need) cpp = need;
+    if (cpp < 1) cpp = 1;
+    auto kern = k_dw<BT, CPS>;
+    set_kernel_smem(kern, smem);
+    kern<<<pairs * cpp, DW_T, smem, st>>>(d, in, w, step0, ti, cpp);
+    return cudaGetLastError();
+}
+
 template <typename BT, int CPL>
 cudaError_t dw_cpl(const Dims &d, const Inputs &in, const Work &w, int step0, int ti,
                    cudaStream_t st) {
-    // two waves of the two CTAs an SM holds (measured best among one to eight CTAs per SM)
-    int gx = (4 * kRefSms + d.P - 1) / d.P;
-    const int max_groups = d.C * d.W;
-    const int need = (max_groups + kWarps - 1) / kWarps;
-    if (gx > need) gx = need;
-    if (gx < 1) gx = 1;
-    dim3 grid(gx, d.P);
-    k_dw<BT, CPL><<<grid, kBlock, 0, st>>>(d, in, w, step0, ti);
-    return cudaGetLastError();
+    switch (dw_cps(d)) {
+        case 1: return dw_cps_launch<BT, 1>(d, in, w, step0, ti, st);
+        case 2: return dw_cps_launch<BT, 2>(d, in, w, step0, ti, st);
+        case 4: return dw_cps_launch<BT, 4>(d, in, w, step0, ti, st);
+        case 8: return dw_cps_launch<BT, 8>(d, in, w, step0, ti, st);
+        default: return dw_cps_launch<BT, 16>(d, in, w, step0, ti, st);
+    }
 }
 
 }  // namespace

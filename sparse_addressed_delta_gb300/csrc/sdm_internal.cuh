@@ -42,7 +42,13 @@ struct Dims {
     int snapq;      // 1: the snapshot of a float32 bank is stored in bfloat16
     int gate;       // 1: one log-decay per token ([P, T]) instead of one per write entry
     int shared;     // 1: one [S, D] bank for all streams (disjoint slot sets), else [P*S, D]
+    long long spin; // mbarrier polls before a kernel's wait for its copies gives up
+                    // (kSpinLimit unless sdm_set_wait_limit changed it); the waits that
+                    // drain a kernel's copies before it returns always use kSpinLimit
 };
+
+// polls a kernel's waits make before giving up (process-wide; sdm_set_wait_limit)
+long long wait_limit();
 
 // first bank row of stream p: its own block of S rows, or row 0 of a shared bank
 __host__ __device__ __forceinline__ size_t stream_row0(const Dims &d, int p) {
@@ -356,11 +362,17 @@ __device__ __forceinline__ bool mbar_try_wait(unsigned long long *bar, unsigned 
         : "memory");
     return ok != 0;
 }
-// Waits for the phase of `parity` to complete; false if it did not within kSpinLimit polls.
-__device__ __forceinline__ bool mbar_wait_bounded(unsigned long long *bar, unsigned parity) {
-    for (long it = 0; it < kSpinLimit; ++it)
+// Waits for the phase of `parity` to complete; false if it did not within `limit` polls.
+__device__ __forceinline__ bool mbar_wait_bounded(unsigned long long *bar, unsigned parity,
+                                                  long long limit = kSpinLimit) {
+    for (long long it = 0; it < limit; ++it)
         if (mbar_try_wait(bar, parity)) return true;
     return false;
+}
+// Orders this thread's earlier shared-memory accesses (generic proxy) before its later bulk
+// copies (async proxy) into the same bytes.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __host__ __device__ __forceinline__ int goff_stride(int CW) { return CW + 4; }

@@ -299,7 +299,19 @@ __device__ void p1_gram_rows(const P1Chunk<WT> &c, int t0, int t1, int warp, int
                 const int pb = __shfl_sync(0xffffffffu, pos, src);
                 const int gb = __shfl_sync(0xffffffffu, gs, src);
                 const int pe = has ? pb : gb;
-                for (int m = gb + hl; m < pe; m += lpr) {
+                // the members' records four lane-strides at a time, all loaded before any is
+                // added (they have distinct tokens, so the order of the adds changes nothing)
+                int m = gb + hl;
+                for (; m + 3 * lpr < pe; m += 4 * lpr) {
+                    float2 tk[4];
+                    float l[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) { tk[u] = c.tkk[m + u * lpr]; l[u] = c.lws[m + u * lpr]; }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        rw[__float_as_int(tk[u].x)] += kb * tk[u].y * expf(lb - l[u]);
+                }
+                for (; m < pe; m += lpr) {
                     const float2 tk = c.tkk[m];
                     rw[__float_as_int(tk.x)] += kb * tk.y * expf(lb - c.lws[m]);
                 }
@@ -334,7 +346,17 @@ __device__ void p1_gram_rows(const P1Chunk<WT> &c, int t0, int t1, int warp, int
                 const int lob = __shfl_sync(0xffffffffu, lo, src);
                 const int hib = __shfl_sync(0xffffffffu, hi, src);
                 const int he = has ? hib : lob - 1;
-                for (int m = lob + hl; m <= he; m += lpr) {
+                int m = lob + hl;
+                for (; m + 3 * lpr <= he; m += 4 * lpr) {
+                    float2 tk[4];
+                    float l[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) { tk[u] = c.tkk[m + u * lpr]; l[u] = c.lws[m + u * lpr]; }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        rw[__float_as_int(tk[u].x)] += qb * tk[u].y * expf(lb - l[u]);
+                }
+                for (; m <= he; m += lpr) {
                     const float2 tk = c.tkk[m];
                     rw[__float_as_int(tk.x)] += qb * tk.y * expf(lb - c.lws[m]);
                 }

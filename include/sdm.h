@@ -250,7 +250,10 @@ int sdm_phase1_debug(const sdm_shape *shape, const int32_t *write_slots, const v
                      float *QX, void *workspace, size_t workspace_bytes, void *stream);
 
 /* Reads the device status block of the last call that used this workspace. Synchronizes
- * the stream. status: host pointer. Returns SDM_OK, or SDM_ERR_CUDA. */
+ * the stream. status: host pointer. Returns SDM_OK, or SDM_ERR_CUDA. The block's code is
+ * SDM_ERR_DEVICE for a slot outside [0, S), or SDM_ERR_TIMEOUT when a kernel's bounded wait
+ * for its own copies gave up (see sdm_set_wait_limit); the call's results are then
+ * incomplete. */
 int sdm_get_device_status(const void *workspace, sdm_device_status *status, void *stream);
 
 /* Bytes of device workspace sdm_write_read_host needs: the sdm_write_read workspace plus a

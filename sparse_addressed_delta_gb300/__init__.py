@@ -23,7 +23,7 @@ __all__ = ["FLAG_SNAPSHOT_BF16", "FLAG_TOKEN_GATE", "FLAG_SHARED_BANK", "head_sp
            "head_merge", "bank_expand", "bank_sum", "sdm_write_read", "sdm_write_read_save", "sdm_write_read_backward",
            "sdm_write_read_noalloc", "noalloc_device_status", "profile_write_read", "workspace_bytes",
            "backward_workspace_bytes", "launch_count",
-           "phase1_debug", "KERNEL_KINDS",
+           "phase1_debug", "KERNEL_KINDS", "set_wait_limit",
            "device_status", "SdmError", "Shape", "library", "library_path", "version"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -111,6 +111,8 @@ def library() -> ctypes.CDLL:
             for name in ("sdm_bank_expand", "sdm_bank_sum"):
                 getattr(lib, name).argtypes = [vp, vp, i32, ctypes.c_longlong, i32, i32, vp]
                 getattr(lib, name).restype = i32
+            lib.sdm_set_wait_limit.argtypes = [ctypes.c_longlong]
+            lib.sdm_set_wait_limit.restype = ctypes.c_longlong
             lib.sdm_last_error.argtypes = []
             lib.sdm_last_error.restype = ctypes.c_char_p
             lib.sdm_version.argtypes = []
@@ -121,6 +123,13 @@ def library() -> ctypes.CDLL:
 
 def version() -> str:
     return library().sdm_version().decode()
+
+
+def set_wait_limit(polls: int) -> int:
+    """Testing aid: the number of polls after which a kernel's bounded wait for its own copies
+    gives up, for calls queued from now on (process-wide; polls < 1 restores the default).
+    Returns the previous limit."""
+    return int(library().sdm_set_wait_limit(int(polls)))
 
 
 def _check(rc: int) -> None:

@@ -265,10 +265,12 @@ __global__ void __launch_bounds__(NP2) k_phase2_pipe(Dims d, Inputs in, Work w, 
         }
         cp_async_mbar_arrive_noinc(barB);
     };
-    // both parts of stage (ls & 1) for step ls
-    auto wait_stage = [&](int ls) {
+    // both parts of stage (ls & 1) for step ls, within `lim` polls each (the compute warps'
+    // waits use the call's limit; the producer's drain before it leaves the default one)
+    auto wait_stage = [&](int ls, long long lim) {
         const unsigned par = (unsigned)(ls >> 1) & 1u;
-        return mbar_wait_bounded(fullA + (ls & 1), par) && mbar_wait_bounded(fullB + (ls & 1), par);
+        return mbar_wait_bounded(fullA + (ls & 1), par, lim) &&
+               mbar_wait_bounded(fullB + (ls & 1), par, lim);
     };
 
     if (tid == 0) {
@@ -287,7 +289,7 @@ __global__ void __launch_bounds__(NP2) k_phase2_pipe(Dims d, Inputs in, Work w, 
         int issued = 0;
         for (int ls = 0; ls < nsteps; ++ls) {
             const int st = ls & 1;
-            if (ls >= 2 && !mbar_wait_bounded(empty + st, (unsigned)((ls - 2) >> 1) & 1u)) {
+            if (ls >= 2 && !mbar_wait_bounded(empty + st, (unsigned)((ls - 2) >> 1) & 1u, d.spin)) {
                 if (lane == 0) atomicCAS(&w.status->code, 0, (int)SDM_ERR_TIMEOUT);
                 break;
             }
@@ -295,7 +297,7 @@ __global__ void __launch_bounds__(NP2) k_phase2_pipe(Dims d, Inputs in, Work w, 
             issued = ls + 1;
         }
         // leave only after the last issued copies of both stages have landed
-        for (int ls = issued - 2 < 0 ? 0 : issued - 2; ls < issued; ++ls) wait_stage(ls);
+        for (int ls = issued - 2 < 0 ? 0 : issued - 2; ls < issued; ++ls) wait_stage(ls, kSpinLimit);
         cp_async_wait<0>();
         return;
     }
@@ -344,7 +346,7 @@ __global__ void __launch_bounds__(NP2) k_phase2_pipe(Dims d, Inputs in, Work w, 
 
     // the first stage; each later one is awaited by the step before it, ahead of its closing
     // barrier
-    if (compute_sync_or(!wait_stage(0))) {
+    if (compute_sync_or(!wait_stage(0, d.spin))) {
         // a stage did not land: report and stop (the producer drains its own copies)
         if (tid == 0) atomicCAS(&w.status->code, 0, (int)SDM_ERR_TIMEOUT);
         return;
@@ -494,7 +496,7 @@ __global__ void __launch_bounds__(NP2) k_phase2_pipe(Dims d, Inputs in, Work w, 
         bool ok_next = true;
         if (ls + 1 < nsteps) {
             // only part A (slots and links) is needed for the early loads
-            ok_next = mbar_wait_bounded(fullA + (st ^ 1), (unsigned)((ls + 1) >> 1) & 1u);
+            ok_next = mbar_wait_bounded(fullA + (st ^ 1), (unsigned)((ls + 1) >> 1) & 1u, d.spin);
             if (ok_next) prefetch(ls + 1, psm + (st ^ 1) * L.bytes);
         }
         if (compute_sync_or(!ok_next)) {
@@ -598,7 +600,7 @@ __global__ void __launch_bounds__(NP2) k_phase2_pipe(Dims d, Inputs in, Work w, 
                 finish(g, o1, acc);
             }
         }
-        const bool ok = ls + 1 < nsteps ? wait_stage(ls + 1) : true;
+        const bool ok = ls + 1 < nsteps ? wait_stage(ls + 1, d.spin) : true;
         if (compute_sync_or(!ok)) {
             if (tid == 0) atomicCAS(&w.status->code, 0, (int)SDM_ERR_TIMEOUT);
             return;

@@ -155,3 +155,13 @@ def test_binding_flags_match_the_header():
                     "SDM_FLAG_SNAPSHOT_BF16": sdm.FLAG_SNAPSHOT_BF16,
                     "SDM_FLAG_TOKEN_GATE": sdm.FLAG_TOKEN_GATE,
                     "SDM_FLAG_SHARED_BANK": sdm.FLAG_SHARED_BANK}
+
+
+def test_wait_limit_setter_round_trips():
+    """sdm_set_wait_limit returns the previous limit; polls < 1 restores the default."""
+    lib = sdm.library()
+    default = lib.sdm_set_wait_limit(0)
+    assert default == 1 << 22
+    assert lib.sdm_set_wait_limit(5) == default
+    assert lib.sdm_set_wait_limit(-3) == 5
+    assert lib.sdm_set_wait_limit(0) == default

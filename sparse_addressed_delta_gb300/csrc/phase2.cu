@@ -5,7 +5,8 @@
 //   gather   retrieved[t] = sum_j gw[t][j] B[s_tj],  inter[t] = sum_i qw[t][i] B[r_ti]
 //            (B = the bank at the start of the chunk), u_pre = beta (v - retrieved);
 //            f32 rows [P][C][D] of u_pre and inter
-//   dual mm  delta_v = X u_pre;  readings = QX u_pre + inter (TF32 tensor cores)
+//   dual mm  delta_v = X u_pre;  readings = QX u_pre + inter (TF32 tensor cores: tcgen05 in
+//            dualmm_tc.cu when C is a multiple of 128, else mma.sync below)
 //   DW       for every written slot s (one group of the sorted write row):
 //            B[s] = exp(lend_s) B[s] + sum_{members m, sorted order} dw_m delta_v[t_m]
 //            in f32, rounded once at the store; the group's single warp is the row's only
@@ -192,7 +193,13 @@ __global__ void __launch_bounds__(kBlock) k_gather(Dims d, Inputs in, Work w, in
         const float bt = in.beta[tok];
 #pragma unroll
         for (int c = 0; c < CPL; ++c) ar[c] = bt * (vv[c] - ar[c]);
-        store_vec<float, CPL>(w.ret + row, ar);
+        if (dualmm_tc_fits(d)) {   // u_pre transposed for the tensor-core dual matmul
+            float *ut = w.ret + ((size_t)p * D + lane * CPL) * C + t;
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) ut[(size_t)c * C] = ar[c];
+        } else {
+            store_vec<float, CPL>(w.ret + row, ar);
+        }
         store_vec<float, CPL>(w.inter + row, ai);
     };
     if constexpr (WPT == 1) {
@@ -631,6 +638,7 @@ cudaError_t launch_dw(const Dims &d, const Inputs &in, const Work &w, int step0,
 
 cudaError_t launch_dualmm(const Dims &d, const Inputs &in, const Work &w, int step0, int ti,
                           cudaStream_t st) {
+    if (dualmm_tc_fits(d)) return launch_dualmm_tc(d, in, w, step0, ti, st);
     const size_t smem =
         sizeof(float) * ((size_t)2 * MM_R * mm_apitch(d.C) + (size_t)mm_kpad(d.C) * MM_UP);
     dim3 grid((d.C + MM_R - 1) / MM_R, (d.D + MM_N - 1) / MM_N, d.P);

@@ -184,6 +184,13 @@ cudaError_t launch_dualmm(const Dims &d, const Inputs &in, const Work &w, int st
                           cudaStream_t st);
 cudaError_t launch_dw(const Dims &d, const Inputs &in, const Work &w, int step0, int ti,
                       cudaStream_t st);
+// the per-step dual matmul on tcgen05 tensor cores (C a multiple of 128); the gather then
+// writes u_pre transposed ([P][D][C], K-major rows for the tensor cores)
+__host__ __device__ inline bool dualmm_tc_fits(const Dims &d) {
+    return d.per_step && d.C % 128 == 0 && d.D % 64 == 0;
+}
+cudaError_t launch_dualmm_tc(const Dims &d, const Inputs &in, const Work &w, int step0, int ti,
+                             cudaStream_t st);
 cudaError_t launch_phase2_fused(const Dims &d, const Inputs &in, const Work &w, int step0,
                                 int nsteps, cudaStream_t st);
 size_t phase2_pipe_smem(const Dims &d);

@@ -350,6 +350,36 @@ int sdm_bank_expand(const void *param, void *out, int B, long long S, int D, int
  * and rounded once to the dtype (the gradient of the shared parameter bank). B >= 1. */
 int sdm_bank_sum(const void *x, void *out, int B, long long S, int D, int dtype, void *stream);
 
+/* ---------------------------------------------------------------------------------------
+ * Product-key exact top-k, the slot selection upstream of the write/read
+ * (product_key_topk.py: the product_key_topk docstring). A row of raw holds F factors side by
+ * side (widths factors[0..F-1]); slot (c_0, .., c_{F-1}) scores the float32 sum of its factor
+ * values in factor order (with bfloat16 input and F > 2 each partial sum rounded to bfloat16
+ * before the next factor is added) and has index lin = (..(c_0 w_1 + c_1) w_2 ..) w_{F-1} +
+ * c_{F-1}. Scores compare as float32, -0 below +0, NaN as -inf. Each factor is ranked by value
+ * (larger column first on ties); stage 0 keeps the first min(k, w_0) ranks; stage f keeps the
+ * best c = min(k, n m) pairs (i, j) of the previous stage's n ranks and the first
+ * m = min(k, w_f) ranks of factor f with (i + 1)(j + 1) <= c, exact ties to the larger i + j,
+ * then the larger i. With bfloat16 input and F > 2 an intermediate stage compares the rounded
+ * partial sum it passes on. The kept kk = min(k, prod(factors)) slots are returned sorted by
+ * lin, with val = the score rounded to the input dtype. Deterministic.
+ *   raw      device [rows, sum(factors)], dtype SDM_F32 or SDM_BF16
+ *   factors  host [F], 1 <= F <= 4, each width 1..4096
+ *   k        1..256
+ *   val      device [rows, kk], dtype
+ *   lin      device [rows, kk] int64
+ * Returns SDM_OK once queued on stream, or a negative sdm_status (nothing queued). */
+int sdm_product_key_topk(const void *raw, long long rows, const int *factors, int F, int k,
+                         int dtype, void *val, int64_t *lin, void *stream);
+
+/* Its backward: grad_raw [rows, sum(factors)] float32 (device, written whole) =
+ * the gradient of val reaching each factor column of each selected slot, added in output
+ * order (the rounding of partial sums passes it unchanged). lin and grad_val [rows, kk] as the
+ * forward returned / takes them (grad_val in dtype); factors, F and k as in the forward. */
+int sdm_product_key_topk_backward(const int64_t *lin, const void *grad_val, long long rows,
+                                  const int *factors, int F, int k, int dtype, float *grad_raw,
+                                  void *stream);
+
 /* Testing aid: the number of polls after which a kernel's bounded wait for its own bulk copies
  * gives up (default 2^22, seconds at most), for calls queued after this one, process-wide;
  * polls < 1 restores the default. A kernel whose wait gives up sets SDM_ERR_TIMEOUT in the

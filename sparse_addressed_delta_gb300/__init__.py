@@ -23,7 +23,8 @@ __all__ = ["FLAG_SNAPSHOT_BF16", "FLAG_TOKEN_GATE", "FLAG_SHARED_BANK", "head_sp
            "head_merge", "bank_expand", "bank_sum", "sdm_write_read", "sdm_write_read_save", "sdm_write_read_backward",
            "sdm_write_read_noalloc", "noalloc_device_status", "profile_write_read", "workspace_bytes",
            "backward_workspace_bytes", "launch_count",
-           "phase1_debug", "KERNEL_KINDS", "set_wait_limit",
+           "phase1_debug", "KERNEL_KINDS", "set_wait_limit", "product_key_topk",
+           "product_key_topk_backward",
            "device_status", "SdmError", "Shape", "library", "library_path", "version"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -111,6 +112,13 @@ def library() -> ctypes.CDLL:
             for name in ("sdm_bank_expand", "sdm_bank_sum"):
                 getattr(lib, name).argtypes = [vp, vp, i32, ctypes.c_longlong, i32, i32, vp]
                 getattr(lib, name).restype = i32
+            ll = ctypes.c_longlong
+            lib.sdm_product_key_topk.argtypes = [vp, ll, ctypes.POINTER(ctypes.c_int), i32, i32,
+                                                 i32, vp, vp, vp]
+            lib.sdm_product_key_topk.restype = i32
+            lib.sdm_product_key_topk_backward.argtypes = [vp, vp, ll, ctypes.POINTER(ctypes.c_int),
+                                                          i32, i32, i32, vp, vp]
+            lib.sdm_product_key_topk_backward.restype = i32
             lib.sdm_set_wait_limit.argtypes = [ctypes.c_longlong]
             lib.sdm_set_wait_limit.restype = ctypes.c_longlong
             lib.sdm_last_error.argtypes = []
@@ -545,6 +553,52 @@ def noalloc_device_status(device=None, stream=None) -> Dict[str, int]:
         _check(library().sdm_noalloc_get_device_status(ctypes.byref(st), _stream_ptr(stream)))
     return {"code": st.code, "first_bad_token": st.first_bad_token, "bad_slots": st.bad_slots,
             "repeated_write_slots": st.repeated_write_slots}
+
+
+# ------------------------------------------------------------------------------------------
+# product-key exact top-k (product_key_topk.py)
+# ------------------------------------------------------------------------------------------
+
+def _factors_arg(factors):
+    f = [int(x) for x in factors]
+    return (ctypes.c_int * len(f))(*f), len(f)
+
+
+def product_key_topk(raw: torch.Tensor, factors, k: int, stream=None):
+    """Exact top-k over product-key slots: raw [..., sum(factors)] float32 or bfloat16 on a GPU
+    -> (val [..., kk] in raw's dtype, lin [..., kk] int64), kk = min(k, prod(factors)), the kept
+    slots sorted by lin. The selection rule is the pages' (include/sdm.h)."""
+    if raw.device.type != "cuda" or not raw.is_contiguous():
+        raise ValueError("raw must be a contiguous CUDA tensor")
+    fa, F = _factors_arg(factors)
+    if raw.shape[-1] != sum(int(x) for x in factors):
+        raise ValueError("raw's last dimension must be sum(factors)")
+    prod = 1
+    for x in factors:
+        prod *= int(x)
+    kk = min(int(k), prod)
+    rows = raw.numel() // raw.shape[-1]
+    val = torch.empty(raw.shape[:-1] + (kk,), dtype=raw.dtype, device=raw.device)
+    lin = torch.empty(raw.shape[:-1] + (kk,), dtype=torch.int64, device=raw.device)
+    with torch.cuda.device(raw.device):
+        _check(library().sdm_product_key_topk(_ptr(raw), rows, fa, F, int(k),
+                                              _dtype_code(raw.dtype), _ptr(val), _ptr(lin),
+                                              _stream_ptr(stream)))
+    return val, lin
+
+
+def product_key_topk_backward(lin: torch.Tensor, grad_val: torch.Tensor, factors, k: int,
+                              stream=None) -> torch.Tensor:
+    """d(loss)/d(raw) [..., sum(factors)] float32 from the forward's lin and grad_val."""
+    fa, F = _factors_arg(factors)
+    ld = sum(int(x) for x in factors)
+    rows = lin.numel() // lin.shape[-1] if lin.dim() else 0
+    grad_raw = torch.empty(lin.shape[:-1] + (ld,), dtype=torch.float32, device=lin.device)
+    with torch.cuda.device(lin.device):
+        _check(library().sdm_product_key_topk_backward(
+            _ptr(lin), _ptr(grad_val.contiguous()), rows, fa, F, int(k),
+            _dtype_code(grad_val.dtype), _ptr(grad_raw), _stream_ptr(stream)))
+    return grad_raw
 
 
 # ------------------------------------------------------------------------------------------

@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libsdm.so")
 SOURCES = ["api.cu", "phase1.cu", "solve.cu", "phase2.cu", "dualmm_tc.cu", "phase2_fused.cu",
-           "noalloc.cu", "backward.cu", "host_io.cu", "layer_io.cu"]
+           "noalloc.cu", "backward.cu", "host_io.cu", "layer_io.cu", "product_key.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-Xptxas", "-warn-spills"]

@@ -165,3 +165,15 @@ def test_wait_limit_setter_round_trips():
     assert lib.sdm_set_wait_limit(5) == default
     assert lib.sdm_set_wait_limit(-3) == 5
     assert lib.sdm_set_wait_limit(0) == default
+
+
+def test_product_key_refusals_and_empty_call():
+    """Bad widths or k are refused before any work; zero rows queue nothing."""
+    lib = sdm.library()
+    f = (ctypes.c_int * 2)(4, 5000)
+    assert lib.sdm_product_key_topk(None, 1, f, 2, 8, 0, None, None, None) == -2
+    f = (ctypes.c_int * 1)(4)
+    assert lib.sdm_product_key_topk(None, 1, f, 1, 300, 0, None, None, None) == -1
+    f5 = (ctypes.c_int * 5)(2, 2, 2, 2, 2)
+    assert lib.sdm_product_key_topk(None, 1, f5, 5, 8, 0, None, None, None) == -1
+    assert lib.sdm_product_key_topk(None, 0, f, 1, 8, 0, None, None, None) == 0

@@ -206,14 +206,15 @@ def backward(bank, ws, k, g, beta, v, rs, q, valid, grad_readings, nthreads: int
             "grad_log_decay": dg, "grad_read_w": dq, "restored_bank": B}
 
 
-SNAPSHOT_MODES = {"none": 0, "bf16": 1}
+SNAPSHOT_MODES = {"none": 0, "bf16": 1, "fp8": 2}
 
 
 def backward_snapshot(bank, ws, k, g, beta, v, rs, q, valid, grad_readings, *, chunk_size: int,
                       snapshot: str = "bf16", nthreads: int = 1, grad_final_bank=None):
     """Reverse mode as the chunked backward runs it from a stored snapshot: chunks in reverse,
     each restoring its written rows to Q(their value at the chunk start) ("none": Q is the
-    identity; "bf16": float32 then bfloat16 rounding, to nearest even), re-running the chunk and
+    identity; "bf16": float32 then bfloat16 rounding, to nearest even; "fp8": float32 then
+    float8_e4m3fn rounding, to nearest even, saturating at 448), re-running the chunk and
     taking its reverse pass. Same outputs as ``backward``; ``restored_bank`` holds Q(initial
     value) on every row a valid token writes."""
     B = _f64(bank).copy()

@@ -559,7 +559,7 @@ static int backward_stream(int T, int S, int D, int W, int R, double *B, const i
  *   2. re-runs the chunk's tokens from that bank, logging their pre-write rows;
  *   3. takes the reverse pass of those tokens (reverse_tokens), which puts the bank back to
  *      its state at step 1 and carries dB to the chunk before.
- * With Q = identity this is the reverse mode above. Q(x) rounds x first to float32 (the
+ * With Q = identity this is the reverse mode above. For "bf16", Q(x) rounds x first to float32 (the
  * precision of the float32 bank the snapshot is taken from), then to bfloat16, to nearest
  * even: add 0x7fff plus the lowest kept bit to the float32 pattern and clear 16 bits.
  * ------------------------------------------------------------------------------------ */
@@ -571,6 +571,28 @@ static double quant_bf16(double x) {
     u &= 0xffff0000u;
     memcpy(&f, &u, sizeof f);
     return (double)f;
+}
+
+/* Q for "fp8" (memory_ops.py: a snapshot row of head_dim float8_e4m3fn elements, no scale):
+ * x rounded to float32, then to the nearest float8_e4m3fn value, ties to the even code, with
+ * magnitudes past the largest finite one (448) saturating to it (the format has no infinity;
+ * saturation keeps a restored row finite). e4m3fn: exponent bias 7, 3 fraction bits, normal
+ * values from 2^-6, subnormal steps of 2^-9. NaN stays NaN. */
+static double quant_fp8(double x) {
+    double a = (double)(float)x;
+    if (a != a) return a;
+    const int neg = a < 0;
+    a = fabs(a);
+    int e;
+    frexp(a, &e);                   /* a = f 2^e, 0.5 <= f < 1: the binade's exponent is e - 1 */
+    double step = ldexp(1.0, (e - 1 < -6 ? -6 : e - 1) - 3);
+    double r = nearbyint(a / step) * step;   /* exact scaling; ties to even (default mode) */
+    if (r > 448.0) r = 448.0;
+    return neg ? -r : r;
+}
+
+static double quant_mode(int mode, double x) {
+    return mode == 1 ? quant_bf16(x) : (mode == 2 ? quant_fp8(x) : x);
 }
 
 static int backward_snapshot_stream(int T, int C, int S, int D, int W, int R, int mode, double *B,
@@ -619,7 +641,7 @@ static int backward_snapshot_stream(int T, int C, int S, int D, int W, int R, in
             for (int j = 0; j < W; ++j) {
                 const double *sr = snap + ((size_t)t * W + j) * D;
                 double *row = B + (size_t)ws[(size_t)t * W + j] * D;
-                for (int e = 0; e < D; ++e) row[e] = mode ? quant_bf16(sr[e]) : sr[e];
+                for (int e = 0; e < D; ++e) row[e] = quant_mode(mode, sr[e]);
             }
         /* 2. re-run the chunk, logging the pre-write rows at their tokens */
         int rc = sequential_stream(t1 - t0, S, D, W, R, B, ws + (size_t)t0 * W,
@@ -635,7 +657,7 @@ static int backward_snapshot_stream(int T, int C, int S, int D, int W, int R, in
 }
 
 /* Reverse mode with a stored snapshot over all streams (arguments as sdm_oracle_backward,
- * plus the chunk size C and mode 0 = "none", 1 = "bf16"). bank: in = initial bank; out = the
+ * plus the chunk size C and mode 0 = "none", 1 = "bf16", 2 = "fp8"). bank: in = initial bank; out = the
  * bank the backward leaves: every row some valid token writes holds Q(its initial value). */
 int sdm_oracle_backward_snapshot(int P, int T, int C, int S, int D, int W, int R, int mode,
                                  double *bank, const int32_t *ws, const double *k,
@@ -644,7 +666,7 @@ int sdm_oracle_backward_snapshot(int P, int T, int C, int S, int D, int W, int R
                                  const double *dout, const double *dbank_final, double *dbank,
                                  double *dv, double *dbeta, double *dk, double *dg, double *dq,
                                  int nthreads) {
-    if (check_sizes(P, T, S, D, W, R) || C < 1 || (mode != 0 && mode != 1)) return ORACLE_EINVAL;
+    if (check_sizes(P, T, S, D, W, R) || C < 1 || mode < 0 || mode > 2) return ORACLE_EINVAL;
     for (int p = 0; p < P; ++p)
         if (valid[p] < 0 || valid[p] > T) return ORACLE_EINVAL;
     int status = ORACLE_OK;

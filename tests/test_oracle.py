@@ -296,6 +296,14 @@ def bf16_of_f32(x):
     return torch.from_numpy(np.asarray(x, np.float64)).float().bfloat16().double().numpy()
 
 
+def fp8_of_f32(x):
+    """float8_e4m3fn rounding (to nearest even) of the float32 value of x, by torch's
+    conversion (finite inputs inside the format's range)."""
+    import torch
+
+    return torch.from_numpy(np.asarray(x, np.float64)).float().to(torch.float8_e4m3fn).double().numpy()
+
+
 @pytest.mark.parametrize("C", [1, 3, 8, 64])
 @pytest.mark.parametrize("with_final", [False, True])
 def test_backward_snapshot_none_is_the_reverse_mode(C, with_final):
@@ -327,11 +335,13 @@ def test_backward_snapshot_bf16_restores_rounded_initial_rows():
         np.testing.assert_array_equal(got["restored_bank"], expect)
 
 
-def test_backward_snapshot_bf16_is_the_reverse_mode_of_the_rounded_bank():
+@pytest.mark.parametrize("mode", ["bf16", "fp8"])
+def test_backward_snapshot_is_the_reverse_mode_of_the_rounded_bank(mode):
     """When no chunk touches a row that an earlier chunk wrote, every chunk starts from the
     rounded initial values of the rows it writes (and of later chunks' rows it reads), so
-    the bf16-snapshot backward equals the exact reverse mode run on the bank whose written
-    rows are rounded beforehand."""
+    the bf16- or fp8-snapshot backward equals the exact reverse mode run on the bank whose
+    written rows are rounded beforehand (torch's conversion)."""
+    rnd = bf16_of_f32 if mode == "bf16" else fp8_of_f32
     P, T, C, S, D, W, R = 2, 24, 6, 40, 3, 2, 3
     Nt = T // C
     K = S // (Nt + 1)                      # chunk c writes slots [cK, (c+1)K); the top K stay unwritten
@@ -354,14 +364,38 @@ def test_backward_snapshot_bf16_is_the_reverse_mode_of_the_rounded_bank():
             written[p * S + ws[p, t]] = True
     y = dict(x)
     y["bank"] = x["bank"].copy()
-    y["bank"][written] = bf16_of_f32(x["bank"][written])
+    y["bank"][written] = rnd(x["bank"][written])
     ref = oracle.backward(*args(y), dO)
-    got = oracle.backward_snapshot(*args(x), dO, chunk_size=C, snapshot="bf16")
+    got = oracle.backward_snapshot(*args(x), dO, chunk_size=C, snapshot=mode)
     for key in GRAD_KEYS + ("restored_bank",):
         np.testing.assert_array_equal(got[key], ref[key], err_msg=key)
     # and the rounding changes the gradients (the snapshot is not silently exact)
     exact = oracle.backward(*args(x), dO)
     assert rel(got["grad_write_w"], exact["grad_write_w"]) > 1e-6
+
+
+def test_backward_snapshot_fp8_restores_rounded_initial_rows():
+    """An fp8 snapshot leaves every row some valid token writes at fp8(its initial value)
+    (torch's float8_e4m3fn conversion, over normal and subnormal magnitudes), every other row
+    untouched; values past the largest finite code saturate to +-448 (the reading for the
+    format without infinity)."""
+    _, x = rand_case(P=2, T=37, S=11, D=4, W=3, R=2, seed=46)
+    rng = np.random.default_rng(47)
+    x["bank"] = x["bank"] * np.exp(rng.uniform(-12, 5, x["bank"].shape))
+    dO = rng.standard_normal((2, 37, 4))
+    written = np.zeros(2 * 11, bool)
+    for p in range(2):
+        for t in range(x["valid"][p]):
+            written[p * 11 + x["ws"][p, t]] = True
+    big = np.flatnonzero(written)[:2]
+    x["bank"][big[0], 0], x["bank"][big[1], 1] = 1000.0, -5000.0
+    b = x["bank"][written]
+    inside = np.abs(b) <= 448
+    expect = x["bank"].copy()
+    expect[written] = np.where(inside, fp8_of_f32(np.clip(b, -448, 448)), np.sign(b) * 448)
+    got = oracle.backward_snapshot(*args(x), dO, chunk_size=8, snapshot="fp8")
+    np.testing.assert_array_equal(got["restored_bank"], expect)
+    assert got["restored_bank"][big[0], 0] == 448.0 and got["restored_bank"][big[1], 1] == -448.0
 
 
 def test_per_token_gate_gradient_is_the_sum_over_writes():

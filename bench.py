@@ -14,7 +14,7 @@ the per-step CUDA events).
 Other measurements (one JSON line each, same timing rules):
     --workload I                 another of the five workloads (sdm_inputs.WORKLOADS[I])
     --per-step-kernels           Phase 2 as three kernels per step
-    --backward [--snapshot-quant none|bf16]
+    --backward [--snapshot-quant none|bf16|fp8]
                                  the saving forward + backward (one step = both calls)
     --layer-io                   the head split/merge and bank expand/sum kernels, in GB/s
 
@@ -72,8 +72,9 @@ def parse_args():
     ap.add_argument("--layer-io", action="store_true",
                     help="time the layer I/O kernels (head split/merge, bank expand/sum) on the "
                          "batch 4 x 8 heads layout of the ragged workload instead")
-    ap.add_argument("--snapshot-quant", choices=["none", "bf16"], default="none",
-                    help="with --backward: store the snapshot of a float32 bank in bfloat16")
+    ap.add_argument("--snapshot-quant", choices=["none", "bf16", "fp8"], default="none",
+                    help="with --backward: store the snapshot in bfloat16 (float32 banks) or "
+                         "float8_e4m3fn")
     ap.add_argument("--ncu-run", type=int, default=0, metavar="K",
                     help="profiling target: run K plain (eager) calls on the workload and exit, "
                          "printing no benchmark line")
@@ -598,15 +599,18 @@ def run_backward(args):
     tokens = int(inputs["valid"].sum())
     args_in = (d["write_slots"], d["write_w"], d["log_decay"], d["beta"], d["v"],
                d["read_slots"], d["read_w"], d["valid"])
-    # the bank the backward leaves: the initial one, or with a bfloat16 snapshot of a float32
-    # bank, its written rows rounded to bfloat16
+    # the bank the backward leaves: the initial one, or with a reduced snapshot its written rows
+    # rounded (bfloat16 of a float32 bank; float8_e4m3fn, saturating, of either)
     restored = bank0
-    if sq == "bf16" and dt == torch.float32:
+    if sq == "fp8" or (sq == "bf16" and dt == torch.float32):
         rows = np.unique(np.concatenate([p * wl.S + inputs["write_slots"][p, :int(v)].ravel()
                                          for p, v in enumerate(inputs["valid"])]))
         idx = torch.from_numpy(rows.astype(np.int64)).to(dev)
         restored = bank0.clone()
-        restored[idx] = bank0[idx].bfloat16().float()
+        if sq == "bf16":
+            restored[idx] = bank0[idx].bfloat16().float()
+        else:
+            restored[idx] = bank0[idx].float().clamp(-448, 448).to(torch.float8_e4m3fn).to(dt)
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
         sdm.sdm_write_read_save(bank, *args_in, chunk_size=wl.C, workspace=ws, readings=readings,

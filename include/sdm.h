@@ -64,8 +64,8 @@ typedef enum { SDM_F32 = 0, SDM_BF16 = 1 } sdm_dtype;
  *   bank_dtype  SDM_F32 or SDM_BF16
  *   slab_steps  Phase-2 steps whose Phase-1 state is held at once; 0 = automatic. The
  *               results do not depend on it (Phase 1 and the solve are per chunk).
- *   flags       0, or any of SDM_FLAG_PER_STEP_KERNELS, SDM_FLAG_SNAPSHOT_BF16,
- *               SDM_FLAG_TOKEN_GATE, SDM_FLAG_SHARED_BANK
+ *   flags       0, or any of SDM_FLAG_PER_STEP_KERNELS, SDM_FLAG_SNAPSHOT_BF16 or
+ *               SDM_FLAG_SNAPSHOT_FP8, SDM_FLAG_TOKEN_GATE, SDM_FLAG_SHARED_BANK
  * P * ceil(T / C) * C must be below 2^31.
  *
  * Phase 2 runs as one persistent kernel per slab in which each CTA owns one stream and one
@@ -85,6 +85,15 @@ typedef enum { SDM_F32 = 0, SDM_BF16 = 1 } sdm_dtype;
  * sdm_write_read_save and sdm_write_read_backward must be given the same flag; the other
  * entry points ignore it. */
 #define SDM_FLAG_SNAPSHOT_BF16 2
+/* Snapshot of the saving forward in fp8 (memory_ops.py sdm_write_read: snapshot_quant "fp8";
+ * phase2_kernels.py quant_row: a row of head_dim float8_e4m3fn elements, no scale). Each
+ * snapshot element is the row's value (float32 for a float32 bank, the bfloat16 value for a
+ * bfloat16 bank) converted to float8_e4m3fn, to nearest even, saturating at +-448 (the format
+ * has no infinity), which makes sdm_saved_bytes a quarter (float32 banks) or half (bfloat16
+ * banks) of the unquantized snapshot; the backward restores each written row to that rounded
+ * value and computes the gradients from it. Not with SDM_FLAG_SNAPSHOT_BF16; like it, give
+ * sdm_write_read_save and sdm_write_read_backward the same flag. */
+#define SDM_FLAG_SNAPSHOT_FP8 16
 /* One log-decay per token (memory_ops.py sdm_write_read: "g: [..., 1] per-token log-decay,
  * or [..., W] one per write"; key_weighted_decay False). log_decay is then [P, T] float32 and
  * applies to every row the token writes; the backward's grad_log_decay is [P, T], the sum of
@@ -154,8 +163,9 @@ int sdm_write_read(const sdm_shape *shape, void *bank, const int32_t *write_slot
 
 /* Bytes of the snapshot a saving forward keeps for the backward: the pre-write (chunk
  * start) row of every written slot of every chunk, Nt * P * C * W rows of D bank-dtype
- * elements (memory_ops.py: the snapshot of the saving forward, snapshot_quant "none"), or of
- * D bfloat16 elements with SDM_FLAG_SNAPSHOT_BF16 (snapshot_quant "bf16"). */
+ * elements (memory_ops.py: the snapshot of the saving forward, snapshot_quant "none"), of
+ * D bfloat16 elements with SDM_FLAG_SNAPSHOT_BF16 (snapshot_quant "bf16"), or of D one-byte
+ * float8_e4m3fn elements with SDM_FLAG_SNAPSHOT_FP8 (snapshot_quant "fp8"). */
 size_t sdm_saved_bytes(const sdm_shape *shape);
 
 /* The saving forward (memory_ops.py SDMWriteRead.forward): sdm_write_read plus the snapshot.

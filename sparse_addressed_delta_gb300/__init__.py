@@ -19,7 +19,7 @@ from typing import Dict, Optional
 
 import torch
 
-__all__ = ["FLAG_SNAPSHOT_BF16", "FLAG_TOKEN_GATE", "FLAG_SHARED_BANK", "head_split",
+__all__ = ["FLAG_SNAPSHOT_BF16", "FLAG_SNAPSHOT_FP8", "FLAG_TOKEN_GATE", "FLAG_SHARED_BANK", "head_split",
            "head_merge", "bank_expand", "bank_sum", "sdm_write_read", "sdm_write_read_save", "sdm_write_read_backward",
            "sdm_write_read_noalloc", "noalloc_device_status", "profile_write_read", "workspace_bytes",
            "backward_workspace_bytes", "launch_count",
@@ -36,7 +36,8 @@ FLAG_PER_STEP_KERNELS = 1
 FLAG_SNAPSHOT_BF16 = 2
 FLAG_TOKEN_GATE = 4
 FLAG_SHARED_BANK = 8
-SNAPSHOT_QUANT = {"none": 0, "bf16": FLAG_SNAPSHOT_BF16}
+FLAG_SNAPSHOT_FP8 = 16
+SNAPSHOT_QUANT = {"none": 0, "bf16": FLAG_SNAPSHOT_BF16, "fp8": FLAG_SNAPSHOT_FP8}
 _STATUS = {0: "SDM_OK", -1: "SDM_ERR_INVALID", -2: "SDM_ERR_UNSUPPORTED", -3: "SDM_ERR_CUDA",
            -4: "SDM_ERR_TIMEOUT", -5: "SDM_ERR_WORKSPACE", -6: "SDM_ERR_DEVICE"}
 
@@ -361,7 +362,8 @@ def sdm_write_read_save(bank, write_slots, write_w, log_decay, beta, v, read_slo
                         snapshot_quant: str = "none", shared_bank: bool = False):
     """The saving forward: sdm_write_read plus the snapshot the backward needs.
     ``snapshot_quant`` "bf16" stores the snapshot of a float32 bank in bfloat16 (half the
-    bytes; the backward then restores the written rows to their rounded values).
+    bytes), "fp8" in float8_e4m3fn (one byte an element, saturating at +-448); the backward
+    then restores the written rows to their rounded values.
     Returns (readings, saved)."""
     flags |= _snapshot_flag(snapshot_quant)
     P, T, W = write_slots.shape

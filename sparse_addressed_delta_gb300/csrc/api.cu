@@ -72,8 +72,10 @@ int check_shape(const sdm_shape *s, Dims &d) {
                     s->bank_dtype);
     if (s->slab_steps < 0) return fail(SDM_ERR_INVALID, "slab_steps must be >= 0");
     if (s->flags & ~(SDM_FLAG_PER_STEP_KERNELS | SDM_FLAG_SNAPSHOT_BF16 | SDM_FLAG_TOKEN_GATE |
-                     SDM_FLAG_SHARED_BANK))
+                     SDM_FLAG_SHARED_BANK | SDM_FLAG_SNAPSHOT_FP8))
         return fail(SDM_ERR_INVALID, "unknown flags 0x%x", (unsigned)s->flags);
+    if ((s->flags & SDM_FLAG_SNAPSHOT_BF16) && (s->flags & SDM_FLAG_SNAPSHOT_FP8))
+        return fail(SDM_ERR_INVALID, "SDM_FLAG_SNAPSHOT_BF16 and SDM_FLAG_SNAPSHOT_FP8 exclude each other");
     if (s->D != 32 && s->D != 64 && s->D != 128 && s->D != 256 && s->D != 512)
         return fail(SDM_ERR_UNSUPPORTED, "head_dim D=%d has no kernel (32, 64, 128, 256, 512)",
                     s->D);
@@ -87,7 +89,8 @@ int check_shape(const sdm_shape *s, Dims &d) {
     d.bwd = 0;
     d.xp = d.C;
     d.per_step = ((s->flags & SDM_FLAG_PER_STEP_KERNELS) || !phase2_fused_fits(d)) ? 1 : 0;
-    d.snapq = ((s->flags & SDM_FLAG_SNAPSHOT_BF16) && d.dtype == SDM_F32) ? 1 : 0;
+    d.snapq = (s->flags & SDM_FLAG_SNAPSHOT_FP8)
+                  ? 2 : (((s->flags & SDM_FLAG_SNAPSHOT_BF16) && d.dtype == SDM_F32) ? 1 : 0);
     d.gate = (s->flags & SDM_FLAG_TOKEN_GATE) ? 1 : 0;
     d.shared = (s->flags & SDM_FLAG_SHARED_BANK) ? 1 : 0;
     d.spin = wait_limit();
@@ -425,7 +428,7 @@ size_t sdm_saved_bytes(const sdm_shape *shape) {
     Dims d;
     if (check_shape(shape, d)) return 0;
     g_err[0] = 0;
-    const size_t es = (d.dtype == SDM_BF16 || d.snapq) ? 2 : 4;
+    const size_t es = d.snapq == 2 ? 1 : ((d.dtype == SDM_BF16 || d.snapq) ? 2 : 4);
     return (size_t)d.Nt * d.P * d.C * d.W * d.D * es;
 }
 

@@ -39,7 +39,7 @@ __device__ __forceinline__ int local_n(const Dims &d, int step0, int ti, int p) 
 
 // ---------------------------------------------------------------------------------------
 // restore: B0 rows of the written slots from the snapshot (one warp per group); a bfloat16
-// snapshot of a float32 bank puts back the rounded rows
+// (float32 banks) or float8_e4m3fn snapshot puts back the rounded rows
 // ---------------------------------------------------------------------------------------
 template <typename BT, int CPL>
 __global__ void __launch_bounds__(NTB) k_b_restore(Dims d, Inputs in, Work w, int step0, int ti) {
@@ -50,16 +50,19 @@ __global__ void __launch_bounds__(NTB) k_b_restore(Dims d, Inputs in, Work w, in
     const int32_t *goff = w.goff + (size_t)n * goff_stride(CW);
     const int32_t *gslot = w.gslot + (size_t)n * CW;
     BT *bank = static_cast<BT *>(in.bank) + stream_row0(d, p) * D + lane * CPL;
-    // the snapshot is in the bank dtype, or (d.snapq, float32 banks) in bfloat16
+    // the snapshot is in the bank dtype, in bfloat16 (d.snapq 1, float32 banks) or in
+    // float8_e4m3fn (d.snapq 2)
     const size_t s0 = (size_t)(ti * d.P + p) * CW * D + lane * CPL;
     const BT *snap = static_cast<const BT *>(in.snap) + s0;
     const __nv_bfloat16 *snaph = static_cast<const __nv_bfloat16 *>(in.snap) + s0;
+    const unsigned char *snap8 = static_cast<const unsigned char *>(in.snap) + s0;
     for (int g = blockIdx.x * NWB + warp; g < ng; g += gridDim.x * NWB) {
         const int sl = gslot[g];
         if ((unsigned)sl >= (unsigned)d.S) continue;
         float x[CPL];
         const size_t ro = (size_t)(goff[g + 1] - 1) * D;
-        if (d.snapq) load_vec<__nv_bfloat16, CPL, false>(snaph + ro, x);
+        if (d.snapq == 2) load_fp8<CPL>(snap8 + ro, x);
+        else if (d.snapq) load_vec<__nv_bfloat16, CPL, false>(snaph + ro, x);
         else load_vec<BT, CPL, false>(snap + ro, x);
         store_vec<BT, CPL>(bank + (size_t)sl * D, x);
     }

@@ -476,7 +476,9 @@ __global__ void __launch_bounds__(DW_T, 1) k_dw(Dims d, Inputs in, Work w, int s
                 if (snap) {
                     const size_t so = ((size_t)(ti * d.P + p) * CW + (o1 - 1)) * D +
                                       (size_t)cs * DS + lane * CPS;
-                    if (d.snapq)   // float32 bank, bfloat16 snapshot
+                    if (d.snapq == 2)        // float8_e4m3fn snapshot
+                        store_fp8<CPS>(static_cast<unsigned char *>(in.snap) + so, acc);
+                    else if (d.snapq)        // float32 bank, bfloat16 snapshot
                         store_vec<__nv_bfloat16, CPS>(static_cast<__nv_bfloat16 *>(in.snap) + so, acc);
                     else
                         store_vec<BT, CPS>(static_cast<BT *>(in.snap) + so, acc);

@@ -536,7 +536,9 @@ __global__ void __launch_bounds__(NP2) k_phase2_pipe(Dims d, Inputs in, Work w, 
                     dwout[g] = packed;
                     if (in.snap) {
                         const size_t so = ((size_t)(ti * d.P + p) * CW + (o1 - 1)) * D + c0;
-                        if (d.snapq)   // float32 bank, bfloat16 snapshot: 4 columns, 8 bytes
+                        if (d.snapq == 2)      // float8_e4m3fn snapshot: V bytes
+                            store_fp8<V>(static_cast<unsigned char *>(in.snap) + so, b0);
+                        else if (d.snapq)      // float32 bank, bfloat16 snapshot: 4 columns, 8 bytes
                             store_vec<__nv_bfloat16, V>(static_cast<__nv_bfloat16 *>(in.snap) + so, b0);
                         else
                             *reinterpret_cast<uint4 *>(static_cast<BT *>(in.snap) + so) = braw;
@@ -575,10 +577,14 @@ __global__ void __launch_bounds__(NP2) k_phase2_pipe(Dims d, Inputs in, Work w, 
                         reinterpret_cast<BT *>(dwout + g)[c] = o;
                         if (in.snap) {
                             const size_t so = ((size_t)(ti * d.P + p) * CW + (o1 - 1)) * D + c0 + c;
-                            if (d.snapq)
+                            if (d.snapq == 2) {
+                                const float one[1] = {to_f32(b0)};
+                                store_fp8<1>(static_cast<unsigned char *>(in.snap) + so, one);
+                            } else if (d.snapq) {
                                 static_cast<__nv_bfloat16 *>(in.snap)[so] = __float2bfloat16_rn(to_f32(b0));
-                            else
+                            } else {
                                 static_cast<BT *>(in.snap)[so] = b0;
+                            }
                         }
                     }
                 });

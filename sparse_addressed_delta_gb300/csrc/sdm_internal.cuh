@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -39,7 +40,8 @@ struct Dims {
     int bwd;        // 1: Phase 1 also keeps what the backward reads (sorted rows, read plan)
     int xp;         // row pitch (floats) of X and QX in the workspace: C + 4 for the pipelined
                     // Phase 2 (one bulk copy lands rows at a bank-conflict-free pitch), else C
-    int snapq;      // 1: the snapshot of a float32 bank is stored in bfloat16
+    int snapq;      // snapshot elements: 0 the bank dtype, 1 bfloat16 (float32 banks),
+                    // 2 float8_e4m3fn (either bank dtype)
     int gate;       // 1: one log-decay per token ([P, T]) instead of one per write entry
     int shared;     // 1: one [S, D] bank for all streams (disjoint slot sets), else [P*S, D]
     long long spin; // mbarrier polls before a kernel's wait for its copies gives up
@@ -278,6 +280,44 @@ __device__ __forceinline__ void store_vec(T *p, const float (&x)[N]) {
         *reinterpret_cast<unsigned *>(p) = *reinterpret_cast<const unsigned *>(tmp);
     } else {
         p[0] = tmp[0];
+    }
+}
+
+// N consecutive float8_e4m3fn snapshot elements (N a power of two, 1..16; p aligned to N
+// bytes): converted to nearest even, saturating at the largest finite value, and back
+template <int N>
+__device__ __forceinline__ void store_fp8(unsigned char *p, const float (&x)[N]) {
+    alignas(16) unsigned char b[N < 2 ? 2 : N];
+    if constexpr (N == 1) {
+        b[0] = (unsigned char)__nv_cvt_float_to_fp8(x[0], __NV_SATFINITE, __NV_E4M3);
+        p[0] = b[0];
+    } else {
+#pragma unroll
+        for (int c = 0; c < N; c += 2) {
+            const __nv_fp8x2_storage_t two =
+                __nv_cvt_float2_to_fp8x2(make_float2(x[c], x[c + 1]), __NV_SATFINITE, __NV_E4M3);
+            b[c] = (unsigned char)(two & 0xff);
+            b[c + 1] = (unsigned char)(two >> 8);
+        }
+        if constexpr (N == 2) *reinterpret_cast<unsigned short *>(p) = *reinterpret_cast<unsigned short *>(b);
+        else if constexpr (N == 4) *reinterpret_cast<unsigned *>(p) = *reinterpret_cast<unsigned *>(b);
+        else if constexpr (N == 8) *reinterpret_cast<uint2 *>(p) = *reinterpret_cast<uint2 *>(b);
+        else *reinterpret_cast<uint4 *>(p) = *reinterpret_cast<uint4 *>(b);
+    }
+}
+
+template <int N>
+__device__ __forceinline__ void load_fp8(const unsigned char *p, float (&x)[N]) {
+    alignas(16) unsigned char b[N < 2 ? 2 : N];
+    if constexpr (N == 1) b[0] = p[0];
+    else if constexpr (N == 2) *reinterpret_cast<unsigned short *>(b) = *reinterpret_cast<const unsigned short *>(p);
+    else if constexpr (N == 4) *reinterpret_cast<unsigned *>(b) = *reinterpret_cast<const unsigned *>(p);
+    else if constexpr (N == 8) *reinterpret_cast<uint2 *>(b) = *reinterpret_cast<const uint2 *>(p);
+    else *reinterpret_cast<uint4 *>(b) = *reinterpret_cast<const uint4 *>(p);
+#pragma unroll
+    for (int c = 0; c < N; ++c) {
+        const __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)b[c], __NV_E4M3);
+        x[c] = __half2float(__half(h));
     }
 }
 

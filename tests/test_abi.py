@@ -64,7 +64,7 @@ def test_launch_count():
 
 @pytest.mark.parametrize("kw,code", [
     (dict(C=8), -1), (dict(C=300), -1), (dict(W=0), -1), (dict(R=257), -1), (dict(P=0), -1),
-    (dict(T=0), -1), (dict(S=0), -1), (dict(D=96), -2), (dict(dtype=7), -1), (dict(flags=16), -1),
+    (dict(T=0), -1), (dict(S=0), -1), (dict(D=96), -2), (dict(dtype=7), -1), (dict(flags=32), -1),
     (dict(P=1 << 16, T=1 << 16), -1)])
 def test_refusals(kw, code):
     base = dict(P=2, T=64, C=16, S=128, D=64, W=4, R=4, dtype=sdm.SDM_F32, flags=0)
@@ -110,7 +110,7 @@ def test_bf16_snapshot_halves_saved_bytes():
         assert plain == 7 * 3 * 16 * 3 * 64 * (4 if dt == sdm.SDM_F32 else 2)
         assert plain == ratio * half
     with pytest.raises(sdm.SdmError):
-        sdm.saved_bytes(sdm.make_shape(3, 100, 16, 50, 64, 3, 4, sdm.SDM_F32, flags=16))
+        sdm.saved_bytes(sdm.make_shape(3, 100, 16, 50, 64, 3, 4, sdm.SDM_F32, flags=32))
 
 
 def test_token_gate_flag():
@@ -154,7 +154,8 @@ def test_binding_flags_match_the_header():
     assert defs == {"SDM_FLAG_PER_STEP_KERNELS": sdm.FLAG_PER_STEP_KERNELS,
                     "SDM_FLAG_SNAPSHOT_BF16": sdm.FLAG_SNAPSHOT_BF16,
                     "SDM_FLAG_TOKEN_GATE": sdm.FLAG_TOKEN_GATE,
-                    "SDM_FLAG_SHARED_BANK": sdm.FLAG_SHARED_BANK}
+                    "SDM_FLAG_SHARED_BANK": sdm.FLAG_SHARED_BANK,
+                    "SDM_FLAG_SNAPSHOT_FP8": sdm.FLAG_SNAPSHOT_FP8}
 
 
 def test_wait_limit_setter_round_trips():
@@ -177,3 +178,16 @@ def test_product_key_refusals_and_empty_call():
     f5 = (ctypes.c_int * 5)(2, 2, 2, 2, 2)
     assert lib.sdm_product_key_topk(None, 1, f5, 5, 8, 0, None, None, None) == -1
     assert lib.sdm_product_key_topk(None, 0, f, 1, 8, 0, None, None, None) == 0
+
+
+def test_fp8_snapshot_sizes_and_refusals():
+    """An fp8 snapshot holds one byte an element (a quarter of a float32 bank's snapshot, half
+    of a bfloat16 bank's); the two reduced snapshots exclude each other."""
+    import torch
+    for dt, ratio in ((torch.float32, 4), (torch.bfloat16, 2)):
+        full = sdm.make_shape(2, 64, 16, 100, 64, 4, 3, dt)
+        fp8 = sdm.make_shape(2, 64, 16, 100, 64, 4, 3, dt, flags=sdm.FLAG_SNAPSHOT_FP8)
+        assert sdm.saved_bytes(full) == ratio * sdm.saved_bytes(fp8)
+    both = sdm.make_shape(2, 64, 16, 100, 64, 4, 3, torch.float32,
+                          flags=sdm.FLAG_SNAPSHOT_FP8 | sdm.FLAG_SNAPSHOT_BF16)
+    assert sdm.library().sdm_workspace_bytes(ctypes.byref(both)) == 0

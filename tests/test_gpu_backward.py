@@ -287,3 +287,70 @@ def test_bf16_snapshot_is_deterministic_and_halves_the_snapshot():
     half = sdm.make_shape(wl.P, wl.T, wl.C, wl.S, wl.D, wl.W, wl.R, torch.float32,
                           flags=sdm.FLAG_SNAPSHOT_BF16)
     assert sdm.saved_bytes(shape) == 2 * sdm.saved_bytes(half)
+
+
+# ---------------------------------------------------------------------------------------
+# float8_e4m3fn snapshot (SDM_FLAG_SNAPSHOT_FP8; memory_ops.py snapshot_quant "fp8")
+# ---------------------------------------------------------------------------------------
+
+def fp8_rows(x: np.ndarray) -> np.ndarray:
+    """float8_e4m3fn rounding (nearest even, saturating at +-448) of float32 rows, by torch's
+    conversion of the clamped values."""
+    t = torch.from_numpy(np.ascontiguousarray(x, np.float32)).clamp(-448, 448)
+    return t.to(torch.float8_e4m3fn).float().numpy()
+
+
+def oracle_snapshot_mode(wl, inputs, gr, mode):
+    x = oracle.from_stored(inputs, wl.dtype)
+    return oracle.backward_snapshot(x["bank"], x["ws"], x["k"], x["g"], x["beta"], x["v"],
+                                    x["rs"], x["q"], x["valid"],
+                                    si.stored_to_f64(gr, wl.dtype), chunk_size=wl.C,
+                                    snapshot=mode)
+
+
+@pytest.mark.parametrize("flags", [0, sdm.FLAG_PER_STEP_KERNELS])
+@pytest.mark.parametrize("bank_dtype", ["f32", "bf16"])
+def test_fp8_snapshot_matches_the_oracle(flags, bank_dtype):
+    """Gradients within the bank dtype's tolerance of the oracle's reverse pass from an fp8
+    snapshot; the restored bank bit for bit: fp8(initial) on the written rows, initial
+    elsewhere (no chunk touches a row an earlier chunk wrote, so both sides round the same
+    initial values)."""
+    wl, inputs, gr = separated_case(P=3, T=64, C=16, S=100, D=64, W=4, R=3, seed=71)
+    if bank_dtype == "bf16":
+        wl = wl.replace(dtype="bf16")
+        for k in ("bank", "write_w", "v", "read_w"):
+            inputs[k] = si.to_stored(inputs[k].astype(np.float64), "bf16")
+        gr = si.to_stored(si.stored_to_f64(gr, "f32"), "bf16")
+    _, bank, _, out = gpu_backward(wl, inputs, gr, flags=flags, snapshot_quant="fp8")
+    ref = oracle_snapshot_mode(wl, inputs, gr, "fp8")
+    w = written_rows(inputs, wl.S)
+    b0 = si.stored_to_f64(inputs["bank"], wl.dtype).astype(np.float32)
+    expect = b0.copy()
+    expect[w] = fp8_rows(b0[w])
+    assert np.array_equal(bank.float().cpu().numpy(), expect)
+    assert np.array_equal(ref["restored_bank"].astype(np.float32), expect)
+    errs = errors(out, ref)
+    tol = 1e-4 if bank_dtype == "f32" else 2e-2
+    assert all(v <= tol for v in errs.values()), errs
+
+
+@pytest.mark.parametrize("flags", [0, sdm.FLAG_PER_STEP_KERNELS])
+def test_fp8_snapshot_general_slots(flags):
+    """Zipf slots rewritten across chunks, ragged tokens, slabs: the restored bank is
+    fp8(initial) on every written row, bit for bit, and the run is deterministic. (Gradients
+    are not compared here: an intermediate row at an fp8 rounding boundary can round one way
+    from the GPU's float32 value and the other from the oracle's fp64 value, a step of up to
+    one part in sixteen.)"""
+    wl = small_workload(P=2, T=90, C=16, S=30, D=64, W=4, R=3, dtype="f32", ragged=True,
+                        seed=72)
+    inputs, gr, _ = make_case(wl)
+    _, bank, _, out = gpu_backward(wl, inputs, gr, slab_steps=2, flags=flags,
+                                   snapshot_quant="fp8")
+    w = written_rows(inputs, wl.S)
+    expect = inputs["bank"].copy()
+    expect[w] = fp8_rows(inputs["bank"][w])
+    assert np.array_equal(bank.cpu().numpy(), expect)
+    _, _, _, out2 = gpu_backward(wl, inputs, gr, slab_steps=2, flags=flags,
+                                 snapshot_quant="fp8")
+    for k in GRADS:
+        assert torch.equal(out[k], out2[k]), k

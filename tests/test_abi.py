@@ -140,11 +140,12 @@ def test_binding_infers_flags_from_shapes():
         sdm._bank_rows(torch.zeros(P * 7 + 1, 8), P, False)
     assert sdm._snapshot_flag("none") == 0
     assert sdm._snapshot_flag("bf16") == sdm.FLAG_SNAPSHOT_BF16
+    assert sdm._snapshot_flag("fp8") == sdm.FLAG_SNAPSHOT_FP8
     with pytest.raises(ValueError):
-        sdm._snapshot_flag("fp8")
+        sdm._snapshot_flag("int4")                # not built: the pages give no scale scheme
     flags = {sdm.FLAG_PER_STEP_KERNELS, sdm.FLAG_SNAPSHOT_BF16, sdm.FLAG_TOKEN_GATE,
-             sdm.FLAG_SHARED_BANK}
-    assert len(flags) == 4 and all(f & (f - 1) == 0 for f in flags)     # distinct bits
+             sdm.FLAG_SHARED_BANK, sdm.FLAG_SNAPSHOT_FP8}
+    assert len(flags) == 5 and all(f & (f - 1) == 0 for f in flags)     # distinct bits
 
 
 def test_binding_flags_match_the_header():

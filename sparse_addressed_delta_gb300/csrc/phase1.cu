@@ -172,6 +172,95 @@ __device__ int int_scan(int val, int carry_in, int &carry, P1Smem &sm) {
     return out;
 }
 
+// Chunks whose scratch is in global memory work on tiles of G4 = 4 NT entries: four per
+// thread, so that each thread has four global loads in flight and a tile costs one round of
+// barriers for four times the entries.
+constexpr int IT4 = 4;
+constexpr int G4 = IT4 * NT;
+
+// shared memory of those chunks after P1Smem: the per-(item, warp, digit) counts of a radix
+// tile, and the scans' per-thread results
+struct P1Big {
+    int wc[IT4][NW][256];
+    float tv[NT];
+    int ti[NT];
+};
+
+// One stable counting pass of the LSD radix sort over tiles of G4 keys: key k of thread tid in
+// a tile is at position tile + k NT + tid (k-major, so the order (k, warp, lane) is the position
+// order). A key's rank among equal digits of its warp and item (match_any) plus the counts of
+// the earlier (item, warp) pairs of the tile and of the earlier tiles gives its place.
+__device__ void radix_pass4(const unsigned long long *in, unsigned long long *out, int n,
+                            int shift, P1Smem &sm, P1Big &bg) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int *wcf = &bg.wc[0][0][0];
+    for (int i = tid; i < 256; i += NT) sm.hist[i] = 0;
+    for (int i = tid; i < IT4 * NW * 256; i += NT) wcf[i] = 0;
+    __syncthreads();
+    for (int i0 = tid; i0 < n; i0 += G4) {
+        unsigned long long kk[IT4];
+#pragma unroll
+        for (int k = 0; k < IT4; ++k) kk[k] = i0 + k * NT < n ? in[i0 + k * NT] : 0ull;
+#pragma unroll
+        for (int k = 0; k < IT4; ++k)
+            if (i0 + k * NT < n) atomicAdd(&sm.hist[(int)((kk[k] >> shift) & 255ull)], 1);
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int v[8], s = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) { v[k] = sm.hist[lane * 8 + k]; s += v[k]; }
+        int incl = s;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += y;
+        }
+        int run = incl - s;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) { sm.base[lane * 8 + k] = run; run += v[k]; }
+    }
+    __syncthreads();
+    for (int tile = 0; tile < n; tile += G4) {
+        unsigned long long kk[IT4];
+        int dg[IT4], rank[IT4];
+#pragma unroll
+        for (int k = 0; k < IT4; ++k) {
+            const int i = tile + k * NT + tid;
+            kk[k] = i < n ? in[i] : 0ull;
+        }
+#pragma unroll
+        for (int k = 0; k < IT4; ++k) {
+            const int i = tile + k * NT + tid;
+            dg[k] = i < n ? (int)((kk[k] >> shift) & 255ull) : 256;
+            const unsigned peers = __match_any_sync(0xffffffffu, dg[k]);
+            rank[k] = __popc(peers & ((1u << lane) - 1u));
+            if (dg[k] < 256 && lane == __ffs(peers) - 1) bg.wc[k][warp][dg[k]] = __popc(peers);
+        }
+        __syncthreads();
+        for (int dd = tid; dd < 256; dd += NT) {
+            int run = 0;
+#pragma unroll
+            for (int k = 0; k < IT4; ++k)
+#pragma unroll
+                for (int w2 = 0; w2 < NW; ++w2) {
+                    const int c = bg.wc[k][w2][dd];
+                    bg.wc[k][w2][dd] = run;
+                    run += c;
+                }
+            sm.tile_total[dd] = run;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < IT4; ++k)
+            if (dg[k] < 256) out[sm.base[dg[k]] + bg.wc[k][warp][dg[k]] + rank[k]] = kk[k];
+        __syncthreads();
+        for (int dd = tid; dd < 256; dd += NT) sm.base[dd] += sm.tile_total[dd];
+        for (int i = tid; i < IT4 * NW * 256; i += NT) wcf[i] = 0;
+        __syncthreads();
+    }
+}
+
 __device__ __forceinline__ void report_bad_slot(DevStatus *st, int token) {
     atomicAdd(&st->bad_slots, 1ull);
     atomicCAS(&st->first_bad_plus1, 0, token + 1);
@@ -425,8 +514,10 @@ __global__ void __launch_bounds__(NT, 2) k_phase1(Dims d, Inputs in, Work w, int
     }
     unsigned long long *keyB = keyA + CW;
     // chunks whose scratch lives in global memory leave steps 3 and 4 to k_phase1_rows (the
-    // grid then has one CTA per chunk, so the scratch of chunk n stays in slot n)
+    // grid then has one CTA per chunk, so the scratch of chunk n stays in slot n), and work on
+    // tiles of G4 entries with the counts and scan values after P1Smem
     const bool split = !scratch_in_smem;
+    P1Big *bigp = reinterpret_cast<P1Big *>(smem_raw + ((sizeof(P1Smem) + 15) & ~size_t(15)));
 
     for (int n = blockIdx.x; n < N; n += gridDim.x) {
         const int p = n % d.P, ti = step0 + n / d.P;
@@ -459,9 +550,9 @@ __global__ void __launch_bounds__(NT, 2) k_phase1(Dims d, Inputs in, Work w, int
         // 1. keys (a slot outside [0, S) is reported and sorted as slot S, after every real
         //    slot, with weight 0 and log-decay 0: it adds nothing anywhere and no DW writes it)
         int bad = 0;
-        for (int i = tid; i < nw; i += NT) {
-            int s = ws[i];
-            float kk = to_f32(k[i]);
+        auto key_of = [&](int i, int sraw, float kraw, float graw) {
+            int s = sraw;
+            float kk = kraw;
             if ((unsigned)s >= (unsigned)S) {
                 report_bad_slot(w.status, (int)(tok_base + i / W));
                 s = S;
@@ -470,23 +561,58 @@ __global__ void __launch_bounds__(NT, 2) k_phase1(Dims d, Inputs in, Work w, int
             }
             kf[i] = kk;
             // g (0 if dropped), read in step 2
-            pgs[i] = __float_as_int(s == S ? 0.f : g[d.gate ? div_by(i, magW) : i]);
+            pgs[i] = __float_as_int(s == S ? 0.f : graw);
             wsl[i] = s < S ? s : kNoEntry;
             const int t = div_by(i, magW);
             keyA[i] = ((unsigned long long)(unsigned)s << 32) | ((unsigned)t << 8) |
                       (unsigned)(i - t * W);
-        }
-        for (int i = tid; i < nr; i += NT) {
-            const int r = rs[i];
+        };
+        auto read_of = [&](int i, int r, float qraw) {
             if ((unsigned)r >= (unsigned)S) report_bad_slot(w.status, (int)(tok_base + i / R));
             rsl[i] = (unsigned)r < (unsigned)S ? r : kNoEntry;
-            rhi[i] = __float_as_int(to_f32(q[i]));   // q, read back in step 3
+            rhi[i] = __float_as_int(qraw);   // q, read back in step 3
+        };
+        if (split) {
+            // four entries per thread, their loads first
+            for (int i0 = tid; i0 < nw; i0 += G4) {
+                int sv[IT4];
+                float kv[IT4], gv[IT4];
+#pragma unroll
+                for (int u = 0; u < IT4; ++u) {
+                    const int i = i0 + u * NT;
+                    if (i < nw) {
+                        sv[u] = ws[i];
+                        kv[u] = to_f32(k[i]);
+                        gv[u] = g[d.gate ? div_by(i, magW) : i];
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < IT4; ++u)
+                    if (i0 + u * NT < nw) key_of(i0 + u * NT, sv[u], kv[u], gv[u]);
+            }
+            for (int i0 = tid; i0 < nr; i0 += G4) {
+                int rv[IT4];
+                float qv[IT4];
+#pragma unroll
+                for (int u = 0; u < IT4; ++u) {
+                    const int i = i0 + u * NT;
+                    if (i < nr) { rv[u] = rs[i]; qv[u] = to_f32(q[i]); }
+                }
+#pragma unroll
+                for (int u = 0; u < IT4; ++u)
+                    if (i0 + u * NT < nr) read_of(i0 + u * NT, rv[u], qv[u]);
+            }
+        } else {
+            for (int i = tid; i < nw; i += NT)
+                key_of(i, ws[i], to_f32(k[i]), g[d.gate ? div_by(i, magW) : i]);
+            for (int i = tid; i < nr; i += NT) read_of(i, rs[i], to_f32(q[i]));
         }
         // slot S may need one more radix digit than the real slots
         const int npass = __syncthreads_or(bad) ? (32 - __clz(S) + 7) / 8 : passes;
         unsigned long long *src = keyA, *dst = keyB;
         for (int ps = 0; ps < npass; ++ps) {
-            radix_pass(src, dst, nw, 32 + 8 * ps, sm);
+            if (split) radix_pass4(src, dst, nw, 32 + 8 * ps, sm, *bigp);
+            else radix_pass(src, dst, nw, 32 + 8 * ps, sm);
             unsigned long long *t = src; src = dst; dst = t;
         }
         const unsigned long long *srt = src;
@@ -495,7 +621,91 @@ __global__ void __launch_bounds__(NT, 2) k_phase1(Dims d, Inputs in, Work w, int
         // 2. groups and running log-decays along the sorted row
         float carry_v = 0.f;
         int carry_i = 0;
-        for (int tile = 0; tile < nw; tile += NT) {
+        if (split) {
+            // tiles of G4 positions, four consecutive ones per thread: a thread-local segmented
+            // scan, then one across the threads' aggregates, whose exclusive values (read from
+            // shared memory) carry into each thread's positions before its first group head
+            for (int tile = 0; tile < nw; tile += G4) {
+                const int pos0 = tile + IT4 * tid;
+                unsigned long long kk[IT4 + 2];          // positions pos0 - 1 .. pos0 + 4
+#pragma unroll
+                for (int u = 0; u < IT4 + 2; ++u) {
+                    const int ps = pos0 - 1 + u;
+                    kk[u] = (ps >= 0 && ps < nw) ? srt[ps] : ~0ull;
+                }
+                int e[IT4];
+                float gv[IT4], kv[IT4];
+                bool head[IT4], tail[IT4];
+#pragma unroll
+                for (int u = 0; u < IT4; ++u) {
+                    const int ps = pos0 + u;
+                    const bool ok = ps < nw;
+                    const unsigned low = (unsigned)(kk[u + 1] & 0xffffffffu);
+                    const int slot = (int)(kk[u + 1] >> 32);
+                    e[u] = ok ? ent_of(low) : 0;
+                    head[u] = ok && (ps == 0 || (int)(kk[u] >> 32) != slot);
+                    tail[u] = ok && (ps == nw - 1 || (int)(kk[u + 2] >> 32) != slot);
+                    gv[u] = ok ? __int_as_float(pgs[e[u]]) : 0.f;
+                    kv[u] = ok ? kf[e[u]] : 0.f;
+                }
+                // thread-local inclusive values and head counts
+                float lv[IT4];
+                int hc[IT4];
+                bool any_head = false;
+                float run = 0.f;
+                int hrun = 0;
+#pragma unroll
+                for (int u = 0; u < IT4; ++u) {
+                    run = head[u] ? gv[u] : run + gv[u];
+                    any_head |= head[u];
+                    hrun += head[u] ? 1 : 0;
+                    lv[u] = run;
+                    hc[u] = hrun;
+                }
+                float cv;
+                const float incl_v = seg_scan(any_head, run, carry_v, cv, sm);
+                int ci;
+                const int incl_i = int_scan(hrun, carry_i, ci, sm);
+                bigp->tv[tid] = incl_v;
+                bigp->ti[tid] = incl_i;
+                __syncthreads();
+                const float ex_v = tid == 0 ? carry_v : bigp->tv[tid - 1];
+                const int ex_i = tid == 0 ? carry_i : bigp->ti[tid - 1];
+                carry_v = cv;
+                carry_i = ci;
+                bool seen = false;
+#pragma unroll
+                for (int u = 0; u < IT4; ++u) {
+                    const int ps = pos0 + u;
+                    if (ps >= nw) break;
+                    seen |= head[u];
+                    const float l = seen ? lv[u] : ex_v + lv[u];
+                    const int gid = ex_i + hc[u] - 1;
+                    const unsigned low = (unsigned)(kk[u + 1] & 0xffffffffu);
+                    const int slot = (int)(kk[u + 1] >> 32);
+                    perm[ps] = e[u];
+                    inv[e[u]] = ps;
+                    tkk[ps] = make_float2(__int_as_float((int)(low >> 8)), kv[u]);
+                    if (!head[u] && ((unsigned)kk[u] >> 8) == (low >> 8))
+                        atomicAdd(&w.status->repeated_write_slots, 1ull);
+                    lws[ps] = l;
+                    lw[e[u]] = l;
+                    pgid[ps] = gid;
+                    if (head[u]) {
+                        goff[gid] = ps;
+                        gslot[gid] = slot;
+                    }
+                    if (tail[u]) {
+                        lend[gid] = l;
+                        gfac[gid] = expf(l);
+                    }
+                    minfo[ps] = (int)(low >> 8) | (int)((low & 255u) << 8) | (head[u] ? 1 << 16 : 0) |
+                                (tail[u] ? 1 << 17 : 0);
+                }
+                __syncthreads();
+            }
+        }
+        for (int tile = 0; !split && tile < nw; tile += NT) {
             const int pos = tile + tid;
             const bool ok = pos < nw;
             unsigned long long key = ok ? srt[pos] : 0ull;
@@ -544,7 +754,21 @@ __global__ void __launch_bounds__(NT, 2) k_phase1(Dims d, Inputs in, Work w, int
         }
         __syncthreads();
         // group start of every sorted position (one lookup instead of a chain later)
-        for (int pos = tid; pos < nw; pos += NT) pgs[pos] = go[pgid[pos]];
+        if (split) {
+            for (int p0 = tid; p0 < nw; p0 += G4) {
+                int gid[IT4];
+#pragma unroll
+                for (int u = 0; u < IT4; ++u) gid[u] = p0 + u * NT < nw ? pgid[p0 + u * NT] : 0;
+                int gs[IT4];
+#pragma unroll
+                for (int u = 0; u < IT4; ++u) gs[u] = p0 + u * NT < nw ? go[gid[u]] : 0;
+#pragma unroll
+                for (int u = 0; u < IT4; ++u)
+                    if (p0 + u * NT < nw) pgs[p0 + u * NT] = gs[u];
+            }
+        } else {
+            for (int pos = tid; pos < nw; pos += NT) pgs[pos] = go[pgid[pos]];
+        }
         __syncthreads();
 
         const P1Chunk<WT> pc{rs, q, srt, tkk, inv, pgid, pgs, lws, lend, kf, rlo, rhi,
@@ -708,7 +932,7 @@ cudaError_t launch_phase1(const Dims &d, const Inputs &in, const Work &w, int st
                           cudaStream_t st) {
     const size_t full = phase1_scratch_smem(d);
     const int in_smem = full <= kPhase1SmemMax ? 1 : 0;
-    const size_t smem = in_smem ? full : sizeof(P1Smem);
+    const size_t smem = in_smem ? full : ((sizeof(P1Smem) + 15) & ~size_t(15)) + sizeof(P1Big);
     const int grid = w.G;
     const dim3 rows_grid((d.C + KR - 1) / KR, nsteps * d.P);
     if (d.dtype == SDM_BF16) {

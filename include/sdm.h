@@ -250,6 +250,8 @@ int sdm_profile_write_read(const sdm_shape *shape, void *bank, const int32_t *wr
  *                                gather weight q*exp(lr)
  *   A, QK, X, QX [N, C, C]       Gram matrices and the solve (X unit lower triangular, +0
  *                                above the diagonal; QX = QK X)
+ *   dense_groups [N]     int32   groups of the chunk whose Gram pair sums were taken in the
+ *                                dense factor form (0 where the chunk's scratch is on chip)
  * Any output pointer may be NULL (not copied). The workspace is the one sdm_write_read
  * takes for the same shape. The bank is not touched. */
 int sdm_phase1_debug(const sdm_shape *shape, const int32_t *write_slots, const void *write_w,
@@ -257,7 +259,8 @@ int sdm_phase1_debug(const sdm_shape *shape, const int32_t *write_slots, const v
                      const void *read_w, const int32_t *valid_tokens, int32_t *perm,
                      uint8_t *group_start, uint8_t *owner, int32_t *ngroups, float *lw,
                      float *gw, float *dw, float *lr, float *qw, float *A, float *QK, float *X,
-                     float *QX, void *workspace, size_t workspace_bytes, void *stream);
+                     float *QX, int32_t *dense_groups, void *workspace, size_t workspace_bytes,
+                     void *stream);
 
 /* Reads the device status block of the last call that used this workspace. Synchronizes
  * the stream. status: host pointer. Returns SDM_OK, or SDM_ERR_CUDA. The block's code is

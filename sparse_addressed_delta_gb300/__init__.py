@@ -103,7 +103,7 @@ def library() -> ctypes.CDLL:
                                                    + [ctypes.POINTER(ctypes.c_float),
                                                       ctypes.POINTER(ctypes.c_int32), vp])
             lib.sdm_profile_write_read.restype = i32
-            lib.sdm_phase1_debug.argtypes = [sp] + [vp] * 7 + [vp] * 13 + [vp, sz, vp]
+            lib.sdm_phase1_debug.argtypes = [sp] + [vp] * 7 + [vp] * 14 + [vp, sz, vp]
             lib.sdm_phase1_debug.restype = i32
             lib.sdm_get_device_status.argtypes = [vp, ctypes.POINTER(_DeviceStatus), vp]
             lib.sdm_get_device_status.restype = i32
@@ -504,7 +504,8 @@ def phase1_debug(write_slots, write_w, log_decay, beta, read_slots, read_w, vali
                  stream=None) -> Dict[str, torch.Tensor]:
     """Phase 1 and the solve of every chunk (time-major chunk n = ti*P + p), as tensors:
     perm, group_start, owner [N, C*W]; ngroups [N]; lw, gw, dw [N, C*W]; lr, qw [N, C*R];
-    A, QK, X, QX [N, C, C]."""
+    A, QK, X, QX [N, C, C]; dense_groups [N] (the groups whose Gram pair sums were taken in
+    the dense factor form)."""
     P, T, W = write_slots.shape
     R = read_slots.shape[-1]
     dev, dt = write_w.device, write_w.dtype
@@ -522,10 +523,11 @@ def phase1_debug(write_slots, write_w, log_decay, beta, read_slots, read_w, vali
         "qw": torch.empty((N, C * R), **f32), "A": torch.empty((N, C, C), **f32),
         "QK": torch.empty((N, C, C), **f32), "X": torch.empty((N, C, C), **f32),
         "QX": torch.empty((N, C, C), **f32),
+        "dense_groups": torch.empty((N,), dtype=torch.int32, device=dev),
     }
     ws = alloc_workspace(shape, dev)
     order = ["perm", "group_start", "owner", "ngroups", "lw", "gw", "dw", "lr", "qw", "A", "QK",
-             "X", "QX"]
+             "X", "QX", "dense_groups"]
     with torch.cuda.device(dev):
         rc = library().sdm_phase1_debug(
             ctypes.byref(shape), _ptr(write_slots), _ptr(write_w), _ptr(log_decay), _ptr(beta),

@@ -99,7 +99,9 @@ int check_shape(const sdm_shape *s, Dims &d) {
 
 size_t per_chunk_bytes(const Dims &d) {
     const size_t CW = (size_t)d.C * d.W, CR = (size_t)d.C * d.R, CC = (size_t)d.C * d.C;
-    return 4 * (11 * CW + 4) + 4 * 3 * CR + 4 * 4 * CC + 24;
+    const size_t dense =
+        dense_gram(d) ? 4 * (CW + 1 + d.C + 3 * (size_t)d.C * dense_pitch(d.C)) : 0;
+    return 4 * (11 * CW + 4) + 4 * 3 * CR + 4 * 4 * CC + 24 + dense;
 }
 
 int slab_steps(const Dims &d, int requested) {
@@ -107,7 +109,9 @@ int slab_steps(const Dims &d, int requested) {
     const size_t per_step = per_chunk_bytes(d) * d.P;
     if (per_step * d.Nt <= kSlabBudget) return d.Nt;
     long ns = (long)(kSlabBudget / per_step);
-    const long min_steps = (kRefSms + d.P - 1) / d.P;   // at least one chunk per SM
+    // at least two chunks per SM, so that Phase 1 (a CTA per chunk, two fit on an SM) keeps
+    // every SM busy with two chunks at once
+    const long min_steps = (2L * kRefSms + d.P - 1) / d.P;
     if (ns < min_steps) ns = min_steps;
     if (ns < 1) ns = 1;
     return ns < d.Nt ? (int)ns : d.Nt;
@@ -155,6 +159,12 @@ int phase1_ctas(const Dims &d, int ns) {
     F(kf, float, G * CW)                                                      \
     F(rlo, int32_t, G * CR)                                                   \
     F(rhi, int32_t, G * CR)                                                   \
+    F(dpos, int32_t, HS * G * CW)                                             \
+    F(dref, float, HS * N * C)                                                \
+    F(ndense, int32_t, HS * N)                                                \
+    F(dka, float, HS * N * DCC)                                               \
+    F(dkb, float, HS * N * DCC)                                               \
+    F(dkq, float, HS * N * DCC)                                               \
     F(wkey, unsigned long long, B * N * CW)                                   \
     F(wlws, float, B * N * CW)                                                \
     F(wpgs, int32_t, B * N * CW)                                              \
@@ -190,7 +200,8 @@ size_t layout_bytes(const Dims &d, int ns, int G_) {
     const size_t N = (size_t)ns * d.P, P = d.P, CW = (size_t)d.C * d.W, CR = (size_t)d.C * d.R,
                  CC = (size_t)d.C * d.C, CD = (size_t)d.C * d.D, G = G_, B = d.bwd ? 1 : 0,
                  C = d.C, DT = ((size_t)d.D + 31) / 32, CX = (size_t)d.C * d.xp,
-                 GT = d.gate ? 1 : 0;
+                 GT = d.gate ? 1 : 0, HS = dense_gram(d) ? 1 : 0,
+                 DCC = (size_t)d.C * dense_pitch(d.C);
     size_t off = 0;
 #define X_SIZE(name, type, count) off += up(sizeof(type) * (size_t)(count));
     SDM_LAYOUT(X_SIZE)
@@ -202,7 +213,8 @@ Work layout_assign(const Dims &d, int ns, int G_, void *base) {
     const size_t N = (size_t)ns * d.P, P = d.P, CW = (size_t)d.C * d.W, CR = (size_t)d.C * d.R,
                  CC = (size_t)d.C * d.C, CD = (size_t)d.C * d.D, G = G_, B = d.bwd ? 1 : 0,
                  C = d.C, DT = ((size_t)d.D + 31) / 32, CX = (size_t)d.C * d.xp,
-                 GT = d.gate ? 1 : 0;
+                 GT = d.gate ? 1 : 0, HS = dense_gram(d) ? 1 : 0,
+                 DCC = (size_t)d.C * dense_pitch(d.C);
     Work w;
     memset(&w, 0, sizeof(w));
     char *p = static_cast<char *>(base);
@@ -370,7 +382,8 @@ int64_t sdm_launch_count(const sdm_shape *shape) {
     Prepared pr;
     if (prepare(shape, pr)) return 0;
     const int64_t slabs = (pr.d.Nt + pr.ns - 1) / pr.ns;
-    const int64_t p1 = phase1_split(pr.d) ? 2 : 1;   // Phase 1 (+ its row kernel), per slab
+    // Phase 1 (+ its row kernel, + the dense-Gram kernel), per slab
+    const int64_t p1 = phase1_split(pr.d) ? (dense_gram(pr.d) ? 3 : 2) : 1;
     return pr.d.per_step ? slabs * (p1 + 1) + (int64_t)pr.d.Nt * 3 : slabs * (p1 + 2);
 }
 
@@ -507,7 +520,8 @@ int sdm_phase1_debug(const sdm_shape *shape, const int32_t *write_slots, const v
                      const void *read_w, const int32_t *valid_tokens, int32_t *perm,
                      uint8_t *group_start, uint8_t *owner, int32_t *ngroups, float *lw,
                      float *gw, float *dw, float *lr, float *qw, float *A, float *QK, float *X,
-                     float *QX, void *workspace, size_t workspace_bytes, void *stream) {
+                     float *QX, int32_t *dense_groups, void *workspace, size_t workspace_bytes,
+                     void *stream) {
     Prepared pr;
     int rc = prepare(shape, pr);
     if (rc) return rc;
@@ -540,6 +554,12 @@ int sdm_phase1_debug(const sdm_shape *shape, const int32_t *write_slots, const v
             if (!c.dst) continue;
             e = cudaMemcpyAsync(static_cast<char *>(c.dst) + n0 * c.per, c.src, N * c.per,
                                 cudaMemcpyDeviceToDevice, st);
+            if (e != cudaSuccess) return cuda_fail(e, "debug copy");
+        }
+        if (dense_groups) {
+            e = dense_gram(d) ? cudaMemcpyAsync(dense_groups + n0, w.ndense, 4 * N,
+                                                  cudaMemcpyDeviceToDevice, st)
+                                : cudaMemsetAsync(dense_groups + n0, 0, 4 * N, st);
             if (e != cudaSuccess) return cuda_fail(e, "debug copy");
         }
         // X and QX rows at the workspace pitch -> dense [C][C]

@@ -280,6 +280,11 @@ struct P1Chunk {
     int32_t *rlo, *rhi;
     float *wdw, *gw, *qw, *lr, *A, *QK, *dwt;
     int nv, nw, nr, C, W, R, S;
+    // dense Gram groups (global-scratch chunks only; dpos null otherwise)
+    const int32_t *dpos;
+    const float *dref;
+    float *dka, *dkb, *dkq;
+    int nd;
 };
 
 // 3a. weights of the sorted positions [pos0, pos1): gw = k exp(lw), dw = k exp(lend - lw)
@@ -299,13 +304,20 @@ __device__ void p1_weights(const P1Chunk<WT> &c, int pos0, int pos1, int tid, in
 
 // 3b. each read entry in [er_lo, er_hi) finds the last write of its slot at a token <= its own:
 // an upper bound in the sorted write row, four reads per thread at a time, branch-free (the
-// same probe count for all of them, so the four searches overlap); then lr and qw
-template <typename WT>
-__device__ void p1_reads(const P1Chunk<WT> &c, int er_lo, int er_hi, int tid, int nthr) {
+// same probe count for all of them, so the four searches overlap); then lr and qw. With `smp`
+// (every kSampleStep-th key of the row, nsmp of them, in shared memory) the bound is first
+// found among the samples and then inside one window of kSampleStep - 1 keys; else over the
+// whole row.
+constexpr int kSampleStep = 64;
+constexpr int kMaxSamples = kMaxChunk * kMaxWidth / kSampleStep;
+
+template <typename WT, bool SAMPLED = false>
+__device__ void p1_reads(const P1Chunk<WT> &c, int er_lo, int er_hi, int tid, int nthr,
+                         const unsigned long long *smp = nullptr, int nsmp = 0) {
     const unsigned magR = div_magic(c.R);
     for (int er0 = er_lo + tid; er0 < er_hi; er0 += 4 * nthr) {
         unsigned long long target[4];
-        int base[4], r[4];
+        int base[4], r[4], hi[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const int er = er0 + k * nthr;
@@ -313,36 +325,91 @@ __device__ void p1_reads(const P1Chunk<WT> &c, int er_lo, int er_hi, int tid, in
             const int t = er < er_hi ? div_by(er, magR) : 0;
             target[k] = ((unsigned long long)(unsigned)r[k] << 32) | ((unsigned)t << 8) | 255u;
             base[k] = 0;
+            hi[k] = c.nw;
         }
-        for (int len = c.nw; len > 1;) {
+        int len0 = c.nw;
+        if (SAMPLED && c.nw > 0) {
+            // the number of samples <= target, then the window of row keys after the last such
+            // sample and before the next (keys at or past hi count as above every target)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                int b = 0;
+                for (int len = nsmp; len > 1;) {
+                    const int half = len >> 1;
+                    if (smp[b + half - 1] <= target[k]) b += half;
+                    len -= half;
+                }
+                const int ns_le = b + (smp[b] <= target[k] ? 1 : 0);
+                if (ns_le == 0) {
+                    base[k] = 0;
+                    hi[k] = 0;
+                } else {
+                    base[k] = (ns_le - 1) * kSampleStep + 1;
+                    hi[k] = min(ns_le * kSampleStep, c.nw);
+                }
+            }
+            len0 = kSampleStep - 1;
+        }
+        for (int len = len0; len > 1;) {
             const int half = len >> 1;
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-                if (c.srt[base[k] + half - 1] <= target[k]) base[k] += half;
+            for (int k = 0; k < 4; ++k) {
+                const int ix = base[k] + half - 1;
+                if (ix < hi[k] && c.srt[ix] <= target[k]) base[k] += half;
+            }
             len -= half;
         }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const int er = er0 + k * nthr;
             if (er >= er_hi) continue;
-            int lo = 0, hi = -1;
+            int lo = 0, hib = -1;
             float l = 0.f;
             const float qf = __int_as_float(c.rhi[er]);   // q, staged there by step 1
             const bool valid = (unsigned)r[k] < (unsigned)c.S;
             if (valid && c.nw > 0) {
-                const int pos = base[k] + (c.srt[base[k]] <= target[k] ? 1 : 0) - 1;
+                const int ub = base[k] + (base[k] < hi[k] && c.srt[base[k]] <= target[k] ? 1 : 0);
+                const int pos = ub - 1;
                 if (pos >= 0 && (int)(c.srt[pos] >> 32) == r[k]) {
-                    hi = pos;
+                    hib = pos;
                     lo = c.pgs[pos];
                     l = c.lws[pos];
+                    // a dense group's read: rlo = -1 - its dense index (no pair sums)
+                    if (SAMPLED && c.dpos) {
+                        const int dh = c.dpos[pos];
+                        if (dh >= 0) lo = -1 - dh;
+                    }
                 }
             }
             c.rlo[er] = lo;
-            c.rhi[er] = hi;
+            c.rhi[er] = hib;
             c.lr[er] = l;
             c.qw[er] = valid ? qf * expf(l) : 0.f;
         }
     }
+}
+
+// Adds the dense-group values of one batch of a row's entries to the row's staged factors:
+// lanes whose entry belongs to dense group dh >= 0 add v0 (and v1) at column dh of f0 (and
+// f1). Lanes of one group (a repeated slot) are summed in lane order by the lowest of them, so
+// every staged element is a fixed-order sum. `key` separates the two half-warp rows.
+__device__ __forceinline__ void dense_stage(int dh, int key, float v0, float v1, float *f0,
+                                            float *f1, int lane) {
+    const bool dn = dh >= 0;
+    const unsigned peers = __match_any_sync(0xffffffffu, dn ? (key << 16) | dh : -1 - lane);
+    if (dn) {
+        float s0 = 0.f, s1 = 0.f;
+        for (unsigned m = peers; m; m &= m - 1u) {
+            const int src = __ffs(m) - 1;
+            s0 += __shfl_sync(peers, v0, src);
+            s1 += __shfl_sync(peers, v1, src);
+        }
+        if (lane == __ffs(peers) - 1) {
+            f0[dh] += s0;
+            if (f1) f1[dh] += s1;
+        }
+    }
+    __syncwarp();
 }
 
 // 4. rows [t0, t1) of A and QK. A warp takes two token rows at a time when both fit in its row
@@ -350,10 +417,13 @@ __device__ void p1_reads(const P1Chunk<WT> &c, int er_lo, int er_hi, int tid, in
 //    entries are looked up one per lane; entries with earlier members of their group (a ballot)
 //    are then taken in entry order, the lanes of the row over those members (distinct tokens,
 //    so no two lanes add to one element). (token, k) of every sorted position is kept in the
-//    free radix buffer, next to its running log-decay.
-template <typename WT, bool TWO>
+//    free radix buffer, next to its running log-decay. Entries of dense groups take no pair
+//    sums here: they add their factors to the row's staged dense rows (dka, dkb from the
+//    writes, dkq from the reads; `drow` holds 3 dense_pitch(C) floats per row), which
+//    k_gram_dense multiplies out.
+template <typename WT, bool TWO, int kPairAhead>
 __device__ void p1_gram_rows(const P1Chunk<WT> &c, int t0, int t1, int warp, int nwarps, int lane,
-                             float *row) {
+                             float *row, float *drow) {
     const int C = c.C, W = c.W, R = c.R;
     constexpr int lpr = TWO ? 16 : 32;                  // lanes per row
     const int hsel = TWO ? lane >> 4 : 0;
@@ -361,50 +431,72 @@ __device__ void p1_gram_rows(const P1Chunk<WT> &c, int t0, int t1, int warp, int
     const unsigned hmask = TWO ? 0xffffu << (16 * hsel) : 0xffffffffu;
     constexpr int rpw = TWO ? 2 : 1;                    // rows per warp and pass
     float *rw = row + hsel * C;
+    const int dp = dense_pitch(C);
+    const int hp = kPairAhead > 1 && c.dpos ? (c.nd + 3) & ~3 : 0;   // staged dense columns
+                                                     // (only the look-ahead variant stages)
+    float *da = hp ? drow + hsel * 3 * dp : nullptr, *db = da + dp, *dq = db + dp;
     for (int tb = t0 + warp * rpw; tb < t1; tb += nwarps * rpw) {
         const int t = tb + hsel;
         const bool live = t < t1;                       // else this half only joins the shuffles
         const bool act = live && t < c.nv;
         for (int x = hl; x < C; x += lpr) rw[x] = 0.f;
+        for (int x = hl; x < hp; x += lpr) { da[x] = 0.f; db[x] = 0.f; dq[x] = 0.f; }
         __syncwarp();
         for (int j0 = 0; j0 < W; j0 += lpr) {
             const int j = j0 + hl;
             float ka = 0.f, la = 0.f;
-            int pos = 0, gs = 0;
+            int pos = 0, gs = 0, dh = -1;
             if (act && j < W) {
                 const int e = t * W + j;
                 ka = c.kf[e];
                 pos = c.inv[e];
                 gs = c.pgs[pos];
                 la = c.lws[pos];
+                if (hp) dh = c.dpos[pos];
             }
-            unsigned todo = __ballot_sync(0xffffffffu, ka != 0.f && pos > gs) & hmask;
+            if (hp) {
+                float va = 0.f, vb = 0.f;
+                if (dh >= 0) {
+                    const float r = c.dref[dh];
+                    va = ka * expf(la - r);
+                    vb = ka * expf(r - la);
+                }
+                dense_stage(dh, hsel, va, vb, da, db, lane);
+            }
+            unsigned todo = __ballot_sync(0xffffffffu, ka != 0.f && pos > gs && dh < 0) & hmask;
             while (__any_sync(0xffffffffu, todo != 0u)) {
-                const bool has = todo != 0u;
-                const int src = has ? __ffs(todo) - 1 : lane;
-                todo &= todo - 1u;
-                const float kb = __shfl_sync(0xffffffffu, ka, src);
-                const float lb = __shfl_sync(0xffffffffu, la, src);
-                const int pb = __shfl_sync(0xffffffffu, pos, src);
-                const int gb = __shfl_sync(0xffffffffu, gs, src);
-                const int pe = has ? pb : gb;
-                // the members' records four lane-strides at a time, all loaded before any is
-                // added (they have distinct tokens, so the order of the adds changes nothing)
-                int m = gb + hl;
-                for (; m + 3 * lpr < pe; m += 4 * lpr) {
-                    float2 tk[4];
-                    float l[4];
+                // up to kPairAhead entries at a time: the first lane-stride of each one's
+                // earlier members is loaded before any is added; the adds then run entry by
+                // entry as before (members of one entry have distinct tokens, so no two lanes
+                // add to one element, and each element sees the entries in row order)
+                float kb[kPairAhead], lb[kPairAhead], l1[kPairAhead];
+                int gb[kPairAhead], pe[kPairAhead];
+                float2 tk1[kPairAhead];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) { tk[u] = c.tkk[m + u * lpr]; l[u] = c.lws[m + u * lpr]; }
+                for (int u = 0; u < kPairAhead; ++u) {
+                    const bool has = todo != 0u;
+                    const int src = has ? __ffs(todo) - 1 : lane;
+                    todo &= todo - 1u;
+                    kb[u] = __shfl_sync(0xffffffffu, ka, src);
+                    lb[u] = __shfl_sync(0xffffffffu, la, src);
+                    const int pb = __shfl_sync(0xffffffffu, pos, src);
+                    gb[u] = __shfl_sync(0xffffffffu, gs, src);
+                    pe[u] = has ? pb : gb[u];
+                    if (gb[u] + hl < pe[u]) {
+                        tk1[u] = c.tkk[gb[u] + hl];
+                        l1[u] = c.lws[gb[u] + hl];
+                    }
+                }
 #pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        rw[__float_as_int(tk[u].x)] += kb * tk[u].y * expf(lb - l[u]);
+                for (int u = 0; u < kPairAhead; ++u) {
+                    if (gb[u] + hl < pe[u])
+                        rw[__float_as_int(tk1[u].x)] += kb[u] * tk1[u].y * expf(lb[u] - l1[u]);
+                    for (int m = gb[u] + hl + lpr; m < pe[u]; m += lpr) {
+                        const float2 tk = c.tkk[m];
+                        rw[__float_as_int(tk.x)] += kb[u] * tk.y * expf(lb[u] - c.lws[m]);
+                    }
+                    __syncwarp();
                 }
-                for (; m < pe; m += lpr) {
-                    const float2 tk = c.tkk[m];
-                    rw[__float_as_int(tk.x)] += kb * tk.y * expf(lb - c.lws[m]);
-                }
-                __syncwarp();
             }
         }
         if (live)
@@ -425,44 +517,169 @@ __device__ void p1_gram_rows(const P1Chunk<WT> &c, int t0, int t1, int warp, int
                     la = c.lr[er];
                 }
             }
-            unsigned todo = __ballot_sync(0xffffffffu, hi >= 0) & hmask;
+            if (hp) {
+                const int dh = hi >= 0 && lo < 0 ? -1 - lo : -1;
+                const float vq = dh >= 0 ? qa * expf(la - c.dref[dh]) : 0.f;
+                dense_stage(dh, hsel, vq, 0.f, dq, nullptr, lane);
+            }
+            unsigned todo = __ballot_sync(0xffffffffu, hi >= 0 && lo >= 0) & hmask;
             while (__any_sync(0xffffffffu, todo != 0u)) {
-                const bool has = todo != 0u;
-                const int src = has ? __ffs(todo) - 1 : lane;
-                todo &= todo - 1u;
-                const float qb = __shfl_sync(0xffffffffu, qa, src);
-                const float lb = __shfl_sync(0xffffffffu, la, src);
-                const int lob = __shfl_sync(0xffffffffu, lo, src);
-                const int hib = __shfl_sync(0xffffffffu, hi, src);
-                const int he = has ? hib : lob - 1;
-                int m = lob + hl;
-                for (; m + 3 * lpr <= he; m += 4 * lpr) {
-                    float2 tk[4];
-                    float l[4];
+                // as for the writes: kPairAhead read entries' first member loads in flight
+                float qb[kPairAhead], lb[kPairAhead], l1[kPairAhead];
+                int lob[kPairAhead], he[kPairAhead];
+                float2 tk1[kPairAhead];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) { tk[u] = c.tkk[m + u * lpr]; l[u] = c.lws[m + u * lpr]; }
+                for (int u = 0; u < kPairAhead; ++u) {
+                    const bool has = todo != 0u;
+                    const int src = has ? __ffs(todo) - 1 : lane;
+                    todo &= todo - 1u;
+                    qb[u] = __shfl_sync(0xffffffffu, qa, src);
+                    lb[u] = __shfl_sync(0xffffffffu, la, src);
+                    lob[u] = __shfl_sync(0xffffffffu, lo, src);
+                    const int hib = __shfl_sync(0xffffffffu, hi, src);
+                    he[u] = has ? hib : lob[u] - 1;
+                    if (lob[u] + hl <= he[u]) {
+                        tk1[u] = c.tkk[lob[u] + hl];
+                        l1[u] = c.lws[lob[u] + hl];
+                    }
+                }
 #pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        rw[__float_as_int(tk[u].x)] += qb * tk[u].y * expf(lb - l[u]);
+                for (int u = 0; u < kPairAhead; ++u) {
+                    if (lob[u] + hl <= he[u])
+                        rw[__float_as_int(tk1[u].x)] += qb[u] * tk1[u].y * expf(lb[u] - l1[u]);
+                    for (int m = lob[u] + hl + lpr; m <= he[u]; m += lpr) {
+                        const float2 tk = c.tkk[m];
+                        rw[__float_as_int(tk.x)] += qb[u] * tk.y * expf(lb[u] - c.lws[m]);
+                    }
+                    __syncwarp();
                 }
-                for (; m <= he; m += lpr) {
-                    const float2 tk = c.tkk[m];
-                    rw[__float_as_int(tk.x)] += qb * tk.y * expf(lb - c.lws[m]);
-                }
-                __syncwarp();
             }
         }
-        if (live)
+        if (live) {
             for (int x = hl; x < C; x += lpr) c.QK[(size_t)t * C + x] = rw[x];
+            for (int x = hl; x < hp; x += lpr) {
+                c.dka[(size_t)t * dp + x] = da[x];
+                c.dkb[(size_t)t * dp + x] = db[x];
+                c.dkq[(size_t)t * dp + x] = dq[x];
+            }
+        }
         __syncwarp();
     }
 }
 
-template <typename WT>
+// AHEAD: Gram row entries whose first member loads are in flight at once
+template <typename WT, int AHEAD>
 __device__ __forceinline__ void p1_gram(const P1Chunk<WT> &c, int t0, int t1, int warp, int nwarps,
-                                        int lane, float *row) {
-    if (2 * c.C <= kMaxChunk) p1_gram_rows<WT, true>(c, t0, t1, warp, nwarps, lane, row);
-    else p1_gram_rows<WT, false>(c, t0, t1, warp, nwarps, lane, row);
+                                        int lane, float *row, float *drow) {
+    if (2 * c.C <= kMaxChunk) p1_gram_rows<WT, true, AHEAD>(c, t0, t1, warp, nwarps, lane, row, drow);
+    else p1_gram_rows<WT, false, AHEAD>(c, t0, t1, warp, nwarps, lane, row, drow);
+}
+
+// Dense Gram groups of a chunk whose scratch is in global memory. A group of n members costs
+// about n^2 pair terms in the row kernel but a fixed C^2 multiply-adds as a dense factor, so the
+// large groups go dense: those of at least thr members, thr the least of (C/8) << L
+// (L = 0..7) that leaves at most C of them, in group order; of these, the ones whose running
+// log-decays lie within kDenseSpan of each other (finite), with the middle of that range as the
+// reference (so every factor exp(lw - ref), exp(ref - lw) is at most exp(kDenseSpan / 2)). Sets
+// dpos of their members (the caller has set it to -1 at every position), dref and ndense.
+__device__ void p1_dense_select(const int32_t *go, int ng, const float *lws, int C, int32_t *dpos,
+                                float *dref, int32_t *ndense, P1Smem &sm, P1Big &bg) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int NL = 8;
+    const int thr0 = C / 8;
+    if (tid <= NL) sm.hist[tid] = 0;
+    __syncthreads();
+    int cnt[NL];
+#pragma unroll
+    for (int l = 0; l < NL; ++l) cnt[l] = 0;
+    for (int g = tid; g < ng; g += NT) {
+        const int sz = go[g + 1] - go[g];
+#pragma unroll
+        for (int l = 0; l < NL; ++l) cnt[l] += sz >= (thr0 << l) ? 1 : 0;
+    }
+#pragma unroll
+    for (int l = 0; l < NL; ++l) {
+        int v = cnt[l];
+#pragma unroll
+        for (int off = 16; off; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+        if (lane == 0 && v) atomicAdd(&sm.hist[l], v);
+    }
+    __syncthreads();
+    int thr = -1;
+    for (int l = 0; l < NL && thr < 0; ++l)
+        if (sm.hist[l] <= C) thr = thr0 << l;
+    if (thr < 0) {                     // cannot happen for distinct slots; no dense groups
+        if (tid == 0) *ndense = 0;
+        __syncthreads();
+        return;
+    }
+    // the candidates, in any order, then ranked into group order
+    int *list = bg.ti;
+    int *sorted = &bg.wc[0][0][0];
+    int *hidx = sorted + kMaxChunk;
+    float *ref = reinterpret_cast<float *>(sorted + 2 * kMaxChunk);
+    for (int g0 = 0; g0 < ng; g0 += NT) {
+        const int g = g0 + tid;
+        const bool take = g < ng && go[g + 1] - go[g] >= thr;
+        const unsigned b = __ballot_sync(0xffffffffu, take);
+        int base = 0;
+        if (lane == 0 && b) base = atomicAdd(&sm.hist[NL], __popc(b));
+        base = __shfl_sync(0xffffffffu, base, 0);
+        if (take) list[base + __popc(b & ((1u << lane) - 1u))] = g;
+    }
+    __syncthreads();
+    const int nc = sm.hist[NL];
+    if (tid < nc) {
+        const int gi = list[tid];
+        int r = 0;
+        for (int j = 0; j < nc; ++j) r += list[j] < gi ? 1 : 0;
+        sorted[r] = gi;
+    }
+    __syncthreads();
+    // the range of each candidate's running log-decays, one warp per candidate
+    for (int k = warp; k < nc; k += NW) {
+        const int g = sorted[k];
+        float mn = 3.0e38f, mx = -3.0e38f;
+        bool bad = false;
+        for (int pos = go[g] + lane; pos < go[g + 1]; pos += 32) {
+            const float l = lws[pos];
+            bad |= !(fabsf(l) <= 3.0e38f);           // NaN or infinite
+            mn = fminf(mn, l);
+            mx = fmaxf(mx, l);
+        }
+#pragma unroll
+        for (int off = 16; off; off >>= 1) {
+            mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        }
+        bad = __any_sync(0xffffffffu, bad);
+        if (lane == 0) {
+            hidx[k] = !bad && mx - mn <= kDenseSpan ? 1 : 0;
+            ref[k] = 0.5f * (mx + mn);
+        }
+    }
+    __syncthreads();
+    int h = -1;
+    if (tid < nc && hidx[tid]) {
+        h = 0;
+        for (int j = 0; j < tid; ++j) h += hidx[j];
+        dref[h] = ref[tid];
+    }
+    if (tid == 0) {
+        int tot = 0;
+        for (int j = 0; j < nc; ++j) tot += hidx[j];
+        *ndense = tot;
+    }
+    __syncthreads();
+    if (tid < nc) list[tid] = h;
+    __syncthreads();
+    for (int k = warp; k < nc; k += NW) {
+        const int hk = list[k];
+        if (hk < 0) continue;
+        const int g = sorted[k];
+        for (int pos = go[g] + lane; pos < go[g + 1]; pos += 32) dpos[pos] = hk;
+    }
+    __syncthreads();
 }
 
 template <typename WT>
@@ -754,6 +971,7 @@ __global__ void __launch_bounds__(NT, 2) k_phase1(Dims d, Inputs in, Work w, int
         }
         __syncthreads();
         // group start of every sorted position (one lookup instead of a chain later)
+        int32_t *dpos = split && C >= kDenseMinChunk ? w.dpos + (size_t)blockIdx.x * CW : nullptr;
         if (split) {
             for (int p0 = tid; p0 < nw; p0 += G4) {
                 int gid[IT4];
@@ -764,17 +982,23 @@ __global__ void __launch_bounds__(NT, 2) k_phase1(Dims d, Inputs in, Work w, int
                 for (int u = 0; u < IT4; ++u) gs[u] = p0 + u * NT < nw ? go[gid[u]] : 0;
 #pragma unroll
                 for (int u = 0; u < IT4; ++u)
-                    if (p0 + u * NT < nw) pgs[p0 + u * NT] = gs[u];
+                    if (p0 + u * NT < nw) {
+                        pgs[p0 + u * NT] = gs[u];
+                        if (dpos) dpos[p0 + u * NT] = -1;
+                    }
             }
         } else {
             for (int pos = tid; pos < nw; pos += NT) pgs[pos] = go[pgid[pos]];
         }
         __syncthreads();
+        if (dpos)
+            p1_dense_select(go, ng, lws, C, dpos, w.dref + (size_t)n * C, w.ndense + n, sm, *bigp);
 
         const P1Chunk<WT> pc{rs, q, srt, tkk, inv, pgid, pgs, lws, lend, kf, rlo, rhi,
                              wdw, gw, qw, lr, A, QK,
                              d.bwd ? w.dwt + (size_t)n * CW : nullptr,
-                             nv, nw, nr, C, W, R, S};
+                             nv, nw, nr, C, W, R, S,
+                             nullptr, nullptr, nullptr, nullptr, nullptr, 0};
         if (split) {
             // steps 3 and 4 run in k_phase1_rows, over many CTAs per chunk; it finds the
             // sorted row in the radix buffer recorded here
@@ -784,7 +1008,7 @@ __global__ void __launch_bounds__(NT, 2) k_phase1(Dims d, Inputs in, Work w, int
             p1_weights(pc, 0, nw, tid, NT);
             p1_reads(pc, 0, nr, tid, NT);
             __syncthreads();
-            p1_gram(pc, 0, C, warp, NW, lane, sm.row[warp]);
+            p1_gram<WT, 1>(pc, 0, C, warp, NW, lane, sm.row[warp], nullptr);
         }
         // tails of the per-entry rows past the valid entries (read by nothing but the debug
         // copy; written so that every output element is defined)
@@ -882,13 +1106,28 @@ __global__ void __launch_bounds__(NT, 2) k_phase1(Dims d, Inputs in, Work w, int
 
 // Steps 3 and 4 of the chunks whose scratch is in global memory: CTA (rb, n) takes a share of
 // chunk n's sorted positions (weights), the reads of its KR token rows and those rows of A and
-// QK. 8 warps, one row at a time each.
+// QK. 8 warps, one row at a time each. BIG (C >= kDenseMinChunk): the chunk's large groups are
+// dense (staged rows per warp), the reads search a sample of the sorted row first, and the
+// Gram rows keep four entries' member loads in flight; shared memory (dynamic):
+//   rows [8][kMaxChunk] float | BIG: drows [8][3 kMaxChunk] float, samples [kMaxSamples] u64
 constexpr int KR = 16;          // token rows per CTA
 constexpr int NTR = 256;
 
-template <typename WT>
-__global__ void __launch_bounds__(NTR) k_phase1_rows(Dims d, Inputs in, Work w, int step0) {
-    __shared__ float rows[NTR / 32][kMaxChunk];
+constexpr size_t rows_smem(bool big) {
+    return sizeof(float) * (NTR / 32) * kMaxChunk +
+           (big ? sizeof(float) * (NTR / 32) * 3 * kMaxChunk +
+                      sizeof(unsigned long long) * kMaxSamples
+                : 0);
+}
+
+template <typename WT, bool BIG>
+__global__ void __launch_bounds__(NTR, BIG ? 4 : 6) k_phase1_rows(Dims d, Inputs in, Work w,
+                                                                  int step0) {
+    extern __shared__ __align__(16) unsigned char rsm[];
+    float *rows = reinterpret_cast<float *>(rsm);
+    float *drows = BIG ? rows + (NTR / 32) * kMaxChunk : nullptr;
+    unsigned long long *smp =
+        BIG ? reinterpret_cast<unsigned long long *>(drows + (NTR / 32) * 3 * kMaxChunk) : nullptr;
     const int n = blockIdx.y, rb = blockIdx.x, nrb = gridDim.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int C = d.C, W = d.W, R = d.R, CW = C * W, CR = C * R, CC = C * C;
@@ -900,22 +1139,109 @@ __global__ void __launch_bounds__(NTR) k_phase1_rows(Dims d, Inputs in, Work w, 
     const unsigned long long *keyA = w.keys + (size_t)n * 2 * CW;
     const unsigned long long *srt = w.p1sel[n] ? keyA + CW : keyA;
     const float2 *tkk = reinterpret_cast<const float2 *>(w.p1sel[n] ? keyA : keyA + CW);
-    const P1Chunk<WT> pc{in.rs + tok_base * R, static_cast<const WT *>(in.qw) + tok_base * R,
+    P1Chunk<WT> pc{in.rs + tok_base * R, static_cast<const WT *>(in.qw) + tok_base * R,
                          srt, tkk, w.inv + (size_t)n * CW, w.pgid + (size_t)n * CW,
                          w.pgs + (size_t)n * CW, w.lws + (size_t)n * CW, w.lend + (size_t)n * CW,
                          w.kf + (size_t)n * CW, w.rlo + (size_t)n * CR, w.rhi + (size_t)n * CR,
                          w.wdw + (size_t)n * CW, w.gw + (size_t)n * CW, w.qw + (size_t)n * CR,
                          w.lr + (size_t)n * CR, w.A + (size_t)n * CC, w.QK + (size_t)n * CC,
                          d.bwd ? w.dwt + (size_t)n * CW : nullptr,
-                         nv, nw, nr, C, W, R, d.S};
+                         nv, nw, nr, C, W, R, d.S,
+                         nullptr, nullptr, nullptr, nullptr, nullptr, 0};
+    if (BIG && w.ndense[n] > 0) {
+        pc.dpos = w.dpos + (size_t)n * CW;
+        pc.dref = w.dref + (size_t)n * C;
+        pc.dka = w.dka + (size_t)n * C * dense_pitch(C);
+        pc.dkb = w.dkb + (size_t)n * C * dense_pitch(C);
+        pc.dkq = w.dkq + (size_t)n * C * dense_pitch(C);
+        pc.nd = w.ndense[n];
+    }
+    const int nsmp = BIG ? (nw + kSampleStep - 1) / kSampleStep : 0;
+    if (BIG)
+        for (int i = tid; i < nsmp; i += NTR) smp[i] = srt[(size_t)i * kSampleStep];
     const int per = (nw + nrb - 1) / nrb;
     const int pos0 = rb * per, pos1 = pos0 + per < nw ? pos0 + per : nw;
     p1_weights(pc, pos0, pos1, tid, NTR);
+    __syncthreads();
     const int t0 = rb * KR, t1 = t0 + KR < C ? t0 + KR : C;
     const int r1 = (t1 < nv ? t1 : nv) * R;
-    p1_reads(pc, t0 * R < r1 ? t0 * R : r1, r1, tid, NTR);
+    p1_reads<WT, BIG>(pc, t0 * R < r1 ? t0 * R : r1, r1, tid, NTR, smp, nsmp);
     __syncthreads();
-    p1_gram(pc, t0, t1, warp, NTR / 32, lane, rows[warp]);
+    p1_gram<WT, BIG ? 4 : 1>(pc, t0, t1, warp, NTR / 32, lane, rows + warp * kMaxChunk,
+                             BIG ? drows + warp * 3 * kMaxChunk : nullptr);
+}
+
+// The dense groups' part of A and QK, after k_phase1_rows wrote the pair sums of the other
+// groups: A[t][u] += sum_h dka[t][h] dkb[u][h] for u < t and QK[t][u] += sum_h dkq[t][h]
+// dkb[u][h] for u <= t, h ascending (one fused multiply-add chain per element, so each element
+// is a fixed-order sum). One CTA per 64 x 64 tile on or below the diagonal of a chunk; 256
+// threads, 4 x 4 elements of both products each, the factors staged 16 columns at a time.
+constexpr int GDT = 64, GDK = 16;
+
+__global__ void __launch_bounds__(256) k_gram_dense(Dims d, Work w) {
+    __shared__ __align__(16) float sa[GDK][GDT + 4];
+    __shared__ __align__(16) float sq[GDK][GDT + 4];
+    __shared__ __align__(16) float sb[GDK][GDT + 4];
+    const int n = blockIdx.y;
+    const int nd = w.ndense[n];
+    if (nd == 0) return;
+    const int C = d.C, dp = dense_pitch(C), hp = (nd + 3) & ~3;
+    int ti = 0, rem = blockIdx.x;        // tile (ti, ui), ui <= ti, row-major over the triangle
+    while (rem > ti) { rem -= ti + 1; ++ti; }
+    const int t0 = ti * GDT, u0 = rem * GDT;
+    const size_t fo = (size_t)n * C * dp;
+    const float *ka = w.dka + fo, *kb = w.dkb + fo, *kq = w.dkq + fo;
+    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+    const int lr = tid >> 2, lk = (tid & 3) * 4;   // the element group this thread stages
+    float accA[4][4], accQ[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) { accA[i][j] = 0.f; accQ[i][j] = 0.f; }
+    for (int k0 = 0; k0 < hp; k0 += GDK) {
+        const int k = k0 + lk;
+        float4 va = make_float4(0.f, 0.f, 0.f, 0.f), vq = va, vb = va;
+        if (k < hp) {                    // hp and k are multiples of 4: the float4 is inside
+            if (t0 + lr < C) {
+                va = *reinterpret_cast<const float4 *>(ka + (size_t)(t0 + lr) * dp + k);
+                vq = *reinterpret_cast<const float4 *>(kq + (size_t)(t0 + lr) * dp + k);
+            }
+            if (u0 + lr < C) vb = *reinterpret_cast<const float4 *>(kb + (size_t)(u0 + lr) * dp + k);
+        }
+        __syncthreads();
+        sa[lk][lr] = va.x; sa[lk + 1][lr] = va.y; sa[lk + 2][lr] = va.z; sa[lk + 3][lr] = va.w;
+        sq[lk][lr] = vq.x; sq[lk + 1][lr] = vq.y; sq[lk + 2][lr] = vq.z; sq[lk + 3][lr] = vq.w;
+        sb[lk][lr] = vb.x; sb[lk + 1][lr] = vb.y; sb[lk + 2][lr] = vb.z; sb[lk + 3][lr] = vb.w;
+        __syncthreads();
+#pragma unroll
+        for (int kk = 0; kk < GDK; ++kk) {
+            const float4 a4 = *reinterpret_cast<const float4 *>(&sa[kk][ty * 4]);
+            const float4 q4 = *reinterpret_cast<const float4 *>(&sq[kk][ty * 4]);
+            const float4 b4 = *reinterpret_cast<const float4 *>(&sb[kk][tx * 4]);
+            const float a[4] = {a4.x, a4.y, a4.z, a4.w}, q[4] = {q4.x, q4.y, q4.z, q4.w};
+            const float b[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    accA[i][j] = fmaf(a[i], b[j], accA[i][j]);
+                    accQ[i][j] = fmaf(q[i], b[j], accQ[i][j]);
+                }
+        }
+    }
+    float *A = w.A + (size_t)n * C * C, *QK = w.QK + (size_t)n * C * C;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int t = t0 + ty * 4 + i;
+        if (t >= C) continue;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int u = u0 + tx * 4 + j;
+            if (u > t || u >= C) continue;
+            if (u < t) A[(size_t)t * C + u] += accA[i][j];
+            QK[(size_t)t * C + u] += accQ[i][j];
+        }
+    }
 }
 
 }  // namespace
@@ -928,6 +1254,17 @@ size_t phase1_scratch_smem(const Dims &d) {
 
 bool phase1_split(const Dims &d) { return phase1_scratch_smem(d) > kPhase1SmemMax; }
 
+namespace {
+void launch_rows(void (*kern)(Dims, Inputs, Work, int), bool big, dim3 grid, const Dims &d,
+                 const Inputs &in, const Work &w, int step0, cudaStream_t st) {
+    const size_t smem = rows_smem(big);
+    set_kernel_smem(kern, smem);
+    kern<<<grid, NTR, smem, st>>>(d, in, w, step0);
+}
+}  // namespace
+
+bool dense_gram(const Dims &d) { return phase1_split(d) && d.C >= kDenseMinChunk; }
+
 cudaError_t launch_phase1(const Dims &d, const Inputs &in, const Work &w, int step0, int nsteps,
                           cudaStream_t st) {
     const size_t full = phase1_scratch_smem(d);
@@ -935,16 +1272,24 @@ cudaError_t launch_phase1(const Dims &d, const Inputs &in, const Work &w, int st
     const size_t smem = in_smem ? full : ((sizeof(P1Smem) + 15) & ~size_t(15)) + sizeof(P1Big);
     const int grid = w.G;
     const dim3 rows_grid((d.C + KR - 1) / KR, nsteps * d.P);
+    const bool big = dense_gram(d);
     if (d.dtype == SDM_BF16) {
         auto kern = k_phase1<__nv_bfloat16>;
         set_kernel_smem(kern, smem);
         kern<<<grid, NT, smem, st>>>(d, in, w, step0, nsteps, in_smem);
-        if (!in_smem) k_phase1_rows<__nv_bfloat16><<<rows_grid, NTR, 0, st>>>(d, in, w, step0);
+        if (!in_smem) launch_rows(big ? k_phase1_rows<__nv_bfloat16, true>
+                                      : k_phase1_rows<__nv_bfloat16, false>,
+                                  big, rows_grid, d, in, w, step0, st);
     } else {
         auto kern = k_phase1<float>;
         set_kernel_smem(kern, smem);
         kern<<<grid, NT, smem, st>>>(d, in, w, step0, nsteps, in_smem);
-        if (!in_smem) k_phase1_rows<float><<<rows_grid, NTR, 0, st>>>(d, in, w, step0);
+        if (!in_smem) launch_rows(big ? k_phase1_rows<float, true> : k_phase1_rows<float, false>,
+                                  big, rows_grid, d, in, w, step0, st);
+    }
+    if (dense_gram(d)) {
+        const int nt = (d.C + GDT - 1) / GDT;
+        k_gram_dense<<<dim3(nt * (nt + 1) / 2, nsteps * d.P), 256, 0, st>>>(d, w);
     }
     return cudaGetLastError();
 }

@@ -23,6 +23,10 @@ constexpr size_t kPhase1SmemMax = 110 * 1024;        // Phase-1 scratch kept on 
 constexpr size_t kPipeSmemMax = 224 * 1024;          // pipelined Phase 2 when two stages fit
 constexpr long kSpinLimit = 1L << 22;   // mbarrier polls before a wait gives up (seconds at most)
 constexpr int32_t kNoEntry = INT32_MIN;  // Work::wsl / rsl: no entry
+constexpr float kDenseSpan = 64.f;      // widest running log-decay range of a dense Gram group
+constexpr int kDenseMinChunk = 128;     // smallest chunk whose large groups go dense
+// row pitch (floats) of the dense Gram factors: C rounded up to 16 bytes
+__host__ __device__ __forceinline__ int dense_pitch(int C) { return (C + 3) & ~3; }
 
 // Device status block at the start of the workspace (sdm_device_status, with the first bad
 // token stored +1 so that a zero fill means "none").
@@ -99,6 +103,17 @@ struct Work {
     float *kf;          // [G][CW]  write weight of each entry as float (0 for a bad slot)
     int32_t *rlo;       // [G][CR]  first write position of the read's slot group
     int32_t *rhi;       // [G][CR]  last write position at or before the read's token (-1: none)
+    // dense Gram groups of the chunks whose Phase-1 scratch is in global memory (sized only
+    // then): large groups whose pair sums are taken as the product of two per-token factors
+    // around a reference log-decay of the group (k_gram_dense), DC = C of them at most
+    int32_t *dpos;      // [G][CW]  dense index of each sorted position's group (-1: pair sums)
+    float *dref;        // [N][DC]  reference log-decay of each dense group
+    int32_t *ndense;    // [N]      dense groups of the chunk
+    float *dka;         // [N][C][dense_pitch] sum over the token's writes of group h of
+                        //           k exp(lw - ref)
+    float *dkb;         // [N][C][dense_pitch] the same with exp(ref - lw)
+    float *dkq;         // [N][C][dense_pitch] sum over the token's reads of group h of
+                        //           q exp(lr - ref)
     // kept for the backward (sized only when Dims::bwd)
     unsigned long long *wkey;   // [N][CW]  sorted write keys (slot << 32 | t << 8 | j)
     float *wlws;        // [N][CW]   running log-decay at each sorted position
@@ -198,6 +213,9 @@ cudaError_t launch_phase2_fused(const Dims &d, const Inputs &in, const Work &w, 
 size_t phase2_pipe_smem(const Dims &d);
 // Phase-1 scratch in global memory: steps 3 and 4 run in a second kernel over row blocks
 bool phase1_split(const Dims &d);
+// chunks whose Phase-1 scratch is in global memory and whose large groups' Gram sums go dense
+// (k_gram_dense): C >= kDenseMinChunk
+bool dense_gram(const Dims &d);
 // sdm_write_read_host: arrays copied from mapped page-locked host memory by one kernel
 // (device addresses of the host pages; 16-byte aligned; sizes in 16-byte units)
 struct HostCopyTable {

@@ -36,7 +36,7 @@ def test_workspace_bytes_host_only():
     n = sdm.workspace_bytes(s)
     assert n > 0 and n % 256 == 0
     # the slab is bounded: more tokens do not grow the workspace past the slab budget
-    big = sdm.make_shape(4, 16384, 256, 1 << 20, 256, 256, 256, sdm.SDM_BF16)
+    big = sdm.make_shape(4, 1 << 17, 256, 1 << 20, 256, 256, 256, sdm.SDM_BF16)
     huge = sdm.make_shape(4, 1 << 19, 256, 1 << 20, 256, 256, 256, sdm.SDM_BF16)
     assert sdm.workspace_bytes(huge) == sdm.workspace_bytes(big)
     # explicit slabs: fewer steps held, less workspace
@@ -57,9 +57,9 @@ def test_launch_count():
                        flags=sdm.FLAG_PER_STEP_KERNELS)
     assert sdm.launch_count(s) == 2 * slabs + 3 * nt
     # chunks whose metadata does not fit on chip twice take the per-step kernels; chunks whose
-    # Phase-1 scratch does not fit on chip add Phase 1's row kernel
+    # Phase-1 scratch does not fit on chip add Phase 1's row and dense-Gram kernels
     s = sdm.make_shape(16, 4096, 128, 131072, 128, 64, 64, sdm.SDM_F32, slab_steps=32)
-    assert sdm.launch_count(s) == 3 + 3 * 32
+    assert sdm.launch_count(s) == 4 + 3 * 32
 
 
 @pytest.mark.parametrize("kw,code", [

@@ -173,19 +173,47 @@ def test_repeated_write_slot_is_counted():
 
 def _phase1_launches(wl) -> int:
     """Phase-1 launches per slab for the shape of ``wl``: 1 with the chunk's scratch on chip,
-    2 when Phase 1 splits into the sort kernel and the row kernel over global scratch (the
-    per-step launch count of one slab is Phase 1 + solve + 3 per step)."""
+    2 when Phase 1 splits into the sort kernel and the row kernel over global scratch, 3 with
+    the dense-Gram kernel (C >= 128) (the per-step launch count of one slab is Phase 1 + solve
+    + 3 per step)."""
     shape = sdm.make_shape(wl.P, wl.T, wl.C, wl.S, wl.D, wl.W, wl.R,
                            torch.float32 if wl.dtype == "f32" else torch.bfloat16,
                            wl.Nt, sdm.FLAG_PER_STEP_KERNELS)
     return sdm.launch_count(shape) - 1 - 3 * wl.Nt
 
 
-def _check_phase1(wl, values=True):
+def _dense_groups(slots, lw, C):
+    """Groups of one chunk that the split Phase-1 path should take in the dense Gram form
+    (slots and lw of the chunk's valid write entries, token-major): none below C = 128; else
+    the groups of at least thr members, thr the least of (C/8) * 2^L (L < 8) that leaves at
+    most C of them, whose running log-decays lie within 64 of each other."""
+    s, l = slots.ravel(), lw.ravel()
+    if s.size == 0 or C < 128:
+        return 0
+    _, inv, cnt = np.unique(s, return_inverse=True, return_counts=True)
+    thr0 = max(4, C // 8)
+    for lev in range(8):
+        thr = thr0 << lev
+        if (cnt >= thr).sum() <= C:
+            break
+    else:
+        return 0
+    n = 0
+    for gi in np.nonzero(cnt >= thr)[0]:
+        ls = l[inv == gi]
+        span = ls.max() - ls.min()
+        assert abs(span - 64.0) > 1e-3, "a group's span is too close to the dense limit"
+        n += int(span <= 64.0)
+    return n
+
+
+def _check_phase1(wl, values=True, inputs=None, dense=None):
     """Phase 1 and the solve against the oracle, chunk by chunk: the dedup plan (perm, group
     starts, owners, group count) bit for bit, and (``values``) lw, gw, dw, lr, qw, A, QK, X and
-    QX within float32 rounding of the oracle's chunked form."""
-    inputs = si.generate(wl)
+    QX within float32 rounding of the oracle's chunked form. ``dense`` (split path, with
+    ``values``): check each chunk's dense Gram group count against the rule and require at
+    least that many dense groups over the call (True: at least one)."""
+    inputs = si.generate(wl) if inputs is None else inputs
     dev = to_device(inputs, wl)
     out = sdm.phase1_debug(dev["write_slots"], dev["write_w"], dev["log_decay"], dev["beta"],
                            dev["read_slots"], dev["read_w"], dev["valid"], S=wl.S, D=wl.D,
@@ -196,6 +224,8 @@ def _check_phase1(wl, values=True):
     C, W = wl.C, wl.W
     perm, gs, ow = (out[k].cpu().numpy() for k in ("perm", "group_start", "owner"))
     ng = out["ngroups"].cpu().numpy()
+    ndense = out["dense_groups"].cpu().numpy()
+    dense_total = 0
     for ti in range(wl.Nt):
         for p in range(wl.P):
             n = ti * wl.P + p
@@ -210,12 +240,19 @@ def _check_phase1(wl, values=True):
             if not values:
                 continue
             _, _, d = oracle.chunked(C, *oracle_args(x), debug=(p, ti))
+            if dense is not None:
+                want = _dense_groups(inputs["write_slots"][p, ti * C:ti * C + nv],
+                                     d["lw"][:nv], C)
+                assert int(ndense[n]) == want, (ti, p, int(ndense[n]), want)
+                dense_total += want
             for key, ref in (("lw", d["lw"]), ("gw", d["gw"]), ("dw", d["dw"]), ("lr", d["lr"]),
                              ("qw", d["qw"]), ("A", d["A"]), ("QK", d["QK"]), ("X", d["X"]),
                              ("QX", d["QX"])):
                 got = out[key][n].double().cpu().numpy().reshape(ref.shape)
                 scale = max(np.abs(ref).max(), 1e-30)
                 assert np.abs(got - ref).max() <= 2e-6 * scale + 1e-30, (key, ti, p)
+    if dense is not None:
+        assert dense_total >= (1 if dense is True else dense), dense_total
 
 
 def test_phase1_plan_and_intermediates():
@@ -223,6 +260,15 @@ def test_phase1_plan_and_intermediates():
     wl = small_workload(P=2, T=70, C=16, S=20, D=32, W=4, R=3, ragged=True, seed=15)
     assert _phase1_launches(wl) == 1
     _check_phase1(wl)
+
+
+def _steep_odd_slots(inputs, factor=40.0):
+    """The log-decays of the writes to odd slots times ``factor``: large groups of odd slots
+    then span far more than the dense form's limit and keep their pair sums."""
+    g = inputs["log_decay"]
+    odd = (inputs["write_slots"] % 2) == 1
+    inputs["log_decay"] = np.where(odd, g * np.float32(factor), g).astype(np.float32)
+    return inputs
 
 
 @pytest.mark.parametrize("wl,values", [
@@ -241,10 +287,61 @@ def test_phase1_plan_and_intermediates():
                     slots="mix", ragged=False, seed=19), False),
 ], ids=["c64_w32_zipf", "c128_w64_uniform", "c256_w32_mix", "c256_w256_mix_plan"])
 def test_phase1_split_path(wl, values):
-    """The Phase-1 path over global scratch (sort kernel + row kernel), which the larger
-    workloads take: its dedup plan bit for bit, and the values within float32 rounding."""
-    assert _phase1_launches(wl) == 2
-    _check_phase1(wl, values)
+    """The Phase-1 path over global scratch (sort kernel + row kernel + dense-Gram kernel),
+    which the larger workloads take: its dedup plan bit for bit, and the values within float32
+    rounding."""
+    assert _phase1_launches(wl) == (3 if wl.C >= 128 else 2)
+    _check_phase1(wl, values, dense=False if values else None)
+
+
+@pytest.mark.parametrize("case", ["mix", "steep_odd", "crowded"])
+def test_phase1_dense_gram_groups(case):
+    """The large groups' Gram sums in the dense factor form, against the oracle's pair sums:
+    - mix: the half-Zipf(1.2) mix at C=256, whose hot slots go dense;
+    - steep_odd: the same with 40x the log-decay on odd slots, whose large groups then span
+      past the dense limit and keep their pair sums beside the dense even ones;
+    - crowded: 300 slots under 64 writes per token, so more than C groups reach the first
+      size threshold and the threshold doubles."""
+    if case == "crowded":
+        wl = small_workload(P=1, T=256 + 60, C=256, S=300, D=64, W=64, R=48, dtype="f32",
+                            slots="uniform", ragged=False, seed=21)
+    else:
+        wl = small_workload(P=1, T=300, C=256, S=4096, D=64, W=32, R=32, dtype="bf16",
+                            slots="mix", ragged=False, seed=20)
+    assert _phase1_launches(wl) == 3
+    inputs = si.generate(wl)
+    if case == "steep_odd":
+        inputs = _steep_odd_slots(inputs)
+    _check_phase1(wl, True, inputs=inputs, dense=True)
+    if case == "steep_odd":
+        # the large odd groups really were left to the pair sums
+        x = oracle.from_stored(inputs, wl.dtype)
+        _, _, d = oracle.chunked(wl.C, *oracle_args(x), debug=(0, 0))
+        s = inputs["write_slots"][0, :wl.C].ravel()
+        l = d["lw"].ravel()
+        _, inv, cnt = np.unique(s, return_inverse=True, return_counts=True)
+        odd_big = [gi for gi in np.nonzero(cnt >= 32)[0] if s[inv == gi][0] % 2 == 1]
+        assert odd_big and all(np.ptp(l[inv == gi]) > 64.0 for gi in odd_big)
+    # the dense form gives the same bits on a second call (fixed-order sums)
+    dev = to_device(inputs, wl)
+    outs = [sdm.phase1_debug(dev["write_slots"], dev["write_w"], dev["log_decay"], dev["beta"],
+                             dev["read_slots"], dev["read_w"], dev["valid"], S=wl.S, D=wl.D,
+                             chunk_size=wl.C) for _ in range(2)]
+    for k in ("A", "QK", "X", "QX"):
+        assert torch.equal(outs[0][k], outs[1][k]), k
+
+
+def test_full_size_dense_gram_path():
+    """The widest workload's chunk shape (C=256, W=R=256, the mix) reaches the dense form and
+    stays within tolerance end to end (two streams, four chunks each)."""
+    wl = small_workload(P=2, T=4 * 256, C=256, S=1 << 20, D=64, W=256, R=256, dtype="bf16",
+                        slots="mix", ragged=False, seed=22)
+    dev = to_device(si.generate(wl), wl)
+    out = sdm.phase1_debug(dev["write_slots"], dev["write_w"], dev["log_decay"], dev["beta"],
+                           dev["read_slots"], dev["read_w"], dev["valid"], S=wl.S, D=wl.D,
+                           chunk_size=wl.C)
+    assert (out["dense_groups"].cpu().numpy() > 16).all()
+    check(wl)
 
 
 @pytest.mark.parametrize("cfg", [1, 2, 3, 4])

@@ -493,7 +493,7 @@ def run_ours(args):
                 "unit": pk_unit, "frac": ach / pk, "peak_source": pk_src,
                 "alg_units_per_launch": units, "alg_unit": unit_name,
                 "launch_us": secs * 1e6,
-                "traffic": traffic_record(dom, wl.name) if bound == "hbm" else None}
+                "traffic": traffic_record(dom, wl.name)}
     p2_ms = fam_ms["gather"] + fam_ms["dw"] + fam_ms["phase2"]
     p2_secs = p2_ms / args.profile_steps / 1e3
     p2_ach = alg["phase2"] / p2_secs / 1e9

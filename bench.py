@@ -72,6 +72,8 @@ def parse_args():
     ap.add_argument("--layer-io", action="store_true",
                     help="time the layer I/O kernels (head split/merge, bank expand/sum) on the "
                          "batch 4 x 8 heads layout of the ragged workload instead")
+    ap.add_argument("--product-key", action="store_true",
+                    help="time the product-key exact top-k (forward and backward) instead")
     ap.add_argument("--snapshot-quant", choices=["none", "bf16", "fp8"], default="none",
                     help="with --backward: store the snapshot in bfloat16 (float32 banks) or "
                          "float8_e4m3fn")
@@ -771,8 +773,63 @@ def run_layer_io(args):
     print(json.dumps(line), flush=True)
 
 
+def run_product_key(args):
+    """The product-key exact top-k on the GPU: 65536 rows of N(0, 1) scores in bfloat16 and
+    float32, k = 256, two factors of 512 (2^18 slots) and four of 32 (2^20 slots). Forward and
+    backward are each timed with CUDA events over K launches after W warm-ups, L2 flushed (512
+    MiB write) before each; rows/s per case."""
+    import torch
+
+    import sparse_addressed_delta_gb300 as sdm
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    rows, k = 65536, 256
+    g = torch.Generator(device=dev).manual_seed(7)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    res = {}
+    clocks = ClockSampler(0)
+    for dt in (torch.bfloat16, torch.float32):
+        for factors in ((512, 512), (32, 32, 32, 32)):
+            raw = torch.randn((rows, sum(factors)), device=dev, generator=g).to(dt)
+            val, lin = sdm.product_key_topk(raw, factors, k)
+            gv = torch.randn(val.shape, device=dev, generator=g).to(dt)
+
+            def timed(fn):
+                for _ in range(args.warmup):
+                    fn()
+                ts = []
+                for _ in range(args.steps):
+                    flush.zero_()
+                    a = torch.cuda.Event(enable_timing=True)
+                    b = torch.cuda.Event(enable_timing=True)
+                    a.record()
+                    fn()
+                    b.record()
+                    b.synchronize()
+                    ts.append(a.elapsed_time(b))
+                return statistics.median(ts)
+            fwd = timed(lambda: sdm.product_key_topk(raw, factors, k))
+            bwd = timed(lambda: sdm.product_key_topk_backward(lin, gv, factors, k))
+            name = f"{'bf16' if dt == torch.bfloat16 else 'f32'}_F{len(factors)}x{factors[0]}"
+            res[name] = {"forward_ms": fwd, "forward_rows_per_s": rows / fwd * 1e3,
+                         "backward_ms": bwd, "backward_rows_per_s": rows / bwd * 1e3}
+    clk = clocks.stop()
+    line = {"metric": "product-key exact top-k rows/s (forward)",
+            "value": statistics.mean(r["forward_rows_per_s"] for r in res.values()),
+            "unit": "rows/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "higher_is_better": True, "dtype": "bf16+f32", "data": "synthetic",
+            "config": {"workload": f"{rows} rows, k={k}, factors 2 x 512 and 4 x 32",
+                       "l2": "flushed before every launch (512 MiB write)"},
+            "cases": res, "clocks": clk, "gpu": torch.cuda.get_device_name(dev)}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.product_key:
+        run_product_key(args)
+        return
     if args.ncu_run:
         run_for_profiler(args)
         return

@@ -370,21 +370,44 @@ __global__ void __launch_bounds__(MM_T) k_dualmm(Dims d, Inputs in, Work w, int 
 // A CTA owns one chunk and one slice of DS = 32 CPS columns, and first copies the chunk's
 // delta_v slice ([C][DS] float32, at most 128 KB) into shared memory: every delta_v row is read
 // by every group that row's token writes (W groups), so from L2 those few rows would be
-// requested by every SM at once. The CTA's warps then take the chunk's groups in a stride, in
-// the DW order Phase 1 wrote (hot groups first, then by size, so the long member lists spread
-// over the warps). A warp holds the metadata of 32 of its groups (lane l: group l, loaded one
-// batch ahead), loads the B0 slices of U groups before adding any, and reads the members'
-// delta_v from shared memory (member records 32 at a time, one batch ahead).
+// requested by every SM at once. The hot groups (the first ones of the DW order Phase 1 wrote:
+// at least kHotGroup members) come first, a share of them per CTA, each summed by the whole
+// CTA: their metadata, member records and B0 slices are staged in shared memory in one pass
+// per round, every warp sums a fixed share of a group's members (in sorted order), and the
+// shares are added to exp(lend) B0 in warp order. A hot group summed by one warp would hold
+// that warp (and the step) for its whole member list. The other groups go to the warps in a
+// stride: a warp holds the metadata of 32 of its groups (lane l: group l, loaded one batch
+// ahead), loads the B0 slices of U groups before adding any, and reads the members' delta_v
+// from shared memory (member records 32 at a time, one batch ahead).
 // ---------------------------------------------------------------------------------------
 constexpr int DW_T = 1024;                   // threads per DW CTA (32 warps, 64 registers each)
 constexpr int DW_W = DW_T / 32;
 constexpr size_t kDwSmem = 128 * 1024;       // delta_v slice of a chunk in shared memory
+constexpr int kDwHB = 16;                    // hot groups staged per round
+constexpr int kDwRec = 2048;                 // member records staged per round
 
-// columns per lane of a DW slice: the slice DS = 32 * CPS divides D, and C * DS floats fit in
-// kDwSmem
-__host__ __device__ inline int dw_cps(const Dims &d) {
+// the round's hot groups in shared memory (after the partial sums, B0 slices and records)
+struct DwHot {
+    int o0[kDwHB], nm[kDwHB], sl[kDwHB], roff[kDwHB + 1], toff[kDwHB + 1];
+    float f[kDwHB];
+    int cnt, big;
+};
+
+// dynamic shared memory of k_dw: delta_v slice [C][DS], partial sums [DW_W][DS], B0 slices
+// [kDwHB][DS], records (token, weight) [kDwRec] x 2, DwHot
+inline size_t dw_smem_bytes(int C, int DS) {
+    return sizeof(float) * ((size_t)C * DS + (size_t)DW_W * DS + (size_t)kDwHB * DS) +
+           8 * (size_t)kDwRec + sizeof(DwHot);
+}
+
+constexpr size_t kDwSmemMax = 200 * 1024;    // all of k_dw's shared memory
+
+// columns per lane of a DW slice: the slice DS = 32 * CPS divides D, C * DS floats fit in
+// kDwSmem and the whole layout in kDwSmemMax
+inline int dw_cps(const Dims &d) {
     int ds = d.D;
-    while ((size_t)d.C * ds * 4 > kDwSmem && ds > 32) ds >>= 1;
+    while (((size_t)d.C * ds * 4 > kDwSmem || dw_smem_bytes(d.C, ds) > kDwSmemMax) && ds > 32)
+        ds >>= 1;
     return ds / 32;
 }
 
@@ -414,6 +437,7 @@ __global__ void __launch_bounds__(DW_T, 1) k_dw(Dims d, Inputs in, Work w, int s
     }
 
     const int ng = w.ngroups[n];
+    const int nhot = w.ng4[n].y;                       // gord positions [0, nhot): hot groups
     const int32_t *goff = w.goff + (size_t)n * goff_stride(CW);
     const int32_t *gslot = w.gslot + (size_t)n * CW;
     const int32_t *gord = w.gord + (size_t)n * CW;
@@ -423,7 +447,7 @@ __global__ void __launch_bounds__(DW_T, 1) k_dw(Dims d, Inputs in, Work w, int s
     BT *bank = static_cast<BT *>(in.bank) + stream_row0(d, p) * D + (size_t)cs * DS + lane * CPS;
     const float *dvl = dvs + lane * CPS;
     const unsigned magic = div_magic(W);
-    const int base = ck * DW_W + warp, stride = cpp * DW_W;
+    const int base = nhot + ck * DW_W + warp, stride = cpp * DW_W;
     const int mine = base < ng ? (ng - base + stride - 1) / stride : 0;
     const bool snap = in.snap != nullptr;
 
@@ -447,6 +471,155 @@ __global__ void __launch_bounds__(DW_T, 1) k_dw(Dims d, Inputs in, Work w, int s
     meta(32, nslot, no0, no1, nt1, nf, nw1);
     cp_async_wait<0>();
     __syncthreads();
+
+    // hot groups at gord positions ck, ck + cpp, ... (< nhot), by the whole CTA, in rounds:
+    // a group's members split into chunks of 32 (in sorted order); the warps take the round's
+    // chunks one each, and warp i adds group i's chunk sums to exp(lend) B0 in chunk order, so
+    // every row is a fixed-order sum that depends on its own group alone
+    {
+        float *part = dvs + (size_t)C * DS;            // [DW_W][DS] chunk sums
+        float *b0s = part + DW_W * DS;
+        int *rec_t = reinterpret_cast<int *>(b0s + kDwHB * DS);
+        float *rec_w = reinterpret_cast<float *>(rec_t + kDwRec);
+        DwHot &hv = *reinterpret_cast<DwHot *>(rec_w + kDwRec);
+        for (int h0 = 0; ck + h0 * cpp < nhot;) {
+            if (warp == 0) {
+                // the round: the next groups of this CTA whose records and chunks fit together;
+                // a first group that alone does not fit is summed from global memory (big)
+                const int q = ck + (h0 + lane) * cpp;
+                const bool have = lane < kDwHB && q < nhot;
+                int o0 = 0, nm = 0, sl = -1;
+                float f = 0.f;
+                if (have) {
+                    const int g = gord[q];
+                    o0 = goff[g];
+                    nm = goff[g + 1] - o0;
+                    sl = gslot[g];
+                    if ((unsigned)sl >= (unsigned)d.S) sl = -1;
+                    f = gfac[g];
+                }
+                int inc = nm, tinc = (nm + 31) >> 5;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, inc, off);
+                    const int z = __shfl_up_sync(0xffffffffu, tinc, off);
+                    if (lane >= off) { inc += y; tinc += z; }
+                }
+                const unsigned fit =
+                    __ballot_sync(0xffffffffu, have && inc <= kDwRec && tinc <= DW_W);
+                int cnt = __ffs(~fit) - 1;                 // leading lanes that fit
+                const int big = cnt == 0 ? 1 : 0;          // lane 0 has a group (the loop test)
+                if (big) cnt = 1;
+                const int tot = big ? 0 : __shfl_sync(0xffffffffu, inc, cnt - 1);
+                const int ttot = big ? DW_W : __shfl_sync(0xffffffffu, tinc, cnt - 1);
+                if (lane < cnt) {
+                    hv.o0[lane] = o0;
+                    hv.nm[lane] = nm;
+                    hv.sl[lane] = sl;
+                    hv.f[lane] = f;
+                    hv.roff[lane] = big ? 0 : inc - nm;
+                    hv.toff[lane] = big ? 0 : tinc - ((nm + 31) >> 5);
+                }
+                if (lane == 0) {
+                    hv.roff[cnt] = tot;
+                    hv.toff[cnt] = ttot;
+                    hv.cnt = cnt;
+                    hv.big = big;
+                }
+            }
+            __syncthreads();
+            const int cnt = hv.cnt, big = hv.big, tot = hv.roff[cnt], ntask = hv.toff[cnt];
+            for (int idx = tid; idx < tot; idx += DW_T) {
+                int i = 0;
+                while (i + 1 < cnt && hv.roff[i + 1] <= idx) ++i;
+                const int pos = hv.o0[i] + (idx - hv.roff[i]);
+                rec_t[idx] = div_by(perm[pos], magic);
+                rec_w[idx] = wdw[pos];
+            }
+            if (warp < cnt && hv.sl[warp] >= 0) {
+                Raw<BT, CPS> r;
+                raw_load(bank + (size_t)hv.sl[warp] * D, r);
+                float a[CPS];
+                raw_widen(r, a);
+#pragma unroll
+                for (int c = 0; c < CPS; ++c) b0s[warp * DS + lane * CPS + c] = a[c];
+            }
+            __syncthreads();
+            float acc[CPS];
+#pragma unroll
+            for (int c = 0; c < CPS; ++c) acc[c] = 0.f;
+            if (!big) {
+                // task `warp`: chunk warp - toff[i] of group i (records in shared memory)
+                if (warp < ntask) {
+                    int i = 0;
+                    while (i + 1 < cnt && hv.toff[i + 1] <= warp) ++i;
+                    const int m0 = (warp - hv.toff[i]) * 32;
+                    const int m1 = hv.nm[i] - m0 < 32 ? hv.nm[i] : m0 + 32;
+                    const int r0 = hv.roff[i];
+                    for (int m = m0; m < m1; ++m) {
+                        float x[CPS];
+                        const float wv = rec_w[r0 + m];
+                        load_vec<float, CPS, false>(dvl + rec_t[r0 + m] * DS, x);
+#pragma unroll
+                        for (int c = 0; c < CPS; ++c) acc[c] = fmaf(wv, x[c], acc[c]);
+                    }
+                }
+            } else {
+                // one large group: warp w sums its chunks w, w + DW_W, ... in order (records
+                // from global memory)
+                const int o0 = hv.o0[0], nm = hv.nm[0];
+                for (int m0 = warp * 32; m0 < nm; m0 += DW_W * 32) {
+                    int t = 0;
+                    float wl = 0.f;
+                    if (m0 + lane < nm) {
+                        t = div_by(perm[o0 + m0 + lane], magic);
+                        wl = wdw[o0 + m0 + lane];
+                    }
+                    const int mc = nm - m0 < 32 ? nm - m0 : 32;
+                    for (int v = 0; v < mc; ++v) {
+                        float x[CPS];
+                        const int tv = __shfl_sync(0xffffffffu, t, v);
+                        const float wv = __shfl_sync(0xffffffffu, wl, v);
+                        load_vec<float, CPS, false>(dvl + tv * DS, x);
+#pragma unroll
+                        for (int c = 0; c < CPS; ++c) acc[c] = fmaf(wv, x[c], acc[c]);
+                    }
+                }
+            }
+            if (warp < ntask) {
+#pragma unroll
+                for (int c = 0; c < CPS; ++c) part[warp * DS + lane * CPS + c] = acc[c];
+            }
+            __syncthreads();
+            if (warp < cnt && hv.sl[warp] >= 0) {
+                const int i = warp;
+                float b0[CPS], out[CPS];
+                const float f = hv.f[i];
+#pragma unroll
+                for (int c = 0; c < CPS; ++c) {
+                    b0[c] = b0s[i * DS + lane * CPS + c];
+                    out[c] = b0[c] * f;
+                }
+                if (snap) {
+                    const size_t so =
+                        ((size_t)(ti * d.P + p) * CW + (hv.o0[i] + hv.nm[i] - 1)) * D +
+                        (size_t)cs * DS + lane * CPS;
+                    if (d.snapq == 2)
+                        store_fp8<CPS>(static_cast<unsigned char *>(in.snap) + so, b0);
+                    else if (d.snapq)
+                        store_vec<__nv_bfloat16, CPS>(static_cast<__nv_bfloat16 *>(in.snap) + so, b0);
+                    else
+                        store_vec<BT, CPS>(static_cast<BT *>(in.snap) + so, b0);
+                }
+                for (int j = hv.toff[i]; j < hv.toff[i + 1]; ++j)
+#pragma unroll
+                    for (int c = 0; c < CPS; ++c) out[c] += part[j * DS + lane * CPS + c];
+                store_vec<BT, CPS>(bank + (size_t)hv.sl[i] * D, out);
+            }
+            __syncthreads();
+            h0 += cnt;
+        }
+    }
 
     for (int b = 0; b < mine; b += 32) {
         if (b > 0) {
@@ -590,7 +763,7 @@ template <typename BT, int CPS>
 cudaError_t dw_cps_launch(const Dims &d, const Inputs &in, const Work &w, int step0, int ti,
                           cudaStream_t st) {
     // one 32-warp CTA per SM, the SMs shared out over the (chunk, slice) pairs in whole waves
-    const size_t smem = (size_t)d.C * 32 * CPS * 4;
+    const size_t smem = dw_smem_bytes(d.C, 32 * CPS);
     const int pairs = d.P * (d.D / (32 * CPS));
     int cpp = kRefSms / pairs;
     const int need = (d.C * d.W + DW_W - 1) / DW_W;

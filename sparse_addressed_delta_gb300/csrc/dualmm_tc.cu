@@ -8,19 +8,22 @@
 // n-tile, p) computes 128 rows x NT columns of both products: two float32 accumulators in
 // tensor memory (2 NT columns), written by tcgen05.mma kind::tf32 (M = 128, N = NT, K = 8),
 // issued by one thread, over K = the tokens the rows can see (X and QX are lower triangular)
-// that are valid, in K-blocks of 32 staged in shared memory twice over (the next block is
-// loaded while the tensor cores work on the current ones; tcgen05.commit on the block's
-// mbarrier releases its buffer). Operands are K-major with no swizzle: the canonical layout of
-// 8-row x 16-byte core matrices, element (r, k) of a tile at ((r / 8) KB/4 + k / 4) 32 +
-// (r % 8) 4 + k % 4 floats (KB = 32), i.e. core matrices 128 bytes apart along K (the leading
-// byte offset) and 1024 bytes apart along the rows (the stride byte offset). X and QX rows are
-// copied as they are; u_pre [k][n] is transposed into the B tile (n, k) while staging. bfloat16
-// banks: one TF32 product (operands rounded to nearest on the bit pattern); float32 banks: the
-// 3xTF32 split (lo * hi + hi * lo + hi * hi, each operand's hi its TF32 rounding and lo the
-// rounded rest) for float32 accuracy. The epilogue: warp w reads accumulator lanes 32 w .. 32 w
-// + 31 (one row per thread) with tcgen05.ld, adds inter and stores both rows. Every wait is
-// bounded; a wait that gives up sets SDM_ERR_TIMEOUT in the device status, and the kernel still
-// waits (with the default limit) for the products it issued before freeing tensor memory.
+// that are valid, in K-blocks of 32. The tensor memory accelerator copies each block's three
+// tiles (128 rows of X and of QX, NT rows of u_pre transposed; 32 floats = 128 bytes of K per
+// row) into shared memory with the 128-byte swizzle, which is the K-major layout the matrix
+// descriptors read (8-row groups 1024 bytes apart; a K = 8 step is 32 bytes further along the
+// row). NSTAGE blocks are in flight: a block's copies complete on its `full` mbarrier, and
+// tcgen05.commit of its products on its `empty` mbarrier releases the stage for the block
+// NSTAGE later. bfloat16 banks: one TF32 product (the tensor core reads the top 19 bits of each
+// float); float32 banks: the 3xTF32 split (lo * hi + hi * lo + hi * hi, each operand's lo the
+// part of it the TF32 read drops, formed in shared memory next to the tile) for float32
+// accuracy. The epilogue: warp w reads accumulator lanes 32 w .. 32 w + 31 (one row per
+// thread) with tcgen05.ld, adds inter and stores both rows. Every wait is bounded; a wait that
+// gives up sets SDM_ERR_TIMEOUT in the device status, and the kernel still waits (with the
+// default limit) for the copies and products it issued before freeing tensor memory.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "sdm_internal.cuh"
 
 namespace sdm {
@@ -28,34 +31,38 @@ namespace {
 
 constexpr int TC_T = 128;        // threads: four warps, one per 32 accumulator lanes
 constexpr int TC_M = 128;        // rows per CTA (one MMA M)
-constexpr int TC_KB = 32;        // K per staged block (4 MMAs of K = 8)
+constexpr int TC_KB = 32;        // K per staged block: one 128-byte swizzle row of floats
 
-__host__ __device__ constexpr int tc_tile_floats(int rows) { return rows * TC_KB; }
-
-// stage s holds the X tile and the QX tile [128 x 32] and the B tile [NT x 32] (raw float32:
-// the tensor core reads the TF32 truncation of each value, the "hi" part), and for float32
-// banks the same three tiles again with the "lo" parts x - trunc_tf32(x)
+// stage s: the X tile [128 x 32], the QX tile [128 x 32] and the u_pre tile [NT x 32] as the
+// tensor memory accelerator writes them (128-byte swizzle), and for float32 banks the same
+// three tiles again with the lo parts
 template <int NT, int PARTS>
 struct TcSmem {
-    static constexpr int A = tc_tile_floats(TC_M), B = tc_tile_floats(NT);
-    static constexpr int TILES = 2 * A + B;                      // floats of one part
-    static constexpr int STAGE = PARTS * TILES;
-    // K-blocks in flight: as many as about 220 KB of shared memory holds (one CTA per SM, so
-    // that a CTA's loads overlap instead of taking a round trip per block)
-    static constexpr int NS0 = (220 * 1024) / (int)(sizeof(float) * STAGE);
+    static constexpr int A_BYTES = TC_M * TC_KB * 4;
+    static constexpr int B_BYTES = NT * TC_KB * 4;
+    static constexpr int PART = 2 * A_BYTES + B_BYTES;
+    static constexpr int STAGE = PARTS * PART;
+    static constexpr int NS0 = (200 * 1024) / STAGE;
     static constexpr int NSTAGE = NS0 > 8 ? 8 : (NS0 < 2 ? 2 : NS0);
-    static constexpr size_t BYTES = sizeof(float) * NSTAGE * STAGE + 64;
+    // + the alignment of the tiles to 1024 bytes, the barriers and the tensor memory address
+    static constexpr size_t BYTES = (size_t)NSTAGE * STAGE + 1024 + 16 * NSTAGE + 16;
 };
 
-__device__ __forceinline__ int tc_off(int r, int k) {
-    return ((r >> 3) * (TC_KB / 4) + (k >> 2)) * 32 + (r & 7) * 4 + (k & 3);
+// shared-memory matrix descriptor of a K-major tile with the 128-byte swizzle: start address,
+// leading byte offset 16 (unused for this layout), stride byte offset 1024 (the next 8 rows),
+// descriptor version 1, layout type 2 (128-byte swizzle)
+__device__ __forceinline__ uint64_t tc_desc(uint32_t addr) {
+    return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) |
+           ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
-__device__ __forceinline__ uint64_t tc_desc(uint32_t addr) {
-    // start address, leading byte offset 128 (next core matrix along K), stride byte offset
-    // 1024 (next 8 rows), descriptor version 1, no swizzle
-    return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)(128 >> 4) << 16) |
-           ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46);
+__device__ __forceinline__ void tma_load2d(void *dst, const CUtensorMap *map, int x, int y,
+                                           unsigned long long *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
 }
 
 __device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
@@ -96,40 +103,39 @@ __device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// 16 bytes global -> shared, the bytes past `src_bytes` (0..16) zero-filled
-__device__ __forceinline__ void cp_async16_zfill(void *dst, const void *src, int src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_u32(dst)), "l"(src),
-                 "r"(src_bytes)
-                 : "memory");
-}
-
 // x - (x with its 13 low mantissa bits cleared): the part of x the TF32 product drops
 __device__ __forceinline__ float tf32_rest(float x) {
     return x - __uint_as_float(__float_as_uint(x) & 0xffffe000u);
 }
 
 template <typename BT, int NT>
-__global__ void __launch_bounds__(TC_T, 1) k_dualmm_tc(Dims d, Inputs in, Work w, int step0, int ti) {
+__global__ void __launch_bounds__(TC_T, 1)
+    k_dualmm_tc(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CUtensorMap mq,
+                const __grid_constant__ CUtensorMap mu, Dims d, Inputs in, Work w, int step0,
+                int ti) {
     constexpr int PARTS = sizeof(BT) == 4 ? 2 : 1;
     using L = TcSmem<NT, PARTS>;
     constexpr int NS = L::NSTAGE;
-    extern __shared__ __align__(1024) float tsm[];
-    unsigned long long *bar = reinterpret_cast<unsigned long long *>(tsm + NS * L::STAGE);
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + NS);
+    extern __shared__ __align__(1024) unsigned char tsm_raw[];
+    unsigned char *tsm = tsm_raw + ((1024u - (smem_u32(tsm_raw) & 1023u)) & 1023u);
+    unsigned long long *full = reinterpret_cast<unsigned long long *>(tsm + NS * L::STAGE);
+    unsigned long long *empty = full + NS;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(empty + NS);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int mt = blockIdx.x, nt = blockIdx.y, p = blockIdx.z;
     const int C = d.C, D = d.D, m0 = mt * TC_M, n0 = nt * NT;
     const int n = (ti - step0) * d.P + p;
     const int nv = w.nvalid[n];
-    const float *X = w.X + (size_t)n * C * d.xp;
-    const float *QX = w.QX + (size_t)n * C * d.xp;
-    const float *UT = w.ret + (size_t)p * D * C;     // u_pre transposed, [D][C]
     // K: the tokens these rows see (k <= row) that are valid
     const int kend = m0 + TC_M < nv ? m0 + TC_M : nv;
     const int nkb = kend > 0 ? (kend + TC_KB - 1) / TC_KB : 0;
+    const int ya = n * C + m0, yb = p * D + n0;      // tile rows in the tensor maps
 
     if (tid == 0) {
-        for (int s = 0; s < NS; ++s) mbar_init(bar + s, 1);
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(full + s, 1);
+            mbar_init(empty + s, 1);
+        }
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -145,56 +151,50 @@ __global__ void __launch_bounds__(TC_T, 1) k_dualmm_tc(Dims d, Inputs in, Work w
     const uint32_t idesc = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(NT >> 3) << 17) |
                            ((uint32_t)(TC_M >> 4) << 24);
 
-    // the copies of K-block kb into stage kb % NS (one commit group per block)
+    // thread 0: the copies of K-block kb into stage kb % NS
+    int loaded = 0;
     auto load = [&](int kb) {
-        if (kb < nkb) {
-            float *st = tsm + (kb % NS) * L::STAGE;
-            const int k0 = kb * TC_KB;
-            for (int i = tid; i < TC_M * (TC_KB / 4); i += TC_T) {
-                const int r = i >> 3, k = (i & 7) * 4;
-                const size_t g = (size_t)(m0 + r) * d.xp + k0 + k;
-                cp_async16(st + tc_off(r, k), X + g);
-                cp_async16(st + L::A + tc_off(r, k), QX + g);
-            }
-            for (int i = tid; i < NT * (TC_KB / 4); i += TC_T) {
-                const int c = i >> 3, k = (i & 7) * 4;
-                int valid = nv - (k0 + k);
-                valid = valid < 0 ? 0 : (valid > 4 ? 4 : valid);
-                cp_async16_zfill(st + 2 * L::A + tc_off(c, k), UT + (size_t)(n0 + c) * C + k0 + k,
-                                 4 * valid);
-            }
-        }
-        cp_async_commit();
+        const int s = kb % NS;
+        unsigned char *st = tsm + s * L::STAGE;
+        mbar_arrive_expect_tx(full + s, (unsigned)L::PART);
+        tma_load2d(st, &mx, kb * TC_KB, ya, full + s);
+        tma_load2d(st + L::A_BYTES, &mq, kb * TC_KB, ya, full + s);
+        tma_load2d(st + 2 * L::A_BYTES, &mu, kb * TC_KB, yb, full + s);
+        loaded = kb + 1;
     };
+    if (tid == 0)
+        for (int kb = 0; kb < NS && kb < nkb; ++kb) load(kb);
 
     bool ok = true;
     int issued = 0;      // K-blocks whose products were issued (the same count in every thread)
-    for (int kb = 0; kb < NS - 1; ++kb) load(kb);
     for (int kb = 0; kb < nkb; ++kb) {
         const int s = kb % NS;
-        float *st = tsm + s * L::STAGE;
-        cp_async_wait<NS - 2>();        // this thread's copies of block kb landed
-        __syncthreads();                // everyone's
+        unsigned char *st = tsm + s * L::STAGE;
+        const bool landed = mbar_wait_bounded(full + s, (unsigned)(kb / NS) & 1u, d.spin);
+        if (!__syncthreads_and(landed)) {                // one decision for the whole CTA
+            ok = false;
+            break;
+        }
         if constexpr (PARTS == 2) {
-            // the lo parts of the three tiles
-            float *lo = st + L::TILES;
-            for (int i = tid; i < L::TILES; i += TC_T) lo[i] = tf32_rest(st[i]);
+            const float *hi = reinterpret_cast<const float *>(st);
+            float *lo = reinterpret_cast<float *>(st + L::PART);
+            for (int i = tid; i < L::PART / 4; i += TC_T) lo[i] = tf32_rest(hi[i]);
+            fence_proxy_async_smem();                    // the lo tiles, before the tensor cores
             __syncthreads();
         }
-        fence_proxy_async_smem();       // the tiles, before the tensor cores read them
-        __syncthreads();
         if (tid == 0) {
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             const uint32_t sa = smem_u32(st);
+#pragma unroll
             for (int ks = 0; ks < TC_KB / 8; ++ks) {
-                const uint32_t kofs = ks * 256;   // two 16-byte k-groups per K = 8
-                const uint64_t ax = tc_desc(sa + kofs), aq = tc_desc(sa + 4 * L::A + kofs);
-                const uint64_t bh = tc_desc(sa + 4 * 2 * L::A + kofs);
+                const uint32_t kofs = ks * 32;           // K = 8 floats along the swizzled row
+                const uint64_t ax = tc_desc(sa + kofs), aq = tc_desc(sa + L::A_BYTES + kofs);
+                const uint64_t bh = tc_desc(sa + 2 * L::A_BYTES + kofs);
                 const uint32_t acc = (kb > 0 || ks > 0) ? 1u : 0u;
                 if constexpr (PARTS == 2) {
-                    const uint32_t lb = sa + 4 * L::TILES;
-                    const uint64_t axl = tc_desc(lb + kofs), aql = tc_desc(lb + 4 * L::A + kofs);
-                    const uint64_t bl = tc_desc(lb + 4 * 2 * L::A + kofs);
+                    const uint32_t lb = sa + L::PART;
+                    const uint64_t axl = tc_desc(lb + kofs), aql = tc_desc(lb + L::A_BYTES + kofs);
+                    const uint64_t bl = tc_desc(lb + 2 * L::A_BYTES + kofs);
                     tc_mma(tmem, axl, bh, idesc, acc);
                     tc_mma(tmem, ax, bl, idesc, 1u);
                     tc_mma(tmem, ax, bh, idesc, 1u);
@@ -206,32 +206,37 @@ __global__ void __launch_bounds__(TC_T, 1) k_dualmm_tc(Dims d, Inputs in, Work w
                     tc_mma(tmem + NT, aq, bh, idesc, acc);
                 }
             }
-            tc_commit(bar + s);
+            tc_commit(empty + s);
         }
         issued = kb + 1;
-        // block kb + NS - 1 goes into the stage block kb - 1 used: wait for its products
-        const int nb = kb + NS - 1;
-        if (kb >= 1 && nb < nkb) {
-            const int pb = kb - 1;
-            const bool landed = mbar_wait_bounded(bar + (pb % NS), (unsigned)(pb / NS) & 1u, d.spin);
-            if (!__syncthreads_and(landed)) {            // one decision for the whole CTA
+        // stage s takes block kb + NS once the products of block kb have read it
+        if (kb + NS < nkb) {
+            bool freed = true;
+            if (tid == 0) {
+                freed = mbar_wait_bounded(empty + s, (unsigned)(kb / NS) & 1u, d.spin);
+                if (freed) load(kb + NS);
+            }
+            if (!__syncthreads_and(freed)) {
                 ok = false;
                 break;
             }
         }
-        load(nb);
     }
-    cp_async_wait<0>();
-    // every issued product done (the last commit covers the earlier ones); after a give-up the
-    // wait keeps the default limit, so that nothing is in flight when tensor memory is freed
+    // every issued product done (the last commit covers the earlier ones), and after a give-up
+    // every issued copy landed, before tensor memory is freed and the CTA leaves; the waits
+    // after a give-up keep the default limit
     if (issued > 0) {
         const int last = issued - 1;
         const unsigned par = (unsigned)(last / NS) & 1u;
-        bool landed = mbar_wait_bounded(bar + (last % NS), par, ok ? d.spin : kSpinLimit);
-        if (!landed) landed = mbar_wait_bounded(bar + (last % NS), par);
-        ok = __syncthreads_and(ok && landed);
+        bool done = mbar_wait_bounded(empty + (last % NS), par, ok ? d.spin : kSpinLimit);
+        if (!done) done = mbar_wait_bounded(empty + (last % NS), par);
+        ok = __syncthreads_and(ok && done);
     }
-    if (!ok && tid == 0) atomicCAS(&w.status->code, 0, (int)SDM_ERR_TIMEOUT);
+    if (!ok && tid == 0) {
+        for (int kb = issued; kb < loaded; ++kb)
+            mbar_wait_bounded(full + (kb % NS), (unsigned)(kb / NS) & 1u);
+        atomicCAS(&w.status->code, 0, (int)SDM_ERR_TIMEOUT);
+    }
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 
     if (ok) {
@@ -279,13 +284,68 @@ __global__ void __launch_bounds__(TC_T, 1) k_dualmm_tc(Dims d, Inputs in, Work w
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * NT));
 }
 
+// The three tensor maps of a workspace and column tile (X and QX: [N C rows][xp] floats, box 32
+// x 128; u_pre transposed: [P D rows][C] floats, box 32 x NT; 128-byte swizzle), encoded once
+// per workspace address and shape (the calling thread's last ones are kept).
+struct TcMaps {
+    CUtensorMap x, q, u;
+};
+
+cudaError_t tc_maps(const Dims &d, const Work &w, int NT, const TcMaps *&out) {
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    if (!encode) {
+        cudaDriverEntryPointQueryResult q;
+        void *fn = nullptr;
+        const cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn,
+                                                               12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+            return e != cudaSuccess ? e : cudaErrorNotSupported;
+        encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    thread_local struct {
+        const void *x, *q, *u;
+        int C, D, P, ns, xp, NT;
+        TcMaps m;
+    } cache = {};
+    if (!(cache.x == w.X && cache.q == w.QX && cache.u == w.ret && cache.C == d.C &&
+          cache.D == d.D && cache.P == d.P && cache.ns == w.ns && cache.xp == d.xp &&
+          cache.NT == NT)) {
+        const cuuint64_t rows = (cuuint64_t)w.ns * d.P * d.C;
+        const cuuint64_t dx[2] = {(cuuint64_t)d.xp, rows}, sx[1] = {(cuuint64_t)d.xp * 4};
+        const cuuint64_t du[2] = {(cuuint64_t)d.C, (cuuint64_t)d.P * d.D},
+                         su[1] = {(cuuint64_t)d.C * 4};
+        const cuuint32_t bx[2] = {TC_KB, TC_M}, bu[2] = {TC_KB, (cuuint32_t)NT}, es[2] = {1, 1};
+        auto enc = [&](CUtensorMap *m, void *base, const cuuint64_t *dim, const cuuint64_t *str,
+                       const cuuint32_t *box) {
+            return encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dim, str, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        };
+        if (enc(&cache.m.x, w.X, dx, sx, bx) != CUDA_SUCCESS ||
+            enc(&cache.m.q, w.QX, dx, sx, bx) != CUDA_SUCCESS ||
+            enc(&cache.m.u, w.ret, du, su, bu) != CUDA_SUCCESS) {
+            cache.x = nullptr;
+            return cudaErrorInvalidValue;
+        }
+        cache.x = w.X; cache.q = w.QX; cache.u = w.ret;
+        cache.C = d.C; cache.D = d.D; cache.P = d.P; cache.ns = w.ns; cache.xp = d.xp;
+        cache.NT = NT;
+    }
+    out = &cache.m;
+    return cudaSuccess;
+}
+
 template <typename BT, int NT>
 cudaError_t launch_tc(const Dims &d, const Inputs &in, const Work &w, int step0, int ti,
                       cudaStream_t st) {
+    const TcMaps *m = nullptr;
+    const cudaError_t e = tc_maps(d, w, NT, m);
+    if (e != cudaSuccess) return e;
     constexpr size_t smem = TcSmem<NT, sizeof(BT) == 4 ? 2 : 1>::BYTES;
     auto kern = k_dualmm_tc<BT, NT>;
     set_kernel_smem(kern, smem);
-    kern<<<dim3(d.C / TC_M, d.D / NT, d.P), TC_T, smem, st>>>(d, in, w, step0, ti);
+    kern<<<dim3(d.C / TC_M, d.D / NT, d.P), TC_T, smem, st>>>(m->x, m->q, m->u, d, in, w, step0,
+                                                               ti);
     return cudaGetLastError();
 }
 
@@ -294,7 +354,7 @@ cudaError_t launch_tc(const Dims &d, const Inputs &in, const Work &w, int step0,
 cudaError_t launch_dualmm_tc(const Dims &d, const Inputs &in, const Work &w, int step0, int ti,
                              cudaStream_t st) {
     // the widest column tile (64, 32 or 16) that still gives about one CTA per SM: the step's
-    // products are small, and each CTA's time is its loads of X and QX rows
+    // products are small, and each CTA's time is its copies of X and QX tiles
     const long tiles = (long)d.P * (d.C / TC_M) * (d.D / 64);
     const int nt = tiles >= kRefSms ? 64 : (2 * tiles >= kRefSms ? 32 : 16);
     if (d.dtype == SDM_BF16) {

@@ -202,6 +202,13 @@ __global__ void __launch_bounds__(kBlock) k_gather(Dims d, Inputs in, Work w, in
         }
         store_vec<float, CPL>(w.inter + row, ai);
     };
+    // a padding token's u_pre column is zero for the tensor-core dual matmul, whose K-blocks
+    // of 32 tokens reach past the valid ones (its X and QX entries there are 0)
+    if (!active && gtok < d.P * C && sub == 0 && dualmm_tc_fits(d)) {
+        float *ut = w.ret + ((size_t)p * D + lane * CPL) * C + t;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) ut[(size_t)c * C] = 0.f;
+    }
     if constexpr (WPT == 1) {
         if (active) finish();
     } else {

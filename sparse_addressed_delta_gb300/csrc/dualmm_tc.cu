@@ -42,10 +42,12 @@ struct TcSmem {
     static constexpr int B_BYTES = NT * TC_KB * 4;
     static constexpr int PART = 2 * A_BYTES + B_BYTES;
     static constexpr int STAGE = PARTS * PART;
-    static constexpr int NS0 = (200 * 1024) / STAGE;
+    static constexpr int I_BYTES = TC_M * NT * 4;        // the inter tile [128][NT]
+    static constexpr int NS0 = (212 * 1024 - I_BYTES) / STAGE;
     static constexpr int NSTAGE = NS0 > 8 ? 8 : (NS0 < 2 ? 2 : NS0);
-    // + the alignment of the tiles to 1024 bytes, the barriers and the tensor memory address
-    static constexpr size_t BYTES = (size_t)NSTAGE * STAGE + 1024 + 16 * NSTAGE + 16;
+    // + the alignment of the tiles to 1024 bytes, the barriers, flags and the tensor memory
+    // address
+    static constexpr size_t BYTES = (size_t)NSTAGE * STAGE + I_BYTES + 1024 + 16 * NSTAGE + 64;
 };
 
 // shared-memory matrix descriptor of a K-major tile with the 128-byte swizzle: start address,
@@ -111,16 +113,20 @@ __device__ __forceinline__ float tf32_rest(float x) {
 template <typename BT, int NT>
 __global__ void __launch_bounds__(TC_T, 1)
     k_dualmm_tc(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CUtensorMap mq,
-                const __grid_constant__ CUtensorMap mu, Dims d, Inputs in, Work w, int step0,
-                int ti) {
+                const __grid_constant__ CUtensorMap mu, const __grid_constant__ CUtensorMap mi,
+                Dims d, Inputs in, Work w, int step0, int ti) {
     constexpr int PARTS = sizeof(BT) == 4 ? 2 : 1;
     using L = TcSmem<NT, PARTS>;
     constexpr int NS = L::NSTAGE;
     extern __shared__ __align__(1024) unsigned char tsm_raw[];
     unsigned char *tsm = tsm_raw + ((1024u - (smem_u32(tsm_raw) & 1023u)) & 1023u);
-    unsigned long long *full = reinterpret_cast<unsigned long long *>(tsm + NS * L::STAGE);
+    float *itile = reinterpret_cast<float *>(tsm + NS * L::STAGE);     // [128][NT]
+    unsigned long long *full =
+        reinterpret_cast<unsigned long long *>(tsm + NS * L::STAGE + L::I_BYTES);
     unsigned long long *empty = full + NS;
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(empty + NS);
+    unsigned long long *ibar = empty + NS;
+    int *flag = reinterpret_cast<int *>(ibar + 1);   // [0] blocks issued, [1] loaded, [2] failed
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(flag + 4);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int mt = blockIdx.x, nt = blockIdx.y, p = blockIdx.z;
     const int C = d.C, D = d.D, m0 = mt * TC_M, n0 = nt * NT;
@@ -131,11 +137,14 @@ __global__ void __launch_bounds__(TC_T, 1)
     const int nkb = kend > 0 ? (kend + TC_KB - 1) / TC_KB : 0;
     const int ya = n * C + m0, yb = p * D + n0;      // tile rows in the tensor maps
 
+    const bool irows = m0 < nv;                      // live rows: the inter tile is read
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
             mbar_init(full + s, 1);
             mbar_init(empty + s, 1);
         }
+        mbar_init(ibar, 1);
+        flag[0] = flag[1] = flag[2] = 0;
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -151,8 +160,7 @@ __global__ void __launch_bounds__(TC_T, 1)
     const uint32_t idesc = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(NT >> 3) << 17) |
                            ((uint32_t)(TC_M >> 4) << 24);
 
-    // thread 0: the copies of K-block kb into stage kb % NS
-    int loaded = 0;
+    // the copies of K-block kb into stage kb % NS
     auto load = [&](int kb) {
         const int s = kb % NS;
         unsigned char *st = tsm + s * L::STAGE;
@@ -160,68 +168,105 @@ __global__ void __launch_bounds__(TC_T, 1)
         tma_load2d(st, &mx, kb * TC_KB, ya, full + s);
         tma_load2d(st + L::A_BYTES, &mq, kb * TC_KB, ya, full + s);
         tma_load2d(st + 2 * L::A_BYTES, &mu, kb * TC_KB, yb, full + s);
-        loaded = kb + 1;
     };
-    if (tid == 0)
-        for (int kb = 0; kb < NS && kb < nkb; ++kb) load(kb);
-
-    bool ok = true;
-    int issued = 0;      // K-blocks whose products were issued (the same count in every thread)
-    for (int kb = 0; kb < nkb; ++kb) {
+    // the products of K-block kb (one thread), released on empty[kb % NS]
+    auto mma = [&](int kb) {
         const int s = kb % NS;
-        unsigned char *st = tsm + s * L::STAGE;
-        const bool landed = mbar_wait_bounded(full + s, (unsigned)(kb / NS) & 1u, d.spin);
-        if (!__syncthreads_and(landed)) {                // one decision for the whole CTA
-            ok = false;
-            break;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint32_t sa = smem_u32(tsm + s * L::STAGE);
+#pragma unroll
+        for (int ks = 0; ks < TC_KB / 8; ++ks) {
+            const uint32_t kofs = ks * 32;               // K = 8 floats along the swizzled row
+            const uint64_t ax = tc_desc(sa + kofs), aq = tc_desc(sa + L::A_BYTES + kofs);
+            const uint64_t bh = tc_desc(sa + 2 * L::A_BYTES + kofs);
+            const uint32_t acc = (kb > 0 || ks > 0) ? 1u : 0u;
+            if constexpr (PARTS == 2) {
+                const uint32_t lb = sa + L::PART;
+                const uint64_t axl = tc_desc(lb + kofs), aql = tc_desc(lb + L::A_BYTES + kofs);
+                const uint64_t bl = tc_desc(lb + 2 * L::A_BYTES + kofs);
+                tc_mma(tmem, axl, bh, idesc, acc);
+                tc_mma(tmem, ax, bl, idesc, 1u);
+                tc_mma(tmem, ax, bh, idesc, 1u);
+                tc_mma(tmem + NT, aql, bh, idesc, acc);
+                tc_mma(tmem + NT, aq, bl, idesc, 1u);
+                tc_mma(tmem + NT, aq, bh, idesc, 1u);
+            } else {
+                tc_mma(tmem, ax, bh, idesc, acc);
+                tc_mma(tmem + NT, aq, bh, idesc, acc);
+            }
         }
-        if constexpr (PARTS == 2) {
+        tc_commit(empty + s);
+    };
+    // the inter tile, for the epilogue
+    if (tid == 32 && irows) {
+        mbar_arrive_expect_tx(ibar, (unsigned)L::I_BYTES);
+        tma_load2d(itile, &mi, n0, p * C + m0, ibar);
+    }
+
+    if constexpr (PARTS == 1) {
+        // thread 32 copies, thread 0 issues the products as blocks land; a stage is copied
+        // again once the products of the block NS earlier have read it
+        if (tid == 32) {
+            int kb = 0;
+            for (; kb < nkb; ++kb) {
+                const int s = kb % NS;
+                if (kb >= NS && !mbar_wait_bounded(empty + s, (unsigned)((kb / NS) - 1) & 1u, d.spin))
+                    break;
+                load(kb);
+            }
+            flag[1] = kb;
+            if (kb < nkb) flag[2] = 1;
+        } else if (tid == 0) {
+            int kb = 0;
+            for (; kb < nkb; ++kb) {
+                if (!mbar_wait_bounded(full + (kb % NS), (unsigned)(kb / NS) & 1u, d.spin)) break;
+                mma(kb);
+            }
+            flag[0] = kb;
+            if (kb < nkb) flag[2] = 1;
+        }
+    } else {
+        // float32 banks: every thread forms the lo parts of a landed block before its products
+        int nload = 0;                                   // blocks whose copies thread 0 issued
+        if (tid == 0)
+            for (; nload < NS && nload < nkb; ++nload) load(nload);
+        int kb = 0;
+        for (; kb < nkb; ++kb) {
+            const int s = kb % NS;
+            unsigned char *st = tsm + s * L::STAGE;
+            const bool landed = mbar_wait_bounded(full + s, (unsigned)(kb / NS) & 1u, d.spin);
+            if (!__syncthreads_and(landed)) break;      // one decision for the whole CTA
             const float *hi = reinterpret_cast<const float *>(st);
             float *lo = reinterpret_cast<float *>(st + L::PART);
             for (int i = tid; i < L::PART / 4; i += TC_T) lo[i] = tf32_rest(hi[i]);
             fence_proxy_async_smem();                    // the lo tiles, before the tensor cores
             __syncthreads();
-        }
-        if (tid == 0) {
-            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            const uint32_t sa = smem_u32(st);
-#pragma unroll
-            for (int ks = 0; ks < TC_KB / 8; ++ks) {
-                const uint32_t kofs = ks * 32;           // K = 8 floats along the swizzled row
-                const uint64_t ax = tc_desc(sa + kofs), aq = tc_desc(sa + L::A_BYTES + kofs);
-                const uint64_t bh = tc_desc(sa + 2 * L::A_BYTES + kofs);
-                const uint32_t acc = (kb > 0 || ks > 0) ? 1u : 0u;
-                if constexpr (PARTS == 2) {
-                    const uint32_t lb = sa + L::PART;
-                    const uint64_t axl = tc_desc(lb + kofs), aql = tc_desc(lb + L::A_BYTES + kofs);
-                    const uint64_t bl = tc_desc(lb + 2 * L::A_BYTES + kofs);
-                    tc_mma(tmem, axl, bh, idesc, acc);
-                    tc_mma(tmem, ax, bl, idesc, 1u);
-                    tc_mma(tmem, ax, bh, idesc, 1u);
-                    tc_mma(tmem + NT, aql, bh, idesc, acc);
-                    tc_mma(tmem + NT, aq, bl, idesc, 1u);
-                    tc_mma(tmem + NT, aq, bh, idesc, 1u);
-                } else {
-                    tc_mma(tmem, ax, bh, idesc, acc);
-                    tc_mma(tmem + NT, aq, bh, idesc, acc);
+            if (tid == 0) mma(kb);
+            // stage s takes block kb + NS once the products of block kb have read it
+            if (kb + NS < nkb) {
+                bool freed = true;
+                if (tid == 0) {
+                    freed = mbar_wait_bounded(empty + s, (unsigned)(kb / NS) & 1u, d.spin);
+                    if (freed) {
+                        load(kb + NS);
+                        nload = kb + NS + 1;
+                    }
+                }
+                if (!__syncthreads_and(freed)) {
+                    ++kb;
+                    break;
                 }
             }
-            tc_commit(empty + s);
         }
-        issued = kb + 1;
-        // stage s takes block kb + NS once the products of block kb have read it
-        if (kb + NS < nkb) {
-            bool freed = true;
-            if (tid == 0) {
-                freed = mbar_wait_bounded(empty + s, (unsigned)(kb / NS) & 1u, d.spin);
-                if (freed) load(kb + NS);
-            }
-            if (!__syncthreads_and(freed)) {
-                ok = false;
-                break;
-            }
+        if (tid == 0) {
+            flag[0] = kb;
+            flag[1] = nload;
+            if (kb < nkb) flag[2] = 1;
         }
     }
+    __syncthreads();
+    const int issued = flag[0], loaded = flag[1];
+    bool ok = flag[2] == 0;
     // every issued product done (the last commit covers the earlier ones), and after a give-up
     // every issued copy landed, before tensor memory is freed and the CTA leaves; the waits
     // after a give-up keep the default limit
@@ -231,6 +276,11 @@ __global__ void __launch_bounds__(TC_T, 1)
         bool done = mbar_wait_bounded(empty + (last % NS), par, ok ? d.spin : kSpinLimit);
         if (!done) done = mbar_wait_bounded(empty + (last % NS), par);
         ok = __syncthreads_and(ok && done);
+    }
+    if (irows) {
+        bool got = mbar_wait_bounded(ibar, 0u, ok ? d.spin : kSpinLimit);
+        if (!got) got = mbar_wait_bounded(ibar, 0u);
+        ok = __syncthreads_and(ok && got);
     }
     if (!ok && tid == 0) {
         for (int kb = issued; kb < loaded; ++kb)
@@ -245,7 +295,7 @@ __global__ void __launch_bounds__(TC_T, 1)
         const size_t tok = (size_t)p * d.T + (size_t)ti * C + row;
         const bool out_row = (size_t)ti * C + row < (size_t)d.T;
         float *dvrow = w.dv + ((size_t)p * C + row) * D + n0;
-        const float *irow = w.inter + ((size_t)p * C + row) * D + n0;
+        const float *irow = itile + (32 * warp + lane) * NT;
         BT *orow = static_cast<BT *>(in.readings) + tok * D + n0;
         constexpr int CW_ = NT < 32 ? NT : 32;          // accumulator columns per load
         for (int c0 = 0; c0 < NT; c0 += CW_) {
@@ -288,7 +338,7 @@ __global__ void __launch_bounds__(TC_T, 1)
 // x 128; u_pre transposed: [P D rows][C] floats, box 32 x NT; 128-byte swizzle), encoded once
 // per workspace address and shape (the calling thread's last ones are kept).
 struct TcMaps {
-    CUtensorMap x, q, u;
+    CUtensorMap x, q, u, i;
 };
 
 cudaError_t tc_maps(const Dims &d, const Work &w, int NT, const TcMaps *&out) {
@@ -303,31 +353,37 @@ cudaError_t tc_maps(const Dims &d, const Work &w, int NT, const TcMaps *&out) {
         encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
     thread_local struct {
-        const void *x, *q, *u;
+        const void *x, *q, *u, *i;
         int C, D, P, ns, xp, NT;
         TcMaps m;
     } cache = {};
-    if (!(cache.x == w.X && cache.q == w.QX && cache.u == w.ret && cache.C == d.C &&
+    if (!(cache.x == w.X && cache.q == w.QX && cache.u == w.ret && cache.i == w.inter &&
+          cache.C == d.C &&
           cache.D == d.D && cache.P == d.P && cache.ns == w.ns && cache.xp == d.xp &&
           cache.NT == NT)) {
         const cuuint64_t rows = (cuuint64_t)w.ns * d.P * d.C;
         const cuuint64_t dx[2] = {(cuuint64_t)d.xp, rows}, sx[1] = {(cuuint64_t)d.xp * 4};
         const cuuint64_t du[2] = {(cuuint64_t)d.C, (cuuint64_t)d.P * d.D},
                          su[1] = {(cuuint64_t)d.C * 4};
-        const cuuint32_t bx[2] = {TC_KB, TC_M}, bu[2] = {TC_KB, (cuuint32_t)NT}, es[2] = {1, 1};
+        const cuuint64_t di[2] = {(cuuint64_t)d.D, (cuuint64_t)d.P * d.C},
+                         si[1] = {(cuuint64_t)d.D * 4};
+        const cuuint32_t bx[2] = {TC_KB, TC_M}, bu[2] = {TC_KB, (cuuint32_t)NT},
+                         bi[2] = {(cuuint32_t)NT, TC_M}, es[2] = {1, 1};
         auto enc = [&](CUtensorMap *m, void *base, const cuuint64_t *dim, const cuuint64_t *str,
-                       const cuuint32_t *box) {
+                       const cuuint32_t *box, CUtensorMapSwizzle sw) {
             return encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dim, str, box, es,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         };
-        if (enc(&cache.m.x, w.X, dx, sx, bx) != CUDA_SUCCESS ||
-            enc(&cache.m.q, w.QX, dx, sx, bx) != CUDA_SUCCESS ||
-            enc(&cache.m.u, w.ret, du, su, bu) != CUDA_SUCCESS) {
+        const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
+        if (enc(&cache.m.x, w.X, dx, sx, bx, sw) != CUDA_SUCCESS ||
+            enc(&cache.m.q, w.QX, dx, sx, bx, sw) != CUDA_SUCCESS ||
+            enc(&cache.m.u, w.ret, du, su, bu, sw) != CUDA_SUCCESS ||
+            enc(&cache.m.i, w.inter, di, si, bi, CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS) {
             cache.x = nullptr;
             return cudaErrorInvalidValue;
         }
-        cache.x = w.X; cache.q = w.QX; cache.u = w.ret;
+        cache.x = w.X; cache.q = w.QX; cache.u = w.ret; cache.i = w.inter;
         cache.C = d.C; cache.D = d.D; cache.P = d.P; cache.ns = w.ns; cache.xp = d.xp;
         cache.NT = NT;
     }
@@ -344,8 +400,8 @@ cudaError_t launch_tc(const Dims &d, const Inputs &in, const Work &w, int step0,
     constexpr size_t smem = TcSmem<NT, sizeof(BT) == 4 ? 2 : 1>::BYTES;
     auto kern = k_dualmm_tc<BT, NT>;
     set_kernel_smem(kern, smem);
-    kern<<<dim3(d.C / TC_M, d.D / NT, d.P), TC_T, smem, st>>>(m->x, m->q, m->u, d, in, w, step0,
-                                                               ti);
+    kern<<<dim3(d.C / TC_M, d.D / NT, d.P), TC_T, smem, st>>>(m->x, m->q, m->u, m->i, d, in, w,
+                                                               step0, ti);
     return cudaGetLastError();
 }
 

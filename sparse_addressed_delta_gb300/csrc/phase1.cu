@@ -285,10 +285,12 @@ struct P1Chunk {
     const float *dref;
     float *dka, *dkb, *dkq;
     int nd;
+    float *lw;          // token-major running log-decay of the writes (written by the Gram rows)
 };
 
-// 3a. weights of the sorted positions [pos0, pos1): gw = k exp(lw), dw = k exp(lend - lw)
-template <typename WT>
+// 3a. weights of the sorted positions [pos0, pos1): gw = k exp(lw) (unless GW is false: the
+// Gram rows write it token-major), dw = k exp(lend - lw)
+template <typename WT, bool GW = true>
 __device__ void p1_weights(const P1Chunk<WT> &c, int pos0, int pos1, int tid, int nthr) {
     for (int pos = pos0 + tid; pos < pos1; pos += nthr) {
         const unsigned low = (unsigned)c.srt[pos];
@@ -297,7 +299,7 @@ __device__ void p1_weights(const P1Chunk<WT> &c, int pos0, int pos1, int tid, in
         const float l = c.lws[pos];
         const float dwv = kk * expf(c.lend[c.pgid[pos]] - l);
         c.wdw[pos] = dwv;
-        c.gw[e] = kk * expf(l);
+        if (GW) c.gw[e] = kk * expf(l);
         if (c.dwt) c.dwt[e] = dwv;
     }
 }
@@ -421,7 +423,7 @@ __device__ __forceinline__ void dense_stage(int dh, int key, float v0, float v1,
 //    sums here: they add their factors to the row's staged dense rows (dka, dkb from the
 //    writes, dkq from the reads; `drow` holds 3 dense_pitch(C) floats per row), which
 //    k_gram_dense multiplies out.
-template <typename WT, bool TWO, int kPairAhead>
+template <typename WT, bool TWO, int kPairAhead, bool WGL>
 __device__ void p1_gram_rows(const P1Chunk<WT> &c, int t0, int t1, int warp, int nwarps, int lane,
                              float *row, float *drow) {
     const int C = c.C, W = c.W, R = c.R;
@@ -453,6 +455,10 @@ __device__ void p1_gram_rows(const P1Chunk<WT> &c, int t0, int t1, int warp, int
                 gs = c.pgs[pos];
                 la = c.lws[pos];
                 if (hp) dh = c.dpos[pos];
+                if (WGL) {                   // the token-major running sum and gather weight
+                    c.lw[e] = la;
+                    c.gw[e] = ka * expf(la);
+                }
             }
             if (hp) {
                 float va = 0.f, vb = 0.f;
@@ -567,12 +573,15 @@ __device__ void p1_gram_rows(const P1Chunk<WT> &c, int t0, int t1, int warp, int
     }
 }
 
-// AHEAD: Gram row entries whose first member loads are in flight at once
-template <typename WT, int AHEAD>
+// AHEAD: Gram row entries whose first member loads are in flight at once; WGL: the rows also
+// write the token-major lw and gw of their write entries
+template <typename WT, int AHEAD, bool WGL>
 __device__ __forceinline__ void p1_gram(const P1Chunk<WT> &c, int t0, int t1, int warp, int nwarps,
                                         int lane, float *row, float *drow) {
-    if (2 * c.C <= kMaxChunk) p1_gram_rows<WT, true, AHEAD>(c, t0, t1, warp, nwarps, lane, row, drow);
-    else p1_gram_rows<WT, false, AHEAD>(c, t0, t1, warp, nwarps, lane, row, drow);
+    if (2 * c.C <= kMaxChunk)
+        p1_gram_rows<WT, true, AHEAD, WGL>(c, t0, t1, warp, nwarps, lane, row, drow);
+    else
+        p1_gram_rows<WT, false, AHEAD, WGL>(c, t0, t1, warp, nwarps, lane, row, drow);
 }
 
 // Dense Gram groups of a chunk whose scratch is in global memory. A group of n members costs
@@ -905,8 +914,7 @@ __global__ void __launch_bounds__(NT, 2) k_phase1(Dims d, Inputs in, Work w, int
                     tkk[ps] = make_float2(__int_as_float((int)(low >> 8)), kv[u]);
                     if (!head[u] && ((unsigned)kk[u] >> 8) == (low >> 8))
                         atomicAdd(&w.status->repeated_write_slots, 1ull);
-                    lws[ps] = l;
-                    lw[e[u]] = l;
+                    lws[ps] = l;          // lw[e] is written token-major by k_phase1_rows
                     pgid[ps] = gid;
                     if (head[u]) {
                         goff[gid] = ps;
@@ -998,7 +1006,7 @@ __global__ void __launch_bounds__(NT, 2) k_phase1(Dims d, Inputs in, Work w, int
                              wdw, gw, qw, lr, A, QK,
                              d.bwd ? w.dwt + (size_t)n * CW : nullptr,
                              nv, nw, nr, C, W, R, S,
-                             nullptr, nullptr, nullptr, nullptr, nullptr, 0};
+                             nullptr, nullptr, nullptr, nullptr, nullptr, 0, lw};
         if (split) {
             // steps 3 and 4 run in k_phase1_rows, over many CTAs per chunk; it finds the
             // sorted row in the radix buffer recorded here
@@ -1008,7 +1016,7 @@ __global__ void __launch_bounds__(NT, 2) k_phase1(Dims d, Inputs in, Work w, int
             p1_weights(pc, 0, nw, tid, NT);
             p1_reads(pc, 0, nr, tid, NT);
             __syncthreads();
-            p1_gram<WT, 1>(pc, 0, C, warp, NW, lane, sm.row[warp], nullptr);
+            p1_gram<WT, 1, false>(pc, 0, C, warp, NW, lane, sm.row[warp], nullptr);
         }
         // tails of the per-entry rows past the valid entries (read by nothing but the debug
         // copy; written so that every output element is defined)
@@ -1147,7 +1155,7 @@ __global__ void __launch_bounds__(NTR, BIG ? 4 : 6) k_phase1_rows(Dims d, Inputs
                          w.lr + (size_t)n * CR, w.A + (size_t)n * CC, w.QK + (size_t)n * CC,
                          d.bwd ? w.dwt + (size_t)n * CW : nullptr,
                          nv, nw, nr, C, W, R, d.S,
-                         nullptr, nullptr, nullptr, nullptr, nullptr, 0};
+                         nullptr, nullptr, nullptr, nullptr, nullptr, 0, w.lw + (size_t)n * CW};
     if (BIG && w.ndense[n] > 0) {
         pc.dpos = w.dpos + (size_t)n * CW;
         pc.dref = w.dref + (size_t)n * C;
@@ -1161,14 +1169,14 @@ __global__ void __launch_bounds__(NTR, BIG ? 4 : 6) k_phase1_rows(Dims d, Inputs
         for (int i = tid; i < nsmp; i += NTR) smp[i] = srt[(size_t)i * kSampleStep];
     const int per = (nw + nrb - 1) / nrb;
     const int pos0 = rb * per, pos1 = pos0 + per < nw ? pos0 + per : nw;
-    p1_weights(pc, pos0, pos1, tid, NTR);
+    p1_weights<WT, false>(pc, pos0, pos1, tid, NTR);
     __syncthreads();
     const int t0 = rb * KR, t1 = t0 + KR < C ? t0 + KR : C;
     const int r1 = (t1 < nv ? t1 : nv) * R;
     p1_reads<WT, BIG>(pc, t0 * R < r1 ? t0 * R : r1, r1, tid, NTR, smp, nsmp);
     __syncthreads();
-    p1_gram<WT, BIG ? 4 : 1>(pc, t0, t1, warp, NTR / 32, lane, rows + warp * kMaxChunk,
-                             BIG ? drows + warp * 3 * kMaxChunk : nullptr);
+    p1_gram<WT, BIG ? 4 : 1, true>(pc, t0, t1, warp, NTR / 32, lane, rows + warp * kMaxChunk,
+                                   BIG ? drows + warp * 3 * kMaxChunk : nullptr);
 }
 
 // The dense groups' part of A and QK, after k_phase1_rows wrote the pair sums of the other

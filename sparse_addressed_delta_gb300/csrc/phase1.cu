@@ -293,14 +293,16 @@ struct P1Chunk {
 template <typename WT, bool GW = true>
 __device__ void p1_weights(const P1Chunk<WT> &c, int pos0, int pos1, int tid, int nthr) {
     for (int pos = pos0 + tid; pos < pos1; pos += nthr) {
-        const unsigned low = (unsigned)c.srt[pos];
-        const int e = (int)(low >> 8) * c.W + (int)(low & 255u);
-        const float kk = c.kf[e];
+        const float kk = c.tkk[pos].y;                 // the entry's k, in sorted order
         const float l = c.lws[pos];
         const float dwv = kk * expf(c.lend[c.pgid[pos]] - l);
         c.wdw[pos] = dwv;
-        if (GW) c.gw[e] = kk * expf(l);
-        if (c.dwt) c.dwt[e] = dwv;
+        if (GW || c.dwt) {
+            const unsigned low = (unsigned)c.srt[pos];
+            const int e = (int)(low >> 8) * c.W + (int)(low & 255u);
+            if (GW) c.gw[e] = kk * expf(l);
+            if (c.dwt) c.dwt[e] = dwv;
+        }
     }
 }
 

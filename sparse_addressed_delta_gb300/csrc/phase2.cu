@@ -135,18 +135,14 @@ __global__ void __launch_bounds__(kBlock) k_gather(Dims d, Inputs in, Work w, in
                     }
                 }
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
-#pragma unroll
-                    for (int c = 0; c < CPL; ++c) ar[c] = fmaf(wt[u], x[u][c], ar[c]);
+                for (int u = 0; u < 4; ++u) axpy(ar, wt[u], x[u]);
             }
             for (; j < j1; ++j) {
                 const int s = ws[j];
                 if ((unsigned)s >= S) continue;
                 float x[CPL];
                 load_vec<BT, CPL, true>(bank + (size_t)s * D, x);
-                const float wt = gw[j];
-#pragma unroll
-                for (int c = 0; c < CPL; ++c) ar[c] = fmaf(wt, x[c], ar[c]);
+                axpy(ar, gw[j], x);
             }
         }
         {
@@ -169,18 +165,14 @@ __global__ void __launch_bounds__(kBlock) k_gather(Dims d, Inputs in, Work w, in
                     }
                 }
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
-#pragma unroll
-                    for (int c = 0; c < CPL; ++c) ai[c] = fmaf(wt[u], x[u][c], ai[c]);
+                for (int u = 0; u < 4; ++u) axpy(ai, wt[u], x[u]);
             }
             for (; i < i1; ++i) {
                 const int s = rs[i];
                 if ((unsigned)s >= S) continue;
                 float x[CPL];
                 load_vec<BT, CPL, true>(bank + (size_t)s * D, x);
-                const float wt = qw[i];
-#pragma unroll
-                for (int c = 0; c < CPL; ++c) ai[c] = fmaf(wt, x[c], ai[c]);
+                axpy(ai, qw[i], x);
             }
         }
     }
@@ -567,8 +559,7 @@ __global__ void __launch_bounds__(DW_T, 1) k_dw(Dims d, Inputs in, Work w, int s
                         float x[CPS];
                         const float wv = rec_w[r0 + m];
                         load_vec<float, CPS, false>(dvl + rec_t[r0 + m] * DS, x);
-#pragma unroll
-                        for (int c = 0; c < CPS; ++c) acc[c] = fmaf(wv, x[c], acc[c]);
+                        axpy(acc, wv, x);
                     }
                 }
             } else {
@@ -588,8 +579,7 @@ __global__ void __launch_bounds__(DW_T, 1) k_dw(Dims d, Inputs in, Work w, int s
                         const int tv = __shfl_sync(0xffffffffu, t, v);
                         const float wv = __shfl_sync(0xffffffffu, wl, v);
                         load_vec<float, CPS, false>(dvl + tv * DS, x);
-#pragma unroll
-                        for (int c = 0; c < CPS; ++c) acc[c] = fmaf(wv, x[c], acc[c]);
+                        axpy(acc, wv, x);
                     }
                 }
             }
@@ -693,8 +683,7 @@ __global__ void __launch_bounds__(DW_T, 1) k_dw(Dims d, Inputs in, Work w, int s
 #pragma unroll
                         for (int v = 0; v < 4; ++v) {
                             if (v0 + v >= mc) break;
-#pragma unroll
-                            for (int c = 0; c < CPS; ++c) acc[c] = fmaf(wv[v], y[v][c], acc[c]);
+                            axpy(acc, wv[v], y[v]);
                         }
                     }
                     ct = nt;

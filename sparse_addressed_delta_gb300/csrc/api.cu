@@ -101,7 +101,8 @@ size_t per_chunk_bytes(const Dims &d) {
     const size_t CW = (size_t)d.C * d.W, CR = (size_t)d.C * d.R, CC = (size_t)d.C * d.C;
     const size_t dense =
         dense_gram(d) ? 4 * (CW + 1 + d.C + 3 * (size_t)d.C * dense_pitch(d.C)) : 0;
-    return 4 * (11 * CW + 4) + 4 * 3 * CR + 4 * 4 * CC + 24 + dense;
+    const size_t pair = phase1_split(d) ? 4 * CW : 0;   // (g, k) pairs in place of k alone
+    return 4 * (11 * CW + 4) + 4 * 3 * CR + 4 * 4 * CC + 24 + dense + pair;
 }
 
 int slab_steps(const Dims &d, int requested) {
@@ -156,7 +157,8 @@ int phase1_ctas(const Dims &d, int ns) {
     F(pgid, int32_t, G * CW)                                                  \
     F(pgs, int32_t, G * CW)                                                   \
     F(lend, float, G * CW)                                                    \
-    F(kf, float, G * CW)                                                      \
+    F(kf, float, (1 - PS) * G * CW)                                           \
+    F(gk, float2, PS * G * CW)                                                \
     F(rlo, int32_t, G * CR)                                                   \
     F(rhi, int32_t, G * CR)                                                   \
     F(dpos, int32_t, HS * G * CW)                                             \
@@ -201,6 +203,7 @@ size_t layout_bytes(const Dims &d, int ns, int G_) {
                  CC = (size_t)d.C * d.C, CD = (size_t)d.C * d.D, G = G_, B = d.bwd ? 1 : 0,
                  C = d.C, DT = ((size_t)d.D + 31) / 32, CX = (size_t)d.C * d.xp,
                  GT = d.gate ? 1 : 0, HS = dense_gram(d) ? 1 : 0,
+                 PS = phase1_split(d) ? 1 : 0,
                  DCC = (size_t)d.C * dense_pitch(d.C);
     size_t off = 0;
 #define X_SIZE(name, type, count) off += up(sizeof(type) * (size_t)(count));
@@ -214,6 +217,7 @@ Work layout_assign(const Dims &d, int ns, int G_, void *base) {
                  CC = (size_t)d.C * d.C, CD = (size_t)d.C * d.D, G = G_, B = d.bwd ? 1 : 0,
                  C = d.C, DT = ((size_t)d.D + 31) / 32, CX = (size_t)d.C * d.xp,
                  GT = d.gate ? 1 : 0, HS = dense_gram(d) ? 1 : 0,
+                 PS = phase1_split(d) ? 1 : 0,
                  DCC = (size_t)d.C * dense_pitch(d.C);
     Work w;
     memset(&w, 0, sizeof(w));

@@ -286,6 +286,7 @@ struct P1Chunk {
     float *dka, *dkb, *dkq;
     int nd;
     float *lw;          // token-major running log-decay of the writes (written by the Gram rows)
+    const float2 *gk;   // (g, k) per entry when the scratch is in HBM (else k is in kf)
 };
 
 // 3a. weights of the sorted positions [pos0, pos1): gw = k exp(lw) (unless GW is false: the
@@ -452,7 +453,7 @@ __device__ void p1_gram_rows(const P1Chunk<WT> &c, int t0, int t1, int warp, int
             int pos = 0, gs = 0, dh = -1;
             if (act && j < W) {
                 const int e = t * W + j;
-                ka = c.kf[e];
+                ka = c.gk ? c.gk[e].y : c.kf[e];
                 pos = c.inv[e];
                 gs = c.pgs[pos];
                 la = c.lws[pos];
@@ -716,7 +717,8 @@ __global__ void __launch_bounds__(NT, 2) k_phase1(Dims d, Inputs in, Work w, int
     unsigned long long *keyA;
     int32_t *inv, *pgid, *pgs, *rlo, *rhi;
     int32_t *sgo = nullptr;   // group starts of the chunk on chip (else the chunk's goff row)
-    float *lws, *lend, *kf;
+    float *lws, *lend, *kf = nullptr;
+    float2 *gk = nullptr;      // (g, k) per entry (scratch in HBM)
     if (scratch_in_smem) {
         unsigned char *q = smem_raw + ((sizeof(P1Smem) + 15) & ~size_t(15));
         keyA = reinterpret_cast<unsigned long long *>(q); q += sizeof(unsigned long long) * 2 * CW;
@@ -736,7 +738,7 @@ __global__ void __launch_bounds__(NT, 2) k_phase1(Dims d, Inputs in, Work w, int
         pgs = w.pgs + (size_t)blockIdx.x * CW;
         lws = w.lws + (size_t)blockIdx.x * CW;
         lend = w.lend + (size_t)blockIdx.x * CW;
-        kf = w.kf + (size_t)blockIdx.x * CW;
+        gk = w.gk + (size_t)blockIdx.x * CW;
         rlo = w.rlo + (size_t)blockIdx.x * CR;
         rhi = w.rhi + (size_t)blockIdx.x * CR;
     }
@@ -787,9 +789,15 @@ __global__ void __launch_bounds__(NT, 2) k_phase1(Dims d, Inputs in, Work w, int
                 kk = 0.f;
                 bad = 1;
             }
-            kf[i] = kk;
-            // g (0 if dropped), read in step 2
-            pgs[i] = __float_as_int(s == S ? 0.f : graw);
+            // k and g (0 if dropped), read in step 2: one (g, k) pair with the scratch in
+            // HBM (a single random read per sorted position there), else two arrays on chip
+            const float gg = s == S ? 0.f : graw;
+            if (gk) {
+                gk[i] = make_float2(gg, kk);
+            } else {
+                kf[i] = kk;
+                pgs[i] = __float_as_int(gg);
+            }
             wsl[i] = s < S ? s : kNoEntry;
             const int t = div_by(i, magW);
             keyA[i] = ((unsigned long long)(unsigned)s << 32) | ((unsigned)t << 8) |
@@ -873,8 +881,9 @@ __global__ void __launch_bounds__(NT, 2) k_phase1(Dims d, Inputs in, Work w, int
                     e[u] = ok ? ent_of(low) : 0;
                     head[u] = ok && (ps == 0 || (int)(kk[u] >> 32) != slot);
                     tail[u] = ok && (ps == nw - 1 || (int)(kk[u + 2] >> 32) != slot);
-                    gv[u] = ok ? __int_as_float(pgs[e[u]]) : 0.f;
-                    kv[u] = ok ? kf[e[u]] : 0.f;
+                    const float2 pr = ok ? gk[e[u]] : make_float2(0.f, 0.f);
+                    gv[u] = pr.x;
+                    kv[u] = pr.y;
                 }
                 // thread-local inclusive values and head counts
                 float lv[IT4];
@@ -1008,7 +1017,7 @@ __global__ void __launch_bounds__(NT, 2) k_phase1(Dims d, Inputs in, Work w, int
                              wdw, gw, qw, lr, A, QK,
                              d.bwd ? w.dwt + (size_t)n * CW : nullptr,
                              nv, nw, nr, C, W, R, S,
-                             nullptr, nullptr, nullptr, nullptr, nullptr, 0, lw};
+                             nullptr, nullptr, nullptr, nullptr, nullptr, 0, lw, nullptr};
         if (split) {
             // steps 3 and 4 run in k_phase1_rows, over many CTAs per chunk; it finds the
             // sorted row in the radix buffer recorded here
@@ -1152,12 +1161,13 @@ __global__ void __launch_bounds__(NTR, BIG ? 4 : 6) k_phase1_rows(Dims d, Inputs
     P1Chunk<WT> pc{in.rs + tok_base * R, static_cast<const WT *>(in.qw) + tok_base * R,
                          srt, tkk, w.inv + (size_t)n * CW, w.pgid + (size_t)n * CW,
                          w.pgs + (size_t)n * CW, w.lws + (size_t)n * CW, w.lend + (size_t)n * CW,
-                         w.kf + (size_t)n * CW, w.rlo + (size_t)n * CR, w.rhi + (size_t)n * CR,
+                         nullptr, w.rlo + (size_t)n * CR, w.rhi + (size_t)n * CR,
                          w.wdw + (size_t)n * CW, w.gw + (size_t)n * CW, w.qw + (size_t)n * CR,
                          w.lr + (size_t)n * CR, w.A + (size_t)n * CC, w.QK + (size_t)n * CC,
                          d.bwd ? w.dwt + (size_t)n * CW : nullptr,
                          nv, nw, nr, C, W, R, d.S,
-                         nullptr, nullptr, nullptr, nullptr, nullptr, 0, w.lw + (size_t)n * CW};
+                         nullptr, nullptr, nullptr, nullptr, nullptr, 0, w.lw + (size_t)n * CW,
+                         w.gk + (size_t)n * CW};
     if (BIG && w.ndense[n] > 0) {
         pc.dpos = w.dpos + (size_t)n * CW;
         pc.dref = w.dref + (size_t)n * C;

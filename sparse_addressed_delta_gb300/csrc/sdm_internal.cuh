@@ -100,7 +100,10 @@ struct Work {
     int32_t *pgid;      // [G][CW]  group id of each sorted position
     int32_t *pgs;       // [G][CW]  group start position of each sorted position
     float *lend;        // [G][CW]  log-decay total of each group
-    float *kf;          // [G][CW]  write weight of each entry as float (0 for a bad slot)
+    float *kf;          // [G][CW]  write weight of each entry as float (0 for a bad slot);
+                        //          chunks whose Phase-1 scratch is on chip only
+    float2 *gk;         // [G][CW]  (log-decay, write weight) of each entry, entry order (0, 0
+                        //          for a bad slot); chunks whose Phase-1 scratch is in HBM
     int32_t *rlo;       // [G][CR]  first write position of the read's slot group
     int32_t *rhi;       // [G][CR]  last write position at or before the read's token (-1: none)
     // dense Gram groups of the chunks whose Phase-1 scratch is in global memory (sized only

@@ -178,24 +178,25 @@ __device__ int int_scan(int val, int carry_in, int &carry, P1Smem &sm) {
 constexpr int IT4 = 4;
 constexpr int G4 = IT4 * NT;
 
-// shared memory of those chunks after P1Smem: the per-(item, warp, digit) counts of a radix
-// tile, and the scans' per-thread results
+// shared memory of those chunks after P1Smem: the per-(warp, digit) counts of a radix tile, and
+// the scans' per-thread results
 struct P1Big {
-    int wc[IT4][NW][256];
+    int wc[NW][256];
     float tv[NT];
     int ti[NT];
 };
 
-// One stable counting pass of the LSD radix sort over tiles of G4 keys: key k of thread tid in
-// a tile is at position tile + k NT + tid (k-major, so the order (k, warp, lane) is the position
-// order). A key's rank among equal digits of its warp and item (match_any) plus the counts of
-// the earlier (item, warp) pairs of the tile and of the earlier tiles gives its place.
+// One stable counting pass of the LSD radix sort over tiles of G4 keys: warp w of the tile takes
+// the IT4 x 32 keys from tile + IT4 32 w on (item k of lane l at + 32 k + l), so the order
+// (warp, item, lane) is the position order. A warp ranks its items one after another against
+// its own running count per digit (match_any within the item), then the counts of the earlier
+// warps and tiles give each key its place.
 __device__ void radix_pass4(const unsigned long long *in, unsigned long long *out, int n,
                             int shift, P1Smem &sm, P1Big &bg) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    int *wcf = &bg.wc[0][0][0];
+    int *wcf = &bg.wc[0][0];
     for (int i = tid; i < 256; i += NT) sm.hist[i] = 0;
-    for (int i = tid; i < IT4 * NW * 256; i += NT) wcf[i] = 0;
+    for (int i = tid; i < NW * 256; i += NT) wcf[i] = 0;
     __syncthreads();
     for (int i0 = tid; i0 < n; i0 += G4) {
         unsigned long long kk[IT4];
@@ -221,42 +222,45 @@ __device__ void radix_pass4(const unsigned long long *in, unsigned long long *ou
         for (int k = 0; k < 8; ++k) { sm.base[lane * 8 + k] = run; run += v[k]; }
     }
     __syncthreads();
+    const unsigned lt = (1u << lane) - 1u;
     for (int tile = 0; tile < n; tile += G4) {
+        const int wbase = tile + warp * (IT4 * 32);
         unsigned long long kk[IT4];
         int dg[IT4], rank[IT4];
 #pragma unroll
         for (int k = 0; k < IT4; ++k) {
-            const int i = tile + k * NT + tid;
+            const int i = wbase + k * 32 + lane;
             kk[k] = i < n ? in[i] : 0ull;
         }
 #pragma unroll
         for (int k = 0; k < IT4; ++k) {
-            const int i = tile + k * NT + tid;
+            const int i = wbase + k * 32 + lane;
             dg[k] = i < n ? (int)((kk[k] >> shift) & 255ull) : 256;
             const unsigned peers = __match_any_sync(0xffffffffu, dg[k]);
-            rank[k] = __popc(peers & ((1u << lane) - 1u));
-            if (dg[k] < 256 && lane == __ffs(peers) - 1) bg.wc[k][warp][dg[k]] = __popc(peers);
+            const int before = dg[k] < 256 ? bg.wc[warp][dg[k]] : 0;
+            rank[k] = before + __popc(peers & lt);
+            __syncwarp();
+            if (dg[k] < 256 && lane == __ffs(peers) - 1) bg.wc[warp][dg[k]] = before + __popc(peers);
+            __syncwarp();
         }
         __syncthreads();
         for (int dd = tid; dd < 256; dd += NT) {
             int run = 0;
 #pragma unroll
-            for (int k = 0; k < IT4; ++k)
-#pragma unroll
-                for (int w2 = 0; w2 < NW; ++w2) {
-                    const int c = bg.wc[k][w2][dd];
-                    bg.wc[k][w2][dd] = run;
-                    run += c;
-                }
+            for (int w2 = 0; w2 < NW; ++w2) {
+                const int c = bg.wc[w2][dd];
+                bg.wc[w2][dd] = run;
+                run += c;
+            }
             sm.tile_total[dd] = run;
         }
         __syncthreads();
 #pragma unroll
         for (int k = 0; k < IT4; ++k)
-            if (dg[k] < 256) out[sm.base[dg[k]] + bg.wc[k][warp][dg[k]] + rank[k]] = kk[k];
+            if (dg[k] < 256) out[sm.base[dg[k]] + bg.wc[warp][dg[k]] + rank[k]] = kk[k];
         __syncthreads();
         for (int dd = tid; dd < 256; dd += NT) sm.base[dd] += sm.tile_total[dd];
-        for (int i = tid; i < IT4 * NW * 256; i += NT) wcf[i] = 0;
+        for (int i = tid; i < NW * 256; i += NT) wcf[i] = 0;
         __syncthreads();
     }
 }
@@ -627,7 +631,7 @@ __device__ void p1_dense_select(const int32_t *go, int ng, const float *lws, int
     }
     // the candidates, in any order, then ranked into group order
     int *list = bg.ti;
-    int *sorted = &bg.wc[0][0][0];
+    int *sorted = &bg.wc[0][0];
     int *hidx = sorted + kMaxChunk;
     float *ref = reinterpret_cast<float *>(sorted + 2 * kMaxChunk);
     for (int g0 = 0; g0 < ng; g0 += NT) {

@@ -1081,18 +1081,21 @@ __global__ void __launch_bounds__(NT, 2) k_phase1(Dims d, Inputs in, Work w, int
             if (tid == 0) { w.rng[n] = rcarry; rgoff[rcarry] = nr; }
             __syncthreads();
         }
-        // 6. the DW order for the pipelined Phase 2: the groups of >= kHotGroup members first,
-        //    then the others by size, largest first (a counting sort over 1 + kHotGroup size
-        //    classes; the order inside a class is arbitrary, as a group's sum does not depend
-        //    on which thread computes it). Warp-aggregated shared-memory atomics.
+        // 6. the DW order of Phase 2: the hot groups (at least hmin members) first, then the
+        //    others by size, largest first (a counting sort over 1 + hmin size classes; the
+        //    order inside a class is arbitrary, as a group's sum does not depend on which
+        //    thread computes it). Warp-aggregated shared-memory atomics. The pipelined kernel
+        //    gives each hot group a warp (hmin = kHotGroup); the per-step DW sums them with the
+        //    whole CTA, which pays off from about C/8 members on (hmin = max(kHotGroup, C/8)).
         {
-            constexpr int NB = kHotGroup + 1;
+            const int hmin = d.per_step && C / 8 > kHotGroup ? C / 8 : kHotGroup;
+            const int NB = hmin + 1;
             int *cnt = sm.hist, *cur = sm.hist + NB, *bas = sm.base;
             for (int i = tid; i < 2 * NB; i += NT) sm.hist[i] = 0;
             __syncthreads();
             auto digit = [&](int g) {
                 const int sz = go[g + 1] - go[g];
-                return sz >= kHotGroup ? 0 : 1 + kHotGroup - sz;
+                return sz >= hmin ? 0 : 1 + hmin - sz;
             };
             for (int g0 = 0; g0 < ng; g0 += NT) {
                 const int g = g0 + tid;

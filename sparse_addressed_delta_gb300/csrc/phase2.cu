@@ -370,10 +370,10 @@ __global__ void __launch_bounds__(MM_T) k_dualmm(Dims d, Inputs in, Work w, int 
 // delta_v slice ([C][DS] float32, at most 128 KB) into shared memory: every delta_v row is read
 // by every group that row's token writes (W groups), so from L2 those few rows would be
 // requested by every SM at once. The hot groups (the first ones of the DW order Phase 1 wrote:
-// at least kHotGroup members) come first, a share of them per CTA, each summed by the whole
-// CTA: their metadata, member records and B0 slices are staged in shared memory in one pass
-// per round, every warp sums a fixed share of a group's members (in sorted order), and the
-// shares are added to exp(lend) B0 in warp order. A hot group summed by one warp would hold
+// at least max(kHotGroup, C/8) members) come first, a share of them per CTA, each summed by the
+// whole CTA in rounds: their metadata, member records and B0 slices are staged in shared memory,
+// a group's members are cut into chunks of 32 (sorted order), each warp sums one chunk, and the
+// chunk sums are added to exp(lend) B0 in chunk order. A hot group summed by one warp would hold
 // that warp (and the step) for its whole member list. The other groups go to the warps in a
 // stride: a warp holds the metadata of 32 of its groups (lane l: group l, loaded one batch
 // ahead), loads the B0 slices of U groups before adding any, and reads the members' delta_v

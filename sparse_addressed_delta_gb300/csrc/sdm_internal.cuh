@@ -74,8 +74,9 @@ struct Work {
                         //           stride keeps every chunk's row 16-byte aligned)
     int4 *ng4;          // [N]       (ngroups, hot groups, 0, 0) as one 16-byte word
     int32_t *p1sel;     // [N]       radix buffer holding the sorted write row (scratch in HBM)
-    int32_t *gord;      // [N][CW]   DW order: the groups of >= kHotGroup members (ascending),
-                        //           then the others by size, largest first (ascending within)
+    int32_t *gord;      // [N][CW]   DW order: the hot groups (>= kHotGroup members, or C/8 if
+                        //           more, for the per-step DW), then the others by size,
+                        //           largest first
     int32_t *gslot;     // [N][CW]   slot of each group
     float *gfac;        // [N][CW]   exp(lend) of each group
     int32_t *ngroups;   // [N]

@@ -112,3 +112,56 @@ def test_algorithmic_bytes_by_sets(i):
             dw_rows += len(uw)
     assert got == {"gather": g_rows * row, "dw": 2 * dw_rows * row,
                    "phase2": (g_rows + dw_rows) * row}
+
+
+@pytest.mark.parametrize("i", [1, 2, 4])
+def test_gram_pairs_by_slot_lists(i):
+    """The Phase-1 roofline's unit: per chunk, the pairs of writes of one slot at tokens u < t
+    (terms of A) and the pairs (read of slot s at token t, write of s at u <= t) (terms of QK),
+    counted here slot by slot from lists of tokens."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    wl = small(i, T=300)
+    x = si.generate(wl)
+    want = 0
+    for p in range(wl.P):
+        for c0 in range(0, int(x["valid"][p]), wl.C):
+            c1 = min(int(x["valid"][p]), c0 + wl.C)
+            wtok = {}
+            for t in range(c1 - c0):
+                for s in x["write_slots"][p, c0 + t].tolist():
+                    wtok.setdefault(s, []).append(t)
+            for toks in wtok.values():
+                want += sum(1 for a in range(len(toks)) for b in range(a + 1, len(toks))
+                            if toks[a] < toks[b])
+            for t in range(c1 - c0):
+                for s in x["read_slots"][p, c0 + t].tolist():
+                    want += sum(1 for u in wtok.get(s, ()) if u <= t)
+    assert bench.gram_pairs(wl, x) == want
+
+
+def test_traffic_record_follows_its_sources(tmp_path, monkeypatch):
+    """A recorded DRAM byte count is reported for its own kernel family and workload only, and
+    only while the sources it names are unchanged."""
+    sys.path.insert(0, ROOT)
+    import hashlib
+    import json
+
+    import bench
+
+    src = tmp_path / "sparse_addressed_delta_gb300" / "csrc"
+    src.mkdir(parents=True)
+    (src / "k.cu").write_text("kernel one\n")
+    digest = hashlib.sha256(b"kernel one\n").hexdigest()[:16]
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    (prof / "ncu_traffic.json").write_text(json.dumps({"dw": [{
+        "kernel": "k_dw", "workload": "w_a", "sources": ["k.cu"], "sources_sha256_16": digest,
+        "dram_bytes_per_launch": 1234, "capture": "test"}]}))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.traffic_record("dw", "w_a") == 1234.0
+    assert bench.traffic_record("dw", "w_b") is None
+    assert bench.traffic_record("gather", "w_a") is None
+    (src / "k.cu").write_text("kernel two\n")
+    assert bench.traffic_record("dw", "w_a") is None

@@ -192,3 +192,21 @@ def test_fp8_snapshot_sizes_and_refusals():
     both = sdm.make_shape(2, 64, 16, 100, 64, 4, 3, torch.float32,
                           flags=sdm.FLAG_SNAPSHOT_FP8 | sdm.FLAG_SNAPSHOT_BF16)
     assert sdm.library().sdm_workspace_bytes(ctypes.byref(both)) == 0
+
+
+def test_phase1_launches_by_chunk_class():
+    """Phase 1 per slab: one kernel with the chunk's scratch on chip; the sort and row kernels
+    over global scratch; and the dense-Gram kernel besides from C = 128 on (shapes chosen so
+    that one slab holds every step, per-step Phase 2: 3 launches per step)."""
+    for (C, W, p1) in ((16, 4, 1), (64, 32, 2), (128, 64, 3), (256, 32, 3)):
+        T = 2 * C
+        s = sdm.make_shape(1, T, C, 4096, 64, W, W, sdm.SDM_F32, flags=sdm.FLAG_PER_STEP_KERNELS)
+        assert sdm.launch_count(s) == p1 + 1 + 3 * 2, (C, W)
+
+
+def test_dense_gram_workspace_is_bounded():
+    """The dense Gram factors add three C x C float arrays per chunk for C >= 128, and the
+    workspace still does not grow with T."""
+    a = sdm.make_shape(2, 1 << 16, 128, 1 << 16, 64, 64, 64, sdm.SDM_BF16)
+    b = sdm.make_shape(2, 1 << 18, 128, 1 << 16, 64, 64, 64, sdm.SDM_BF16)
+    assert sdm.workspace_bytes(a) == sdm.workspace_bytes(b)

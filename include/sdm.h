@@ -62,8 +62,11 @@ typedef enum { SDM_F32 = 0, SDM_BF16 = 1 } sdm_dtype;
  *   W  write slots per token, 1..256 (MAX_WIDTH); distinct within a token
  *   R  read slots per token, 1..256
  *   bank_dtype  SDM_F32 or SDM_BF16
- *   slab_steps  Phase-2 steps whose Phase-1 state is held at once; 0 = automatic. The
- *               results do not depend on it (Phase 1 and the solve are per chunk).
+ *   slab_steps  Phase-2 steps whose Phase-1 state is held at once; 0 = automatic: every
+ *               step when the state of all of them fits in 256 MiB, else as many as fit but
+ *               at least two chunks per SM (ceil(304 / P) steps), so the workspace does not
+ *               grow with T. The results do not depend on it (Phase 1 and the solve are per
+ *               chunk).
  *   flags       0, or any of SDM_FLAG_PER_STEP_KERNELS, SDM_FLAG_SNAPSHOT_BF16 or
  *               SDM_FLAG_SNAPSHOT_FP8, SDM_FLAG_TOKEN_GATE, SDM_FLAG_SHARED_BANK
  * P * ceil(T / C) * C must be below 2^31.
